@@ -1,0 +1,363 @@
+"""CPU oracle for the single-GPU MoE expert layer behind the "grouped_mm" backend.
+
+TEST INFRASTRUCTURE ONLY.  Nothing in the product path imports this module:
+only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` use it.  It shares no code with the CUDA library; both sides are
+fed the same seeded bf16 inputs and nothing else.
+
+Everything here is plain float64 numpy (bf16 inputs are widened exactly).  A
+matrix product (``@``) is the only library step; there is no blocking, fusion
+or reordering beyond what the definitions below state.
+
+Sources (page title, section):
+
+* NeMo AutoModel blog, zh-CN translation ("Accelerating Transformers
+  fine-tuning with NVIDIA NeMo AutoModel"), table "专家后端 / Expert backends":
+  eager = a for-loop over the selected experts (used for correctness checks);
+  batched_mm = copy the expert parameters and run one batched GEMM;
+  grouped_mm = sort the tokens by their assigned expert and run a single
+  grouped GEMM, with no parameter copies.
+* same page, "v4 死锁原因 / why v4 deadlocks" and "动态权重加载 / dynamic weight
+  loading": experts are stored as fused 3-D parameter tensors, one per
+  projection, not as one module per expert.
+* same page, "关于路由门的说明 / note on the routing gate": the NeMo numbers use a
+  balanced routing gate that forces tokens evenly across experts.
+* DeepEP paragraphs of the same page and of "英伟达开源MoE新方案" (section
+  "DeepEP"): the layer dispatches tokens to experts and combines the results.
+
+The pages fix neither the router formula, the activation, the gate's exact
+rule nor any tensor shape.  Readings taken here (each also listed in the
+design notes):
+
+* router: logits = x W_r^T (+ b); p = softmax over all E; top-k chosen on the
+  fp32-rounded logits, largest first, ties to the lower expert index;
+  w = p[selected] / sum(p[selected]).
+* balanced gate: slot (t, j) goes to expert (t*k + j) mod E; its weight is the
+  router softmax renormalised over those k experts.
+* permutation: stable counting sort of the slots s = t*k + j by expert.
+* expert MLP: SwiGLU, h = silu(gate) * up, gate = first I rows of W_gu[e].
+* combine: out[t] = sum_j w[t,j] * y[t,j] (+ shared expert, weight 1).
+
+Parity status: every function below is pinned by a test in
+``tests/test_oracle_pins.py`` (closed forms, invariants, brute force, library
+special cases, finite differences).
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+
+# --------------------------------------------------------------------------
+# bf16 widening (the oracle's own; the CUDA path has its own)
+# --------------------------------------------------------------------------
+def widen_bf16(bits: np.ndarray) -> np.ndarray:
+    """bfloat16 raw bits -> float64, exactly (a bf16 is the top half of an fp32)."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16
+    return b.view(np.float32).astype(np.float64)
+
+
+# --------------------------------------------------------------------------
+# Router (logits, softmax, top-k, renormalisation, balanced gate)
+# --------------------------------------------------------------------------
+def router_logits(x: np.ndarray, w_router: np.ndarray, bias: np.ndarray | None = None) -> np.ndarray:
+    """logits[t, e] = sum_h x[t, h] * W_r[e, h] (+ bias[e]).
+
+    The router is the linear layer in front of the experts; the pages call it
+    the native router ("原生路由器", note on the routing gate).  The bias is the
+    learned-style per-expert skew of the skewed workloads.
+    """
+    logits = x @ w_router.T
+    if bias is not None:
+        logits = logits + np.asarray(bias, dtype=np.float64)[None, :]
+    return logits
+
+
+def softmax(logits: np.ndarray) -> np.ndarray:
+    """Row softmax, p[t,e] = exp(l[t,e] - max_e l) / sum_e exp(l[t,e] - max_e l)."""
+    m = logits.max(axis=1, keepdims=True)
+    z = np.exp(logits - m)
+    return z / z.sum(axis=1, keepdims=True)
+
+
+def select_topk(decision_logits: np.ndarray, k: int) -> np.ndarray:
+    """Top-k expert ids per token by repeated argmax.
+
+    Selection j picks the largest remaining logit; among equal logits the lower
+    expert index is taken first (np.argmax returns the first maximum).  The
+    decision is taken on the values as given (callers pass fp32-rounded logits,
+    the precision the kernel decides in).  Returns int32 [T, k] in selection
+    order.  Finite logits are assumed.
+    """
+    T, E = decision_logits.shape
+    assert 1 <= k <= E
+    work = np.asarray(decision_logits, dtype=np.float64).copy()
+    idx = np.empty((T, k), dtype=np.int32)
+    rows = np.arange(T)
+    for j in range(k):
+        sel = np.argmax(work, axis=1)
+        idx[:, j] = sel
+        work[rows, sel] = -np.inf
+    return idx
+
+
+def balanced_topk(T: int, E: int, k: int) -> np.ndarray:
+    """Balanced gate: slot (t, j) -> expert (t*k + j) mod E.
+
+    Forces an even token-to-expert split (note on the routing gate): when E
+    divides T*k every expert receives exactly T*k/E slots, and the k experts
+    of one token are distinct whenever k <= E.
+    """
+    s = np.arange(T * k, dtype=np.int64).reshape(T, k)
+    return (s % E).astype(np.int32)
+
+
+def renormalised_weights(p: np.ndarray, idx: np.ndarray) -> np.ndarray:
+    """w[t, j] = p[t, idx[t,j]] / sum_j' p[t, idx[t,j']]."""
+    rows = np.arange(p.shape[0])[:, None]
+    psel = p[rows, idx]
+    return psel / psel.sum(axis=1, keepdims=True)
+
+
+def route(logits: np.ndarray, k: int, balanced: bool = False, decision_logits=None):
+    """Full router step: returns (topk_idx int32 [T,k], topk_w float64 [T,k], p).
+
+    ``decision_logits`` (default: ``logits`` rounded to fp32) is what top-k
+    compares; softmax and weights always use ``logits``.
+    """
+    T, E = logits.shape
+    p = softmax(logits)
+    if balanced:
+        idx = balanced_topk(T, E, k)
+    else:
+        if decision_logits is None:
+            decision_logits = logits.astype(np.float32)
+        idx = select_topk(decision_logits, k)
+    return idx, renormalised_weights(p, idx), p
+
+
+# --------------------------------------------------------------------------
+# Sort token-slots by expert (grouped_mm "sort the tokens by expert")
+# --------------------------------------------------------------------------
+def permute(topk_idx: np.ndarray, E: int):
+    """Counting sort of the T*k slots by expert, stable in slot id s = t*k + j.
+
+    Returns (expert_offsets int32 [E+1], perm_slot int32 [S], slot_perm int32 [S]):
+    rows expert_offsets[e] .. expert_offsets[e+1]-1 of the sorted order belong
+    to expert e; perm_slot[r] is the slot at sorted row r and slot_perm is its
+    inverse.  Only token ids move; no expert weight is copied (grouped_mm row
+    of the expert-backend table).
+    """
+    flat = np.asarray(topk_idx, dtype=np.int64).ravel()
+    S = flat.size
+    counts = np.zeros(E, dtype=np.int64)
+    for e in flat:
+        counts[e] += 1
+    offsets = np.zeros(E + 1, dtype=np.int64)
+    offsets[1:] = np.cumsum(counts)
+    fill = offsets[:-1].copy()
+    perm_slot = np.empty(S, dtype=np.int64)
+    for s in range(S):
+        e = flat[s]
+        perm_slot[fill[e]] = s
+        fill[e] += 1
+    slot_perm = np.empty(S, dtype=np.int64)
+    slot_perm[perm_slot] = np.arange(S)
+    return offsets.astype(np.int32), perm_slot.astype(np.int32), slot_perm.astype(np.int32)
+
+
+# --------------------------------------------------------------------------
+# Expert MLP (SwiGLU) in the three backends of the expert-backend table
+# --------------------------------------------------------------------------
+def silu(z: np.ndarray) -> np.ndarray:
+    """silu(z) = z * sigmoid(z) = z / (1 + exp(-z))."""
+    return z / (1.0 + np.exp(-z))
+
+
+def sigmoid(z: np.ndarray) -> np.ndarray:
+    return 1.0 / (1.0 + np.exp(-z))
+
+
+def swiglu_mlp(xr: np.ndarray, w_gu: np.ndarray, w_down: np.ndarray):
+    """One expert on rows xr [n, H]: gu = xr W_gu^T, h = silu(gate) * up, y = h W_down^T.
+
+    W_gu is [2I, H] with the gate rows first; W_down is [H, I].
+    Returns (y [n,H], gu [n,2I], h [n,I]).
+    """
+    I = w_down.shape[1]
+    gu = xr @ w_gu.T
+    h = silu(gu[:, :I]) * gu[:, I:]
+    return h @ w_down.T, gu, h
+
+
+def experts_grouped(x, offsets, perm_slot, k, w_gu, w_down):
+    """grouped_mm backend: tokens already sorted by expert, one GEMM per group.
+
+    Returns y_perm [S, H], gu_perm [S, 2I], h_perm [S, I] in sorted-row order.
+    """
+    S = perm_slot.size
+    E, twoI, H = w_gu.shape
+    I = twoI // 2
+    y = np.zeros((S, H))
+    gu = np.zeros((S, twoI))
+    h = np.zeros((S, I))
+    for e in range(E):
+        r0, r1 = int(offsets[e]), int(offsets[e + 1])
+        if r1 == r0:
+            continue
+        tok = perm_slot[r0:r1] // k
+        y[r0:r1], gu[r0:r1], h[r0:r1] = swiglu_mlp(x[tok], w_gu[e], w_down[e])
+    return y, gu, h
+
+
+def experts_eager(x, topk_idx, w_gu, w_down):
+    """eager backend: for-loop over the selected experts, token by token.
+
+    Returns y_slot [T, k, H] (each slot's unweighted expert output).
+    """
+    T, k = topk_idx.shape
+    H = x.shape[1]
+    y = np.zeros((T, k, H))
+    for e in np.unique(topk_idx):
+        for t in range(T):
+            for j in range(k):
+                if topk_idx[t, j] == e:
+                    y[t, j] = swiglu_mlp(x[t:t + 1], w_gu[e], w_down[e])[0][0]
+    return y
+
+
+def experts_batched(x, topk_idx, w_gu, w_down):
+    """batched_mm backend: copy each slot's expert parameters, one batched GEMM.
+
+    Returns y_slot [T, k, H].  Memory grows with T*k*(3*I*H); tiny inputs only.
+    """
+    T, k = topk_idx.shape
+    I = w_down.shape[2]
+    flat = topk_idx.ravel()
+    xs = np.repeat(x, k, axis=0)                  # [S, H]
+    wg = w_gu[flat]                               # [S, 2I, H]  (parameter copies)
+    wd = w_down[flat]                             # [S, H, I]
+    gu = np.einsum("sh,sih->si", xs, wg)
+    h = silu(gu[:, :I]) * gu[:, I:]
+    y = np.einsum("si,shi->sh", h, wd)
+    return y.reshape(T, k, -1)
+
+
+def combine(y_perm, slot_perm, topk_w, y_shared=None):
+    """Weighted un-permute: out[t] = sum_j w[t,j] * y_perm[slot_perm[t*k+j]] (+ y_shared[t])."""
+    T, k = topk_w.shape
+    out = np.zeros((T, y_perm.shape[1]))
+    for j in range(k):
+        rows = slot_perm.reshape(T, k)[:, j]
+        out += topk_w[:, j:j + 1] * y_perm[rows]
+    if y_shared is not None:
+        out = out + y_shared
+    return out
+
+
+def combine_slots(y_slot, topk_w, y_shared=None):
+    """Same weighted sum for outputs already in slot order [T, k, H]."""
+    out = np.einsum("tk,tkh->th", topk_w, y_slot)
+    if y_shared is not None:
+        out = out + y_shared
+    return out
+
+
+# --------------------------------------------------------------------------
+# Whole layer, forward
+# --------------------------------------------------------------------------
+def layer_forward(x, w_router, w_gu, w_down, k, balanced=False, bias=None,
+                  w_sh_gu=None, w_sh_down=None, topk_idx=None, decision_logits=None):
+    """MoE layer forward through the grouped path.
+
+    All arrays float64 except ids.  ``topk_idx`` overrides the selection (used
+    when comparing against a device whose fp32 logits sit on a near-tie).
+    Returns a dict with every intermediate the backward needs.
+    """
+    E = w_gu.shape[0]
+    logits = router_logits(x, w_router, bias)
+    idx, w, p = route(logits, k, balanced=balanced, decision_logits=decision_logits)
+    if topk_idx is not None:
+        idx = np.asarray(topk_idx, dtype=np.int32)
+        w = renormalised_weights(p, idx)
+    offsets, perm_slot, slot_perm = permute(idx, E)
+    y_perm, gu_perm, h_perm = experts_grouped(x, offsets, perm_slot, k, w_gu, w_down)
+    y_sh = gu_sh = None
+    if w_sh_gu is not None:
+        y_sh, gu_sh, _ = swiglu_mlp(x, w_sh_gu, w_sh_down)
+    out = combine(y_perm, slot_perm, w, y_sh)
+    return dict(logits=logits, p=p, topk_idx=idx, topk_w=w, expert_offsets=offsets,
+                perm_slot=perm_slot, slot_perm=slot_perm, gu_perm=gu_perm, h_perm=h_perm,
+                y_perm=y_perm, y_shared=y_sh, gu_shared=gu_sh, out=out)
+
+
+# --------------------------------------------------------------------------
+# Whole layer, backward (hand-derived; pinned by finite differences)
+# --------------------------------------------------------------------------
+def swiglu_mlp_backward(xr, gu, w_gu, w_down, dy):
+    """Backward of y = (silu(g) * u) W_down^T with [g|u] = xr W_gu^T.
+
+    dy [n,H] is the gradient at y.  Returns (dx [n,H], dW_gu [2I,H], dW_down [H,I]).
+    dh = dy W_down; dg = dh * u * s * (1 + g (1 - s)) with s = sigmoid(g);
+    du = dh * silu(g).
+    """
+    I = w_down.shape[1]
+    g, u = gu[:, :I], gu[:, I:]
+    s = sigmoid(g)
+    h = g * s * u
+    dW_down = dy.T @ h
+    dh = dy @ w_down
+    dg = dh * u * s * (1.0 + g * (1.0 - s))
+    du = dh * g * s
+    dgu = np.concatenate([dg, du], axis=1)
+    return dgu @ w_gu, dgu.T @ xr, dW_down
+
+
+def layer_backward(fwd: dict, grad_out, x, w_router, w_gu, w_down, k,
+                   w_sh_gu=None, w_sh_down=None):
+    """Gradients of the layer output w.r.t. x, W_r, router bias and every expert weight.
+
+    Per slot (t, j) routed to e with weight w:  y = MLP_e(x[t]),
+    dL/dw[t,j] = <dout[t], y>, the expert sees dy = w * dout[t].  Router:
+    w = p[sel]/P, so dp[sel_j] = (dw_j - sum_i w_i dw_i) / P and every other
+    dp is 0; through the softmax dl = p * (dp - <dp, p>).  dW_r = dl^T x,
+    db = sum_t dl[t], and x also receives dl W_r.  Top-k selection itself is
+    piecewise constant and passes no gradient.
+    """
+    T, H = x.shape
+    E = w_gu.shape[0]
+    idx, w, p = fwd["topk_idx"], fwd["topk_w"], fwd["p"]
+    offsets, perm_slot = fwd["expert_offsets"], fwd["perm_slot"]
+    gu_perm, y_perm = fwd["gu_perm"], fwd["y_perm"]
+    dx = np.zeros((T, H))
+    dW_gu = np.zeros_like(w_gu)
+    dW_down = np.zeros_like(w_down)
+    dw = np.zeros((T, k))
+    for e in range(E):
+        r0, r1 = int(offsets[e]), int(offsets[e + 1])
+        if r1 == r0:
+            continue
+        slots = perm_slot[r0:r1].astype(np.int64)
+        tok, j = slots // k, slots % k
+        dout_r = grad_out[tok]
+        dw[tok, j] = np.sum(dout_r * y_perm[r0:r1], axis=1)
+        dy = w[tok, j][:, None] * dout_r
+        dxr, dW_gu[e], dW_down[e] = swiglu_mlp_backward(x[tok], gu_perm[r0:r1], w_gu[e], w_down[e], dy)
+        np.add.at(dx, tok, dxr)
+    # router
+    rows = np.arange(T)[:, None]
+    P = p[rows, idx].sum(axis=1, keepdims=True)
+    dp_sel = (dw - np.sum(w * dw, axis=1, keepdims=True)) / P
+    dp = np.zeros_like(p)
+    np.add.at(dp, (np.repeat(np.arange(T), k), idx.ravel()), dp_sel.ravel())
+    dl = p * (dp - np.sum(dp * p, axis=1, keepdims=True))
+    dW_r = dl.T @ x
+    db = dl.sum(axis=0)
+    dx += dl @ w_router
+    res = dict(grad_x=dx, grad_w_router=dW_r, grad_router_bias=db, grad_w_gate_up=dW_gu,
+               grad_w_down=dW_down, grad_topk_w=dw, grad_logits=dl)
+    if w_sh_gu is not None:
+        dxs, res["grad_w_sh_gate_up"], res["grad_w_sh_down"] = swiglu_mlp_backward(
+            x, fwd["gu_shared"], w_sh_gu, w_sh_down, grad_out)
+        res["grad_x"] = res["grad_x"] + dxs
+    return res

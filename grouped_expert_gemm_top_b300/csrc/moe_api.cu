@@ -1,0 +1,677 @@
+// Host side of the C ABI declared in include/moe.h: argument validation,
+// workspace layout, TMA tensor-map encoding and the launch sequence of every
+// call.  Nothing here allocates device memory or synchronises (except
+// moe_read_device_status).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "gemm.cuh"
+#include "kernels_misc.cuh"
+#include "moe.h"
+
+namespace {
+
+using moe::GemmArgs;
+using moe::GemmCfg;
+
+constexpr int32_t kAbiVersion = 1;
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+// ------------------------------------------------------------------ shapes
+moe_status check_dims(const moe_dims* d) {
+  if (!d) return MOE_ERR_INVALID_ARG;
+  if (d->T < 1 || d->H < 64 || d->E < 1 || d->k < 1 || d->I < 64 || d->I_shared < 0)
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (d->H % 64 || d->I % 64 || d->I_shared % 64) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (d->E > moe::kMaxGroups || d->k > d->E || d->k > 32) return MOE_ERR_UNSUPPORTED_SHAPE;
+  const long long S = (long long)d->T * d->k;
+  if (S + (long long)d->E * moe::kPadRows >= (1LL << 31)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if ((long long)d->H * 2 * d->I >= (1LL << 40)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  return MOE_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Layout {
+  size_t status, counts, h, h_sh, fwd_end;
+  size_t poff, row_tok, dgu, hw, dxs, dwp, dl, dgu_sh, hw_sh, dxs_sh, total;
+  int sort_blocks;
+  long long S, S_pad_max;
+  int nNB_I;  // 256-wide column blocks of the intermediate (dgrad-down tiles)
+};
+
+Layout make_layout(const moe_dims& d, bool bwd) {
+  Layout L{};
+  L.S = (long long)d.T * d.k;
+  L.S_pad_max = L.S + (long long)d.E * (moe::kPadRows - 1);
+  L.S_pad_max = (L.S_pad_max + moe::kPadRows - 1) / moe::kPadRows * moe::kPadRows;
+  L.sort_blocks = (int)((L.S + moe::kSortChunk - 1) / moe::kSortChunk);
+  L.nNB_I = (d.I + 255) / 256;
+  size_t o = 0;
+  L.status = o; o += kAlign;
+  L.counts = o; o = align_up(o + (size_t)L.sort_blocks * d.E * 4);
+  L.h = o; o = align_up(o + (size_t)L.S * d.I * 2);
+  L.h_sh = o; o = align_up(o + (size_t)d.T * d.I_shared * 2);
+  L.fwd_end = o;
+  if (bwd) {
+    const size_t P = (size_t)L.S_pad_max;
+    L.poff = o; o = align_up(o + (size_t)(d.E + 1) * 4);
+    L.row_tok = o; o = align_up(o + P * 4);
+    L.dgu = o; o = align_up(o + P * 2 * d.I * 2);
+    L.hw = o; o = align_up(o + P * d.I * 2);
+    L.dxs = o; o = align_up(o + P * d.H * 2);
+    L.dwp = o; o = align_up(o + P * L.nNB_I * 4);
+    L.dl = o; o = align_up(o + (size_t)L.S * 4);
+    L.dgu_sh = o; o = align_up(o + (size_t)d.T * 2 * d.I_shared * 2);
+    L.hw_sh = o; o = align_up(o + (size_t)d.T * d.I_shared * 2);
+    L.dxs_sh = o; o = align_up(o + (size_t)(d.I_shared ? d.T : 0) * d.H * 2);
+  }
+  L.total = o;
+  return L;
+}
+
+template <class T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+// ------------------------------------------------------------------ device info
+int sm_count() {
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  int v = cache[dev].load();
+  if (v == 0) {
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+      v = 148;
+    cache[dev].store(v);
+  }
+  return v;
+}
+
+// ------------------------------------------------------------------ tensor maps
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// bf16 tensor [depth][rows][inner], 128-byte swizzle, zero fill outside.
+bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t depth,
+              uint32_t box_inner, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {inner, rows, depth};
+  const cuuint64_t strides[2] = {inner * 2, inner * rows * 2};
+  const cuuint32_t box[3] = {box_inner, box_rows, 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  const cuuint32_t rank = depth > 1 ? 3 : 2;
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// A 3-D map whose depth is 1 is still built as 3-D (the kernel passes a group coordinate).
+bool make_map3(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t depth,
+               uint32_t box_inner, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {inner, rows, depth};
+  const cuuint64_t strides[2] = {inner * 2, inner * rows * 2};
+  const cuuint32_t box[3] = {box_inner, box_rows, 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ------------------------------------------------------------------ kernel accounting
+struct Timing {
+  std::mutex mu;
+  bool on = false;
+  std::vector<cudaEvent_t> pool;
+  struct Rec {
+    int id;
+    cudaEvent_t a, b;
+  };
+  std::vector<Rec> recs;
+  std::atomic<long long> launches[MOE_K_COUNT];
+  Timing() {
+    for (auto& l : launches) l.store(0);
+  }
+};
+
+Timing& timing() {
+  static Timing t;
+  return t;
+}
+
+cudaEvent_t pooled_event() {
+  Timing& T = timing();
+  std::lock_guard<std::mutex> g(T.mu);
+  if (!T.pool.empty()) {
+    cudaEvent_t e = T.pool.back();
+    T.pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+// Counts one launch of `id`; while timing is on, brackets it with events.
+struct KernelScope {
+  int id;
+  cudaStream_t st;
+  cudaEvent_t a = nullptr;
+  KernelScope(int id_, cudaStream_t st_) : id(id_), st(st_) {
+    Timing& T = timing();
+    T.launches[id].fetch_add(1);
+    if (T.on) {
+      a = pooled_event();
+      if (a && cudaEventRecord(a, st) != cudaSuccess) a = nullptr;
+    }
+  }
+  ~KernelScope() {
+    if (!a) return;
+    cudaEvent_t b = pooled_event();
+    if (!b || cudaEventRecord(b, st) != cudaSuccess) return;
+    Timing& T = timing();
+    std::lock_guard<std::mutex> g(T.mu);
+    T.recs.push_back({id, a, b});
+  }
+};
+
+// ------------------------------------------------------------------ GEMM configs
+using moe::EPI_DGRAD_SWIGLU;
+using moe::EPI_ROUTER;
+using moe::EPI_STORE;
+using moe::EPI_SWIGLU;
+using moe::KMAJ_GATHER;
+using moe::KMAJ_TILE;
+using moe::MN_GATHER;
+using moe::MN_TILE;
+using moe::RAGGED_K;
+using moe::RAGGED_M;
+
+template <int BN>
+using CfgRouter = GemmCfg<BN, (BN >= 256 ? 4 : 6), KMAJ_TILE, KMAJ_TILE, RAGGED_M, EPI_ROUTER, false, false>;
+using CfgGateUp = GemmCfg<256, 4, KMAJ_GATHER, KMAJ_TILE, RAGGED_M, EPI_SWIGLU, true, true>;
+using CfgGateUpShared = GemmCfg<256, 4, KMAJ_TILE, KMAJ_TILE, RAGGED_M, EPI_SWIGLU, false, true>;
+using CfgDown = GemmCfg<256, 4, KMAJ_TILE, KMAJ_TILE, RAGGED_M, EPI_STORE, true, false>;
+using CfgDownShared = GemmCfg<256, 4, KMAJ_TILE, KMAJ_TILE, RAGGED_M, EPI_STORE, false, false>;
+using CfgDgradDown = GemmCfg<256, 4, KMAJ_GATHER, MN_TILE, RAGGED_M, EPI_DGRAD_SWIGLU, true, false>;
+using CfgDgradDownShared =
+    GemmCfg<256, 4, KMAJ_TILE, MN_TILE, RAGGED_M, EPI_DGRAD_SWIGLU, false, false>;
+using CfgDgradGateUp = GemmCfg<256, 4, KMAJ_TILE, MN_TILE, RAGGED_M, EPI_STORE, true, false>;
+using CfgDgradGateUpShared = GemmCfg<256, 4, KMAJ_TILE, MN_TILE, RAGGED_M, EPI_STORE, false, false>;
+using CfgWgradDown = GemmCfg<256, 4, MN_GATHER, MN_TILE, RAGGED_K, EPI_STORE, false, false>;
+using CfgWgradGateUp = GemmCfg<256, 4, MN_TILE, MN_GATHER, RAGGED_K, EPI_STORE, false, false>;
+using CfgWgradShared = GemmCfg<256, 4, MN_TILE, MN_TILE, RAGGED_K, EPI_STORE, false, false>;
+
+template <class C>
+moe_status launch_gemm(int kid, const CUtensorMap& A, const CUtensorMap& B, const GemmArgs& a,
+                       long long tile_bound, cudaStream_t st) {
+  static std::atomic<uint64_t> configured{0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(configured.load() & bit)) {
+    if (cudaFuncSetAttribute(moe::grouped_gemm_kernel<C>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::SMEM_BYTES) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    configured.fetch_or(bit);
+  }
+  long long grid = sm_count();
+  if (tile_bound < grid) grid = tile_bound;
+  if (grid < 1) return MOE_OK;
+  KernelScope ks(kid, st);
+  moe::grouped_gemm_kernel<C><<<(int)grid, moe::kGemmThreads, C::SMEM_BYTES, st>>>(A, B, a);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+GemmArgs base_args(int* status) {
+  GemmArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.a_idx_div = a.b_idx_div = 1;
+  a.status = status;
+  return a;
+}
+
+long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
+
+
+
+moe_status launched(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+}  // namespace
+
+// =====================================================================================
+extern "C" {
+
+int32_t moe_abi_version(void) { return kAbiVersion; }
+
+const char* moe_status_string(int32_t s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument (null pointer, misalignment or bad enum)";
+    case MOE_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case MOE_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case MOE_ERR_CUDA: return "CUDA call failed";
+    case MOE_ERR_DEVICE_INDEX: return "device saw an expert id outside [0, E)";
+    case MOE_ERR_TIMEOUT: return "device-side wait timed out";
+    default: return "unknown status";
+  }
+}
+
+moe_status moe_workspace_size(const moe_dims* d, int32_t with_backward, size_t* bytes) {
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  const moe_status s = check_dims(d);
+  if (s != MOE_OK) return s;
+  *bytes = make_layout(*d, with_backward != 0).total;
+  return MOE_OK;
+}
+
+moe_status moe_route(const moe_dims* d, int32_t gate_mode, const moe_bf16* x,
+                     const moe_bf16* w_router, const float* router_bias, float* logits_out,
+                     int32_t* topk_idx, float* topk_w, void* workspace, size_t workspace_bytes,
+                     void* stream) {
+  moe_status s = check_dims(d);
+  if (s != MOE_OK) return s;
+  if (gate_mode != MOE_GATE_SOFTMAX_TOPK && gate_mode != MOE_GATE_BALANCED)
+    return MOE_ERR_INVALID_ARG;
+  if (!x || !w_router || !topk_idx || !topk_w || !workspace) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w_router) || !aligned16(workspace)) return MOE_ERR_INVALID_ARG;
+  if (workspace_bytes < kAlign) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int bn = 16;
+  while (bn < d->E) bn *= 2;
+  CUtensorMap tA, tB;
+  if (!make_map(&tA, x, d->H, d->T, 1, 64, 128)) return MOE_ERR_CUDA;
+  if (!make_map(&tB, w_router, d->H, d->E, 1, 64, bn)) return MOE_ERR_CUDA;
+  GemmArgs a = base_args(at<int>(workspace, 0));
+  a.N = d->E;
+  a.K = d->H;
+  a.G = 1;
+  a.single_rows = d->T;
+  a.bias = router_bias;
+  a.logits_out = logits_out;
+  a.topk_idx = topk_idx;
+  a.topk_w = topk_w;
+  a.E = d->E;
+  a.k = d->k;
+  a.gate_mode = gate_mode;
+  const long long tiles = cdiv(d->T, moe::BM);
+  switch (bn) {
+    case 16: return launch_gemm<CfgRouter<16>>(MOE_K_ROUTER, tA, tB, a, tiles, st);
+    case 32: return launch_gemm<CfgRouter<32>>(MOE_K_ROUTER, tA, tB, a, tiles, st);
+    case 64: return launch_gemm<CfgRouter<64>>(MOE_K_ROUTER, tA, tB, a, tiles, st);
+    case 128: return launch_gemm<CfgRouter<128>>(MOE_K_ROUTER, tA, tB, a, tiles, st);
+    default: return launch_gemm<CfgRouter<256>>(MOE_K_ROUTER, tA, tB, a, tiles, st);
+  }
+}
+
+moe_status moe_permute(const moe_dims* d, const int32_t* topk_idx, int32_t* expert_offsets,
+                       int32_t* perm_slot, int32_t* slot_perm, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  moe_status s = check_dims(d);
+  if (s != MOE_OK) return s;
+  if (!topk_idx || !expert_offsets || !perm_slot || !slot_perm || !workspace)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(workspace)) return MOE_ERR_INVALID_ARG;
+  const Layout L = make_layout(*d, false);
+  if (workspace_bytes < L.h) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int32_t* counts = at<int32_t>(workspace, L.counts);
+  { KernelScope ks(MOE_K_SORT_HISTOGRAM, st);
+  moe::sort_histogram_kernel<<<L.sort_blocks, moe::kSortThreads, 0, st>>>(
+      topk_idx, (int)L.S, d->E, counts, at<int>(workspace, 0)); }
+  { KernelScope ks(MOE_K_SORT_SCATTER, st);
+  moe::sort_scatter_kernel<<<L.sort_blocks, moe::kSortThreads, 0, st>>>(
+      topk_idx, (int)L.S, d->E, L.sort_blocks, counts, expert_offsets, perm_slot, slot_perm); }
+  return launched(cudaGetLastError());
+}
+
+moe_status moe_grouped_mlp_fwd(const moe_dims* d, const moe_bf16* x,
+                               const int32_t* expert_offsets, const int32_t* perm_slot,
+                               const moe_bf16* w_gate_up, const moe_bf16* w_down,
+                               moe_bf16* gu_saved, moe_bf16* y_perm,
+                               const moe_bf16* w_sh_gate_up, const moe_bf16* w_sh_down,
+                               moe_bf16* sh_gu_saved, moe_bf16* y_shared, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+  moe_status s = check_dims(d);
+  if (s != MOE_OK) return s;
+  if (!x || !expert_offsets || !perm_slot || !w_gate_up || !w_down || !y_perm || !workspace)
+    return MOE_ERR_INVALID_ARG;
+  if (d->I_shared > 0 && (!w_sh_gate_up || !w_sh_down || !y_shared)) return MOE_ERR_INVALID_ARG;
+  for (const void* p : {(const void*)x, (const void*)w_gate_up, (const void*)w_down,
+                        (const void*)gu_saved, (const void*)y_perm, (const void*)w_sh_gate_up,
+                        (const void*)w_sh_down, (const void*)sh_gu_saved, (const void*)y_shared,
+                        (const void*)workspace})
+    if (!aligned16(p)) return MOE_ERR_INVALID_ARG;
+  const Layout L = make_layout(*d, false);
+  if (workspace_bytes < L.fwd_end) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int* status = at<int>(workspace, 0);
+  __nv_bfloat16* h = at<__nv_bfloat16>(workspace, L.h);
+  const int T = d->T, H = d->H, E = d->E, I = d->I;
+  const long long S = L.S;
+  {  // gate/up grouped GEMM + SwiGLU
+    CUtensorMap tA, tB;
+    if (!make_map(&tA, x, H, T, 1, 64, 1)) return MOE_ERR_CUDA;
+    if (!make_map3(&tB, w_gate_up, H, 2LL * I, E, 64, 128)) return MOE_ERR_CUDA;
+    GemmArgs a = base_args(status);
+    a.N = 2 * I; a.K = H; a.G = E; a.offsets = expert_offsets;
+    a.a_idx = perm_slot; a.a_idx_div = d->k; a.a_idx_len = (int)S; a.a_src_rows = T;
+    a.gu_out = reinterpret_cast<__nv_bfloat16*>(gu_saved); a.h_out = h; a.inter = I;
+    s = launch_gemm<CfgGateUp>(MOE_K_GATE_UP, tA, tB, a, (cdiv(S, moe::BM) + E) * cdiv(I, 128), st);
+    if (s != MOE_OK) return s;
+  }
+  {  // down grouped GEMM
+    CUtensorMap tA, tB;
+    if (!make_map(&tA, h, I, S, 1, 64, 128)) return MOE_ERR_CUDA;
+    if (!make_map3(&tB, w_down, I, H, E, 64, 128)) return MOE_ERR_CUDA;
+    GemmArgs a = base_args(status);
+    a.N = H; a.K = I; a.G = E; a.offsets = expert_offsets;
+    a.d = reinterpret_cast<__nv_bfloat16*>(y_perm); a.ldd = H;
+    s = launch_gemm<CfgDown>(MOE_K_DOWN, tA, tB, a, (cdiv(S, moe::BM) + E) * cdiv(H, 256), st);
+    if (s != MOE_OK) return s;
+  }
+  if (d->I_shared > 0) {
+    const int Is = d->I_shared;
+    __nv_bfloat16* hs = at<__nv_bfloat16>(workspace, L.h_sh);
+    {
+      CUtensorMap tA, tB;
+      if (!make_map(&tA, x, H, T, 1, 64, 128)) return MOE_ERR_CUDA;
+      if (!make_map(&tB, w_sh_gate_up, H, 2LL * Is, 1, 64, 128)) return MOE_ERR_CUDA;
+      GemmArgs a = base_args(status);
+      a.N = 2 * Is; a.K = H; a.G = 1; a.single_rows = T;
+      a.gu_out = reinterpret_cast<__nv_bfloat16*>(sh_gu_saved); a.h_out = hs; a.inter = Is;
+      s = launch_gemm<CfgGateUpShared>(MOE_K_SHARED_GATE_UP, tA, tB, a, cdiv(T, moe::BM) * cdiv(Is, 128), st);
+      if (s != MOE_OK) return s;
+    }
+    {
+      CUtensorMap tA, tB;
+      if (!make_map(&tA, hs, Is, T, 1, 64, 128)) return MOE_ERR_CUDA;
+      if (!make_map(&tB, w_sh_down, Is, H, 1, 64, 128)) return MOE_ERR_CUDA;
+      GemmArgs a = base_args(status);
+      a.N = H; a.K = Is; a.G = 1; a.single_rows = T;
+      a.d = reinterpret_cast<__nv_bfloat16*>(y_shared); a.ldd = H;
+      s = launch_gemm<CfgDownShared>(MOE_K_SHARED_DOWN, tA, tB, a, cdiv(T, moe::BM) * cdiv(H, 256), st);
+      if (s != MOE_OK) return s;
+    }
+  }
+  return MOE_OK;
+}
+
+moe_status moe_unpermute_combine(const moe_dims* d, const moe_bf16* y_perm,
+                                 const int32_t* slot_perm, const float* topk_w,
+                                 const moe_bf16* y_shared, moe_bf16* out, void* stream) {
+  moe_status s = check_dims(d);
+  if (s != MOE_OK) return s;
+  if (!y_perm || !slot_perm || !topk_w || !out) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(y_perm) || !aligned16(out) || !aligned16(y_shared)) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int threads = 256;
+  const long long blocks = cdiv((long long)d->T * 32, threads);
+  KernelScope ks(MOE_K_COMBINE, st);
+  moe::combine_kernel<<<(unsigned)blocks, threads, 0, st>>>(
+      reinterpret_cast<const __nv_bfloat16*>(y_perm), slot_perm, topk_w,
+      reinterpret_cast<const __nv_bfloat16*>(y_shared), reinterpret_cast<__nv_bfloat16*>(out),
+      d->T, d->H, d->k, d->T * d->k);
+  return launched(cudaGetLastError());
+}
+
+moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_bf16* x,
+                         const moe_bf16* w_router, const int32_t* topk_idx, const float* topk_w,
+                         const int32_t* expert_offsets, const int32_t* perm_slot,
+                         const int32_t* slot_perm, const moe_bf16* w_gate_up,
+                         const moe_bf16* w_down, const moe_bf16* gu_saved,
+                         const moe_bf16* w_sh_gate_up, const moe_bf16* w_sh_down,
+                         const moe_bf16* sh_gu_saved, moe_bf16* grad_x, moe_bf16* grad_w_router,
+                         float* grad_router_bias, moe_bf16* grad_w_gate_up,
+                         moe_bf16* grad_w_down, moe_bf16* grad_w_sh_gate_up,
+                         moe_bf16* grad_w_sh_down, void* workspace, size_t workspace_bytes,
+                         void* stream) {
+  moe_status s = check_dims(d);
+  if (s != MOE_OK) return s;
+  if (!grad_out || !x || !w_router || !topk_idx || !topk_w || !expert_offsets || !perm_slot ||
+      !slot_perm || !w_gate_up || !w_down || !gu_saved || !grad_x || !grad_w_router ||
+      !grad_w_gate_up || !grad_w_down || !workspace)
+    return MOE_ERR_INVALID_ARG;
+  if (d->I_shared > 0 && (!w_sh_gate_up || !w_sh_down || !sh_gu_saved || !grad_w_sh_gate_up ||
+                          !grad_w_sh_down))
+    return MOE_ERR_INVALID_ARG;
+  for (const void* p : {(const void*)grad_out, (const void*)x, (const void*)w_router,
+                        (const void*)w_gate_up, (const void*)w_down, (const void*)gu_saved,
+                        (const void*)w_sh_gate_up, (const void*)w_sh_down,
+                        (const void*)sh_gu_saved, (const void*)grad_x,
+                        (const void*)grad_w_router, (const void*)grad_w_gate_up,
+                        (const void*)grad_w_down, (const void*)grad_w_sh_gate_up,
+                        (const void*)grad_w_sh_down, (const void*)workspace})
+    if (!aligned16(p)) return MOE_ERR_INVALID_ARG;
+  const Layout L = make_layout(*d, true);
+  if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int* status = at<int>(workspace, 0);
+  const int T = d->T, H = d->H, E = d->E, I = d->I, k = d->k;
+  const long long S = L.S, P = L.S_pad_max;
+  int32_t* poff = at<int32_t>(workspace, L.poff);
+  int32_t* row_tok = at<int32_t>(workspace, L.row_tok);
+  __nv_bfloat16* dgu = at<__nv_bfloat16>(workspace, L.dgu);
+  __nv_bfloat16* hw = at<__nv_bfloat16>(workspace, L.hw);
+  __nv_bfloat16* dxs = at<__nv_bfloat16>(workspace, L.dxs);
+  float* dwp = at<float>(workspace, L.dwp);
+  float* dl = at<float>(workspace, L.dl);
+
+  { KernelScope ks(MOE_K_PAD_OFFSETS, st);
+    moe::pad_offsets_kernel<<<1, 32, 0, st>>>(expert_offsets, E, poff); }
+  KernelScope ks_rows(MOE_K_PADDED_ROWS, st);
+  moe::padded_row_tokens_kernel<<<(unsigned)cdiv(P, 256), 256, 0, st>>>(
+      expert_offsets, poff, perm_slot, E, k, (int)P, row_tok);
+  if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+
+  {  // down-projection data gradient + SwiGLU backward (+ dw partials)
+    CUtensorMap tA, tB;
+    if (!make_map(&tA, grad_out, H, T, 1, 64, 1)) return MOE_ERR_CUDA;
+    if (!make_map3(&tB, w_down, I, H, E, 64, 64)) return MOE_ERR_CUDA;
+    GemmArgs a = base_args(status);
+    a.N = I; a.K = H; a.G = E; a.offsets = expert_offsets; a.padded = 1;
+    a.a_idx = row_tok; a.a_idx_len = (int)P; a.a_src_rows = T;
+    a.inter = I; a.gu_saved = reinterpret_cast<const __nv_bfloat16*>(gu_saved);
+    a.perm_slot = perm_slot; a.slot_w = topk_w; a.dgu_out = dgu; a.hw_out = hw; a.dw_part = dwp;
+    s = launch_gemm<CfgDgradDown>(MOE_K_DGRAD_DOWN, tA, tB, a, cdiv(P, moe::BM) * L.nNB_I, st);
+    if (s != MOE_OK) return s;
+  }
+  { KernelScope ks(MOE_K_ROUTER_BWD, st);
+  moe::router_backward_kernel<<<(unsigned)cdiv(T, 128), 128, 0, st>>>(
+      topk_idx, topk_w, slot_perm, expert_offsets, poff, dwp, L.nNB_I, T, k, E, (int)P, dl); }
+  if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+  {  // gate/up data gradient -> per-slot dx
+    CUtensorMap tA, tB;
+    if (!make_map(&tA, dgu, 2LL * I, P, 1, 64, 128)) return MOE_ERR_CUDA;
+    if (!make_map3(&tB, w_gate_up, H, 2LL * I, E, 64, 64)) return MOE_ERR_CUDA;
+    GemmArgs a = base_args(status);
+    a.N = H; a.K = 2 * I; a.G = E; a.offsets = expert_offsets; a.padded = 1;
+    a.d = dxs; a.ldd = H;
+    s = launch_gemm<CfgDgradGateUp>(MOE_K_DGRAD_GATE_UP, tA, tB, a, cdiv(P, moe::BM) * cdiv(H, 256), st);
+    if (s != MOE_OK) return s;
+  }
+  __nv_bfloat16* dxs_sh = nullptr;
+  if (d->I_shared > 0) {
+    const int Is = d->I_shared;
+    __nv_bfloat16* dgu_sh = at<__nv_bfloat16>(workspace, L.dgu_sh);
+    __nv_bfloat16* hw_sh = at<__nv_bfloat16>(workspace, L.hw_sh);
+    dxs_sh = at<__nv_bfloat16>(workspace, L.dxs_sh);
+    {
+      CUtensorMap tA, tB;
+      if (!make_map(&tA, grad_out, H, T, 1, 64, 128)) return MOE_ERR_CUDA;
+      if (!make_map(&tB, w_sh_down, Is, H, 1, 64, 64)) return MOE_ERR_CUDA;
+      GemmArgs a = base_args(status);
+      a.N = Is; a.K = H; a.G = 1; a.single_rows = T;
+      a.inter = Is; a.gu_saved = reinterpret_cast<const __nv_bfloat16*>(sh_gu_saved);
+      a.dgu_out = dgu_sh; a.hw_out = hw_sh;
+      s = launch_gemm<CfgDgradDownShared>(MOE_K_SHARED_DGRAD_DOWN, tA, tB, a, cdiv(T, moe::BM) * cdiv(Is, 256), st);
+      if (s != MOE_OK) return s;
+    }
+    {
+      CUtensorMap tA, tB;
+      if (!make_map(&tA, dgu_sh, 2LL * Is, T, 1, 64, 128)) return MOE_ERR_CUDA;
+      if (!make_map(&tB, w_sh_gate_up, H, 2LL * Is, 1, 64, 64)) return MOE_ERR_CUDA;
+      GemmArgs a = base_args(status);
+      a.N = H; a.K = 2 * Is; a.G = 1; a.single_rows = T;
+      a.d = dxs_sh; a.ldd = H;
+      s = launch_gemm<CfgDgradGateUpShared>(MOE_K_SHARED_DGRAD_GATE_UP, tA, tB, a, cdiv(T, moe::BM) * cdiv(H, 256), st);
+      if (s != MOE_OK) return s;
+    }
+  }
+  { KernelScope ks(MOE_K_DX_GATHER, st);
+  moe::dx_gather_kernel<<<(unsigned)cdiv((long long)T * 32, 256), 256, 0, st>>>(
+      dxs, topk_idx, slot_perm, expert_offsets, poff, dl,
+      reinterpret_cast<const __nv_bfloat16*>(w_router), dxs_sh,
+      reinterpret_cast<__nv_bfloat16*>(grad_x), T, H, k, E, (int)P); }
+  { KernelScope ks(MOE_K_ROUTER_WGRAD, st);
+  moe::router_wgrad_kernel<<<dim3((unsigned)cdiv(H, 256), E), 128, 0, st>>>(
+      reinterpret_cast<const __nv_bfloat16*>(x), expert_offsets, perm_slot, dl, H, k,
+      reinterpret_cast<__nv_bfloat16*>(grad_w_router), grad_router_bias); }
+  if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+  {  // dW_down[e] = sum over the expert's rows of dout[token]^T (w h)
+    CUtensorMap tA, tB;
+    if (!make_map(&tA, grad_out, H, T, 1, 64, 1)) return MOE_ERR_CUDA;
+    if (!make_map(&tB, hw, I, P, 1, 64, 64)) return MOE_ERR_CUDA;
+    GemmArgs a = base_args(status);
+    a.M = H; a.N = I; a.G = E; a.offsets = expert_offsets; a.padded = 1;
+    a.a_idx = row_tok; a.a_idx_len = (int)P; a.a_src_rows = T;
+    a.d = reinterpret_cast<__nv_bfloat16*>(grad_w_down); a.ldd = I;
+    a.d_group_stride = (long long)H * I;
+    s = launch_gemm<CfgWgradDown>(MOE_K_WGRAD_DOWN, tA, tB, a, (long long)E * cdiv(H, moe::BM) * cdiv(I, 256), st);
+    if (s != MOE_OK) return s;
+  }
+  {  // dW_gu[e] = sum over the expert's rows of [dg|du]^T x[token]
+    CUtensorMap tA, tB;
+    if (!make_map(&tA, dgu, 2LL * I, P, 1, 64, 64)) return MOE_ERR_CUDA;
+    if (!make_map(&tB, x, H, T, 1, 64, 1)) return MOE_ERR_CUDA;
+    GemmArgs a = base_args(status);
+    a.M = 2 * I; a.N = H; a.G = E; a.offsets = expert_offsets; a.padded = 1;
+    a.b_idx = row_tok; a.b_idx_len = (int)P; a.b_src_rows = T;
+    a.d = reinterpret_cast<__nv_bfloat16*>(grad_w_gate_up); a.ldd = H;
+    a.d_group_stride = 2LL * I * H;
+    s = launch_gemm<CfgWgradGateUp>(MOE_K_WGRAD_GATE_UP, tA, tB, a,
+                                    (long long)E * cdiv(2 * I, moe::BM) * cdiv(H, 256), st);
+    if (s != MOE_OK) return s;
+  }
+  if (d->I_shared > 0) {
+    const int Is = d->I_shared;
+    __nv_bfloat16* dgu_sh = at<__nv_bfloat16>(workspace, L.dgu_sh);
+    __nv_bfloat16* hw_sh = at<__nv_bfloat16>(workspace, L.hw_sh);
+    {
+      CUtensorMap tA, tB;
+      if (!make_map(&tA, grad_out, H, T, 1, 64, 64)) return MOE_ERR_CUDA;
+      if (!make_map(&tB, hw_sh, Is, T, 1, 64, 64)) return MOE_ERR_CUDA;
+      GemmArgs a = base_args(status);
+      a.M = H; a.N = Is; a.G = 1; a.single_rows = T;
+      a.d = reinterpret_cast<__nv_bfloat16*>(grad_w_sh_down); a.ldd = Is;
+      s = launch_gemm<CfgWgradShared>(MOE_K_SHARED_WGRAD_DOWN, tA, tB, a, cdiv(H, moe::BM) * cdiv(Is, 256), st);
+      if (s != MOE_OK) return s;
+    }
+    {
+      CUtensorMap tA, tB;
+      if (!make_map(&tA, dgu_sh, 2LL * Is, T, 1, 64, 64)) return MOE_ERR_CUDA;
+      if (!make_map(&tB, x, H, T, 1, 64, 64)) return MOE_ERR_CUDA;
+      GemmArgs a = base_args(status);
+      a.M = 2 * Is; a.N = H; a.G = 1; a.single_rows = T;
+      a.d = reinterpret_cast<__nv_bfloat16*>(grad_w_sh_gate_up); a.ldd = H;
+      s = launch_gemm<CfgWgradShared>(MOE_K_SHARED_WGRAD_GATE_UP, tA, tB, a, cdiv(2 * Is, moe::BM) * cdiv(H, 256), st);
+      if (s != MOE_OK) return s;
+    }
+  }
+  return MOE_OK;
+}
+
+int32_t moe_kernel_count(void) { return MOE_K_COUNT; }
+
+const char* moe_kernel_name(int32_t id) {
+  static const char* names[MOE_K_COUNT] = {
+      "router", "sort_histogram", "sort_scatter", "gate_up", "down", "shared_gate_up",
+      "shared_down", "combine", "pad_offsets", "padded_rows", "dgrad_down", "router_bwd",
+      "dgrad_gate_up", "shared_dgrad_down", "shared_dgrad_gate_up", "dx_gather",
+      "router_wgrad", "wgrad_down", "wgrad_gate_up", "shared_wgrad_down",
+      "shared_wgrad_gate_up"};
+  return (id >= 0 && id < MOE_K_COUNT) ? names[id] : "unknown";
+}
+
+moe_status moe_timing_enable(int32_t on) {
+  Timing& T = timing();
+  std::lock_guard<std::mutex> g(T.mu);
+  T.on = on != 0;
+  return MOE_OK;
+}
+
+moe_status moe_kernel_stats(int32_t reset, int64_t* launches, double* event_ms) {
+  Timing& T = timing();
+  std::lock_guard<std::mutex> g(T.mu);
+  moe_status st = MOE_OK;
+  if (launches)
+    for (int i = 0; i < MOE_K_COUNT; ++i) launches[i] = T.launches[i].load();
+  if (event_ms) {
+    for (int i = 0; i < MOE_K_COUNT; ++i) event_ms[i] = 0.0;
+    for (const auto& r : T.recs) {
+      float ms = 0.f;
+      if (cudaEventSynchronize(r.b) != cudaSuccess || cudaEventElapsedTime(&ms, r.a, r.b) != cudaSuccess) {
+        st = MOE_ERR_CUDA;
+        continue;
+      }
+      event_ms[r.id] += ms;
+    }
+  }
+  if (reset) {
+    for (auto& l : T.launches) l.store(0);
+    for (const auto& r : T.recs) {
+      T.pool.push_back(r.a);
+      T.pool.push_back(r.b);
+    }
+    T.recs.clear();
+  }
+  return st;
+}
+
+moe_status moe_read_device_status(void* workspace, size_t workspace_bytes, void* stream,
+                                  int32_t clear, int32_t* device_status) {
+  if (!workspace || !device_status) return MOE_ERR_INVALID_ARG;
+  if (workspace_bytes < kAlign) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  if (cudaMemcpyAsync(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (clear) {
+    if (cudaMemsetAsync(workspace, 0, sizeof(int32_t), st) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  *device_status = v;
+  return MOE_OK;
+}
+
+}  // extern "C"

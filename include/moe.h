@@ -1,0 +1,246 @@
+/*
+ * moe.h — C ABI of the B300 (sm_103a) MoE expert layer.
+ *
+ * The layer is the single-GPU expert block behind the "grouped_mm" expert
+ * backend: a router picks k experts per token, the token-slots are sorted by
+ * expert, each expert's SwiGLU MLP runs as one grouped GEMM over its rows
+ * without copying any expert parameters, and the expert outputs are combined
+ * back per token with the router weights; forward and backward.
+ *
+ * Source: NeMo AutoModel blog (zh-CN / ja translations of "Accelerating
+ * Transformers fine-tuning with NVIDIA NeMo AutoModel"), table
+ * "专家后端 / エキスパートバックエンド" (expert backends), grouped_mm row:
+ * sort the tokens by assigned expert and run a single grouped GEMM, memory
+ * efficient, no parameter copies; "v4 死锁原因" (why v4 deadlocks): experts
+ * are fused 3-D parameter tensors; "关于路由门的说明" (note on the routing
+ * gate): the balanced gate forces tokens evenly across experts.  Readings of
+ * what the pages leave open (router formula, activation, gate rule) are given
+ * at each call.
+ *
+ * Conventions for every call
+ *   - All tensor arguments are DEVICE pointers to row-major, densely packed
+ *     arrays owned by the caller.  bf16 tensors are raw bfloat16 bits
+ *     (moe_bf16) and must be 16-byte aligned.  The library never allocates,
+ *     frees or copies expert weights; weights are read-only.
+ *   - Every compute call is asynchronous on `stream` (a cudaStream_t; NULL is
+ *     the legacy default stream) and never synchronises, except
+ *     moe_read_device_status.
+ *   - Host-side validation happens before anything is launched; a rejected
+ *     call launches nothing and returns MOE_ERR_INVALID_ARG,
+ *     MOE_ERR_UNSUPPORTED_SHAPE or MOE_ERR_WORKSPACE_TOO_SMALL.  A failed
+ *     launch returns MOE_ERR_CUDA.  Problems found on the device (an expert
+ *     id outside [0, E), a wait that ran out of time) are written to the
+ *     status word in the workspace; read it with moe_read_device_status.
+ *     There is no CPU fallback.
+ *   - Deterministic: identical inputs give bit-identical outputs.
+ *
+ * Shapes: T tokens, H hidden, E experts, k experts per token, I expert
+ * intermediate size, I_shared intermediate size of the optional always-on
+ * shared expert (0 = none), S = T*k token-slots, slot s = t*k + j.
+ * Supported: 1 <= E <= 256, 1 <= k <= min(E, 32), H and I (and I_shared when
+ * non-zero) positive multiples of 64, T >= 1, T*k < 2^31.
+ */
+#ifndef MOE_B300_H
+#define MOE_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t moe_bf16; /* raw bfloat16 bits */
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,         /* null pointer, misalignment, bad enum */
+  MOE_ERR_UNSUPPORTED_SHAPE = 2,   /* dims outside the supported set above */
+  MOE_ERR_WORKSPACE_TOO_SMALL = 3, /* workspace_bytes < moe_workspace_size() */
+  MOE_ERR_CUDA = 4,                /* a CUDA runtime/driver call failed */
+  MOE_ERR_DEVICE_INDEX = 5,        /* device saw an expert id outside [0, E) */
+  MOE_ERR_TIMEOUT = 6              /* a device-side wait ran out of time */
+} moe_status;
+
+typedef enum {
+  MOE_GATE_SOFTMAX_TOPK = 0, /* learned router: softmax, top-k, renormalise */
+  MOE_GATE_BALANCED = 1      /* balanced gate: slot (t,j) -> expert (t*k+j) mod E */
+} moe_gate_mode;
+
+typedef struct {
+  int32_t T, H, E, k, I, I_shared;
+} moe_dims;
+
+/* Version of this ABI (bumped on any signature change). */
+int32_t moe_abi_version(void);
+
+/* Static text for a moe_status value. */
+const char* moe_status_string(int32_t status);
+
+/*
+ * Bytes of device workspace the calls below need for these dims.  One
+ * workspace can serve moe_route, moe_permute, moe_grouped_mlp_fwd and (when
+ * with_backward != 0) moe_layer_bwd.  The first 256 bytes hold the device
+ * status word; callers zero them once (cudaMemset) before first use.
+ * Errors: MOE_ERR_INVALID_ARG (null), MOE_ERR_UNSUPPORTED_SHAPE.
+ */
+moe_status moe_workspace_size(const moe_dims* d, int32_t with_backward, size_t* bytes);
+
+/*
+ * Router (note on the routing gate; the pages name the native router but not
+ * its formula — reading used here):
+ *   logits[t,e] = sum_h x[t,h] W_r[e,h] + bias[e]     (fp32 accumulate)
+ *   p[t,:] = softmax(logits[t,:]) over all E experts
+ *   SOFTMAX_TOPK: topk_idx[t,0..k-1] = the k largest logits, largest first,
+ *                 equal logits -> lower expert id first
+ *   BALANCED:     topk_idx[t,j] = (t*k + j) mod E  (exactly T*k/E slots per
+ *                 expert when E divides T*k; distinct experts when k <= E)
+ *   topk_w[t,j] = p[t,topk_idx[t,j]] / sum_j' p[t,topk_idx[t,j']]
+ * x: bf16 [T,H]; w_router: bf16 [E,H]; router_bias: fp32 [E] or NULL;
+ * logits_out: fp32 [T,E] or NULL; topk_idx: int32 [T,k]; topk_w: fp32 [T,k].
+ */
+moe_status moe_route(const moe_dims* d, int32_t gate_mode, const moe_bf16* x,
+                     const moe_bf16* w_router, const float* router_bias, float* logits_out,
+                     int32_t* topk_idx, float* topk_w, void* workspace, size_t workspace_bytes,
+                     void* stream);
+
+/*
+ * Sort the token-slots by expert (grouped_mm row: "sort the tokens by their
+ * assigned expert"): a stable counting sort of s = 0..S-1 by topk_idx[s].
+ *   expert_offsets: int32 [E+1], expert e owns sorted rows
+ *                   expert_offsets[e] .. expert_offsets[e+1]-1; offsets[E] = S
+ *   perm_slot:      int32 [S], slot id at sorted row r (ascending within an expert)
+ *   slot_perm:      int32 [S], sorted row of slot s (inverse of perm_slot)
+ * Only ids move; no expert weight is touched.  Expert ids outside [0, E) are
+ * skipped and reported as MOE_ERR_DEVICE_INDEX in the status word.
+ */
+moe_status moe_permute(const moe_dims* d, const int32_t* topk_idx, int32_t* expert_offsets,
+                       int32_t* perm_slot, int32_t* slot_perm, void* workspace,
+                       size_t workspace_bytes, void* stream);
+
+/*
+ * Grouped expert MLP on the sorted rows (grouped_mm row: one grouped GEMM per
+ * projection over the expert-sorted tokens, no parameter copies).  For sorted
+ * row r of expert e, with token t = perm_slot[r] / k:
+ *   [g | u] = x[t] W_gu[e]^T        (W_gu[e] rows 0..I-1 = gate, I..2I-1 = up)
+ *   h = silu(g) * u                  (SwiGLU; the pages do not name the activation)
+ *   y_perm[r] = h W_down[e]^T
+ * w_gate_up: bf16 [E,2I,H]; w_down: bf16 [E,H,I] (fused 3-D expert tensors,
+ * "v4 死锁原因"); gu_saved: bf16 [S,2I] pre-activations for the backward, or
+ * NULL; y_perm: bf16 [S,H].  g, u and h are rounded to bf16 once.
+ * Shared expert (d->I_shared > 0): y_shared[t] = SwiGLU-MLP(x[t]) with
+ * w_sh_gate_up bf16 [2*I_shared,H], w_sh_down bf16 [H,I_shared]; sh_gu_saved
+ * bf16 [T,2*I_shared] or NULL; y_shared bf16 [T,H].  Pass NULLs when
+ * I_shared == 0.
+ */
+moe_status moe_grouped_mlp_fwd(const moe_dims* d, const moe_bf16* x,
+                               const int32_t* expert_offsets, const int32_t* perm_slot,
+                               const moe_bf16* w_gate_up, const moe_bf16* w_down,
+                               moe_bf16* gu_saved, moe_bf16* y_perm,
+                               const moe_bf16* w_sh_gate_up, const moe_bf16* w_sh_down,
+                               moe_bf16* sh_gu_saved, moe_bf16* y_shared, void* workspace,
+                               size_t workspace_bytes, void* stream);
+
+/*
+ * Weighted un-permute / combine (the "combine" half of dispatch-and-combine,
+ * DeepEP paragraphs):
+ *   out[t] = sum_{j=0..k-1} topk_w[t,j] * y_perm[slot_perm[t*k+j]]  (+ y_shared[t])
+ * summed in fp32 in j order, rounded to bf16 once.  y_perm bf16 [S,H];
+ * slot_perm int32 [S]; topk_w fp32 [T,k]; y_shared bf16 [T,H] or NULL;
+ * out bf16 [T,H].  Needs no workspace.
+ */
+moe_status moe_unpermute_combine(const moe_dims* d, const moe_bf16* y_perm,
+                                 const int32_t* slot_perm, const float* topk_w,
+                                 const moe_bf16* y_shared, moe_bf16* out, void* stream);
+
+/*
+ * Backward of the whole layer (the pages time forward+loss and backward
+ * separately, single-node 30B benchmark table; full-parameter fine-tuning
+ * updates every parameter).  Given grad_out = dL/d(out) bf16 [T,H], the
+ * forward's inputs and saved routing (topk_idx, topk_w, expert_offsets,
+ * perm_slot, slot_perm) and saved pre-activations (gu_saved, sh_gu_saved),
+ * writes bf16 gradients:
+ *   grad_x [T,H], grad_w_router [E,H], grad_w_gate_up [E,2I,H],
+ *   grad_w_down [E,H,I], and when I_shared > 0 grad_w_sh_gate_up
+ *   [2*I_shared,H], grad_w_sh_down [H,I_shared]; grad_router_bias fp32 [E]
+ *   or NULL.
+ * SwiGLU is recomputed from the saved (g, u).  Router: the renormalised
+ * top-k weights are a softmax over the chosen logits, so
+ * dlogit[t,e_j] = w_j (dw_j - sum_i w_i dw_i) with dw_j = <dout[t], y_j>,
+ * and top-k selection itself passes no gradient.  Experts that received no
+ * token get exact-zero weight gradients.
+ */
+moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_bf16* x,
+                         const moe_bf16* w_router, const int32_t* topk_idx, const float* topk_w,
+                         const int32_t* expert_offsets, const int32_t* perm_slot,
+                         const int32_t* slot_perm, const moe_bf16* w_gate_up,
+                         const moe_bf16* w_down, const moe_bf16* gu_saved,
+                         const moe_bf16* w_sh_gate_up, const moe_bf16* w_sh_down,
+                         const moe_bf16* sh_gu_saved, moe_bf16* grad_x, moe_bf16* grad_w_router,
+                         float* grad_router_bias, moe_bf16* grad_w_gate_up,
+                         moe_bf16* grad_w_down, moe_bf16* grad_w_sh_gate_up,
+                         moe_bf16* grad_w_sh_down, void* workspace, size_t workspace_bytes,
+                         void* stream);
+
+/*
+ * Synchronise `stream`, then copy the workspace's device status word to
+ * *device_status (a moe_status value; MOE_OK if nothing was recorded).  When
+ * clear != 0 the word is reset to MOE_OK afterwards.  For tests and
+ * debugging; this is the only call that synchronises.
+ */
+moe_status moe_read_device_status(void* workspace, size_t workspace_bytes, void* stream,
+                                  int32_t clear, int32_t* device_status);
+
+/*
+ * Kernel accounting, for benchmarks and tests (no counterpart on the pages).
+ * Every kernel the calls above launch is counted under one of the ids below.
+ * While timing is enabled, each launch is also bracketed by a pair of CUDA
+ * events recorded on the launch stream.
+ */
+typedef enum {
+  MOE_K_ROUTER = 0,          /* moe_route: router GEMM + softmax/top-k epilogue */
+  MOE_K_SORT_HISTOGRAM,      /* moe_permute, pass 1 */
+  MOE_K_SORT_SCATTER,        /* moe_permute, pass 2 */
+  MOE_K_GATE_UP,             /* grouped gate/up GEMM + SwiGLU */
+  MOE_K_DOWN,                /* grouped down GEMM */
+  MOE_K_SHARED_GATE_UP,      /* shared expert gate/up GEMM + SwiGLU */
+  MOE_K_SHARED_DOWN,         /* shared expert down GEMM */
+  MOE_K_COMBINE,             /* weighted un-permute / combine */
+  MOE_K_PAD_OFFSETS,         /* backward: padded expert offsets */
+  MOE_K_PADDED_ROWS,         /* backward: token of every padded row */
+  MOE_K_DGRAD_DOWN,          /* backward: down data-gradient + SwiGLU backward */
+  MOE_K_ROUTER_BWD,          /* backward: router logit gradient */
+  MOE_K_DGRAD_GATE_UP,       /* backward: gate/up data-gradient (per slot) */
+  MOE_K_SHARED_DGRAD_DOWN,
+  MOE_K_SHARED_DGRAD_GATE_UP,
+  MOE_K_DX_GATHER,           /* backward: per-token sum of slot gradients + router term */
+  MOE_K_ROUTER_WGRAD,        /* backward: router weight (and bias) gradient */
+  MOE_K_WGRAD_DOWN,          /* backward: grouped down weight-gradient GEMM */
+  MOE_K_WGRAD_GATE_UP,       /* backward: grouped gate/up weight-gradient GEMM */
+  MOE_K_SHARED_WGRAD_DOWN,
+  MOE_K_SHARED_WGRAD_GATE_UP,
+  MOE_K_COUNT
+} moe_kernel_id;
+
+/* Number of kernel ids (MOE_K_COUNT) and a static name for each. */
+int32_t moe_kernel_count(void);
+const char* moe_kernel_name(int32_t id);
+
+/* Turn per-launch event timing on or off (host-side state shared by all
+ * streams of the process).  Events are created lazily and reused. */
+moe_status moe_timing_enable(int32_t on);
+
+/*
+ * launches[i]: kernels of id i launched since the last reset (always
+ * counted).  event_ms[i]: summed event-timed duration of the launches of id i
+ * recorded while timing was enabled (waits for those events to complete).
+ * Either array (length moe_kernel_count()) may be NULL.  reset != 0 clears
+ * both afterwards.  Errors: MOE_ERR_CUDA if an event query fails.
+ */
+moe_status moe_kernel_stats(int32_t reset, int64_t* launches, double* event_ms);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_B300_H */

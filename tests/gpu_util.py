@@ -1,0 +1,103 @@
+"""Helpers shared by the GPU parity tests: device upload of the seeded inputs,
+running the layer through the C ABI, and the bf16 tolerance check.
+
+Tolerance (bf16 outputs and gradients, fp32 accumulation): relative L2 error
+<= 1e-2 and max-abs error <= 2e-2 * max|reference|.  The absolute bound is
+scaled by the reference magnitude because the tiny workload's outputs are
+~1e-4 (an unscaled 2e-2 would accept anything there) while summed weight
+gradients reach magnitudes where one bf16 rounding alone exceeds 2e-2.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from grouped_expert_gemm_top_b300 import inputs as G
+from grouped_expert_gemm_top_b300 import moe as M
+from oracle import moe_oracle as O
+
+REL_L2 = 1e-2
+MAX_ABS_FRAC = 2e-2
+
+
+def dev_bf16(bits: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def dev_f32(a) -> torch.Tensor | None:
+    return None if a is None else torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).cuda()
+
+
+def to_f64(t: torch.Tensor) -> np.ndarray:
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def check_close(got, ref, name, rel_l2=REL_L2, frac=MAX_ABS_FRAC):
+    got = to_f64(got) if isinstance(got, torch.Tensor) else np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert got.shape == ref.shape, (name, got.shape, ref.shape)
+    assert np.isfinite(got).all(), f"{name}: non-finite values"
+    diff = got - ref
+    nref = np.linalg.norm(ref)
+    rl2 = np.linalg.norm(diff) / (nref if nref > 0 else 1.0)
+    mabs = float(np.abs(diff).max()) if diff.size else 0.0
+    scale = float(np.abs(ref).max()) if ref.size else 0.0
+    if nref == 0:
+        assert mabs == 0.0, f"{name}: expected exact zeros, max-abs {mabs}"
+        return dict(rel_l2=0.0, max_abs=0.0)
+    assert rl2 <= rel_l2, f"{name}: rel-L2 {rl2:.3e} > {rel_l2}"
+    assert mabs <= frac * scale, f"{name}: max-abs {mabs:.3e} > {frac} * {scale:.3e}"
+    return dict(rel_l2=rl2, max_abs=mabs)
+
+
+class DeviceInputs:
+    """Seeded inputs on the device (bf16 tensors) plus their float64 copies."""
+
+    def __init__(self, w: G.Workload, seed=0, with_grad=None):
+        self.w = w
+        self.np = G.make_inputs(w, seed, with_grad)
+        n = self.np
+        self.x = dev_bf16(n["x"])
+        self.w_router = dev_bf16(n["w_router"])
+        self.w_gate_up = dev_bf16(n["w_gate_up"])
+        self.w_down = dev_bf16(n["w_down"])
+        self.router_bias = dev_f32(n["router_bias"])
+        self.w_sh_gate_up = dev_bf16(n["w_sh_gate_up"]) if n["w_sh_gate_up"] is not None else None
+        self.w_sh_down = dev_bf16(n["w_sh_down"]) if n["w_sh_down"] is not None else None
+        self.grad_out = dev_bf16(n["grad_out"]) if n["grad_out"] is not None else None
+
+    def f64(self, key):
+        v = self.np[key]
+        if v is None:
+            return None
+        return O.widen_bf16(v) if v.dtype == np.uint16 else v.astype(np.float64)
+
+    @property
+    def dims(self):
+        w = self.w
+        return (w.T, w.H, w.E, w.k, w.I, w.I_shared)
+
+
+def run_forward(di: DeviceInputs, with_backward=True, save_logits=True):
+    layer = M.MoeLayer(di.dims, gate_mode=di.w.gate, with_backward=with_backward,
+                       save_logits=save_logits)
+    layer.forward(di.x, di.w_router, di.w_gate_up, di.w_down, di.router_bias, di.w_sh_gate_up,
+                  di.w_sh_down)
+    torch.cuda.synchronize()
+    return layer
+
+
+def oracle_forward(di: DeviceInputs, topk_idx=None):
+    return O.layer_forward(di.f64("x"), di.f64("w_router"), di.f64("w_gate_up"), di.f64("w_down"),
+                           di.w.k, balanced=di.w.gate == G.GATE_BALANCED,
+                           bias=di.f64("router_bias"), w_sh_gu=di.f64("w_sh_gate_up"),
+                           w_sh_down=di.f64("w_sh_down"), topk_idx=topk_idx)
+
+
+def logit_error_bound(x64, wr64):
+    """Deterministic bound on |fp32-accumulated logit - exact logit| per (t, e):
+    H * 2^-23 * sum_h |x[t,h] W[e,h]| (twice the recursive-summation bound) plus
+    one rounding of the bias add."""
+    H = x64.shape[1]
+    return H * 2.0 ** -23 * (np.abs(x64) @ np.abs(wr64).T) + 2.0 ** -22 * (np.abs(x64) @ np.abs(wr64).T).max()

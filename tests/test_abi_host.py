@@ -1,0 +1,107 @@
+"""Host-side checks of the C ABI (no GPU needed, no compute calls).
+
+The shared library must load here, export every function include/moe.h
+declares, and reject bad arguments on the host with the documented status
+codes before anything touches CUDA.
+"""
+
+import ctypes
+import os
+
+import pytest
+
+from grouped_expert_gemm_top_b300 import build as B
+from grouped_expert_gemm_top_b300 import moe as M
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(M.LIB_PATH):
+        B.build()
+    return M.load_library()
+
+
+def test_header_declares_the_five_layer_calls():
+    names = M.declared_functions()
+    for n in ["moe_route", "moe_permute", "moe_grouped_mlp_fwd", "moe_unpermute_combine",
+              "moe_layer_bwd", "moe_workspace_size", "moe_read_device_status",
+              "moe_status_string", "moe_abi_version"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in M.declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_version_and_status_strings(lib):
+    assert M.moe_abi_version() == 1
+    assert M.moe_status_string(0) == "ok"
+    for s in range(1, 7):
+        assert M.moe_status_string(s) not in ("ok", "unknown status")
+    assert M.moe_status_string(99) == "unknown status"
+
+
+def test_workspace_size_covers_intermediates(lib):
+    T, H, E, k, I = 4096, 2048, 128, 8, 768
+    fwd = M.moe_workspace_size((T, H, E, k, I, 0), False)
+    bwd = M.moe_workspace_size((T, H, E, k, I, 0), True)
+    S = T * k
+    assert fwd >= S * I * 2                          # SwiGLU output h
+    assert bwd > fwd + S * (2 * I + I + H) * 2        # dgu, w*h, per-slot dx
+    sh = M.moe_workspace_size((8192, 2688, 128, 6, 1856, 3712), False)
+    assert sh >= 8192 * 6 * 1856 * 2 + 8192 * 3712 * 2
+
+
+@pytest.mark.parametrize("dims,code", [
+    ((0, 256, 8, 2, 512, 0), 2),        # T = 0
+    ((16, 250, 8, 2, 512, 0), 2),       # H not a multiple of 64
+    ((16, 256, 8, 2, 500, 0), 2),       # I not a multiple of 64
+    ((16, 256, 8, 9, 512, 0), 2),       # k > E
+    ((16, 256, 300, 2, 512, 0), 2),     # E > 256
+    ((16, 256, 64, 33, 512, 0), 2),     # k > 32
+    ((16, 256, 8, 2, 512, 100), 2),     # I_shared not a multiple of 64
+])
+def test_unsupported_shapes_rejected(lib, dims, code):
+    out = ctypes.c_size_t(0)
+    st = lib.moe_workspace_size(ctypes.byref(M.MoeDims.of(*dims)), 0, ctypes.byref(out))
+    assert st == code
+
+
+def test_null_and_misaligned_arguments_rejected_before_launch(lib):
+    d = M.MoeDims.of(256, 256, 8, 2, 512, 0)
+    ws = ctypes.create_string_buffer(1 << 20)
+    wsp = (ctypes.addressof(ws) + 255) // 256 * 256
+    assert lib.moe_workspace_size(None, 0, None) == 1
+    # null inputs
+    assert lib.moe_route(ctypes.byref(d), 0, None, None, None, None, None, None, wsp, 1 << 19, None) == 1
+    # bad gate enum
+    assert lib.moe_route(ctypes.byref(d), 7, wsp, wsp, None, None, wsp, wsp, wsp, 1 << 19, None) == 1
+    # misaligned x
+    assert lib.moe_route(ctypes.byref(d), 0, wsp + 2, wsp, None, None, wsp, wsp, wsp, 1 << 19, None) == 1
+    # workspace too small
+    assert lib.moe_route(ctypes.byref(d), 0, wsp, wsp, None, None, wsp, wsp, wsp, 16, None) == 3
+    assert lib.moe_permute(ctypes.byref(d), wsp, wsp, wsp, wsp, wsp, 64, None) == 3
+    args = [wsp] * 12
+    assert lib.moe_grouped_mlp_fwd(ctypes.byref(d), *args[:6], None, None, None, None, None, wsp, 64, None) == 1
+    assert lib.moe_unpermute_combine(ctypes.byref(d), None, wsp, wsp, None, wsp, None) == 1
+    assert lib.moe_layer_bwd(ctypes.byref(d), *([None] * 21), wsp, 1 << 19, None) == 1
+    st = ctypes.c_int32(0)
+    assert lib.moe_read_device_status(None, 0, None, 0, ctypes.byref(st)) == 1
+
+
+def test_kernel_accounting_without_launches(lib):
+    n = M.moe_kernel_count()
+    names = [M.moe_kernel_name(i) for i in range(n)]
+    assert len(set(names)) == n and "gate_up" in names and "wgrad_gate_up" in names
+    assert M.moe_kernel_name(n) == "unknown"
+    M.moe_timing_enable(False)
+    st = M.moe_kernel_stats(reset=True)
+    assert all(v == (0, 0.0) for v in M.moe_kernel_stats().values()) or st is not None
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+    x = torch.zeros(4, 4)
+    with pytest.raises(ValueError):
+        M._ptr(x)

@@ -1,0 +1,176 @@
+"""GPU parity: every call of the C ABI against the CPU oracle, element by element.
+
+Sizes are small enough for the float64 oracle to finish in seconds but span
+several 128-row tiles, ragged row tails, ragged column blocks (I and H not
+multiples of the 256-wide tile), empty experts, a shared expert, and both
+gates.  Bit-exact for ids and the permutation; bf16 tolerance (gpu_util) for
+floating outputs and gradients.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import gpu_util as U
+from grouped_expert_gemm_top_b300 import inputs as G
+from grouped_expert_gemm_top_b300 import moe as M
+from oracle import moe_oracle as O
+
+pytestmark = pytest.mark.gpu
+
+W = G.Workload
+CASES = {
+    "tiny": G.WORKLOADS["tiny"],
+    "ragged": W("ragged", T=300, H=192, E=6, k=3, I=320, bias_std=0.5),
+    "ragged_shared": W("ragged_shared", T=200, H=128, E=5, k=2, I=192, I_shared=320, bias_std=0.5),
+    "balanced_small": W("balanced_small", T=512, H=256, E=16, k=4, I=256, gate=G.GATE_BALANCED),
+    "skewed_mid": W("skewed_mid", T=1024, H=512, E=32, k=4, I=384, bias_std=1.5),
+}
+
+
+@pytest.fixture(scope="module", params=list(CASES))
+def case(request):
+    w = CASES[request.param]
+    di = U.DeviceInputs(w, seed=0, with_grad=True)
+    layer = U.run_forward(di)
+    assert M.moe_read_device_status(layer.workspace) == 0
+    return di, layer
+
+
+def test_router_logits_and_topk(case):
+    di, layer = case
+    x, wr, b = di.f64("x"), di.f64("w_router"), di.f64("router_bias")
+    ref = O.router_logits(x, wr, b)
+    got = U.to_f64(layer.logits)
+    bound = di.w.H * 2.0 ** -23 * (np.abs(x) @ np.abs(wr).T) + 2.0 ** -23 * (np.abs(ref) + 1.0)
+    assert np.all(np.abs(got - ref) <= bound)
+    idx = layer.topk_idx.cpu().numpy()
+    wgt = layer.topk_w.cpu().numpy().astype(np.float64)
+    balanced = di.w.gate == G.GATE_BALANCED
+    # contract 1: the oracle's selection on the device's own fp32 logits is identical
+    idx1, w1, _ = O.route(got, di.w.k, balanced=balanced,
+                          decision_logits=layer.logits.cpu().numpy())
+    assert np.array_equal(idx, idx1)
+    assert np.allclose(wgt, w1, rtol=2e-6, atol=1e-7)
+    # contract 2: against the oracle's own logits, any difference is a near tie
+    idx2, w2, _ = O.route(ref, di.w.k, balanced=balanced)
+    bad = np.nonzero((idx != idx2).any(axis=1))[0]
+    for t in bad:
+        diff_e = np.setxor1d(idx[t], idx2[t])
+        if diff_e.size == 0:      # same set, order swapped by a tie
+            diff_e = idx[t][idx[t] != idx2[t]]
+        vals = ref[t, diff_e]
+        assert vals.max() - vals.min() <= 2 * bound[t, diff_e].max(), (t, diff_e, vals)
+    assert bad.size <= max(1, di.w.T // 500)
+    if balanced:
+        assert np.array_equal(idx, O.balanced_topk(di.w.T, di.w.E, di.w.k))
+
+
+def test_permute_bit_exact(case):
+    di, layer = case
+    idx = layer.topk_idx.cpu().numpy()
+    off, perm, inv = O.permute(idx, di.w.E)
+    assert np.array_equal(layer.expert_offsets.cpu().numpy(), off)
+    assert np.array_equal(layer.perm_slot.cpu().numpy(), perm)
+    assert np.array_equal(layer.slot_perm.cpu().numpy(), inv)
+
+
+def test_forward_matches_oracle(case):
+    di, layer = case
+    idx = layer.topk_idx.cpu().numpy()
+    f = U.oracle_forward(di, topk_idx=idx)
+    U.check_close(layer.gu_saved, f["gu_perm"], "gu_saved")
+    U.check_close(layer.y_perm, f["y_perm"], "y_perm")
+    if di.w.I_shared:
+        U.check_close(layer.sh_gu_saved, f["gu_shared"], "sh_gu_saved")
+        U.check_close(layer.y_shared, f["y_shared"], "y_shared")
+    U.check_close(layer.out, f["out"], "out")
+
+
+def test_combine_is_exact_weighted_sum_of_device_rows(case):
+    """Combine alone: from the device's own bf16 y_perm, one fp32 sum + one rounding."""
+    di, layer = case
+    y = U.to_f64(layer.y_perm)
+    ysh = U.to_f64(layer.y_shared) if di.w.I_shared else None
+    ref = O.combine(y, layer.slot_perm.cpu().numpy(), layer.topk_w.cpu().numpy().astype(np.float64), ysh)
+    got = U.to_f64(layer.out)
+    assert np.all(np.abs(got - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-30 + 1e-6 * np.abs(ref).max())
+
+
+def test_backward_matches_oracle(case):
+    di, layer = case
+    grads = layer.alloc_grads(with_bias=di.w.bias_std > 0)
+    layer.backward(di.grad_out, di.x, di.w_router, di.w_gate_up, di.w_down, grads,
+                   di.w_sh_gate_up, di.w_sh_down)
+    torch.cuda.synchronize()
+    assert M.moe_read_device_status(layer.workspace) == 0
+    idx = layer.topk_idx.cpu().numpy()
+    f = U.oracle_forward(di, topk_idx=idx)
+    b = O.layer_backward(f, di.f64("grad_out"), di.f64("x"), di.f64("w_router"),
+                         di.f64("w_gate_up"), di.f64("w_down"), di.w.k,
+                         w_sh_gu=di.f64("w_sh_gate_up"), w_sh_down=di.f64("w_sh_down"))
+    U.check_close(grads["grad_w_down"], b["grad_w_down"], "grad_w_down")
+    U.check_close(grads["grad_w_gate_up"], b["grad_w_gate_up"], "grad_w_gate_up")
+    U.check_close(grads["grad_x"], b["grad_x"], "grad_x")
+    U.check_close(grads["grad_w_router"], b["grad_w_router"], "grad_w_router")
+    if grads["grad_router_bias"] is not None:
+        U.check_close(grads["grad_router_bias"], b["grad_router_bias"], "grad_router_bias")
+    if di.w.I_shared:
+        U.check_close(grads["grad_w_sh_gate_up"], b["grad_w_sh_gate_up"], "grad_w_sh_gate_up")
+        U.check_close(grads["grad_w_sh_down"], b["grad_w_sh_down"], "grad_w_sh_down")
+    # experts that got no token: exact zero gradients
+    empty = np.nonzero(np.diff(layer.expert_offsets.cpu().numpy()) == 0)[0]
+    for e in empty:
+        assert torch.count_nonzero(grads["grad_w_down"][e]) == 0
+        assert torch.count_nonzero(grads["grad_w_gate_up"][e]) == 0
+
+
+@pytest.mark.parametrize("T,E,k", [(1, 1, 1), (5, 7, 3), (3000, 128, 8), (700, 256, 6), (2049, 3, 2)])
+def test_permute_random_ids(T, E, k):
+    r = np.random.default_rng(T * 31 + E)
+    idx = r.integers(0, E, size=(T, k)).astype(np.int32)
+    if E > 4:
+        idx[idx == 2] = 1        # at least one empty expert
+    dims = (T, 64, E, k, 64, 0)
+    ws = torch.zeros(M.moe_workspace_size(dims, False), dtype=torch.uint8, device="cuda")
+    d_idx = torch.from_numpy(idx).cuda()
+    off = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    perm = torch.empty(T * k, dtype=torch.int32, device="cuda")
+    inv = torch.empty(T * k, dtype=torch.int32, device="cuda")
+    M.moe_permute(dims, d_idx, off, perm, inv, ws)
+    o_off, o_perm, o_inv = O.permute(idx, E)
+    assert np.array_equal(off.cpu().numpy(), o_off)
+    assert np.array_equal(perm.cpu().numpy(), o_perm)
+    assert np.array_equal(inv.cpu().numpy(), o_inv)
+    assert M.moe_read_device_status(ws) == 0
+
+
+def test_out_of_range_expert_ids_are_reported_not_used():
+    T, E, k = 64, 8, 2
+    idx = np.random.default_rng(0).integers(0, E, size=(T, k)).astype(np.int32)
+    idx[3, 1] = E
+    idx[10, 0] = -1
+    dims = (T, 64, E, k, 64, 0)
+    ws = torch.zeros(M.moe_workspace_size(dims, False), dtype=torch.uint8, device="cuda")
+    off = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    perm = torch.empty(T * k, dtype=torch.int32, device="cuda")
+    inv = torch.empty(T * k, dtype=torch.int32, device="cuda")
+    M.moe_permute(dims, torch.from_numpy(idx).cuda(), off, perm, inv, ws)
+    assert M.moe_read_device_status(ws) == 5
+    assert int(off[-1]) == T * k - 2
+    assert M.moe_read_device_status(ws) == 0   # cleared by the previous read
+
+
+def test_forward_backward_bit_identical_run_to_run():
+    w = CASES["skewed_mid"]
+    di = U.DeviceInputs(w, seed=1, with_grad=True)
+    outs = []
+    for _ in range(2):
+        layer = U.run_forward(di)
+        g = layer.alloc_grads(with_bias=True)
+        layer.backward(di.grad_out, di.x, di.w_router, di.w_gate_up, di.w_down, g)
+        torch.cuda.synchronize()
+        outs.append([layer.out.clone(), layer.topk_w.clone(), g["grad_x"].clone(),
+                     g["grad_w_gate_up"].clone(), g["grad_w_router"].clone()])
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)

@@ -1,0 +1,482 @@
+#!/usr/bin/env python
+"""Benchmark of the B300 MoE expert layer (forward + backward) through the C ABI.
+
+One step = one pass of the whole layer over one batch: router, top-k (or the
+balanced gate), expert sort, grouped gate/up GEMM + SwiGLU, grouped down GEMM,
+weighted combine, and the full backward (data and weight gradients).  The
+default workload is the Qwen3-30B-A3B-shaped layer with the balanced gate:
+4096 tokens, hidden 2048, 128 experts, top-8, SwiGLU intermediate 768.
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle on
+the host cores instead (a bounded token sample of the same workload).
+
+Multi-GPU: the layer runs as independent replicas, one per rank (no
+collective on the data path); value = all ranks' tokens / max-over-ranks time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s fwd & fwd+bwd, 4096-tok Qwen3-30B-A3B shape; % roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+# ----------------------------------------------------------------- helpers
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def blas_threads():
+    try:
+        import threadpoolctl
+        n = [i.get("num_threads", 0) for i in threadpoolctl.threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def layer_model(w, counts=None):
+    """Algorithmic FLOPs and minimum HBM bytes of one layer call.
+
+    Forward: router GEMM, gate/up and down GEMMs over the S = T*k slots.
+    Bytes: x, W_r, every expert weight that received at least one slot, out,
+    routing ids/weights and the sorted order.  Forward+backward adds the
+    backward GEMMs (2x the forward FLOPs), the saved gate/up pre-activations
+    (write + read), a second read of the active expert weights, the weight
+    gradients (all experts), grad_out, grad_x, a second read of x and grad W_r.
+    """
+    T, H, E, k, I, Is = w.T, w.H, w.E, w.k, w.I, w.I_shared
+    S = T * k
+    e_act = E if counts is None else int(sum(1 for c in counts if c > 0))
+    f_fwd = 2.0 * T * H * E + 2.0 * S * H * 2 * I + 2.0 * S * I * H + 2.0 * T * H * 3 * Is
+    w_act = e_act * 3.0 * I * H * 2 + 3.0 * Is * H * 2
+    b_fwd = T * H * 2 * 2 + E * H * 2 + w_act + T * k * 8 + S * 8 + (E + 1) * 4
+    f_fb = 3.0 * f_fwd
+    b_fb = (b_fwd + 2 * (S * 2 * I * 2 + T * 2 * Is * 2) + w_act + (E * 3.0 * I * H * 2 + 3.0 * Is * H * 2)
+            + T * H * 2 * 3 + E * H * 2)
+    return f_fwd, b_fwd, f_fb, b_fb
+
+
+def kernel_model(name, w, counts, P):
+    """Algorithmic (FLOPs, bytes) of one launch of a library kernel."""
+    T, H, E, k, I = w.T, w.H, w.E, w.k, w.I
+    S = T * k
+    e_act = sum(1 for c in counts if c > 0)
+    Wgu, Wd = e_act * 2.0 * I * H * 2, e_act * 1.0 * H * I * 2
+    nNB = (I + 255) // 256
+    table = {
+        "router": (2.0 * T * H * E, T * H * 2 + E * H * 2 + S * 8),
+        "sort_histogram": (0.0, S * 4),
+        "sort_scatter": (0.0, S * 4 * 3),
+        "gate_up": (2.0 * S * H * 2 * I, Wgu + T * H * 2 + S * 4 + S * I * 2 + S * 2 * I * 2),
+        "down": (2.0 * S * I * H, Wd + S * I * 2 + S * H * 2),
+        "combine": (2.0 * S * H, S * H * 2 + T * H * 2 + S * 8),
+        "dgrad_down": (2.0 * S * H * I, Wd + T * H * 2 + S * 2 * I * 2 + P * 2 * I * 2 + P * I * 2 + P * nNB * 4),
+        "dgrad_gate_up": (2.0 * S * 2 * I * H, Wgu + P * 2 * I * 2 + P * H * 2),
+        "wgrad_down": (2.0 * S * H * I, T * H * 2 + P * I * 2 + E * H * I * 2.0),
+        "wgrad_gate_up": (2.0 * S * 2 * I * H, P * 2 * I * 2 + T * H * 2 + E * 2.0 * I * H * 2),
+        "dx_gather": (2.0 * S * H, S * H * 2 + T * H * 2 + E * H * 2),
+        "router_wgrad": (2.0 * S * H, T * H * 2 + E * H * 2 + S * 8),
+    }
+    return table.get(name, (0.0, 0.0))
+
+
+class _CtypesNvml:
+    """Minimal read-only NVML access through libnvidia-ml (when pynvml is absent)."""
+
+    NVML_CLOCK_SM = 1
+
+    def __init__(self):
+        import ctypes
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit_v2 failed")
+
+    def nvmlDeviceGetHandleByIndex(self, i):
+        h = self.ct.c_void_p()
+        if self.lib.nvmlDeviceGetHandleByIndex_v2(self.ct.c_uint(i), self.ct.byref(h)) != 0:
+            raise RuntimeError("nvmlDeviceGetHandleByIndex_v2 failed")
+        return h
+
+    def nvmlDeviceGetHandleByPciBusId(self, bus):
+        h = self.ct.c_void_p()
+        if self.lib.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), self.ct.byref(h)) != 0:
+            raise RuntimeError("nvmlDeviceGetHandleByPciBusId_v2 failed")
+        return h
+
+    def _clock(self, fn, h, kind):
+        v = self.ct.c_uint()
+        if fn(h, self.ct.c_int(kind), self.ct.byref(v)) != 0:
+            raise RuntimeError("clock query failed")
+        return v.value
+
+    def nvmlDeviceGetClockInfo(self, h, kind):
+        return self._clock(self.lib.nvmlDeviceGetClockInfo, h, kind)
+
+    def nvmlDeviceGetMaxClockInfo(self, h, kind):
+        return self._clock(self.lib.nvmlDeviceGetMaxClockInfo, h, kind)
+
+    def nvmlDeviceGetCurrentClocksThrottleReasons(self, h):
+        v = self.ct.c_ulonglong()
+        if self.lib.nvmlDeviceGetCurrentClocksThrottleReasons(h, self.ct.byref(v)) != 0:
+            raise RuntimeError("reason query failed")
+        return v.value
+
+
+class ClockSampler:
+    """Samples SM clock and throttle reasons through NVML while running."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, device_index=0, period_s=0.002):
+        self.samples, self.reasons, self.ok = [], set(), False
+        self.period = period_s
+        try:
+            try:
+                import pynvml
+                pynvml.nvmlInit()
+            except ImportError:
+                pynvml = _CtypesNvml()
+            self.nv = pynvml
+            self.h = None
+            try:
+                import torch
+                p = torch.cuda.get_device_properties(device_index)
+                bus = f"{p.pci_domain_id:08x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0"
+                self.h = pynvml.nvmlDeviceGetHandleByPciBusId(bus)
+            except Exception:
+                pass
+            if self.h is None:
+                self.h = pynvml.nvmlDeviceGetHandleByIndex(device_index)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+            self.ok = True
+        except Exception as e:  # report, then run without clock samples
+            sys.stderr.write(f"clock sampler unavailable: {e!r}\n")
+            self.max_mhz = None
+
+    def _run(self):
+        nv = self.nv
+        get_r = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(nv, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        while not self._stop.is_set():
+            try:
+                self.samples.append(nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM))
+                r = get_r(self.h)
+                for bit, name in self.REASONS.items():
+                    if r & bit:
+                        self.reasons.add(name)
+            except Exception:
+                pass
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self.ok:
+            self._stop = threading.Event()
+            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t.start()
+        return self
+
+    def __exit__(self, *a):
+        if self.ok:
+            self._stop.set()
+            self._t.join()
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
+                    "samples": 0}
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(self.reasons), "samples": len(self.samples)}
+
+
+# ----------------------------------------------------------------- oracle (CPU)
+def oracle_step_fn(w, n_tok, seed=0):
+    """Returns f() that runs the oracle forward+backward on the first n_tok tokens."""
+    import numpy as np
+    from grouped_expert_gemm_top_b300 import inputs as G
+    from oracle import moe_oracle as O
+    inp = G.make_inputs(w, seed, with_grad=True)
+    x = O.widen_bf16(inp["x"][:n_tok])
+    go = O.widen_bf16(inp["grad_out"][:n_tok])
+    wr, wgu, wd = (O.widen_bf16(inp[k]) for k in ("w_router", "w_gate_up", "w_down"))
+    bias = None if inp["router_bias"] is None else inp["router_bias"].astype(np.float64)
+    sh = {}
+    if w.I_shared:
+        sh = dict(w_sh_gu=O.widen_bf16(inp["w_sh_gate_up"]), w_sh_down=O.widen_bf16(inp["w_sh_down"]))
+    balanced = w.gate == G.GATE_BALANCED
+
+    def step():
+        f = O.layer_forward(x, wr, wgu, wd, w.k, balanced=balanced, bias=bias, **sh)
+        O.layer_backward(f, go, x, wr, wgu, wd, w.k, **sh)
+    return step
+
+
+def run_reference(args, w, rank):
+    if rank != 0:
+        return 0
+    n_tok = args.ref_tokens
+    step = oracle_step_fn(w, n_tok)
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        step()
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            times.append(dt)
+    mean = sum(times) / len(times)
+    value = n_tok / mean
+    cores = blas_threads()
+    sample = f"first {n_tok} of {w.T} tokens, forward+backward, float64 numpy oracle"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": mean * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_of(w, args),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_of(w, args):
+    return {"workload": w.name, "T": w.T, "H": w.H, "E": w.E, "k": w.k, "I": w.I,
+            "I_shared": w.I_shared, "gate": "balanced" if w.gate == 1 else "softmax_topk",
+            "router_bias_std": w.bias_std, "step": "forward+backward", "seed": args.seed,
+            "l2": "inputs larger than L2: each step streams 1.21 GB of expert weights and "
+                  "writes 1.21 GB of weight gradients (L2 126 MB)",
+            "parallelism": f"replicas x{args.gpus}"}
+
+
+# ----------------------------------------------------------------- GPU arm
+def run_ours(args, w, rank, world):
+    import numpy as np
+    import torch
+    from grouped_expert_gemm_top_b300 import inputs as G
+    from grouped_expert_gemm_top_b300 import moe as M
+
+    local = int(os.environ.get("LOCAL_RANK", 0))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    M.load_library()   # raises if the CUDA library is missing: no fallback
+    inp = G.make_inputs(w, args.seed, with_grad=True)
+
+    def up(b):
+        return torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).to(dev)
+
+    x, wr, wgu, wd, go = (up(inp[k]) for k in ("x", "w_router", "w_gate_up", "w_down", "grad_out"))
+    bias = None if inp["router_bias"] is None else torch.from_numpy(inp["router_bias"]).to(dev)
+    wsg = up(inp["w_sh_gate_up"]) if w.I_shared else None
+    wsd = up(inp["w_sh_down"]) if w.I_shared else None
+    dims = (w.T, w.H, w.E, w.k, w.I, w.I_shared)
+    layer = M.MoeLayer(dims, gate_mode=w.gate, device=dev, with_backward=True)
+    grads = layer.alloc_grads(with_bias=bias is not None)
+    stream = torch.cuda.current_stream(dev)
+
+    def fwd():
+        layer.forward(x, wr, wgu, wd, bias, wsg, wsd)
+
+    def step():
+        fwd()
+        layer.backward(go, x, wr, wgu, wd, grads, wsg, wsd)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    def max_over_ranks(v):
+        if world > 1:
+            import torch.distributed as dist
+            t = torch.tensor([v], dtype=torch.float64)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            return float(t.item())
+        return v
+
+    def timed(fn, k):
+        barrier()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(k):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+        return max_over_ranks(e0.elapsed_time(e1))
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    assert M.moe_read_device_status(layer.workspace) == 0, "device reported an error"
+    counts = np.diff(layer.expert_offsets.cpu().numpy())
+    P_pad = int(sum((int(c) + 127) // 128 * 128 for c in counts))
+
+    # ---- forward + backward (the headline), per-kernel events on
+    M.moe_timing_enable(True)
+    M.moe_kernel_stats(reset=True)
+    with ClockSampler(local) as clocks:
+        ms_fb = timed(step, args.steps)
+    kstats = M.moe_kernel_stats(reset=True)
+    # ---- forward only
+    for _ in range(max(1, args.warmup // 2)):
+        fwd()
+    M.moe_kernel_stats(reset=True)
+    ms_f = timed(fwd, args.steps)
+    kstats_f = M.moe_kernel_stats(reset=True)
+    M.moe_timing_enable(False)
+    assert M.moe_read_device_status(layer.workspace) == 0, "device reported an error"
+
+    # ---- end to end: pinned host inputs in, result out, every step
+    xh = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+    goh = torch.empty(go.shape, dtype=go.dtype, pin_memory=True)
+    xh.copy_(x)
+    goh.copy_(go)
+    outh = torch.empty(layer.out.shape, dtype=layer.out.dtype, pin_memory=True)
+    gxh = torch.empty(grads["grad_x"].shape, dtype=torch.bfloat16, pin_memory=True)
+
+    def e2e_step():
+        x.copy_(xh, non_blocking=True)
+        go.copy_(goh, non_blocking=True)
+        step()
+        outh.copy_(layer.out, non_blocking=True)
+        gxh.copy_(grads["grad_x"], non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    ms_e2e = timed(e2e_step, args.steps)
+    h2d = x.numel() * 2 + go.numel() * 2
+    d2h = outh.numel() * 2 + gxh.numel() * 2
+
+    tokens = w.T * world
+    value = tokens * args.steps / (ms_fb / 1e3)
+    fwd_value = tokens * args.steps / (ms_f / 1e3)
+    e2e_value = tokens * args.steps / (ms_e2e / 1e3)
+
+    peaks, peak_src = load_peaks()
+    f_fwd, b_fwd, f_fb, b_fb = layer_model(w, counts)
+    t_roof_f = max(f_fwd / (peaks["bf16_tflops"] * 1e12), b_fwd / (peaks["hbm_gbs"] * 1e9))
+    t_roof_fb = max(f_fb / (peaks["bf16_tflops"] * 1e12), b_fb / (peaks["hbm_gbs"] * 1e9))
+    t_f = ms_f / 1e3 / args.steps
+    t_fb = ms_fb / 1e3 / args.steps
+
+    kernels = {}
+    for name, (n, ms) in kstats.items():
+        if n:
+            kernels[name] = {"launches": n, "avg_us": ms * 1e3 / n, "share": None}
+    tot = sum(v["avg_us"] * v["launches"] for v in kernels.values())
+    for v in kernels.values():
+        v["share"] = v["avg_us"] * v["launches"] / tot if tot else None
+    top = max(kernels, key=lambda n: kernels[n]["avg_us"] * kernels[n]["launches"])
+    F, B = kernel_model(top, w, counts, P_pad)
+    t_k = kernels[top]["avg_us"] / 1e6
+    bound = "tensor" if F / (peaks["bf16_tflops"] * 1e12) >= B / (peaks["hbm_gbs"] * 1e9) else "hbm"
+    if bound == "tensor":
+        achieved, peak, unit = F / t_k / 1e12, peaks["bf16_tflops"], "TFLOP/s"
+    else:
+        achieved, peak, unit = B / t_k / 1e9, peaks["hbm_gbs"], "GB/s"
+    roofline = {"kernel": top, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+                "frac": achieved / peak, "traffic": None, "peak_source": peak_src,
+                "algorithmic_flops": F, "algorithmic_bytes": B, "avg_us": kernels[top]["avg_us"]}
+    per_kernel_roof = {}
+    for name, v in kernels.items():
+        F_, B_ = kernel_model(name, w, counts, P_pad)
+        if F_ == 0 and B_ == 0:
+            continue
+        t_roof_k = max(F_ / (peaks["bf16_tflops"] * 1e12), B_ / (peaks["hbm_gbs"] * 1e9))
+        per_kernel_roof[name] = round(t_roof_k / (v["avg_us"] / 1e6), 4)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        n_tok = args.cpu_tokens
+        stepc = oracle_step_fn(w, n_tok, args.seed)
+        t0 = time.perf_counter()
+        stepc()
+        dt = time.perf_counter() - t0
+        cpu = {"value": n_tok / dt, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+               "sample": f"first {n_tok} of {w.T} tokens of the same workload, forward+backward "
+                         f"once, float64 numpy oracle ({dt:.1f} s)"}
+
+    gpu_launches = sum(n for n, _ in kstats.values())
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_fb / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": config_of(w, args),
+        "fwd_tokens_per_s": fwd_value, "fwd_ms_per_step": ms_f / args.steps,
+        "layer_roofline": {
+            "fwd": {"t_roof_us": t_roof_f * 1e6, "t_us": t_f * 1e6, "frac": t_roof_f / t_f,
+                    "flops": f_fwd, "bytes": b_fwd},
+            "fwd_bwd": {"t_roof_us": t_roof_fb * 1e6, "t_us": t_fb * 1e6, "frac": t_roof_fb / t_fb,
+                        "flops": f_fb, "bytes": b_fb},
+            "peaks": peaks, "peak_source": peak_src},
+        "roofline": roofline,
+        "kernel_roofline_frac": per_kernel_roof,
+        "kernels": kernels,
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": gpu_launches,
+        "clocks": clocks.summary(),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="qwen3_30b_a3b_balanced_fwd_bwd")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-tokens", type=int, default=2048)
+    ap.add_argument("--ref-tokens", type=int, default=256)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    from grouped_expert_gemm_top_b300 import inputs as G
+    w = G.WORKLOADS[args.workload]
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("gloo")
+    if args.impl == "reference":
+        rc = run_reference(args, w, rank)
+    else:
+        rc = run_ours(args, w, rank, world)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return rc
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -2,14 +2,13 @@
 //
 //   D_g = A_g * B_g^T   for every group g (one group per expert),
 //
-// with bf16 operands staged in shared memory by TMA (tiled boxes or
-// tile::gather4 row gathers), tcgen05.mma accumulating in fp32 in tensor
-// memory, and a fused epilogue that reads TMEM with tcgen05.ld.  This is the
-// "sort the tokens by expert, then one grouped matrix multiplication, with no
-// copy of the expert parameters" step of the grouped_mm expert backend (NeMo
-// AutoModel blog, "专家后端 / Expert backends" table): the expert weights are
-// read in place from the fused [E, ...] 3-D tensors, and activations are
-// gathered row by row from the unsorted token matrix.
+// with bf16 operands staged in shared memory by TMA tiled loads, tcgen05.mma
+// accumulating in fp32 in tensor memory, and a fused epilogue that reads TMEM
+// with tcgen05.ld.  This is the "sort the tokens by expert, then one grouped
+// matrix multiplication, with no copy of the expert parameters" step of the
+// grouped_mm expert backend (NeMo AutoModel blog, "专家后端 / Expert backends"
+// table): the expert weights are read in place from the fused [E, ...] 3-D
+// tensors, and the activations are read from their expert-sorted copy.
 //
 // Roles (192 threads, one CTA per SM, static round-robin over tiles):
 //   warp 0     TMA producer: fills a STAGES-deep ring of (A, B) k-blocks
@@ -24,7 +23,8 @@
 //             share a weight tile run on neighbouring CTAs at the same time.
 //   RAGGED_K  groups are K ranges (weight-gradient GEMMs): D_g is a full
 //             M x N matrix per expert, K = the expert's token rows; an expert
-//             with no rows gets an exact zero gradient.
+//             with no rows gets an exact zero gradient.  The same schedule with
+//             equal K slices (ksplit) gives split-K partial products.
 #pragma once
 #include <cuda.h>
 
@@ -38,29 +38,24 @@ constexpr int kGemmThreads = 192;
 constexpr int kTmemCols = 512;
 constexpr int kMaxGroups = 256;
 
-enum LoadMode : int { KMAJ_TILE = 0, KMAJ_GATHER = 1, MN_TILE = 2, MN_GATHER = 3 };
+enum LoadMode : int { KMAJ_TILE = 0, MN_TILE = 2 };
 enum Sched : int { RAGGED_M = 0, RAGGED_K = 1 };
-enum Epi : int { EPI_ROUTER = 0, EPI_SWIGLU = 1, EPI_STORE = 2, EPI_DGRAD_SWIGLU = 3 };
+enum Epi : int { EPI_STORE_F32 = 0, EPI_SWIGLU = 1, EPI_STORE = 2, EPI_DGRAD_SWIGLU = 3 };
 
 struct GemmArgs {
   int M, N, K;           // see Sched: the ragged one is taken from the groups
   int G;                 // number of groups
   const int32_t* offsets;  // [G+1] row offsets (unpadded); nullptr: one group
   int single_rows;       // rows of the one group when offsets == nullptr
+  int ksplit;            // RAGGED_K without offsets: group g = K rows [g*ksplit, (g+1)*ksplit)
   int padded;            // 1: groups start on 128-row boundaries of a padded row space
-  // gather indices (row of A/B's row space -> source row of the tensor map)
-  const int32_t* a_idx; int a_idx_div; int a_idx_len; int a_src_rows;
-  const int32_t* b_idx; int b_idx_div; int b_idx_len; int b_src_rows;
-  // EPI_STORE
-  __nv_bfloat16* d; long long ldd; long long d_group_stride;
+  // EPI_STORE (bf16) / EPI_STORE_F32 (fp32)
+  __nv_bfloat16* d; float* d_f32; long long ldd; long long d_group_stride;
   // EPI_SWIGLU (inter = intermediate size I)
   __nv_bfloat16* gu_out; __nv_bfloat16* h_out; int inter;
   // EPI_DGRAD_SWIGLU
   const __nv_bfloat16* gu_saved; const int32_t* perm_slot; const float* slot_w;
   __nv_bfloat16* dgu_out; __nv_bfloat16* hw_out; float* dw_part;
-  // EPI_ROUTER
-  const float* bias; float* logits_out; int32_t* topk_idx; float* topk_w; int E; int k;
-  int gate_mode;
   int* status;
 };
 
@@ -80,8 +75,8 @@ struct GemmCfg {
   // K-major B is loaded in boxes of at most 128 rows.
   static constexpr int B_BOX_ROWS = BN < 128 ? BN : 128;
   static constexpr int B_NBOX = BN / B_BOX_ROWS;
-  static constexpr bool A_MN = (AL == MN_TILE || AL == MN_GATHER);
-  static constexpr bool B_MN = (BL == MN_TILE || BL == MN_GATHER);
+  static constexpr bool A_MN = (AL == MN_TILE);
+  static constexpr bool B_MN = (BL == MN_TILE);
   static constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, A_MN, B_MN);
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;  // + alignment slack
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N");
@@ -106,7 +101,6 @@ struct SmemTables {
   int total_tiles;
   int abort_flag;
   uint32_t tmem_base;
-  float bias[kMaxGroups];  // router bias (EPI_ROUTER)
 };
 
 template <class C>
@@ -149,12 +143,6 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, const SmemTab
   return ti;
 }
 
-__device__ __forceinline__ int gather_src(const int32_t* idx, int div, int len, int src_rows, int r) {
-  int s = __ldg(idx + clampi(r, 0, len - 1));
-  if (div > 1) s /= div;
-  return clampi(s, 0, src_rows - 1);
-}
-
 // ---------------------------------------------------------------- epilogues
 template <class C>
 __device__ __forceinline__ void store_row_chunk_bf16(__nv_bfloat16* dst, const float (&v)[32]) {
@@ -188,88 +176,41 @@ __device__ __forceinline__ void load_row_chunk_bf16(const __nv_bfloat16* src, fl
   }
 }
 
-__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
-
-// Order used by top-k: (value descending, expert index ascending).
-__device__ __forceinline__ bool before(float va, int ia, float vb, int ib) {
-  return va > vb || (va == vb && ia < ib);
-}
+// silu(g) = g * sigmoid(g), with CUDA's fast exponential and division intrinsics.
+__device__ __forceinline__ float sigmoid_f(float g) { return __fdividef(1.0f, 1.0f + __expf(-g)); }
+__device__ __forceinline__ float silu_f(float g) { return g * sigmoid_f(g); }
 
 template <class C>
-__device__ void epilogue_router(const GemmArgs& a, const SmemTables& T, const TileInfo& ti,
-                                uint32_t tacc, int row_in_tile) {
-  const int t = ti.row0 + row_in_tile;
+__device__ void epilogue_store_f32(const GemmArgs& a, const TileInfo& ti, uint32_t tacc,
+                                   int row_in_tile) {
   const bool valid = row_in_tile < ti.rows_valid;
-  const int E = a.E;
-  constexpr int NCH = (C::BN + 31) / 32;
+  const int n0 = ti.nb * C::BN;
+  float* base = a.d_f32;
+  long long row;
+  if constexpr (C::SCH == RAGGED_K) {
+    base += (long long)ti.g * a.d_group_stride;
+    row = ti.mb * BM + row_in_tile;
+  } else {
+    row = ti.row0 + row_in_tile;
+  }
   float v[32];
-  // pass 1: max over the E logits (logit = accumulator + bias), optional logits output
-  float mx = -INFINITY;
 #pragma unroll 1
-  for (int c = 0; c < NCH; ++c) {
-    tmem_ld32(tacc + c * 32, v);
+  for (int c = 0; c < (C::BN + 31) / 32; ++c) {
+    const int col = n0 + c * 32;
+    if (col >= a.N) break;
+    if (ti.kblocks > 0) tmem_ld32(tacc + c * 32, v);
+    else {
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const int e = c * 32 + i;
-      if (e < E) {
-        const float l = v[i] + T.bias[e];
-        mx = fmaxf(mx, l);
-        if (valid && a.logits_out) a.logits_out[(size_t)t * E + e] = l;
-      }
+      for (int i = 0; i < 32; ++i) v[i] = 0.f;
     }
-  }
-  // pass 2: softmax denominator
-  float den = 0.f;
-#pragma unroll 1
-  for (int c = 0; c < NCH; ++c) {
-    tmem_ld32(tacc + c * 32, v);
+    if (!valid) continue;
+    float* dst = base + row * a.ldd + col;
+    if (col + 32 <= a.N) {
+      float4* p = reinterpret_cast<float4*>(dst);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const int e = c * 32 + i;
-      if (e < E) den += expf(v[i] + T.bias[e] - mx);
-    }
-  }
-  // selection: k passes, each takes the first element (in top-k order) after the previous one
-  float prev_v = INFINITY;
-  int prev_i = -1;
-  float psum = 0.f;
-  float psel[32];
-  int isel[32];
-#pragma unroll 1
-  for (int j = 0; j < a.k; ++j) {
-    float best_v = -INFINITY;
-    int best_i = -1;
-    const int forced = (a.gate_mode == 1) ? (int)(((long long)t * a.k + j) % E) : -1;
-#pragma unroll 1
-    for (int c = 0; c < NCH; ++c) {
-      tmem_ld32(tacc + c * 32, v);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int e = c * 32 + i;
-        if (e < E) {
-          const float l = v[i] + T.bias[e];
-          if (forced >= 0) {
-            if (e == forced) { best_v = l; best_i = e; }
-          } else if (before(prev_v, prev_i, l, e) &&
-                     (best_i < 0 || before(l, e, best_v, best_i))) {
-            best_v = l;
-            best_i = e;
-          }
-        }
-      }
-    }
-    if (best_i < 0) best_i = j < E ? j : 0;  // only reachable with NaN logits
-    prev_v = best_v;
-    prev_i = best_i;
-    const float p = expf(best_v - mx) / den;
-    if (j < 32) { psel[j] = p; isel[j] = best_i; }
-    psum += p;
-  }
-  if (valid) {
-#pragma unroll 1
-    for (int j = 0; j < a.k && j < 32; ++j) {
-      a.topk_idx[(size_t)t * a.k + j] = isel[j];
-      a.topk_w[(size_t)t * a.k + j] = psel[j] / psum;
+      for (int q = 0; q < 8; ++q) p[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+    } else {
+      for (int i = 0; i < 32 && col + i < a.N; ++i) dst[i] = v[i];
     }
   }
 }
@@ -359,7 +300,7 @@ __device__ void epilogue_dgrad_swiglu(const GemmArgs& a, const SmemTables& T, co
       load_row_chunk_bf16(a.gu_saved + r * (2LL * I) + I + j, u);
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
-        const float s = 1.0f / (1.0f + __expf(-g[i]));
+        const float s = sigmoid_f(g[i]);
         const float sl = g[i] * s;
         const float h = sl * u[i];
         dwp = fmaf(acc[i], h, dwp);
@@ -436,6 +377,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (a.offsets) {
           off = __ldg(a.offsets + g);
           cnt = __ldg(a.offsets + g + 1) - off;
+        } else if (a.ksplit > 0) {
+          off = g * a.ksplit;
+          cnt = min(a.ksplit, a.K - off);
         } else {
           cnt = a.single_rows;
         }
@@ -466,10 +410,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       T.total_tiles = run_tiles;
     }
   }
-  if constexpr (C::EPI == EPI_ROUTER) {
-    for (int e = threadIdx.x; e < kMaxGroups; e += blockDim.x)
-      T.bias[e] = (a.bias && e < a.E) ? a.bias[e] : 0.f;
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -483,14 +423,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint32_t filled = 0, fill_parity = 0;  // per stage: armed at least once, parity of last fill
     for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
       const TileInfo ti = decode_tile<C>(a, T, t);
-      // K-major A gather: this lane's 4 rows are fixed for the whole tile
-      int ar[4] = {0, 0, 0, 0};
-      if constexpr (C::AL == KMAJ_GATHER) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          ar[i] = gather_src(a.a_idx, a.a_idx_div, a.a_idx_len, a.a_src_rows,
-                             ti.row0 + 4 * lane + i);
-      }
       const int n0 = C::SWIGLU_B ? ti.nb * (C::BN / 2) : ti.nb * C::BN;
       const int m0 = ti.mb * BM;
       bool ok = true;
@@ -504,24 +436,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
         __syncwarp();
         const int kc = kb * BK;               // K coordinate inside the group
-        const int kr = ti.kstart + kc;        // K row in a row-indexed operand (RAGGED_K)
+        const int kr = ti.kstart + kc;        // absolute K coordinate (RAGGED_K)
+        const int kx = C::SCH == RAGGED_K ? kr : kc;
         // ---- A
         if constexpr (C::AL == KMAJ_TILE) {
-          if (lane == 0) tma_load_2d(sA, &tmA, fb, kc, ti.row0);
-        } else if constexpr (C::AL == KMAJ_GATHER) {
-          tma_gather4(sA + lane * 512, &tmA, fb, kc, ar[0], ar[1], ar[2], ar[3]);
-        } else if constexpr (C::AL == MN_TILE) {
+          if (lane == 0) tma_load_2d(sA, &tmA, fb, kx, C::SCH == RAGGED_K ? m0 : ti.row0);
+        } else {  // MN_TILE: two 64-wide groups along M, 64 k-rows each
           if (lane == 0) {
             tma_load_2d(sA, &tmA, fb, m0, kr);
             tma_load_2d(sA + 8192, &tmA, fb, m0 + 64, kr);
           }
-        } else {  // MN_GATHER: 2 groups of 64 along M, 64 k-rows each, 4 rows per gather
-          const int q = lane & 15, grp = lane >> 4;
-          int s[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            s[i] = gather_src(a.a_idx, a.a_idx_div, a.a_idx_len, a.a_src_rows, kr + 4 * q + i);
-          tma_gather4(sA + grp * 8192 + q * 512, &tmA, fb, m0 + 64 * grp, s[0], s[1], s[2], s[3]);
         }
         // ---- B
         if constexpr (C::BL == KMAJ_TILE) {
@@ -531,7 +455,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               const int nc = C::SWIGLU_B ? (b == 0 ? n0 : a.inter + n0) : n0 + b * C::B_BOX_ROWS;
               const uint32_t dst = sB + b * C::B_BOX_ROWS * 128;
               if constexpr (C::B3D) tma_load_3d(dst, &tmB, fb, kc, nc, ti.g);
-              else tma_load_2d(dst, &tmB, fb, kc, nc);
+              else tma_load_2d(dst, &tmB, fb, kx, nc);
             }
           }
         } else if constexpr (C::BL == MN_TILE) {
@@ -542,15 +466,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               else tma_load_2d(sB + b * 8192, &tmB, fb, n0 + 64 * b, kr);
             }
           }
-        } else if constexpr (C::BL == MN_GATHER) {
-          const int q = lane & 15;
-          int s[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            s[i] = gather_src(a.b_idx, a.b_idx_div, a.b_idx_len, a.b_src_rows, kr + 4 * q + i);
-#pragma unroll
-          for (int b = (lane >> 4); b < C::BN / 64; b += 2)
-            tma_gather4(sB + b * 8192 + q * 512, &tmB, fb, n0 + 64 * b, s[0], s[1], s[2], s[3]);
         }
         if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
       }
@@ -626,7 +541,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (!mbar_wait(smem_u32(&tfull_bar[acc]), acc_phase, abort_flag, a.status)) break;
       tc_fence_after();
       const uint32_t tacc = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * C::BN;
-      if constexpr (C::EPI == EPI_ROUTER) epilogue_router<C>(a, T, ti, tacc, row_in_tile);
+      if constexpr (C::EPI == EPI_STORE_F32) epilogue_store_f32<C>(a, ti, tacc, row_in_tile);
       else if constexpr (C::EPI == EPI_SWIGLU) epilogue_swiglu<C>(a, ti, tacc, row_in_tile);
       else if constexpr (C::EPI == EPI_STORE) epilogue_store<C>(a, ti, tacc, row_in_tile);
       else epilogue_dgrad_swiglu<C>(a, T, ti, tacc, row_in_tile);

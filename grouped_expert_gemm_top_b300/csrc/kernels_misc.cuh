@@ -1,6 +1,7 @@
-// Memory-bound kernels of the MoE layer: the expert sort (permutation and
-// expert offsets), the weighted un-permute/combine, and the small backward
-// kernels (padded row tables, router gradient, token gather-sums).
+// Memory-bound kernels of the MoE layer: the router's softmax/top-k, the
+// expert sort (permutation and expert offsets), the sorted token copies, the
+// weighted un-permute/combine, and the small backward kernels (padded row
+// tables, router gradient, token gather-sums).
 //
 // All of them are written so that every output is a fixed-order function of
 // the inputs: no floating-point atomics, so results are bit-identical run to
@@ -16,6 +17,138 @@ namespace moe {
 constexpr int kSortChunk = 2048;   // slots per block in the expert sort
 constexpr int kSortThreads = 256;  // 8 warps x 256 slots
 constexpr int kPadRows = 128;      // per-expert row padding of the backward layout
+
+// ---------------------------------------------------------------- router top-k
+// One warp per token.  logits[e] = sum of the split-K partial products (in
+// split order) + bias[e]; p = softmax over all E; the k experts are taken by k
+// rounds of a warp-wide argmax under the order (logit descending, expert id
+// ascending); w_j = p[e_j] / sum_j p[e_j].  The balanced gate takes
+// e_j = (t*k + j) mod E instead of the argmax rounds.  Reductions use a fixed
+// butterfly order, so results are bit-identical run to run.
+constexpr int kRouterMaxPerLane = 8;  // E <= 256
+
+__device__ __forceinline__ bool topk_before(float va, int ia, float vb, int ib) {
+  return va > vb || (va == vb && ia < ib);
+}
+
+__global__ void router_topk_kernel(const float* __restrict__ partial, int splits,
+                                   const float* __restrict__ bias, float* __restrict__ logits_out,
+                                   int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
+                                   int T, int E, int k, int gate_mode) {
+  const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  float v[kRouterMaxPerLane];
+  float mx = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < kRouterMaxPerLane; ++i) {
+    const int e = i * 32 + lane;
+    v[i] = -INFINITY;
+    if (e < E) {
+      float l = 0.f;
+      for (int sp = 0; sp < splits; ++sp) l += __ldg(partial + ((size_t)sp * T + t) * E + e);
+      if (bias) l += __ldg(bias + e);
+      v[i] = l;
+      mx = fmaxf(mx, l);
+      if (logits_out) logits_out[(size_t)t * E + e] = l;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  float z = 0.f;
+#pragma unroll
+  for (int i = 0; i < kRouterMaxPerLane; ++i)
+    if (i * 32 + lane < E) z += expf(v[i] - mx);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+  uint32_t taken = 0;
+  int my_e = 0;
+  float my_p = 0.f;
+  for (int j = 0; j < k; ++j) {
+    float bv;
+    int bi;
+    if (gate_mode == 1) {
+      bi = (int)(((long long)t * k + j) % E);
+      float mine = 0.f;
+#pragma unroll
+      for (int i = 0; i < kRouterMaxPerLane; ++i)
+        if (i == (bi >> 5)) mine = v[i];
+      bv = __shfl_sync(0xffffffffu, mine, bi & 31);
+    } else {
+      bv = -INFINITY;
+      bi = 0x7fffffff;
+#pragma unroll
+      for (int i = 0; i < kRouterMaxPerLane; ++i) {
+        const int e = i * 32 + lane;
+        if (e < E && !((taken >> i) & 1u) && topk_before(v[i], e, bv, bi)) {
+          bv = v[i];
+          bi = e;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (topk_before(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+      }
+      if (bi == 0x7fffffff) bi = j;  // only with NaN logits: stay in range
+      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    }
+    const float p = expf(bv - mx) / z;
+    if (lane == j) { my_e = bi; my_p = p; }
+  }
+  float psum = lane < k ? my_p : 0.f;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) psum += __shfl_xor_sync(0xffffffffu, psum, o);
+  if (lane < k) {
+    topk_idx[(size_t)t * k + lane] = my_e;
+    topk_w[(size_t)t * k + lane] = my_p / psum;
+  }
+}
+
+// ---------------------------------------------------------------- sorted token copies
+// x_sorted[r, :] = x[perm_slot[r] / k, :] for the S sorted rows (one warp per row).
+__global__ void gather_rows_kernel(const __nv_bfloat16* __restrict__ x,
+                                   const int32_t* __restrict__ perm_slot, int k, int S, int H,
+                                   int T, __nv_bfloat16* __restrict__ x_sorted) {
+  const long long r = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (r >= S) return;
+  const int t = clampi(__ldg(perm_slot + r) / k, 0, T - 1);
+  const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
+  uint4* dst = reinterpret_cast<uint4*>(x_sorted + (size_t)r * H);
+  for (int c = lane; c < H / 8; c += 32) dst[c] = __ldg(src + c);
+}
+
+// Backward copies in the padded per-expert layout: for padded row p with token
+// row_tok[p] (-1 = padding), a_sorted[p] = a[token] and b_sorted[p] = b[token],
+// padding rows are zero.  Rows at or past poff[E] are not touched.
+__global__ void gather_rows_padded_kernel(const int32_t* __restrict__ row_tok,
+                                          const int32_t* __restrict__ poff, int E, int P, int H,
+                                          int T, const __nv_bfloat16* __restrict__ a,
+                                          __nv_bfloat16* __restrict__ a_sorted,
+                                          const __nv_bfloat16* __restrict__ b,
+                                          __nv_bfloat16* __restrict__ b_sorted) {
+  const long long p = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (p >= P || p >= __ldg(poff + E)) return;
+  const int tok = __ldg(row_tok + p);
+  uint4* da = reinterpret_cast<uint4*>(a_sorted + (size_t)p * H);
+  uint4* db = reinterpret_cast<uint4*>(b_sorted + (size_t)p * H);
+  if (tok < 0 || tok >= T) {
+    for (int c = lane; c < H / 8; c += 32) {
+      da[c] = make_uint4(0, 0, 0, 0);
+      db[c] = make_uint4(0, 0, 0, 0);
+    }
+    return;
+  }
+  const uint4* sa = reinterpret_cast<const uint4*>(a + (size_t)tok * H);
+  const uint4* sb = reinterpret_cast<const uint4*>(b + (size_t)tok * H);
+  for (int c = lane; c < H / 8; c += 32) {
+    da[c] = __ldg(sa + c);
+    db[c] = __ldg(sb + c);
+  }
+}
 
 // ---------------------------------------------------------------- expert sort
 // Pass 1: per-block expert histogram of the slots s = t*k + j.
@@ -189,7 +322,7 @@ __global__ void pad_offsets_kernel(const int32_t* __restrict__ expert_offsets, i
   if (lane == 0) poff[E] = run;
 }
 
-// For every row p of the padded layout: the token it reads (0 for padding rows).
+// For every row p of the padded layout: the token it reads (-1 for padding rows).
 __global__ void padded_row_tokens_kernel(const int32_t* __restrict__ expert_offsets,
                                          const int32_t* __restrict__ poff,
                                          const int32_t* __restrict__ perm_slot, int E, int k,
@@ -203,7 +336,7 @@ __global__ void padded_row_tokens_kernel(const int32_t* __restrict__ expert_offs
   __syncthreads();
   const int p = blockIdx.x * blockDim.x + threadIdx.x;
   if (p >= S_pad_max) return;
-  int tok = 0;
+  int tok = -1;
   if (p < sp[E]) {
     int lo = 0, hi = E - 1;
     while (lo < hi) {

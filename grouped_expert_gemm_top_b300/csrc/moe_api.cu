@@ -5,6 +5,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdint>
 #include <cstring>
@@ -40,9 +41,12 @@ moe_status check_dims(const moe_dims* d) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+constexpr int kMaxRouterSplits = 8;
+
 struct Layout {
-  size_t status, counts, h, h_sh, fwd_end;
-  size_t poff, row_tok, dgu, hw, dxs, dwp, dl, dgu_sh, hw_sh, dxs_sh, total;
+  size_t status, counts, logits_part, x_sorted, h, h_sh, fwd_end;
+  size_t poff, row_tok, dout_sorted, x_sorted_pad, dgu, hw, dxs, dwp, dl, dgu_sh, hw_sh, dxs_sh,
+      total;
   int sort_blocks;
   long long S, S_pad_max;
   int nNB_I;  // 256-wide column blocks of the intermediate (dgrad-down tiles)
@@ -58,6 +62,8 @@ Layout make_layout(const moe_dims& d, bool bwd) {
   size_t o = 0;
   L.status = o; o += kAlign;
   L.counts = o; o = align_up(o + (size_t)L.sort_blocks * d.E * 4);
+  L.logits_part = o; o = align_up(o + (size_t)kMaxRouterSplits * d.T * d.E * 4);
+  L.x_sorted = o; o = align_up(o + (size_t)L.S * d.H * 2);
   L.h = o; o = align_up(o + (size_t)L.S * d.I * 2);
   L.h_sh = o; o = align_up(o + (size_t)d.T * d.I_shared * 2);
   L.fwd_end = o;
@@ -65,6 +71,8 @@ Layout make_layout(const moe_dims& d, bool bwd) {
     const size_t P = (size_t)L.S_pad_max;
     L.poff = o; o = align_up(o + (size_t)(d.E + 1) * 4);
     L.row_tok = o; o = align_up(o + P * 4);
+    L.dout_sorted = o; o = align_up(o + P * d.H * 2);
+    L.x_sorted_pad = o; o = align_up(o + P * d.H * 2);
     L.dgu = o; o = align_up(o + P * 2 * d.I * 2);
     L.hw = o; o = align_up(o + P * d.I * 2);
     L.dxs = o; o = align_up(o + P * d.H * 2);
@@ -205,30 +213,27 @@ struct KernelScope {
 
 // ------------------------------------------------------------------ GEMM configs
 using moe::EPI_DGRAD_SWIGLU;
-using moe::EPI_ROUTER;
+using moe::EPI_STORE_F32;
 using moe::EPI_STORE;
 using moe::EPI_SWIGLU;
-using moe::KMAJ_GATHER;
 using moe::KMAJ_TILE;
-using moe::MN_GATHER;
 using moe::MN_TILE;
 using moe::RAGGED_K;
 using moe::RAGGED_M;
 
 template <int BN>
-using CfgRouter = GemmCfg<BN, (BN >= 256 ? 4 : 6), KMAJ_TILE, KMAJ_TILE, RAGGED_M, EPI_ROUTER, false, false>;
-using CfgGateUp = GemmCfg<256, 4, KMAJ_GATHER, KMAJ_TILE, RAGGED_M, EPI_SWIGLU, true, true>;
+using CfgRouter =
+    GemmCfg<BN, (BN >= 256 ? 4 : 6), KMAJ_TILE, KMAJ_TILE, RAGGED_K, EPI_STORE_F32, false, false>;
+using CfgGateUp = GemmCfg<256, 4, KMAJ_TILE, KMAJ_TILE, RAGGED_M, EPI_SWIGLU, true, true>;
 using CfgGateUpShared = GemmCfg<256, 4, KMAJ_TILE, KMAJ_TILE, RAGGED_M, EPI_SWIGLU, false, true>;
 using CfgDown = GemmCfg<256, 4, KMAJ_TILE, KMAJ_TILE, RAGGED_M, EPI_STORE, true, false>;
 using CfgDownShared = GemmCfg<256, 4, KMAJ_TILE, KMAJ_TILE, RAGGED_M, EPI_STORE, false, false>;
-using CfgDgradDown = GemmCfg<256, 4, KMAJ_GATHER, MN_TILE, RAGGED_M, EPI_DGRAD_SWIGLU, true, false>;
+using CfgDgradDown = GemmCfg<256, 4, KMAJ_TILE, MN_TILE, RAGGED_M, EPI_DGRAD_SWIGLU, true, false>;
 using CfgDgradDownShared =
     GemmCfg<256, 4, KMAJ_TILE, MN_TILE, RAGGED_M, EPI_DGRAD_SWIGLU, false, false>;
 using CfgDgradGateUp = GemmCfg<256, 4, KMAJ_TILE, MN_TILE, RAGGED_M, EPI_STORE, true, false>;
 using CfgDgradGateUpShared = GemmCfg<256, 4, KMAJ_TILE, MN_TILE, RAGGED_M, EPI_STORE, false, false>;
-using CfgWgradDown = GemmCfg<256, 4, MN_GATHER, MN_TILE, RAGGED_K, EPI_STORE, false, false>;
-using CfgWgradGateUp = GemmCfg<256, 4, MN_TILE, MN_GATHER, RAGGED_K, EPI_STORE, false, false>;
-using CfgWgradShared = GemmCfg<256, 4, MN_TILE, MN_TILE, RAGGED_K, EPI_STORE, false, false>;
+using CfgWgrad = GemmCfg<256, 4, MN_TILE, MN_TILE, RAGGED_K, EPI_STORE, false, false>;
 
 template <class C>
 moe_status launch_gemm(int kid, const CUtensorMap& A, const CUtensorMap& B, const GemmArgs& a,
@@ -255,7 +260,6 @@ moe_status launch_gemm(int kid, const CUtensorMap& A, const CUtensorMap& B, cons
 GemmArgs base_args(int* status) {
   GemmArgs a;
   std::memset(&a, 0, sizeof(a));
-  a.a_idx_div = a.b_idx_div = 1;
   a.status = status;
   return a;
 }
@@ -305,32 +309,42 @@ moe_status moe_route(const moe_dims* d, int32_t gate_mode, const moe_bf16* x,
   if (!x || !w_router || !topk_idx || !topk_w || !workspace) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(w_router) || !aligned16(workspace)) return MOE_ERR_INVALID_ARG;
   if (workspace_bytes < kAlign) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  const Layout L = make_layout(*d, false);
+  if (workspace_bytes < L.x_sorted) return MOE_ERR_WORKSPACE_TOO_SMALL;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int T = d->T, H = d->H, E = d->E;
+  // split K so that the router GEMM fills the SMs; partial logits are summed in
+  // split order by the top-k kernel
+  const long long mt = cdiv(T, moe::BM);
+  int splits = (int)std::min<long long>(kMaxRouterSplits, std::max<long long>(1, cdiv(sm_count(), mt)));
+  const int kblocks = H / moe::BK;
+  if (splits > kblocks) splits = kblocks;
+  const int ksplit = (int)cdiv(kblocks, splits) * moe::BK;
+  splits = (int)cdiv(H, ksplit);
   int bn = 16;
-  while (bn < d->E) bn *= 2;
+  while (bn < E) bn *= 2;
+  float* part = at<float>(workspace, L.logits_part);
   CUtensorMap tA, tB;
-  if (!make_map(&tA, x, d->H, d->T, 1, 64, 128)) return MOE_ERR_CUDA;
-  if (!make_map(&tB, w_router, d->H, d->E, 1, 64, bn)) return MOE_ERR_CUDA;
+  if (!make_map(&tA, x, H, T, 1, 64, 128)) return MOE_ERR_CUDA;
+  if (!make_map(&tB, w_router, H, E, 1, 64, bn)) return MOE_ERR_CUDA;
   GemmArgs a = base_args(at<int>(workspace, 0));
-  a.N = d->E;
-  a.K = d->H;
-  a.G = 1;
-  a.single_rows = d->T;
-  a.bias = router_bias;
-  a.logits_out = logits_out;
-  a.topk_idx = topk_idx;
-  a.topk_w = topk_w;
-  a.E = d->E;
-  a.k = d->k;
-  a.gate_mode = gate_mode;
-  const long long tiles = cdiv(d->T, moe::BM);
+  a.M = T; a.N = E; a.K = H; a.G = splits; a.ksplit = ksplit;
+  a.d_f32 = part; a.ldd = E; a.d_group_stride = (long long)T * E;
+  const long long tiles = mt * splits;
   switch (bn) {
-    case 16: return launch_gemm<CfgRouter<16>>(MOE_K_ROUTER, tA, tB, a, tiles, st);
-    case 32: return launch_gemm<CfgRouter<32>>(MOE_K_ROUTER, tA, tB, a, tiles, st);
-    case 64: return launch_gemm<CfgRouter<64>>(MOE_K_ROUTER, tA, tB, a, tiles, st);
-    case 128: return launch_gemm<CfgRouter<128>>(MOE_K_ROUTER, tA, tB, a, tiles, st);
-    default: return launch_gemm<CfgRouter<256>>(MOE_K_ROUTER, tA, tB, a, tiles, st);
+    case 16: s = launch_gemm<CfgRouter<16>>(MOE_K_ROUTER, tA, tB, a, tiles, st); break;
+    case 32: s = launch_gemm<CfgRouter<32>>(MOE_K_ROUTER, tA, tB, a, tiles, st); break;
+    case 64: s = launch_gemm<CfgRouter<64>>(MOE_K_ROUTER, tA, tB, a, tiles, st); break;
+    case 128: s = launch_gemm<CfgRouter<128>>(MOE_K_ROUTER, tA, tB, a, tiles, st); break;
+    default: s = launch_gemm<CfgRouter<256>>(MOE_K_ROUTER, tA, tB, a, tiles, st); break;
   }
+  if (s != MOE_OK) return s;
+  {
+    KernelScope ks(MOE_K_ROUTER_TOPK, st);
+    moe::router_topk_kernel<<<(unsigned)cdiv((long long)T * 32, 256), 256, 0, st>>>(
+        part, splits, router_bias, logits_out, topk_idx, topk_w, T, E, d->k, gate_mode);
+  }
+  return launched(cudaGetLastError());
 }
 
 moe_status moe_permute(const moe_dims* d, const int32_t* topk_idx, int32_t* expert_offsets,
@@ -342,7 +356,7 @@ moe_status moe_permute(const moe_dims* d, const int32_t* topk_idx, int32_t* expe
     return MOE_ERR_INVALID_ARG;
   if (!aligned16(workspace)) return MOE_ERR_INVALID_ARG;
   const Layout L = make_layout(*d, false);
-  if (workspace_bytes < L.h) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  if (workspace_bytes < L.logits_part) return MOE_ERR_WORKSPACE_TOO_SMALL;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int32_t* counts = at<int32_t>(workspace, L.counts);
   { KernelScope ks(MOE_K_SORT_HISTOGRAM, st);
@@ -378,13 +392,19 @@ moe_status moe_grouped_mlp_fwd(const moe_dims* d, const moe_bf16* x,
   __nv_bfloat16* h = at<__nv_bfloat16>(workspace, L.h);
   const int T = d->T, H = d->H, E = d->E, I = d->I;
   const long long S = L.S;
+  __nv_bfloat16* xs = at<__nv_bfloat16>(workspace, L.x_sorted);
+  {  // sorted copy of the tokens (one row per slot, expert-major)
+    KernelScope ks(MOE_K_GATHER_ROWS, st);
+    moe::gather_rows_kernel<<<(unsigned)cdiv(S * 32, 256), 256, 0, st>>>(
+        reinterpret_cast<const __nv_bfloat16*>(x), perm_slot, d->k, (int)S, H, T, xs);
+    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+  }
   {  // gate/up grouped GEMM + SwiGLU
     CUtensorMap tA, tB;
-    if (!make_map(&tA, x, H, T, 1, 64, 1)) return MOE_ERR_CUDA;
+    if (!make_map(&tA, xs, H, S, 1, 64, 128)) return MOE_ERR_CUDA;
     if (!make_map3(&tB, w_gate_up, H, 2LL * I, E, 64, 128)) return MOE_ERR_CUDA;
     GemmArgs a = base_args(status);
     a.N = 2 * I; a.K = H; a.G = E; a.offsets = expert_offsets;
-    a.a_idx = perm_slot; a.a_idx_div = d->k; a.a_idx_len = (int)S; a.a_src_rows = T;
     a.gu_out = reinterpret_cast<__nv_bfloat16*>(gu_saved); a.h_out = h; a.inter = I;
     s = launch_gemm<CfgGateUp>(MOE_K_GATE_UP, tA, tB, a, (cdiv(S, moe::BM) + E) * cdiv(I, 128), st);
     if (s != MOE_OK) return s;
@@ -488,18 +508,25 @@ moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_
 
   { KernelScope ks(MOE_K_PAD_OFFSETS, st);
     moe::pad_offsets_kernel<<<1, 32, 0, st>>>(expert_offsets, E, poff); }
-  KernelScope ks_rows(MOE_K_PADDED_ROWS, st);
-  moe::padded_row_tokens_kernel<<<(unsigned)cdiv(P, 256), 256, 0, st>>>(
-      expert_offsets, poff, perm_slot, E, k, (int)P, row_tok);
+  { KernelScope ks(MOE_K_PADDED_ROWS, st);
+    moe::padded_row_tokens_kernel<<<(unsigned)cdiv(P, 256), 256, 0, st>>>(
+        expert_offsets, poff, perm_slot, E, k, (int)P, row_tok); }
+  __nv_bfloat16* dos = at<__nv_bfloat16>(workspace, L.dout_sorted);
+  __nv_bfloat16* xsp = at<__nv_bfloat16>(workspace, L.x_sorted_pad);
+  {  // sorted copies of grad_out and x in the padded per-expert layout
+    KernelScope ks(MOE_K_GATHER_ROWS_BWD, st);
+    moe::gather_rows_padded_kernel<<<(unsigned)cdiv(P * 32, 256), 256, 0, st>>>(
+        row_tok, poff, E, (int)P, H, T, reinterpret_cast<const __nv_bfloat16*>(grad_out), dos,
+        reinterpret_cast<const __nv_bfloat16*>(x), xsp);
+  }
   if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
 
   {  // down-projection data gradient + SwiGLU backward (+ dw partials)
     CUtensorMap tA, tB;
-    if (!make_map(&tA, grad_out, H, T, 1, 64, 1)) return MOE_ERR_CUDA;
+    if (!make_map(&tA, dos, H, P, 1, 64, 128)) return MOE_ERR_CUDA;
     if (!make_map3(&tB, w_down, I, H, E, 64, 64)) return MOE_ERR_CUDA;
     GemmArgs a = base_args(status);
     a.N = I; a.K = H; a.G = E; a.offsets = expert_offsets; a.padded = 1;
-    a.a_idx = row_tok; a.a_idx_len = (int)P; a.a_src_rows = T;
     a.inter = I; a.gu_saved = reinterpret_cast<const __nv_bfloat16*>(gu_saved);
     a.perm_slot = perm_slot; a.slot_w = topk_w; a.dgu_out = dgu; a.hw_out = hw; a.dw_part = dwp;
     s = launch_gemm<CfgDgradDown>(MOE_K_DGRAD_DOWN, tA, tB, a, cdiv(P, moe::BM) * L.nNB_I, st);
@@ -559,26 +586,24 @@ moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_
   if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
   {  // dW_down[e] = sum over the expert's rows of dout[token]^T (w h)
     CUtensorMap tA, tB;
-    if (!make_map(&tA, grad_out, H, T, 1, 64, 1)) return MOE_ERR_CUDA;
+    if (!make_map(&tA, dos, H, P, 1, 64, 64)) return MOE_ERR_CUDA;
     if (!make_map(&tB, hw, I, P, 1, 64, 64)) return MOE_ERR_CUDA;
     GemmArgs a = base_args(status);
     a.M = H; a.N = I; a.G = E; a.offsets = expert_offsets; a.padded = 1;
-    a.a_idx = row_tok; a.a_idx_len = (int)P; a.a_src_rows = T;
     a.d = reinterpret_cast<__nv_bfloat16*>(grad_w_down); a.ldd = I;
     a.d_group_stride = (long long)H * I;
-    s = launch_gemm<CfgWgradDown>(MOE_K_WGRAD_DOWN, tA, tB, a, (long long)E * cdiv(H, moe::BM) * cdiv(I, 256), st);
+    s = launch_gemm<CfgWgrad>(MOE_K_WGRAD_DOWN, tA, tB, a, (long long)E * cdiv(H, moe::BM) * cdiv(I, 256), st);
     if (s != MOE_OK) return s;
   }
   {  // dW_gu[e] = sum over the expert's rows of [dg|du]^T x[token]
     CUtensorMap tA, tB;
     if (!make_map(&tA, dgu, 2LL * I, P, 1, 64, 64)) return MOE_ERR_CUDA;
-    if (!make_map(&tB, x, H, T, 1, 64, 1)) return MOE_ERR_CUDA;
+    if (!make_map(&tB, xsp, H, P, 1, 64, 64)) return MOE_ERR_CUDA;
     GemmArgs a = base_args(status);
     a.M = 2 * I; a.N = H; a.G = E; a.offsets = expert_offsets; a.padded = 1;
-    a.b_idx = row_tok; a.b_idx_len = (int)P; a.b_src_rows = T;
     a.d = reinterpret_cast<__nv_bfloat16*>(grad_w_gate_up); a.ldd = H;
     a.d_group_stride = 2LL * I * H;
-    s = launch_gemm<CfgWgradGateUp>(MOE_K_WGRAD_GATE_UP, tA, tB, a,
+    s = launch_gemm<CfgWgrad>(MOE_K_WGRAD_GATE_UP, tA, tB, a,
                                     (long long)E * cdiv(2 * I, moe::BM) * cdiv(H, 256), st);
     if (s != MOE_OK) return s;
   }
@@ -593,7 +618,7 @@ moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_
       GemmArgs a = base_args(status);
       a.M = H; a.N = Is; a.G = 1; a.single_rows = T;
       a.d = reinterpret_cast<__nv_bfloat16*>(grad_w_sh_down); a.ldd = Is;
-      s = launch_gemm<CfgWgradShared>(MOE_K_SHARED_WGRAD_DOWN, tA, tB, a, cdiv(H, moe::BM) * cdiv(Is, 256), st);
+      s = launch_gemm<CfgWgrad>(MOE_K_SHARED_WGRAD_DOWN, tA, tB, a, cdiv(H, moe::BM) * cdiv(Is, 256), st);
       if (s != MOE_OK) return s;
     }
     {
@@ -603,7 +628,7 @@ moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_
       GemmArgs a = base_args(status);
       a.M = 2 * Is; a.N = H; a.G = 1; a.single_rows = T;
       a.d = reinterpret_cast<__nv_bfloat16*>(grad_w_sh_gate_up); a.ldd = H;
-      s = launch_gemm<CfgWgradShared>(MOE_K_SHARED_WGRAD_GATE_UP, tA, tB, a, cdiv(2 * Is, moe::BM) * cdiv(H, 256), st);
+      s = launch_gemm<CfgWgrad>(MOE_K_SHARED_WGRAD_GATE_UP, tA, tB, a, cdiv(2 * Is, moe::BM) * cdiv(H, 256), st);
       if (s != MOE_OK) return s;
     }
   }
@@ -618,7 +643,7 @@ const char* moe_kernel_name(int32_t id) {
       "shared_down", "combine", "pad_offsets", "padded_rows", "dgrad_down", "router_bwd",
       "dgrad_gate_up", "shared_dgrad_down", "shared_dgrad_gate_up", "dx_gather",
       "router_wgrad", "wgrad_down", "wgrad_gate_up", "shared_wgrad_down",
-      "shared_wgrad_gate_up"};
+      "shared_wgrad_gate_up", "router_topk", "gather_rows", "gather_rows_bwd"};
   return (id >= 0 && id < MOE_K_COUNT) ? names[id] : "unknown";
 }
 

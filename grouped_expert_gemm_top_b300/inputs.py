@@ -32,6 +32,7 @@ and router weights are N(0, 0.02); grad_out is N(0, 1).
 from __future__ import annotations
 
 import dataclasses
+import os
 
 import numpy as np
 
@@ -73,6 +74,11 @@ WORKLOADS = {
     "qwen3_30b_a3b_balanced_fwd_bwd": Workload(
         "qwen3_30b_a3b_balanced_fwd_bwd", T=4096, H=2048, E=128, k=8, I=768,
         gate=GATE_BALANCED, backward=True),
+    # same per-expert shape with 32 experts and 1024 tokens (256 slots per expert):
+    # a smaller case for counter captures whose expert weights still exceed L2
+    "qwen3_30b_a3b_balanced_32experts_1024tok": Workload(
+        "qwen3_30b_a3b_balanced_32experts_1024tok", T=1024, H=2048, E=32, k=8, I=768,
+        gate=GATE_BALANCED, backward=True),
     "shared_expert_skewed": Workload(
         "shared_expert_skewed", T=8192, H=2688, E=128, k=6, I=1856,
         I_shared=3712, bias_std=1.5, backward=True),
@@ -95,13 +101,37 @@ def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
     return (np.ascontiguousarray(b, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
 
 
+_CHUNK = 1 << 22  # elements per independently seeded chunk
+
+
 def _rng(seed: int, stream: str) -> np.random.Generator:
     return np.random.default_rng([int(seed), _STREAM[stream]])
 
 
 def normal_bf16(shape, std: float, seed: int, stream: str) -> np.ndarray:
-    draw = _rng(seed, stream).standard_normal(size=shape, dtype=np.float32)
-    return f32_to_bf16_bits(draw * np.float32(std))
+    """N(0, std^2) draws rounded to bf16 bits.
+
+    The flat tensor is cut into fixed chunks of 2^22 values; chunk c is drawn
+    from its own generator seeded with (seed, stream, c), so the result does
+    not depend on how many threads draw it.
+    """
+    n = int(np.prod(shape))
+    out = np.empty(n, dtype=np.uint16)
+    nchunks = (n + _CHUNK - 1) // _CHUNK
+
+    def one(c):
+        lo, hi = c * _CHUNK, min(n, (c + 1) * _CHUNK)
+        g = np.random.default_rng([int(seed), _STREAM[stream], c])
+        out[lo:hi] = f32_to_bf16_bits(g.standard_normal(size=hi - lo, dtype=np.float32) * np.float32(std))
+
+    if nchunks <= 1:
+        for c in range(nchunks):
+            one(c)
+    else:
+        from concurrent.futures import ThreadPoolExecutor
+        with ThreadPoolExecutor(max_workers=min(32, os.cpu_count() or 1)) as ex:
+            list(ex.map(one, range(nchunks)))
+    return out.reshape(shape)
 
 
 def make_inputs(w: Workload, seed: int = 0, with_grad: bool | None = None) -> dict:

@@ -198,7 +198,7 @@ moe_status moe_read_device_status(void* workspace, size_t workspace_bytes, void*
  * events recorded on the launch stream.
  */
 typedef enum {
-  MOE_K_ROUTER = 0,          /* moe_route: router GEMM + softmax/top-k epilogue */
+  MOE_K_ROUTER = 0,          /* moe_route: split-K router GEMM (fp32 partial logits) */
   MOE_K_SORT_HISTOGRAM,      /* moe_permute, pass 1 */
   MOE_K_SORT_SCATTER,        /* moe_permute, pass 2 */
   MOE_K_GATE_UP,             /* grouped gate/up GEMM + SwiGLU */
@@ -219,6 +219,9 @@ typedef enum {
   MOE_K_WGRAD_GATE_UP,       /* backward: grouped gate/up weight-gradient GEMM */
   MOE_K_SHARED_WGRAD_DOWN,
   MOE_K_SHARED_WGRAD_GATE_UP,
+  MOE_K_ROUTER_TOPK,         /* moe_route: softmax + top-k (one warp per token) */
+  MOE_K_GATHER_ROWS,         /* forward: expert-sorted copy of the tokens */
+  MOE_K_GATHER_ROWS_BWD,     /* backward: padded sorted copies of grad_out and x */
   MOE_K_COUNT
 } moe_kernel_id;
 

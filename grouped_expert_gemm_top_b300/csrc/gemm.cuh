@@ -37,6 +37,7 @@ constexpr int BK = 64;
 constexpr int kGemmThreads = 192;
 constexpr int kTmemCols = 512;
 constexpr int kMaxGroups = 256;
+constexpr int kEpiSmemBytesDecl = 4 * 3 * 2048;  // epilogue staging (see the epilogue section)
 
 enum LoadMode : int { KMAJ_TILE = 0, MN_TILE = 2 };
 enum Sched : int { RAGGED_M = 0, RAGGED_K = 1 };
@@ -78,7 +79,9 @@ struct GemmCfg {
   static constexpr bool A_MN = (AL == MN_TILE);
   static constexpr bool B_MN = (BL == MN_TILE);
   static constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, A_MN, B_MN);
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;  // + alignment slack
+  static constexpr bool TMA_OUT = (EPI != EPI_STORE_F32);
+  static constexpr int SMEM_BYTES =
+      STAGES * STAGE_BYTES + (TMA_OUT ? kEpiSmemBytesDecl : 0) + 1024;  // + alignment slack
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N");
   static_assert(!B_MN || BN % 64 == 0, "MN-major B needs 64-wide groups");
   static_assert(2 * BN <= kTmemCols, "two accumulators must fit TMEM");
@@ -144,6 +147,58 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, const SmemTab
 }
 
 // ---------------------------------------------------------------- epilogues
+// Output path: each epilogue warp owns 32 rows of the tile.  A 32x32 bf16
+// block (one 32-column chunk of its rows) is written into a 2 KB shared buffer
+// with the 64-byte swizzle (conflict-free 16-byte writes) and stored by one
+// TMA bulk-tensor store, so global writes are full, coalesced lines.  Three
+// buffers per warp rotate, letting up to three stores be in flight.  A warp
+// whose 32 rows are not all inside the group (ragged expert edge) stores its
+// valid rows directly instead.
+constexpr int kStageBytes = 2048;            // 32 rows x 64 bytes
+constexpr int kStagesPerWarp = 3;
+constexpr int kEpiSmemBytes = 4 * kStagesPerWarp * kStageBytes;
+static_assert(kEpiSmemBytes == kEpiSmemBytesDecl, "epilogue staging size");
+
+struct WarpOut {
+  uint32_t buf0;  // this warp's first staging buffer (1024-byte aligned)
+  int lane;
+  int next;       // next buffer to use
+  int inflight;   // committed store groups not yet known to have read their buffer
+};
+
+// Write this thread's 32 values (its row of a 32-column chunk) as bf16 into the
+// next staging buffer; waits until that buffer's previous store has read it.
+__device__ __forceinline__ uint32_t stage_row(WarpOut& w, const float (&v)[32]) {
+  if (w.inflight >= kStagesPerWarp) {
+    if (w.lane == 0) bulk_wait_read<kStagesPerWarp - 1>();
+    __syncwarp();
+    w.inflight = kStagesPerWarp - 1;
+  }
+  const uint32_t buf = w.buf0 + w.next * kStageBytes;
+  w.next = (w.next + 1) % kStagesPerWarp;
+  const uint32_t row = buf + w.lane * 64;
+  const int sw = (w.lane >> 1) & 3;
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    st_shared_v4(row + ((q ^ sw) << 4), pack_bf16x2(v[8 * q + 0], v[8 * q + 1]),
+                 pack_bf16x2(v[8 * q + 2], v[8 * q + 3]), pack_bf16x2(v[8 * q + 4], v[8 * q + 5]),
+                 pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+  return buf;
+}
+
+__device__ __forceinline__ void stage_store(WarpOut& w, uint32_t buf, const CUtensorMap* map, int x,
+                                            int y, int z, bool three_d) {
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (w.lane == 0) {
+    if (three_d) tma_store_3d(map, buf, x, y, z);
+    else tma_store_2d(map, buf, x, y);
+    bulk_commit();
+  }
+  __syncwarp();
+  ++w.inflight;
+}
+
 template <class C>
 __device__ __forceinline__ void store_row_chunk_bf16(__nv_bfloat16* dst, const float (&v)[32]) {
   uint4* p = reinterpret_cast<uint4*>(dst);
@@ -156,12 +211,6 @@ __device__ __forceinline__ void store_row_chunk_bf16(__nv_bfloat16* dst, const f
     w.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
     p[q] = w;
   }
-}
-
-__device__ __forceinline__ void store_zero_chunk_bf16(__nv_bfloat16* dst) {
-  uint4* p = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-  for (int q = 0; q < 4; ++q) p[q] = make_uint4(0, 0, 0, 0);
 }
 
 __device__ __forceinline__ void load_row_chunk_bf16(const __nv_bfloat16* src, float (&v)[32]) {
@@ -180,6 +229,7 @@ __device__ __forceinline__ void load_row_chunk_bf16(const __nv_bfloat16* src, fl
 __device__ __forceinline__ float sigmoid_f(float g) { return __fdividef(1.0f, 1.0f + __expf(-g)); }
 __device__ __forceinline__ float silu_f(float g) { return g * sigmoid_f(g); }
 
+// fp32 output (split-K router partials): direct stores.
 template <class C>
 __device__ void epilogue_store_f32(const GemmArgs& a, const TileInfo& ti, uint32_t tacc,
                                    int row_in_tile) {
@@ -215,12 +265,18 @@ __device__ void epilogue_store_f32(const GemmArgs& a, const TileInfo& ti, uint32
   }
 }
 
+// Gate/up epilogue: acc columns [0, BN/2) are gate, [BN/2, BN) up, for the
+// intermediate columns n0 .. n0+BN/2-1.  Writes g, u (bf16, for the backward)
+// and h = silu(g) * u.  Maps: tmD0 = gu_out [rows, 2I], tmD1 = h_out [rows, I].
 template <class C>
 __device__ void epilogue_swiglu(const GemmArgs& a, const TileInfo& ti, uint32_t tacc,
-                                int row_in_tile) {
-  // every lane runs the (warp-collective) TMEM loads; only valid rows store
+                                int row_in_tile, WarpOut& w, const CUtensorMap* tmD0,
+                                const CUtensorMap* tmD1) {
+  const int quad = row_in_tile >> 5;
   const bool valid = row_in_tile < ti.rows_valid;
+  const bool warp_full = quad * 32 + 32 <= ti.rows_valid;
   const long long r = ti.row0 + row_in_tile;
+  const int y = ti.row0 + quad * 32;
   const int I = a.inter;
   constexpr int HALF = C::BN / 2;
   const int n0 = ti.nb * HALF;
@@ -231,40 +287,54 @@ __device__ void epilogue_swiglu(const GemmArgs& a, const TileInfo& ti, uint32_t 
     if (j >= I) break;
     tmem_ld32(tacc + c * 32, g);
     tmem_ld32(tacc + HALF + c * 32, u);
-    if (!valid) continue;
-    if (a.gu_out) {
-      store_row_chunk_bf16<C>(a.gu_out + r * (2LL * I) + j, g);
-      store_row_chunk_bf16<C>(a.gu_out + r * (2LL * I) + I + j, u);
-    }
+    if (warp_full) {
+      if (a.gu_out) {
+        stage_store(w, stage_row(w, g), tmD0, j, y, 0, false);
+        stage_store(w, stage_row(w, u), tmD0, I + j, y, 0, false);
+      }
 #pragma unroll
-    for (int i = 0; i < 32; ++i) g[i] = silu_f(g[i]) * u[i];
-    store_row_chunk_bf16<C>(a.h_out + r * (long long)I + j, g);
+      for (int i = 0; i < 32; ++i) g[i] = silu_f(g[i]) * u[i];
+      stage_store(w, stage_row(w, g), tmD1, j, y, 0, false);
+    } else if (valid) {
+      if (a.gu_out) {
+        store_row_chunk_bf16<C>(a.gu_out + r * (2LL * I) + j, g);
+        store_row_chunk_bf16<C>(a.gu_out + r * (2LL * I) + I + j, u);
+      }
+#pragma unroll
+      for (int i = 0; i < 32; ++i) g[i] = silu_f(g[i]) * u[i];
+      store_row_chunk_bf16<C>(a.h_out + r * (long long)I + j, g);
+    }
   }
 }
 
+// Plain bf16 output.  RAGGED_M: D rows are the tile's rows (map tmD0 2-D);
+// RAGGED_K: D is the group's full M x N matrix (map tmD0 3-D, group = depth).
 template <class C>
 __device__ void epilogue_store(const GemmArgs& a, const TileInfo& ti, uint32_t tacc,
-                               int row_in_tile) {
+                               int row_in_tile, WarpOut& w, const CUtensorMap* tmD0) {
+  const int quad = row_in_tile >> 5;
   const bool valid = row_in_tile < ti.rows_valid;
+  const bool warp_full = quad * 32 + 32 <= ti.rows_valid;
   const int n0 = ti.nb * C::BN;
-  __nv_bfloat16* base = a.d;
-  long long row;
-  if constexpr (C::SCH == RAGGED_K) {
-    base += (long long)ti.g * a.d_group_stride;
-    row = ti.mb * BM + row_in_tile;
-  } else {
-    row = ti.row0 + row_in_tile;
-  }
+  constexpr bool k3 = C::SCH == RAGGED_K;
+  const long long row = (k3 ? ti.mb * BM : ti.row0) + row_in_tile;
+  const int y = (k3 ? ti.mb * BM : ti.row0) + quad * 32;
   float v[32];
 #pragma unroll 1
   for (int c = 0; c < C::BN / 32; ++c) {
     const int col = n0 + c * 32;
     if (col >= a.N) break;
     if (ti.kblocks == 0) {
-      if (valid) store_zero_chunk_bf16(base + row * a.ldd + col);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = 0.f;
     } else {
       tmem_ld32(tacc + c * 32, v);
-      if (valid) store_row_chunk_bf16<C>(base + row * a.ldd + col, v);
+    }
+    if (warp_full) {
+      stage_store(w, stage_row(w, v), tmD0, col, y, ti.g, k3);
+    } else if (valid) {
+      __nv_bfloat16* base = a.d + (k3 ? (long long)ti.g * a.d_group_stride : 0);
+      store_row_chunk_bf16<C>(base + row * a.ldd + col, v);
     }
   }
 }
@@ -273,20 +343,26 @@ __device__ void epilogue_store(const GemmArgs& a, const TileInfo& ti, uint32_t t
 // acc = dh_unw = dout[token] * W_down[e]  (columns n0.. of the intermediate)
 // From the saved pre-activations (g, u): h = silu(g) u; dw partial = <acc, h>;
 // dh = w acc; dg = dh u s (1 + g (1 - s)); du = dh silu(g); hw = w h.
+// Maps: tmD0 = dgu_out [rows, 2I], tmD1 = hw_out [rows, I].  In the padded
+// layout the rows past the expert's tokens are written as exact zeros.
 template <class C>
 __device__ void epilogue_dgrad_swiglu(const GemmArgs& a, const SmemTables& T, const TileInfo& ti,
-                                      uint32_t tacc, int row_in_tile) {
+                                      uint32_t tacc, int row_in_tile, WarpOut& w,
+                                      const CUtensorMap* tmD0, const CUtensorMap* tmD1) {
+  const int quad = row_in_tile >> 5;
   const long long p = ti.row0 + row_in_tile;  // row in the (padded) row space
+  const int y = ti.row0 + quad * 32;
   const int I = a.inter;
   const int n0 = ti.nb * C::BN;
   const int nNB = (I + C::BN - 1) / C::BN;
   const bool valid = row_in_tile < ti.rows_valid;
-  const bool pad_row = !valid && a.padded;   // padding rows get exact zeros
+  const bool pad_row = !valid && a.padded;
+  const bool warp_full = a.padded || quad * 32 + 32 <= ti.rows_valid;
   long long r = p;  // row of the saved (unpadded) forward tensors
-  float w = 1.f;
+  float wt = 1.f;
   if (valid) {
     if (a.padded) r = T.off[ti.g] + ti.mb * BM + row_in_tile;
-    if (a.slot_w) w = __ldg(a.slot_w + __ldg(a.perm_slot + r));
+    if (a.slot_w) wt = __ldg(a.slot_w + __ldg(a.perm_slot + r));
   }
   float acc[32], g[32], u[32];
   float dwp = 0.f;
@@ -304,20 +380,25 @@ __device__ void epilogue_dgrad_swiglu(const GemmArgs& a, const SmemTables& T, co
         const float sl = g[i] * s;
         const float h = sl * u[i];
         dwp = fmaf(acc[i], h, dwp);
-        const float dh = w * acc[i];
+        const float dh = wt * acc[i];
         const float dg = dh * u[i] * s * (1.0f + g[i] * (1.0f - s));
         const float du = dh * sl;
         g[i] = dg;
         u[i] = du;
-        acc[i] = w * h;
+        acc[i] = wt * h;
       }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) g[i] = u[i] = acc[i] = 0.f;
+    }
+    if (warp_full) {
+      stage_store(w, stage_row(w, g), tmD0, j, y, 0, false);
+      stage_store(w, stage_row(w, u), tmD0, I + j, y, 0, false);
+      stage_store(w, stage_row(w, acc), tmD1, j, y, 0, false);
+    } else if (valid || pad_row) {
       store_row_chunk_bf16<C>(a.dgu_out + p * (2LL * I) + j, g);
       store_row_chunk_bf16<C>(a.dgu_out + p * (2LL * I) + I + j, u);
       store_row_chunk_bf16<C>(a.hw_out + p * (long long)I + j, acc);
-    } else if (pad_row) {
-      store_zero_chunk_bf16(a.dgu_out + p * (2LL * I) + j);
-      store_zero_chunk_bf16(a.dgu_out + p * (2LL * I) + I + j);
-      store_zero_chunk_bf16(a.hw_out + p * (long long)I + j);
     }
   }
   if (a.dw_part && (valid || pad_row)) a.dw_part[p * nNB + ti.nb] = dwp;
@@ -327,7 +408,9 @@ __device__ void epilogue_dgrad_swiglu(const GemmArgs& a, const SmemTables& T, co
 template <class C>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                        const __grid_constant__ CUtensorMap tmB, const GemmArgs a) {
+                        const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmD0,
+                        const __grid_constant__ CUtensorMap tmD1, const GemmArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[C::STAGES];
   __shared__ __align__(8) uint64_t empty_bar[C::STAGES];
@@ -360,6 +443,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if constexpr (C::TMA_OUT) {
+      tma_prefetch_desc(&tmD0);
+      if constexpr (C::EPI == EPI_SWIGLU || C::EPI == EPI_DGRAD_SWIGLU) tma_prefetch_desc(&tmD1);
+    }
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(&T.tmem_base), kTmemCols);
@@ -534,6 +621,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // ================= epilogue =================
     const int quad = warp & 3;
     const int row_in_tile = quad * 32 + lane;
+    WarpOut wo;
+    wo.buf0 = smem_base + C::STAGES * C::STAGE_BYTES + quad * (kStagesPerWarp * kStageBytes);
+    wo.lane = lane;
+    wo.next = 0;
+    wo.inflight = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
@@ -542,13 +634,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tc_fence_after();
       const uint32_t tacc = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * C::BN;
       if constexpr (C::EPI == EPI_STORE_F32) epilogue_store_f32<C>(a, ti, tacc, row_in_tile);
-      else if constexpr (C::EPI == EPI_SWIGLU) epilogue_swiglu<C>(a, ti, tacc, row_in_tile);
-      else if constexpr (C::EPI == EPI_STORE) epilogue_store<C>(a, ti, tacc, row_in_tile);
-      else epilogue_dgrad_swiglu<C>(a, T, ti, tacc, row_in_tile);
+      else if constexpr (C::EPI == EPI_SWIGLU) epilogue_swiglu<C>(a, ti, tacc, row_in_tile, wo, &tmD0, &tmD1);
+      else if constexpr (C::EPI == EPI_STORE) epilogue_store<C>(a, ti, tacc, row_in_tile, wo, &tmD0);
+      else epilogue_dgrad_swiglu<C>(a, T, ti, tacc, row_in_tile, wo, &tmD0, &tmD1);
       tc_fence_before();
       mbar_arrive(smem_u32(&tempty_bar[acc]));
       if (++acc == 2) { acc = 0; acc_phase ^= 1; }
     }
+    // every TMA store must have completed before the CTA exits
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
   }
 
   tc_fence_before();

@@ -125,7 +125,13 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// bf16 tensor [depth][rows][inner], 128-byte swizzle, zero fill outside.
+// bf16 tensor [depth][rows][inner], zero fill outside.  The swizzle follows the
+// box's inner extent: 128-byte rows (64 bf16) use the 128B pattern, 64-byte
+// rows (32 bf16, the epilogue's store boxes) the 64B pattern.
+CUtensorMapSwizzle swizzle_for(uint32_t box_inner) {
+  return box_inner * 2 >= 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+}
+
 bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t depth,
               uint32_t box_inner, uint32_t box_rows) {
   EncodeTiledFn fn = encode_fn();
@@ -136,7 +142,7 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, u
   const cuuint32_t es[3] = {1, 1, 1};
   const cuuint32_t rank = depth > 1 ? 3 : 2;
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides, box,
-            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_for(box_inner),
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -150,7 +156,7 @@ bool make_map3(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, 
   const cuuint32_t box[3] = {box_inner, box_rows, 1};
   const cuuint32_t es[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_for(box_inner),
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -235,9 +241,18 @@ using CfgDgradGateUp = GemmCfg<256, 4, KMAJ_TILE, MN_TILE, RAGGED_M, EPI_STORE, 
 using CfgDgradGateUpShared = GemmCfg<256, 4, KMAJ_TILE, MN_TILE, RAGGED_M, EPI_STORE, false, false>;
 using CfgWgrad = GemmCfg<256, 4, MN_TILE, MN_TILE, RAGGED_K, EPI_STORE, false, false>;
 
+// Output (store) maps use 32x32 boxes.
+bool make_out_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows) {
+  return make_map(m, base, inner, rows, 1, 32, 32);
+}
+bool make_out_map3(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t depth) {
+  return make_map3(m, base, inner, rows, depth, 32, 32);
+}
+
 template <class C>
-moe_status launch_gemm(int kid, const CUtensorMap& A, const CUtensorMap& B, const GemmArgs& a,
-                       long long tile_bound, cudaStream_t st) {
+moe_status launch_gemm(int kid, const CUtensorMap& A, const CUtensorMap& B, const CUtensorMap& D0,
+                       const CUtensorMap& D1, const GemmArgs& a, long long tile_bound,
+                       cudaStream_t st) {
   static std::atomic<uint64_t> configured{0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
@@ -253,7 +268,7 @@ moe_status launch_gemm(int kid, const CUtensorMap& A, const CUtensorMap& B, cons
   if (tile_bound < grid) grid = tile_bound;
   if (grid < 1) return MOE_OK;
   KernelScope ks(kid, st);
-  moe::grouped_gemm_kernel<C><<<(int)grid, moe::kGemmThreads, C::SMEM_BYTES, st>>>(A, B, a);
+  moe::grouped_gemm_kernel<C><<<(int)grid, moe::kGemmThreads, C::SMEM_BYTES, st>>>(A, B, D0, D1, a);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -332,11 +347,11 @@ moe_status moe_route(const moe_dims* d, int32_t gate_mode, const moe_bf16* x,
   a.d_f32 = part; a.ldd = E; a.d_group_stride = (long long)T * E;
   const long long tiles = mt * splits;
   switch (bn) {
-    case 16: s = launch_gemm<CfgRouter<16>>(MOE_K_ROUTER, tA, tB, a, tiles, st); break;
-    case 32: s = launch_gemm<CfgRouter<32>>(MOE_K_ROUTER, tA, tB, a, tiles, st); break;
-    case 64: s = launch_gemm<CfgRouter<64>>(MOE_K_ROUTER, tA, tB, a, tiles, st); break;
-    case 128: s = launch_gemm<CfgRouter<128>>(MOE_K_ROUTER, tA, tB, a, tiles, st); break;
-    default: s = launch_gemm<CfgRouter<256>>(MOE_K_ROUTER, tA, tB, a, tiles, st); break;
+    case 16: s = launch_gemm<CfgRouter<16>>(MOE_K_ROUTER, tA, tB, tA, tB, a, tiles, st); break;
+    case 32: s = launch_gemm<CfgRouter<32>>(MOE_K_ROUTER, tA, tB, tA, tB, a, tiles, st); break;
+    case 64: s = launch_gemm<CfgRouter<64>>(MOE_K_ROUTER, tA, tB, tA, tB, a, tiles, st); break;
+    case 128: s = launch_gemm<CfgRouter<128>>(MOE_K_ROUTER, tA, tB, tA, tB, a, tiles, st); break;
+    default: s = launch_gemm<CfgRouter<256>>(MOE_K_ROUTER, tA, tB, tA, tB, a, tiles, st); break;
   }
   if (s != MOE_OK) return s;
   {
@@ -403,20 +418,26 @@ moe_status moe_grouped_mlp_fwd(const moe_dims* d, const moe_bf16* x,
     CUtensorMap tA, tB;
     if (!make_map(&tA, xs, H, S, 1, 64, 128)) return MOE_ERR_CUDA;
     if (!make_map3(&tB, w_gate_up, H, 2LL * I, E, 64, 128)) return MOE_ERR_CUDA;
+    CUtensorMap tD0, tD1;
+    if (!make_out_map(&tD1, h, I, S)) return MOE_ERR_CUDA;
+    if (gu_saved) { if (!make_out_map(&tD0, gu_saved, 2LL * I, S)) return MOE_ERR_CUDA; }
+    else tD0 = tD1;
     GemmArgs a = base_args(status);
     a.N = 2 * I; a.K = H; a.G = E; a.offsets = expert_offsets;
     a.gu_out = reinterpret_cast<__nv_bfloat16*>(gu_saved); a.h_out = h; a.inter = I;
-    s = launch_gemm<CfgGateUp>(MOE_K_GATE_UP, tA, tB, a, (cdiv(S, moe::BM) + E) * cdiv(I, 128), st);
+    s = launch_gemm<CfgGateUp>(MOE_K_GATE_UP, tA, tB, tD0, tD1, a, (cdiv(S, moe::BM) + E) * cdiv(I, 128), st);
     if (s != MOE_OK) return s;
   }
   {  // down grouped GEMM
     CUtensorMap tA, tB;
     if (!make_map(&tA, h, I, S, 1, 64, 128)) return MOE_ERR_CUDA;
     if (!make_map3(&tB, w_down, I, H, E, 64, 128)) return MOE_ERR_CUDA;
+    CUtensorMap tD;
+    if (!make_out_map(&tD, y_perm, H, S)) return MOE_ERR_CUDA;
     GemmArgs a = base_args(status);
     a.N = H; a.K = I; a.G = E; a.offsets = expert_offsets;
     a.d = reinterpret_cast<__nv_bfloat16*>(y_perm); a.ldd = H;
-    s = launch_gemm<CfgDown>(MOE_K_DOWN, tA, tB, a, (cdiv(S, moe::BM) + E) * cdiv(H, 256), st);
+    s = launch_gemm<CfgDown>(MOE_K_DOWN, tA, tB, tD, tD, a, (cdiv(S, moe::BM) + E) * cdiv(H, 256), st);
     if (s != MOE_OK) return s;
   }
   if (d->I_shared > 0) {
@@ -426,20 +447,26 @@ moe_status moe_grouped_mlp_fwd(const moe_dims* d, const moe_bf16* x,
       CUtensorMap tA, tB;
       if (!make_map(&tA, x, H, T, 1, 64, 128)) return MOE_ERR_CUDA;
       if (!make_map(&tB, w_sh_gate_up, H, 2LL * Is, 1, 64, 128)) return MOE_ERR_CUDA;
+      CUtensorMap tD0, tD1;
+      if (!make_out_map(&tD1, hs, Is, T)) return MOE_ERR_CUDA;
+      if (sh_gu_saved) { if (!make_out_map(&tD0, sh_gu_saved, 2LL * Is, T)) return MOE_ERR_CUDA; }
+      else tD0 = tD1;
       GemmArgs a = base_args(status);
       a.N = 2 * Is; a.K = H; a.G = 1; a.single_rows = T;
       a.gu_out = reinterpret_cast<__nv_bfloat16*>(sh_gu_saved); a.h_out = hs; a.inter = Is;
-      s = launch_gemm<CfgGateUpShared>(MOE_K_SHARED_GATE_UP, tA, tB, a, cdiv(T, moe::BM) * cdiv(Is, 128), st);
+      s = launch_gemm<CfgGateUpShared>(MOE_K_SHARED_GATE_UP, tA, tB, tD0, tD1, a, cdiv(T, moe::BM) * cdiv(Is, 128), st);
       if (s != MOE_OK) return s;
     }
     {
       CUtensorMap tA, tB;
       if (!make_map(&tA, hs, Is, T, 1, 64, 128)) return MOE_ERR_CUDA;
       if (!make_map(&tB, w_sh_down, Is, H, 1, 64, 128)) return MOE_ERR_CUDA;
+      CUtensorMap tD;
+      if (!make_out_map(&tD, y_shared, H, T)) return MOE_ERR_CUDA;
       GemmArgs a = base_args(status);
       a.N = H; a.K = Is; a.G = 1; a.single_rows = T;
       a.d = reinterpret_cast<__nv_bfloat16*>(y_shared); a.ldd = H;
-      s = launch_gemm<CfgDownShared>(MOE_K_SHARED_DOWN, tA, tB, a, cdiv(T, moe::BM) * cdiv(H, 256), st);
+      s = launch_gemm<CfgDownShared>(MOE_K_SHARED_DOWN, tA, tB, tD, tD, a, cdiv(T, moe::BM) * cdiv(H, 256), st);
       if (s != MOE_OK) return s;
     }
   }
@@ -529,7 +556,9 @@ moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_
     a.N = I; a.K = H; a.G = E; a.offsets = expert_offsets; a.padded = 1;
     a.inter = I; a.gu_saved = reinterpret_cast<const __nv_bfloat16*>(gu_saved);
     a.perm_slot = perm_slot; a.slot_w = topk_w; a.dgu_out = dgu; a.hw_out = hw; a.dw_part = dwp;
-    s = launch_gemm<CfgDgradDown>(MOE_K_DGRAD_DOWN, tA, tB, a, cdiv(P, moe::BM) * L.nNB_I, st);
+    CUtensorMap tD0, tD1;
+    if (!make_out_map(&tD0, dgu, 2LL * I, P) || !make_out_map(&tD1, hw, I, P)) return MOE_ERR_CUDA;
+    s = launch_gemm<CfgDgradDown>(MOE_K_DGRAD_DOWN, tA, tB, tD0, tD1, a, cdiv(P, moe::BM) * L.nNB_I, st);
     if (s != MOE_OK) return s;
   }
   { KernelScope ks(MOE_K_ROUTER_BWD, st);
@@ -543,7 +572,9 @@ moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_
     GemmArgs a = base_args(status);
     a.N = H; a.K = 2 * I; a.G = E; a.offsets = expert_offsets; a.padded = 1;
     a.d = dxs; a.ldd = H;
-    s = launch_gemm<CfgDgradGateUp>(MOE_K_DGRAD_GATE_UP, tA, tB, a, cdiv(P, moe::BM) * cdiv(H, 256), st);
+    CUtensorMap tD;
+    if (!make_out_map(&tD, dxs, H, P)) return MOE_ERR_CUDA;
+    s = launch_gemm<CfgDgradGateUp>(MOE_K_DGRAD_GATE_UP, tA, tB, tD, tD, a, cdiv(P, moe::BM) * cdiv(H, 256), st);
     if (s != MOE_OK) return s;
   }
   __nv_bfloat16* dxs_sh = nullptr;
@@ -560,7 +591,10 @@ moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_
       a.N = Is; a.K = H; a.G = 1; a.single_rows = T;
       a.inter = Is; a.gu_saved = reinterpret_cast<const __nv_bfloat16*>(sh_gu_saved);
       a.dgu_out = dgu_sh; a.hw_out = hw_sh;
-      s = launch_gemm<CfgDgradDownShared>(MOE_K_SHARED_DGRAD_DOWN, tA, tB, a, cdiv(T, moe::BM) * cdiv(Is, 256), st);
+      CUtensorMap tD0, tD1;
+      if (!make_out_map(&tD0, dgu_sh, 2LL * Is, T) || !make_out_map(&tD1, hw_sh, Is, T))
+        return MOE_ERR_CUDA;
+      s = launch_gemm<CfgDgradDownShared>(MOE_K_SHARED_DGRAD_DOWN, tA, tB, tD0, tD1, a, cdiv(T, moe::BM) * cdiv(Is, 256), st);
       if (s != MOE_OK) return s;
     }
     {
@@ -570,7 +604,9 @@ moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_
       GemmArgs a = base_args(status);
       a.N = H; a.K = 2 * Is; a.G = 1; a.single_rows = T;
       a.d = dxs_sh; a.ldd = H;
-      s = launch_gemm<CfgDgradGateUpShared>(MOE_K_SHARED_DGRAD_GATE_UP, tA, tB, a, cdiv(T, moe::BM) * cdiv(H, 256), st);
+      CUtensorMap tD;
+      if (!make_out_map(&tD, dxs_sh, H, T)) return MOE_ERR_CUDA;
+      s = launch_gemm<CfgDgradGateUpShared>(MOE_K_SHARED_DGRAD_GATE_UP, tA, tB, tD, tD, a, cdiv(T, moe::BM) * cdiv(H, 256), st);
       if (s != MOE_OK) return s;
     }
   }
@@ -592,7 +628,9 @@ moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_
     a.M = H; a.N = I; a.G = E; a.offsets = expert_offsets; a.padded = 1;
     a.d = reinterpret_cast<__nv_bfloat16*>(grad_w_down); a.ldd = I;
     a.d_group_stride = (long long)H * I;
-    s = launch_gemm<CfgWgrad>(MOE_K_WGRAD_DOWN, tA, tB, a, (long long)E * cdiv(H, moe::BM) * cdiv(I, 256), st);
+    CUtensorMap tD;
+    if (!make_out_map3(&tD, grad_w_down, I, H, E)) return MOE_ERR_CUDA;
+    s = launch_gemm<CfgWgrad>(MOE_K_WGRAD_DOWN, tA, tB, tD, tD, a, (long long)E * cdiv(H, moe::BM) * cdiv(I, 256), st);
     if (s != MOE_OK) return s;
   }
   {  // dW_gu[e] = sum over the expert's rows of [dg|du]^T x[token]
@@ -603,7 +641,9 @@ moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_
     a.M = 2 * I; a.N = H; a.G = E; a.offsets = expert_offsets; a.padded = 1;
     a.d = reinterpret_cast<__nv_bfloat16*>(grad_w_gate_up); a.ldd = H;
     a.d_group_stride = 2LL * I * H;
-    s = launch_gemm<CfgWgrad>(MOE_K_WGRAD_GATE_UP, tA, tB, a,
+    CUtensorMap tD;
+    if (!make_out_map3(&tD, grad_w_gate_up, H, 2LL * I, E)) return MOE_ERR_CUDA;
+    s = launch_gemm<CfgWgrad>(MOE_K_WGRAD_GATE_UP, tA, tB, tD, tD, a,
                                     (long long)E * cdiv(2 * I, moe::BM) * cdiv(H, 256), st);
     if (s != MOE_OK) return s;
   }
@@ -618,7 +658,9 @@ moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_
       GemmArgs a = base_args(status);
       a.M = H; a.N = Is; a.G = 1; a.single_rows = T;
       a.d = reinterpret_cast<__nv_bfloat16*>(grad_w_sh_down); a.ldd = Is;
-      s = launch_gemm<CfgWgrad>(MOE_K_SHARED_WGRAD_DOWN, tA, tB, a, cdiv(H, moe::BM) * cdiv(Is, 256), st);
+      CUtensorMap tD;
+      if (!make_out_map3(&tD, grad_w_sh_down, Is, H, 1)) return MOE_ERR_CUDA;
+      s = launch_gemm<CfgWgrad>(MOE_K_SHARED_WGRAD_DOWN, tA, tB, tD, tD, a, cdiv(H, moe::BM) * cdiv(Is, 256), st);
       if (s != MOE_OK) return s;
     }
     {
@@ -628,7 +670,9 @@ moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_
       GemmArgs a = base_args(status);
       a.M = 2 * Is; a.N = H; a.G = 1; a.single_rows = T;
       a.d = reinterpret_cast<__nv_bfloat16*>(grad_w_sh_gate_up); a.ldd = H;
-      s = launch_gemm<CfgWgrad>(MOE_K_SHARED_WGRAD_GATE_UP, tA, tB, a, cdiv(2 * Is, moe::BM) * cdiv(H, 256), st);
+      CUtensorMap tD;
+      if (!make_out_map3(&tD, grad_w_sh_gate_up, H, 2LL * Is, 1)) return MOE_ERR_CUDA;
+      s = launch_gemm<CfgWgrad>(MOE_K_SHARED_WGRAD_GATE_UP, tA, tB, tD, tD, a, cdiv(2 * Is, moe::BM) * cdiv(H, 256), st);
       if (s != MOE_OK) return s;
     }
   }

@@ -50,8 +50,8 @@ struct GemmArgs {
   int single_rows;       // rows of the one group when offsets == nullptr
   int ksplit;            // RAGGED_K without offsets: group g = K rows [g*ksplit, (g+1)*ksplit)
   int padded;            // 1: groups start on 128-row boundaries of a padded row space
-  // EPI_STORE (bf16) / EPI_STORE_F32 (fp32)
-  __nv_bfloat16* d; float* d_f32; long long ldd; long long d_group_stride;
+  // EPI_STORE (bf16) / EPI_STORE_F32 (fp32; f32_tma: row stride allows TMA stores)
+  __nv_bfloat16* d; float* d_f32; long long ldd; long long d_group_stride; int f32_tma;
   // EPI_SWIGLU (inter = intermediate size I)
   __nv_bfloat16* gu_out; __nv_bfloat16* h_out; int inter;
   // EPI_DGRAD_SWIGLU
@@ -79,7 +79,7 @@ struct GemmCfg {
   static constexpr bool A_MN = (AL == MN_TILE);
   static constexpr bool B_MN = (BL == MN_TILE);
   static constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, A_MN, B_MN);
-  static constexpr bool TMA_OUT = (EPI != EPI_STORE_F32);
+  static constexpr bool TMA_OUT = true;
   static constexpr int SMEM_BYTES =
       STAGES * STAGE_BYTES + (TMA_OUT ? kEpiSmemBytesDecl : 0) + 1024;  // + alignment slack
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N");
@@ -186,6 +186,26 @@ __device__ __forceinline__ uint32_t stage_row(WarpOut& w, const float (&v)[32]) 
   return buf;
 }
 
+// fp32 variant: 16 values (64 bytes) of this thread's row, v[16*half .. 16*half+15].
+__device__ __forceinline__ uint32_t stage_row_f32(WarpOut& w, const float (&v)[32], int half) {
+  if (w.inflight >= kStagesPerWarp) {
+    if (w.lane == 0) bulk_wait_read<kStagesPerWarp - 1>();
+    __syncwarp();
+    w.inflight = kStagesPerWarp - 1;
+  }
+  const uint32_t buf = w.buf0 + w.next * kStageBytes;
+  w.next = (w.next + 1) % kStagesPerWarp;
+  const uint32_t row = buf + w.lane * 64;
+  const int sw = (w.lane >> 1) & 3;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int b = 16 * half + 4 * q;
+    st_shared_v4(row + ((q ^ sw) << 4), __float_as_uint(v[b]), __float_as_uint(v[b + 1]),
+                 __float_as_uint(v[b + 2]), __float_as_uint(v[b + 3]));
+  }
+  return buf;
+}
+
 __device__ __forceinline__ void stage_store(WarpOut& w, uint32_t buf, const CUtensorMap* map, int x,
                                             int y, int z, bool three_d) {
   fence_proxy_async_smem();
@@ -229,20 +249,19 @@ __device__ __forceinline__ void load_row_chunk_bf16(const __nv_bfloat16* src, fl
 __device__ __forceinline__ float sigmoid_f(float g) { return __fdividef(1.0f, 1.0f + __expf(-g)); }
 __device__ __forceinline__ float silu_f(float g) { return g * sigmoid_f(g); }
 
-// fp32 output (split-K router partials): direct stores.
+// fp32 output (split-K router partials).  RAGGED_K: D is the group's (split's)
+// M x N slice, map tmD0 3-D [groups][M][N] with 16x32 fp32 boxes.
 template <class C>
 __device__ void epilogue_store_f32(const GemmArgs& a, const TileInfo& ti, uint32_t tacc,
-                                   int row_in_tile) {
+                                   int row_in_tile, WarpOut& w, const CUtensorMap* tmD0) {
+  const int quad = row_in_tile >> 5;
   const bool valid = row_in_tile < ti.rows_valid;
+  const bool warp_full = a.f32_tma && quad * 32 + 32 <= ti.rows_valid;
   const int n0 = ti.nb * C::BN;
-  float* base = a.d_f32;
-  long long row;
-  if constexpr (C::SCH == RAGGED_K) {
-    base += (long long)ti.g * a.d_group_stride;
-    row = ti.mb * BM + row_in_tile;
-  } else {
-    row = ti.row0 + row_in_tile;
-  }
+  constexpr bool k3 = C::SCH == RAGGED_K;
+  float* base = a.d_f32 + (k3 ? (long long)ti.g * a.d_group_stride : 0);
+  const long long row = (k3 ? ti.mb * BM : ti.row0) + row_in_tile;
+  const int y = (k3 ? ti.mb * BM : ti.row0) + quad * 32;
   float v[32];
 #pragma unroll 1
   for (int c = 0; c < (C::BN + 31) / 32; ++c) {
@@ -253,13 +272,11 @@ __device__ void epilogue_store_f32(const GemmArgs& a, const TileInfo& ti, uint32
 #pragma unroll
       for (int i = 0; i < 32; ++i) v[i] = 0.f;
     }
-    if (!valid) continue;
-    float* dst = base + row * a.ldd + col;
-    if (col + 32 <= a.N) {
-      float4* p = reinterpret_cast<float4*>(dst);
-#pragma unroll
-      for (int q = 0; q < 8; ++q) p[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-    } else {
+    if (warp_full) {
+      stage_store(w, stage_row_f32(w, v, 0), tmD0, col, y, ti.g, k3);
+      if (col + 16 < a.N) stage_store(w, stage_row_f32(w, v, 1), tmD0, col + 16, y, ti.g, k3);
+    } else if (valid) {
+      float* dst = base + row * a.ldd + col;
       for (int i = 0; i < 32 && col + i < a.N; ++i) dst[i] = v[i];
     }
   }
@@ -633,7 +650,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (!mbar_wait(smem_u32(&tfull_bar[acc]), acc_phase, abort_flag, a.status)) break;
       tc_fence_after();
       const uint32_t tacc = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * C::BN;
-      if constexpr (C::EPI == EPI_STORE_F32) epilogue_store_f32<C>(a, ti, tacc, row_in_tile);
+      if constexpr (C::EPI == EPI_STORE_F32) epilogue_store_f32<C>(a, ti, tacc, row_in_tile, wo, &tmD0);
       else if constexpr (C::EPI == EPI_SWIGLU) epilogue_swiglu<C>(a, ti, tacc, row_in_tile, wo, &tmD0, &tmD1);
       else if constexpr (C::EPI == EPI_STORE) epilogue_store<C>(a, ti, tacc, row_in_tile, wo, &tmD0);
       else epilogue_dgrad_swiglu<C>(a, T, ti, tacc, row_in_tile, wo, &tmD0, &tmD1);

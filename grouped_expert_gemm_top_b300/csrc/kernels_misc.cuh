@@ -14,8 +14,9 @@
 
 namespace moe {
 
-constexpr int kSortChunk = 2048;   // slots per block in the expert sort
-constexpr int kSortThreads = 256;  // 8 warps x 256 slots
+constexpr int kSortThreads = 256;                     // 8 warps
+constexpr int kSortPerLane = 4;                       // slots per lane
+constexpr int kSortChunk = kSortThreads * kSortPerLane;  // slots per block
 constexpr int kPadRows = 128;      // per-expert row padding of the backward layout
 
 // ---------------------------------------------------------------- router top-k
@@ -26,6 +27,7 @@ constexpr int kPadRows = 128;      // per-expert row padding of the backward lay
 // e_j = (t*k + j) mod E instead of the argmax rounds.  Reductions use a fixed
 // butterfly order, so results are bit-identical run to run.
 constexpr int kRouterMaxPerLane = 8;  // E <= 256
+constexpr int kMaxSplitsRouter = 8;   // split-K slices of the router GEMM
 
 __device__ __forceinline__ bool topk_before(float va, int ia, float vb, int ib) {
   return va > vb || (va == vb && ia < ib);
@@ -45,8 +47,14 @@ __global__ void router_topk_kernel(const float* __restrict__ partial, int splits
     const int e = i * 32 + lane;
     v[i] = -INFINITY;
     if (e < E) {
+      float part[kMaxSplitsRouter];
+#pragma unroll
+      for (int sp = 0; sp < kMaxSplitsRouter; ++sp)
+        part[sp] = sp < splits ? __ldg(partial + ((size_t)sp * T + t) * E + e) : 0.f;
       float l = 0.f;
-      for (int sp = 0; sp < splits; ++sp) l += __ldg(partial + ((size_t)sp * T + t) * E + e);
+#pragma unroll
+      for (int sp = 0; sp < kMaxSplitsRouter; ++sp)
+        if (sp < splits) l += part[sp];
       if (bias) l += __ldg(bias + e);
       v[i] = l;
       mx = fmaxf(mx, l);
@@ -120,47 +128,24 @@ __global__ void gather_rows_kernel(const __nv_bfloat16* __restrict__ x,
   for (int c = lane; c < H / 8; c += 32) dst[c] = __ldg(src + c);
 }
 
-// Backward copies in the padded per-expert layout: for padded row p with token
-// row_tok[p] (-1 = padding), a_sorted[p] = a[token] and b_sorted[p] = b[token],
-// padding rows are zero.  Rows at or past poff[E] are not touched.
-__global__ void gather_rows_padded_kernel(const int32_t* __restrict__ row_tok,
-                                          const int32_t* __restrict__ poff, int E, int P, int H,
-                                          int T, const __nv_bfloat16* __restrict__ a,
-                                          __nv_bfloat16* __restrict__ a_sorted,
-                                          const __nv_bfloat16* __restrict__ b,
-                                          __nv_bfloat16* __restrict__ b_sorted) {
-  const long long p = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (p >= P || p >= __ldg(poff + E)) return;
-  const int tok = __ldg(row_tok + p);
-  uint4* da = reinterpret_cast<uint4*>(a_sorted + (size_t)p * H);
-  uint4* db = reinterpret_cast<uint4*>(b_sorted + (size_t)p * H);
-  if (tok < 0 || tok >= T) {
-    for (int c = lane; c < H / 8; c += 32) {
-      da[c] = make_uint4(0, 0, 0, 0);
-      db[c] = make_uint4(0, 0, 0, 0);
-    }
-    return;
-  }
-  const uint4* sa = reinterpret_cast<const uint4*>(a + (size_t)tok * H);
-  const uint4* sb = reinterpret_cast<const uint4*>(b + (size_t)tok * H);
-  for (int c = lane; c < H / 8; c += 32) {
-    da[c] = __ldg(sa + c);
-    db[c] = __ldg(sb + c);
-  }
-}
-
 // ---------------------------------------------------------------- expert sort
 // Pass 1: per-block expert histogram of the slots s = t*k + j.
 __global__ void sort_histogram_kernel(const int32_t* __restrict__ topk_idx, int S, int E,
                                       int32_t* __restrict__ block_counts, int* status) {
   __shared__ int hist[256];
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
-  __syncthreads();
+  int ids[kSortPerLane];
   const int s0 = blockIdx.x * kSortChunk;
-  const int s1 = min(S, s0 + kSortChunk);
-  for (int s = s0 + threadIdx.x; s < s1; s += blockDim.x) {
-    const int e = __ldg(topk_idx + s);
+#pragma unroll
+  for (int i = 0; i < kSortPerLane; ++i) {
+    const int s = s0 + i * kSortThreads + threadIdx.x;
+    ids[i] = s < S ? __ldg(topk_idx + s) : -2;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < kSortPerLane; ++i) {
+    const int e = ids[i];
+    if (e == -2) continue;
     if (e < 0 || e >= E) { record_status(status, MOE_DEV_BAD_INDEX); continue; }
     atomicAdd(&hist[e], 1);
   }
@@ -168,8 +153,9 @@ __global__ void sort_histogram_kernel(const int32_t* __restrict__ topk_idx, int 
   for (int e = threadIdx.x; e < E; e += blockDim.x) block_counts[(size_t)blockIdx.x * E + e] = hist[e];
 }
 
-// Pass 2: global offsets + stable scatter.  Each warp walks its 256 slots in
-// order, 32 at a time; lanes holding the same expert are ranked by lane id
+// Pass 2: global offsets + stable scatter.  Warp w of block b owns the
+// contiguous slots [b*C + w*C/8, b*C + (w+1)*C/8), held in registers, walked
+// 32 at a time in order; lanes holding the same expert are ranked by lane id
 // (match_any), so the sorted order within an expert is ascending slot id.
 __global__ void sort_scatter_kernel(const int32_t* __restrict__ topk_idx, int S, int E,
                                     int num_blocks, const int32_t* __restrict__ block_counts,
@@ -180,12 +166,20 @@ __global__ void sort_scatter_kernel(const int32_t* __restrict__ topk_idx, int S,
   __shared__ int total[256];
   __shared__ int wcount[8][256];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int w0 = blockIdx.x * kSortChunk + warp * (kSortChunk / 8);
+  int ids[kSortPerLane];
+#pragma unroll
+  for (int i = 0; i < kSortPerLane; ++i) {
+    const int s = w0 + i * 32 + lane;
+    int e = s < S ? __ldg(topk_idx + s) : -1;
+    ids[i] = (e >= E || e < 0) ? -1 : e;
+  }
   // expert totals and this block's start inside each expert
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     int tot = 0, before = 0;
     for (int b = 0; b < num_blocks; ++b) {
       const int c = __ldg(block_counts + (size_t)b * E + e);
-      if (b < (int)blockIdx.x) before += c;
+      before += (b < (int)blockIdx.x) ? c : 0;
       tot += c;
     }
     total[e] = tot;
@@ -215,12 +209,9 @@ __global__ void sort_scatter_kernel(const int32_t* __restrict__ topk_idx, int S,
     if (blockIdx.x == 0 && lane == 0) expert_offsets[E] = run;
   }
   // per-warp counts
-  const int w0 = blockIdx.x * kSortChunk + warp * (kSortChunk / 8);
-  const int w1 = min(S, w0 + kSortChunk / 8);
-  for (int g = w0; g < w1; g += 32) {
-    const int s = g + lane;
-    int e = (s < w1) ? __ldg(topk_idx + s) : -1;
-    if (e >= E) e = -1;
+#pragma unroll
+  for (int i = 0; i < kSortPerLane; ++i) {
+    const int e = ids[i];
     const unsigned m = __match_any_sync(0xffffffffu, e);
     if (e >= 0 && lane == __ffs(m) - 1) wcount[warp][e] += __popc(m);
     __syncwarp();
@@ -236,14 +227,13 @@ __global__ void sort_scatter_kernel(const int32_t* __restrict__ topk_idx, int S,
     }
   }
   __syncthreads();
-  for (int g = w0; g < w1; g += 32) {
-    const int s = g + lane;
-    int e = (s < w1) ? __ldg(topk_idx + s) : -1;
-    if (e >= E) e = -1;
+#pragma unroll
+  for (int i = 0; i < kSortPerLane; ++i) {
+    const int e = ids[i];
     const unsigned m = __match_any_sync(0xffffffffu, e);
     if (e >= 0) {
-      const int rank = __popc(m & ((1u << lane) - 1u));
-      const int pos = wcount[warp][e] + rank;
+      const int pos = wcount[warp][e] + __popc(m & ((1u << lane) - 1u));
+      const int s = w0 + i * 32 + lane;
       perm_slot[pos] = s;
       slot_perm[s] = pos;
     }
@@ -255,40 +245,54 @@ __global__ void sort_scatter_kernel(const int32_t* __restrict__ topk_idx, int S,
 
 // ---------------------------------------------------------------- combine
 // out[t] = sum_j w[t,j] * y_perm[slot_perm[t*k+j]] (+ y_shared[t]); fp32 sum in
-// j order, one bf16 rounding.  One warp per token, 16-byte loads.
+// j order, one bf16 rounding.  One warp per token; the k row indices and
+// weights sit in registers so each lane has k independent 16-byte loads in
+// flight per chunk.
+template <int KMAX>
 __global__ void combine_kernel(const __nv_bfloat16* __restrict__ y_perm,
                                const int32_t* __restrict__ slot_perm,
                                const float* __restrict__ topk_w,
                                const __nv_bfloat16* __restrict__ y_shared,
                                __nv_bfloat16* __restrict__ out, int T, int H, int k, int S) {
-  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
-  if (warp >= T) return;
-  const int t = warp;
+  if (t >= T) return;
   int row_l = 0;
   float w_l = 0.f;
   if (lane < k) {
     row_l = clampi(__ldg(slot_perm + (size_t)t * k + lane), 0, S - 1);
     w_l = __ldg(topk_w + (size_t)t * k + lane);
   }
-  const int nchunk = H / 8;
-  for (int c = lane; c < nchunk; c += 32) {
+  int rows[KMAX];
+  float ws[KMAX];
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j) {
+    rows[j] = __shfl_sync(0xffffffffu, row_l, j);
+    ws[j] = __shfl_sync(0xffffffffu, w_l, j);
+  }
+  for (int c = lane; c < H / 8; c += 32) {
+    uint4 v[KMAX];
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j)
+      if (j < k) v[j] = __ldg(reinterpret_cast<const uint4*>(y_perm + (size_t)rows[j] * H) + c);
+    uint4 vs = make_uint4(0, 0, 0, 0);
+    if (y_shared) vs = __ldg(reinterpret_cast<const uint4*>(y_shared + (size_t)t * H) + c);
     float acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-    for (int j = 0; j < k; ++j) {
-      const int row = __shfl_sync(0xffffffffu, row_l, j);
-      const float w = __shfl_sync(0xffffffffu, w_l, j);
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(y_perm + (size_t)row * H) + c);
-      acc[0] = fmaf(w, bf16lo(v.x), acc[0]); acc[1] = fmaf(w, bf16hi(v.x), acc[1]);
-      acc[2] = fmaf(w, bf16lo(v.y), acc[2]); acc[3] = fmaf(w, bf16hi(v.y), acc[3]);
-      acc[4] = fmaf(w, bf16lo(v.z), acc[4]); acc[5] = fmaf(w, bf16hi(v.z), acc[5]);
-      acc[6] = fmaf(w, bf16lo(v.w), acc[6]); acc[7] = fmaf(w, bf16hi(v.w), acc[7]);
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+      if (j < k) {
+        const float w = ws[j];
+        acc[0] = fmaf(w, bf16lo(v[j].x), acc[0]); acc[1] = fmaf(w, bf16hi(v[j].x), acc[1]);
+        acc[2] = fmaf(w, bf16lo(v[j].y), acc[2]); acc[3] = fmaf(w, bf16hi(v[j].y), acc[3]);
+        acc[4] = fmaf(w, bf16lo(v[j].z), acc[4]); acc[5] = fmaf(w, bf16hi(v[j].z), acc[5]);
+        acc[6] = fmaf(w, bf16lo(v[j].w), acc[6]); acc[7] = fmaf(w, bf16hi(v[j].w), acc[7]);
+      }
     }
     if (y_shared) {
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(y_shared + (size_t)t * H) + c);
-      acc[0] += bf16lo(v.x); acc[1] += bf16hi(v.x); acc[2] += bf16lo(v.y); acc[3] += bf16hi(v.y);
-      acc[4] += bf16lo(v.z); acc[5] += bf16hi(v.z); acc[6] += bf16lo(v.w); acc[7] += bf16hi(v.w);
+      acc[0] += bf16lo(vs.x); acc[1] += bf16hi(vs.x); acc[2] += bf16lo(vs.y); acc[3] += bf16hi(vs.y);
+      acc[4] += bf16lo(vs.z); acc[5] += bf16hi(vs.z); acc[6] += bf16lo(vs.w); acc[7] += bf16hi(vs.w);
     }
     uint4 o;
     o.x = pack_bf16x2(acc[0], acc[1]); o.y = pack_bf16x2(acc[2], acc[3]);
@@ -298,130 +302,157 @@ __global__ void combine_kernel(const __nv_bfloat16* __restrict__ y_perm,
 }
 
 // ---------------------------------------------------------------- backward helpers
-// Padded offsets: every expert's rows start on a 128-row boundary.
-__global__ void pad_offsets_kernel(const int32_t* __restrict__ expert_offsets, int E,
-                                   int32_t* __restrict__ poff) {
-  const int lane = threadIdx.x;
+// Padded per-expert layout: expert e's rows start at poff[e], a multiple of
+// 128, and occupy ceil(n_e / 128) * 128 rows; the rows past its n_e tokens are
+// zero in every sorted copy, so weight-gradient GEMMs can run whole 64-row
+// k-blocks.
+
+// Exclusive scan of the padded group sizes into sp[0..E] (one warp).
+__device__ __forceinline__ void padded_scan_warp(const int* so, int E, int* sp, int lane) {
   int run = 0;
   for (int b0 = 0; b0 < E; b0 += 32) {
     const int e = b0 + lane;
-    int v = 0;
-    if (e < E) {
-      const int n = __ldg(expert_offsets + e + 1) - __ldg(expert_offsets + e);
-      v = ((n + kPadRows - 1) / kPadRows) * kPadRows;
-    }
+    const int n = e < E ? so[e + 1] - so[e] : 0;
+    const int v = ((n + kPadRows - 1) / kPadRows) * kPadRows;
     int inc = v;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
       const int x = __shfl_up_sync(0xffffffffu, inc, d);
       if (lane >= d) inc += x;
     }
-    if (e < E) poff[e] = run + inc - v;
+    if (e < E) sp[e] = run + inc - v;
     run += __shfl_sync(0xffffffffu, inc, 31);
   }
-  if (lane == 0) poff[E] = run;
+  if (lane == 0) sp[E] = run;
 }
 
-// For every row p of the padded layout: the token it reads (-1 for padding rows).
-__global__ void padded_row_tokens_kernel(const int32_t* __restrict__ expert_offsets,
-                                         const int32_t* __restrict__ poff,
+// Padded offsets, and the padded sorted copies of grad_out and x
+// (a_sorted[p] = a[token of row p], zero rows for padding).  One warp per row,
+// grid-stride; block 0 also writes poff[0..E].
+__global__ void bwd_sorted_copies_kernel(const int32_t* __restrict__ expert_offsets,
                                          const int32_t* __restrict__ perm_slot, int E, int k,
-                                         int S_pad_max, int32_t* __restrict__ row_tok) {
-  __shared__ int sp[257];
+                                         int H, int T, const __nv_bfloat16* __restrict__ a,
+                                         __nv_bfloat16* __restrict__ a_sorted,
+                                         const __nv_bfloat16* __restrict__ b,
+                                         __nv_bfloat16* __restrict__ b_sorted,
+                                         int32_t* __restrict__ poff) {
   __shared__ int so[257];
-  for (int e = threadIdx.x; e <= E; e += blockDim.x) {
-    sp[e] = poff[e];
-    so[e] = expert_offsets[e];
-  }
+  __shared__ int sp[257];
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) so[e] = __ldg(expert_offsets + e);
   __syncthreads();
-  const int p = blockIdx.x * blockDim.x + threadIdx.x;
-  if (p >= S_pad_max) return;
-  int tok = -1;
-  if (p < sp[E]) {
+  if (threadIdx.x < 32) padded_scan_warp(so, E, sp, threadIdx.x);
+  __syncthreads();
+  if (blockIdx.x == 0)
+    for (int e = threadIdx.x; e <= E; e += blockDim.x) poff[e] = sp[e];
+  const int lane = threadIdx.x & 31;
+  const long long nwarps = (long long)gridDim.x * (blockDim.x >> 5);
+  for (long long p = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); p < sp[E];
+       p += nwarps) {
     int lo = 0, hi = E - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
       if (sp[mid] <= p) lo = mid; else hi = mid - 1;
     }
-    const int i = p - sp[lo];
-    if (i < so[lo + 1] - so[lo]) tok = __ldg(perm_slot + so[lo] + i) / k;
+    const int i = (int)(p - sp[lo]);
+    int tok = -1;
+    if (i < so[lo + 1] - so[lo]) tok = clampi(__ldg(perm_slot + so[lo] + i) / k, 0, T - 1);
+    uint4* da = reinterpret_cast<uint4*>(a_sorted + (size_t)p * H);
+    uint4* db = reinterpret_cast<uint4*>(b_sorted + (size_t)p * H);
+    if (tok < 0) {
+      for (int c = lane; c < H / 8; c += 32) {
+        da[c] = make_uint4(0, 0, 0, 0);
+        db[c] = make_uint4(0, 0, 0, 0);
+      }
+    } else {
+      const uint4* sa = reinterpret_cast<const uint4*>(a + (size_t)tok * H);
+      const uint4* sb = reinterpret_cast<const uint4*>(b + (size_t)tok * H);
+      for (int c = lane; c < H / 8; c += 32) {
+        const uint4 va = __ldg(sa + c);
+        const uint4 vb = __ldg(sb + c);
+        da[c] = va;
+        db[c] = vb;
+      }
+    }
   }
-  row_tok[p] = tok;
 }
 
-// Router backward, one thread per token.  dw[j] = sum of the down-projection
-// partials; the renormalised top-k weights are a softmax over the chosen
-// logits, so dlogit[j] = w_j (dw_j - sum_i w_i dw_i) and every other logit
-// gets zero.  Output dl per slot (fp32).
-__global__ void router_backward_kernel(const int32_t* __restrict__ topk_idx,
-                                       const float* __restrict__ topk_w,
-                                       const int32_t* __restrict__ slot_perm,
-                                       const int32_t* __restrict__ expert_offsets,
-                                       const int32_t* __restrict__ poff,
-                                       const float* __restrict__ dw_part, int nNB, int T, int k,
-                                       int E, int P, float* __restrict__ dl) {
-  const int t = blockIdx.x * blockDim.x + threadIdx.x;
-  if (t >= T) return;
-  float dw[32], w[32];
-  float dot = 0.f;
-  for (int j = 0; j < k; ++j) {
-    const int s = t * k + j;
-    const int e = clampi(__ldg(topk_idx + s), 0, E - 1);
-    const int p = clampi(__ldg(slot_perm + s) - __ldg(expert_offsets + e) + __ldg(poff + e), 0, P - 1);
-    float sum = 0.f;
-    for (int b = 0; b < nNB; ++b) sum += __ldg(dw_part + (size_t)p * nNB + b);
-    dw[j] = sum;
-    w[j] = __ldg(topk_w + s);
-    dot = fmaf(w[j], sum, dot);
-  }
-  for (int j = 0; j < k; ++j) dl[(size_t)t * k + j] = w[j] * (dw[j] - dot);
-}
-
-// dx[t] = sum_j dx_slot[p(t,j)] + sum_j dl[t,j] W_r[e_j] (+ dx_shared[t]).  One warp per token.
+// Router backward fused with the per-token gradient gather, one warp per token.
+// Router: dw_j = sum of the down-projection partials of slot j; the renormalised
+// top-k weights are a softmax over the chosen logits, so
+// dlogit_j = w_j (dw_j - sum_i w_i dw_i) (every other logit gets zero); dl is
+// written per slot for the router weight gradient.
+// dx[t] = sum_j dx_slot[p(t,j)] + sum_j dlogit_j W_r[e_j] (+ dx_shared[t]).
+template <int KMAX>
 __global__ void dx_gather_kernel(const __nv_bfloat16* __restrict__ dx_slot,
                                  const int32_t* __restrict__ topk_idx,
+                                 const float* __restrict__ topk_w,
                                  const int32_t* __restrict__ slot_perm,
                                  const int32_t* __restrict__ expert_offsets,
-                                 const int32_t* __restrict__ poff, const float* __restrict__ dl,
-                                 const __nv_bfloat16* __restrict__ w_router,
+                                 const int32_t* __restrict__ poff, const float* __restrict__ dw_part,
+                                 int nNB, const __nv_bfloat16* __restrict__ w_router,
                                  const __nv_bfloat16* __restrict__ dx_shared,
-                                 __nv_bfloat16* __restrict__ dx, int T, int H, int k, int E,
-                                 int P) {
-  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+                                 float* __restrict__ dl_out, __nv_bfloat16* __restrict__ dx, int T,
+                                 int H, int k, int E, int P) {
+  const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
-  if (warp >= T) return;
-  const int t = warp;
+  if (t >= T) return;
   int row_l = 0, e_l = 0;
-  float dl_l = 0.f;
+  float dw_l = 0.f, w_l = 0.f;
   if (lane < k) {
     const int s = t * k + lane;
     e_l = clampi(__ldg(topk_idx + s), 0, E - 1);
     row_l = clampi(__ldg(slot_perm + s) - __ldg(expert_offsets + e_l) + __ldg(poff + e_l), 0, P - 1);
-    dl_l = __ldg(dl + s);
+    for (int b = 0; b < nNB; ++b) dw_l += __ldg(dw_part + (size_t)row_l * nNB + b);
+    w_l = __ldg(topk_w + s);
+  }
+  float dot = w_l * dw_l;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+  const float dl_l = w_l * (dw_l - dot);
+  if (lane < k) dl_out[(size_t)t * k + lane] = dl_l;
+  int rows[KMAX], es[KMAX];
+  float dls[KMAX];
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j) {
+    rows[j] = __shfl_sync(0xffffffffu, row_l, j);
+    es[j] = __shfl_sync(0xffffffffu, e_l, j);
+    dls[j] = __shfl_sync(0xffffffffu, dl_l, j);
   }
   for (int c = lane; c < H / 8; c += 32) {
+    uint4 v[KMAX], r[KMAX];
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+      if (j < k) {
+        v[j] = __ldg(reinterpret_cast<const uint4*>(dx_slot + (size_t)rows[j] * H) + c);
+        r[j] = __ldg(reinterpret_cast<const uint4*>(w_router + (size_t)es[j] * H) + c);
+      }
+    }
+    uint4 vs = make_uint4(0, 0, 0, 0);
+    if (dx_shared) vs = __ldg(reinterpret_cast<const uint4*>(dx_shared + (size_t)t * H) + c);
     float acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-    for (int j = 0; j < k; ++j) {
-      const int row = __shfl_sync(0xffffffffu, row_l, j);
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(dx_slot + (size_t)row * H) + c);
-      acc[0] += bf16lo(v.x); acc[1] += bf16hi(v.x); acc[2] += bf16lo(v.y); acc[3] += bf16hi(v.y);
-      acc[4] += bf16lo(v.z); acc[5] += bf16hi(v.z); acc[6] += bf16lo(v.w); acc[7] += bf16hi(v.w);
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+      if (j < k) {
+        acc[0] += bf16lo(v[j].x); acc[1] += bf16hi(v[j].x); acc[2] += bf16lo(v[j].y);
+        acc[3] += bf16hi(v[j].y); acc[4] += bf16lo(v[j].z); acc[5] += bf16hi(v[j].z);
+        acc[6] += bf16lo(v[j].w); acc[7] += bf16hi(v[j].w);
+      }
     }
-    for (int j = 0; j < k; ++j) {
-      const int e = __shfl_sync(0xffffffffu, e_l, j);
-      const float d = __shfl_sync(0xffffffffu, dl_l, j);
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(w_router + (size_t)e * H) + c);
-      acc[0] = fmaf(d, bf16lo(v.x), acc[0]); acc[1] = fmaf(d, bf16hi(v.x), acc[1]);
-      acc[2] = fmaf(d, bf16lo(v.y), acc[2]); acc[3] = fmaf(d, bf16hi(v.y), acc[3]);
-      acc[4] = fmaf(d, bf16lo(v.z), acc[4]); acc[5] = fmaf(d, bf16hi(v.z), acc[5]);
-      acc[6] = fmaf(d, bf16lo(v.w), acc[6]); acc[7] = fmaf(d, bf16hi(v.w), acc[7]);
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+      if (j < k) {
+        const float d = dls[j];
+        acc[0] = fmaf(d, bf16lo(r[j].x), acc[0]); acc[1] = fmaf(d, bf16hi(r[j].x), acc[1]);
+        acc[2] = fmaf(d, bf16lo(r[j].y), acc[2]); acc[3] = fmaf(d, bf16hi(r[j].y), acc[3]);
+        acc[4] = fmaf(d, bf16lo(r[j].z), acc[4]); acc[5] = fmaf(d, bf16hi(r[j].z), acc[5]);
+        acc[6] = fmaf(d, bf16lo(r[j].w), acc[6]); acc[7] = fmaf(d, bf16hi(r[j].w), acc[7]);
+      }
     }
     if (dx_shared) {
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(dx_shared + (size_t)t * H) + c);
-      acc[0] += bf16lo(v.x); acc[1] += bf16hi(v.x); acc[2] += bf16lo(v.y); acc[3] += bf16hi(v.y);
-      acc[4] += bf16lo(v.z); acc[5] += bf16hi(v.z); acc[6] += bf16lo(v.w); acc[7] += bf16hi(v.w);
+      acc[0] += bf16lo(vs.x); acc[1] += bf16hi(vs.x); acc[2] += bf16lo(vs.y); acc[3] += bf16hi(vs.y);
+      acc[4] += bf16lo(vs.z); acc[5] += bf16hi(vs.z); acc[6] += bf16lo(vs.w); acc[7] += bf16hi(vs.w);
     }
     uint4 o;
     o.x = pack_bf16x2(acc[0], acc[1]); o.y = pack_bf16x2(acc[2], acc[3]);
@@ -431,8 +462,9 @@ __global__ void dx_gather_kernel(const __nv_bfloat16* __restrict__ dx_slot,
 }
 
 // dW_r[e, :] = sum over the rows of expert e (sorted order) of dl[slot] * x[token, :];
-// db[e] = sum of those dl.  Block = (expert, 256-column chunk), 4 warps split the
-// rows round-robin and their partials are added in warp order.
+// db[e] = sum of those dl.  Block = (expert, 256-column chunk); the expert's
+// rows are taken 32 at a time (lane j loads row j's slot and dl), 4 warps take
+// every 4th batch, and the 4 partials are added in warp order.
 __global__ void router_wgrad_kernel(const __nv_bfloat16* __restrict__ x,
                                     const int32_t* __restrict__ expert_offsets,
                                     const int32_t* __restrict__ perm_slot,
@@ -444,21 +476,35 @@ __global__ void router_wgrad_kernel(const __nv_bfloat16* __restrict__ x,
   const int e = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c0 = blockIdx.x * 256 + lane * 8;  // 8 columns per lane
+  const bool col_ok = c0 < H;
   const int r0 = __ldg(expert_offsets + e), r1 = __ldg(expert_offsets + e + 1);
   float acc[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc[i] = 0.f;
   float bsum = 0.f;
-  for (int r = r0 + warp; r < r1; r += 4) {
-    const int s = __ldg(perm_slot + r);
-    const float d = __ldg(dl + s);
-    bsum += d;
-    if (c0 < H) {
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(x + (size_t)(s / k) * H + c0));
-      acc[0] = fmaf(d, bf16lo(v.x), acc[0]); acc[1] = fmaf(d, bf16hi(v.x), acc[1]);
-      acc[2] = fmaf(d, bf16lo(v.y), acc[2]); acc[3] = fmaf(d, bf16hi(v.y), acc[3]);
-      acc[4] = fmaf(d, bf16lo(v.z), acc[4]); acc[5] = fmaf(d, bf16hi(v.z), acc[5]);
-      acc[6] = fmaf(d, bf16lo(v.w), acc[6]); acc[7] = fmaf(d, bf16hi(v.w), acc[7]);
+  for (int rb = r0 + warp * 32; rb < r1; rb += 4 * 32) {
+    int tok_l = 0;
+    float d_l = 0.f;
+    if (rb + lane < r1) {
+      const int s = __ldg(perm_slot + rb + lane);
+      tok_l = s / k;
+      d_l = __ldg(dl + s);
+    }
+    const int nb = min(32, r1 - rb);
+#pragma unroll 8
+    for (int j = 0; j < 32; ++j) {
+      const int tok = __shfl_sync(0xffffffffu, tok_l, j);
+      const float d = __shfl_sync(0xffffffffu, d_l, j);
+      if (j < nb) {
+        bsum += d;
+        if (col_ok) {
+          const uint4 v = __ldg(reinterpret_cast<const uint4*>(x + (size_t)tok * H + c0));
+          acc[0] = fmaf(d, bf16lo(v.x), acc[0]); acc[1] = fmaf(d, bf16hi(v.x), acc[1]);
+          acc[2] = fmaf(d, bf16lo(v.y), acc[2]); acc[3] = fmaf(d, bf16hi(v.y), acc[3]);
+          acc[4] = fmaf(d, bf16lo(v.z), acc[4]); acc[5] = fmaf(d, bf16hi(v.z), acc[5]);
+          acc[6] = fmaf(d, bf16lo(v.w), acc[6]); acc[7] = fmaf(d, bf16hi(v.w), acc[7]);
+        }
+      }
     }
   }
 #pragma unroll
@@ -471,7 +517,7 @@ __global__ void router_wgrad_kernel(const __nv_bfloat16* __restrict__ x,
     for (int i = 0; i < 8; ++i)
       o[i] = ((part[0][lane * 8 + i] + part[1][lane * 8 + i]) + part[2][lane * 8 + i]) +
              part[3][lane * 8 + i];
-    if (c0 < H) {
+    if (col_ok) {
       uint4 v;
       v.x = pack_bf16x2(o[0], o[1]); v.y = pack_bf16x2(o[2], o[3]);
       v.z = pack_bf16x2(o[4], o[5]); v.w = pack_bf16x2(o[6], o[7]);

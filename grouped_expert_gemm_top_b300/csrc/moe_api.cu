@@ -21,7 +21,7 @@ namespace {
 using moe::GemmArgs;
 using moe::GemmCfg;
 
-constexpr int32_t kAbiVersion = 1;
+constexpr int32_t kAbiVersion = 2;
 constexpr size_t kAlign = 256;
 
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
@@ -45,7 +45,7 @@ constexpr int kMaxRouterSplits = 8;
 
 struct Layout {
   size_t status, counts, logits_part, x_sorted, h, h_sh, fwd_end;
-  size_t poff, row_tok, dout_sorted, x_sorted_pad, dgu, hw, dxs, dwp, dl, dgu_sh, hw_sh, dxs_sh,
+  size_t poff, dout_sorted, x_sorted_pad, dgu, hw, dxs, dwp, dl, dgu_sh, hw_sh, dxs_sh,
       total;
   int sort_blocks;
   long long S, S_pad_max;
@@ -70,7 +70,6 @@ Layout make_layout(const moe_dims& d, bool bwd) {
   if (bwd) {
     const size_t P = (size_t)L.S_pad_max;
     L.poff = o; o = align_up(o + (size_t)(d.E + 1) * 4);
-    L.row_tok = o; o = align_up(o + P * 4);
     L.dout_sorted = o; o = align_up(o + P * d.H * 2);
     L.x_sorted_pad = o; o = align_up(o + P * d.H * 2);
     L.dgu = o; o = align_up(o + P * 2 * d.I * 2);
@@ -241,6 +240,20 @@ using CfgDgradGateUp = GemmCfg<256, 4, KMAJ_TILE, MN_TILE, RAGGED_M, EPI_STORE, 
 using CfgDgradGateUpShared = GemmCfg<256, 4, KMAJ_TILE, MN_TILE, RAGGED_M, EPI_STORE, false, false>;
 using CfgWgrad = GemmCfg<256, 4, MN_TILE, MN_TILE, RAGGED_K, EPI_STORE, false, false>;
 
+// fp32 [depth][rows][inner] output map with 16x32 boxes (64-byte rows).
+bool make_out_map3_f32(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows,
+                       uint64_t depth) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {inner, rows, depth};
+  const cuuint64_t strides[2] = {inner * 4, inner * rows * 4};
+  const cuuint32_t box[3] = {16, 32, 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Output (store) maps use 32x32 boxes.
 bool make_out_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows) {
   return make_map(m, base, inner, rows, 1, 32, 32);
@@ -345,13 +358,15 @@ moe_status moe_route(const moe_dims* d, int32_t gate_mode, const moe_bf16* x,
   GemmArgs a = base_args(at<int>(workspace, 0));
   a.M = T; a.N = E; a.K = H; a.G = splits; a.ksplit = ksplit;
   a.d_f32 = part; a.ldd = E; a.d_group_stride = (long long)T * E;
+  CUtensorMap tD = tA;
+  a.f32_tma = (E % 4 == 0) && make_out_map3_f32(&tD, part, E, T, splits) ? 1 : 0;
   const long long tiles = mt * splits;
   switch (bn) {
-    case 16: s = launch_gemm<CfgRouter<16>>(MOE_K_ROUTER, tA, tB, tA, tB, a, tiles, st); break;
-    case 32: s = launch_gemm<CfgRouter<32>>(MOE_K_ROUTER, tA, tB, tA, tB, a, tiles, st); break;
-    case 64: s = launch_gemm<CfgRouter<64>>(MOE_K_ROUTER, tA, tB, tA, tB, a, tiles, st); break;
-    case 128: s = launch_gemm<CfgRouter<128>>(MOE_K_ROUTER, tA, tB, tA, tB, a, tiles, st); break;
-    default: s = launch_gemm<CfgRouter<256>>(MOE_K_ROUTER, tA, tB, tA, tB, a, tiles, st); break;
+    case 16: s = launch_gemm<CfgRouter<16>>(MOE_K_ROUTER, tA, tB, tD, tD, a, tiles, st); break;
+    case 32: s = launch_gemm<CfgRouter<32>>(MOE_K_ROUTER, tA, tB, tD, tD, a, tiles, st); break;
+    case 64: s = launch_gemm<CfgRouter<64>>(MOE_K_ROUTER, tA, tB, tD, tD, a, tiles, st); break;
+    case 128: s = launch_gemm<CfgRouter<128>>(MOE_K_ROUTER, tA, tB, tD, tD, a, tiles, st); break;
+    default: s = launch_gemm<CfgRouter<256>>(MOE_K_ROUTER, tA, tB, tD, tD, a, tiles, st); break;
   }
   if (s != MOE_OK) return s;
   {
@@ -484,10 +499,15 @@ moe_status moe_unpermute_combine(const moe_dims* d, const moe_bf16* y_perm,
   const int threads = 256;
   const long long blocks = cdiv((long long)d->T * 32, threads);
   KernelScope ks(MOE_K_COMBINE, st);
-  moe::combine_kernel<<<(unsigned)blocks, threads, 0, st>>>(
-      reinterpret_cast<const __nv_bfloat16*>(y_perm), slot_perm, topk_w,
-      reinterpret_cast<const __nv_bfloat16*>(y_shared), reinterpret_cast<__nv_bfloat16*>(out),
-      d->T, d->H, d->k, d->T * d->k);
+  auto* yp = reinterpret_cast<const __nv_bfloat16*>(y_perm);
+  auto* ys = reinterpret_cast<const __nv_bfloat16*>(y_shared);
+  auto* o = reinterpret_cast<__nv_bfloat16*>(out);
+  if (d->k <= 8)
+    moe::combine_kernel<8><<<(unsigned)blocks, threads, 0, st>>>(yp, slot_perm, topk_w, ys, o, d->T,
+                                                                  d->H, d->k, d->T * d->k);
+  else
+    moe::combine_kernel<32><<<(unsigned)blocks, threads, 0, st>>>(yp, slot_perm, topk_w, ys, o, d->T,
+                                                                   d->H, d->k, d->T * d->k);
   return launched(cudaGetLastError());
 }
 
@@ -526,25 +546,19 @@ moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_
   const int T = d->T, H = d->H, E = d->E, I = d->I, k = d->k;
   const long long S = L.S, P = L.S_pad_max;
   int32_t* poff = at<int32_t>(workspace, L.poff);
-  int32_t* row_tok = at<int32_t>(workspace, L.row_tok);
   __nv_bfloat16* dgu = at<__nv_bfloat16>(workspace, L.dgu);
   __nv_bfloat16* hw = at<__nv_bfloat16>(workspace, L.hw);
   __nv_bfloat16* dxs = at<__nv_bfloat16>(workspace, L.dxs);
   float* dwp = at<float>(workspace, L.dwp);
   float* dl = at<float>(workspace, L.dl);
 
-  { KernelScope ks(MOE_K_PAD_OFFSETS, st);
-    moe::pad_offsets_kernel<<<1, 32, 0, st>>>(expert_offsets, E, poff); }
-  { KernelScope ks(MOE_K_PADDED_ROWS, st);
-    moe::padded_row_tokens_kernel<<<(unsigned)cdiv(P, 256), 256, 0, st>>>(
-        expert_offsets, poff, perm_slot, E, k, (int)P, row_tok); }
   __nv_bfloat16* dos = at<__nv_bfloat16>(workspace, L.dout_sorted);
   __nv_bfloat16* xsp = at<__nv_bfloat16>(workspace, L.x_sorted_pad);
-  {  // sorted copies of grad_out and x in the padded per-expert layout
+  {  // padded offsets + padded sorted copies of grad_out and x
     KernelScope ks(MOE_K_GATHER_ROWS_BWD, st);
-    moe::gather_rows_padded_kernel<<<(unsigned)cdiv(P * 32, 256), 256, 0, st>>>(
-        row_tok, poff, E, (int)P, H, T, reinterpret_cast<const __nv_bfloat16*>(grad_out), dos,
-        reinterpret_cast<const __nv_bfloat16*>(x), xsp);
+    moe::bwd_sorted_copies_kernel<<<(unsigned)std::max(1, 8 * sm_count()), 256, 0, st>>>(
+        expert_offsets, perm_slot, E, k, H, T, reinterpret_cast<const __nv_bfloat16*>(grad_out),
+        dos, reinterpret_cast<const __nv_bfloat16*>(x), xsp, poff);
   }
   if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
 
@@ -561,10 +575,6 @@ moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_
     s = launch_gemm<CfgDgradDown>(MOE_K_DGRAD_DOWN, tA, tB, tD0, tD1, a, cdiv(P, moe::BM) * L.nNB_I, st);
     if (s != MOE_OK) return s;
   }
-  { KernelScope ks(MOE_K_ROUTER_BWD, st);
-  moe::router_backward_kernel<<<(unsigned)cdiv(T, 128), 128, 0, st>>>(
-      topk_idx, topk_w, slot_perm, expert_offsets, poff, dwp, L.nNB_I, T, k, E, (int)P, dl); }
-  if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
   {  // gate/up data gradient -> per-slot dx
     CUtensorMap tA, tB;
     if (!make_map(&tA, dgu, 2LL * I, P, 1, 64, 128)) return MOE_ERR_CUDA;
@@ -610,11 +620,20 @@ moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_
       if (s != MOE_OK) return s;
     }
   }
-  { KernelScope ks(MOE_K_DX_GATHER, st);
-  moe::dx_gather_kernel<<<(unsigned)cdiv((long long)T * 32, 256), 256, 0, st>>>(
-      dxs, topk_idx, slot_perm, expert_offsets, poff, dl,
-      reinterpret_cast<const __nv_bfloat16*>(w_router), dxs_sh,
-      reinterpret_cast<__nv_bfloat16*>(grad_x), T, H, k, E, (int)P); }
+  {  // router backward + per-token gather of the slot gradients
+    KernelScope ks(MOE_K_DX_GATHER, st);
+    const unsigned blocks = (unsigned)cdiv((long long)T * 32, 256);
+    auto* wr = reinterpret_cast<const __nv_bfloat16*>(w_router);
+    auto* gx = reinterpret_cast<__nv_bfloat16*>(grad_x);
+    if (k <= 8)
+      moe::dx_gather_kernel<8><<<blocks, 256, 0, st>>>(dxs, topk_idx, topk_w, slot_perm,
+                                                       expert_offsets, poff, dwp, L.nNB_I, wr,
+                                                       dxs_sh, dl, gx, T, H, k, E, (int)P);
+    else
+      moe::dx_gather_kernel<32><<<blocks, 256, 0, st>>>(dxs, topk_idx, topk_w, slot_perm,
+                                                        expert_offsets, poff, dwp, L.nNB_I, wr,
+                                                        dxs_sh, dl, gx, T, H, k, E, (int)P);
+  }
   { KernelScope ks(MOE_K_ROUTER_WGRAD, st);
   moe::router_wgrad_kernel<<<dim3((unsigned)cdiv(H, 256), E), 128, 0, st>>>(
       reinterpret_cast<const __nv_bfloat16*>(x), expert_offsets, perm_slot, dl, H, k,
@@ -683,11 +702,11 @@ int32_t moe_kernel_count(void) { return MOE_K_COUNT; }
 
 const char* moe_kernel_name(int32_t id) {
   static const char* names[MOE_K_COUNT] = {
-      "router", "sort_histogram", "sort_scatter", "gate_up", "down", "shared_gate_up",
-      "shared_down", "combine", "pad_offsets", "padded_rows", "dgrad_down", "router_bwd",
+      "router", "router_topk", "sort_histogram", "sort_scatter", "gather_rows", "gate_up",
+      "down", "shared_gate_up", "shared_down", "combine", "gather_rows_bwd", "dgrad_down",
       "dgrad_gate_up", "shared_dgrad_down", "shared_dgrad_gate_up", "dx_gather",
       "router_wgrad", "wgrad_down", "wgrad_gate_up", "shared_wgrad_down",
-      "shared_wgrad_gate_up", "router_topk", "gather_rows", "gather_rows_bwd"};
+      "shared_wgrad_gate_up"};
   return (id >= 0 && id < MOE_K_COUNT) ? names[id] : "unknown";
 }
 

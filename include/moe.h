@@ -199,29 +199,26 @@ moe_status moe_read_device_status(void* workspace, size_t workspace_bytes, void*
  */
 typedef enum {
   MOE_K_ROUTER = 0,          /* moe_route: split-K router GEMM (fp32 partial logits) */
-  MOE_K_SORT_HISTOGRAM,      /* moe_permute, pass 1 */
-  MOE_K_SORT_SCATTER,        /* moe_permute, pass 2 */
+  MOE_K_ROUTER_TOPK,         /* moe_route: softmax + top-k (one warp per token) */
+  MOE_K_SORT_HISTOGRAM,      /* moe_permute, pass 1: per-block expert histograms */
+  MOE_K_SORT_SCATTER,        /* moe_permute, pass 2: scan + stable scatter */
+  MOE_K_GATHER_ROWS,         /* forward: expert-sorted copy of the tokens */
   MOE_K_GATE_UP,             /* grouped gate/up GEMM + SwiGLU */
   MOE_K_DOWN,                /* grouped down GEMM */
   MOE_K_SHARED_GATE_UP,      /* shared expert gate/up GEMM + SwiGLU */
   MOE_K_SHARED_DOWN,         /* shared expert down GEMM */
   MOE_K_COMBINE,             /* weighted un-permute / combine */
-  MOE_K_PAD_OFFSETS,         /* backward: padded expert offsets */
-  MOE_K_PADDED_ROWS,         /* backward: token of every padded row */
+  MOE_K_GATHER_ROWS_BWD,     /* backward: padded offsets + padded sorted grad_out and x */
   MOE_K_DGRAD_DOWN,          /* backward: down data-gradient + SwiGLU backward */
-  MOE_K_ROUTER_BWD,          /* backward: router logit gradient */
   MOE_K_DGRAD_GATE_UP,       /* backward: gate/up data-gradient (per slot) */
   MOE_K_SHARED_DGRAD_DOWN,
   MOE_K_SHARED_DGRAD_GATE_UP,
-  MOE_K_DX_GATHER,           /* backward: per-token sum of slot gradients + router term */
+  MOE_K_DX_GATHER,           /* backward: router logit gradient + per-token sum of slot gradients */
   MOE_K_ROUTER_WGRAD,        /* backward: router weight (and bias) gradient */
   MOE_K_WGRAD_DOWN,          /* backward: grouped down weight-gradient GEMM */
   MOE_K_WGRAD_GATE_UP,       /* backward: grouped gate/up weight-gradient GEMM */
   MOE_K_SHARED_WGRAD_DOWN,
   MOE_K_SHARED_WGRAD_GATE_UP,
-  MOE_K_ROUTER_TOPK,         /* moe_route: softmax + top-k (one warp per token) */
-  MOE_K_GATHER_ROWS,         /* forward: expert-sorted copy of the tokens */
-  MOE_K_GATHER_ROWS_BWD,     /* backward: padded sorted copies of grad_out and x */
   MOE_K_COUNT
 } moe_kernel_id;
 

@@ -10,10 +10,16 @@
 // table): the expert weights are read in place from the fused [E, ...] 3-D
 // tensors, and the activations are read from their expert-sorted copy.
 //
-// Roles (192 threads, one CTA per SM, static round-robin over tiles):
+// Roles (one CTA per SM, static round-robin over tiles):
 //   warp 0     TMA producer: fills a STAGES-deep ring of (A, B) k-blocks
 //   warp 1     TMEM allocator and single-thread UMMA issuer
-//   warps 2-5  epilogue: warp w reads TMEM lanes 32*(w%4) .. 32*(w%4)+31
+//   warps 2..  EPI_WARPS epilogue warps: warp w reads TMEM lanes
+//              32*(w%4) .. 32*(w%4)+31; with 8 epilogue warps the two warps of
+//              a lane quadrant split the tile's columns in halves
+//   last 4     gather warps (only when an operand is gathered): copy the
+//              token rows of that operand straight from the unsorted matrix
+//              into the swizzled stage with 16-byte cp.async (LSU path), so
+//              no expert-sorted copy of the activations is ever written
 // Two TMEM accumulators (2 x BN fp32 columns) let the epilogue of tile i run
 // while the mainloop of tile i+1 fills the other one.
 //
@@ -34,12 +40,13 @@ namespace moe {
 
 constexpr int BM = 128;
 constexpr int BK = 64;
-constexpr int kGemmThreads = 192;
 constexpr int kTmemCols = 512;
 constexpr int kMaxGroups = 256;
-constexpr int kEpiSmemBytesDecl = 4 * 3 * 2048;  // epilogue staging (see the epilogue section)
+constexpr int kEpiStagingPerWarp = 3 * 2048;  // epilogue staging (see the epilogue section)
 
-enum LoadMode : int { KMAJ_TILE = 0, MN_TILE = 2 };
+// TILE: TMA tile loads.  GATHER: rows (K-major: M rows; MN-major: K rows) are
+// token rows of a [tokens, ld] matrix, selected through the expert sort.
+enum LoadMode : int { KMAJ_TILE = 0, KMAJ_GATHER = 1, MN_TILE = 2, MN_GATHER = 3 };
 enum Sched : int { RAGGED_M = 0, RAGGED_K = 1 };
 enum Epi : int { EPI_STORE_F32 = 0, EPI_SWIGLU = 1, EPI_STORE = 2, EPI_DGRAD_SWIGLU = 3 };
 
@@ -50,6 +57,9 @@ struct GemmArgs {
   int single_rows;       // rows of the one group when offsets == nullptr
   int ksplit;            // RAGGED_K without offsets: group g = K rows [g*ksplit, (g+1)*ksplit)
   int padded;            // 1: groups start on 128-row boundaries of a padded row space
+  // gathered operand: row i of group g reads gsrc[gperm[off_g + min(i, n_g-1)] / gdiv]
+  const __nv_bfloat16* gsrc; long long gld; const int32_t* gperm; int gdiv; int gsrc_rows;
+  int32_t* poff_out;     // optional: CTA 0 publishes the group starts (padded offsets) here
   // EPI_STORE (bf16) / EPI_STORE_F32 (fp32; f32_tma: row stride allows TMA stores)
   __nv_bfloat16* d; float* d_f32; long long ldd; long long d_group_stride; int f32_tma;
   // EPI_SWIGLU (inter = intermediate size I)
@@ -60,8 +70,19 @@ struct GemmArgs {
   int* status;
 };
 
-template <int BN_, int STAGES_, int AL_, int BL_, int SCH_, int EPI_, bool B3D_, bool SWIGLU_B_>
+template <int BN_, int STAGES_, int AL_, int BL_, int SCH_, int EPI_, bool B3D_, bool SWIGLU_B_,
+          int EPI_WARPS_ = 4>
 struct GemmCfg {
+  static constexpr int EPI_WARPS = EPI_WARPS_;
+  static constexpr bool A_GATHER = (AL_ == KMAJ_GATHER || AL_ == MN_GATHER);
+  static constexpr bool B_GATHER = (BL_ == MN_GATHER);
+  static constexpr bool GATHER = A_GATHER || B_GATHER;
+  static constexpr int GATHER_WARPS = GATHER ? 4 : 0;
+  static constexpr int THREADS = 64 + 32 * (EPI_WARPS + GATHER_WARPS);
+  static constexpr int GATHER_LAG = STAGES_ - 2;  // stages a gather thread keeps in flight
+  static_assert(!GATHER || GATHER_LAG >= 1, "gathers need >= 3 stages");
+  static_assert(BL_ != KMAJ_GATHER, "B is gathered only MN-major");
+  static_assert(EPI_WARPS == 4 || EPI_WARPS == 8, "4 or 8 epilogue warps");
   static constexpr int BN = BN_;
   static constexpr int STAGES = STAGES_;
   static constexpr int AL = AL_;
@@ -76,12 +97,15 @@ struct GemmCfg {
   // K-major B is loaded in boxes of at most 128 rows.
   static constexpr int B_BOX_ROWS = BN < 128 ? BN : 128;
   static constexpr int B_NBOX = BN / B_BOX_ROWS;
-  static constexpr bool A_MN = (AL == MN_TILE);
-  static constexpr bool B_MN = (BL == MN_TILE);
+  static constexpr bool A_MN = (AL == MN_TILE || AL == MN_GATHER);
+  static constexpr bool B_MN = (BL == MN_TILE || BL == MN_GATHER);
+  static constexpr int TMA_BYTES = (A_GATHER ? 0 : A_BYTES) + (B_GATHER ? 0 : B_BYTES);
+  static constexpr uint32_t FULL_ARRIVALS = 1 + (GATHER ? 32 * GATHER_WARPS : 0);
+  static_assert(!SWIGLU_B || BN == 256, "the gate/up tile pairs 128 gate with 128 up columns");
   static constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, A_MN, B_MN);
   static constexpr bool TMA_OUT = true;
   static constexpr int SMEM_BYTES =
-      STAGES * STAGE_BYTES + (TMA_OUT ? kEpiSmemBytesDecl : 0) + 1024;  // + alignment slack
+      STAGES * STAGE_BYTES + (TMA_OUT ? EPI_WARPS * kEpiStagingPerWarp : 0) + 1024;  // + align
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N");
   static_assert(!B_MN || BN % 64 == 0, "MN-major B needs 64-wide groups");
   static_assert(2 * BN <= kTmemCols, "two accumulators must fit TMEM");
@@ -156,8 +180,7 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, const SmemTab
 // valid rows directly instead.
 constexpr int kStageBytes = 2048;            // 32 rows x 64 bytes
 constexpr int kStagesPerWarp = 3;
-constexpr int kEpiSmemBytes = 4 * kStagesPerWarp * kStageBytes;
-static_assert(kEpiSmemBytes == kEpiSmemBytesDecl, "epilogue staging size");
+static_assert(kStagesPerWarp * kStageBytes == kEpiStagingPerWarp, "epilogue staging size");
 
 struct WarpOut {
   uint32_t buf0;  // this warp's first staging buffer (1024-byte aligned)
@@ -253,7 +276,8 @@ __device__ __forceinline__ float silu_f(float g) { return g * sigmoid_f(g); }
 // M x N slice, map tmD0 3-D [groups][M][N] with 16x32 fp32 boxes.
 template <class C>
 __device__ void epilogue_store_f32(const GemmArgs& a, const TileInfo& ti, uint32_t tacc,
-                                   int row_in_tile, WarpOut& w, const CUtensorMap* tmD0) {
+                                   int row_in_tile, WarpOut& w, const CUtensorMap* tmD0, int cpart,
+                                   int nparts) {
   const int quad = row_in_tile >> 5;
   const bool valid = row_in_tile < ti.rows_valid;
   const bool warp_full = a.f32_tma && quad * 32 + 32 <= ti.rows_valid;
@@ -263,8 +287,9 @@ __device__ void epilogue_store_f32(const GemmArgs& a, const TileInfo& ti, uint32
   const long long row = (k3 ? ti.mb * BM : ti.row0) + row_in_tile;
   const int y = (k3 ? ti.mb * BM : ti.row0) + quad * 32;
   float v[32];
+  constexpr int NCH = (C::BN + 31) / 32;
 #pragma unroll 1
-  for (int c = 0; c < (C::BN + 31) / 32; ++c) {
+  for (int c = cpart * NCH / nparts; c < (cpart + 1) * NCH / nparts; ++c) {
     const int col = n0 + c * 32;
     if (col >= a.N) break;
     if (ti.kblocks > 0) tmem_ld32(tacc + c * 32, v);
@@ -288,7 +313,7 @@ __device__ void epilogue_store_f32(const GemmArgs& a, const TileInfo& ti, uint32
 template <class C>
 __device__ void epilogue_swiglu(const GemmArgs& a, const TileInfo& ti, uint32_t tacc,
                                 int row_in_tile, WarpOut& w, const CUtensorMap* tmD0,
-                                const CUtensorMap* tmD1) {
+                                const CUtensorMap* tmD1, int cpart, int nparts) {
   const int quad = row_in_tile >> 5;
   const bool valid = row_in_tile < ti.rows_valid;
   const bool warp_full = quad * 32 + 32 <= ti.rows_valid;
@@ -298,8 +323,9 @@ __device__ void epilogue_swiglu(const GemmArgs& a, const TileInfo& ti, uint32_t 
   constexpr int HALF = C::BN / 2;
   const int n0 = ti.nb * HALF;
   float g[32], u[32];
+  constexpr int NCH = HALF / 32;
 #pragma unroll 1
-  for (int c = 0; c < HALF / 32; ++c) {
+  for (int c = cpart * NCH / nparts; c < (cpart + 1) * NCH / nparts; ++c) {
     const int j = n0 + c * 32;
     if (j >= I) break;
     tmem_ld32(tacc + c * 32, g);
@@ -328,7 +354,8 @@ __device__ void epilogue_swiglu(const GemmArgs& a, const TileInfo& ti, uint32_t 
 // RAGGED_K: D is the group's full M x N matrix (map tmD0 3-D, group = depth).
 template <class C>
 __device__ void epilogue_store(const GemmArgs& a, const TileInfo& ti, uint32_t tacc,
-                               int row_in_tile, WarpOut& w, const CUtensorMap* tmD0) {
+                               int row_in_tile, WarpOut& w, const CUtensorMap* tmD0, int cpart,
+                               int nparts) {
   const int quad = row_in_tile >> 5;
   const bool valid = row_in_tile < ti.rows_valid;
   const bool warp_full = quad * 32 + 32 <= ti.rows_valid;
@@ -337,8 +364,9 @@ __device__ void epilogue_store(const GemmArgs& a, const TileInfo& ti, uint32_t t
   const long long row = (k3 ? ti.mb * BM : ti.row0) + row_in_tile;
   const int y = (k3 ? ti.mb * BM : ti.row0) + quad * 32;
   float v[32];
+  constexpr int NCH = C::BN / 32;
 #pragma unroll 1
-  for (int c = 0; c < C::BN / 32; ++c) {
+  for (int c = cpart * NCH / nparts; c < (cpart + 1) * NCH / nparts; ++c) {
     const int col = n0 + c * 32;
     if (col >= a.N) break;
     if (ti.kblocks == 0) {
@@ -365,13 +393,15 @@ __device__ void epilogue_store(const GemmArgs& a, const TileInfo& ti, uint32_t t
 template <class C>
 __device__ void epilogue_dgrad_swiglu(const GemmArgs& a, const SmemTables& T, const TileInfo& ti,
                                       uint32_t tacc, int row_in_tile, WarpOut& w,
-                                      const CUtensorMap* tmD0, const CUtensorMap* tmD1) {
+                                      const CUtensorMap* tmD0, const CUtensorMap* tmD1, int cpart,
+                                      int nparts) {
   const int quad = row_in_tile >> 5;
   const long long p = ti.row0 + row_in_tile;  // row in the (padded) row space
   const int y = ti.row0 + quad * 32;
   const int I = a.inter;
   const int n0 = ti.nb * C::BN;
   const int nNB = (I + C::BN - 1) / C::BN;
+  const int npart_cols = nNB * nparts;  // dw partials per row
   const bool valid = row_in_tile < ti.rows_valid;
   const bool pad_row = !valid && a.padded;
   const bool warp_full = a.padded || quad * 32 + 32 <= ti.rows_valid;
@@ -383,8 +413,9 @@ __device__ void epilogue_dgrad_swiglu(const GemmArgs& a, const SmemTables& T, co
   }
   float acc[32], g[32], u[32];
   float dwp = 0.f;
+  constexpr int NCH = C::BN / 32;
 #pragma unroll 1
-  for (int c = 0; c < C::BN / 32; ++c) {
+  for (int c = cpart * NCH / nparts; c < (cpart + 1) * NCH / nparts; ++c) {
     const int j = n0 + c * 32;
     if (j >= I) break;
     tmem_ld32(tacc + c * 32, acc);
@@ -418,12 +449,139 @@ __device__ void epilogue_dgrad_swiglu(const GemmArgs& a, const SmemTables& T, co
       store_row_chunk_bf16<C>(a.hw_out + p * (long long)I + j, acc);
     }
   }
-  if (a.dw_part && (valid || pad_row)) a.dw_part[p * nNB + ti.nb] = dwp;
+  if (a.dw_part && (valid || pad_row)) a.dw_part[p * npart_cols + ti.nb * nparts + cpart] = dwp;
+}
+
+// ---------------------------------------------------------------- gather warps
+// Source token row for row i of group g (rows past the group's tokens reuse its
+// last token: finite values, results masked or multiplied by zero).
+__device__ __forceinline__ int gather_row(const GemmArgs& a, const SmemTables& T, int g, int i) {
+  const int n = T.cnt[g];
+  const int r = T.off[g] + (i < n ? i : n - 1);
+  return clampi(__ldg(a.gperm + r) / a.gdiv, 0, a.gsrc_rows - 1);
+}
+
+// First tile at or after t0 (stride gridDim.x) that has k-blocks; total if none.
+template <class C>
+__device__ __forceinline__ int next_work_tile(const GemmArgs& a, const SmemTables& T, int t0,
+                                              int total, TileInfo& out) {
+  for (int t = t0; t < total; t += gridDim.x) {
+    out = decode_tile<C>(a, T, t);
+    if (out.kblocks > 0) return t;
+  }
+  return total;
+}
+
+// The gather warps walk the same (tile, k-block) sequence as the TMA producer.
+// Token ids are software-pipelined: the ids of the next stage (or of the next
+// tile) are loaded before the current stage's copies are issued, so their
+// latency overlaps the copies in flight.
+template <class C>
+__device__ void gather_role(const GemmArgs& a, const SmemTables& T, uint32_t smem_base,
+                           uint64_t* full_bar, uint64_t* empty_bar, volatile int* abort_flag,
+                           int gw, int lane, int total) {
+  constexpr int LAG = C::GATHER_LAG;
+  constexpr bool KM = (C::AL == KMAJ_GATHER);
+  int stage = 0;
+  uint32_t phase = 0;
+  uint32_t ring = 0;  // stages with copies issued but not yet signalled (4 bits each, FIFO)
+  int rn = 0;
+  TileInfo ti, tn;
+  int t = next_work_tile<C>(a, T, blockIdx.x, total, ti);
+  int src[8], src_n[8];  // K-major: this lane's rows gw*32 + 4*i + (lane >> 3)
+  int kid = 0;           // MN-major: k-row gw*16 + (lane & 15) of the current stage
+  if (t < total) {
+    if constexpr (KM) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        src[i] = gather_row(a, T, ti.g, ti.mb * BM + gw * 32 + 4 * i + (lane >> 3));
+    } else {
+      kid = gather_row(a, T, ti.g, gw * 16 + (lane & 15));
+    }
+  }
+  int kb = 0;
+  int t_next = total;
+  while (t < total && !*abort_flag) {
+    if (kb == 0) {
+      t_next = next_work_tile<C>(a, T, t + gridDim.x, total, tn);
+      if constexpr (KM) {
+        if (t_next < total) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            src_n[i] = gather_row(a, T, tn.g, tn.mb * BM + gw * 32 + 4 * i + (lane >> 3));
+        }
+      }
+    }
+    int kid_n = 0;
+    if constexpr (!KM) {
+      if (kb + 1 < ti.kblocks) kid_n = gather_row(a, T, ti.g, (kb + 1) * BK + gw * 16 + (lane & 15));
+      else if (t_next < total) kid_n = gather_row(a, T, tn.g, gw * 16 + (lane & 15));
+    }
+    if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1, abort_flag, a.status)) break;
+    const uint32_t sA = smem_base + stage * C::STAGE_BYTES;
+    const uint32_t sB = sA + C::A_BYTES;
+    if constexpr (KM) {
+      const int c = lane & 7;
+      const __nv_bfloat16* col = a.gsrc + kb * BK + c * 8;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int r = gw * 32 + 4 * i + (lane >> 3);
+        cp_async_16(sA + r * 128 + ((c ^ (r & 7)) << 4), col + (size_t)src[i] * a.gld);
+      }
+    } else {
+      // MN-major: operand extent X along M/N, X/8 16-byte chunks per k-row
+      constexpr int X = C::A_GATHER ? BM : C::BN;
+      constexpr int CPR = X / 8;
+      constexpr int RPI = 32 / CPR;  // k-rows per warp instruction
+      const uint32_t sOp = C::A_GATHER ? sA : sB;
+      const int mn0 = C::A_GATHER ? ti.mb * BM : (C::SWIGLU_B ? ti.nb * (C::BN / 2) : ti.nb * C::BN);
+      const int cc = lane % CPR;
+      const int j = cc >> 3, c = cc & 7;
+      const __nv_bfloat16* col = a.gsrc + mn0 + j * 64 + c * 8;
+#pragma unroll
+      for (int q = 0; q < 16 / RPI; ++q) {
+        const int rl = q * RPI + lane / CPR;  // 0..15 within this warp's k-rows
+        const int r = gw * 16 + rl;
+        const int srow = __shfl_sync(0xffffffffu, kid, rl);
+        cp_async_16(sOp + j * 8192 + r * 128 + ((c ^ (r & 7)) << 4), col + (size_t)srow * a.gld);
+      }
+    }
+    cp_async_commit();
+    ring |= (uint32_t)stage << (4 * rn);
+    ++rn;
+    if (rn > LAG) {
+      cp_async_wait<LAG>();
+      fence_proxy_async_smem();
+      mbar_arrive(smem_u32(&full_bar[ring & 15u]));
+      ring >>= 4;
+      --rn;
+    }
+    if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
+    // advance to the next (tile, k-block)
+    if (++kb == ti.kblocks) {
+      kb = 0;
+      t = t_next;
+      ti = tn;
+      if constexpr (KM) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) src[i] = src_n[i];
+      }
+    }
+    if constexpr (!KM) kid = kid_n;
+  }
+  // signal the stages still in flight
+  cp_async_wait<0>();
+  fence_proxy_async_smem();
+  while (rn > 0) {
+    mbar_arrive(smem_u32(&full_bar[ring & 15u]));
+    ring >>= 4;
+    --rn;
+  }
 }
 
 // ---------------------------------------------------------------- the kernel
 template <class C>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __launch_bounds__(C::THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmD0,
@@ -446,12 +604,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   // ---- set-up: barriers, TMEM, group tables
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(smem_u32(&full_bar[s]), 1);
+      mbar_init(smem_u32(&full_bar[s]), C::FULL_ARRIVALS);
       mbar_init(smem_u32(&empty_bar[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&tfull_bar[b]), 1);
-      mbar_init(smem_u32(&tempty_bar[b]), 128);
+      mbar_init(smem_u32(&tempty_bar[b]), 32 * C::EPI_WARPS);
     }
     mbar_init(smem_u32(&drain_bar), 1);
     T.abort_flag = 0;
@@ -513,6 +671,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       T.tile_prefix[a.G] = run_tiles;
       T.total_tiles = run_tiles;
     }
+    if (a.poff_out && blockIdx.x == 0) {
+      __syncwarp();
+      for (int g = lane; g < a.G; g += 32) a.poff_out[g] = T.start[g];
+      if (lane == 0) a.poff_out[a.G] = run_rows;
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -535,7 +698,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const uint32_t fb = smem_u32(&full_bar[stage]);
         const uint32_t sA = smem_base + stage * C::STAGE_BYTES;
         const uint32_t sB = sA + C::A_BYTES;
-        if (lane == 0) mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+        if (lane == 0) mbar_arrive_expect_tx(fb, C::TMA_BYTES);
         filled |= 1u << stage;
         fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
         __syncwarp();
@@ -543,7 +706,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int kr = ti.kstart + kc;        // absolute K coordinate (RAGGED_K)
         const int kx = C::SCH == RAGGED_K ? kr : kc;
         // ---- A
-        if constexpr (C::AL == KMAJ_TILE) {
+        if constexpr (C::A_GATHER) {
+          // A comes from the gather warps
+        } else if constexpr (C::AL == KMAJ_TILE) {
           if (lane == 0) tma_load_2d(sA, &tmA, fb, kx, C::SCH == RAGGED_K ? m0 : ti.row0);
         } else {  // MN_TILE: two 64-wide groups along M, 64 k-rows each
           if (lane == 0) {
@@ -634,12 +799,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       __syncwarp();
     }
+  } else if (C::GATHER && warp >= 2 + C::EPI_WARPS) {
+    // ================= gather warps (LSU cp.async) =================
+    gather_role<C>(a, T, smem_base, full_bar, empty_bar, abort_flag, warp - 2 - C::EPI_WARPS,
+                   lane, total);
   } else {
     // ================= epilogue =================
     const int quad = warp & 3;
+    const int epi = warp - 2;                  // 0 .. EPI_WARPS-1
+    const int cpart = epi >> 2;                // column part of this warp
+    constexpr int nparts = C::EPI_WARPS / 4;
     const int row_in_tile = quad * 32 + lane;
     WarpOut wo;
-    wo.buf0 = smem_base + C::STAGES * C::STAGE_BYTES + quad * (kStagesPerWarp * kStageBytes);
+    wo.buf0 = smem_base + C::STAGES * C::STAGE_BYTES + epi * (kStagesPerWarp * kStageBytes);
     wo.lane = lane;
     wo.next = 0;
     wo.inflight = 0;
@@ -650,10 +822,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (!mbar_wait(smem_u32(&tfull_bar[acc]), acc_phase, abort_flag, a.status)) break;
       tc_fence_after();
       const uint32_t tacc = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * C::BN;
-      if constexpr (C::EPI == EPI_STORE_F32) epilogue_store_f32<C>(a, ti, tacc, row_in_tile, wo, &tmD0);
-      else if constexpr (C::EPI == EPI_SWIGLU) epilogue_swiglu<C>(a, ti, tacc, row_in_tile, wo, &tmD0, &tmD1);
-      else if constexpr (C::EPI == EPI_STORE) epilogue_store<C>(a, ti, tacc, row_in_tile, wo, &tmD0);
-      else epilogue_dgrad_swiglu<C>(a, T, ti, tacc, row_in_tile, wo, &tmD0, &tmD1);
+      if constexpr (C::EPI == EPI_STORE_F32)
+        epilogue_store_f32<C>(a, ti, tacc, row_in_tile, wo, &tmD0, cpart, nparts);
+      else if constexpr (C::EPI == EPI_SWIGLU)
+        epilogue_swiglu<C>(a, ti, tacc, row_in_tile, wo, &tmD0, &tmD1, cpart, nparts);
+      else if constexpr (C::EPI == EPI_STORE)
+        epilogue_store<C>(a, ti, tacc, row_in_tile, wo, &tmD0, cpart, nparts);
+      else
+        epilogue_dgrad_swiglu<C>(a, T, ti, tacc, row_in_tile, wo, &tmD0, &tmD1, cpart, nparts);
       tc_fence_before();
       mbar_arrive(smem_u32(&tempty_bar[acc]));
       if (++acc == 2) { acc = 0; acc_phase ^= 1; }

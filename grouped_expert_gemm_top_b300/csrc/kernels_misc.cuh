@@ -1,7 +1,7 @@
 // Memory-bound kernels of the MoE layer: the router's softmax/top-k, the
-// expert sort (permutation and expert offsets), the sorted token copies, the
-// weighted un-permute/combine, and the small backward kernels (padded row
-// tables, router gradient, token gather-sums).
+// expert sort (permutation and expert offsets), the weighted
+// un-permute/combine, and the backward's router gradient and token
+// gather-sums.
 //
 // All of them are written so that every output is a fixed-order function of
 // the inputs: no floating-point atomics, so results are bit-identical run to
@@ -112,20 +112,6 @@ __global__ void router_topk_kernel(const float* __restrict__ partial, int splits
     topk_idx[(size_t)t * k + lane] = my_e;
     topk_w[(size_t)t * k + lane] = my_p / psum;
   }
-}
-
-// ---------------------------------------------------------------- sorted token copies
-// x_sorted[r, :] = x[perm_slot[r] / k, :] for the S sorted rows (one warp per row).
-__global__ void gather_rows_kernel(const __nv_bfloat16* __restrict__ x,
-                                   const int32_t* __restrict__ perm_slot, int k, int S, int H,
-                                   int T, __nv_bfloat16* __restrict__ x_sorted) {
-  const long long r = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (r >= S) return;
-  const int t = clampi(__ldg(perm_slot + r) / k, 0, T - 1);
-  const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
-  uint4* dst = reinterpret_cast<uint4*>(x_sorted + (size_t)r * H);
-  for (int c = lane; c < H / 8; c += 32) dst[c] = __ldg(src + c);
 }
 
 // ---------------------------------------------------------------- expert sort
@@ -307,43 +293,22 @@ __global__ void combine_kernel(const __nv_bfloat16* __restrict__ y_perm,
 // zero in every sorted copy, so weight-gradient GEMMs can run whole 64-row
 // k-blocks.
 
-// Exclusive scan of the padded group sizes into sp[0..E] (one warp).
-__device__ __forceinline__ void padded_scan_warp(const int* so, int E, int* sp, int lane) {
-  int run = 0;
-  for (int b0 = 0; b0 < E; b0 += 32) {
-    const int e = b0 + lane;
-    const int n = e < E ? so[e + 1] - so[e] : 0;
-    const int v = ((n + kPadRows - 1) / kPadRows) * kPadRows;
-    int inc = v;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const int x = __shfl_up_sync(0xffffffffu, inc, d);
-      if (lane >= d) inc += x;
-    }
-    if (e < E) sp[e] = run + inc - v;
-    run += __shfl_sync(0xffffffffu, inc, 31);
-  }
-  if (lane == 0) sp[E] = run;
-}
-
-// Padded offsets, and the padded sorted copies of grad_out and x
-// (a_sorted[p] = a[token of row p], zero rows for padding).  One warp per row,
-// grid-stride; block 0 also writes poff[0..E].
-__global__ void bwd_sorted_copies_kernel(const int32_t* __restrict__ expert_offsets,
-                                         const int32_t* __restrict__ perm_slot, int E, int k,
-                                         int H, int T, const __nv_bfloat16* __restrict__ a,
-                                         __nv_bfloat16* __restrict__ a_sorted,
-                                         const __nv_bfloat16* __restrict__ b,
-                                         __nv_bfloat16* __restrict__ b_sorted,
-                                         int32_t* __restrict__ poff) {
-  __shared__ int so[257];
+// Padded sorted copy of the tokens for the gate/up weight gradient: row p of
+// expert e's padded block [poff[e], poff[e+1]) holds x[token of sorted row
+// offsets[e] + (p - poff[e])], or zeros past the expert's tokens.  One warp
+// per row, grid-stride; rows at or past poff[E] are not touched.
+__global__ void sorted_rows_padded_kernel(const int32_t* __restrict__ poff,
+                                          const int32_t* __restrict__ expert_offsets,
+                                          const int32_t* __restrict__ perm_slot, int E, int k,
+                                          int H, int T, const __nv_bfloat16* __restrict__ x,
+                                          __nv_bfloat16* __restrict__ x_sorted) {
   __shared__ int sp[257];
-  for (int e = threadIdx.x; e <= E; e += blockDim.x) so[e] = __ldg(expert_offsets + e);
+  __shared__ int so[257];
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) {
+    sp[e] = __ldg(poff + e);
+    so[e] = __ldg(expert_offsets + e);
+  }
   __syncthreads();
-  if (threadIdx.x < 32) padded_scan_warp(so, E, sp, threadIdx.x);
-  __syncthreads();
-  if (blockIdx.x == 0)
-    for (int e = threadIdx.x; e <= E; e += blockDim.x) poff[e] = sp[e];
   const int lane = threadIdx.x & 31;
   const long long nwarps = (long long)gridDim.x * (blockDim.x >> 5);
   for (long long p = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); p < sp[E];
@@ -354,24 +319,13 @@ __global__ void bwd_sorted_copies_kernel(const int32_t* __restrict__ expert_offs
       if (sp[mid] <= p) lo = mid; else hi = mid - 1;
     }
     const int i = (int)(p - sp[lo]);
-    int tok = -1;
-    if (i < so[lo + 1] - so[lo]) tok = clampi(__ldg(perm_slot + so[lo] + i) / k, 0, T - 1);
-    uint4* da = reinterpret_cast<uint4*>(a_sorted + (size_t)p * H);
-    uint4* db = reinterpret_cast<uint4*>(b_sorted + (size_t)p * H);
-    if (tok < 0) {
-      for (int c = lane; c < H / 8; c += 32) {
-        da[c] = make_uint4(0, 0, 0, 0);
-        db[c] = make_uint4(0, 0, 0, 0);
-      }
+    uint4* dst = reinterpret_cast<uint4*>(x_sorted + (size_t)p * H);
+    if (i < so[lo + 1] - so[lo]) {
+      const int tok = clampi(__ldg(perm_slot + so[lo] + i) / k, 0, T - 1);
+      const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)tok * H);
+      for (int c = lane; c < H / 8; c += 32) dst[c] = __ldg(src + c);
     } else {
-      const uint4* sa = reinterpret_cast<const uint4*>(a + (size_t)tok * H);
-      const uint4* sb = reinterpret_cast<const uint4*>(b + (size_t)tok * H);
-      for (int c = lane; c < H / 8; c += 32) {
-        const uint4 va = __ldg(sa + c);
-        const uint4 vb = __ldg(sb + c);
-        da[c] = va;
-        db[c] = vb;
-      }
+      for (int c = lane; c < H / 8; c += 32) dst[c] = make_uint4(0, 0, 0, 0);
     }
   }
 }

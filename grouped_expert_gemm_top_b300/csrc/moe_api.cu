@@ -21,7 +21,7 @@ namespace {
 using moe::GemmArgs;
 using moe::GemmCfg;
 
-constexpr int32_t kAbiVersion = 2;
+constexpr int32_t kAbiVersion = 3;
 constexpr size_t kAlign = 256;
 
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
@@ -42,14 +42,16 @@ moe_status check_dims(const moe_dims* d) {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 constexpr int kMaxRouterSplits = 8;
+constexpr int kDwParts = 1;  // column parts of the down data-gradient epilogue (epilogue warps / 4)
 
 struct Layout {
-  size_t status, counts, logits_part, x_sorted, h, h_sh, fwd_end;
-  size_t poff, dout_sorted, x_sorted_pad, dgu, hw, dxs, dwp, dl, dgu_sh, hw_sh, dxs_sh,
+  size_t status, counts, logits_part, h, h_sh, fwd_end;
+  size_t poff, x_sorted_pad, dgu, hw, dxs, dwp, dl, dgu_sh, hw_sh, dxs_sh,
       total;
   int sort_blocks;
   long long S, S_pad_max;
   int nNB_I;  // 256-wide column blocks of the intermediate (dgrad-down tiles)
+  int nDW;    // dw partials per padded row (column blocks x epilogue column parts)
 };
 
 Layout make_layout(const moe_dims& d, bool bwd) {
@@ -59,23 +61,22 @@ Layout make_layout(const moe_dims& d, bool bwd) {
   L.S_pad_max = (L.S_pad_max + moe::kPadRows - 1) / moe::kPadRows * moe::kPadRows;
   L.sort_blocks = (int)((L.S + moe::kSortChunk - 1) / moe::kSortChunk);
   L.nNB_I = (d.I + 255) / 256;
+  L.nDW = L.nNB_I * kDwParts;
   size_t o = 0;
   L.status = o; o += kAlign;
   L.counts = o; o = align_up(o + (size_t)L.sort_blocks * d.E * 4);
   L.logits_part = o; o = align_up(o + (size_t)kMaxRouterSplits * d.T * d.E * 4);
-  L.x_sorted = o; o = align_up(o + (size_t)L.S * d.H * 2);
   L.h = o; o = align_up(o + (size_t)L.S * d.I * 2);
   L.h_sh = o; o = align_up(o + (size_t)d.T * d.I_shared * 2);
   L.fwd_end = o;
   if (bwd) {
     const size_t P = (size_t)L.S_pad_max;
     L.poff = o; o = align_up(o + (size_t)(d.E + 1) * 4);
-    L.dout_sorted = o; o = align_up(o + P * d.H * 2);
     L.x_sorted_pad = o; o = align_up(o + P * d.H * 2);
     L.dgu = o; o = align_up(o + P * 2 * d.I * 2);
     L.hw = o; o = align_up(o + P * d.I * 2);
     L.dxs = o; o = align_up(o + P * d.H * 2);
-    L.dwp = o; o = align_up(o + P * L.nNB_I * 4);
+    L.dwp = o; o = align_up(o + P * L.nDW * 4);
     L.dl = o; o = align_up(o + (size_t)L.S * 4);
     L.dgu_sh = o; o = align_up(o + (size_t)d.T * 2 * d.I_shared * 2);
     L.hw_sh = o; o = align_up(o + (size_t)d.T * d.I_shared * 2);
@@ -221,7 +222,9 @@ using moe::EPI_DGRAD_SWIGLU;
 using moe::EPI_STORE_F32;
 using moe::EPI_STORE;
 using moe::EPI_SWIGLU;
+using moe::KMAJ_GATHER;
 using moe::KMAJ_TILE;
+using moe::MN_GATHER;
 using moe::MN_TILE;
 using moe::RAGGED_K;
 using moe::RAGGED_M;
@@ -229,16 +232,19 @@ using moe::RAGGED_M;
 template <int BN>
 using CfgRouter =
     GemmCfg<BN, (BN >= 256 ? 4 : 6), KMAJ_TILE, KMAJ_TILE, RAGGED_K, EPI_STORE_F32, false, false>;
-using CfgGateUp = GemmCfg<256, 4, KMAJ_TILE, KMAJ_TILE, RAGGED_M, EPI_SWIGLU, true, true>;
+using CfgGateUp = GemmCfg<256, 4, KMAJ_GATHER, KMAJ_TILE, RAGGED_M, EPI_SWIGLU, true, true>;
 using CfgGateUpShared = GemmCfg<256, 4, KMAJ_TILE, KMAJ_TILE, RAGGED_M, EPI_SWIGLU, false, true>;
 using CfgDown = GemmCfg<256, 4, KMAJ_TILE, KMAJ_TILE, RAGGED_M, EPI_STORE, true, false>;
 using CfgDownShared = GemmCfg<256, 4, KMAJ_TILE, KMAJ_TILE, RAGGED_M, EPI_STORE, false, false>;
-using CfgDgradDown = GemmCfg<256, 4, KMAJ_TILE, MN_TILE, RAGGED_M, EPI_DGRAD_SWIGLU, true, false>;
+using CfgDgradDown =
+    GemmCfg<256, 4, KMAJ_GATHER, MN_TILE, RAGGED_M, EPI_DGRAD_SWIGLU, true, false, 4 * kDwParts>;
 using CfgDgradDownShared =
     GemmCfg<256, 4, KMAJ_TILE, MN_TILE, RAGGED_M, EPI_DGRAD_SWIGLU, false, false>;
 using CfgDgradGateUp = GemmCfg<256, 4, KMAJ_TILE, MN_TILE, RAGGED_M, EPI_STORE, true, false>;
 using CfgDgradGateUpShared = GemmCfg<256, 4, KMAJ_TILE, MN_TILE, RAGGED_M, EPI_STORE, false, false>;
 using CfgWgrad = GemmCfg<256, 4, MN_TILE, MN_TILE, RAGGED_K, EPI_STORE, false, false>;
+using CfgWgradDown = GemmCfg<256, 4, MN_GATHER, MN_TILE, RAGGED_K, EPI_STORE, false, false>;
+
 
 // fp32 [depth][rows][inner] output map with 16x32 boxes (64-byte rows).
 bool make_out_map3_f32(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows,
@@ -281,7 +287,7 @@ moe_status launch_gemm(int kid, const CUtensorMap& A, const CUtensorMap& B, cons
   if (tile_bound < grid) grid = tile_bound;
   if (grid < 1) return MOE_OK;
   KernelScope ks(kid, st);
-  moe::grouped_gemm_kernel<C><<<(int)grid, moe::kGemmThreads, C::SMEM_BYTES, st>>>(A, B, D0, D1, a);
+  moe::grouped_gemm_kernel<C><<<(int)grid, C::THREADS, C::SMEM_BYTES, st>>>(A, B, D0, D1, a);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -338,7 +344,7 @@ moe_status moe_route(const moe_dims* d, int32_t gate_mode, const moe_bf16* x,
   if (!aligned16(x) || !aligned16(w_router) || !aligned16(workspace)) return MOE_ERR_INVALID_ARG;
   if (workspace_bytes < kAlign) return MOE_ERR_WORKSPACE_TOO_SMALL;
   const Layout L = make_layout(*d, false);
-  if (workspace_bytes < L.x_sorted) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  if (workspace_bytes < L.h) return MOE_ERR_WORKSPACE_TOO_SMALL;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int T = d->T, H = d->H, E = d->E;
   // split K so that the router GEMM fills the SMs; partial logits are summed in
@@ -422,23 +428,18 @@ moe_status moe_grouped_mlp_fwd(const moe_dims* d, const moe_bf16* x,
   __nv_bfloat16* h = at<__nv_bfloat16>(workspace, L.h);
   const int T = d->T, H = d->H, E = d->E, I = d->I;
   const long long S = L.S;
-  __nv_bfloat16* xs = at<__nv_bfloat16>(workspace, L.x_sorted);
-  {  // sorted copy of the tokens (one row per slot, expert-major)
-    KernelScope ks(MOE_K_GATHER_ROWS, st);
-    moe::gather_rows_kernel<<<(unsigned)cdiv(S * 32, 256), 256, 0, st>>>(
-        reinterpret_cast<const __nv_bfloat16*>(x), perm_slot, d->k, (int)S, H, T, xs);
-    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
-  }
-  {  // gate/up grouped GEMM + SwiGLU
-    CUtensorMap tA, tB;
-    if (!make_map(&tA, xs, H, S, 1, 64, 128)) return MOE_ERR_CUDA;
+  {  // gate/up grouped GEMM + SwiGLU; A = token rows of x gathered through the sort
+    CUtensorMap tB;
     if (!make_map3(&tB, w_gate_up, H, 2LL * I, E, 64, 128)) return MOE_ERR_CUDA;
+    const CUtensorMap& tA = tB;  // unused: A is gathered
     CUtensorMap tD0, tD1;
     if (!make_out_map(&tD1, h, I, S)) return MOE_ERR_CUDA;
     if (gu_saved) { if (!make_out_map(&tD0, gu_saved, 2LL * I, S)) return MOE_ERR_CUDA; }
     else tD0 = tD1;
     GemmArgs a = base_args(status);
     a.N = 2 * I; a.K = H; a.G = E; a.offsets = expert_offsets;
+    a.gsrc = reinterpret_cast<const __nv_bfloat16*>(x); a.gld = H; a.gperm = perm_slot;
+    a.gdiv = d->k; a.gsrc_rows = T;
     a.gu_out = reinterpret_cast<__nv_bfloat16*>(gu_saved); a.h_out = h; a.inter = I;
     s = launch_gemm<CfgGateUp>(MOE_K_GATE_UP, tA, tB, tD0, tD1, a, (cdiv(S, moe::BM) + E) * cdiv(I, 128), st);
     if (s != MOE_OK) return s;
@@ -552,22 +553,16 @@ moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_
   float* dwp = at<float>(workspace, L.dwp);
   float* dl = at<float>(workspace, L.dl);
 
-  __nv_bfloat16* dos = at<__nv_bfloat16>(workspace, L.dout_sorted);
-  __nv_bfloat16* xsp = at<__nv_bfloat16>(workspace, L.x_sorted_pad);
-  {  // padded offsets + padded sorted copies of grad_out and x
-    KernelScope ks(MOE_K_GATHER_ROWS_BWD, st);
-    moe::bwd_sorted_copies_kernel<<<(unsigned)std::max(1, 8 * sm_count()), 256, 0, st>>>(
-        expert_offsets, perm_slot, E, k, H, T, reinterpret_cast<const __nv_bfloat16*>(grad_out),
-        dos, reinterpret_cast<const __nv_bfloat16*>(x), xsp, poff);
-  }
-  if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
-
-  {  // down-projection data gradient + SwiGLU backward (+ dw partials)
-    CUtensorMap tA, tB;
-    if (!make_map(&tA, dos, H, P, 1, 64, 128)) return MOE_ERR_CUDA;
+  const auto* gob = reinterpret_cast<const __nv_bfloat16*>(grad_out);
+  const auto* xb = reinterpret_cast<const __nv_bfloat16*>(x);
+  {  // down-projection data gradient + SwiGLU backward (+ dw partials); A = grad_out rows
+    CUtensorMap tB;
     if (!make_map3(&tB, w_down, I, H, E, 64, 64)) return MOE_ERR_CUDA;
+    const CUtensorMap& tA = tB;  // unused: A is gathered
     GemmArgs a = base_args(status);
     a.N = I; a.K = H; a.G = E; a.offsets = expert_offsets; a.padded = 1;
+    a.gsrc = gob; a.gld = H; a.gperm = perm_slot; a.gdiv = k; a.gsrc_rows = T;
+    a.poff_out = poff;
     a.inter = I; a.gu_saved = reinterpret_cast<const __nv_bfloat16*>(gu_saved);
     a.perm_slot = perm_slot; a.slot_w = topk_w; a.dgu_out = dgu; a.hw_out = hw; a.dw_part = dwp;
     CUtensorMap tD0, tD1;
@@ -627,11 +622,11 @@ moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_
     auto* gx = reinterpret_cast<__nv_bfloat16*>(grad_x);
     if (k <= 8)
       moe::dx_gather_kernel<8><<<blocks, 256, 0, st>>>(dxs, topk_idx, topk_w, slot_perm,
-                                                       expert_offsets, poff, dwp, L.nNB_I, wr,
+                                                       expert_offsets, poff, dwp, L.nDW, wr,
                                                        dxs_sh, dl, gx, T, H, k, E, (int)P);
     else
       moe::dx_gather_kernel<32><<<blocks, 256, 0, st>>>(dxs, topk_idx, topk_w, slot_perm,
-                                                        expert_offsets, poff, dwp, L.nNB_I, wr,
+                                                        expert_offsets, poff, dwp, L.nDW, wr,
                                                         dxs_sh, dl, gx, T, H, k, E, (int)P);
   }
   { KernelScope ks(MOE_K_ROUTER_WGRAD, st);
@@ -641,16 +636,24 @@ moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_
   if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
   {  // dW_down[e] = sum over the expert's rows of dout[token]^T (w h)
     CUtensorMap tA, tB;
-    if (!make_map(&tA, dos, H, P, 1, 64, 64)) return MOE_ERR_CUDA;
     if (!make_map(&tB, hw, I, P, 1, 64, 64)) return MOE_ERR_CUDA;
+    tA = tB;  // unused: A = grad_out rows, gathered
     GemmArgs a = base_args(status);
     a.M = H; a.N = I; a.G = E; a.offsets = expert_offsets; a.padded = 1;
+    a.gsrc = gob; a.gld = H; a.gperm = perm_slot; a.gdiv = k; a.gsrc_rows = T;
     a.d = reinterpret_cast<__nv_bfloat16*>(grad_w_down); a.ldd = I;
     a.d_group_stride = (long long)H * I;
     CUtensorMap tD;
     if (!make_out_map3(&tD, grad_w_down, I, H, E)) return MOE_ERR_CUDA;
-    s = launch_gemm<CfgWgrad>(MOE_K_WGRAD_DOWN, tA, tB, tD, tD, a, (long long)E * cdiv(H, moe::BM) * cdiv(I, 256), st);
+    s = launch_gemm<CfgWgradDown>(MOE_K_WGRAD_DOWN, tA, tB, tD, tD, a, (long long)E * cdiv(H, moe::BM) * cdiv(I, 256), st);
     if (s != MOE_OK) return s;
+  }
+  __nv_bfloat16* xsp = at<__nv_bfloat16>(workspace, L.x_sorted_pad);
+  {  // padded sorted copy of x (B operand of the gate/up weight gradient)
+    KernelScope ks(MOE_K_SORTED_X_BWD, st);
+    moe::sorted_rows_padded_kernel<<<(unsigned)std::max(1, 8 * sm_count()), 256, 0, st>>>(
+        poff, expert_offsets, perm_slot, E, k, H, T, xb, xsp);
+    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
   }
   {  // dW_gu[e] = sum over the expert's rows of [dg|du]^T x[token]
     CUtensorMap tA, tB;
@@ -702,11 +705,11 @@ int32_t moe_kernel_count(void) { return MOE_K_COUNT; }
 
 const char* moe_kernel_name(int32_t id) {
   static const char* names[MOE_K_COUNT] = {
-      "router", "router_topk", "sort_histogram", "sort_scatter", "gather_rows", "gate_up",
-      "down", "shared_gate_up", "shared_down", "combine", "gather_rows_bwd", "dgrad_down",
+      "router", "router_topk", "sort_histogram", "sort_scatter", "gate_up",
+      "down", "shared_gate_up", "shared_down", "combine", "dgrad_down",
       "dgrad_gate_up", "shared_dgrad_down", "shared_dgrad_gate_up", "dx_gather",
       "router_wgrad", "wgrad_down", "wgrad_gate_up", "shared_wgrad_down",
-      "shared_wgrad_gate_up"};
+      "shared_wgrad_gate_up", "sorted_x_bwd"};
   return (id >= 0 && id < MOE_K_COUNT) ? names[id] : "unknown";
 }
 

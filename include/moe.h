@@ -202,14 +202,12 @@ typedef enum {
   MOE_K_ROUTER_TOPK,         /* moe_route: softmax + top-k (one warp per token) */
   MOE_K_SORT_HISTOGRAM,      /* moe_permute, pass 1: per-block expert histograms */
   MOE_K_SORT_SCATTER,        /* moe_permute, pass 2: scan + stable scatter */
-  MOE_K_GATHER_ROWS,         /* forward: expert-sorted copy of the tokens */
-  MOE_K_GATE_UP,             /* grouped gate/up GEMM + SwiGLU */
+  MOE_K_GATE_UP,             /* grouped gate/up GEMM + SwiGLU (token rows gathered in-kernel) */
   MOE_K_DOWN,                /* grouped down GEMM */
   MOE_K_SHARED_GATE_UP,      /* shared expert gate/up GEMM + SwiGLU */
   MOE_K_SHARED_DOWN,         /* shared expert down GEMM */
   MOE_K_COMBINE,             /* weighted un-permute / combine */
-  MOE_K_GATHER_ROWS_BWD,     /* backward: padded offsets + padded sorted grad_out and x */
-  MOE_K_DGRAD_DOWN,          /* backward: down data-gradient + SwiGLU backward */
+  MOE_K_DGRAD_DOWN,          /* backward: down data-gradient + SwiGLU backward (+ padded offsets) */
   MOE_K_DGRAD_GATE_UP,       /* backward: gate/up data-gradient (per slot) */
   MOE_K_SHARED_DGRAD_DOWN,
   MOE_K_SHARED_DGRAD_GATE_UP,
@@ -219,6 +217,7 @@ typedef enum {
   MOE_K_WGRAD_GATE_UP,       /* backward: grouped gate/up weight-gradient GEMM */
   MOE_K_SHARED_WGRAD_DOWN,
   MOE_K_SHARED_WGRAD_GATE_UP,
+  MOE_K_SORTED_X_BWD,        /* backward: padded sorted copy of x for the gate/up weight gradient */
   MOE_K_COUNT
 } moe_kernel_id;
 

@@ -71,8 +71,12 @@ struct GemmArgs {
 };
 
 template <int BN_, int STAGES_, int AL_, int BL_, int SCH_, int EPI_, bool B3D_, bool SWIGLU_B_,
-          int EPI_WARPS_ = 4>
+          int EPI_WARPS_ = 4, bool MC_ = false>
 struct GemmCfg {
+  // MC: 2-CTA clusters; the two CTAs take adjacent M-tiles of the same
+  // (group, n-block) and each TMA-multicasts half of the shared B tile.
+  static constexpr bool MC = MC_;
+  static constexpr int CL = MC ? 2 : 1;
   static constexpr int EPI_WARPS = EPI_WARPS_;
   static constexpr bool A_GATHER = (AL_ == KMAJ_GATHER || AL_ == MN_GATHER);
   static constexpr bool B_GATHER = (BL_ == MN_GATHER);
@@ -114,6 +118,7 @@ struct GemmCfg {
 
 struct TileInfo {
   int g, mb, nb;
+  bool phantom;    // MC pair slot past the group's last M-tile: loads only, no output
   int row0;        // RAGGED_M: first row of the M-tile in the A/D row space
   int rows_valid;  // RAGGED_M: rows of the group inside this tile (<= 128)
   int kstart;      // RAGGED_K: first K row of the group
@@ -136,8 +141,12 @@ __device__ __forceinline__ int num_nblocks(const GemmArgs& a) {
   return (a.N + C::BN - 1) / C::BN;
 }
 
+// Work unit t -> tile.  Without MC a unit is one tile (m-block fastest).  With
+// MC a unit is a pair of adjacent m-blocks of one (group, n-block); CTA rank r
+// of the cluster takes m-block 2p + r.
 template <class C>
-__device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, const SmemTables& T, int t) {
+__device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, const SmemTables& T, int t,
+                                                int rank = 0) {
   TileInfo ti;
   const int nNB = num_nblocks<C>(a);
   if constexpr (C::SCH == RAGGED_M) {
@@ -149,21 +158,25 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, const SmemTab
     ti.g = lo;
     const int local = t - T.tile_prefix[lo];
     const int mt = (T.cnt[lo] + BM - 1) / BM;
-    ti.nb = local / mt;
-    ti.mb = local - ti.nb * mt;
+    const int mu = (mt + C::CL - 1) / C::CL;  // units along M
+    ti.nb = local / mu;
+    ti.mb = (local - ti.nb * mu) * C::CL + rank;
+    ti.phantom = ti.mb >= mt;
     ti.row0 = T.start[lo] + ti.mb * BM;
-    ti.rows_valid = min(BM, T.cnt[lo] - ti.mb * BM);
+    ti.rows_valid = ti.phantom ? 0 : min(BM, T.cnt[lo] - ti.mb * BM);
     ti.kstart = 0;
     ti.kblocks = a.K / BK;
   } else {
     const int nMB = (a.M + BM - 1) / BM;
-    const int per = nMB * nNB;
+    const int mu = (nMB + C::CL - 1) / C::CL;
+    const int per = mu * nNB;
     ti.g = min(t / per, a.G - 1);
     const int local = t - ti.g * per;
-    ti.nb = local / nMB;
-    ti.mb = local - ti.nb * nMB;
+    ti.nb = local / mu;
+    ti.mb = (local - ti.nb * mu) * C::CL + rank;
+    ti.phantom = ti.mb >= nMB;
     ti.row0 = ti.mb * BM;
-    ti.rows_valid = min(BM, a.M - ti.mb * BM);
+    ti.rows_valid = ti.phantom ? 0 : min(BM, a.M - ti.mb * BM);
     ti.kstart = T.start[ti.g];
     ti.kblocks = (T.cnt[ti.g] + BK - 1) / BK;
   }
@@ -464,9 +477,9 @@ __device__ __forceinline__ int gather_row(const GemmArgs& a, const SmemTables& T
 // First tile at or after t0 (stride gridDim.x) that has k-blocks; total if none.
 template <class C>
 __device__ __forceinline__ int next_work_tile(const GemmArgs& a, const SmemTables& T, int t0,
-                                              int total, TileInfo& out) {
-  for (int t = t0; t < total; t += gridDim.x) {
-    out = decode_tile<C>(a, T, t);
+                                              int total, int rank, int ustep, TileInfo& out) {
+  for (int t = t0; t < total; t += ustep) {
+    out = decode_tile<C>(a, T, t, rank);
     if (out.kblocks > 0) return t;
   }
   return total;
@@ -479,7 +492,7 @@ __device__ __forceinline__ int next_work_tile(const GemmArgs& a, const SmemTable
 template <class C>
 __device__ void gather_role(const GemmArgs& a, const SmemTables& T, uint32_t smem_base,
                            uint64_t* full_bar, uint64_t* empty_bar, volatile int* abort_flag,
-                           int gw, int lane, int total) {
+                           int gw, int lane, int total, int rank, int unit0, int ustep) {
   constexpr int LAG = C::GATHER_LAG;
   constexpr bool KM = (C::AL == KMAJ_GATHER);
   int stage = 0;
@@ -487,7 +500,7 @@ __device__ void gather_role(const GemmArgs& a, const SmemTables& T, uint32_t sme
   uint32_t ring = 0;  // stages with copies issued but not yet signalled (4 bits each, FIFO)
   int rn = 0;
   TileInfo ti, tn;
-  int t = next_work_tile<C>(a, T, blockIdx.x, total, ti);
+  int t = next_work_tile<C>(a, T, unit0, total, rank, ustep, ti);
   int src[8], src_n[8];  // K-major: this lane's rows gw*32 + 4*i + (lane >> 3)
   int kid = 0;           // MN-major: k-row gw*16 + (lane & 15) of the current stage
   if (t < total) {
@@ -503,7 +516,7 @@ __device__ void gather_role(const GemmArgs& a, const SmemTables& T, uint32_t sme
   int t_next = total;
   while (t < total && !*abort_flag) {
     if (kb == 0) {
-      t_next = next_work_tile<C>(a, T, t + gridDim.x, total, tn);
+      t_next = next_work_tile<C>(a, T, t + ustep, total, rank, ustep, tn);
       if constexpr (KM) {
         if (t_next < total) {
 #pragma unroll
@@ -520,7 +533,9 @@ __device__ void gather_role(const GemmArgs& a, const SmemTables& T, uint32_t sme
     if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1, abort_flag, a.status)) break;
     const uint32_t sA = smem_base + stage * C::STAGE_BYTES;
     const uint32_t sB = sA + C::A_BYTES;
-    if constexpr (KM) {
+    if (ti.phantom) {
+      // pair slot past the group's last tile: the stage is not read into any output
+    } else if constexpr (KM) {
       const int c = lane & 7;
       const __nv_bfloat16* col = a.gsrc + kb * BK + c * 8;
 #pragma unroll
@@ -605,7 +620,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(smem_u32(&full_bar[s]), C::FULL_ARRIVALS);
-      mbar_init(smem_u32(&empty_bar[s]), 1);
+      mbar_init(smem_u32(&empty_bar[s]), C::CL);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&tfull_bar[b]), 1);
@@ -648,8 +663,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         if (cnt < 0) cnt = 0;
       }
       const int mt = (cnt + BM - 1) / BM;
-      // lanes past the last group contribute nothing (no tiles, no rows)
-      const int tiles = (g >= a.G) ? 0 : ((C::SCH == RAGGED_M) ? mt * nNB : nMB * nNB);
+      // work units of this group (tiles, or m-block pairs with MC); lanes past
+      // the last group contribute nothing (no units, no rows)
+      const int mu = ((C::SCH == RAGGED_M ? mt : nMB) + C::CL - 1) / C::CL;
+      const int tiles = (g >= a.G) ? 0 : mu * nNB;
       const int rows = a.padded ? mt * BM : cnt;
       int ti = tiles, ro = rows;
 #pragma unroll
@@ -678,18 +695,23 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     }
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (C::MC) cluster_sync();  // the peer's barriers are initialised before any remote op
+  else __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = T.tmem_base;
   const int total = T.total_tiles;
+  const int rank = C::MC ? (int)cluster_ctarank() : 0;
+  const int unit0 = blockIdx.x / C::CL;
+  const int ustep = gridDim.x / C::CL;
+  constexpr uint16_t kPair = 0x3;
 
   if (warp == 0) {
     // ================= TMA producer =================
     int stage = 0;
     uint32_t phase = 0;
     uint32_t filled = 0, fill_parity = 0;  // per stage: armed at least once, parity of last fill
-    for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
-      const TileInfo ti = decode_tile<C>(a, T, t);
+    for (int t = unit0; t < total && !*abort_flag; t += ustep) {
+      const TileInfo ti = decode_tile<C>(a, T, t, rank);
       const int n0 = C::SWIGLU_B ? ti.nb * (C::BN / 2) : ti.nb * C::BN;
       const int m0 = ti.mb * BM;
       bool ok = true;
@@ -721,24 +743,43 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           if (lane == 0) {
 #pragma unroll
             for (int b = 0; b < C::B_NBOX; ++b) {
+              // with MC each CTA loads its share of the boxes, multicast to the pair
+              if (C::MC && (b * C::CL) / C::B_NBOX != rank) continue;
               const int nc = C::SWIGLU_B ? (b == 0 ? n0 : a.inter + n0) : n0 + b * C::B_BOX_ROWS;
               const uint32_t dst = sB + b * C::B_BOX_ROWS * 128;
-              if constexpr (C::B3D) tma_load_3d(dst, &tmB, fb, kc, nc, ti.g);
-              else tma_load_2d(dst, &tmB, fb, kx, nc);
+              if constexpr (C::MC) {
+                if constexpr (C::B3D) tma_load_3d_mc(dst, &tmB, fb, kc, nc, ti.g, kPair);
+                else tma_load_2d_mc(dst, &tmB, fb, kx, nc, kPair);
+              } else {
+                if constexpr (C::B3D) tma_load_3d(dst, &tmB, fb, kc, nc, ti.g);
+                else tma_load_2d(dst, &tmB, fb, kx, nc);
+              }
             }
           }
         } else if constexpr (C::BL == MN_TILE) {
           if (lane == 0) {
 #pragma unroll
             for (int b = 0; b < C::BN / 64; ++b) {
-              if constexpr (C::B3D) tma_load_3d(sB + b * 8192, &tmB, fb, n0 + 64 * b, kc, ti.g);
-              else tma_load_2d(sB + b * 8192, &tmB, fb, n0 + 64 * b, kr);
+              if (C::MC && (b * C::CL) / (C::BN / 64) != rank) continue;
+              if constexpr (C::MC) {
+                if constexpr (C::B3D) tma_load_3d_mc(sB + b * 8192, &tmB, fb, n0 + 64 * b, kc, ti.g, kPair);
+                else tma_load_2d_mc(sB + b * 8192, &tmB, fb, n0 + 64 * b, kr, kPair);
+              } else {
+                if constexpr (C::B3D) tma_load_3d(sB + b * 8192, &tmB, fb, n0 + 64 * b, kc, ti.g);
+                else tma_load_2d(sB + b * 8192, &tmB, fb, n0 + 64 * b, kr);
+              }
             }
           }
         }
         if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
       }
       if (!ok) break;
+    }
+    // wait until every stage this CTA filled has been released by all consumers
+    // (with MC this includes the peer's commits, which arrive remotely)
+    for (int i = 0; i < C::STAGES && !*abort_flag; ++i) {
+      if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1, abort_flag, a.status)) break;
+      if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
     }
     if (*abort_flag) {
       // let copies already in flight land before the CTA can exit (bounded)
@@ -756,8 +797,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     uint32_t phase = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
-      const TileInfo ti = decode_tile<C>(a, T, t);
+    for (int t = unit0; t < total && !*abort_flag; t += ustep) {
+      const TileInfo ti = decode_tile<C>(a, T, t, rank);
       if (!mbar_wait(smem_u32(&tempty_bar[acc]), acc_phase ^ 1, abort_flag, a.status)) break;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + acc * C::BN;
@@ -776,7 +817,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                                         : smem_desc_sw128(sB + kk * 32, 16, 1024);
             umma_bf16(d_tmem, ad, bd, C::IDESC, (kb | kk) != 0 ? 1u : 0u);
           }
-          umma_commit(smem_u32(&empty_bar[stage]));
+          if constexpr (C::MC) umma_commit_mc(smem_u32(&empty_bar[stage]), kPair);
+          else umma_commit(smem_u32(&empty_bar[stage]));
         }
         __syncwarp();
         if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
@@ -802,7 +844,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   } else if (C::GATHER && warp >= 2 + C::EPI_WARPS) {
     // ================= gather warps (LSU cp.async) =================
     gather_role<C>(a, T, smem_base, full_bar, empty_bar, abort_flag, warp - 2 - C::EPI_WARPS,
-                   lane, total);
+                   lane, total, rank, unit0, ustep);
   } else {
     // ================= epilogue =================
     const int quad = warp & 3;
@@ -817,12 +859,14 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     wo.inflight = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
-      const TileInfo ti = decode_tile<C>(a, T, t);
+    for (int t = unit0; t < total && !*abort_flag; t += ustep) {
+      const TileInfo ti = decode_tile<C>(a, T, t, rank);
       if (!mbar_wait(smem_u32(&tfull_bar[acc]), acc_phase, abort_flag, a.status)) break;
       tc_fence_after();
       const uint32_t tacc = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * C::BN;
-      if constexpr (C::EPI == EPI_STORE_F32)
+      if (ti.phantom) {
+        // pair slot past the group's last tile: nothing to store
+      } else if constexpr (C::EPI == EPI_STORE_F32)
         epilogue_store_f32<C>(a, ti, tacc, row_in_tile, wo, &tmD0, cpart, nparts);
       else if constexpr (C::EPI == EPI_SWIGLU)
         epilogue_swiglu<C>(a, ti, tacc, row_in_tile, wo, &tmD0, &tmD1, cpart, nparts);
@@ -840,7 +884,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   }
 
   tc_fence_before();
-  __syncthreads();
+  if constexpr (C::MC) cluster_sync();  // no CTA leaves while its peer may still write to it
+  else __syncthreads();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);

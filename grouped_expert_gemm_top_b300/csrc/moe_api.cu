@@ -232,19 +232,22 @@ using moe::RAGGED_M;
 template <int BN>
 using CfgRouter =
     GemmCfg<BN, (BN >= 256 ? 4 : 6), KMAJ_TILE, KMAJ_TILE, RAGGED_K, EPI_STORE_F32, false, false>;
-using CfgGateUp = GemmCfg<256, 4, KMAJ_GATHER, KMAJ_TILE, RAGGED_M, EPI_SWIGLU, true, true>;
-using CfgGateUpShared = GemmCfg<256, 4, KMAJ_TILE, KMAJ_TILE, RAGGED_M, EPI_SWIGLU, false, true>;
-using CfgDown = GemmCfg<256, 4, KMAJ_TILE, KMAJ_TILE, RAGGED_M, EPI_STORE, true, false>;
-using CfgDownShared = GemmCfg<256, 4, KMAJ_TILE, KMAJ_TILE, RAGGED_M, EPI_STORE, false, false>;
-using CfgDgradDown =
-    GemmCfg<256, 4, KMAJ_GATHER, MN_TILE, RAGGED_M, EPI_DGRAD_SWIGLU, true, false, 4 * kDwParts>;
+// Every BN=256 GEMM runs as 2-CTA clusters sharing the B tile by TMA multicast.
+constexpr bool kMC = true;
+using CfgGateUp = GemmCfg<256, 4, KMAJ_GATHER, KMAJ_TILE, RAGGED_M, EPI_SWIGLU, true, true, 4, kMC>;
+using CfgGateUpShared =
+    GemmCfg<256, 4, KMAJ_TILE, KMAJ_TILE, RAGGED_M, EPI_SWIGLU, false, true, 4, kMC>;
+using CfgDown = GemmCfg<256, 4, KMAJ_TILE, KMAJ_TILE, RAGGED_M, EPI_STORE, true, false, 4, kMC>;
+using CfgDownShared = GemmCfg<256, 4, KMAJ_TILE, KMAJ_TILE, RAGGED_M, EPI_STORE, false, false, 4, kMC>;
+using CfgDgradDown = GemmCfg<256, 4, KMAJ_GATHER, MN_TILE, RAGGED_M, EPI_DGRAD_SWIGLU, true, false,
+                             4 * kDwParts, kMC>;
 using CfgDgradDownShared =
-    GemmCfg<256, 4, KMAJ_TILE, MN_TILE, RAGGED_M, EPI_DGRAD_SWIGLU, false, false>;
-using CfgDgradGateUp = GemmCfg<256, 4, KMAJ_TILE, MN_TILE, RAGGED_M, EPI_STORE, true, false>;
-using CfgDgradGateUpShared = GemmCfg<256, 4, KMAJ_TILE, MN_TILE, RAGGED_M, EPI_STORE, false, false>;
-using CfgWgrad = GemmCfg<256, 4, MN_TILE, MN_TILE, RAGGED_K, EPI_STORE, false, false>;
-using CfgWgradDown = GemmCfg<256, 4, MN_GATHER, MN_TILE, RAGGED_K, EPI_STORE, false, false>;
-
+    GemmCfg<256, 4, KMAJ_TILE, MN_TILE, RAGGED_M, EPI_DGRAD_SWIGLU, false, false, 4, kMC>;
+using CfgDgradGateUp = GemmCfg<256, 4, KMAJ_TILE, MN_TILE, RAGGED_M, EPI_STORE, true, false, 4, kMC>;
+using CfgDgradGateUpShared =
+    GemmCfg<256, 4, KMAJ_TILE, MN_TILE, RAGGED_M, EPI_STORE, false, false, 4, kMC>;
+using CfgWgrad = GemmCfg<256, 4, MN_TILE, MN_TILE, RAGGED_K, EPI_STORE, false, false, 4, kMC>;
+using CfgWgradDown = GemmCfg<256, 4, MN_GATHER, MN_TILE, RAGGED_K, EPI_STORE, false, false, 4, kMC>;
 
 // fp32 [depth][rows][inner] output map with 16x32 boxes (64-byte rows).
 bool make_out_map3_f32(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows,
@@ -283,12 +286,43 @@ moe_status launch_gemm(int kid, const CUtensorMap& A, const CUtensorMap& B, cons
       return MOE_ERR_CUDA;
     configured.fetch_or(bit);
   }
-  long long grid = sm_count();
-  if (tile_bound < grid) grid = tile_bound;
-  if (grid < 1) return MOE_OK;
-  KernelScope ks(kid, st);
-  moe::grouped_gemm_kernel<C><<<(int)grid, C::THREADS, C::SMEM_BYTES, st>>>(A, B, D0, D1, a);
-  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  if constexpr (C::MC) {
+    // 2-CTA clusters; as many as can be resident at once (one CTA per SM)
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(C::THREADS);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    static std::atomic<int> max_clusters[64];
+    int mc = max_clusters[dev & 63].load();
+    if (mc == 0) {
+      cfg.gridDim = dim3(2 * (sm_count() / 2));
+      if (cudaOccupancyMaxActiveClusters(&mc, moe::grouped_gemm_kernel<C>, &cfg) != cudaSuccess ||
+          mc <= 0)
+        mc = sm_count() / 2;
+      max_clusters[dev & 63].store(mc);
+    }
+    const long long clusters = std::min<long long>(mc, (tile_bound + 1) / 2 + 1);
+    if (clusters < 1) return MOE_OK;
+    cfg.gridDim = dim3((unsigned)(2 * clusters));
+    KernelScope ks(kid, st);
+    if (cudaLaunchKernelEx(&cfg, moe::grouped_gemm_kernel<C>, A, B, D0, D1, a) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  } else {
+    long long grid = sm_count();
+    if (tile_bound < grid) grid = tile_bound;
+    if (grid < 1) return MOE_OK;
+    KernelScope ks(kid, st);
+    moe::grouped_gemm_kernel<C><<<(int)grid, C::THREADS, C::SMEM_BYTES, st>>>(A, B, D0, D1, a);
+    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  }
 }
 
 GemmArgs base_args(int* status) {

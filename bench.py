@@ -103,6 +103,25 @@ def kernel_model(name, w, counts, P):
     return table.get(name, (0.0, 0.0))
 
 
+def measured_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu capture, or None when the
+    GEMM kernel sources changed since the capture (or no capture covers it)."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f)
+        h = hashlib.md5()
+        for name in ("gemm.cuh", "ptx.cuh"):
+            with open(os.path.join(ROOT, "grouped_expert_gemm_top_b300", "csrc", name), "rb") as f:
+                h.update(f.read())
+        k = rec["kernels"].get(kernel)
+        if h.hexdigest() != rec["kernel_source_md5"] or not k or k["workload"] != workload:
+            return None
+        return k["dram_bytes_per_launch"]
+    except Exception:
+        return None
+
+
 class _CtypesNvml:
     """Minimal read-only NVML access through libnvidia-ml (when pynvml is absent)."""
 
@@ -406,7 +425,8 @@ def run_ours(args, w, rank, world):
     else:
         achieved, peak, unit = B / t_k / 1e9, peaks["hbm_gbs"], "GB/s"
     roofline = {"kernel": top, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
-                "frac": achieved / peak, "traffic": None, "peak_source": peak_src,
+                "frac": achieved / peak, "traffic": measured_traffic(top, w.name),
+                "peak_source": peak_src,
                 "algorithmic_flops": F, "algorithmic_bytes": B, "avg_us": kernels[top]["avg_us"]}
     per_kernel_roof = {}
     for name, v in kernels.items():

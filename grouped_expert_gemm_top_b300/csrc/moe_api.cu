@@ -800,3 +800,62 @@ moe_status moe_read_device_status(void* workspace, size_t workspace_bytes, void*
 }
 
 }  // extern "C"
+
+// =====================================================================================
+// Allocation-free variant of the expert sort (moe_permute) for callers that
+// cannot allocate device memory: code running where cudaMalloc is not allowed
+// or not wanted (inside a pre-sized memory pool, a plugin whose host owns all
+// device allocations, or a program that must not allocate after start-up), so
+// they cannot provide the workspace moe_permute needs.
+//
+// The sort's only scratch is the per-block expert histogram.  Here it lives in
+// a file-scope device array of fixed size; every call on a device shares it.
+namespace {
+
+// 65536 int32 = 256 KiB per device; holds ceil(T*k / 1024) * E block counts.
+constexpr long long kStaticScratchInts = 65536;
+
+static __device__ __align__(256) int32_t g_sort_scratch[kStaticScratchInts];
+
+constexpr int kMaxScratchDevices = 64;
+std::mutex g_scratch_mu;
+int32_t* g_scratch_ptr[kMaxScratchDevices] = {};
+
+// Device address of g_sort_scratch on the current device, looked up once per
+// device (in host code the symbol's name is only a stand-in, not an address).
+int32_t* static_scratch_for_current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxScratchDevices) return nullptr;
+  std::lock_guard<std::mutex> g(g_scratch_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_sort_scratch) != cudaSuccess || !p) return nullptr;
+    g_scratch_ptr[dev] = static_cast<int32_t*>(p);
+  }
+  return g_scratch_ptr[dev];
+}
+
+}  // namespace
+
+extern "C" moe_status moe_permute_static_scratch(const moe_dims* d, const int32_t* topk_idx,
+                                                 int32_t* expert_offsets, int32_t* perm_slot,
+                                                 int32_t* slot_perm, int32_t* device_status,
+                                                 void* stream) {
+  moe_status s = check_dims(d);
+  if (s != MOE_OK) return s;
+  if (!topk_idx || !expert_offsets || !perm_slot || !slot_perm) return MOE_ERR_INVALID_ARG;
+  const long long S = (long long)d->T * d->k;
+  const long long blocks = (S + moe::kSortChunk - 1) / moe::kSortChunk;
+  // the block histograms must fit the fixed device array
+  if (blocks * d->E > kStaticScratchInts) return MOE_ERR_UNSUPPORTED_SHAPE;
+  int32_t* counts = static_scratch_for_current_device();
+  if (!counts) return MOE_ERR_CUDA;
+  // Nothing in the array needs clearing: pass 1 writes every (block, expert)
+  // count that pass 2 reads.
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  moe::sort_histogram_kernel<<<(unsigned)blocks, moe::kSortThreads, 0, st>>>(
+      topk_idx, (int)S, d->E, counts, device_status);
+  moe::sort_scatter_kernel<<<(unsigned)blocks, moe::kSortThreads, 0, st>>>(
+      topk_idx, (int)S, d->E, (int)blocks, counts, expert_offsets, perm_slot, slot_perm);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}

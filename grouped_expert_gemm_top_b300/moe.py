@@ -63,6 +63,7 @@ _SIGS = {
     "moe_unpermute_combine": ([_DIMS, _P, _P, _P, _P, _P, _P], _I32),
     "moe_layer_bwd": ([_DIMS] + [_P] * 21 + [_P, _SZ, _P], _I32),
     "moe_read_device_status": ([_P, _SZ, _P, _I32, ctypes.POINTER(_I32)], _I32),
+    "moe_permute_static_scratch": ([_DIMS, _P, _P, _P, _P, _P, _P], _I32),
     "moe_kernel_count": ([], _I32),
     "moe_kernel_name": ([_I32], ctypes.c_char_p),
     "moe_timing_enable": ([_I32], _I32),
@@ -191,6 +192,16 @@ def moe_read_device_status(workspace, clear: bool = True, stream=None) -> int:
     _check("moe_read_device_status", load_library().moe_read_device_status(
         p, n, _stream(stream), int(clear), ctypes.byref(out)))
     return out.value
+
+
+def moe_permute_static_scratch(dims, topk_idx, expert_offsets, perm_slot, slot_perm,
+                               device_status=None, stream=None):
+    """moe_permute without a workspace, for callers that cannot allocate device
+    memory: the sort's scratch is a fixed 256 KiB array inside the library
+    (shared by every call on a device, so calls must not overlap on the GPU)."""
+    _check("moe_permute_static_scratch", load_library().moe_permute_static_scratch(
+        ctypes.byref(_dims(dims)), _ptr(topk_idx), _ptr(expert_offsets), _ptr(perm_slot),
+        _ptr(slot_perm), _ptr(device_status), _stream(stream)))
 
 
 def moe_kernel_count() -> int:

@@ -192,6 +192,38 @@ moe_status moe_read_device_status(void* workspace, size_t workspace_bytes, void*
                                   int32_t clear, int32_t* device_status);
 
 /*
+ * Allocation-free variant of moe_permute (no counterpart on the pages).
+ *
+ * For callers that cannot allocate device memory, so cannot pass the
+ * workspace moe_permute needs: code running where cudaMalloc is not allowed
+ * or not wanted (inside a pre-sized memory pool, a plugin whose host owns all
+ * device allocations, a program that must not allocate after start-up).
+ * Results are identical to moe_permute's: same expert_offsets [E+1],
+ * perm_slot [S] and slot_perm [S] (device pointers, caller-owned).
+ *
+ * Its scratch (the per-block expert histograms, ceil(T*k / 1024) * E int32)
+ * lives in a fixed 256 KiB device array built into the library, which every
+ * GPU that loads the library holds until the process exits.  Limit:
+ * ceil(T*k / 1024) * E <= 65536 (e.g. T*k <= 524288 slots with E = 128);
+ * larger shapes return MOE_ERR_UNSUPPORTED_SHAPE before anything is launched.
+ * The call allocates nothing (no cudaMalloc, cudaFree or allocating library
+ * routine).  The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) for that device; make that first call before any
+ * stream capture.  Every call on a device shares the one array and it keeps
+ * the last call's contents (nothing in it needs clearing: each call writes
+ * every entry it reads); calls whose work overlaps on the GPU (different
+ * streams, no ordering between them) race on it.
+ * device_status: optional device int32 (NULL to skip); expert ids outside
+ * [0, E) are skipped and MOE_ERR_DEVICE_INDEX is recorded there if it holds
+ * MOE_OK (the caller zeroes it).
+ * Errors: MOE_ERR_INVALID_ARG (null pointer), MOE_ERR_UNSUPPORTED_SHAPE,
+ * MOE_ERR_CUDA (symbol lookup or launch failed).
+ */
+moe_status moe_permute_static_scratch(const moe_dims* d, const int32_t* topk_idx,
+                                      int32_t* expert_offsets, int32_t* perm_slot,
+                                      int32_t* slot_perm, int32_t* device_status, void* stream);
+
+/*
  * Kernel accounting, for benchmarks and tests (no counterpart on the pages).
  * Every kernel the calls above launch is counted under one of the ids below.
  * While timing is enabled, each launch is also bracketed by a pair of CUDA

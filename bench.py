@@ -283,6 +283,22 @@ def run_reference(args, w, rank):
     return 0
 
 
+def max_over_ranks_ms(v, world):
+    """The slowest rank's time (replicas: the job ends when the last one does)."""
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([float(v)], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+    return float(v)
+
+
+def job_tokens_per_s(tokens_per_rank_step, world, steps, max_ms):
+    """Whole-job throughput: every rank's tokens over the max-over-ranks time."""
+    return tokens_per_rank_step * world * steps / (max_ms / 1e3)
+
+
 def config_of(w, args):
     return {"workload": w.name, "T": w.T, "H": w.H, "E": w.E, "k": w.k, "I": w.I,
             "I_shared": w.I_shared, "gate": "balanced" if w.gate == 1 else "softmax_topk",
@@ -335,12 +351,7 @@ def run_ours(args, w, rank, world):
             dist.barrier()
 
     def max_over_ranks(v):
-        if world > 1:
-            import torch.distributed as dist
-            t = torch.tensor([v], dtype=torch.float64)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            return float(t.item())
-        return v
+        return max_over_ranks_ms(v, world)
 
     def timed(fn, k):
         barrier()
@@ -397,10 +408,9 @@ def run_ours(args, w, rank, world):
     h2d = x.numel() * 2 + go.numel() * 2
     d2h = outh.numel() * 2 + gxh.numel() * 2
 
-    tokens = w.T * world
-    value = tokens * args.steps / (ms_fb / 1e3)
-    fwd_value = tokens * args.steps / (ms_f / 1e3)
-    e2e_value = tokens * args.steps / (ms_e2e / 1e3)
+    value = job_tokens_per_s(w.T, world, args.steps, ms_fb)
+    fwd_value = job_tokens_per_s(w.T, world, args.steps, ms_f)
+    e2e_value = job_tokens_per_s(w.T, world, args.steps, ms_e2e)
 
     peaks, peak_src = load_peaks()
     f_fwd, b_fwd, f_fb, b_fb = layer_model(w, counts)

@@ -57,6 +57,7 @@ class DeviceInputs:
     def __init__(self, w: G.Workload, seed=0, with_grad=None):
         self.w = w
         self.np = G.make_inputs(w, seed, with_grad)
+        self._f64 = {}
         n = self.np
         self.x = dev_bf16(n["x"])
         self.w_router = dev_bf16(n["w_router"])
@@ -68,10 +69,13 @@ class DeviceInputs:
         self.grad_out = dev_bf16(n["grad_out"]) if n["grad_out"] is not None else None
 
     def f64(self, key):
-        v = self.np[key]
-        if v is None:
-            return None
-        return O.widen_bf16(v) if v.dtype == np.uint16 else v.astype(np.float64)
+        """float64 copy of an input, widened once and kept (full-size weights are GBs)."""
+        if key not in self._f64:
+            v = self.np[key]
+            if v is None:
+                return None
+            self._f64[key] = O.widen_bf16(v) if v.dtype == np.uint16 else v.astype(np.float64)
+        return self._f64[key]
 
     @property
     def dims(self):

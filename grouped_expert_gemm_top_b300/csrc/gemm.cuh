@@ -42,7 +42,6 @@ constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int kTmemCols = 512;
 constexpr int kMaxGroups = 256;
-constexpr int kEpiStagingPerWarp = 3 * 2048;  // epilogue staging (see the epilogue section)
 
 // TILE: TMA tile loads.  GATHER: rows (K-major: M rows; MN-major: K rows) are
 // token rows of a [tokens, ld] matrix, selected through the expert sort.
@@ -71,13 +70,24 @@ struct GemmArgs {
 };
 
 template <int BN_, int STAGES_, int AL_, int BL_, int SCH_, int EPI_, bool B3D_, bool SWIGLU_B_,
-          int EPI_WARPS_ = 4, bool MC_ = false>
+          int EPI_WARPS_ = 4, bool MC_ = false, bool PAIR_ = false, int EPI_BUFS_ = 3>
 struct GemmCfg {
   // MC: 2-CTA clusters; the two CTAs take adjacent M-tiles of the same
   // (group, n-block) and each TMA-multicasts half of the shared B tile.
+  // PAIR: 2-CTA clusters computing one 256 x BN tile with CTA-pair UMMAs
+  // (cta_group::2): each CTA stages its own 128 A rows and only HALF of the B
+  // tile, the even CTA issues the UMMAs, and each CTA's TMEM receives its own
+  // 128 rows.  Per SM this halves the B bytes pulled from L2 per FLOP.
   static constexpr bool MC = MC_;
-  static constexpr int CL = MC ? 2 : 1;
+  static constexpr bool PAIR = PAIR_;
+  static_assert(!(MC && PAIR), "MC and PAIR are alternatives");
+  static constexpr int CL = (MC || PAIR) ? 2 : 1;
   static constexpr int EPI_WARPS = EPI_WARPS_;
+  // staging buffers per epilogue warp = TMA stores it keeps in flight; the
+  // weight-gradient GEMMs, whose output is most of their traffic, need more
+  static constexpr int EPI_BUFS = EPI_BUFS_;
+  // one staging buffer: 32 rows x 64 bf16 columns, or 32 rows x 16 fp32 columns
+  static constexpr int EPI_BUF_BYTES = EPI_ == EPI_STORE_F32 ? 2048 : 4096;
   static constexpr bool A_GATHER = (AL_ == KMAJ_GATHER || AL_ == MN_GATHER);
   static constexpr bool B_GATHER = (BL_ == MN_GATHER);
   static constexpr bool GATHER = A_GATHER || B_GATHER;
@@ -96,7 +106,8 @@ struct GemmCfg {
   static constexpr bool B3D = B3D_;
   static constexpr bool SWIGLU_B = SWIGLU_B_;
   static constexpr int A_BYTES = BM * BK * 2;
-  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int B_ROWS = PAIR ? BN / 2 : BN;  // B rows (N extent) staged by this CTA
+  static constexpr int B_BYTES = B_ROWS * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   // K-major B is loaded in boxes of at most 128 rows.
   static constexpr int B_BOX_ROWS = BN < 128 ? BN : 128;
@@ -104,12 +115,18 @@ struct GemmCfg {
   static constexpr bool A_MN = (AL == MN_TILE || AL == MN_GATHER);
   static constexpr bool B_MN = (BL == MN_TILE || BL == MN_GATHER);
   static constexpr int TMA_BYTES = (A_GATHER ? 0 : A_BYTES) + (B_GATHER ? 0 : B_BYTES);
-  static constexpr uint32_t FULL_ARRIVALS = 1 + (GATHER ? 32 * GATHER_WARPS : 0);
+  // The pair's stages complete on the even CTA's full barriers: the TMA bytes of
+  // both CTAs and one arrival per gather warp of both CTAs.
+  static constexpr uint32_t FULL_TX = TMA_BYTES * (PAIR ? 2 : 1);
+  static constexpr uint32_t FULL_ARRIVALS = 1 + (GATHER ? GATHER_WARPS * (PAIR ? 2 : 1) : 0);
+  // one arrival per epilogue warp (of both CTAs with PAIR) frees a TMEM accumulator
+  static constexpr uint32_t TEMPTY_ARRIVALS = EPI_WARPS * (PAIR ? 2 : 1);
+  static_assert(!PAIR || (BN == 256 && !B_GATHER), "PAIR splits a 256-wide TMA-loaded B tile");
   static_assert(!SWIGLU_B || BN == 256, "the gate/up tile pairs 128 gate with 128 up columns");
-  static constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, A_MN, B_MN);
+  static constexpr uint32_t IDESC = idesc_bf16_f32(PAIR ? 2 * BM : BM, BN, A_MN, B_MN);
   static constexpr bool TMA_OUT = true;
   static constexpr int SMEM_BYTES =
-      STAGES * STAGE_BYTES + (TMA_OUT ? EPI_WARPS * kEpiStagingPerWarp : 0) + 1024;  // + align
+      STAGES * STAGE_BYTES + (TMA_OUT ? EPI_WARPS * EPI_BUFS * EPI_BUF_BYTES : 0) + 1024;  // + align
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N");
   static_assert(!B_MN || BN % 64 == 0, "MN-major B needs 64-wide groups");
   static_assert(2 * BN <= kTmemCols, "two accumulators must fit TMEM");
@@ -184,66 +201,43 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, const SmemTab
 }
 
 // ---------------------------------------------------------------- epilogues
-// Output path: each epilogue warp owns 32 rows of the tile.  A 32x32 bf16
-// block (one 32-column chunk of its rows) is written into a 2 KB shared buffer
-// with the 64-byte swizzle (conflict-free 16-byte writes) and stored by one
-// TMA bulk-tensor store, so global writes are full, coalesced lines.  Three
-// buffers per warp rotate, letting up to three stores be in flight.  A warp
-// whose 32 rows are not all inside the group (ragged expert edge) stores its
-// valid rows directly instead.
-constexpr int kStageBytes = 2048;            // 32 rows x 64 bytes
-constexpr int kStagesPerWarp = 3;
-static_assert(kStagesPerWarp * kStageBytes == kEpiStagingPerWarp, "epilogue staging size");
-
+// Output path: each epilogue warp owns 32 rows of the tile.  bf16 outputs leave
+// in blocks of 32 rows x 64 columns (4 KB): the warp writes its rows of a block
+// into a shared staging buffer with the 128-byte swizzle (conflict-free 16-byte
+// writes) and one TMA bulk-tensor store sends it, so global writes are whole
+// 128-byte lines and each store moves 4 KB.  (The fp32 split-K router partials
+// use 32 x 16 fp32 blocks of 2 KB with the 64-byte swizzle.)  NB buffers per
+// warp rotate, letting up to NB stores be in flight.  A warp whose 32 rows are
+// not all inside the group (ragged expert edge) writes its valid rows directly.
+template <int NB, int BYTES>
 struct WarpOut {
   uint32_t buf0;  // this warp's first staging buffer (1024-byte aligned)
   int lane;
   int next;       // next buffer to use
-  int inflight;   // committed store groups not yet known to have read their buffer
+  int inflight;   // committed stores not yet known to have read their buffer
 };
 
-// Write this thread's 32 values (its row of a 32-column chunk) as bf16 into the
-// next staging buffer; waits until that buffer's previous store has read it.
-__device__ __forceinline__ uint32_t stage_row(WarpOut& w, const float (&v)[32]) {
-  if (w.inflight >= kStagesPerWarp) {
-    if (w.lane == 0) bulk_wait_read<kStagesPerWarp - 1>();
+// Take the next K staging buffers (the first is returned, the others follow at
+// BYTES strides; callers take K consecutive buffers with K dividing NB, so they
+// never wrap).  Buffer next+i was last read by the store issued NB-i stores ago,
+// so at most NB-K stores may still be pending.
+template <int K, int NB, int BYTES>
+__device__ __forceinline__ uint32_t stage_acquire(WarpOut<NB, BYTES>& w) {
+  static_assert(K <= NB, "staging ring too small");
+  if (w.inflight > NB - K) {
+    if (w.lane == 0) bulk_wait_read<NB - K>();
     __syncwarp();
-    w.inflight = kStagesPerWarp - 1;
+    w.inflight = NB - K;
   }
-  const uint32_t buf = w.buf0 + w.next * kStageBytes;
-  w.next = (w.next + 1) % kStagesPerWarp;
-  const uint32_t row = buf + w.lane * 64;
-  const int sw = (w.lane >> 1) & 3;
-#pragma unroll
-  for (int q = 0; q < 4; ++q)
-    st_shared_v4(row + ((q ^ sw) << 4), pack_bf16x2(v[8 * q + 0], v[8 * q + 1]),
-                 pack_bf16x2(v[8 * q + 2], v[8 * q + 3]), pack_bf16x2(v[8 * q + 4], v[8 * q + 5]),
-                 pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+  const uint32_t buf = w.buf0 + w.next * BYTES;
+  w.next = (w.next + 1) % NB;
   return buf;
 }
 
-// fp32 variant: 16 values (64 bytes) of this thread's row, v[16*half .. 16*half+15].
-__device__ __forceinline__ uint32_t stage_row_f32(WarpOut& w, const float (&v)[32], int half) {
-  if (w.inflight >= kStagesPerWarp) {
-    if (w.lane == 0) bulk_wait_read<kStagesPerWarp - 1>();
-    __syncwarp();
-    w.inflight = kStagesPerWarp - 1;
-  }
-  const uint32_t buf = w.buf0 + w.next * kStageBytes;
-  w.next = (w.next + 1) % kStagesPerWarp;
-  const uint32_t row = buf + w.lane * 64;
-  const int sw = (w.lane >> 1) & 3;
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const int b = 16 * half + 4 * q;
-    st_shared_v4(row + ((q ^ sw) << 4), __float_as_uint(v[b]), __float_as_uint(v[b + 1]),
-                 __float_as_uint(v[b + 2]), __float_as_uint(v[b + 3]));
-  }
-  return buf;
-}
-
-__device__ __forceinline__ void stage_store(WarpOut& w, uint32_t buf, const CUtensorMap* map, int x,
-                                            int y, int z, bool three_d) {
+template <int NB, int BYTES>
+__device__ __forceinline__ void stage_store(WarpOut<NB, BYTES>& w, uint32_t buf,
+                                            const CUtensorMap* map, int x, int y, int z,
+                                            bool three_d) {
   fence_proxy_async_smem();
   __syncwarp();
   if (w.lane == 0) {
@@ -255,30 +249,26 @@ __device__ __forceinline__ void stage_store(WarpOut& w, uint32_t buf, const CUte
   ++w.inflight;
 }
 
-template <class C>
-__device__ __forceinline__ void store_row_chunk_bf16(__nv_bfloat16* dst, const float (&v)[32]) {
-  uint4* p = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    uint4 w;
-    w.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
-    w.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
-    w.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
-    w.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
-    p[q] = w;
-  }
+// 16-byte piece p (bf16 columns 8p .. 8p+7 of a 64-column block) of this
+// thread's row (row = lane), 128-byte swizzle.
+__device__ __forceinline__ void put128(uint32_t buf, int lane, int p, uint32_t x0, uint32_t x1,
+                                       uint32_t x2, uint32_t x3) {
+  st_shared_v4(buf + lane * 128 + ((p ^ (lane & 7)) << 4), x0, x1, x2, x3);
 }
 
-__device__ __forceinline__ void load_row_chunk_bf16(const __nv_bfloat16* src, float (&v)[32]) {
-  const uint4* p = reinterpret_cast<const uint4*>(src);
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    uint4 w = __ldg(p + q);
-    v[8 * q + 0] = bf16lo(w.x); v[8 * q + 1] = bf16hi(w.x);
-    v[8 * q + 2] = bf16lo(w.y); v[8 * q + 3] = bf16hi(w.y);
-    v[8 * q + 4] = bf16lo(w.z); v[8 * q + 5] = bf16hi(w.z);
-    v[8 * q + 6] = bf16lo(w.w); v[8 * q + 7] = bf16hi(w.w);
-  }
+__device__ __forceinline__ void st_global_16(__nv_bfloat16* dst, uint32_t x0, uint32_t x1,
+                                             uint32_t x2, uint32_t x3) {
+  *reinterpret_cast<uint4*>(dst) = make_uint4(x0, x1, x2, x3);
+}
+
+// 64-column blocks [g0, g1) of this warp's column part that lie inside N
+// (every output width is a multiple of 64).
+__device__ __forceinline__ void block_range(int cpart, int nparts, int nblk, int n0, int N, int& g0,
+                                            int& g1) {
+  g0 = cpart * nblk / nparts;
+  g1 = (cpart + 1) * nblk / nparts;
+  const int inside = N > n0 ? (N - n0) / 64 : 0;
+  if (g1 > inside) g1 = inside;
 }
 
 // silu(g) = g * sigmoid(g), with CUDA's fast exponential and division intrinsics.
@@ -287,9 +277,9 @@ __device__ __forceinline__ float silu_f(float g) { return g * sigmoid_f(g); }
 
 // fp32 output (split-K router partials).  RAGGED_K: D is the group's (split's)
 // M x N slice, map tmD0 3-D [groups][M][N] with 16x32 fp32 boxes.
-template <class C>
+template <class C, class W>
 __device__ void epilogue_store_f32(const GemmArgs& a, const TileInfo& ti, uint32_t tacc,
-                                   int row_in_tile, WarpOut& w, const CUtensorMap* tmD0, int cpart,
+                                   int row_in_tile, W& w, const CUtensorMap* tmD0, int cpart,
                                    int nparts) {
   const int quad = row_in_tile >> 5;
   const bool valid = row_in_tile < ti.rows_valid;
@@ -311,8 +301,20 @@ __device__ void epilogue_store_f32(const GemmArgs& a, const TileInfo& ti, uint32
       for (int i = 0; i < 32; ++i) v[i] = 0.f;
     }
     if (warp_full) {
-      stage_store(w, stage_row_f32(w, v, 0), tmD0, col, y, ti.g, k3);
-      if (col + 16 < a.N) stage_store(w, stage_row_f32(w, v, 1), tmD0, col + 16, y, ti.g, k3);
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        if (half == 1 && col + 16 >= a.N) break;
+        const uint32_t buf = stage_acquire<1>(w);
+        const uint32_t rowp = buf + w.lane * 64;
+        const int sw = (w.lane >> 1) & 3;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int e = 16 * half + 4 * q;
+          st_shared_v4(rowp + ((q ^ sw) << 4), __float_as_uint(v[e]), __float_as_uint(v[e + 1]),
+                       __float_as_uint(v[e + 2]), __float_as_uint(v[e + 3]));
+        }
+        stage_store(w, buf, tmD0, col + 16 * half, y, ti.g, k3);
+      }
     } else if (valid) {
       float* dst = base + row * a.ldd + col;
       for (int i = 0; i < 32 && col + i < a.N; ++i) dst[i] = v[i];
@@ -323,9 +325,9 @@ __device__ void epilogue_store_f32(const GemmArgs& a, const TileInfo& ti, uint32
 // Gate/up epilogue: acc columns [0, BN/2) are gate, [BN/2, BN) up, for the
 // intermediate columns n0 .. n0+BN/2-1.  Writes g, u (bf16, for the backward)
 // and h = silu(g) * u.  Maps: tmD0 = gu_out [rows, 2I], tmD1 = h_out [rows, I].
-template <class C>
+template <class C, class W>
 __device__ void epilogue_swiglu(const GemmArgs& a, const TileInfo& ti, uint32_t tacc,
-                                int row_in_tile, WarpOut& w, const CUtensorMap* tmD0,
+                                int row_in_tile, W& w, const CUtensorMap* tmD0,
                                 const CUtensorMap* tmD1, int cpart, int nparts) {
   const int quad = row_in_tile >> 5;
   const bool valid = row_in_tile < ti.rows_valid;
@@ -335,39 +337,70 @@ __device__ void epilogue_swiglu(const GemmArgs& a, const TileInfo& ti, uint32_t 
   const int I = a.inter;
   constexpr int HALF = C::BN / 2;
   const int n0 = ti.nb * HALF;
-  float g[32], u[32];
-  constexpr int NCH = HALF / 32;
+  const bool keep_gu = a.gu_out != nullptr;
+  int g0, g1;
+  block_range(cpart, nparts, HALF / 64, n0, I, g0, g1);
 #pragma unroll 1
-  for (int c = cpart * NCH / nparts; c < (cpart + 1) * NCH / nparts; ++c) {
-    const int j = n0 + c * 32;
-    if (j >= I) break;
-    tmem_ld32(tacc + c * 32, g);
-    tmem_ld32(tacc + HALF + c * 32, u);
+  for (int gi = g0; gi < g1; ++gi) {
+    const int j = n0 + gi * 64;
+    uint32_t bg = 0, bu = 0, bh = 0;
     if (warp_full) {
-      if (a.gu_out) {
-        stage_store(w, stage_row(w, g), tmD0, j, y, 0, false);
-        stage_store(w, stage_row(w, u), tmD0, I + j, y, 0, false);
+      if (keep_gu) {
+        bg = stage_acquire<3>(w);
+        bu = stage_acquire<1>(w);  // inside the three just made free
       }
+      bh = stage_acquire<1>(w);
+    }
+#pragma unroll 1
+    for (int h = 0; h < 2; ++h) {
+      uint32_t g[32], u[32];
+      tmem_ld32_issue(tacc + gi * 64 + h * 32, g);
+      tmem_ld32_issue(tacc + HALF + gi * 64 + h * 32, u);
+      tmem_ld_wait2(g, u);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) g[i] = silu_f(g[i]) * u[i];
-      stage_store(w, stage_row(w, g), tmD1, j, y, 0, false);
-    } else if (valid) {
-      if (a.gu_out) {
-        store_row_chunk_bf16<C>(a.gu_out + r * (2LL * I) + j, g);
-        store_row_chunk_bf16<C>(a.gu_out + r * (2LL * I) + I + j, u);
+      for (int q = 0; q < 4; ++q) {
+        uint32_t pg[4], pu[4], ph[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int e = 8 * q + 2 * i;
+          const float ga = __uint_as_float(g[e]), gb = __uint_as_float(g[e + 1]);
+          const float ua = __uint_as_float(u[e]), ub = __uint_as_float(u[e + 1]);
+          pg[i] = pack_bf16x2(ga, gb);
+          pu[i] = pack_bf16x2(ua, ub);
+          ph[i] = pack_bf16x2(silu_f(ga) * ua, silu_f(gb) * ub);
+        }
+        const int pc = 4 * h + q;  // piece within the 64-column block
+        if (warp_full) {
+          if (keep_gu) {
+            put128(bg, w.lane, pc, pg[0], pg[1], pg[2], pg[3]);
+            put128(bu, w.lane, pc, pu[0], pu[1], pu[2], pu[3]);
+          }
+          put128(bh, w.lane, pc, ph[0], ph[1], ph[2], ph[3]);
+        } else if (valid) {
+          const int col = j + 8 * pc;
+          if (keep_gu) {
+            st_global_16(a.gu_out + r * (2LL * I) + col, pg[0], pg[1], pg[2], pg[3]);
+            st_global_16(a.gu_out + r * (2LL * I) + I + col, pu[0], pu[1], pu[2], pu[3]);
+          }
+          st_global_16(a.h_out + r * (long long)I + col, ph[0], ph[1], ph[2], ph[3]);
+        }
       }
-#pragma unroll
-      for (int i = 0; i < 32; ++i) g[i] = silu_f(g[i]) * u[i];
-      store_row_chunk_bf16<C>(a.h_out + r * (long long)I + j, g);
+    }
+    if (warp_full) {
+      if (keep_gu) {
+        stage_store(w, bg, tmD0, j, y, 0, false);
+        stage_store(w, bu, tmD0, I + j, y, 0, false);
+      }
+      stage_store(w, bh, tmD1, j, y, 0, false);
     }
   }
 }
 
 // Plain bf16 output.  RAGGED_M: D rows are the tile's rows (map tmD0 2-D);
 // RAGGED_K: D is the group's full M x N matrix (map tmD0 3-D, group = depth).
-template <class C>
+template <class C, class W>
 __device__ void epilogue_store(const GemmArgs& a, const TileInfo& ti, uint32_t tacc,
-                               int row_in_tile, WarpOut& w, const CUtensorMap* tmD0, int cpart,
+                               int row_in_tile, W& w, const CUtensorMap* tmD0, int cpart,
                                int nparts) {
   const int quad = row_in_tile >> 5;
   const bool valid = row_in_tile < ti.rows_valid;
@@ -376,24 +409,36 @@ __device__ void epilogue_store(const GemmArgs& a, const TileInfo& ti, uint32_t t
   constexpr bool k3 = C::SCH == RAGGED_K;
   const long long row = (k3 ? ti.mb * BM : ti.row0) + row_in_tile;
   const int y = (k3 ? ti.mb * BM : ti.row0) + quad * 32;
-  float v[32];
-  constexpr int NCH = C::BN / 32;
+  const bool live = ti.kblocks > 0;  // an expert with no rows has an exact zero gradient
+  __nv_bfloat16* drow = a.d + (k3 ? (long long)ti.g * a.d_group_stride : 0) + row * a.ldd;
+  int g0, g1;
+  block_range(cpart, nparts, C::BN / 64, n0, a.N, g0, g1);
 #pragma unroll 1
-  for (int c = cpart * NCH / nparts; c < (cpart + 1) * NCH / nparts; ++c) {
-    const int col = n0 + c * 32;
-    if (col >= a.N) break;
-    if (ti.kblocks == 0) {
+  for (int gi = g0; gi < g1; ++gi) {
+    const int col = n0 + gi * 64;
+    const uint32_t buf = warp_full ? stage_acquire<1>(w) : 0u;
+#pragma unroll 1
+    for (int h = 0; h < 2; ++h) {
+      uint32_t v[32];
+      if (live) {
+        tmem_ld32_issue(tacc + gi * 64 + h * 32, v);
+        tmem_ld_wait(v);
+      } else {
 #pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = 0.f;
-    } else {
-      tmem_ld32(tacc + c * 32, v);
+        for (int i = 0; i < 32; ++i) v[i] = 0u;
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint32_t x[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          x[i] = pack_bf16x2(__uint_as_float(v[8 * q + 2 * i]), __uint_as_float(v[8 * q + 2 * i + 1]));
+        const int pc = 4 * h + q;
+        if (warp_full) put128(buf, w.lane, pc, x[0], x[1], x[2], x[3]);
+        else if (valid) st_global_16(drow + col + 8 * pc, x[0], x[1], x[2], x[3]);
+      }
     }
-    if (warp_full) {
-      stage_store(w, stage_row(w, v), tmD0, col, y, ti.g, k3);
-    } else if (valid) {
-      __nv_bfloat16* base = a.d + (k3 ? (long long)ti.g * a.d_group_stride : 0);
-      store_row_chunk_bf16<C>(base + row * a.ldd + col, v);
-    }
+    if (warp_full) stage_store(w, buf, tmD0, col, y, ti.g, k3);
   }
 }
 
@@ -402,10 +447,11 @@ __device__ void epilogue_store(const GemmArgs& a, const TileInfo& ti, uint32_t t
 // From the saved pre-activations (g, u): h = silu(g) u; dw partial = <acc, h>;
 // dh = w acc; dg = dh u s (1 + g (1 - s)); du = dh silu(g); hw = w h.
 // Maps: tmD0 = dgu_out [rows, 2I], tmD1 = hw_out [rows, I].  In the padded
-// layout the rows past the expert's tokens are written as exact zeros.
-template <class C>
+// layout the rows past the expert's tokens are written as exact zeros.  The
+// saved (g, u) of the next 32 columns are loaded while this half is computed.
+template <class C, class W>
 __device__ void epilogue_dgrad_swiglu(const GemmArgs& a, const SmemTables& T, const TileInfo& ti,
-                                      uint32_t tacc, int row_in_tile, WarpOut& w,
+                                      uint32_t tacc, int row_in_tile, W& w,
                                       const CUtensorMap* tmD0, const CUtensorMap* tmD1, int cpart,
                                       int nparts) {
   const int quad = row_in_tile >> 5;
@@ -424,42 +470,84 @@ __device__ void epilogue_dgrad_swiglu(const GemmArgs& a, const SmemTables& T, co
     if (a.padded) r = T.off[ti.g] + ti.mb * BM + row_in_tile;
     if (a.slot_w) wt = __ldg(a.slot_w + __ldg(a.perm_slot + r));
   }
-  float acc[32], g[32], u[32];
+  const __nv_bfloat16* gsrc = a.gu_saved + r * (2LL * I);
+  int g0, g1;
+  block_range(cpart, nparts, C::BN / 64, n0, I, g0, g1);
   float dwp = 0.f;
-  constexpr int NCH = C::BN / 32;
+  uint4 gs[4], us[4];  // saved g, u of the current 32 columns (valid rows)
+  auto load_gu = [&](int col, uint4 (&gd)[4], uint4 (&ud)[4]) {
+    const uint4* pg = reinterpret_cast<const uint4*>(gsrc + col);
+    const uint4* pu = reinterpret_cast<const uint4*>(gsrc + I + col);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) { gd[q] = __ldg(pg + q); ud[q] = __ldg(pu + q); }
+  };
+  if (valid && g0 < g1) load_gu(n0 + g0 * 64, gs, us);
 #pragma unroll 1
-  for (int c = cpart * NCH / nparts; c < (cpart + 1) * NCH / nparts; ++c) {
-    const int j = n0 + c * 32;
-    if (j >= I) break;
-    tmem_ld32(tacc + c * 32, acc);
-    if (valid) {
-      load_row_chunk_bf16(a.gu_saved + r * (2LL * I) + j, g);
-      load_row_chunk_bf16(a.gu_saved + r * (2LL * I) + I + j, u);
+  for (int gi = g0; gi < g1; ++gi) {
+    const int j = n0 + gi * 64;
+    uint32_t bdg = 0, bdu = 0, bhw = 0;
+    if (warp_full) {
+      bdg = stage_acquire<3>(w);
+      bdu = stage_acquire<1>(w);  // inside the three just made free
+      bhw = stage_acquire<1>(w);
+    }
+#pragma unroll 1
+    for (int h = 0; h < 2; ++h) {
+      uint32_t acc[32];
+      tmem_ld32_issue(tacc + gi * 64 + h * 32, acc);
+      uint4 gn[4], un[4];
+      const int nxt = j + 32 * (h + 1);  // next 32 columns of this warp, if any
+      const bool more = valid && (h == 0 || gi + 1 < g1);
+      if (more) load_gu(nxt, gn, un);
+      tmem_ld_wait(acc);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float s = sigmoid_f(g[i]);
-        const float sl = g[i] * s;
-        const float h = sl * u[i];
-        dwp = fmaf(acc[i], h, dwp);
-        const float dh = wt * acc[i];
-        const float dg = dh * u[i] * s * (1.0f + g[i] * (1.0f - s));
-        const float du = dh * sl;
-        g[i] = dg;
-        u[i] = du;
-        acc[i] = wt * h;
+      for (int q = 0; q < 4; ++q) {
+        uint32_t pdg[4] = {0u, 0u, 0u, 0u}, pdu[4] = {0u, 0u, 0u, 0u}, phw[4] = {0u, 0u, 0u, 0u};
+        if (valid) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint32_t gw = (&gs[q].x)[i], uw = (&us[q].x)[i];
+            float dg2[2], du2[2], hw2[2];
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+              const float gg = t ? bf16hi(gw) : bf16lo(gw);
+              const float uu = t ? bf16hi(uw) : bf16lo(uw);
+              const float ac = __uint_as_float(acc[8 * q + 2 * i + t]);
+              const float s = sigmoid_f(gg);
+              const float sl = gg * s;
+              const float hh = sl * uu;
+              dwp = fmaf(ac, hh, dwp);
+              const float dh = wt * ac;
+              dg2[t] = dh * uu * s * (1.0f + gg * (1.0f - s));
+              du2[t] = dh * sl;
+              hw2[t] = wt * hh;
+            }
+            pdg[i] = pack_bf16x2(dg2[0], dg2[1]);
+            pdu[i] = pack_bf16x2(du2[0], du2[1]);
+            phw[i] = pack_bf16x2(hw2[0], hw2[1]);
+          }
+        }
+        const int pc = 4 * h + q;
+        if (warp_full) {
+          put128(bdg, w.lane, pc, pdg[0], pdg[1], pdg[2], pdg[3]);
+          put128(bdu, w.lane, pc, pdu[0], pdu[1], pdu[2], pdu[3]);
+          put128(bhw, w.lane, pc, phw[0], phw[1], phw[2], phw[3]);
+        } else if (valid || pad_row) {
+          const int col = j + 8 * pc;
+          st_global_16(a.dgu_out + p * (2LL * I) + col, pdg[0], pdg[1], pdg[2], pdg[3]);
+          st_global_16(a.dgu_out + p * (2LL * I) + I + col, pdu[0], pdu[1], pdu[2], pdu[3]);
+          st_global_16(a.hw_out + p * (long long)I + col, phw[0], phw[1], phw[2], phw[3]);
+        }
       }
-    } else {
+      if (more) {
 #pragma unroll
-      for (int i = 0; i < 32; ++i) g[i] = u[i] = acc[i] = 0.f;
+        for (int q = 0; q < 4; ++q) { gs[q] = gn[q]; us[q] = un[q]; }
+      }
     }
     if (warp_full) {
-      stage_store(w, stage_row(w, g), tmD0, j, y, 0, false);
-      stage_store(w, stage_row(w, u), tmD0, I + j, y, 0, false);
-      stage_store(w, stage_row(w, acc), tmD1, j, y, 0, false);
-    } else if (valid || pad_row) {
-      store_row_chunk_bf16<C>(a.dgu_out + p * (2LL * I) + j, g);
-      store_row_chunk_bf16<C>(a.dgu_out + p * (2LL * I) + I + j, u);
-      store_row_chunk_bf16<C>(a.hw_out + p * (long long)I + j, acc);
+      stage_store(w, bdg, tmD0, j, y, 0, false);
+      stage_store(w, bdu, tmD0, I + j, y, 0, false);
+      stage_store(w, bhw, tmD1, j, y, 0, false);
     }
   }
   if (a.dw_part && (valid || pad_row)) a.dw_part[p * npart_cols + ti.nb * nparts + cpart] = dwp;
@@ -483,6 +571,21 @@ __device__ __forceinline__ int next_work_tile(const GemmArgs& a, const SmemTable
     if (out.kblocks > 0) return t;
   }
   return total;
+}
+
+// This warp's copies into a gathered stage are complete (each thread has
+// waited for its own and fenced them to the async proxy): one arrival per warp
+// on the stage's full barrier; with PAIR the even CTA's, whose thread issues
+// the UMMAs.  The copies sit in this SM's shared memory, which the pair UMMA
+// reads on this SM, so the arrival needs no cluster-scope release (one would
+// also wait for the copies of later stages still in flight).
+template <class C>
+__device__ __forceinline__ void arrive_full(uint64_t* full_bar, uint32_t stage, int lane, int rank) {
+  __syncwarp();
+  if (lane == 0) {
+    if (C::PAIR && rank != 0) mbar_arrive_remote(mapa_shared(smem_u32(&full_bar[stage]), 0));
+    else mbar_arrive(smem_u32(&full_bar[stage]));
+  }
 }
 
 // The gather warps walk the same (tile, k-block) sequence as the TMA producer.
@@ -567,7 +670,7 @@ __device__ void gather_role(const GemmArgs& a, const SmemTables& T, uint32_t sme
     if (rn > LAG) {
       cp_async_wait<LAG>();
       fence_proxy_async_smem();
-      mbar_arrive(smem_u32(&full_bar[ring & 15u]));
+      arrive_full<C>(full_bar, ring & 15u, lane, rank);
       ring >>= 4;
       --rn;
     }
@@ -588,7 +691,7 @@ __device__ void gather_role(const GemmArgs& a, const SmemTables& T, uint32_t sme
   cp_async_wait<0>();
   fence_proxy_async_smem();
   while (rn > 0) {
-    mbar_arrive(smem_u32(&full_bar[ring & 15u]));
+    arrive_full<C>(full_bar, ring & 15u, lane, rank);
     ring >>= 4;
     --rn;
   }
@@ -620,11 +723,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(smem_u32(&full_bar[s]), C::FULL_ARRIVALS);
-      mbar_init(smem_u32(&empty_bar[s]), C::CL);
+      // MC: both CTAs' UMMA commits release a stage; PAIR: the even CTA's alone
+      mbar_init(smem_u32(&empty_bar[s]), C::MC ? 2 : 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&tfull_bar[b]), 1);
-      mbar_init(smem_u32(&tempty_bar[b]), 32 * C::EPI_WARPS);
+      mbar_init(smem_u32(&tempty_bar[b]), C::TEMPTY_ARRIVALS);
     }
     mbar_init(smem_u32(&drain_bar), 1);
     T.abort_flag = 0;
@@ -639,8 +743,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     }
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(&T.tmem_base), kTmemCols);
-    tmem_relinquish();
+    if constexpr (C::PAIR) {
+      tmem_alloc_pair(smem_u32(&T.tmem_base), kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(&T.tmem_base), kTmemCols);
+      tmem_relinquish();
+    }
   }
   if (warp == 2) {
     // group tables (one warp; G <= 256)
@@ -695,12 +804,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     }
   }
   tc_fence_before();
-  if constexpr (C::MC) cluster_sync();  // the peer's barriers are initialised before any remote op
+  if constexpr (C::CL == 2) cluster_sync();  // the peer's barriers are initialised before any remote op
   else __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = T.tmem_base;
   const int total = T.total_tiles;
-  const int rank = C::MC ? (int)cluster_ctarank() : 0;
+  const int rank = C::CL == 2 ? (int)cluster_ctarank() : 0;
+  const bool leader = rank == 0;  // PAIR: the CTA whose thread issues the pair's UMMAs
   const int unit0 = blockIdx.x / C::CL;
   const int ustep = gridDim.x / C::CL;
   constexpr uint16_t kPair = 0x3;
@@ -718,11 +828,14 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       for (int kb = 0; kb < ti.kblocks; ++kb) {
         if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1, abort_flag, a.status)) { ok = false; break; }
         const uint32_t fb = smem_u32(&full_bar[stage]);
+        const uint32_t fbp = C::PAIR ? mapa_shared(fb, 0) : fb;  // barrier the copies complete on
         const uint32_t sA = smem_base + stage * C::STAGE_BYTES;
         const uint32_t sB = sA + C::A_BYTES;
-        if (lane == 0) mbar_arrive_expect_tx(fb, C::TMA_BYTES);
-        filled |= 1u << stage;
-        fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
+        if (!C::PAIR || leader) {
+          if (lane == 0) mbar_arrive_expect_tx(fb, C::FULL_TX);
+          filled |= 1u << stage;
+          fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
+        }
         __syncwarp();
         const int kc = kb * BK;               // K coordinate inside the group
         const int kr = ti.kstart + kc;        // absolute K coordinate (RAGGED_K)
@@ -731,15 +844,40 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         if constexpr (C::A_GATHER) {
           // A comes from the gather warps
         } else if constexpr (C::AL == KMAJ_TILE) {
-          if (lane == 0) tma_load_2d(sA, &tmA, fb, kx, C::SCH == RAGGED_K ? m0 : ti.row0);
+          if (lane == 0) {
+            if constexpr (C::PAIR) tma_load_2d_pair(sA, &tmA, fbp, kx, C::SCH == RAGGED_K ? m0 : ti.row0);
+            else tma_load_2d(sA, &tmA, fb, kx, C::SCH == RAGGED_K ? m0 : ti.row0);
+          }
         } else {  // MN_TILE: two 64-wide groups along M, 64 k-rows each
           if (lane == 0) {
-            tma_load_2d(sA, &tmA, fb, m0, kr);
-            tma_load_2d(sA + 8192, &tmA, fb, m0 + 64, kr);
+            if constexpr (C::PAIR) {
+              tma_load_2d_pair(sA, &tmA, fbp, m0, kr);
+              tma_load_2d_pair(sA + 8192, &tmA, fbp, m0 + 64, kr);
+            } else {
+              tma_load_2d(sA, &tmA, fb, m0, kr);
+              tma_load_2d(sA + 8192, &tmA, fb, m0 + 64, kr);
+            }
           }
         }
         // ---- B
-        if constexpr (C::BL == KMAJ_TILE) {
+        if constexpr (C::PAIR && C::BL == KMAJ_TILE) {
+          // this CTA's half of the B tile: 128 rows (SwiGLU: rank 0 gate, rank 1 up)
+          if (lane == 0) {
+            const int nc = C::SWIGLU_B ? (rank == 0 ? n0 : a.inter + n0) : n0 + rank * 128;
+            if constexpr (C::B3D) tma_load_3d_pair(sB, &tmB, fbp, kc, nc, ti.g);
+            else tma_load_2d_pair(sB, &tmB, fbp, kx, nc);
+          }
+        } else if constexpr (C::PAIR && C::BL == MN_TILE) {
+          // this CTA's half: two 64-wide N groups
+          if (lane == 0) {
+#pragma unroll
+            for (int b = 0; b < 2; ++b) {
+              const int nc = n0 + 128 * rank + 64 * b;
+              if constexpr (C::B3D) tma_load_3d_pair(sB + b * 8192, &tmB, fbp, nc, kc, ti.g);
+              else tma_load_2d_pair(sB + b * 8192, &tmB, fbp, nc, kr);
+            }
+          }
+        } else if constexpr (C::BL == KMAJ_TILE) {
           if (lane == 0) {
 #pragma unroll
             for (int b = 0; b < C::B_NBOX; ++b) {
@@ -797,7 +935,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     uint32_t phase = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int t = unit0; t < total && !*abort_flag; t += ustep) {
+    // with PAIR the odd CTA issues nothing: the even CTA's UMMAs cover both
+    for (int t = unit0; t < total && !*abort_flag && (!C::PAIR || leader); t += ustep) {
       const TileInfo ti = decode_tile<C>(a, T, t, rank);
       if (!mbar_wait(smem_u32(&tempty_bar[acc]), acc_phase ^ 1, abort_flag, a.status)) break;
       tc_fence_after();
@@ -815,9 +954,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                                         : smem_desc_sw128(sA + kk * 32, 16, 1024);
             const uint64_t bd = C::B_MN ? smem_desc_sw128(sB + kk * 2048, 8192, 1024)
                                         : smem_desc_sw128(sB + kk * 32, 16, 1024);
-            umma_bf16(d_tmem, ad, bd, C::IDESC, (kb | kk) != 0 ? 1u : 0u);
+            if constexpr (C::PAIR) umma_bf16_pair(d_tmem, ad, bd, C::IDESC, (kb | kk) != 0 ? 1u : 0u);
+            else umma_bf16(d_tmem, ad, bd, C::IDESC, (kb | kk) != 0 ? 1u : 0u);
           }
-          if constexpr (C::MC) umma_commit_mc(smem_u32(&empty_bar[stage]), kPair);
+          if constexpr (C::PAIR) umma_commit_pair(smem_u32(&empty_bar[stage]));
+          else if constexpr (C::MC) umma_commit_mc(smem_u32(&empty_bar[stage]), kPair);
           else umma_commit(smem_u32(&empty_bar[stage]));
         }
         __syncwarp();
@@ -825,16 +966,25 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       }
       if (!ok) break;
       if (lane == 0) {
-        if (ti.kblocks > 0) umma_commit(smem_u32(&tfull_bar[acc]));
-        else mbar_arrive(smem_u32(&tfull_bar[acc]));
+        if constexpr (C::PAIR) {
+          if (ti.kblocks > 0) umma_commit_pair(smem_u32(&tfull_bar[acc]));
+          else {
+            mbar_arrive(smem_u32(&tfull_bar[acc]));
+            mbar_arrive_remote(mapa_shared(smem_u32(&tfull_bar[acc]), 1));
+          }
+        } else {
+          if (ti.kblocks > 0) umma_commit(smem_u32(&tfull_bar[acc]));
+          else mbar_arrive(smem_u32(&tfull_bar[acc]));
+        }
       }
       __syncwarp();
       if (++acc == 2) { acc = 0; acc_phase ^= 1; }
     }
-    if (*abort_flag) {
+    if (*abort_flag && (!C::PAIR || leader)) {
       // wait (bounded) for UMMAs already issued before TMEM is released
       if (lane == 0) {
-        umma_commit(smem_u32(&drain_bar));
+        if constexpr (C::PAIR) umma_commit_pair(smem_u32(&drain_bar));
+        else umma_commit(smem_u32(&drain_bar));
         const unsigned long long t0 = globaltimer();
         while (!mbar_try_wait(smem_u32(&drain_bar), 0) && globaltimer() - t0 < 20000000ull) {
         }
@@ -852,8 +1002,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     const int cpart = epi >> 2;                // column part of this warp
     constexpr int nparts = C::EPI_WARPS / 4;
     const int row_in_tile = quad * 32 + lane;
-    WarpOut wo;
-    wo.buf0 = smem_base + C::STAGES * C::STAGE_BYTES + epi * (kStagesPerWarp * kStageBytes);
+    WarpOut<C::EPI_BUFS, C::EPI_BUF_BYTES> wo;
+    wo.buf0 = smem_base + C::STAGES * C::STAGE_BYTES + epi * (C::EPI_BUFS * C::EPI_BUF_BYTES);
     wo.lane = lane;
     wo.next = 0;
     wo.inflight = 0;
@@ -874,8 +1024,14 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         epilogue_store<C>(a, ti, tacc, row_in_tile, wo, &tmD0, cpart, nparts);
       else
         epilogue_dgrad_swiglu<C>(a, T, ti, tacc, row_in_tile, wo, &tmD0, &tmD1, cpart, nparts);
+      // the accumulator's TMEM has been read: one arrival per warp (PAIR: on the
+      // even CTA's barrier, whose thread overwrites both CTAs' accumulators)
       tc_fence_before();
-      mbar_arrive(smem_u32(&tempty_bar[acc]));
+      __syncwarp();
+      if (lane == 0) {
+        if constexpr (C::PAIR) mbar_arrive_remote(mapa_shared(smem_u32(&tempty_bar[acc]), 0));
+        else mbar_arrive(smem_u32(&tempty_bar[acc]));
+      }
       if (++acc == 2) { acc = 0; acc_phase ^= 1; }
     }
     // every TMA store must have completed before the CTA exits
@@ -884,11 +1040,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   }
 
   tc_fence_before();
-  if constexpr (C::MC) cluster_sync();  // no CTA leaves while its peer may still write to it
+  if constexpr (C::CL == 2) cluster_sync();  // no CTA leaves while its peer may still write to it
   else __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
+    if constexpr (C::PAIR) tmem_dealloc_pair(tmem_base, kTmemCols);
+    else tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 

@@ -232,22 +232,25 @@ using moe::RAGGED_M;
 template <int BN>
 using CfgRouter =
     GemmCfg<BN, (BN >= 256 ? 4 : 6), KMAJ_TILE, KMAJ_TILE, RAGGED_K, EPI_STORE_F32, false, false>;
-// Every BN=256 GEMM runs as 2-CTA clusters sharing the B tile by TMA multicast.
-constexpr bool kMC = true;
-using CfgGateUp = GemmCfg<256, 4, KMAJ_GATHER, KMAJ_TILE, RAGGED_M, EPI_SWIGLU, true, true, 4, kMC>;
-using CfgGateUpShared =
-    GemmCfg<256, 4, KMAJ_TILE, KMAJ_TILE, RAGGED_M, EPI_SWIGLU, false, true, 4, kMC>;
-using CfgDown = GemmCfg<256, 4, KMAJ_TILE, KMAJ_TILE, RAGGED_M, EPI_STORE, true, false, 4, kMC>;
-using CfgDownShared = GemmCfg<256, 4, KMAJ_TILE, KMAJ_TILE, RAGGED_M, EPI_STORE, false, false, 4, kMC>;
-using CfgDgradDown = GemmCfg<256, 4, KMAJ_GATHER, MN_TILE, RAGGED_M, EPI_DGRAD_SWIGLU, true, false,
-                             4 * kDwParts, kMC>;
-using CfgDgradDownShared =
-    GemmCfg<256, 4, KMAJ_TILE, MN_TILE, RAGGED_M, EPI_DGRAD_SWIGLU, false, false, 4, kMC>;
-using CfgDgradGateUp = GemmCfg<256, 4, KMAJ_TILE, MN_TILE, RAGGED_M, EPI_STORE, true, false, 4, kMC>;
-using CfgDgradGateUpShared =
-    GemmCfg<256, 4, KMAJ_TILE, MN_TILE, RAGGED_M, EPI_STORE, false, false, 4, kMC>;
-using CfgWgrad = GemmCfg<256, 4, MN_TILE, MN_TILE, RAGGED_K, EPI_STORE, false, false, 4, kMC>;
-using CfgWgradDown = GemmCfg<256, 4, MN_GATHER, MN_TILE, RAGGED_K, EPI_STORE, false, false, 4, kMC>;
+// Every BN=256 GEMM runs as CTA pairs: 256 x 256 tiles by cta_group::2 UMMAs,
+// each CTA staging its 128 A rows and half of the B tile (32 KB per stage).
+// The ragged-M GEMMs stream K = 768..2048 per tile through 5 stages with 3
+// epilogue store buffers (4 KB) per warp; the weight-gradient GEMMs (K = one
+// expert's tokens, output-dominated traffic) use 4 stages and 5 buffers.
+template <int STAGES, int AL, int BL, int SCH, int EPI, bool B3D, bool SWIGLU_B, int EPI_WARPS = 4,
+          int EPI_BUFS = 3>
+using PairCfg = GemmCfg<256, STAGES, AL, BL, SCH, EPI, B3D, SWIGLU_B, EPI_WARPS, false, true, EPI_BUFS>;
+using CfgGateUp = PairCfg<5, KMAJ_GATHER, KMAJ_TILE, RAGGED_M, EPI_SWIGLU, true, true>;
+using CfgGateUpShared = PairCfg<5, KMAJ_TILE, KMAJ_TILE, RAGGED_M, EPI_SWIGLU, false, true>;
+using CfgDown = PairCfg<5, KMAJ_TILE, KMAJ_TILE, RAGGED_M, EPI_STORE, true, false>;
+using CfgDownShared = PairCfg<5, KMAJ_TILE, KMAJ_TILE, RAGGED_M, EPI_STORE, false, false>;
+using CfgDgradDown =
+    PairCfg<5, KMAJ_GATHER, MN_TILE, RAGGED_M, EPI_DGRAD_SWIGLU, true, false, 4 * kDwParts>;
+using CfgDgradDownShared = PairCfg<5, KMAJ_TILE, MN_TILE, RAGGED_M, EPI_DGRAD_SWIGLU, false, false>;
+using CfgDgradGateUp = PairCfg<5, KMAJ_TILE, MN_TILE, RAGGED_M, EPI_STORE, true, false>;
+using CfgDgradGateUpShared = PairCfg<5, KMAJ_TILE, MN_TILE, RAGGED_M, EPI_STORE, false, false>;
+using CfgWgrad = PairCfg<4, MN_TILE, MN_TILE, RAGGED_K, EPI_STORE, false, false, 4, 5>;
+using CfgWgradDown = PairCfg<4, MN_GATHER, MN_TILE, RAGGED_K, EPI_STORE, false, false, 4, 5>;
 
 // fp32 [depth][rows][inner] output map with 16x32 boxes (64-byte rows).
 bool make_out_map3_f32(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows,
@@ -263,12 +266,12 @@ bool make_out_map3_f32(CUtensorMap* m, const void* base, uint64_t inner, uint64_
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Output (store) maps use 32x32 boxes.
+// bf16 output (store) maps: 64-column x 32-row boxes, 128-byte swizzle.
 bool make_out_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows) {
-  return make_map(m, base, inner, rows, 1, 32, 32);
+  return make_map(m, base, inner, rows, 1, 64, 32);
 }
 bool make_out_map3(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t depth) {
-  return make_map3(m, base, inner, rows, depth, 32, 32);
+  return make_map3(m, base, inner, rows, depth, 64, 32);
 }
 
 template <class C>
@@ -286,7 +289,7 @@ moe_status launch_gemm(int kid, const CUtensorMap& A, const CUtensorMap& B, cons
       return MOE_ERR_CUDA;
     configured.fetch_or(bit);
   }
-  if constexpr (C::MC) {
+  if constexpr (C::CL == 2) {
     // 2-CTA clusters; as many as can be resident at once (one CTA per SM)
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -579,7 +582,7 @@ moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int* status = at<int>(workspace, 0);
   const int T = d->T, H = d->H, E = d->E, I = d->I, k = d->k;
-  const long long S = L.S, P = L.S_pad_max;
+  const long long P = L.S_pad_max;
   int32_t* poff = at<int32_t>(workspace, L.poff);
   __nv_bfloat16* dgu = at<__nv_bfloat16>(workspace, L.dgu);
   __nv_bfloat16* hw = at<__nv_bfloat16>(workspace, L.hw);

@@ -55,6 +55,7 @@ struct GemmArgs {
   const int32_t* offsets;  // [G+1] row offsets (unpadded); nullptr: one group
   int single_rows;       // rows of the one group when offsets == nullptr
   int ksplit;            // RAGGED_K without offsets: group g = K rows [g*ksplit, (g+1)*ksplit)
+  int kres;              // RAGGED_K: groups with at most kres rows are left to the resident kernel
   int padded;            // 1: groups start on 128-row boundaries of a padded row space
   // gathered operand: row i of group g reads gsrc[gperm[off_g + min(i, n_g-1)] / gdiv]
   const __nv_bfloat16* gsrc; long long gld; const int32_t* gperm; int gdiv; int gsrc_rows;
@@ -152,6 +153,59 @@ struct SmemTables {
   uint32_t tmem_base;
 };
 
+// Group tables (one warp; G <= 256): rows and offsets of every group, its
+// start in the (padded or not) row space, and the prefix sums of its work units
+// (units(cnt) for a group of cnt rows).  CTA 0 optionally publishes the starts.
+template <class UnitsFn>
+__device__ __forceinline__ void build_group_tables(const GemmArgs& a, SmemTables& T, int lane,
+                                                   UnitsFn units) {
+  int run_tiles = 0, run_rows = 0;
+  for (int base = 0; base < a.G; base += 32) {
+    const int g = base + lane;
+    int cnt = 0, off = 0;
+    if (g < a.G) {
+      if (a.offsets) {
+        off = __ldg(a.offsets + g);
+        cnt = __ldg(a.offsets + g + 1) - off;
+      } else if (a.ksplit > 0) {
+        off = g * a.ksplit;
+        cnt = min(a.ksplit, a.K - off);
+      } else {
+        cnt = a.single_rows;
+      }
+      if (cnt < 0) cnt = 0;
+    }
+    const int mt = (cnt + BM - 1) / BM;
+    // lanes past the last group contribute nothing (no units, no rows)
+    const int tiles = (g >= a.G) ? 0 : units(cnt);
+    const int rows = a.padded ? mt * BM : cnt;
+    int ti = tiles, ro = rows;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int x = __shfl_up_sync(0xffffffffu, ti, d);
+      const int y = __shfl_up_sync(0xffffffffu, ro, d);
+      if (lane >= d) { ti += x; ro += y; }
+    }
+    if (g < a.G) {
+      T.tile_prefix[g] = run_tiles + ti - tiles;
+      T.start[g] = a.padded ? run_rows + ro - rows : off;
+      T.cnt[g] = cnt;
+      T.off[g] = off;
+    }
+    run_tiles += __shfl_sync(0xffffffffu, ti, 31);
+    run_rows += __shfl_sync(0xffffffffu, ro, 31);
+  }
+  if (lane == 0) {
+    T.tile_prefix[a.G] = run_tiles;
+    T.total_tiles = run_tiles;
+  }
+  if (a.poff_out && blockIdx.x == 0) {
+    __syncwarp();
+    for (int g = lane; g < a.G; g += 32) a.poff_out[g] = T.start[g];
+    if (lane == 0) a.poff_out[a.G] = run_rows;
+  }
+}
+
 template <class C>
 __device__ __forceinline__ int num_nblocks(const GemmArgs& a) {
   if (C::SWIGLU_B) return (a.inter + C::BN / 2 - 1) / (C::BN / 2);
@@ -184,11 +238,16 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, const SmemTab
     ti.kstart = 0;
     ti.kblocks = a.K / BK;
   } else {
+    // groups own contiguous unit ranges (none for a group left to the resident kernel)
     const int nMB = (a.M + BM - 1) / BM;
     const int mu = (nMB + C::CL - 1) / C::CL;
-    const int per = mu * nNB;
-    ti.g = min(t / per, a.G - 1);
-    const int local = t - ti.g * per;
+    int lo = 0, hi = a.G - 1;
+    while (lo < hi) {
+      int mid = (lo + hi + 1) >> 1;
+      if (T.tile_prefix[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    ti.g = lo;
+    const int local = t - T.tile_prefix[lo];
     ti.nb = local / mu;
     ti.mb = (local - ti.nb * mu) * C::CL + rank;
     ti.phantom = ti.mb >= nMB;
@@ -656,12 +715,16 @@ __device__ void gather_role(const GemmArgs& a, const SmemTables& T, uint32_t sme
       const int cc = lane % CPR;
       const int j = cc >> 3, c = cc & 7;
       const __nv_bfloat16* col = a.gsrc + mn0 + j * 64 + c * 8;
+      // extents are multiples of 64: a 64-wide group past the row is not copied
+      // (its rows or columns are not stored)
+      const bool inside = mn0 + j * 64 < (C::A_GATHER ? a.M : a.N);
 #pragma unroll
       for (int q = 0; q < 16 / RPI; ++q) {
         const int rl = q * RPI + lane / CPR;  // 0..15 within this warp's k-rows
         const int r = gw * 16 + rl;
         const int srow = __shfl_sync(0xffffffffu, kid, rl);
-        cp_async_16(sOp + j * 8192 + r * 128 + ((c ^ (r & 7)) << 4), col + (size_t)srow * a.gld);
+        if (inside)
+          cp_async_16(sOp + j * 8192 + r * 128 + ((c ^ (r & 7)) << 4), col + (size_t)srow * a.gld);
       }
     }
     cp_async_commit();
@@ -752,56 +815,17 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     }
   }
   if (warp == 2) {
-    // group tables (one warp; G <= 256)
     const int nNB = num_nblocks<C>(a);
     const int nMB = (a.M + BM - 1) / BM;
-    int run_tiles = 0, run_rows = 0;
-    for (int base = 0; base < a.G; base += 32) {
-      const int g = base + lane;
-      int cnt = 0, off = 0;
-      if (g < a.G) {
-        if (a.offsets) {
-          off = __ldg(a.offsets + g);
-          cnt = __ldg(a.offsets + g + 1) - off;
-        } else if (a.ksplit > 0) {
-          off = g * a.ksplit;
-          cnt = min(a.ksplit, a.K - off);
-        } else {
-          cnt = a.single_rows;
-        }
-        if (cnt < 0) cnt = 0;
-      }
+    build_group_tables(a, T, lane, [&](int cnt) {
+      // work units of this group (tiles, or m-block pairs with CTA pairs); a
+      // weight-gradient launch that leaves experts with at most kres rows to
+      // the resident-operand kernel gives them none
+      if (C::SCH == RAGGED_K && a.kres > 0 && cnt <= a.kres) return 0;
       const int mt = (cnt + BM - 1) / BM;
-      // work units of this group (tiles, or m-block pairs with MC); lanes past
-      // the last group contribute nothing (no units, no rows)
       const int mu = ((C::SCH == RAGGED_M ? mt : nMB) + C::CL - 1) / C::CL;
-      const int tiles = (g >= a.G) ? 0 : mu * nNB;
-      const int rows = a.padded ? mt * BM : cnt;
-      int ti = tiles, ro = rows;
-#pragma unroll
-      for (int d = 1; d < 32; d <<= 1) {
-        const int x = __shfl_up_sync(0xffffffffu, ti, d);
-        const int y = __shfl_up_sync(0xffffffffu, ro, d);
-        if (lane >= d) { ti += x; ro += y; }
-      }
-      if (g < a.G) {
-        T.tile_prefix[g] = run_tiles + ti - tiles;
-        T.start[g] = a.padded ? run_rows + ro - rows : off;
-        T.cnt[g] = cnt;
-        T.off[g] = off;
-      }
-      run_tiles += __shfl_sync(0xffffffffu, ti, 31);
-      run_rows += __shfl_sync(0xffffffffu, ro, 31);
-    }
-    if (lane == 0) {
-      T.tile_prefix[a.G] = run_tiles;
-      T.total_tiles = run_tiles;
-    }
-    if (a.poff_out && blockIdx.x == 0) {
-      __syncwarp();
-      for (int g = lane; g < a.G; g += 32) a.poff_out[g] = T.start[g];
-      if (lane == 0) a.poff_out[a.G] = run_rows;
-    }
+      return mu * nNB;
+    });
   }
   tc_fence_before();
   if constexpr (C::CL == 2) cluster_sync();  // the peer's barriers are initialised before any remote op

@@ -1,0 +1,423 @@
+// Weight-gradient GEMM with one operand resident in shared memory.
+//
+//   D_g[m, n] = sum over the expert's K token rows k of A_g[k, m] B_g[k, n]
+//
+// (dW_gu[e] = [dg|du]^T x, dW_down[e] = dout^T (w h): both operands are read
+// MN-major from row-per-token matrices.)  The streaming weight-gradient GEMM
+// re-reads both operands for every 256 x 256 output tile although an expert
+// has only K ~ 256 rows, so each SM pulls 128 KB from L2 per 1 us tile and the
+// mainloop is bound by that ingress.  Here, for an expert with K <= 256, one
+// operand's whole K slice (4 k-blocks x 16 KB per CTA) stays in shared memory
+// for a work unit that runs every tile along the other output dimension,
+// streaming only the other operand:
+//   RES_A: unit = (expert, m-block pair), A resident, tiles = the n-blocks,
+//          B streamed by TMA;
+//   RES_B: unit = (expert, n-block), B resident, tiles = the m-block pairs,
+//          A streamed by TMA or gathered from token rows by the LSU warps.
+// Experts with more rows are left to the streaming kernel (GemmArgs::kres).
+//
+// CTA pairs as in the streaming kernel (cta_group::2, 256 x 256 tiles): each
+// CTA holds its own 128 rows of A and half of the B columns; the even CTA
+// issues the UMMAs.  Roles:
+//   warp 0      streamed-operand TMA producer (idle when A is gathered)
+//   warp 1      TMEM allocator; UMMA issuer in the even CTA
+//   warps 2..5  epilogue (the streaming kernel's bf16 store epilogue)
+//   warps 6..9  gather warps (gathered A only)
+//   last warp   resident-operand TMA loader: refills k-block slot kb as soon
+//               as the unit's last UMMA reading it has completed
+#pragma once
+#include "gemm.cuh"
+
+namespace moe {
+
+enum ResMode : int { RES_A = 1, RES_B = 2 };
+
+template <int RES_, int AL_, int STAGES_, int EPI_BUFS_>
+struct ResCfg {
+  static constexpr int RES = RES_;
+  static constexpr int AL = AL_;          // MN_TILE or (RES_B only) MN_GATHER
+  static constexpr int BL = MN_TILE;
+  static constexpr int BN = 256;
+  static constexpr int CL = 2;
+  static constexpr bool PAIR = true;
+  static constexpr bool MC = false;
+  static constexpr bool SWIGLU_B = false;
+  static constexpr int SCH = RAGGED_K;
+  static constexpr int EPI = EPI_STORE;
+  static constexpr int EPI_WARPS = 4;
+  static constexpr int EPI_BUFS = EPI_BUFS_;
+  static constexpr int EPI_BUF_BYTES = 4096;
+  static constexpr bool A_GATHER = AL == MN_GATHER;
+  static constexpr bool GATHER = A_GATHER;
+  static_assert(AL == MN_TILE || AL == MN_GATHER, "weight-gradient operands are MN-major");
+  static_assert(!(RES == RES_A && A_GATHER), "the resident operand is loaded by TMA");
+  static constexpr int GATHER_WARPS = GATHER ? 4 : 0;
+  static constexpr int RES_WARP = 2 + EPI_WARPS + GATHER_WARPS;
+  static constexpr int THREADS = 32 * (RES_WARP + 1);
+  static constexpr int STAGES = STAGES_;
+  static constexpr int GATHER_LAG = STAGES - 2;
+  static_assert(!GATHER || GATHER_LAG >= 1, "gathers need >= 3 stages");
+  static constexpr int BLK = BM * BK * 2;  // one operand's 128 x 64 block of a CTA: 16 KB
+  static constexpr int RSLOTS = 4;         // resident k-blocks
+  static constexpr int KRES = RSLOTS * BK;  // experts with at most 256 rows
+  static constexpr uint32_t IDESC = idesc_bf16_f32(2 * BM, BN, true, true);
+  // the even CTA's full barriers: both CTAs' streamed bytes, or one arrival per gather warp
+  static constexpr uint32_t FULL_TX = GATHER ? 0 : 2 * BLK;
+  static constexpr uint32_t FULL_ARRIVALS = GATHER ? 2 * GATHER_WARPS : 1;
+  static constexpr uint32_t TEMPTY_ARRIVALS = 2 * EPI_WARPS;
+  static constexpr int SMEM_BYTES =
+      (STAGES + RSLOTS) * BLK + EPI_WARPS * EPI_BUFS * EPI_BUF_BYTES + 1024;
+  static_assert(SMEM_BYTES <= 227 * 1024 - 8 * 1024, "dynamic + static shared memory per CTA");
+};
+
+struct ResUnit {
+  int g, outer, ntiles, kstart, kblocks;
+};
+
+template <class C>
+__device__ __forceinline__ int res_nmb(const GemmArgs& a) { return (a.M + BM - 1) / BM; }
+template <class C>
+__device__ __forceinline__ int res_nnb(const GemmArgs& a) { return (a.N + C::BN - 1) / C::BN; }
+
+template <class C>
+__device__ __forceinline__ ResUnit res_unit(const GemmArgs& a, const SmemTables& T, int t) {
+  int lo = 0, hi = a.G - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (T.tile_prefix[mid] <= t) lo = mid; else hi = mid - 1;
+  }
+  ResUnit u;
+  u.g = lo;
+  u.outer = t - T.tile_prefix[lo];
+  u.ntiles = C::RES == RES_A ? res_nnb<C>(a) : (res_nmb<C>(a) + 1) / 2;
+  u.kstart = T.start[lo];
+  u.kblocks = (T.cnt[lo] + BK - 1) / BK;
+  return u;
+}
+
+template <class C>
+__device__ __forceinline__ TileInfo res_tile(const GemmArgs& a, const ResUnit& u, int j, int rank) {
+  TileInfo ti;
+  const int p = C::RES == RES_A ? u.outer : j;
+  ti.g = u.g;
+  ti.nb = C::RES == RES_A ? j : u.outer;
+  ti.mb = 2 * p + rank;
+  const int nMB = res_nmb<C>(a);
+  ti.phantom = ti.mb >= nMB;
+  ti.row0 = ti.mb * BM;
+  ti.rows_valid = ti.phantom ? 0 : min(BM, a.M - ti.mb * BM);
+  ti.kstart = u.kstart;
+  ti.kblocks = u.kblocks;
+  return ti;
+}
+
+// MN-major block of an operand (two 64-wide groups of 64 k-rows) by TMA, to
+// this CTA's shared memory, completing on the even CTA's barrier `barp`.
+__device__ __forceinline__ void res_load_block(uint32_t dst, const CUtensorMap* map, uint32_t barp,
+                                               int x, int k) {
+  tma_load_2d_pair(dst, map, barp, x, k);
+  tma_load_2d_pair(dst + 8192, map, barp, x + 64, k);
+}
+
+template <class C>
+__global__ void __launch_bounds__(C::THREADS, 1)
+    res_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                    const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmD0,
+                    const __grid_constant__ CUtensorMap tmD1, const GemmArgs a) {
+  (void)tmD1;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full_bar[C::STAGES];
+  __shared__ __align__(8) uint64_t empty_bar[C::STAGES];
+  __shared__ __align__(8) uint64_t rfull_bar[C::RSLOTS];
+  __shared__ __align__(8) uint64_t rempty_bar[C::RSLOTS];
+  __shared__ __align__(8) uint64_t tfull_bar[2];
+  __shared__ __align__(8) uint64_t tempty_bar[2];
+  __shared__ __align__(8) uint64_t drain_bar;
+  __shared__ SmemTables T;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t smem_base = smem_u32(smem);
+  const uint32_t res_base = smem_base + C::STAGES * C::BLK;
+  volatile int* abort_flag = &T.abort_flag;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(smem_u32(&full_bar[s]), C::FULL_ARRIVALS);
+      mbar_init(smem_u32(&empty_bar[s]), 1);
+    }
+    for (int s = 0; s < C::RSLOTS; ++s) {
+      mbar_init(smem_u32(&rfull_bar[s]), 1);
+      mbar_init(smem_u32(&rempty_bar[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&tfull_bar[b]), 1);
+      mbar_init(smem_u32(&tempty_bar[b]), C::TEMPTY_ARRIVALS);
+    }
+    mbar_init(smem_u32(&drain_bar), 1);
+    T.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmD0);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(&T.tmem_base), kTmemCols);
+    tmem_relinquish_pair();
+  }
+  if (warp == 2) {
+    const int nMB = res_nmb<C>(a), nNB = res_nnb<C>(a);
+    build_group_tables(a, T, lane, [&](int cnt) {
+      if (cnt > C::KRES) return 0;  // left to the streaming kernel
+      return C::RES == RES_A ? (nMB + 1) / 2 : nNB;
+    });
+  }
+  tc_fence_before();
+  cluster_sync();  // the peer's barriers are initialised before any remote op
+  tc_fence_after();
+  const uint32_t tmem_base = T.tmem_base;
+  const int total = T.total_tiles;
+  const int rank = (int)cluster_ctarank();
+  const bool leader = rank == 0;
+  const int unit0 = blockIdx.x / 2;
+  const int ustep = gridDim.x / 2;
+
+  if (warp == 0) {
+    // ================= streamed-operand producer =================
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t filled = 0, fill_parity = 0;
+    for (int t = unit0; t < total && !*abort_flag && !C::GATHER; t += ustep) {
+      const ResUnit u = res_unit<C>(a, T, t);
+      bool ok = true;
+      for (int j = 0; j < u.ntiles && ok; ++j) {
+        const TileInfo ti = res_tile<C>(a, u, j, rank);
+        for (int kb = 0; kb < u.kblocks; ++kb) {
+          if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1, abort_flag, a.status)) { ok = false; break; }
+          const uint32_t fb = smem_u32(&full_bar[stage]);
+          const uint32_t sS = smem_base + stage * C::BLK;
+          if (leader) {
+            if (lane == 0) mbar_arrive_expect_tx(fb, C::FULL_TX);
+            filled |= 1u << stage;
+            fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
+          }
+          if (lane == 0) {
+            const int kr = u.kstart + kb * BK;
+            if constexpr (C::RES == RES_A) res_load_block(sS, &tmB, mapa_shared(fb, 0), ti.nb * C::BN + 128 * rank, kr);
+            else res_load_block(sS, &tmA, mapa_shared(fb, 0), ti.mb * BM, kr);
+          }
+          __syncwarp();
+          if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
+        }
+      }
+      if (!ok) break;
+    }
+    if (!C::GATHER) {
+      for (int i = 0; i < C::STAGES && !*abort_flag; ++i) {
+        if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1, abort_flag, a.status)) break;
+        if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
+      }
+      if (*abort_flag) {
+        for (int s = 0; s < C::STAGES; ++s) {
+          if (!((filled >> s) & 1u)) continue;
+          const unsigned long long t0 = globaltimer();
+          while (!mbar_try_wait(smem_u32(&full_bar[s]), (fill_parity >> s) & 1u) &&
+                 globaltimer() - t0 < 20000000ull) {
+          }
+        }
+      }
+    }
+  } else if (warp == C::RES_WARP) {
+    // ================= resident-operand loader =================
+    uint32_t rph = 0;     // per slot: parity bit of its uses so far
+    uint32_t armed = 0;   // slots with a load issued (for the abort drain)
+    uint32_t arm_par = 0;
+    for (int t = unit0; t < total && !*abort_flag; t += ustep) {
+      const ResUnit u = res_unit<C>(a, T, t);
+      bool ok = true;
+      for (int kb = 0; kb < u.kblocks; ++kb) {
+        if (!mbar_wait(smem_u32(&rempty_bar[kb]), ((rph >> kb) & 1u) ^ 1u, abort_flag, a.status)) { ok = false; break; }
+        const uint32_t rb = smem_u32(&rfull_bar[kb]);
+        const uint32_t slot = res_base + kb * C::BLK;
+        if (leader) {
+          if (lane == 0) mbar_arrive_expect_tx(rb, 2 * C::BLK);
+          armed |= 1u << kb;
+          arm_par = (arm_par & ~(1u << kb)) | (((rph >> kb) & 1u) << kb);
+        }
+        if (lane == 0) {
+          const int kr = u.kstart + kb * BK;
+          if constexpr (C::RES == RES_A) res_load_block(slot, &tmA, mapa_shared(rb, 0), (2 * u.outer + rank) * BM, kr);
+          else res_load_block(slot, &tmB, mapa_shared(rb, 0), u.outer * C::BN + 128 * rank, kr);
+        }
+        __syncwarp();
+        rph ^= 1u << kb;
+      }
+      if (!ok) break;
+    }
+    if (*abort_flag) {
+      for (int s = 0; s < C::RSLOTS; ++s) {
+        if (!((armed >> s) & 1u)) continue;
+        const unsigned long long t0 = globaltimer();
+        while (!mbar_try_wait(smem_u32(&rfull_bar[s]), (arm_par >> s) & 1u) &&
+               globaltimer() - t0 < 20000000ull) {
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ================= UMMA issuer (even CTA) =================
+    int stage = 0;
+    uint32_t phase = 0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    uint32_t rph = 0;  // per slot: parity of the next resident fill
+    bool ok = true;
+    for (int t = unit0; t < total && !*abort_flag && leader && ok; t += ustep) {
+      const ResUnit u = res_unit<C>(a, T, t);
+      for (int j = 0; j < u.ntiles && ok; ++j) {
+        if (!mbar_wait(smem_u32(&tempty_bar[acc]), acc_phase ^ 1, abort_flag, a.status)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * C::BN;
+        const bool last = j == u.ntiles - 1;
+        for (int kb = 0; kb < u.kblocks; ++kb) {
+          if (j == 0 && !mbar_wait(smem_u32(&rfull_bar[kb]), (rph >> kb) & 1u, abort_flag, a.status)) { ok = false; break; }
+          if (!mbar_wait(smem_u32(&full_bar[stage]), phase, abort_flag, a.status)) { ok = false; break; }
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t sR = res_base + kb * C::BLK;
+            const uint32_t sS = smem_base + stage * C::BLK;
+            const uint32_t sA = C::RES == RES_A ? sR : sS;
+            const uint32_t sB = C::RES == RES_A ? sS : sR;
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk)
+              umma_bf16_pair(d_tmem, smem_desc_sw128(sA + kk * 2048, 8192, 1024),
+                             smem_desc_sw128(sB + kk * 2048, 8192, 1024), C::IDESC,
+                             (kb | kk) != 0 ? 1u : 0u);
+            umma_commit_pair(smem_u32(&empty_bar[stage]));
+            if (last) umma_commit_pair(smem_u32(&rempty_bar[kb]));
+          }
+          __syncwarp();
+          if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+        if (lane == 0) {
+          if (u.kblocks > 0) umma_commit_pair(smem_u32(&tfull_bar[acc]));
+          else {
+            mbar_arrive(smem_u32(&tfull_bar[acc]));
+            mbar_arrive_remote(mapa_shared(smem_u32(&tfull_bar[acc]), 1));
+          }
+        }
+        __syncwarp();
+        if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+      }
+      for (int kb = 0; kb < u.kblocks; ++kb) rph ^= 1u << kb;
+    }
+    if (*abort_flag && leader) {
+      if (lane == 0) {
+        umma_commit_pair(smem_u32(&drain_bar));
+        const unsigned long long t0 = globaltimer();
+        while (!mbar_try_wait(smem_u32(&drain_bar), 0) && globaltimer() - t0 < 20000000ull) {
+        }
+      }
+      __syncwarp();
+    }
+  } else if (C::GATHER && warp >= 2 + C::EPI_WARPS) {
+    // ================= gather warps: streamed A from token rows =================
+    constexpr int LAG = C::GATHER_LAG;
+    const int gw = warp - 2 - C::EPI_WARPS;
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t ring = 0;
+    int rn = 0;
+    bool ok = true;
+    for (int t = unit0; t < total && !*abort_flag && ok; t += ustep) {
+      const ResUnit u = res_unit<C>(a, T, t);
+      for (int j = 0; j < u.ntiles && ok; ++j) {
+        const TileInfo ti = res_tile<C>(a, u, j, rank);
+        for (int kb = 0; kb < u.kblocks; ++kb) {
+          // token row of k-row gw*16 + (lane & 15) of this k-block (loaded before the wait)
+          const int kid = gather_row(a, T, u.g, kb * BK + gw * 16 + (lane & 15));
+          if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1, abort_flag, a.status)) { ok = false; break; }
+          const uint32_t sS = smem_base + stage * C::BLK;
+          if (!ti.phantom) {
+            // 128 M-columns = 16 chunks of 16 bytes per k-row; 2 k-rows per instruction
+            const int cc = lane & 15;
+            const int jg = cc >> 3, c = cc & 7;
+            const __nv_bfloat16* col = a.gsrc + ti.mb * BM + jg * 64 + c * 8;
+            // M is a multiple of 64: the upper 64-column group of the last
+            // m-block may lie past the row (not copied; its rows are not stored)
+            const bool inside = ti.mb * BM + jg * 64 < a.M;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const int rl = 2 * q + (lane >> 4);  // 0..15 within this warp's k-rows
+              const int r = gw * 16 + rl;
+              const int srow = __shfl_sync(0xffffffffu, kid, rl);
+              if (inside)
+                cp_async_16(sS + jg * 8192 + r * 128 + ((c ^ (r & 7)) << 4), col + (size_t)srow * a.gld);
+            }
+          }
+          cp_async_commit();
+          ring |= (uint32_t)stage << (4 * rn);
+          ++rn;
+          if (rn > LAG) {
+            cp_async_wait<LAG>();
+            fence_proxy_async_smem();
+            arrive_full<C>(full_bar, ring & 15u, lane, rank);
+            ring >>= 4;
+            --rn;
+          }
+          if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
+        }
+      }
+    }
+    cp_async_wait<0>();
+    fence_proxy_async_smem();
+    while (rn > 0) {
+      arrive_full<C>(full_bar, ring & 15u, lane, rank);
+      ring >>= 4;
+      --rn;
+    }
+  } else if (warp >= 2 && warp < 2 + C::EPI_WARPS) {
+    // ================= epilogue =================
+    const int quad = warp & 3;
+    const int epi = warp - 2;
+    const int row_in_tile = quad * 32 + lane;
+    WarpOut<C::EPI_BUFS, C::EPI_BUF_BYTES> wo;
+    wo.buf0 = smem_base + (C::STAGES + C::RSLOTS) * C::BLK + epi * (C::EPI_BUFS * C::EPI_BUF_BYTES);
+    wo.lane = lane;
+    wo.next = 0;
+    wo.inflight = 0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (int t = unit0; t < total && !*abort_flag && ok; t += ustep) {
+      const ResUnit u = res_unit<C>(a, T, t);
+      for (int j = 0; j < u.ntiles; ++j) {
+        const TileInfo ti = res_tile<C>(a, u, j, rank);
+        if (!mbar_wait(smem_u32(&tfull_bar[acc]), acc_phase, abort_flag, a.status)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t tacc = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * C::BN;
+        if (!ti.phantom) epilogue_store<C>(a, ti, tacc, row_in_tile, wo, &tmD0, 0, 1);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(&tempty_bar[acc]), 0));
+        if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+      }
+    }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  cluster_sync();  // no CTA leaves while its peer may still read or write it
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, kTmemCols);
+  }
+}
+
+}  // namespace moe

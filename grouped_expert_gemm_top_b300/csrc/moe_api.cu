@@ -13,6 +13,7 @@
 #include <vector>
 
 #include "gemm.cuh"
+#include "gemm_res.cuh"
 #include "kernels_misc.cuh"
 #include "moe.h"
 
@@ -21,7 +22,7 @@ namespace {
 using moe::GemmArgs;
 using moe::GemmCfg;
 
-constexpr int32_t kAbiVersion = 3;
+constexpr int32_t kAbiVersion = 4;
 constexpr size_t kAlign = 256;
 
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
@@ -251,6 +252,11 @@ using CfgDgradGateUp = PairCfg<5, KMAJ_TILE, MN_TILE, RAGGED_M, EPI_STORE, true,
 using CfgDgradGateUpShared = PairCfg<5, KMAJ_TILE, MN_TILE, RAGGED_M, EPI_STORE, false, false>;
 using CfgWgrad = PairCfg<4, MN_TILE, MN_TILE, RAGGED_K, EPI_STORE, false, false, 4, 5>;
 using CfgWgradDown = PairCfg<4, MN_GATHER, MN_TILE, RAGGED_K, EPI_STORE, false, false, 4, 5>;
+// Experts with at most 256 rows: one operand resident in shared memory.
+// gate/up: unit = (expert, 2 m-blocks of the 2I rows), [dg|du]^T resident, x streamed;
+// down: unit = (expert, n-block of I), w h resident, dout rows gathered per tile.
+using CfgWgradRes = moe::ResCfg<moe::RES_A, MN_TILE, 7, 2>;
+using CfgWgradDownRes = moe::ResCfg<moe::RES_B, MN_GATHER, 7, 2>;
 
 // fp32 [depth][rows][inner] output map with 16x32 boxes (64-byte rows).
 bool make_out_map3_f32(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows,
@@ -274,17 +280,20 @@ bool make_out_map3(CUtensorMap* m, const void* base, uint64_t inner, uint64_t ro
   return make_map3(m, base, inner, rows, depth, 64, 32);
 }
 
-template <class C>
+// RES: the resident-operand weight-gradient kernel (same parameters).
+template <class C, bool RES = false>
 moe_status launch_gemm(int kid, const CUtensorMap& A, const CUtensorMap& B, const CUtensorMap& D0,
                        const CUtensorMap& D1, const GemmArgs& a, long long tile_bound,
                        cudaStream_t st) {
+  void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, GemmArgs);
+  if constexpr (RES) kern = moe::res_gemm_kernel<C>;
+  else kern = moe::grouped_gemm_kernel<C>;
   static std::atomic<uint64_t> configured{0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
   const uint64_t bit = 1ull << (dev & 63);
   if (!(configured.load() & bit)) {
-    if (cudaFuncSetAttribute(moe::grouped_gemm_kernel<C>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::SMEM_BYTES) != cudaSuccess)
       return MOE_ERR_CUDA;
     configured.fetch_or(bit);
@@ -306,7 +315,7 @@ moe_status launch_gemm(int kid, const CUtensorMap& A, const CUtensorMap& B, cons
     int mc = max_clusters[dev & 63].load();
     if (mc == 0) {
       cfg.gridDim = dim3(2 * (sm_count() / 2));
-      if (cudaOccupancyMaxActiveClusters(&mc, moe::grouped_gemm_kernel<C>, &cfg) != cudaSuccess ||
+      if (cudaOccupancyMaxActiveClusters(&mc, kern, &cfg) != cudaSuccess ||
           mc <= 0)
         mc = sm_count() / 2;
       max_clusters[dev & 63].store(mc);
@@ -315,7 +324,7 @@ moe_status launch_gemm(int kid, const CUtensorMap& A, const CUtensorMap& B, cons
     if (clusters < 1) return MOE_OK;
     cfg.gridDim = dim3((unsigned)(2 * clusters));
     KernelScope ks(kid, st);
-    if (cudaLaunchKernelEx(&cfg, moe::grouped_gemm_kernel<C>, A, B, D0, D1, a) != cudaSuccess)
+    if (cudaLaunchKernelEx(&cfg, kern, A, B, D0, D1, a) != cudaSuccess)
       return MOE_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
   } else {
@@ -682,7 +691,13 @@ moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_
     a.d_group_stride = (long long)H * I;
     CUtensorMap tD;
     if (!make_out_map3(&tD, grad_w_down, I, H, E)) return MOE_ERR_CUDA;
-    s = launch_gemm<CfgWgradDown>(MOE_K_WGRAD_DOWN, tA, tB, tD, tD, a, (long long)E * cdiv(H, moe::BM) * cdiv(I, 256), st);
+    s = launch_gemm<CfgWgradDownRes, true>(MOE_K_WGRAD_DOWN, tA, tB, tD, tD, a,
+                                           (long long)E * cdiv(I, 256), st);
+    if (s != MOE_OK) return s;
+    a.kres = CfgWgradDownRes::KRES;  // the experts with more rows
+    s = launch_gemm<CfgWgradDown>(MOE_K_WGRAD_DOWN_LONG, tA, tB, tD, tD, a,
+                                  (long long)std::min<long long>(E, L.S / (CfgWgradDownRes::KRES + 1)) *
+                                      cdiv(H, moe::BM) * cdiv(I, 256), st);
     if (s != MOE_OK) return s;
   }
   __nv_bfloat16* xsp = at<__nv_bfloat16>(workspace, L.x_sorted_pad);
@@ -702,8 +717,13 @@ moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_
     a.d_group_stride = 2LL * I * H;
     CUtensorMap tD;
     if (!make_out_map3(&tD, grad_w_gate_up, H, 2LL * I, E)) return MOE_ERR_CUDA;
-    s = launch_gemm<CfgWgrad>(MOE_K_WGRAD_GATE_UP, tA, tB, tD, tD, a,
-                                    (long long)E * cdiv(2 * I, moe::BM) * cdiv(H, 256), st);
+    s = launch_gemm<CfgWgradRes, true>(MOE_K_WGRAD_GATE_UP, tA, tB, tD, tD, a,
+                                       (long long)E * cdiv(cdiv(2 * I, moe::BM), 2), st);
+    if (s != MOE_OK) return s;
+    a.kres = CfgWgradRes::KRES;  // the experts with more rows
+    s = launch_gemm<CfgWgrad>(MOE_K_WGRAD_GATE_UP_LONG, tA, tB, tD, tD, a,
+                              (long long)std::min<long long>(E, L.S / (CfgWgradRes::KRES + 1)) *
+                                  cdiv(2 * I, moe::BM) * cdiv(H, 256), st);
     if (s != MOE_OK) return s;
   }
   if (d->I_shared > 0) {
@@ -746,7 +766,7 @@ const char* moe_kernel_name(int32_t id) {
       "down", "shared_gate_up", "shared_down", "combine", "dgrad_down",
       "dgrad_gate_up", "shared_dgrad_down", "shared_dgrad_gate_up", "dx_gather",
       "router_wgrad", "wgrad_down", "wgrad_gate_up", "shared_wgrad_down",
-      "shared_wgrad_gate_up", "sorted_x_bwd"};
+      "shared_wgrad_gate_up", "sorted_x_bwd", "wgrad_down_long", "wgrad_gate_up_long"};
   return (id >= 0 && id < MOE_K_COUNT) ? names[id] : "unknown";
 }
 

@@ -55,7 +55,6 @@ struct GemmArgs {
   const int32_t* offsets;  // [G+1] row offsets (unpadded); nullptr: one group
   int single_rows;       // rows of the one group when offsets == nullptr
   int ksplit;            // RAGGED_K without offsets: group g = K rows [g*ksplit, (g+1)*ksplit)
-  int kres;              // RAGGED_K: groups with at most kres rows are left to the resident kernel
   int padded;            // 1: groups start on 128-row boundaries of a padded row space
   // gathered operand: row i of group g reads gsrc[gperm[off_g + min(i, n_g-1)] / gdiv]
   const __nv_bfloat16* gsrc; long long gld; const int32_t* gperm; int gdiv; int gsrc_rows;
@@ -159,14 +158,30 @@ struct SmemTables {
 template <class UnitsFn>
 __device__ __forceinline__ void build_group_tables(const GemmArgs& a, SmemTables& T, int lane,
                                                    UnitsFn units) {
+  // every lane's offsets first (G <= 256: up to 8 per lane), so their load
+  // latencies overlap instead of adding up chunk by chunk
+  constexpr int kChunks = kMaxGroups / 32;
+  int pre_off[kChunks], pre_end[kChunks];
+#pragma unroll
+  for (int c = 0; c < kChunks; ++c) {
+    const int g = 32 * c + lane;
+    pre_off[c] = pre_end[c] = 0;
+    if (a.offsets && g < a.G) {
+      pre_off[c] = __ldg(a.offsets + g);
+      pre_end[c] = __ldg(a.offsets + g + 1);
+    }
+  }
   int run_tiles = 0, run_rows = 0;
-  for (int base = 0; base < a.G; base += 32) {
+#pragma unroll
+  for (int c = 0; c < kChunks; ++c) {
+    const int base = 32 * c;
+    if (base >= a.G) break;
     const int g = base + lane;
     int cnt = 0, off = 0;
     if (g < a.G) {
       if (a.offsets) {
-        off = __ldg(a.offsets + g);
-        cnt = __ldg(a.offsets + g + 1) - off;
+        off = pre_off[c];
+        cnt = pre_end[c] - off;
       } else if (a.ksplit > 0) {
         off = g * a.ksplit;
         cnt = min(a.ksplit, a.K - off);
@@ -238,7 +253,7 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, const SmemTab
     ti.kstart = 0;
     ti.kblocks = a.K / BK;
   } else {
-    // groups own contiguous unit ranges (none for a group left to the resident kernel)
+    // groups own contiguous unit ranges
     const int nMB = (a.M + BM - 1) / BM;
     const int mu = (nMB + C::CL - 1) / C::CL;
     int lo = 0, hi = a.G - 1;
@@ -805,6 +820,20 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       if constexpr (C::EPI == EPI_SWIGLU || C::EPI == EPI_DGRAD_SWIGLU) tma_prefetch_desc(&tmD1);
     }
   }
+  if (warp == 2) {
+    const int nNB = num_nblocks<C>(a);
+    const int nMB = (a.M + BM - 1) / BM;
+    build_group_tables(a, T, lane, [&](int cnt) {
+      // work units of this group (tiles, or m-block pairs with CTA pairs)
+      const int mt = (cnt + BM - 1) / BM;
+      const int mu = ((C::SCH == RAGGED_M ? mt : nMB) + C::CL - 1) / C::CL;
+      return mu * nNB;
+    });
+  }
+  __syncthreads();
+  // no work (every CTA of a cluster sees the same tables): leave before
+  // touching tensor memory or the peer
+  if (T.total_tiles == 0) return;
   if (warp == 1) {
     if constexpr (C::PAIR) {
       tmem_alloc_pair(smem_u32(&T.tmem_base), kTmemCols);
@@ -813,19 +842,6 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       tmem_alloc(smem_u32(&T.tmem_base), kTmemCols);
       tmem_relinquish();
     }
-  }
-  if (warp == 2) {
-    const int nNB = num_nblocks<C>(a);
-    const int nMB = (a.M + BM - 1) / BM;
-    build_group_tables(a, T, lane, [&](int cnt) {
-      // work units of this group (tiles, or m-block pairs with CTA pairs); a
-      // weight-gradient launch that leaves experts with at most kres rows to
-      // the resident-operand kernel gives them none
-      if (C::SCH == RAGGED_K && a.kres > 0 && cnt <= a.kres) return 0;
-      const int mt = (cnt + BM - 1) / BM;
-      const int mu = ((C::SCH == RAGGED_M ? mt : nMB) + C::CL - 1) / C::CL;
-      return mu * nNB;
-    });
   }
   tc_fence_before();
   if constexpr (C::CL == 2) cluster_sync();  // the peer's barriers are initialised before any remote op

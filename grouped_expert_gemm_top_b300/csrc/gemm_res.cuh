@@ -14,7 +14,8 @@
 //          B streamed by TMA;
 //   RES_B: unit = (expert, n-block), B resident, tiles = the m-block pairs,
 //          A streamed by TMA or gathered from token rows by the LSU warps.
-// Experts with more rows are left to the streaming kernel (GemmArgs::kres).
+// An expert with more rows gets one unit per output tile instead, and the four
+// resident slots become a 4-deep ring through which that operand streams.
 //
 // CTA pairs as in the streaming kernel (cta_group::2, 256 x 256 tiles): each
 // CTA holds its own 128 rows of A and half of the B columns; the even CTA
@@ -23,8 +24,8 @@
 //   warp 1      TMEM allocator; UMMA issuer in the even CTA
 //   warps 2..5  epilogue (the streaming kernel's bf16 store epilogue)
 //   warps 6..9  gather warps (gathered A only)
-//   last warp   resident-operand TMA loader: refills k-block slot kb as soon
-//               as the unit's last UMMA reading it has completed
+//   last warp   resident-operand TMA loader: refills k-block slot kb % 4 as
+//               soon as the last UMMA reading it has completed
 #pragma once
 #include "gemm.cuh"
 
@@ -59,7 +60,7 @@ struct ResCfg {
   static_assert(!GATHER || GATHER_LAG >= 1, "gathers need >= 3 stages");
   static constexpr int BLK = BM * BK * 2;  // one operand's 128 x 64 block of a CTA: 16 KB
   static constexpr int RSLOTS = 4;         // resident k-blocks
-  static constexpr int KRES = RSLOTS * BK;  // experts with at most 256 rows
+  static constexpr int KRES = RSLOTS * BK;  // experts with at most 256 rows stay resident
   static constexpr uint32_t IDESC = idesc_bf16_f32(2 * BM, BN, true, true);
   // the even CTA's full barriers: both CTAs' streamed bytes, or one arrival per gather warp
   static constexpr uint32_t FULL_TX = GATHER ? 0 : 2 * BLK;
@@ -70,8 +71,11 @@ struct ResCfg {
   static_assert(SMEM_BYTES <= 227 * 1024 - 8 * 1024, "dynamic + static shared memory per CTA");
 };
 
+// A work unit: resident (the expert's K fits the slots) or one streamed tile.
 struct ResUnit {
-  int g, outer, ntiles, kstart, kblocks;
+  int g, ntiles, kstart, kblocks;
+  bool stream;
+  int p, nb;  // the resident operand's pair (RES_A) or n-block (RES_B); both for a streamed tile
 };
 
 template <class C>
@@ -88,8 +92,18 @@ __device__ __forceinline__ ResUnit res_unit(const GemmArgs& a, const SmemTables&
   }
   ResUnit u;
   u.g = lo;
-  u.outer = t - T.tile_prefix[lo];
-  u.ntiles = C::RES == RES_A ? res_nnb<C>(a) : (res_nmb<C>(a) + 1) / 2;
+  const int local = t - T.tile_prefix[lo];
+  const int mu = (res_nmb<C>(a) + 1) / 2;
+  u.stream = T.cnt[lo] > C::KRES;
+  if (u.stream) {  // one tile; m-block pairs fastest
+    u.ntiles = 1;
+    u.p = local % mu;
+    u.nb = local / mu;
+  } else {
+    u.ntiles = C::RES == RES_A ? res_nnb<C>(a) : mu;
+    u.p = local;
+    u.nb = local;
+  }
   u.kstart = T.start[lo];
   u.kblocks = (T.cnt[lo] + BK - 1) / BK;
   return u;
@@ -98,9 +112,9 @@ __device__ __forceinline__ ResUnit res_unit(const GemmArgs& a, const SmemTables&
 template <class C>
 __device__ __forceinline__ TileInfo res_tile(const GemmArgs& a, const ResUnit& u, int j, int rank) {
   TileInfo ti;
-  const int p = C::RES == RES_A ? u.outer : j;
+  const int p = (u.stream || C::RES == RES_A) ? u.p : j;
   ti.g = u.g;
-  ti.nb = C::RES == RES_A ? j : u.outer;
+  ti.nb = (u.stream || C::RES == RES_B) ? u.nb : j;
   ti.mb = 2 * p + rank;
   const int nMB = res_nmb<C>(a);
   ti.phantom = ti.mb >= nMB;
@@ -166,16 +180,19 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     tma_prefetch_desc(&tmB);
     tma_prefetch_desc(&tmD0);
   }
-  if (warp == 1) {
-    tmem_alloc_pair(smem_u32(&T.tmem_base), kTmemCols);
-    tmem_relinquish_pair();
-  }
   if (warp == 2) {
     const int nMB = res_nmb<C>(a), nNB = res_nnb<C>(a);
     build_group_tables(a, T, lane, [&](int cnt) {
-      if (cnt > C::KRES) return 0;  // left to the streaming kernel
-      return C::RES == RES_A ? (nMB + 1) / 2 : nNB;
+      const int mu = (nMB + 1) / 2;
+      if (cnt > C::KRES) return mu * nNB;  // one unit per streamed tile
+      return C::RES == RES_A ? mu : nNB;
     });
+  }
+  __syncthreads();
+  if (T.total_tiles == 0) return;  // no work: leave before touching tensor memory or the peer
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(&T.tmem_base), kTmemCols);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
   cluster_sync();  // the peer's barriers are initialised before any remote op
@@ -241,21 +258,22 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       const ResUnit u = res_unit<C>(a, T, t);
       bool ok = true;
       for (int kb = 0; kb < u.kblocks; ++kb) {
-        if (!mbar_wait(smem_u32(&rempty_bar[kb]), ((rph >> kb) & 1u) ^ 1u, abort_flag, a.status)) { ok = false; break; }
-        const uint32_t rb = smem_u32(&rfull_bar[kb]);
-        const uint32_t slot = res_base + kb * C::BLK;
+        const int sl = kb % C::RSLOTS;
+        if (!mbar_wait(smem_u32(&rempty_bar[sl]), ((rph >> sl) & 1u) ^ 1u, abort_flag, a.status)) { ok = false; break; }
+        const uint32_t rb = smem_u32(&rfull_bar[sl]);
+        const uint32_t slot = res_base + sl * C::BLK;
         if (leader) {
           if (lane == 0) mbar_arrive_expect_tx(rb, 2 * C::BLK);
-          armed |= 1u << kb;
-          arm_par = (arm_par & ~(1u << kb)) | (((rph >> kb) & 1u) << kb);
+          armed |= 1u << sl;
+          arm_par = (arm_par & ~(1u << sl)) | (((rph >> sl) & 1u) << sl);
         }
         if (lane == 0) {
           const int kr = u.kstart + kb * BK;
-          if constexpr (C::RES == RES_A) res_load_block(slot, &tmA, mapa_shared(rb, 0), (2 * u.outer + rank) * BM, kr);
-          else res_load_block(slot, &tmB, mapa_shared(rb, 0), u.outer * C::BN + 128 * rank, kr);
+          if constexpr (C::RES == RES_A) res_load_block(slot, &tmA, mapa_shared(rb, 0), (2 * u.p + rank) * BM, kr);
+          else res_load_block(slot, &tmB, mapa_shared(rb, 0), u.nb * C::BN + 128 * rank, kr);
         }
         __syncwarp();
-        rph ^= 1u << kb;
+        rph ^= 1u << sl;
       }
       if (!ok) break;
     }
@@ -284,11 +302,17 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const uint32_t d_tmem = tmem_base + acc * C::BN;
         const bool last = j == u.ntiles - 1;
         for (int kb = 0; kb < u.kblocks; ++kb) {
-          if (j == 0 && !mbar_wait(smem_u32(&rfull_bar[kb]), (rph >> kb) & 1u, abort_flag, a.status)) { ok = false; break; }
+          // the resident operand's block kb: in slot kb % 4, filled once per
+          // unit (the first tile waits for it) or, streamed, once per k-block
+          const int sl = kb % C::RSLOTS;
+          if (j == 0) {
+            if (!mbar_wait(smem_u32(&rfull_bar[sl]), (rph >> sl) & 1u, abort_flag, a.status)) { ok = false; break; }
+            rph ^= 1u << sl;
+          }
           if (!mbar_wait(smem_u32(&full_bar[stage]), phase, abort_flag, a.status)) { ok = false; break; }
           tc_fence_after();
           if (lane == 0) {
-            const uint32_t sR = res_base + kb * C::BLK;
+            const uint32_t sR = res_base + sl * C::BLK;
             const uint32_t sS = smem_base + stage * C::BLK;
             const uint32_t sA = C::RES == RES_A ? sR : sS;
             const uint32_t sB = C::RES == RES_A ? sS : sR;
@@ -298,7 +322,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                              smem_desc_sw128(sB + kk * 2048, 8192, 1024), C::IDESC,
                              (kb | kk) != 0 ? 1u : 0u);
             umma_commit_pair(smem_u32(&empty_bar[stage]));
-            if (last) umma_commit_pair(smem_u32(&rempty_bar[kb]));
+            if (last) umma_commit_pair(smem_u32(&rempty_bar[sl]));
           }
           __syncwarp();
           if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
@@ -314,7 +338,6 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         __syncwarp();
         if (++acc == 2) { acc = 0; acc_phase ^= 1; }
       }
-      for (int kb = 0; kb < u.kblocks; ++kb) rph ^= 1u << kb;
     }
     if (*abort_flag && leader) {
       if (lane == 0) {

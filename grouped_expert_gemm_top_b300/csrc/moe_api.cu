@@ -22,7 +22,7 @@ namespace {
 using moe::GemmArgs;
 using moe::GemmCfg;
 
-constexpr int32_t kAbiVersion = 4;
+constexpr int32_t kAbiVersion = 5;
 constexpr size_t kAlign = 256;
 
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
@@ -251,8 +251,8 @@ using CfgDgradDownShared = PairCfg<5, KMAJ_TILE, MN_TILE, RAGGED_M, EPI_DGRAD_SW
 using CfgDgradGateUp = PairCfg<5, KMAJ_TILE, MN_TILE, RAGGED_M, EPI_STORE, true, false>;
 using CfgDgradGateUpShared = PairCfg<5, KMAJ_TILE, MN_TILE, RAGGED_M, EPI_STORE, false, false>;
 using CfgWgrad = PairCfg<4, MN_TILE, MN_TILE, RAGGED_K, EPI_STORE, false, false, 4, 5>;
-using CfgWgradDown = PairCfg<4, MN_GATHER, MN_TILE, RAGGED_K, EPI_STORE, false, false, 4, 5>;
-// Experts with at most 256 rows: one operand resident in shared memory.
+// Expert weight gradients: one operand resident in shared memory for experts
+// with at most 256 rows (streamed through the same slots for larger ones).
 // gate/up: unit = (expert, 2 m-blocks of the 2I rows), [dg|du]^T resident, x streamed;
 // down: unit = (expert, n-block of I), w h resident, dout rows gathered per tile.
 using CfgWgradRes = moe::ResCfg<moe::RES_A, MN_TILE, 7, 2>;
@@ -692,12 +692,7 @@ moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_
     CUtensorMap tD;
     if (!make_out_map3(&tD, grad_w_down, I, H, E)) return MOE_ERR_CUDA;
     s = launch_gemm<CfgWgradDownRes, true>(MOE_K_WGRAD_DOWN, tA, tB, tD, tD, a,
-                                           (long long)E * cdiv(I, 256), st);
-    if (s != MOE_OK) return s;
-    a.kres = CfgWgradDownRes::KRES;  // the experts with more rows
-    s = launch_gemm<CfgWgradDown>(MOE_K_WGRAD_DOWN_LONG, tA, tB, tD, tD, a,
-                                  (long long)std::min<long long>(E, L.S / (CfgWgradDownRes::KRES + 1)) *
-                                      cdiv(H, moe::BM) * cdiv(I, 256), st);
+                                           (long long)E * cdiv(H, 2 * moe::BM) * cdiv(I, 256), st);
     if (s != MOE_OK) return s;
   }
   __nv_bfloat16* xsp = at<__nv_bfloat16>(workspace, L.x_sorted_pad);
@@ -718,12 +713,7 @@ moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_
     CUtensorMap tD;
     if (!make_out_map3(&tD, grad_w_gate_up, H, 2LL * I, E)) return MOE_ERR_CUDA;
     s = launch_gemm<CfgWgradRes, true>(MOE_K_WGRAD_GATE_UP, tA, tB, tD, tD, a,
-                                       (long long)E * cdiv(cdiv(2 * I, moe::BM), 2), st);
-    if (s != MOE_OK) return s;
-    a.kres = CfgWgradRes::KRES;  // the experts with more rows
-    s = launch_gemm<CfgWgrad>(MOE_K_WGRAD_GATE_UP_LONG, tA, tB, tD, tD, a,
-                              (long long)std::min<long long>(E, L.S / (CfgWgradRes::KRES + 1)) *
-                                  cdiv(2 * I, moe::BM) * cdiv(H, 256), st);
+                                       (long long)E * cdiv(2 * I, 2 * moe::BM) * cdiv(H, 256), st);
     if (s != MOE_OK) return s;
   }
   if (d->I_shared > 0) {
@@ -766,7 +756,7 @@ const char* moe_kernel_name(int32_t id) {
       "down", "shared_gate_up", "shared_down", "combine", "dgrad_down",
       "dgrad_gate_up", "shared_dgrad_down", "shared_dgrad_gate_up", "dx_gather",
       "router_wgrad", "wgrad_down", "wgrad_gate_up", "shared_wgrad_down",
-      "shared_wgrad_gate_up", "sorted_x_bwd", "wgrad_down_long", "wgrad_gate_up_long"};
+      "shared_wgrad_gate_up", "sorted_x_bwd"};
   return (id >= 0 && id < MOE_K_COUNT) ? names[id] : "unknown";
 }
 

@@ -11,21 +11,24 @@
 // for a work unit that runs every tile along the other output dimension,
 // streaming only the other operand:
 //   RES_A: unit = (expert, m-block pair), A resident, tiles = the n-blocks,
-//          B streamed by TMA;
+//          B streamed;
 //   RES_B: unit = (expert, n-block), B resident, tiles = the m-block pairs,
-//          A streamed by TMA or gathered from token rows by the LSU warps.
+//          A streamed.
+// An operand comes by TMA from a row-per-slot matrix, or is gathered by the
+// LSU warps straight from the token rows it is a copy of.
 // An expert with more rows gets one unit per output tile instead, and the four
 // resident slots become a 4-deep ring through which that operand streams.
 //
 // CTA pairs as in the streaming kernel (cta_group::2, 256 x 256 tiles): each
 // CTA holds its own 128 rows of A and half of the B columns; the even CTA
 // issues the UMMAs.  Roles:
-//   warp 0      streamed-operand TMA producer (idle when A is gathered)
+//   warp 0      streamed-operand TMA producer (idle when it is gathered)
 //   warp 1      TMEM allocator; UMMA issuer in the even CTA
 //   warps 2..5  epilogue (the streaming kernel's bf16 store epilogue)
-//   warps 6..9  gather warps (gathered A only)
-//   last warp   resident-operand TMA loader: refills k-block slot kb % 4 as
-//               soon as the last UMMA reading it has completed
+//   warps 6..9  gather warps (a gathered operand only)
+//   last warp   resident-operand TMA loader (idle when it is gathered):
+//               refills k-block slot kb % 4 as soon as the last UMMA reading
+//               it has completed
 #pragma once
 #include "gemm.cuh"
 
@@ -33,11 +36,11 @@ namespace moe {
 
 enum ResMode : int { RES_A = 1, RES_B = 2 };
 
-template <int RES_, int AL_, int STAGES_, int EPI_BUFS_>
+template <int RES_, int AL_, int BL_, int STAGES_, int EPI_BUFS_>
 struct ResCfg {
   static constexpr int RES = RES_;
-  static constexpr int AL = AL_;          // MN_TILE or (RES_B only) MN_GATHER
-  static constexpr int BL = MN_TILE;
+  static constexpr int AL = AL_;  // MN_TILE or (streamed, RES_B) MN_GATHER
+  static constexpr int BL = BL_;  // MN_TILE or (streamed, RES_A) MN_GATHER
   static constexpr int BN = 256;
   static constexpr int CL = 2;
   static constexpr bool PAIR = true;
@@ -49,9 +52,14 @@ struct ResCfg {
   static constexpr int EPI_BUFS = EPI_BUFS_;
   static constexpr int EPI_BUF_BYTES = 4096;
   static constexpr bool A_GATHER = AL == MN_GATHER;
-  static constexpr bool GATHER = A_GATHER;
-  static_assert(AL == MN_TILE || AL == MN_GATHER, "weight-gradient operands are MN-major");
-  static_assert(!(RES == RES_A && A_GATHER), "the resident operand is loaded by TMA");
+  static constexpr bool B_GATHER = BL == MN_GATHER;
+  static constexpr bool GATHER = A_GATHER || B_GATHER;
+  // which operand the gather warps fill: the streamed one, or the resident one
+  static constexpr bool STREAM_GATHER = RES == RES_A ? B_GATHER : A_GATHER;
+  static constexpr bool RES_GATHER = RES == RES_A ? A_GATHER : B_GATHER;
+  static_assert(!(A_GATHER && B_GATHER), "one gathered operand");
+  static_assert((AL == MN_TILE || AL == MN_GATHER) && (BL == MN_TILE || BL == MN_GATHER),
+                "weight-gradient operands are MN-major");
   static constexpr int GATHER_WARPS = GATHER ? 4 : 0;
   static constexpr int RES_WARP = 2 + EPI_WARPS + GATHER_WARPS;
   static constexpr int THREADS = 32 * (RES_WARP + 1);
@@ -62,9 +70,11 @@ struct ResCfg {
   static constexpr int RSLOTS = 4;         // resident k-blocks
   static constexpr int KRES = RSLOTS * BK;  // experts with at most 256 rows stay resident
   static constexpr uint32_t IDESC = idesc_bf16_f32(2 * BM, BN, true, true);
-  // the even CTA's full barriers: both CTAs' streamed bytes, or one arrival per gather warp
-  static constexpr uint32_t FULL_TX = GATHER ? 0 : 2 * BLK;
-  static constexpr uint32_t FULL_ARRIVALS = GATHER ? 2 * GATHER_WARPS : 1;
+  // the even CTA's full barriers (streamed stages) and rfull barriers (resident
+  // slots): both CTAs' TMA bytes, or one arrival per gather warp of both CTAs
+  static constexpr uint32_t FULL_TX = STREAM_GATHER ? 0 : 2 * BLK;
+  static constexpr uint32_t FULL_ARRIVALS = STREAM_GATHER ? 2 * GATHER_WARPS : 1;
+  static constexpr uint32_t RFULL_ARRIVALS = RES_GATHER ? 2 * GATHER_WARPS : 1;
   static constexpr uint32_t TEMPTY_ARRIVALS = 2 * EPI_WARPS;
   static constexpr int SMEM_BYTES =
       (STAGES + RSLOTS) * BLK + EPI_WARPS * EPI_BUFS * EPI_BUF_BYTES + 1024;
@@ -125,6 +135,27 @@ __device__ __forceinline__ TileInfo res_tile(const GemmArgs& a, const ResUnit& u
   return ti;
 }
 
+// Gather warp gw's 16 k-rows of an MN-major 128-column block (64 k-rows, two
+// 64-wide groups, 128-byte swizzle) from the token rows: k-row r of the block
+// is token row `kid` of lane r - 16 gw; columns x0 .. x0+127 (a 64-column
+// group at or past xlim, possible when the extent is a multiple of 64 but not
+// of 128, is not copied: its rows or columns are not stored).
+template <class GA>
+__device__ __forceinline__ void gather_block(const GA& a, uint32_t dst, int x0, int xlim, int kid,
+                                             int gw, int lane) {
+  const int cc = lane & 15;
+  const int jg = cc >> 3, c = cc & 7;
+  const __nv_bfloat16* col = a.gsrc + x0 + jg * 64 + c * 8;
+  const bool inside = x0 + jg * 64 < xlim;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const int rl = 2 * q + (lane >> 4);  // 0..15 within this warp's k-rows
+    const int r = gw * 16 + rl;
+    const int srow = __shfl_sync(0xffffffffu, kid, rl);
+    if (inside) cp_async_16(dst + jg * 8192 + r * 128 + ((c ^ (r & 7)) << 4), col + (size_t)srow * a.gld);
+  }
+}
+
 // MN-major block of an operand (two 64-wide groups of 64 k-rows) by TMA, to
 // this CTA's shared memory, completing on the even CTA's barrier `barp`.
 __device__ __forceinline__ void res_load_block(uint32_t dst, const CUtensorMap* map, uint32_t barp,
@@ -164,7 +195,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       mbar_init(smem_u32(&empty_bar[s]), 1);
     }
     for (int s = 0; s < C::RSLOTS; ++s) {
-      mbar_init(smem_u32(&rfull_bar[s]), 1);
+      mbar_init(smem_u32(&rfull_bar[s]), C::RFULL_ARRIVALS);
       mbar_init(smem_u32(&rempty_bar[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -209,7 +240,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     int stage = 0;
     uint32_t phase = 0;
     uint32_t filled = 0, fill_parity = 0;
-    for (int t = unit0; t < total && !*abort_flag && !C::GATHER; t += ustep) {
+    for (int t = unit0; t < total && !*abort_flag && !C::STREAM_GATHER; t += ustep) {
       const ResUnit u = res_unit<C>(a, T, t);
       bool ok = true;
       for (int j = 0; j < u.ntiles && ok; ++j) {
@@ -234,7 +265,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       }
       if (!ok) break;
     }
-    if (!C::GATHER) {
+    if (!C::STREAM_GATHER) {
       for (int i = 0; i < C::STAGES && !*abort_flag; ++i) {
         if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1, abort_flag, a.status)) break;
         if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
@@ -254,7 +285,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     uint32_t rph = 0;     // per slot: parity bit of its uses so far
     uint32_t armed = 0;   // slots with a load issued (for the abort drain)
     uint32_t arm_par = 0;
-    for (int t = unit0; t < total && !*abort_flag; t += ustep) {
+    for (int t = unit0; t < total && !*abort_flag && !C::RES_GATHER; t += ustep) {
       const ResUnit u = res_unit<C>(a, T, t);
       bool ok = true;
       for (int kb = 0; kb < u.kblocks; ++kb) {
@@ -349,60 +380,86 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       __syncwarp();
     }
   } else if (C::GATHER && warp >= 2 + C::EPI_WARPS) {
-    // ================= gather warps: streamed A from token rows =================
-    constexpr int LAG = C::GATHER_LAG;
+    // ================= gather warps: an operand from token rows =================
     const int gw = warp - 2 - C::EPI_WARPS;
-    int stage = 0;
-    uint32_t phase = 0;
-    uint32_t ring = 0;
+    const int xlim = C::A_GATHER ? a.M : a.N;
+    uint32_t ring = 0;  // slots or stages copied but not yet signalled (4 bits each, FIFO)
     int rn = 0;
     bool ok = true;
-    for (int t = unit0; t < total && !*abort_flag && ok; t += ustep) {
-      const ResUnit u = res_unit<C>(a, T, t);
-      for (int j = 0; j < u.ntiles && ok; ++j) {
-        const TileInfo ti = res_tile<C>(a, u, j, rank);
-        for (int kb = 0; kb < u.kblocks; ++kb) {
-          // token row of k-row gw*16 + (lane & 15) of this k-block (loaded before the wait)
-          const int kid = gather_row(a, T, u.g, kb * BK + gw * 16 + (lane & 15));
-          if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1, abort_flag, a.status)) { ok = false; break; }
-          const uint32_t sS = smem_base + stage * C::BLK;
-          if (!ti.phantom) {
-            // 128 M-columns = 16 chunks of 16 bytes per k-row; 2 k-rows per instruction
-            const int cc = lane & 15;
-            const int jg = cc >> 3, c = cc & 7;
-            const __nv_bfloat16* col = a.gsrc + ti.mb * BM + jg * 64 + c * 8;
-            // M is a multiple of 64: the upper 64-column group of the last
-            // m-block may lie past the row (not copied; its rows are not stored)
-            const bool inside = ti.mb * BM + jg * 64 < a.M;
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              const int rl = 2 * q + (lane >> 4);  // 0..15 within this warp's k-rows
-              const int r = gw * 16 + rl;
-              const int srow = __shfl_sync(0xffffffffu, kid, rl);
-              if (inside)
-                cp_async_16(sS + jg * 8192 + r * 128 + ((c ^ (r & 7)) << 4), col + (size_t)srow * a.gld);
+    if constexpr (C::STREAM_GATHER) {
+      // the streamed operand, stage by stage; a stage is signalled GATHER_LAG stages later
+      constexpr int LAG = C::GATHER_LAG;
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int t = unit0; t < total && !*abort_flag && ok; t += ustep) {
+        const ResUnit u = res_unit<C>(a, T, t);
+        for (int j = 0; j < u.ntiles && ok; ++j) {
+          const TileInfo ti = res_tile<C>(a, u, j, rank);
+          for (int kb = 0; kb < u.kblocks; ++kb) {
+            // token row of k-row gw*16 + (lane & 15) of this k-block (loaded before the wait)
+            const int kid = gather_row(a, T, u.g, kb * BK + gw * 16 + (lane & 15));
+            if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1, abort_flag, a.status)) { ok = false; break; }
+            // A: this CTA's 128 rows of the tile; B: its half of the 256 columns
+            const int x0 = C::A_GATHER ? ti.mb * BM : ti.nb * C::BN + 128 * rank;
+            if (!(C::A_GATHER && ti.phantom))
+              gather_block(a, smem_base + stage * C::BLK, x0, xlim, kid, gw, lane);
+            cp_async_commit();
+            ring |= (uint32_t)stage << (4 * rn);
+            ++rn;
+            if (rn > LAG) {
+              cp_async_wait<LAG>();
+              fence_proxy_async_smem();
+              arrive_full<C>(full_bar, ring & 15u, lane, rank);
+              ring >>= 4;
+              --rn;
             }
+            if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
           }
+        }
+      }
+      cp_async_wait<0>();
+      fence_proxy_async_smem();
+      while (rn > 0) {
+        arrive_full<C>(full_bar, ring & 15u, lane, rank);
+        ring >>= 4;
+        --rn;
+      }
+    } else {
+      // the resident operand, slot by slot.  Every slot of a unit is signalled
+      // before the next unit's first fill (which waits for this unit's last
+      // UMMA, and so for all of its slots); within a streamed unit a slot is
+      // signalled 2 slots later.
+      constexpr int LAG = 2;
+      uint32_t rph = 0;
+      for (int t = unit0; t < total && !*abort_flag && ok; t += ustep) {
+        const ResUnit u = res_unit<C>(a, T, t);
+        // A: the pair's m-block of this CTA; B: this CTA's half of the n-block
+        const int x0 = C::A_GATHER ? (2 * u.p + rank) * BM : u.nb * C::BN + 128 * rank;
+        for (int kb = 0; kb < u.kblocks; ++kb) {
+          const int sl = kb % C::RSLOTS;
+          const int kid = gather_row(a, T, u.g, kb * BK + gw * 16 + (lane & 15));
+          if (!mbar_wait(smem_u32(&rempty_bar[sl]), ((rph >> sl) & 1u) ^ 1u, abort_flag, a.status)) { ok = false; break; }
+          rph ^= 1u << sl;
+          gather_block(a, res_base + sl * C::BLK, x0, xlim, kid, gw, lane);
           cp_async_commit();
-          ring |= (uint32_t)stage << (4 * rn);
+          ring |= (uint32_t)sl << (4 * rn);
           ++rn;
           if (rn > LAG) {
             cp_async_wait<LAG>();
             fence_proxy_async_smem();
-            arrive_full<C>(full_bar, ring & 15u, lane, rank);
+            arrive_full<C>(rfull_bar, ring & 15u, lane, rank);
             ring >>= 4;
             --rn;
           }
-          if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
+        }
+        cp_async_wait<0>();
+        fence_proxy_async_smem();
+        while (rn > 0) {
+          arrive_full<C>(rfull_bar, ring & 15u, lane, rank);
+          ring >>= 4;
+          --rn;
         }
       }
-    }
-    cp_async_wait<0>();
-    fence_proxy_async_smem();
-    while (rn > 0) {
-      arrive_full<C>(full_bar, ring & 15u, lane, rank);
-      ring >>= 4;
-      --rn;
     }
   } else if (warp >= 2 && warp < 2 + C::EPI_WARPS) {
     // ================= epilogue =================

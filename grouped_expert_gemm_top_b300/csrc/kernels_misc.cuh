@@ -293,43 +293,6 @@ __global__ void combine_kernel(const __nv_bfloat16* __restrict__ y_perm,
 // zero in every sorted copy, so weight-gradient GEMMs can run whole 64-row
 // k-blocks.
 
-// Padded sorted copy of the tokens for the gate/up weight gradient: row p of
-// expert e's padded block [poff[e], poff[e+1]) holds x[token of sorted row
-// offsets[e] + (p - poff[e])], or zeros past the expert's tokens.  One warp
-// per row, grid-stride; rows at or past poff[E] are not touched.
-__global__ void sorted_rows_padded_kernel(const int32_t* __restrict__ poff,
-                                          const int32_t* __restrict__ expert_offsets,
-                                          const int32_t* __restrict__ perm_slot, int E, int k,
-                                          int H, int T, const __nv_bfloat16* __restrict__ x,
-                                          __nv_bfloat16* __restrict__ x_sorted) {
-  __shared__ int sp[257];
-  __shared__ int so[257];
-  for (int e = threadIdx.x; e <= E; e += blockDim.x) {
-    sp[e] = __ldg(poff + e);
-    so[e] = __ldg(expert_offsets + e);
-  }
-  __syncthreads();
-  const int lane = threadIdx.x & 31;
-  const long long nwarps = (long long)gridDim.x * (blockDim.x >> 5);
-  for (long long p = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); p < sp[E];
-       p += nwarps) {
-    int lo = 0, hi = E - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (sp[mid] <= p) lo = mid; else hi = mid - 1;
-    }
-    const int i = (int)(p - sp[lo]);
-    uint4* dst = reinterpret_cast<uint4*>(x_sorted + (size_t)p * H);
-    if (i < so[lo + 1] - so[lo]) {
-      const int tok = clampi(__ldg(perm_slot + so[lo] + i) / k, 0, T - 1);
-      const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)tok * H);
-      for (int c = lane; c < H / 8; c += 32) dst[c] = __ldg(src + c);
-    } else {
-      for (int c = lane; c < H / 8; c += 32) dst[c] = make_uint4(0, 0, 0, 0);
-    }
-  }
-}
-
 // Router backward fused with the per-token gradient gather, one warp per token.
 // Router: dw_j = sum of the down-projection partials of slot j; the renormalised
 // top-k weights are a softmax over the chosen logits, so
@@ -345,8 +308,9 @@ __global__ void dx_gather_kernel(const __nv_bfloat16* __restrict__ dx_slot,
                                  const int32_t* __restrict__ poff, const float* __restrict__ dw_part,
                                  int nNB, const __nv_bfloat16* __restrict__ w_router,
                                  const __nv_bfloat16* __restrict__ dx_shared,
-                                 float* __restrict__ dl_out, __nv_bfloat16* __restrict__ dx, int T,
-                                 int H, int k, int E, int P) {
+                                 float* __restrict__ dl_out, __nv_bfloat16* __restrict__ dl_dense,
+                                 int ldE, __nv_bfloat16* __restrict__ dx, int T, int H, int k, int E,
+                                 int P) {
   const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
@@ -371,6 +335,15 @@ __global__ void dx_gather_kernel(const __nv_bfloat16* __restrict__ dx_slot,
     rows[j] = __shfl_sync(0xffffffffu, row_l, j);
     es[j] = __shfl_sync(0xffffffffu, e_l, j);
     dls[j] = __shfl_sync(0xffffffffu, dl_l, j);
+  }
+  if (dl_dense) {  // row t of the dense [T, ldE] logit gradient (zero off the selected experts)
+    for (int e = lane; e < ldE; e += 32) {
+      float v = 0.f;
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j)
+        if (j < k && es[j] == e) v = dls[j];
+      dl_dense[(size_t)t * ldE + e] = __float2bfloat16_rn(v);
+    }
   }
   for (int c = lane; c < H / 8; c += 32) {
     uint4 v[KMAX], r[KMAX];
@@ -415,70 +388,50 @@ __global__ void dx_gather_kernel(const __nv_bfloat16* __restrict__ dx_slot,
   }
 }
 
-// dW_r[e, :] = sum over the rows of expert e (sorted order) of dl[slot] * x[token, :];
-// db[e] = sum of those dl.  Block = (expert, 256-column chunk); the expert's
-// rows are taken 32 at a time (lane j loads row j's slot and dl), 4 warps take
-// every 4th batch, and the 4 partials are added in warp order.
-__global__ void router_wgrad_kernel(const __nv_bfloat16* __restrict__ x,
-                                    const int32_t* __restrict__ expert_offsets,
-                                    const int32_t* __restrict__ perm_slot,
-                                    const float* __restrict__ dl, int H, int k,
-                                    __nv_bfloat16* __restrict__ dw_router,
-                                    float* __restrict__ dbias) {
-  __shared__ float part[4][256];
-  __shared__ float bpart[4];
-  const int e = blockIdx.y;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int c0 = blockIdx.x * 256 + lane * 8;  // 8 columns per lane
-  const bool col_ok = c0 < H;
-  const int r0 = __ldg(expert_offsets + e), r1 = __ldg(expert_offsets + e + 1);
-  float acc[8];
+// Router weight gradient, second step.  The first is a split-K tensor-core
+// GEMM dW_r = DL^T x over the tokens, where DL [T, E] is the logit gradient
+// (zero off each token's selected experts: the renormalised top-k weights are
+// a softmax over the selected logits) in bf16; it leaves one fp32 partial
+// [E, H] per token split.  Here the splits are added in order and rounded to
+// bf16 (thread = 4 consecutive elements of dW_r, up to 16 splits' loads in
+// flight at once); the first E warps of the grid also form db[e] = sum of the
+// fp32 dl over expert e's rows (sorted order, lane-strided partial sums, then a
+// fixed butterfly).
+__global__ void router_wgrad_reduce_kernel(const float* __restrict__ part, int nsplit, int E, int H,
+                                           const int32_t* __restrict__ expert_offsets,
+                                           const int32_t* __restrict__ perm_slot,
+                                           const float* __restrict__ dl,
+                                           __nv_bfloat16* __restrict__ dw_router,
+                                           float* __restrict__ dbias) {
+  const long long n4 = (long long)E * H / 4;
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n4) {
+    const float4* p = reinterpret_cast<const float4*>(part) + i;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int g0 = 0; g0 < nsplit; g0 += 16) {
+      float4 u[16];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-  float bsum = 0.f;
-  for (int rb = r0 + warp * 32; rb < r1; rb += 4 * 32) {
-    int tok_l = 0;
-    float d_l = 0.f;
-    if (rb + lane < r1) {
-      const int s = __ldg(perm_slot + rb + lane);
-      tok_l = s / k;
-      d_l = __ldg(dl + s);
+      for (int g = 0; g < 16; ++g)
+        if (g0 + g < nsplit) u[g] = __ldg(p + (size_t)(g0 + g) * n4);
+#pragma unroll
+      for (int g = 0; g < 16; ++g)
+        if (g0 + g < nsplit) { o.x += u[g].x; o.y += u[g].y; o.z += u[g].z; o.w += u[g].w; }
     }
-    const int nb = min(32, r1 - rb);
-#pragma unroll 8
-    for (int j = 0; j < 32; ++j) {
-      const int tok = __shfl_sync(0xffffffffu, tok_l, j);
-      const float d = __shfl_sync(0xffffffffu, d_l, j);
-      if (j < nb) {
-        bsum += d;
-        if (col_ok) {
-          const uint4 v = __ldg(reinterpret_cast<const uint4*>(x + (size_t)tok * H + c0));
-          acc[0] = fmaf(d, bf16lo(v.x), acc[0]); acc[1] = fmaf(d, bf16hi(v.x), acc[1]);
-          acc[2] = fmaf(d, bf16lo(v.y), acc[2]); acc[3] = fmaf(d, bf16hi(v.y), acc[3]);
-          acc[4] = fmaf(d, bf16lo(v.z), acc[4]); acc[5] = fmaf(d, bf16hi(v.z), acc[5]);
-          acc[6] = fmaf(d, bf16lo(v.w), acc[6]); acc[7] = fmaf(d, bf16hi(v.w), acc[7]);
-        }
-      }
-    }
+    uint2 w;
+    w.x = pack_bf16x2(o.x, o.y);
+    w.y = pack_bf16x2(o.z, o.w);
+    reinterpret_cast<uint2*>(dw_router)[i] = w;
   }
+  const int gw = (int)(((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (dbias && gw < E) {
+    const int e = gw;
+    const int r0 = __ldg(expert_offsets + e), r1 = __ldg(expert_offsets + e + 1);
+    float b = 0.f;
+    for (int r = r0 + lane; r < r1; r += 32) b += __ldg(dl + __ldg(perm_slot + r));
 #pragma unroll
-  for (int i = 0; i < 8; ++i) part[warp][lane * 8 + i] = acc[i];
-  if (lane == 0) bpart[warp] = bsum;
-  __syncthreads();
-  if (warp == 0) {
-    float o[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      o[i] = ((part[0][lane * 8 + i] + part[1][lane * 8 + i]) + part[2][lane * 8 + i]) +
-             part[3][lane * 8 + i];
-    if (col_ok) {
-      uint4 v;
-      v.x = pack_bf16x2(o[0], o[1]); v.y = pack_bf16x2(o[2], o[3]);
-      v.z = pack_bf16x2(o[4], o[5]); v.w = pack_bf16x2(o[6], o[7]);
-      *reinterpret_cast<uint4*>(dw_router + (size_t)e * H + c0) = v;
-    }
-    if (dbias && blockIdx.x == 0 && lane == 0)
-      dbias[e] = ((bpart[0] + bpart[1]) + bpart[2]) + bpart[3];
+    for (int o = 16; o > 0; o >>= 1) b += __shfl_xor_sync(0xffffffffu, b, o);
+    if (lane == 0) dbias[e] = b;
   }
 }
 

@@ -22,7 +22,7 @@ namespace {
 using moe::GemmArgs;
 using moe::GemmCfg;
 
-constexpr int32_t kAbiVersion = 5;
+constexpr int32_t kAbiVersion = 7;
 constexpr size_t kAlign = 256;
 
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
@@ -47,13 +47,30 @@ constexpr int kDwParts = 1;  // column parts of the down data-gradient epilogue 
 
 struct Layout {
   size_t status, counts, logits_part, h, h_sh, fwd_end;
-  size_t poff, x_sorted_pad, dgu, hw, dxs, dwp, dl, dgu_sh, hw_sh, dxs_sh,
+  size_t poff, dgu, hw, dxs, dwp, dl, dlb, rwp, dgu_sh, hw_sh, dxs_sh,
       total;
   int sort_blocks;
   long long S, S_pad_max;
   int nNB_I;  // 256-wide column blocks of the intermediate (dgrad-down tiles)
   int nDW;    // dw partials per padded row (column blocks x epilogue column parts)
 };
+
+// Split-K of the router weight-gradient GEMM over the tokens: about one wave
+// of 128 x 256 tiles on a 148-SM part, splits of a multiple of 64 tokens.  ldE:
+// row stride of the dense logit gradient (16-byte multiple for TMA).
+struct RwSplit {
+  int nsplit, ksplit, ldE;
+};
+RwSplit rw_split(const moe_dims& d) {
+  RwSplit r;
+  const int tiles = ((d.E + 127) / 128) * ((d.H + 255) / 256);
+  int n = std::max(1, (148 + tiles - 1) / tiles);
+  n = std::min(n, (d.T + 63) / 64);
+  r.ksplit = ((d.T + n - 1) / n + 63) / 64 * 64;
+  r.nsplit = (d.T + r.ksplit - 1) / r.ksplit;
+  r.ldE = (d.E + 7) / 8 * 8;
+  return r;
+}
 
 Layout make_layout(const moe_dims& d, bool bwd) {
   Layout L{};
@@ -73,12 +90,14 @@ Layout make_layout(const moe_dims& d, bool bwd) {
   if (bwd) {
     const size_t P = (size_t)L.S_pad_max;
     L.poff = o; o = align_up(o + (size_t)(d.E + 1) * 4);
-    L.x_sorted_pad = o; o = align_up(o + P * d.H * 2);
     L.dgu = o; o = align_up(o + P * 2 * d.I * 2);
     L.hw = o; o = align_up(o + P * d.I * 2);
     L.dxs = o; o = align_up(o + P * d.H * 2);
     L.dwp = o; o = align_up(o + P * L.nDW * 4);
     L.dl = o; o = align_up(o + (size_t)L.S * 4);
+    const RwSplit rs = rw_split(d);
+    L.dlb = o; o = align_up(o + (size_t)d.T * rs.ldE * 2);
+    L.rwp = o; o = align_up(o + (size_t)rs.nsplit * d.E * d.H * 4);
     L.dgu_sh = o; o = align_up(o + (size_t)d.T * 2 * d.I_shared * 2);
     L.hw_sh = o; o = align_up(o + (size_t)d.T * d.I_shared * 2);
     L.dxs_sh = o; o = align_up(o + (size_t)(d.I_shared ? d.T : 0) * d.H * 2);
@@ -233,6 +252,8 @@ using moe::RAGGED_M;
 template <int BN>
 using CfgRouter =
     GemmCfg<BN, (BN >= 256 ? 4 : 6), KMAJ_TILE, KMAJ_TILE, RAGGED_K, EPI_STORE_F32, false, false>;
+// router weight gradient: A = DL [tokens, E] and B = x [tokens, H], both MN-major
+using CfgRouterW = GemmCfg<256, 4, MN_TILE, MN_TILE, RAGGED_K, EPI_STORE_F32, false, false>;
 // Every BN=256 GEMM runs as CTA pairs: 256 x 256 tiles by cta_group::2 UMMAs,
 // each CTA staging its 128 A rows and half of the B tile (32 KB per stage).
 // The ragged-M GEMMs stream K = 768..2048 per tile through 5 stages with 3
@@ -253,10 +274,11 @@ using CfgDgradGateUpShared = PairCfg<5, KMAJ_TILE, MN_TILE, RAGGED_M, EPI_STORE,
 using CfgWgrad = PairCfg<4, MN_TILE, MN_TILE, RAGGED_K, EPI_STORE, false, false, 4, 5>;
 // Expert weight gradients: one operand resident in shared memory for experts
 // with at most 256 rows (streamed through the same slots for larger ones).
-// gate/up: unit = (expert, 2 m-blocks of the 2I rows), [dg|du]^T resident, x streamed;
+// gate/up: unit = (expert, n-block of H), x rows gathered once into the resident slots,
+//          [dg|du]^T streamed per m-block pair;
 // down: unit = (expert, n-block of I), w h resident, dout rows gathered per tile.
-using CfgWgradRes = moe::ResCfg<moe::RES_A, MN_TILE, 7, 2>;
-using CfgWgradDownRes = moe::ResCfg<moe::RES_B, MN_GATHER, 7, 2>;
+using CfgWgradRes = moe::ResCfg<moe::RES_B, MN_TILE, MN_GATHER, 7, 2>;
+using CfgWgradDownRes = moe::ResCfg<moe::RES_B, MN_GATHER, MN_TILE, 7, 2>;
 
 // fp32 [depth][rows][inner] output map with 16x32 boxes (64-byte rows).
 bool make_out_map3_f32(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows,
@@ -598,6 +620,9 @@ moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_
   __nv_bfloat16* dxs = at<__nv_bfloat16>(workspace, L.dxs);
   float* dwp = at<float>(workspace, L.dwp);
   float* dl = at<float>(workspace, L.dl);
+  const RwSplit rs = rw_split(*d);
+  __nv_bfloat16* dlb = at<__nv_bfloat16>(workspace, L.dlb);
+  float* rwp = at<float>(workspace, L.rwp);
 
   const auto* gob = reinterpret_cast<const __nv_bfloat16*>(grad_out);
   const auto* xb = reinterpret_cast<const __nv_bfloat16*>(x);
@@ -669,17 +694,33 @@ moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_
     if (k <= 8)
       moe::dx_gather_kernel<8><<<blocks, 256, 0, st>>>(dxs, topk_idx, topk_w, slot_perm,
                                                        expert_offsets, poff, dwp, L.nDW, wr,
-                                                       dxs_sh, dl, gx, T, H, k, E, (int)P);
+                                                       dxs_sh, dl, dlb, rs.ldE, gx, T, H, k, E, (int)P);
     else
       moe::dx_gather_kernel<32><<<blocks, 256, 0, st>>>(dxs, topk_idx, topk_w, slot_perm,
                                                         expert_offsets, poff, dwp, L.nDW, wr,
-                                                        dxs_sh, dl, gx, T, H, k, E, (int)P);
+                                                        dxs_sh, dl, dlb, rs.ldE, gx, T, H, k, E, (int)P);
   }
-  { KernelScope ks(MOE_K_ROUTER_WGRAD, st);
-  moe::router_wgrad_kernel<<<dim3((unsigned)cdiv(H, 256), E), 128, 0, st>>>(
-      reinterpret_cast<const __nv_bfloat16*>(x), expert_offsets, perm_slot, dl, H, k,
-      reinterpret_cast<__nv_bfloat16*>(grad_w_router), grad_router_bias); }
-  if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+  {  // router weight gradient: dW_r = DL^T x, split-K over the tokens (fp32 partials) ...
+    CUtensorMap tA, tB, tD;
+    if (!make_map(&tA, dlb, rs.ldE, T, 1, 64, 64)) return MOE_ERR_CUDA;
+    if (!make_map(&tB, x, H, T, 1, 64, 64)) return MOE_ERR_CUDA;
+    if (!make_out_map3_f32(&tD, rwp, H, E, rs.nsplit)) return MOE_ERR_CUDA;
+    GemmArgs a = base_args(status);
+    a.M = E; a.N = H; a.K = T; a.G = rs.nsplit; a.ksplit = rs.ksplit;
+    a.d_f32 = rwp; a.ldd = H; a.d_group_stride = (long long)E * H; a.f32_tma = 1;
+    s = launch_gemm<CfgRouterW>(MOE_K_ROUTER_WGRAD, tA, tB, tD, tD, a,
+                                (long long)rs.nsplit * cdiv(E, moe::BM) * cdiv(H, 256), st);
+    if (s != MOE_OK) return s;
+  }
+  {  // ... then the ordered sum of the splits (and the bias gradient)
+    KernelScope ks(MOE_K_ROUTER_WGRAD_REDUCE, st);
+    const long long n4 = (long long)E * H / 4;
+    const long long blocks = std::max<long long>(cdiv(n4, 256), cdiv((long long)E * 32, 256));
+    moe::router_wgrad_reduce_kernel<<<(unsigned)blocks, 256, 0, st>>>(
+        rwp, rs.nsplit, E, H, expert_offsets, perm_slot, dl,
+        reinterpret_cast<__nv_bfloat16*>(grad_w_router), grad_router_bias);
+    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+  }
   {  // dW_down[e] = sum over the expert's rows of dout[token]^T (w h)
     CUtensorMap tA, tB;
     if (!make_map(&tB, hw, I, P, 1, 64, 64)) return MOE_ERR_CUDA;
@@ -695,19 +736,13 @@ moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_
                                            (long long)E * cdiv(H, 2 * moe::BM) * cdiv(I, 256), st);
     if (s != MOE_OK) return s;
   }
-  __nv_bfloat16* xsp = at<__nv_bfloat16>(workspace, L.x_sorted_pad);
-  {  // padded sorted copy of x (B operand of the gate/up weight gradient)
-    KernelScope ks(MOE_K_SORTED_X_BWD, st);
-    moe::sorted_rows_padded_kernel<<<(unsigned)std::max(1, 8 * sm_count()), 256, 0, st>>>(
-        poff, expert_offsets, perm_slot, E, k, H, T, xb, xsp);
-    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
-  }
   {  // dW_gu[e] = sum over the expert's rows of [dg|du]^T x[token]
     CUtensorMap tA, tB;
     if (!make_map(&tA, dgu, 2LL * I, P, 1, 64, 64)) return MOE_ERR_CUDA;
-    if (!make_map(&tB, xsp, H, P, 1, 64, 64)) return MOE_ERR_CUDA;
+    tB = tA;  // unused: B = x rows, gathered by token
     GemmArgs a = base_args(status);
     a.M = 2 * I; a.N = H; a.G = E; a.offsets = expert_offsets; a.padded = 1;
+    a.gsrc = xb; a.gld = H; a.gperm = perm_slot; a.gdiv = k; a.gsrc_rows = T;
     a.d = reinterpret_cast<__nv_bfloat16*>(grad_w_gate_up); a.ldd = H;
     a.d_group_stride = 2LL * I * H;
     CUtensorMap tD;
@@ -756,7 +791,7 @@ const char* moe_kernel_name(int32_t id) {
       "down", "shared_gate_up", "shared_down", "combine", "dgrad_down",
       "dgrad_gate_up", "shared_dgrad_down", "shared_dgrad_gate_up", "dx_gather",
       "router_wgrad", "wgrad_down", "wgrad_gate_up", "shared_wgrad_down",
-      "shared_wgrad_gate_up", "sorted_x_bwd"};
+      "shared_wgrad_gate_up", "router_wgrad_reduce"};
   return (id >= 0 && id < MOE_K_COUNT) ? names[id] : "unknown";
 }
 

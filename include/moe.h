@@ -244,12 +244,12 @@ typedef enum {
   MOE_K_SHARED_DGRAD_DOWN,
   MOE_K_SHARED_DGRAD_GATE_UP,
   MOE_K_DX_GATHER,           /* backward: router logit gradient + per-token sum of slot gradients */
-  MOE_K_ROUTER_WGRAD,        /* backward: router weight (and bias) gradient */
+  MOE_K_ROUTER_WGRAD,        /* backward: router weight gradient GEMM (split-K over tokens) */
   MOE_K_WGRAD_DOWN,          /* backward: grouped down weight-gradient GEMM */
   MOE_K_WGRAD_GATE_UP,       /* backward: grouped gate/up weight-gradient GEMM */
   MOE_K_SHARED_WGRAD_DOWN,
   MOE_K_SHARED_WGRAD_GATE_UP,
-  MOE_K_SORTED_X_BWD,        /* backward: padded sorted copy of x for the gate/up weight gradient */
+  MOE_K_ROUTER_WGRAD_REDUCE, /* backward: sum of the router weight-gradient splits, bias gradient */
   MOE_K_COUNT
 } moe_kernel_id;
 

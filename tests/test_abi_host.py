@@ -35,7 +35,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert M.moe_abi_version() == 5
+    assert M.moe_abi_version() == 7
     assert M.moe_status_string(0) == "ok"
     for s in range(1, 7):
         assert M.moe_status_string(s) not in ("ok", "unknown status")

@@ -276,9 +276,10 @@ using CfgWgrad = PairCfg<4, MN_TILE, MN_TILE, RAGGED_K, EPI_STORE, false, false,
 // with at most 256 rows (streamed through the same slots for larger ones).
 // gate/up: unit = (expert, n-block of H), x rows gathered once into the resident slots,
 //          [dg|du]^T streamed per m-block pair;
-// down: unit = (expert, n-block of I), w h resident, dout rows gathered per tile.
+// down: unit = (expert, 2 m-blocks of H), dout rows gathered once into the resident slots,
+//       w h streamed per n-block.
 using CfgWgradRes = moe::ResCfg<moe::RES_B, MN_TILE, MN_GATHER, 7, 2>;
-using CfgWgradDownRes = moe::ResCfg<moe::RES_B, MN_GATHER, MN_TILE, 7, 2>;
+using CfgWgradDownRes = moe::ResCfg<moe::RES_A, MN_GATHER, MN_TILE, 7, 2>;
 
 // fp32 [depth][rows][inner] output map with 16x32 boxes (64-byte rows).
 bool make_out_map3_f32(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows,

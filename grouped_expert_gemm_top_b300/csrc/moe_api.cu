@@ -416,10 +416,10 @@ moe_status moe_route(const moe_dims* d, int32_t gate_mode, const moe_bf16* x,
   if (workspace_bytes < L.h) return MOE_ERR_WORKSPACE_TOO_SMALL;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int T = d->T, H = d->H, E = d->E;
-  // split K so that the router GEMM fills the SMs; partial logits are summed in
-  // split order by the top-k kernel
+  // split K so that the router GEMM's tiles fill the SMs in one wave; partial
+  // logits are summed in split order by the top-k kernel
   const long long mt = cdiv(T, moe::BM);
-  int splits = (int)std::min<long long>(kMaxRouterSplits, std::max<long long>(1, cdiv(sm_count(), mt)));
+  int splits = (int)std::min<long long>(kMaxRouterSplits, std::max<long long>(1, sm_count() / mt));
   const int kblocks = H / moe::BK;
   if (splits > kblocks) splits = kblocks;
   const int ksplit = (int)cdiv(kblocks, splits) * moe::BK;

@@ -111,7 +111,7 @@ def measured_traffic(kernel, workload):
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             rec = json.load(f)
         h = hashlib.md5()
-        for name in ("gemm.cuh", "ptx.cuh"):
+        for name in ("gemm.cuh", "gemm_res.cuh", "ptx.cuh"):
             with open(os.path.join(ROOT, "grouped_expert_gemm_top_b300", "csrc", name), "rb") as f:
                 h.update(f.read())
         k = rec["kernels"].get(kernel)

@@ -70,18 +70,14 @@ struct GemmArgs {
 };
 
 template <int BN_, int STAGES_, int AL_, int BL_, int SCH_, int EPI_, bool B3D_, bool SWIGLU_B_,
-          int EPI_WARPS_ = 4, bool MC_ = false, bool PAIR_ = false, int EPI_BUFS_ = 3>
+          int EPI_WARPS_ = 4, bool PAIR_ = false, int EPI_BUFS_ = 3>
 struct GemmCfg {
-  // MC: 2-CTA clusters; the two CTAs take adjacent M-tiles of the same
-  // (group, n-block) and each TMA-multicasts half of the shared B tile.
   // PAIR: 2-CTA clusters computing one 256 x BN tile with CTA-pair UMMAs
   // (cta_group::2): each CTA stages its own 128 A rows and only HALF of the B
   // tile, the even CTA issues the UMMAs, and each CTA's TMEM receives its own
   // 128 rows.  Per SM this halves the B bytes pulled from L2 per FLOP.
-  static constexpr bool MC = MC_;
   static constexpr bool PAIR = PAIR_;
-  static_assert(!(MC && PAIR), "MC and PAIR are alternatives");
-  static constexpr int CL = (MC || PAIR) ? 2 : 1;
+  static constexpr int CL = PAIR ? 2 : 1;
   static constexpr int EPI_WARPS = EPI_WARPS_;
   // staging buffers per epilogue warp = TMA stores it keeps in flight; the
   // weight-gradient GEMMs, whose output is most of their traffic, need more
@@ -135,7 +131,7 @@ struct GemmCfg {
 
 struct TileInfo {
   int g, mb, nb;
-  bool phantom;    // MC pair slot past the group's last M-tile: loads only, no output
+  bool phantom;    // pair slot past the group's last M-tile: loads only, no output
   int row0;        // RAGGED_M: first row of the M-tile in the A/D row space
   int rows_valid;  // RAGGED_M: rows of the group inside this tile (<= 128)
   int kstart;      // RAGGED_K: first K row of the group
@@ -227,8 +223,8 @@ __device__ __forceinline__ int num_nblocks(const GemmArgs& a) {
   return (a.N + C::BN - 1) / C::BN;
 }
 
-// Work unit t -> tile.  Without MC a unit is one tile (m-block fastest).  With
-// MC a unit is a pair of adjacent m-blocks of one (group, n-block); CTA rank r
+// Work unit t -> tile.  Without PAIR a unit is one tile (m-block fastest).  With
+// PAIR a unit is a pair of adjacent m-blocks of one (group, n-block); CTA rank r
 // of the cluster takes m-block 2p + r.
 template <class C>
 __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, const SmemTables& T, int t,
@@ -801,8 +797,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(smem_u32(&full_bar[s]), C::FULL_ARRIVALS);
-      // MC: both CTAs' UMMA commits release a stage; PAIR: the even CTA's alone
-      mbar_init(smem_u32(&empty_bar[s]), C::MC ? 2 : 1);
+      // with PAIR the even CTA's UMMA commit releases the stage in both CTAs
+      mbar_init(smem_u32(&empty_bar[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&tfull_bar[b]), 1);
@@ -853,7 +849,6 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   const bool leader = rank == 0;  // PAIR: the CTA whose thread issues the pair's UMMAs
   const int unit0 = blockIdx.x / C::CL;
   const int ustep = gridDim.x / C::CL;
-  constexpr uint16_t kPair = 0x3;
 
   if (warp == 0) {
     // ================= TMA producer =================
@@ -921,31 +916,18 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           if (lane == 0) {
 #pragma unroll
             for (int b = 0; b < C::B_NBOX; ++b) {
-              // with MC each CTA loads its share of the boxes, multicast to the pair
-              if (C::MC && (b * C::CL) / C::B_NBOX != rank) continue;
               const int nc = C::SWIGLU_B ? (b == 0 ? n0 : a.inter + n0) : n0 + b * C::B_BOX_ROWS;
               const uint32_t dst = sB + b * C::B_BOX_ROWS * 128;
-              if constexpr (C::MC) {
-                if constexpr (C::B3D) tma_load_3d_mc(dst, &tmB, fb, kc, nc, ti.g, kPair);
-                else tma_load_2d_mc(dst, &tmB, fb, kx, nc, kPair);
-              } else {
-                if constexpr (C::B3D) tma_load_3d(dst, &tmB, fb, kc, nc, ti.g);
-                else tma_load_2d(dst, &tmB, fb, kx, nc);
-              }
+              if constexpr (C::B3D) tma_load_3d(dst, &tmB, fb, kc, nc, ti.g);
+              else tma_load_2d(dst, &tmB, fb, kx, nc);
             }
           }
         } else if constexpr (C::BL == MN_TILE) {
           if (lane == 0) {
 #pragma unroll
             for (int b = 0; b < C::BN / 64; ++b) {
-              if (C::MC && (b * C::CL) / (C::BN / 64) != rank) continue;
-              if constexpr (C::MC) {
-                if constexpr (C::B3D) tma_load_3d_mc(sB + b * 8192, &tmB, fb, n0 + 64 * b, kc, ti.g, kPair);
-                else tma_load_2d_mc(sB + b * 8192, &tmB, fb, n0 + 64 * b, kr, kPair);
-              } else {
-                if constexpr (C::B3D) tma_load_3d(sB + b * 8192, &tmB, fb, n0 + 64 * b, kc, ti.g);
-                else tma_load_2d(sB + b * 8192, &tmB, fb, n0 + 64 * b, kr);
-              }
+              if constexpr (C::B3D) tma_load_3d(sB + b * 8192, &tmB, fb, n0 + 64 * b, kc, ti.g);
+              else tma_load_2d(sB + b * 8192, &tmB, fb, n0 + 64 * b, kr);
             }
           }
         }
@@ -954,7 +936,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       if (!ok) break;
     }
     // wait until every stage this CTA filled has been released by all consumers
-    // (with MC this includes the peer's commits, which arrive remotely)
+    // (with PAIR, the even CTA's commits, which arrive remotely in the odd one)
     for (int i = 0; i < C::STAGES && !*abort_flag; ++i) {
       if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1, abort_flag, a.status)) break;
       if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
@@ -998,7 +980,6 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             else umma_bf16(d_tmem, ad, bd, C::IDESC, (kb | kk) != 0 ? 1u : 0u);
           }
           if constexpr (C::PAIR) umma_commit_pair(smem_u32(&empty_bar[stage]));
-          else if constexpr (C::MC) umma_commit_mc(smem_u32(&empty_bar[stage]), kPair);
           else umma_commit(smem_u32(&empty_bar[stage]));
         }
         __syncwarp();

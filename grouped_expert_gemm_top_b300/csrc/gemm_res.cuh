@@ -44,7 +44,6 @@ struct ResCfg {
   static constexpr int BN = 256;
   static constexpr int CL = 2;
   static constexpr bool PAIR = true;
-  static constexpr bool MC = false;
   static constexpr bool SWIGLU_B = false;
   static constexpr int SCH = RAGGED_K;
   static constexpr int EPI = EPI_STORE;

@@ -261,7 +261,7 @@ using CfgRouterW = GemmCfg<256, 4, MN_TILE, MN_TILE, RAGGED_K, EPI_STORE_F32, fa
 // expert's tokens, output-dominated traffic) use 4 stages and 5 buffers.
 template <int STAGES, int AL, int BL, int SCH, int EPI, bool B3D, bool SWIGLU_B, int EPI_WARPS = 4,
           int EPI_BUFS = 3>
-using PairCfg = GemmCfg<256, STAGES, AL, BL, SCH, EPI, B3D, SWIGLU_B, EPI_WARPS, false, true, EPI_BUFS>;
+using PairCfg = GemmCfg<256, STAGES, AL, BL, SCH, EPI, B3D, SWIGLU_B, EPI_WARPS, true, EPI_BUFS>;
 using CfgGateUp = PairCfg<5, KMAJ_GATHER, KMAJ_TILE, RAGGED_M, EPI_SWIGLU, true, true>;
 using CfgGateUpShared = PairCfg<5, KMAJ_TILE, KMAJ_TILE, RAGGED_M, EPI_SWIGLU, false, true>;
 using CfgDown = PairCfg<5, KMAJ_TILE, KMAJ_TILE, RAGGED_M, EPI_STORE, true, false>;

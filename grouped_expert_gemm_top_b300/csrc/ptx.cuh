@@ -1,7 +1,8 @@
-// Inline-PTX building blocks for sm_103a: mbarriers, TMA (tiled and
-// tile::gather4) loads, tcgen05 tensor-memory allocation, UMMA issue and
-// commit, and TMEM loads.  Every spin-wait is bounded: after the time limit it
-// raises the CTA's abort flag and records MOE_DEV_TIMEOUT in the status word.
+// Inline-PTX building blocks for sm_103a: mbarriers, TMA tile loads (one CTA
+// or a CTA pair) and stores, cp.async, tcgen05 tensor-memory allocation, UMMA
+// issue and commit (one CTA or a CTA pair), and TMEM loads.  Every spin-wait
+// is bounded: after the time limit it raises the CTA's abort flag and records
+// MOE_DEV_TIMEOUT in the status word.
 #pragma once
 #include <cstdint>
 #include <cuda_bf16.h>
@@ -107,27 +108,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, uint
       : "memory");
 }
 
-// Multicast tile loads: the box lands at the same shared-memory offset in every
-// CTA of the cluster named in cta_mask, and each destination CTA's mbarrier at
-// `bar`'s offset receives the complete_tx for its copy.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const void* tmap, uint32_t bar, int x,
-                                               int y, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar), "h"(cta_mask)
-      : "memory");
-}
-
-__device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const void* tmap, uint32_t bar, int x,
-                                               int y, int z, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(bar), "h"(cta_mask)
-      : "memory");
-}
-
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -179,17 +159,6 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const void* tmap,
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
                    : "memory");
-}
-
-// Four rows (r0..r3) of one 128-byte column block starting at element x.
-// The tensor map's box must be {64 bf16, 1 row}; 512 bytes land at dst.
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const void* tmap, uint32_t bar, int x,
-                                            int r0, int r1, int r2, int r3) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
-      : "memory");
 }
 
 // TMA stores: shared -> global, tracked per thread with bulk async-groups.
@@ -305,15 +274,6 @@ __device__ __forceinline__ void umma_commit_pair(uint32_t bar) {
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-      : "memory");
-}
-
-// Arrive once on the mbarrier at `bar`'s offset in every CTA of cta_mask when
-// all previously issued tcgen05 ops of this thread finish.
-__device__ __forceinline__ void umma_commit_mc(uint32_t bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(bar), "h"(cta_mask)
       : "memory");
 }
 

@@ -333,6 +333,9 @@ def run_ours(args, w, rank, world):
     grads = layer.alloc_grads(with_bias=bias is not None)
     # forward-only (inference) layer: same calls, no saved pre-activations
     layer_inf = M.MoeLayer(dims, gate_mode=w.gate, device=dev, with_backward=False)
+    # activation recompute: the forward keeps no pre-activations, the backward recomputes them
+    layer_rc = M.MoeLayer(dims, gate_mode=w.gate, device=dev, with_backward=True, recompute=True)
+    grads_rc = layer_rc.alloc_grads(with_bias=bias is not None)
     stream = torch.cuda.current_stream(dev)
 
     def fwd():
@@ -344,6 +347,10 @@ def run_ours(args, w, rank, world):
     def step():
         fwd()
         layer.backward(go, x, wr, wgu, wd, grads, wsg, wsd)
+
+    def step_rc():
+        layer_rc.forward(x, wr, wgu, wd, bias, wsg, wsd)
+        layer_rc.backward(go, x, wr, wgu, wd, grads_rc, wsg, wsd)
 
     def barrier():
         if world > 1:
@@ -372,20 +379,26 @@ def run_ours(args, w, rank, world):
     counts = np.diff(layer.expert_offsets.cpu().numpy())
     P_pad = int(sum((int(c) + 127) // 128 * 128 for c in counts))
 
-    # ---- forward + backward (the headline), per-kernel events on
-    M.moe_timing_enable(True)
-    M.moe_kernel_stats(reset=True)
+    # ---- forward + backward (the headline), no per-kernel instrumentation
     with ClockSampler(local) as clocks:
         ms_fb = timed(step, args.steps)
+    # ---- the same steps again with every kernel bracketed by CUDA events on
+    # its stream: per-kernel times and the dominant kernel's roofline
+    M.moe_timing_enable(True)
+    M.moe_kernel_stats(reset=True)
+    ms_fb_inst = timed(step, args.steps)
     kstats = M.moe_kernel_stats(reset=True)
-    # ---- forward only (inference: no saved pre-activations)
+    M.moe_timing_enable(False)
+    # ---- forward only (inference: no saved pre-activations), uninstrumented
     for _ in range(max(1, args.warmup // 2)):
         fwd_inf()
-    M.moe_kernel_stats(reset=True)
     ms_f = timed(fwd_inf, args.steps)
-    kstats_f = M.moe_kernel_stats(reset=True)
-    M.moe_timing_enable(False)
     assert M.moe_read_device_status(layer.workspace) == 0, "device reported an error"
+    # ---- forward + backward with activation recompute
+    for _ in range(max(1, args.warmup // 2)):
+        step_rc()
+    ms_rc = timed(step_rc, args.steps)
+    assert M.moe_read_device_status(layer_rc.workspace) == 0, "device reported an error"
 
     # ---- end to end: pinned host inputs in, result out, every step
     xh = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
@@ -464,6 +477,14 @@ def run_ours(args, w, rank, world):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic", "config": config_of(w, args),
         "fwd_tokens_per_s": fwd_value, "fwd_ms_per_step": ms_f / args.steps,
+        # the headline steps again with per-kernel CUDA events (source of `kernels`)
+        "ms_per_step_instrumented": ms_fb_inst / args.steps,
+        # forward+backward with activation recompute: the forward keeps no gate/up
+        # pre-activations (S*2I bf16), the backward reruns the gate/up GEMM
+        "recompute": {"tokens_per_s": job_tokens_per_s(w.T, world, args.steps, ms_rc),
+                      "ms_per_step": ms_rc / args.steps,
+                      "saved_bytes_not_held": w.T * w.k * 2 * w.I * 2 + w.T * 2 * w.I_shared * 2,
+                      "extra_flops": 2.0 * w.T * w.k * w.H * 2 * w.I + 2.0 * w.T * w.H * 2 * w.I_shared},
         "layer_roofline": {
             "fwd": {"t_roof_us": t_roof_f * 1e6, "t_us": t_f * 1e6, "frac": t_roof_f / t_f,
                     "flops": f_fwd, "bytes": b_fwd},

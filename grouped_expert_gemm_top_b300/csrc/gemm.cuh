@@ -393,8 +393,9 @@ __device__ void epilogue_store_f32(const GemmArgs& a, const TileInfo& ti, uint32
 }
 
 // Gate/up epilogue: acc columns [0, BN/2) are gate, [BN/2, BN) up, for the
-// intermediate columns n0 .. n0+BN/2-1.  Writes g, u (bf16, for the backward)
-// and h = silu(g) * u.  Maps: tmD0 = gu_out [rows, 2I], tmD1 = h_out [rows, I].
+// intermediate columns n0 .. n0+BN/2-1.  Writes g, u (bf16, for the backward;
+// skipped when gu_out is null) and h = silu(g) * u (skipped when h_out is
+// null).  Maps: tmD0 = gu_out [rows, 2I], tmD1 = h_out [rows, I].
 template <class C, class W>
 __device__ void epilogue_swiglu(const GemmArgs& a, const TileInfo& ti, uint32_t tacc,
                                 int row_in_tile, W& w, const CUtensorMap* tmD0,
@@ -408,6 +409,7 @@ __device__ void epilogue_swiglu(const GemmArgs& a, const TileInfo& ti, uint32_t 
   constexpr int HALF = C::BN / 2;
   const int n0 = ti.nb * HALF;
   const bool keep_gu = a.gu_out != nullptr;
+  const bool keep_h = a.h_out != nullptr;  // a backward recomputing g, u needs no h
   int g0, g1;
   block_range(cpart, nparts, HALF / 64, n0, I, g0, g1);
 #pragma unroll 1
@@ -419,7 +421,7 @@ __device__ void epilogue_swiglu(const GemmArgs& a, const TileInfo& ti, uint32_t 
         bg = stage_acquire<3>(w);
         bu = stage_acquire<1>(w);  // inside the three just made free
       }
-      bh = stage_acquire<1>(w);
+      if (keep_h) bh = stage_acquire<1>(w);
     }
 #pragma unroll 1
     for (int h = 0; h < 2; ++h) {
@@ -445,14 +447,14 @@ __device__ void epilogue_swiglu(const GemmArgs& a, const TileInfo& ti, uint32_t 
             put128(bg, w.lane, pc, pg[0], pg[1], pg[2], pg[3]);
             put128(bu, w.lane, pc, pu[0], pu[1], pu[2], pu[3]);
           }
-          put128(bh, w.lane, pc, ph[0], ph[1], ph[2], ph[3]);
+          if (keep_h) put128(bh, w.lane, pc, ph[0], ph[1], ph[2], ph[3]);
         } else if (valid) {
           const int col = j + 8 * pc;
           if (keep_gu) {
             st_global_16(a.gu_out + r * (2LL * I) + col, pg[0], pg[1], pg[2], pg[3]);
             st_global_16(a.gu_out + r * (2LL * I) + I + col, pu[0], pu[1], pu[2], pu[3]);
           }
-          st_global_16(a.h_out + r * (long long)I + col, ph[0], ph[1], ph[2], ph[3]);
+          if (keep_h) st_global_16(a.h_out + r * (long long)I + col, ph[0], ph[1], ph[2], ph[3]);
         }
       }
     }
@@ -461,7 +463,7 @@ __device__ void epilogue_swiglu(const GemmArgs& a, const TileInfo& ti, uint32_t 
         stage_store(w, bg, tmD0, j, y, 0, false);
         stage_store(w, bu, tmD0, I + j, y, 0, false);
       }
-      stage_store(w, bh, tmD1, j, y, 0, false);
+      if (keep_h) stage_store(w, bh, tmD1, j, y, 0, false);
     }
   }
 }

@@ -47,7 +47,7 @@ constexpr int kDwParts = 1;  // column parts of the down data-gradient epilogue 
 
 struct Layout {
   size_t status, counts, logits_part, h, h_sh, fwd_end;
-  size_t poff, dgu, hw, dxs, dwp, dl, dlb, rwp, dgu_sh, hw_sh, dxs_sh,
+  size_t poff, dgu, hw, dxs, dwp, dl, dlb, rwp, dgu_sh, hw_sh, dxs_sh, gu_rc, sh_gu_rc,
       total;
   int sort_blocks;
   long long S, S_pad_max;
@@ -72,7 +72,9 @@ RwSplit rw_split(const moe_dims& d) {
   return r;
 }
 
-Layout make_layout(const moe_dims& d, bool bwd) {
+// bwd: the backward's buffers; recompute: also room for the gate/up
+// pre-activations the backward recomputes when the forward did not save them.
+Layout make_layout(const moe_dims& d, bool bwd, bool recompute = false) {
   Layout L{};
   L.S = (long long)d.T * d.k;
   L.S_pad_max = L.S + (long long)d.E * (moe::kPadRows - 1);
@@ -101,6 +103,10 @@ Layout make_layout(const moe_dims& d, bool bwd) {
     L.dgu_sh = o; o = align_up(o + (size_t)d.T * 2 * d.I_shared * 2);
     L.hw_sh = o; o = align_up(o + (size_t)d.T * d.I_shared * 2);
     L.dxs_sh = o; o = align_up(o + (size_t)(d.I_shared ? d.T : 0) * d.H * 2);
+    if (recompute) {
+      L.gu_rc = o; o = align_up(o + (size_t)L.S * 2 * d.I * 2);
+      L.sh_gu_rc = o; o = align_up(o + (size_t)d.T * 2 * d.I_shared * 2);
+    }
   }
   L.total = o;
   return L;
@@ -397,7 +403,8 @@ moe_status moe_workspace_size(const moe_dims* d, int32_t with_backward, size_t* 
   if (!bytes) return MOE_ERR_INVALID_ARG;
   const moe_status s = check_dims(d);
   if (s != MOE_OK) return s;
-  *bytes = make_layout(*d, with_backward != 0).total;
+  if (with_backward < 0 || with_backward > 2) return MOE_ERR_INVALID_ARG;
+  *bytes = make_layout(*d, with_backward != 0, with_backward == 2).total;
   return MOE_OK;
 }
 
@@ -473,6 +480,46 @@ moe_status moe_permute(const moe_dims* d, const int32_t* topk_idx, int32_t* expe
   return launched(cudaGetLastError());
 }
 
+// Grouped gate/up GEMM + SwiGLU of the routed experts (A = token rows of x
+// gathered through the sort): gu_out [S,2I] and h_out [S,I] are each optional.
+moe_status launch_gate_up(const moe_dims& d, const moe_bf16* x, const int32_t* expert_offsets,
+                          const int32_t* perm_slot, const moe_bf16* w_gate_up, moe_bf16* gu_out,
+                          __nv_bfloat16* h_out, int* status, cudaStream_t st) {
+  const int H = d.H, E = d.E, I = d.I;
+  const long long S = (long long)d.T * d.k;
+  CUtensorMap tB;
+  if (!make_map3(&tB, w_gate_up, H, 2LL * I, E, 64, 128)) return MOE_ERR_CUDA;
+  const CUtensorMap& tA = tB;  // unused: A is gathered
+  CUtensorMap tD0 = tB, tD1 = tB;
+  if (h_out && !make_out_map(&tD1, h_out, I, S)) return MOE_ERR_CUDA;
+  if (gu_out && !make_out_map(&tD0, gu_out, 2LL * I, S)) return MOE_ERR_CUDA;
+  GemmArgs a = base_args(status);
+  a.N = 2 * I; a.K = H; a.G = E; a.offsets = expert_offsets;
+  a.gsrc = reinterpret_cast<const __nv_bfloat16*>(x); a.gld = H; a.gperm = perm_slot;
+  a.gdiv = d.k; a.gsrc_rows = d.T;
+  a.gu_out = reinterpret_cast<__nv_bfloat16*>(gu_out); a.h_out = h_out; a.inter = I;
+  return launch_gemm<CfgGateUp>(MOE_K_GATE_UP, tA, tB, tD0, tD1, a,
+                                (cdiv(S, moe::BM) + E) * cdiv(I, 128), st);
+}
+
+// The shared expert's gate/up GEMM + SwiGLU (one group, every token).
+moe_status launch_shared_gate_up(const moe_dims& d, const moe_bf16* x, const moe_bf16* w_sh_gate_up,
+                                 moe_bf16* sh_gu_out, __nv_bfloat16* hs_out, int* status,
+                                 cudaStream_t st) {
+  const int T = d.T, H = d.H, Is = d.I_shared;
+  CUtensorMap tA, tB;
+  if (!make_map(&tA, x, H, T, 1, 64, 128)) return MOE_ERR_CUDA;
+  if (!make_map(&tB, w_sh_gate_up, H, 2LL * Is, 1, 64, 128)) return MOE_ERR_CUDA;
+  CUtensorMap tD0 = tA, tD1 = tA;
+  if (hs_out && !make_out_map(&tD1, hs_out, Is, T)) return MOE_ERR_CUDA;
+  if (sh_gu_out && !make_out_map(&tD0, sh_gu_out, 2LL * Is, T)) return MOE_ERR_CUDA;
+  GemmArgs a = base_args(status);
+  a.N = 2 * Is; a.K = H; a.G = 1; a.single_rows = T;
+  a.gu_out = reinterpret_cast<__nv_bfloat16*>(sh_gu_out); a.h_out = hs_out; a.inter = Is;
+  return launch_gemm<CfgGateUpShared>(MOE_K_SHARED_GATE_UP, tA, tB, tD0, tD1, a,
+                                      cdiv(T, moe::BM) * cdiv(Is, 128), st);
+}
+
 moe_status moe_grouped_mlp_fwd(const moe_dims* d, const moe_bf16* x,
                                const int32_t* expert_offsets, const int32_t* perm_slot,
                                const moe_bf16* w_gate_up, const moe_bf16* w_down,
@@ -497,22 +544,8 @@ moe_status moe_grouped_mlp_fwd(const moe_dims* d, const moe_bf16* x,
   __nv_bfloat16* h = at<__nv_bfloat16>(workspace, L.h);
   const int T = d->T, H = d->H, E = d->E, I = d->I;
   const long long S = L.S;
-  {  // gate/up grouped GEMM + SwiGLU; A = token rows of x gathered through the sort
-    CUtensorMap tB;
-    if (!make_map3(&tB, w_gate_up, H, 2LL * I, E, 64, 128)) return MOE_ERR_CUDA;
-    const CUtensorMap& tA = tB;  // unused: A is gathered
-    CUtensorMap tD0, tD1;
-    if (!make_out_map(&tD1, h, I, S)) return MOE_ERR_CUDA;
-    if (gu_saved) { if (!make_out_map(&tD0, gu_saved, 2LL * I, S)) return MOE_ERR_CUDA; }
-    else tD0 = tD1;
-    GemmArgs a = base_args(status);
-    a.N = 2 * I; a.K = H; a.G = E; a.offsets = expert_offsets;
-    a.gsrc = reinterpret_cast<const __nv_bfloat16*>(x); a.gld = H; a.gperm = perm_slot;
-    a.gdiv = d->k; a.gsrc_rows = T;
-    a.gu_out = reinterpret_cast<__nv_bfloat16*>(gu_saved); a.h_out = h; a.inter = I;
-    s = launch_gemm<CfgGateUp>(MOE_K_GATE_UP, tA, tB, tD0, tD1, a, (cdiv(S, moe::BM) + E) * cdiv(I, 128), st);
-    if (s != MOE_OK) return s;
-  }
+  s = launch_gate_up(*d, x, expert_offsets, perm_slot, w_gate_up, gu_saved, h, status, st);
+  if (s != MOE_OK) return s;
   {  // down grouped GEMM
     CUtensorMap tA, tB;
     if (!make_map(&tA, h, I, S, 1, 64, 128)) return MOE_ERR_CUDA;
@@ -528,20 +561,8 @@ moe_status moe_grouped_mlp_fwd(const moe_dims* d, const moe_bf16* x,
   if (d->I_shared > 0) {
     const int Is = d->I_shared;
     __nv_bfloat16* hs = at<__nv_bfloat16>(workspace, L.h_sh);
-    {
-      CUtensorMap tA, tB;
-      if (!make_map(&tA, x, H, T, 1, 64, 128)) return MOE_ERR_CUDA;
-      if (!make_map(&tB, w_sh_gate_up, H, 2LL * Is, 1, 64, 128)) return MOE_ERR_CUDA;
-      CUtensorMap tD0, tD1;
-      if (!make_out_map(&tD1, hs, Is, T)) return MOE_ERR_CUDA;
-      if (sh_gu_saved) { if (!make_out_map(&tD0, sh_gu_saved, 2LL * Is, T)) return MOE_ERR_CUDA; }
-      else tD0 = tD1;
-      GemmArgs a = base_args(status);
-      a.N = 2 * Is; a.K = H; a.G = 1; a.single_rows = T;
-      a.gu_out = reinterpret_cast<__nv_bfloat16*>(sh_gu_saved); a.h_out = hs; a.inter = Is;
-      s = launch_gemm<CfgGateUpShared>(MOE_K_SHARED_GATE_UP, tA, tB, tD0, tD1, a, cdiv(T, moe::BM) * cdiv(Is, 128), st);
-      if (s != MOE_OK) return s;
-    }
+    s = launch_shared_gate_up(*d, x, w_sh_gate_up, sh_gu_saved, hs, status, st);
+    if (s != MOE_OK) return s;
     {
       CUtensorMap tA, tB;
       if (!make_map(&tA, hs, Is, T, 1, 64, 128)) return MOE_ERR_CUDA;
@@ -595,11 +616,10 @@ moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_
   moe_status s = check_dims(d);
   if (s != MOE_OK) return s;
   if (!grad_out || !x || !w_router || !topk_idx || !topk_w || !expert_offsets || !perm_slot ||
-      !slot_perm || !w_gate_up || !w_down || !gu_saved || !grad_x || !grad_w_router ||
-      !grad_w_gate_up || !grad_w_down || !workspace)
+      !slot_perm || !w_gate_up || !w_down || !grad_x || !grad_w_router || !grad_w_gate_up ||
+      !grad_w_down || !workspace)
     return MOE_ERR_INVALID_ARG;
-  if (d->I_shared > 0 && (!w_sh_gate_up || !w_sh_down || !sh_gu_saved || !grad_w_sh_gate_up ||
-                          !grad_w_sh_down))
+  if (d->I_shared > 0 && (!w_sh_gate_up || !w_sh_down || !grad_w_sh_gate_up || !grad_w_sh_down))
     return MOE_ERR_INVALID_ARG;
   for (const void* p : {(const void*)grad_out, (const void*)x, (const void*)w_router,
                         (const void*)w_gate_up, (const void*)w_down, (const void*)gu_saved,
@@ -609,11 +629,27 @@ moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_
                         (const void*)grad_w_down, (const void*)grad_w_sh_gate_up,
                         (const void*)grad_w_sh_down, (const void*)workspace})
     if (!aligned16(p)) return MOE_ERR_INVALID_ARG;
-  const Layout L = make_layout(*d, true);
+  // pre-activations not saved by the forward are recomputed here (activation
+  // recompute), into the workspace
+  const bool rc_gu = gu_saved == nullptr;
+  const bool rc_sh = d->I_shared > 0 && sh_gu_saved == nullptr;
+  const Layout L = make_layout(*d, true, rc_gu || rc_sh);
   if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int* status = at<int>(workspace, 0);
   const int T = d->T, H = d->H, E = d->E, I = d->I, k = d->k;
+  if (rc_gu) {
+    moe_bf16* gu = at<moe_bf16>(workspace, L.gu_rc);
+    s = launch_gate_up(*d, x, expert_offsets, perm_slot, w_gate_up, gu, nullptr, status, st);
+    if (s != MOE_OK) return s;
+    gu_saved = gu;
+  }
+  if (rc_sh) {
+    moe_bf16* gu = at<moe_bf16>(workspace, L.sh_gu_rc);
+    s = launch_shared_gate_up(*d, x, w_sh_gate_up, gu, nullptr, status, st);
+    if (s != MOE_OK) return s;
+    sh_gu_saved = gu;
+  }
   const long long P = L.S_pad_max;
   int32_t* poff = at<int32_t>(workspace, L.poff);
   __nv_bfloat16* dgu = at<__nv_bfloat16>(workspace, L.dgu);

@@ -136,7 +136,9 @@ def moe_status_string(status: int) -> str:
     return load_library().moe_status_string(status).decode()
 
 
-def moe_workspace_size(dims, with_backward: bool) -> int:
+def moe_workspace_size(dims, with_backward) -> int:
+    """with_backward: 0 forward only, 1 backward with saved pre-activations,
+    2 backward that recomputes them (True/False map to 1/0)."""
     out = _SZ(0)
     _check("moe_workspace_size",
            load_library().moe_workspace_size(ctypes.byref(_dims(dims)), int(with_backward), ctypes.byref(out)))
@@ -234,7 +236,9 @@ class MoeLayer:
     """
 
     def __init__(self, dims, gate_mode=MOE_GATE_SOFTMAX_TOPK, device="cuda", with_backward=True,
-                 save_logits=False):
+                 save_logits=False, recompute=False):
+        """recompute: the forward keeps no gate/up pre-activations; the
+        backward recomputes them (activation recompute)."""
         self.dims = _dims(dims)
         T, H, E, k, I, Is = self.dims.as_tuple()
         S = T * k
@@ -247,12 +251,13 @@ class MoeLayer:
         self.expert_offsets = torch.empty(E + 1, dtype=i32, device=dev)
         self.perm_slot = torch.empty(S, dtype=i32, device=dev)
         self.slot_perm = torch.empty(S, dtype=i32, device=dev)
-        self.gu_saved = torch.empty(S, 2 * I, dtype=bf, device=dev) if with_backward else None
+        keep = with_backward and not recompute
+        self.gu_saved = torch.empty(S, 2 * I, dtype=bf, device=dev) if keep else None
         self.y_perm = torch.empty(S, H, dtype=bf, device=dev)
-        self.sh_gu_saved = torch.empty(T, 2 * Is, dtype=bf, device=dev) if (Is and with_backward) else None
+        self.sh_gu_saved = torch.empty(T, 2 * Is, dtype=bf, device=dev) if (Is and keep) else None
         self.y_shared = torch.empty(T, H, dtype=bf, device=dev) if Is else None
         self.out = torch.empty(T, H, dtype=bf, device=dev)
-        nbytes = moe_workspace_size(self.dims, with_backward)
+        nbytes = moe_workspace_size(self.dims, (2 if recompute else 1) if with_backward else 0)
         self.workspace = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
 
     def forward(self, x, w_router, w_gate_up, w_down, router_bias=None, w_sh_gate_up=None,

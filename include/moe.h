@@ -79,10 +79,14 @@ const char* moe_status_string(int32_t status);
 
 /*
  * Bytes of device workspace the calls below need for these dims.  One
- * workspace can serve moe_route, moe_permute, moe_grouped_mlp_fwd and (when
- * with_backward != 0) moe_layer_bwd.  The first 256 bytes hold the device
+ * workspace can serve moe_route, moe_permute, moe_grouped_mlp_fwd and, with
+ * with_backward = 1, moe_layer_bwd given the saved pre-activations; with
+ * with_backward = 2, also moe_layer_bwd recomputing them (gu_saved and/or
+ * sh_gu_saved NULL: room for [S,2I] and [T,2*I_shared] bf16 more).
+ * with_backward = 0: forward calls only.  The first 256 bytes hold the device
  * status word; callers zero them once (cudaMemset) before first use.
- * Errors: MOE_ERR_INVALID_ARG (null), MOE_ERR_UNSUPPORTED_SHAPE.
+ * Errors: MOE_ERR_INVALID_ARG (null, with_backward outside 0..2),
+ * MOE_ERR_UNSUPPORTED_SHAPE.
  */
 moe_status moe_workspace_size(const moe_dims* d, int32_t with_backward, size_t* bytes);
 
@@ -164,6 +168,12 @@ moe_status moe_unpermute_combine(const moe_dims* d, const moe_bf16* y_perm,
  *   grad_w_down [E,H,I], and when I_shared > 0 grad_w_sh_gate_up
  *   [2*I_shared,H], grad_w_sh_down [H,I_shared]; grad_router_bias fp32 [E]
  *   or NULL.
+ * Activation recompute (the activation checkpointing listed among the run's
+ * features, NeMo AutoModel blog, "性能对比", Nemotron 3 Ultra 550B method
+ * table): gu_saved = NULL (and/or sh_gu_saved = NULL) makes
+ * this call recompute those pre-activations with the forward's gate/up GEMM
+ * into the workspace (size it with moe_workspace_size(d, 2, ...)) instead of
+ * reading a copy kept since the forward; the gradients are bit-identical.
  * SwiGLU is recomputed from the saved (g, u).  Router: the renormalised
  * top-k weights are a softmax over the chosen logits, so
  * dlogit[t,e_j] = w_j (dw_j - sum_i w_i dw_i) with dw_j = <dout[t], y_j>,

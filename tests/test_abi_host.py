@@ -51,6 +51,13 @@ def test_workspace_size_covers_intermediates(lib):
     assert bwd > fwd + S * (2 * I + I + H) * 2        # dgu, w*h, per-slot dx
     sh = M.moe_workspace_size((8192, 2688, 128, 6, 1856, 3712), False)
     assert sh >= 8192 * 6 * 1856 * 2 + 8192 * 3712 * 2
+    # activation recompute: room for the recomputed gate/up pre-activations
+    rc = M.moe_workspace_size((T, H, E, k, I, 0), 2)
+    assert rc >= bwd + S * 2 * I * 2
+    d5 = (8192, 2688, 128, 6, 1856, 3712)
+    assert M.moe_workspace_size(d5, 2) >= M.moe_workspace_size(d5, 1) + 8192 * 6 * 2 * 1856 * 2 + 8192 * 2 * 3712 * 2
+    with pytest.raises(M.MoeError):
+        M.moe_workspace_size((T, H, E, k, I, 0), 3)
 
 
 @pytest.mark.parametrize("dims,code", [

@@ -174,3 +174,37 @@ def test_forward_backward_bit_identical_run_to_run():
                      g["grad_w_gate_up"].clone(), g["grad_w_router"].clone()])
     for a, b in zip(*outs):
         assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("name", ["ragged_shared", "skewed_mid"])
+def test_backward_recompute_matches_saved(name):
+    """Activation recompute: a backward that recomputes the gate/up
+    pre-activations (none saved by the forward) gives the same gradients, bit
+    for bit, as one reading the saved copy; and the forward's outputs match."""
+    w = CASES[name]
+    di = U.DeviceInputs(w, seed=1, with_grad=True)
+    outs = []
+    for recompute in (False, True):
+        layer = M.MoeLayer(di.dims, gate_mode=w.gate, with_backward=True, recompute=recompute)
+        layer.forward(di.x, di.w_router, di.w_gate_up, di.w_down, di.router_bias, di.w_sh_gate_up,
+                      di.w_sh_down)
+        assert (layer.gu_saved is None) == recompute
+        grads = layer.alloc_grads(with_bias=w.bias_std > 0)
+        layer.backward(di.grad_out, di.x, di.w_router, di.w_gate_up, di.w_down, grads,
+                       di.w_sh_gate_up, di.w_sh_down)
+        torch.cuda.synchronize()
+        assert M.moe_read_device_status(layer.workspace) == 0
+        outs.append((layer.out.clone(), {k: v.clone() for k, v in grads.items() if v is not None}))
+        idx = layer.topk_idx.cpu().numpy()
+    (o0, g0), (o1, g1) = outs
+    assert torch.equal(o0, o1)
+    assert g0.keys() == g1.keys()
+    for key in g0:
+        assert torch.equal(g0[key], g1[key]), key
+    # and against the oracle (on the device's routing, as in the other tests)
+    f = U.oracle_forward(di, topk_idx=idx)
+    b = O.layer_backward(f, di.f64("grad_out"), di.f64("x"), di.f64("w_router"),
+                         di.f64("w_gate_up"), di.f64("w_down"), w.k,
+                         w_sh_gu=di.f64("w_sh_gate_up"), w_sh_down=di.f64("w_sh_down"))
+    U.check_close(g1["grad_w_gate_up"], b["grad_w_gate_up"], "grad_w_gate_up (recompute)")
+    U.check_close(g1["grad_x"], b["grad_x"], "grad_x (recompute)")

@@ -280,6 +280,94 @@ def test_backward_matches_autograd_of_plain_torch_layer():
         assert np.allclose(t_.grad.numpy(), b[g], atol=1e-10), g
 
 
+# ---------------------------------------------------------------- auxiliary load-balancing loss
+def test_aux_loss_uniform_routing_is_alpha():
+    """Equal logits (uniform p) and the balanced gate (uniform counts): L = alpha."""
+    T, E, k = 12, 4, 2
+    p = O.softmax(np.zeros((T, E)))
+    idx = O.balanced_topk(T, E, k)
+    L, c = O.aux_loss(p, idx, 0.01)
+    assert abs(L - 0.01) < 1e-15
+    assert np.allclose(c, 0.01 * E * (1.0 / E) / T)
+
+
+def test_aux_loss_hand_example():
+    p = np.array([[0.7, 0.3], [0.4, 0.6]])
+    idx = np.array([[0], [0]])
+    L, c = O.aux_loss(p, idx, 0.5)
+    # f = [1, 0], P = [0.55, 0.45]: L = 0.5 * 2 * 0.55; c = 0.5 * 2 * f / 2
+    assert abs(L - 0.55) < 1e-15
+    assert np.allclose(c, [0.5, 0.0])
+
+
+def _loss_and_grads_aux(d, k, G_, alpha, balanced=False):
+    f = O.layer_forward(d["x"], d["w_router"], d["w_gu"], d["w_down"], k, balanced=balanced,
+                        bias=d["bias"])
+    L_aux, c = O.aux_loss(f["p"], f["topk_idx"], alpha)
+    b = O.layer_backward(f, G_, d["x"], d["w_router"], d["w_gu"], d["w_down"], k, aux_coef=c)
+    return float(np.sum(f["out"] * G_)) + L_aux, f, b
+
+
+@pytest.mark.parametrize("balanced", [False, True])
+def test_aux_loss_gradient_matches_finite_differences(balanced):
+    """J = <G, out> + L_aux: the backward with the aux coefficients against
+    central differences in x, W_r and the router bias (routing, hence the
+    counts, unchanged by the probes)."""
+    d = _tiny(T=6, H=8, E=4, k=2, I=8, seed=31)
+    T, H = d["x"].shape
+    G_ = np.random.default_rng(4).normal(size=(T, H))
+    alpha = 0.7   # large, so the aux term is not hidden by the main loss
+    _, f0, b = _loss_and_grads_aux(d, 2, G_, alpha, balanced)
+    eps = 1e-6
+    r = np.random.default_rng(6)
+    for pname, gname in [("x", "grad_x"), ("w_router", "grad_w_router"), ("bias", "grad_router_bias")]:
+        arr = d[pname]
+        for _ in range(10):
+            i = tuple(r.integers(0, s_) for s_ in arr.shape)
+            old = arr[i]
+            arr[i] = old + eps
+            lp, fp_, _ = _loss_and_grads_aux(d, 2, G_, alpha, balanced)
+            arr[i] = old - eps
+            lm, fm_, _ = _loss_and_grads_aux(d, 2, G_, alpha, balanced)
+            arr[i] = old
+            assert np.array_equal(fp_["topk_idx"], f0["topk_idx"]) and np.array_equal(fm_["topk_idx"], f0["topk_idx"])
+            num = (lp - lm) / (2 * eps)
+            assert abs(num - b[gname][i]) <= 1e-6 * max(1.0, abs(num)), (pname, i, num, b[gname][i])
+
+
+def test_aux_loss_gradient_matches_autograd():
+    """Autograd of L_aux = alpha E sum_e f_e mean_t p[t, e] written in torch,
+    with the counts f as constants, plus the main loss."""
+    T, H, E, k, I = 10, 16, 5, 2, 8
+    d = _tiny(T, H, E, k, I, seed=41)
+    G_ = np.random.default_rng(3).normal(size=(T, H))
+    alpha = 0.3
+    _, f, b = _loss_and_grads_aux(d, k, G_, alpha)
+    b0 = O.layer_backward(f, G_, d["x"], d["w_router"], d["w_gu"], d["w_down"], k)
+    x = torch.from_numpy(d["x"]).requires_grad_()
+    wr = torch.from_numpy(d["w_router"]).requires_grad_()
+    bias = torch.from_numpy(d["bias"]).requires_grad_()
+    p = torch.softmax(x @ wr.T + bias, dim=1)
+    counts = torch.zeros(E, dtype=torch.float64)
+    counts.index_add_(0, torch.from_numpy(f["topk_idx"].ravel().astype(np.int64)),
+                      torch.ones(T * k, dtype=torch.float64))
+    l_aux = alpha * E * torch.sum(counts / (T * k) * p.mean(dim=0))
+    l_aux.backward()
+    for t_, g in [(x, "grad_x"), (wr, "grad_w_router"), (bias, "grad_router_bias")]:
+        assert np.allclose(t_.grad.numpy(), b[g] - b0[g], atol=1e-12), g
+
+
+def test_mutation_aux_coefficients_without_token_mean_is_caught(monkeypatch):
+    good = O.aux_loss
+
+    def bad(p, topk_idx, alpha):
+        L, c = good(p, topk_idx, alpha)
+        return L, c * p.shape[0]   # forgets the 1/T of the token mean
+
+    monkeypatch.setattr(O, "aux_loss", bad)
+    assert _pins_fail(lambda: test_aux_loss_gradient_matches_finite_differences(False))
+
+
 # ---------------------------------------------------------------- whole workloads
 def test_tiny_workload_forward_invariants():
     w = G.WORKLOADS["tiny"]

@@ -336,6 +336,9 @@ def run_ours(args, w, rank, world):
     # activation recompute: the forward keeps no pre-activations, the backward recomputes them
     layer_rc = M.MoeLayer(dims, gate_mode=w.gate, device=dev, with_backward=True, recompute=True)
     grads_rc = layer_rc.alloc_grads(with_bias=bias is not None)
+    # with the auxiliary load-balancing loss (alpha = 0.01)
+    layer_aux = M.MoeLayer(dims, gate_mode=w.gate, device=dev, with_backward=True, aux_alpha=0.01)
+    grads_aux = layer_aux.alloc_grads(with_bias=bias is not None)
     stream = torch.cuda.current_stream(dev)
 
     def fwd():
@@ -351,6 +354,10 @@ def run_ours(args, w, rank, world):
     def step_rc():
         layer_rc.forward(x, wr, wgu, wd, bias, wsg, wsd)
         layer_rc.backward(go, x, wr, wgu, wd, grads_rc, wsg, wsd)
+
+    def step_aux():
+        layer_aux.forward(x, wr, wgu, wd, bias, wsg, wsd)
+        layer_aux.backward(go, x, wr, wgu, wd, grads_aux, wsg, wsd)
 
     def barrier():
         if world > 1:
@@ -399,6 +406,11 @@ def run_ours(args, w, rank, world):
         step_rc()
     ms_rc = timed(step_rc, args.steps)
     assert M.moe_read_device_status(layer_rc.workspace) == 0, "device reported an error"
+    # ---- forward + backward with the auxiliary load-balancing loss
+    for _ in range(max(1, args.warmup // 2)):
+        step_aux()
+    ms_aux = timed(step_aux, args.steps)
+    assert M.moe_read_device_status(layer_aux.workspace) == 0, "device reported an error"
 
     # ---- end to end: pinned host inputs in, result out, every step
     xh = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
@@ -485,6 +497,11 @@ def run_ours(args, w, rank, world):
                       "ms_per_step": ms_rc / args.steps,
                       "saved_bytes_not_held": w.T * w.k * 2 * w.I * 2 + w.T * 2 * w.I_shared * 2,
                       "extra_flops": 2.0 * w.T * w.k * w.H * 2 * w.I + 2.0 * w.T * w.H * 2 * w.I_shared},
+        # forward+backward with the auxiliary load-balancing loss (alpha 0.01): its value
+        # on the device, and the step time with its dense router gradient
+        "aux_loss": {"tokens_per_s": job_tokens_per_s(w.T, world, args.steps, ms_aux),
+                     "ms_per_step": ms_aux / args.steps,
+                     "value": float(layer_aux.aux_loss.item()), "alpha": 0.01},
         "layer_roofline": {
             "fwd": {"t_roof_us": t_roof_f * 1e6, "t_us": t_f * 1e6, "frac": t_roof_f / t_f,
                     "flops": f_fwd, "bytes": b_fwd},

@@ -33,12 +33,68 @@ __device__ __forceinline__ bool topk_before(float va, int ia, float vb, int ib) 
   return va > vb || (va == vb && ia < ib);
 }
 
+constexpr int kMaxGroupsRouter = 256;  // E <= 256
+
+// This lane's experts' softmax probabilities p[t, e] (e = 32 i + lane) of
+// token t, from the split-K partial logits (summed in split order) + bias;
+// zero for t >= T or e >= E.
+__device__ __forceinline__ void router_token_probs(const float* __restrict__ partial, int splits,
+                                                   const float* __restrict__ bias, int t, int T,
+                                                   int E, int lane, float (&pl)[kRouterMaxPerLane]) {
+  float mx = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < kRouterMaxPerLane; ++i) {
+    const int e = i * 32 + lane;
+    pl[i] = -INFINITY;
+    if (t < T && e < E) {
+      float l = 0.f;
+      for (int sp = 0; sp < splits; ++sp) l += __ldg(partial + ((size_t)sp * T + t) * E + e);
+      if (bias) l += __ldg(bias + e);
+      pl[i] = l;
+      mx = fmaxf(mx, l);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  float z = 0.f;
+#pragma unroll
+  for (int i = 0; i < kRouterMaxPerLane; ++i) {
+    pl[i] = (i * 32 + lane < E && t < T) ? expf(pl[i] - mx) : 0.f;
+    z += pl[i];
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+#pragma unroll
+  for (int i = 0; i < kRouterMaxPerLane; ++i) pl[i] = t < T ? pl[i] / z : 0.f;
+}
+
+// psum_part (optional): per block (8 tokens), sum over its tokens of p[t, e]
+// for every expert (warp order), for the auxiliary load-balancing loss.
+constexpr int kTopkWarps = 8;  // tokens per block of the top-k kernel
 __global__ void router_topk_kernel(const float* __restrict__ partial, int splits,
                                    const float* __restrict__ bias, float* __restrict__ logits_out,
                                    int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
-                                   int T, int E, int k, int gate_mode) {
+                                   float* __restrict__ psum_part, int T, int E, int k,
+                                   int gate_mode) {
   const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
+  if (psum_part) {
+    // block-wide sum of the tokens' softmax rows (the only block-level step)
+    __shared__ float prow[kTopkWarps][kMaxGroupsRouter];
+    float pl[kRouterMaxPerLane];
+    router_token_probs(partial, splits, bias, t, T, E, lane, pl);
+    const int wi = threadIdx.x >> 5;
+#pragma unroll
+    for (int i = 0; i < kRouterMaxPerLane; ++i)
+      if (i * 32 + lane < E) prow[wi][i * 32 + lane] = pl[i];
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+      float acc = 0.f;
+#pragma unroll
+      for (int w = 0; w < kTopkWarps; ++w) acc += prow[w][e];
+      psum_part[(size_t)blockIdx.x * E + e] = acc;
+    }
+  }
   if (t >= T) return;
   float v[kRouterMaxPerLane];
   float mx = -INFINITY;
@@ -309,8 +365,8 @@ __global__ void dx_gather_kernel(const __nv_bfloat16* __restrict__ dx_slot,
                                  int nNB, const __nv_bfloat16* __restrict__ w_router,
                                  const __nv_bfloat16* __restrict__ dx_shared,
                                  float* __restrict__ dl_out, __nv_bfloat16* __restrict__ dl_dense,
-                                 int ldE, __nv_bfloat16* __restrict__ dx, int T, int H, int k, int E,
-                                 int P) {
+                                 int ldE, int router_term, __nv_bfloat16* __restrict__ dx, int T,
+                                 int H, int k, int E, int P) {
   const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
@@ -351,7 +407,8 @@ __global__ void dx_gather_kernel(const __nv_bfloat16* __restrict__ dx_slot,
     for (int j = 0; j < KMAX; ++j) {
       if (j < k) {
         v[j] = __ldg(reinterpret_cast<const uint4*>(dx_slot + (size_t)rows[j] * H) + c);
-        r[j] = __ldg(reinterpret_cast<const uint4*>(w_router + (size_t)es[j] * H) + c);
+        r[j] = router_term ? __ldg(reinterpret_cast<const uint4*>(w_router + (size_t)es[j] * H) + c)
+                           : make_uint4(0u, 0u, 0u, 0u);
       }
     }
     uint4 vs = make_uint4(0, 0, 0, 0);
@@ -396,11 +453,12 @@ __global__ void dx_gather_kernel(const __nv_bfloat16* __restrict__ dx_slot,
 // bf16 (thread = 4 consecutive elements of dW_r, up to 16 splits' loads in
 // flight at once); the first E warps of the grid also form db[e] = sum of the
 // fp32 dl over expert e's rows (sorted order, lane-strided partial sums, then a
-// fixed butterfly).
+// fixed butterfly; with the auxiliary loss the dense per-block partials).
 __global__ void router_wgrad_reduce_kernel(const float* __restrict__ part, int nsplit, int E, int H,
                                            const int32_t* __restrict__ expert_offsets,
                                            const int32_t* __restrict__ perm_slot,
                                            const float* __restrict__ dl,
+                                           const float* __restrict__ db_part, int db_nblk,
                                            __nv_bfloat16* __restrict__ dw_router,
                                            float* __restrict__ dbias) {
   const long long n4 = (long long)E * H / 4;
@@ -425,14 +483,146 @@ __global__ void router_wgrad_reduce_kernel(const float* __restrict__ part, int n
   const int gw = (int)(((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (dbias && gw < E) {
+    // db[e]: the routed rows' dl or, with the auxiliary loss (dense logit
+    // gradient), the per-block column sums of every token's
     const int e = gw;
-    const int r0 = __ldg(expert_offsets + e), r1 = __ldg(expert_offsets + e + 1);
     float b = 0.f;
-    for (int r = r0 + lane; r < r1; r += 32) b += __ldg(dl + __ldg(perm_slot + r));
+    if (db_part) {
+      for (int blk = lane; blk < db_nblk; blk += 32) b += __ldg(db_part + (size_t)blk * E + e);
+    } else {
+      const int r0 = __ldg(expert_offsets + e), r1 = __ldg(expert_offsets + e + 1);
+      for (int r = r0 + lane; r < r1; r += 32) b += __ldg(dl + __ldg(perm_slot + r));
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) b += __shfl_xor_sync(0xffffffffu, b, o);
     if (lane == 0) dbias[e] = b;
   }
+}
+
+// ---------------------------------------------------------------- auxiliary load-balancing loss
+// Switch-Transformer form (the load-balancing auxiliary loss named on the
+// pages): L_aux = alpha E sum_e f_e P_e with f_e = count_e / (T k) the fraction
+// of slots routed to e and P_e = (1/T) sum_t p[t, e].  The counts pass no
+// gradient, so dL_aux/dp[t, e] = c_e = alpha E f_e / T.
+
+// prob_sum[e] = sum over the top-k kernel's blocks (in order) of their sums of p[t, e].
+__global__ void prob_sum_kernel(const float* __restrict__ psum_part, int nblk, int E,
+                                float* __restrict__ prob_sum) {
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= E) return;
+  float s = 0.f;
+  for (int b = 0; b < nblk; ++b) s += __ldg(psum_part + (size_t)b * E + e);
+  prob_sum[e] = s;
+}
+
+// One block: coef[e] = alpha E f_e / T and loss = sum_e alpha E f_e prob_sum[e] / T
+// (per-thread partial sums over e, then a fixed tree over the block).
+constexpr int kAuxThreads = 256;
+__global__ void aux_loss_kernel(const float* __restrict__ prob_sum,
+                                const int32_t* __restrict__ expert_offsets, int T, int E, int k,
+                                float alpha, float* __restrict__ loss, float* __restrict__ coef) {
+  __shared__ float part[kAuxThreads];
+  float acc = 0.f;
+  for (int e = threadIdx.x; e < E; e += kAuxThreads) {
+    const float f = (float)(__ldg(expert_offsets + e + 1) - __ldg(expert_offsets + e)) /
+                    ((float)T * (float)k);
+    const float c = alpha * (float)E * f / (float)T;
+    if (coef) coef[e] = c;
+    acc += c * __ldg(prob_sum + e);
+  }
+  part[threadIdx.x] = acc;
+  __syncthreads();
+  for (int w = kAuxThreads / 2; w > 0; w >>= 1) {
+    if (threadIdx.x < w) part[threadIdx.x] += part[threadIdx.x + w];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0 && loss) *loss = part[0];
+}
+
+// The dense logit gradient with the auxiliary loss, one warp per token:
+//   p = softmax(logits[t]); s = sum_e c_e p_e;
+//   DL[t, e] = dl_main[t, e] + p_e (c_e - s)
+// where dl_main is the top-k weights' gradient on the token's selected experts
+// (fp32 per slot) and zero elsewhere; DL is written once in bf16 ([T, ldE],
+// zero padding), and each block (8 tokens) writes its fp32 column sums (warp
+// order) for the bias gradient.
+constexpr int kAuxDlWarps = 8;
+template <int KMAX>
+__global__ void aux_dl_kernel(const float* __restrict__ logits, const float* __restrict__ coef,
+                              const int32_t* __restrict__ topk_idx, const float* __restrict__ dl,
+                              int T, int E, int k, int ldE, __nv_bfloat16* __restrict__ dl_dense,
+                              float* __restrict__ db_part) {
+  __shared__ float rows[kAuxDlWarps][kMaxGroupsRouter];
+  const int wi = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kAuxDlWarps + wi;
+  float lv[kRouterMaxPerLane];
+  float mx = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < kRouterMaxPerLane; ++i) {
+    const int e = i * 32 + lane;
+    lv[i] = (t < T && e < E) ? __ldg(logits + (size_t)t * E + e) : -INFINITY;
+    mx = fmaxf(mx, lv[i]);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  float z = 0.f;
+#pragma unroll
+  for (int i = 0; i < kRouterMaxPerLane; ++i) {
+    lv[i] = (t < T && i * 32 + lane < E) ? expf(lv[i] - mx) : 0.f;
+    z += lv[i];
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < kRouterMaxPerLane; ++i) {
+    const int e = i * 32 + lane;
+    lv[i] = t < T ? lv[i] / z : 0.f;
+    if (e < E) s += __ldg(coef + e) * lv[i];
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  int sel_e = -1;
+  float sel_d = 0.f;
+  if (t < T && lane < k) {
+    sel_e = __ldg(topk_idx + (size_t)t * k + lane);
+    sel_d = __ldg(dl + (size_t)t * k + lane);
+  }
+#pragma unroll
+  for (int i = 0; i < kRouterMaxPerLane; ++i) {
+    const int e = i * 32 + lane;
+    float main_d = 0.f;
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+      const int ej = __shfl_sync(0xffffffffu, sel_e, j);
+      const float dj = __shfl_sync(0xffffffffu, sel_d, j);
+      if (j < k && ej == e) main_d = dj;
+    }
+    const float v = (e < E && t < T) ? main_d + lv[i] * (__ldg(coef + (e < E ? e : 0)) - s) : 0.f;
+    if (e < E) rows[wi][e] = v;
+    if (t < T && e < ldE) dl_dense[(size_t)t * ldE + e] = __float2bfloat16_rn(v);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    float acc = 0.f;
+#pragma unroll
+    for (int w = 0; w < kAuxDlWarps; ++w) acc += rows[w][e];
+    db_part[(size_t)blockIdx.x * E + e] = acc;
+  }
+}
+
+// grad_x += r (bf16, 8 elements per thread).
+__global__ void add_bf16_kernel(__nv_bfloat16* __restrict__ dst, const __nv_bfloat16* __restrict__ r,
+                                long long n8) {
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n8) return;
+  uint4 a = reinterpret_cast<const uint4*>(dst)[i];
+  const uint4 b = __ldg(reinterpret_cast<const uint4*>(r) + i);
+  a.x = pack_bf16x2(bf16lo(a.x) + bf16lo(b.x), bf16hi(a.x) + bf16hi(b.x));
+  a.y = pack_bf16x2(bf16lo(a.y) + bf16lo(b.y), bf16hi(a.y) + bf16hi(b.y));
+  a.z = pack_bf16x2(bf16lo(a.z) + bf16lo(b.z), bf16hi(a.z) + bf16hi(b.z));
+  a.w = pack_bf16x2(bf16lo(a.w) + bf16lo(b.w), bf16hi(a.w) + bf16hi(b.w));
+  reinterpret_cast<uint4*>(dst)[i] = a;
 }
 
 }  // namespace moe

@@ -22,7 +22,7 @@ namespace {
 using moe::GemmArgs;
 using moe::GemmCfg;
 
-constexpr int32_t kAbiVersion = 7;
+constexpr int32_t kAbiVersion = 8;
 constexpr size_t kAlign = 256;
 
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
@@ -46,9 +46,9 @@ constexpr int kMaxRouterSplits = 8;
 constexpr int kDwParts = 1;  // column parts of the down data-gradient epilogue (epilogue warps / 4)
 
 struct Layout {
-  size_t status, counts, logits_part, h, h_sh, fwd_end;
-  size_t poff, dgu, hw, dxs, dwp, dl, dlb, rwp, dgu_sh, hw_sh, dxs_sh, gu_rc, sh_gu_rc,
-      total;
+  size_t status, counts, logits_part, psum_part, h, h_sh, fwd_end;
+  size_t poff, dgu, hw, dxs, dwp, dl, dlb, rwp, db_part, dgu_sh, hw_sh, dxs_sh, gu_rc,
+      sh_gu_rc, total;
   int sort_blocks;
   long long S, S_pad_max;
   int nNB_I;  // 256-wide column blocks of the intermediate (dgrad-down tiles)
@@ -86,6 +86,7 @@ Layout make_layout(const moe_dims& d, bool bwd, bool recompute = false) {
   L.status = o; o += kAlign;
   L.counts = o; o = align_up(o + (size_t)L.sort_blocks * d.E * 4);
   L.logits_part = o; o = align_up(o + (size_t)kMaxRouterSplits * d.T * d.E * 4);
+  L.psum_part = o; o = align_up(o + (size_t)((d.T + moe::kTopkWarps - 1) / moe::kTopkWarps) * d.E * 4);
   L.h = o; o = align_up(o + (size_t)L.S * d.I * 2);
   L.h_sh = o; o = align_up(o + (size_t)d.T * d.I_shared * 2);
   L.fwd_end = o;
@@ -100,6 +101,7 @@ Layout make_layout(const moe_dims& d, bool bwd, bool recompute = false) {
     const RwSplit rs = rw_split(d);
     L.dlb = o; o = align_up(o + (size_t)d.T * rs.ldE * 2);
     L.rwp = o; o = align_up(o + (size_t)rs.nsplit * d.E * d.H * 4);
+    L.db_part = o; o = align_up(o + (size_t)((d.T + moe::kAuxDlWarps - 1) / moe::kAuxDlWarps) * d.E * 4);
     L.dgu_sh = o; o = align_up(o + (size_t)d.T * 2 * d.I_shared * 2);
     L.hw_sh = o; o = align_up(o + (size_t)d.T * d.I_shared * 2);
     L.dxs_sh = o; o = align_up(o + (size_t)(d.I_shared ? d.T : 0) * d.H * 2);
@@ -260,6 +262,8 @@ using CfgRouter =
     GemmCfg<BN, (BN >= 256 ? 4 : 6), KMAJ_TILE, KMAJ_TILE, RAGGED_K, EPI_STORE_F32, false, false>;
 // router weight gradient: A = DL [tokens, E] and B = x [tokens, H], both MN-major
 using CfgRouterW = GemmCfg<256, 4, MN_TILE, MN_TILE, RAGGED_K, EPI_STORE_F32, false, false>;
+// router term of grad_x with the auxiliary loss: DL [tokens, E] (K-major) x W_r [E, H] (MN-major)
+using CfgRouterDx = GemmCfg<256, 3, KMAJ_TILE, MN_TILE, RAGGED_M, EPI_STORE, false, false>;
 // Every BN=256 GEMM runs as CTA pairs: 256 x 256 tiles by cta_group::2 UMMAs,
 // each CTA staging its 128 A rows and half of the B tile (32 KB per stage).
 // The ragged-M GEMMs stream K = 768..2048 per tile through 5 stages with 3
@@ -410,8 +414,8 @@ moe_status moe_workspace_size(const moe_dims* d, int32_t with_backward, size_t* 
 
 moe_status moe_route(const moe_dims* d, int32_t gate_mode, const moe_bf16* x,
                      const moe_bf16* w_router, const float* router_bias, float* logits_out,
-                     int32_t* topk_idx, float* topk_w, void* workspace, size_t workspace_bytes,
-                     void* stream) {
+                     int32_t* topk_idx, float* topk_w, float* prob_sum, void* workspace,
+                     size_t workspace_bytes, void* stream) {
   moe_status s = check_dims(d);
   if (s != MOE_OK) return s;
   if (gate_mode != MOE_GATE_SOFTMAX_TOPK && gate_mode != MOE_GATE_BALANCED)
@@ -451,11 +455,29 @@ moe_status moe_route(const moe_dims* d, int32_t gate_mode, const moe_bf16* x,
     default: s = launch_gemm<CfgRouter<256>>(MOE_K_ROUTER, tA, tB, tD, tD, a, tiles, st); break;
   }
   if (s != MOE_OK) return s;
+  const unsigned tk_blocks = (unsigned)cdiv((long long)T, moe::kTopkWarps);
+  float* psum = prob_sum ? at<float>(workspace, L.psum_part) : nullptr;
   {
     KernelScope ks(MOE_K_ROUTER_TOPK, st);
-    moe::router_topk_kernel<<<(unsigned)cdiv((long long)T * 32, 256), 256, 0, st>>>(
-        part, splits, router_bias, logits_out, topk_idx, topk_w, T, E, d->k, gate_mode);
+    moe::router_topk_kernel<<<tk_blocks, 32 * moe::kTopkWarps, 0, st>>>(
+        part, splits, router_bias, logits_out, topk_idx, topk_w, psum, T, E, d->k, gate_mode);
   }
+  if (prob_sum) {  // sum over tokens of the router softmax (auxiliary loss), in block order
+    KernelScope ks(MOE_K_AUX, st);
+    moe::prob_sum_kernel<<<(unsigned)cdiv(E, 128), 128, 0, st>>>(psum, (int)tk_blocks, E, prob_sum);
+  }
+  return launched(cudaGetLastError());
+}
+
+moe_status moe_aux_loss(const moe_dims* d, const float* prob_sum, const int32_t* expert_offsets,
+                        float alpha, float* loss, float* coef, void* stream) {
+  moe_status s = check_dims(d);
+  if (s != MOE_OK) return s;
+  if (!prob_sum || !expert_offsets || (!loss && !coef)) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  KernelScope ks(MOE_K_AUX, st);
+  moe::aux_loss_kernel<<<1, moe::kAuxThreads, 0, st>>>(prob_sum, expert_offsets, d->T, d->E, d->k,
+                                                        alpha, loss, coef);
   return launched(cudaGetLastError());
 }
 
@@ -611,9 +633,12 @@ moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_
                          const moe_bf16* sh_gu_saved, moe_bf16* grad_x, moe_bf16* grad_w_router,
                          float* grad_router_bias, moe_bf16* grad_w_gate_up,
                          moe_bf16* grad_w_down, moe_bf16* grad_w_sh_gate_up,
-                         moe_bf16* grad_w_sh_down, void* workspace, size_t workspace_bytes,
+                         moe_bf16* grad_w_sh_down, const float* router_logits,
+                         const float* aux_coef, void* workspace, size_t workspace_bytes,
                          void* stream) {
   moe_status s = check_dims(d);
+  const bool aux = aux_coef != nullptr;
+  if (aux && !router_logits) return MOE_ERR_INVALID_ARG;
   if (s != MOE_OK) return s;
   if (!grad_out || !x || !w_router || !topk_idx || !topk_w || !expert_offsets || !perm_slot ||
       !slot_perm || !w_gate_up || !w_down || !grad_x || !grad_w_router || !grad_w_gate_up ||
@@ -731,11 +756,25 @@ moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_
     if (k <= 8)
       moe::dx_gather_kernel<8><<<blocks, 256, 0, st>>>(dxs, topk_idx, topk_w, slot_perm,
                                                        expert_offsets, poff, dwp, L.nDW, wr,
-                                                       dxs_sh, dl, dlb, rs.ldE, gx, T, H, k, E, (int)P);
+                                                       dxs_sh, dl, aux ? nullptr : dlb, rs.ldE,
+                                                       aux ? 0 : 1, gx, T, H, k, E, (int)P);
     else
       moe::dx_gather_kernel<32><<<blocks, 256, 0, st>>>(dxs, topk_idx, topk_w, slot_perm,
                                                         expert_offsets, poff, dwp, L.nDW, wr,
-                                                        dxs_sh, dl, dlb, rs.ldE, gx, T, H, k, E, (int)P);
+                                                        dxs_sh, dl, aux ? nullptr : dlb, rs.ldE,
+                                                        aux ? 0 : 1, gx, T, H, k, E, (int)P);
+  }
+  float* dbp = at<float>(workspace, L.db_part);
+  const int aux_blocks = (int)cdiv((long long)T, moe::kAuxDlWarps);
+  if (aux) {  // dense logit gradient with the auxiliary loss's term (and its column sums)
+    KernelScope ks(MOE_K_AUX, st);
+    if (k <= 8)
+      moe::aux_dl_kernel<8><<<(unsigned)aux_blocks, 32 * moe::kAuxDlWarps, 0, st>>>(
+          router_logits, aux_coef, topk_idx, dl, T, E, k, rs.ldE, dlb, dbp);
+    else
+      moe::aux_dl_kernel<32><<<(unsigned)aux_blocks, 32 * moe::kAuxDlWarps, 0, st>>>(
+          router_logits, aux_coef, topk_idx, dl, T, E, k, rs.ldE, dlb, dbp);
+    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
   }
   {  // router weight gradient: dW_r = DL^T x, split-K over the tokens (fp32 partials) ...
     CUtensorMap tA, tB, tD;
@@ -754,8 +793,25 @@ moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_
     const long long n4 = (long long)E * H / 4;
     const long long blocks = std::max<long long>(cdiv(n4, 256), cdiv((long long)E * 32, 256));
     moe::router_wgrad_reduce_kernel<<<(unsigned)blocks, 256, 0, st>>>(
-        rwp, rs.nsplit, E, H, expert_offsets, perm_slot, dl,
+        rwp, rs.nsplit, E, H, expert_offsets, perm_slot, dl, aux ? dbp : nullptr, aux_blocks,
         reinterpret_cast<__nv_bfloat16*>(grad_w_router), grad_router_bias);
+    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  if (aux) {  // the router's term of grad_x, dense over the experts: DL W_r (a small GEMM) ...
+    __nv_bfloat16* rx = dxs;  // free again after the gather-sum
+    CUtensorMap tA, tB, tD;
+    if (!make_map(&tA, dlb, rs.ldE, T, 1, 64, 128)) return MOE_ERR_CUDA;
+    if (!make_map(&tB, w_router, H, E, 1, 64, 64)) return MOE_ERR_CUDA;
+    if (!make_out_map(&tD, rx, H, T)) return MOE_ERR_CUDA;
+    GemmArgs a = base_args(status);
+    a.N = H; a.K = (int)(cdiv(rs.ldE, moe::BK) * moe::BK); a.G = 1; a.single_rows = T;
+    a.d = rx; a.ldd = H;
+    s = launch_gemm<CfgRouterDx>(MOE_K_AUX, tA, tB, tD, tD, a, cdiv(T, moe::BM) * cdiv(H, 256), st);
+    if (s != MOE_OK) return s;
+    KernelScope ks(MOE_K_AUX, st);  // ... added into grad_x
+    const long long n8 = (long long)T * H / 8;
+    moe::add_bf16_kernel<<<(unsigned)cdiv(n8, 256), 256, 0, st>>>(
+        reinterpret_cast<__nv_bfloat16*>(grad_x), rx, n8);
     if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
   }
   {  // dW_down[e] = sum over the expert's rows of dout[token]^T (w h)
@@ -828,7 +884,7 @@ const char* moe_kernel_name(int32_t id) {
       "down", "shared_gate_up", "shared_down", "combine", "dgrad_down",
       "dgrad_gate_up", "shared_dgrad_down", "shared_dgrad_gate_up", "dx_gather",
       "router_wgrad", "wgrad_down", "wgrad_gate_up", "shared_wgrad_down",
-      "shared_wgrad_gate_up", "router_wgrad_reduce"};
+      "shared_wgrad_gate_up", "router_wgrad_reduce", "aux_loss"};
   return (id >= 0 && id < MOE_K_COUNT) ? names[id] : "unknown";
 }
 

@@ -57,11 +57,12 @@ _SIGS = {
     "moe_abi_version": ([], _I32),
     "moe_status_string": ([_I32], ctypes.c_char_p),
     "moe_workspace_size": ([_DIMS, _I32, ctypes.POINTER(_SZ)], _I32),
-    "moe_route": ([_DIMS, _I32, _P, _P, _P, _P, _P, _P, _P, _SZ, _P], _I32),
+    "moe_route": ([_DIMS, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P], _I32),
+    "moe_aux_loss": ([_DIMS, _P, _P, ctypes.c_float, _P, _P, _P], _I32),
     "moe_permute": ([_DIMS, _P, _P, _P, _P, _P, _SZ, _P], _I32),
     "moe_grouped_mlp_fwd": ([_DIMS, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P], _I32),
     "moe_unpermute_combine": ([_DIMS, _P, _P, _P, _P, _P, _P], _I32),
-    "moe_layer_bwd": ([_DIMS] + [_P] * 21 + [_P, _SZ, _P], _I32),
+    "moe_layer_bwd": ([_DIMS] + [_P] * 23 + [_P, _SZ, _P], _I32),
     "moe_read_device_status": ([_P, _SZ, _P, _I32, ctypes.POINTER(_I32)], _I32),
     "moe_permute_static_scratch": ([_DIMS, _P, _P, _P, _P, _P, _P], _I32),
     "moe_kernel_count": ([], _I32),
@@ -146,11 +147,17 @@ def moe_workspace_size(dims, with_backward) -> int:
 
 
 def moe_route(dims, gate_mode, x, w_router, router_bias, logits_out, topk_idx, topk_w, workspace,
-              stream=None):
+              stream=None, prob_sum=None):
     p, n = _ws(workspace)
     _check("moe_route", load_library().moe_route(
         ctypes.byref(_dims(dims)), int(gate_mode), _ptr(x), _ptr(w_router), _ptr(router_bias),
-        _ptr(logits_out), _ptr(topk_idx), _ptr(topk_w), p, n, _stream(stream)))
+        _ptr(logits_out), _ptr(topk_idx), _ptr(topk_w), _ptr(prob_sum), p, n, _stream(stream)))
+
+
+def moe_aux_loss(dims, prob_sum, expert_offsets, alpha, loss, coef, stream=None):
+    _check("moe_aux_loss", load_library().moe_aux_loss(
+        ctypes.byref(_dims(dims)), _ptr(prob_sum), _ptr(expert_offsets), ctypes.c_float(alpha),
+        _ptr(loss), _ptr(coef), _stream(stream)))
 
 
 def moe_permute(dims, topk_idx, expert_offsets, perm_slot, slot_perm, workspace, stream=None):
@@ -178,12 +185,13 @@ def moe_unpermute_combine(dims, y_perm, slot_perm, topk_w, y_shared, out, stream
 def moe_layer_bwd(dims, grad_out, x, w_router, topk_idx, topk_w, expert_offsets, perm_slot,
                   slot_perm, w_gate_up, w_down, gu_saved, w_sh_gate_up, w_sh_down, sh_gu_saved,
                   grad_x, grad_w_router, grad_router_bias, grad_w_gate_up, grad_w_down,
-                  grad_w_sh_gate_up, grad_w_sh_down, workspace, stream=None):
+                  grad_w_sh_gate_up, grad_w_sh_down, workspace, stream=None, router_logits=None,
+                  aux_coef=None):
     p, n = _ws(workspace)
     args = [grad_out, x, w_router, topk_idx, topk_w, expert_offsets, perm_slot, slot_perm,
             w_gate_up, w_down, gu_saved, w_sh_gate_up, w_sh_down, sh_gu_saved, grad_x,
             grad_w_router, grad_router_bias, grad_w_gate_up, grad_w_down, grad_w_sh_gate_up,
-            grad_w_sh_down]
+            grad_w_sh_down, router_logits, aux_coef]
     _check("moe_layer_bwd", load_library().moe_layer_bwd(
         ctypes.byref(_dims(dims)), *[_ptr(a) for a in args], p, n, _stream(stream)))
 
@@ -236,16 +244,23 @@ class MoeLayer:
     """
 
     def __init__(self, dims, gate_mode=MOE_GATE_SOFTMAX_TOPK, device="cuda", with_backward=True,
-                 save_logits=False, recompute=False):
+                 save_logits=False, recompute=False, aux_alpha=None):
         """recompute: the forward keeps no gate/up pre-activations; the
-        backward recomputes them (activation recompute)."""
+        backward recomputes them (activation recompute).  aux_alpha: add the
+        auxiliary load-balancing loss with this coefficient (its value lands
+        in self.aux_loss after forward; its gradient is added in backward)."""
         self.dims = _dims(dims)
         T, H, E, k, I, Is = self.dims.as_tuple()
         S = T * k
         self.gate_mode = gate_mode
         dev = torch.device(device)
         bf, i32, f32 = torch.bfloat16, torch.int32, torch.float32
-        self.logits = torch.empty(T, E, dtype=f32, device=dev) if save_logits else None
+        self.aux_alpha = aux_alpha
+        aux = aux_alpha is not None
+        self.logits = torch.empty(T, E, dtype=f32, device=dev) if (save_logits or aux) else None
+        self.prob_sum = torch.empty(E, dtype=f32, device=dev) if aux else None
+        self.aux_loss = torch.zeros(1, dtype=f32, device=dev) if aux else None
+        self.aux_coef = torch.empty(E, dtype=f32, device=dev) if aux else None
         self.topk_idx = torch.empty(T, k, dtype=i32, device=dev)
         self.topk_w = torch.empty(T, k, dtype=f32, device=dev)
         self.expert_offsets = torch.empty(E + 1, dtype=i32, device=dev)
@@ -264,8 +279,11 @@ class MoeLayer:
                 w_sh_down=None, stream=None):
         d, ws = self.dims, self.workspace
         moe_route(d, self.gate_mode, x, w_router, router_bias, self.logits, self.topk_idx,
-                  self.topk_w, ws, stream)
+                  self.topk_w, ws, stream, prob_sum=self.prob_sum)
         moe_permute(d, self.topk_idx, self.expert_offsets, self.perm_slot, self.slot_perm, ws, stream)
+        if self.aux_alpha is not None:
+            moe_aux_loss(d, self.prob_sum, self.expert_offsets, self.aux_alpha, self.aux_loss,
+                         self.aux_coef, stream)
         moe_grouped_mlp_fwd(d, x, self.expert_offsets, self.perm_slot, w_gate_up, w_down,
                             self.gu_saved, self.y_perm, w_sh_gate_up, w_sh_down, self.sh_gu_saved,
                             self.y_shared, ws, stream)
@@ -293,5 +311,6 @@ class MoeLayer:
                       self.gu_saved, w_sh_gate_up, w_sh_down, self.sh_gu_saved, grads["grad_x"],
                       grads["grad_w_router"], grads["grad_router_bias"], grads["grad_w_gate_up"],
                       grads["grad_w_down"], grads["grad_w_sh_gate_up"], grads["grad_w_sh_down"],
-                      self.workspace, stream)
+                      self.workspace, stream, router_logits=self.logits if self.aux_coef is not None else None,
+                      aux_coef=self.aux_coef)
         return grads

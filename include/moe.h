@@ -100,13 +100,33 @@ moe_status moe_workspace_size(const moe_dims* d, int32_t with_backward, size_t* 
  *   BALANCED:     topk_idx[t,j] = (t*k + j) mod E  (exactly T*k/E slots per
  *                 expert when E divides T*k; distinct experts when k <= E)
  *   topk_w[t,j] = p[t,topk_idx[t,j]] / sum_j' p[t,topk_idx[t,j']]
+ *   prob_sum[e] = sum_t p[t,e]   (optional; for moe_aux_loss)
  * x: bf16 [T,H]; w_router: bf16 [E,H]; router_bias: fp32 [E] or NULL;
- * logits_out: fp32 [T,E] or NULL; topk_idx: int32 [T,k]; topk_w: fp32 [T,k].
+ * logits_out: fp32 [T,E] or NULL; topk_idx: int32 [T,k]; topk_w: fp32 [T,k];
+ * prob_sum: fp32 [E] or NULL (a fixed-order sum: bit-identical run to run).
  */
 moe_status moe_route(const moe_dims* d, int32_t gate_mode, const moe_bf16* x,
                      const moe_bf16* w_router, const float* router_bias, float* logits_out,
-                     int32_t* topk_idx, float* topk_w, void* workspace, size_t workspace_bytes,
-                     void* stream);
+                     int32_t* topk_idx, float* topk_w, float* prob_sum, void* workspace,
+                     size_t workspace_bytes, void* stream);
+
+/*
+ * Auxiliary load-balancing loss ("NVIDIA NeMo AutoModel MoE 微調的 3.7 倍加速突破",
+ * closing paragraph on load balancing: an auxiliary loss keeps token routing
+ * even; the routing-gate note: a load-balancing loss drives expert utilisation
+ * towards uniform).  The pages give no formula; the Switch Transformer form
+ * is used:
+ *   f_e = (expert_offsets[e+1] - expert_offsets[e]) / (T*k)   slots routed to e
+ *   P_e = prob_sum[e] / T                                      mean router probability
+ *   *loss = alpha * E * sum_e f_e P_e     (alpha when routing is uniform)
+ *   coef[e] = alpha * E * f_e / T          (= dloss/dp[t,e]; counts pass no gradient)
+ * prob_sum: fp32 [E] from moe_route; expert_offsets: int32 [E+1] from
+ * moe_permute; loss: fp32 [1] or NULL; coef: fp32 [E] or NULL (not both NULL).
+ * Pass coef and the forward's logits_out to moe_layer_bwd to add the loss's
+ * gradient.  Errors: MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED_SHAPE.
+ */
+moe_status moe_aux_loss(const moe_dims* d, const float* prob_sum, const int32_t* expert_offsets,
+                        float alpha, float* loss, float* coef, void* stream);
 
 /*
  * Sort the token-slots by expert (grouped_mm row: "sort the tokens by their
@@ -177,7 +197,11 @@ moe_status moe_unpermute_combine(const moe_dims* d, const moe_bf16* y_perm,
  * SwiGLU is recomputed from the saved (g, u).  Router: the renormalised
  * top-k weights are a softmax over the chosen logits, so
  * dlogit[t,e_j] = w_j (dw_j - sum_i w_i dw_i) with dw_j = <dout[t], y_j>,
- * and top-k selection itself passes no gradient.  Experts that received no
+ * and top-k selection itself passes no gradient.  With the auxiliary loss
+ * (aux_coef = moe_aux_loss's coef, fp32 [E]; router_logits = the forward's
+ * logits_out, fp32 [T,E]), its gradient p[t,e] (c_e - sum_e' c_e' p[t,e']) is
+ * added for every expert of every token; NULL aux_coef: no auxiliary loss
+ * (router_logits may then be NULL).  Experts that received no
  * token get exact-zero weight gradients.
  */
 moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_bf16* x,
@@ -189,7 +213,8 @@ moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_
                          const moe_bf16* sh_gu_saved, moe_bf16* grad_x, moe_bf16* grad_w_router,
                          float* grad_router_bias, moe_bf16* grad_w_gate_up,
                          moe_bf16* grad_w_down, moe_bf16* grad_w_sh_gate_up,
-                         moe_bf16* grad_w_sh_down, void* workspace, size_t workspace_bytes,
+                         moe_bf16* grad_w_sh_down, const float* router_logits,
+                         const float* aux_coef, void* workspace, size_t workspace_bytes,
                          void* stream);
 
 /*
@@ -260,6 +285,8 @@ typedef enum {
   MOE_K_SHARED_WGRAD_DOWN,
   MOE_K_SHARED_WGRAD_GATE_UP,
   MOE_K_ROUTER_WGRAD_REDUCE, /* backward: sum of the router weight-gradient splits, bias gradient */
+  MOE_K_AUX,                 /* auxiliary loss: probability sums, loss, dense logit gradient,
+                                and the router term of grad_x */
   MOE_K_COUNT
 } moe_kernel_id;
 

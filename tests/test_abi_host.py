@@ -35,7 +35,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert M.moe_abi_version() == 7
+    assert M.moe_abi_version() == 8
     assert M.moe_status_string(0) == "ok"
     for s in range(1, 7):
         assert M.moe_status_string(s) not in ("ok", "unknown status")
@@ -81,18 +81,22 @@ def test_null_and_misaligned_arguments_rejected_before_launch(lib):
     wsp = (ctypes.addressof(ws) + 255) // 256 * 256
     assert lib.moe_workspace_size(None, 0, None) == 1
     # null inputs
-    assert lib.moe_route(ctypes.byref(d), 0, None, None, None, None, None, None, wsp, 1 << 19, None) == 1
+    assert lib.moe_route(ctypes.byref(d), 0, None, None, None, None, None, None, None, wsp, 1 << 19, None) == 1
     # bad gate enum
-    assert lib.moe_route(ctypes.byref(d), 7, wsp, wsp, None, None, wsp, wsp, wsp, 1 << 19, None) == 1
+    assert lib.moe_route(ctypes.byref(d), 7, wsp, wsp, None, None, wsp, wsp, None, wsp, 1 << 19, None) == 1
     # misaligned x
-    assert lib.moe_route(ctypes.byref(d), 0, wsp + 2, wsp, None, None, wsp, wsp, wsp, 1 << 19, None) == 1
+    assert lib.moe_route(ctypes.byref(d), 0, wsp + 2, wsp, None, None, wsp, wsp, None, wsp, 1 << 19, None) == 1
     # workspace too small
-    assert lib.moe_route(ctypes.byref(d), 0, wsp, wsp, None, None, wsp, wsp, wsp, 16, None) == 3
+    assert lib.moe_route(ctypes.byref(d), 0, wsp, wsp, None, None, wsp, wsp, None, wsp, 16, None) == 3
     assert lib.moe_permute(ctypes.byref(d), wsp, wsp, wsp, wsp, wsp, 64, None) == 3
     args = [wsp] * 12
     assert lib.moe_grouped_mlp_fwd(ctypes.byref(d), *args[:6], None, None, None, None, None, wsp, 64, None) == 1
     assert lib.moe_unpermute_combine(ctypes.byref(d), None, wsp, wsp, None, wsp, None) == 1
-    assert lib.moe_layer_bwd(ctypes.byref(d), *([None] * 21), wsp, 1 << 19, None) == 1
+    assert lib.moe_layer_bwd(ctypes.byref(d), *([None] * 23), wsp, 1 << 19, None) == 1
+    # auxiliary loss: needs the probability sums, the offsets and an output
+    f = ctypes.c_float(0.01)
+    assert lib.moe_aux_loss(ctypes.byref(d), None, wsp, f, wsp, wsp, None) == 1
+    assert lib.moe_aux_loss(ctypes.byref(d), wsp, wsp, f, None, None, None) == 1
     st = ctypes.c_int32(0)
     assert lib.moe_read_device_status(None, 0, None, 0, ctypes.byref(st)) == 1
 

@@ -208,3 +208,59 @@ def test_backward_recompute_matches_saved(name):
                          w_sh_gu=di.f64("w_sh_gate_up"), w_sh_down=di.f64("w_sh_down"))
     U.check_close(g1["grad_w_gate_up"], b["grad_w_gate_up"], "grad_w_gate_up (recompute)")
     U.check_close(g1["grad_x"], b["grad_x"], "grad_x (recompute)")
+
+
+@pytest.mark.parametrize("name", ["ragged", "skewed_mid", "balanced_small", "ragged_shared"])
+def test_aux_loss_forward_and_backward(name):
+    """Auxiliary load-balancing loss: the probability sums, the loss and its
+    coefficients against the oracle on the device's routing and fp32 logits;
+    the backward with the loss's gradient against the oracle; the expert
+    weight gradients (which the loss does not reach) bit-identical to a
+    backward without it."""
+    w = CASES[name]
+    # large enough that the loss's logit gradient (~alpha E f_e / T) is of the
+    # order of the main loss's, so that dropping it would fail the comparison
+    alpha = w.T / 4.0
+    di = U.DeviceInputs(w, seed=2, with_grad=True)
+    runs = {}
+    for aux in (None, alpha):
+        layer = M.MoeLayer(di.dims, gate_mode=w.gate, with_backward=True, save_logits=True,
+                           aux_alpha=aux)
+        layer.forward(di.x, di.w_router, di.w_gate_up, di.w_down, di.router_bias, di.w_sh_gate_up,
+                      di.w_sh_down)
+        grads = layer.alloc_grads(with_bias=w.bias_std > 0)
+        layer.backward(di.grad_out, di.x, di.w_router, di.w_gate_up, di.w_down, grads,
+                       di.w_sh_gate_up, di.w_sh_down)
+        torch.cuda.synchronize()
+        assert M.moe_read_device_status(layer.workspace) == 0
+        runs[aux] = (layer, {k: v.clone() for k, v in grads.items() if v is not None})
+    layer, g = runs[alpha]
+    _, g0 = runs[None]
+    idx = layer.topk_idx.cpu().numpy()
+    # forward: on the device's fp32 logits
+    p_dev = O.softmax(U.to_f64(layer.logits))
+    assert np.allclose(U.to_f64(layer.prob_sum), p_dev.sum(axis=0), rtol=1e-5, atol=1e-5)
+    L_ref, c_ref = O.aux_loss(p_dev, idx, alpha)
+    assert abs(float(layer.aux_loss.item()) - L_ref) <= 1e-5 * max(1.0, abs(L_ref))
+    assert np.allclose(U.to_f64(layer.aux_coef), c_ref, rtol=1e-6, atol=0)
+    # backward against the oracle with the same coefficients
+    f = U.oracle_forward(di, topk_idx=idx)
+    b = O.layer_backward(f, di.f64("grad_out"), di.f64("x"), di.f64("w_router"),
+                         di.f64("w_gate_up"), di.f64("w_down"), w.k,
+                         w_sh_gu=di.f64("w_sh_gate_up"), w_sh_down=di.f64("w_sh_down"),
+                         aux_coef=c_ref)
+    U.check_close(g["grad_w_router"], b["grad_w_router"], "grad_w_router (aux)")
+    U.check_close(g["grad_x"], b["grad_x"], "grad_x (aux)")
+    if "grad_router_bias" in g:
+        U.check_close(g["grad_router_bias"], b["grad_router_bias"], "grad_router_bias (aux)")
+    for key in ("grad_w_gate_up", "grad_w_down", "grad_w_sh_gate_up", "grad_w_sh_down"):
+        if key in g:
+            assert torch.equal(g[key], g0[key]), key
+    # with uneven routing the loss changes the router gradient; with equal
+    # counts (balanced gate) c is uniform and p (c - <c, p>) vanishes
+    counts = np.diff(layer.expert_offsets.cpu().numpy())
+    if counts.min() != counts.max():
+        assert not torch.equal(g["grad_w_router"], g0["grad_w_router"])
+    else:
+        assert np.allclose(U.to_f64(g["grad_w_router"]), U.to_f64(g0["grad_w_router"]),
+                           rtol=1e-2, atol=1e-2 * np.abs(U.to_f64(g0["grad_w_router"])).max())

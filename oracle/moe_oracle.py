@@ -47,6 +47,16 @@ design notes):
   sum_e f_e P_e with f_e = the fraction of the T*k slots routed to e and
   P_e = the mean over tokens of p[t, e]; f is a count, so it passes no
   gradient.  Uniform routing and probabilities give L_aux = alpha.
+* expert capacity (the pages name overflow as a risk of uneven routing and
+  give no rule): an expert takes at most C slots; the ones it keeps are its
+  first C in slot order s = t*k + j (the stable sort's order), the rest are
+  dropped.  A dropped slot adds nothing to the output (the layer's residual
+  carries the token) and its weight keeps its value, so the kept weights are
+  not renormalised.  Dropping is piecewise constant in the inputs: it passes
+  no gradient, the dropped slot's dL/dw is 0, and the router gradient keeps
+  its formula.  The counts f of the auxiliary loss are the router's
+  assignment before dropping.  C = ceil(factor * T * k / E) for a capacity
+  factor; C >= max count drops nothing.
 
 Parity status: every function below is pinned by a test in
 ``tests/test_oracle_pins.py`` (closed forms, invariants, brute force, library
@@ -54,6 +64,8 @@ special cases, finite differences).
 """
 
 from __future__ import annotations
+
+import math
 
 import numpy as np
 
@@ -176,6 +188,27 @@ def permute(topk_idx: np.ndarray, E: int):
     return offsets.astype(np.int32), perm_slot.astype(np.int32), slot_perm.astype(np.int32)
 
 
+def expert_capacity(T: int, k: int, E: int, factor: float) -> int:
+    """Slots an expert keeps for capacity factor `factor`: ceil(factor * T * k / E)."""
+    return int(math.ceil(factor * T * k / E))
+
+
+def keep_slots(topk_idx: np.ndarray, E: int, capacity: int | None) -> np.ndarray:
+    """bool [T, k]: slot (t, j) is kept iff fewer than `capacity` earlier slots
+    (in slot order s = t*k + j) went to the same expert.  None: keep every slot."""
+    T, k = topk_idx.shape
+    keep = np.ones((T, k), dtype=bool)
+    if capacity is None:
+        return keep
+    taken = np.zeros(E, dtype=np.int64)
+    for t in range(T):
+        for j in range(k):
+            e = int(topk_idx[t, j])
+            keep[t, j] = taken[e] < capacity
+            taken[e] += 1
+    return keep
+
+
 # --------------------------------------------------------------------------
 # Expert MLP (SwiGLU) in the three backends of the expert-backend table
 # --------------------------------------------------------------------------
@@ -253,13 +286,17 @@ def experts_batched(x, topk_idx, w_gu, w_down):
     return y.reshape(T, k, -1)
 
 
-def combine(y_perm, slot_perm, topk_w, y_shared=None):
-    """Weighted un-permute: out[t] = sum_j w[t,j] * y_perm[slot_perm[t*k+j]] (+ y_shared[t])."""
+def combine(y_perm, slot_perm, topk_w, y_shared=None, keep=None):
+    """Weighted un-permute: out[t] = sum_j w[t,j] * y_perm[slot_perm[t*k+j]] (+ y_shared[t]),
+    over the kept slots only when a keep mask [T, k] is given."""
     T, k = topk_w.shape
     out = np.zeros((T, y_perm.shape[1]))
     for j in range(k):
         rows = slot_perm.reshape(T, k)[:, j]
-        out += topk_w[:, j:j + 1] * y_perm[rows]
+        contrib = topk_w[:, j:j + 1] * y_perm[rows]
+        if keep is not None:
+            contrib = np.where(keep[:, j:j + 1], contrib, 0.0)
+        out += contrib
     if y_shared is not None:
         out = out + y_shared
     return out
@@ -277,11 +314,14 @@ def combine_slots(y_slot, topk_w, y_shared=None):
 # Whole layer, forward
 # --------------------------------------------------------------------------
 def layer_forward(x, w_router, w_gu, w_down, k, balanced=False, bias=None,
-                  w_sh_gu=None, w_sh_down=None, topk_idx=None, decision_logits=None):
+                  w_sh_gu=None, w_sh_down=None, topk_idx=None, decision_logits=None,
+                  capacity=None):
     """MoE layer forward through the grouped path.
 
     All arrays float64 except ids.  ``topk_idx`` overrides the selection (used
     when comparing against a device whose fp32 logits sit on a near-tie).
+    ``capacity``: slots each expert keeps (None: no limit); the expert outputs
+    of dropped slots are still formed here (rows of y_perm) but not combined.
     Returns a dict with every intermediate the backward needs.
     """
     E = w_gu.shape[0]
@@ -295,10 +335,11 @@ def layer_forward(x, w_router, w_gu, w_down, k, balanced=False, bias=None,
     y_sh = gu_sh = None
     if w_sh_gu is not None:
         y_sh, gu_sh, _ = swiglu_mlp(x, w_sh_gu, w_sh_down)
-    out = combine(y_perm, slot_perm, w, y_sh)
+    keep = keep_slots(idx, E, capacity)
+    out = combine(y_perm, slot_perm, w, y_sh, keep=keep)
     return dict(logits=logits, p=p, topk_idx=idx, topk_w=w, expert_offsets=offsets,
                 perm_slot=perm_slot, slot_perm=slot_perm, gu_perm=gu_perm, h_perm=h_perm,
-                y_perm=y_perm, y_shared=y_sh, gu_shared=gu_sh, out=out)
+                y_perm=y_perm, y_shared=y_sh, gu_shared=gu_sh, out=out, keep=keep)
 
 
 # --------------------------------------------------------------------------
@@ -352,13 +393,17 @@ def layer_backward(fwd: dict, grad_out, x, w_router, w_gu, w_down, k,
     db = sum_t dl[t], and x also receives dl W_r.  Top-k selection itself is
     piecewise constant and passes no gradient.  With aux_coef = c (from
     aux_loss), the auxiliary loss adds dL_aux/dp[t, e] = c_e for every expert,
-    so its logit gradient p * (c - <c, p>) is dense.
+    so its logit gradient p * (c - <c, p>) is dense.  A slot the forward
+    dropped (fwd["keep"] False) gets dL/dw = 0 and sends nothing to its expert.
     """
     T, H = x.shape
     E = w_gu.shape[0]
     idx, w, p = fwd["topk_idx"], fwd["topk_w"], fwd["p"]
     offsets, perm_slot = fwd["expert_offsets"], fwd["perm_slot"]
     gu_perm, y_perm = fwd["gu_perm"], fwd["y_perm"]
+    keep = fwd.get("keep")
+    if keep is None:
+        keep = np.ones(idx.shape, dtype=bool)
     dx = np.zeros((T, H))
     dW_gu = np.zeros_like(w_gu)
     dW_down = np.zeros_like(w_down)
@@ -369,7 +414,7 @@ def layer_backward(fwd: dict, grad_out, x, w_router, w_gu, w_down, k,
             continue
         slots = perm_slot[r0:r1].astype(np.int64)
         tok, j = slots // k, slots % k
-        dout_r = grad_out[tok]
+        dout_r = np.where(keep[tok, j][:, None], grad_out[tok], 0.0)
         dw[tok, j] = np.sum(dout_r * y_perm[r0:r1], axis=1)
         dy = w[tok, j][:, None] * dout_r
         dxr, dW_gu[e], dW_down[e] = swiglu_mlp_backward(x[tok], gu_perm[r0:r1], w_gu[e], w_down[e], dy)

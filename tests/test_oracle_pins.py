@@ -192,18 +192,18 @@ def test_combine_hand_example():
 
 
 # ---------------------------------------------------------------- backward
-def _loss_and_grads(d, k, G_, balanced=False, shared=None):
+def _loss_and_grads(d, k, G_, balanced=False, shared=None, capacity=None):
     f = O.layer_forward(d["x"], d["w_router"], d["w_gu"], d["w_down"], k, balanced=balanced,
-                        bias=d["bias"], **(shared or {}))
+                        bias=d["bias"], capacity=capacity, **(shared or {}))
     b = O.layer_backward(f, G_, d["x"], d["w_router"], d["w_gu"], d["w_down"], k,
                          **(shared or {}))
     return float(np.sum(f["out"] * G_)), f, b
 
 
-def _fd_check(d, k, balanced=False, shared=None, n_probe=12, seed=3):
+def _fd_check(d, k, balanced=False, shared=None, n_probe=12, seed=3, capacity=None):
     T, H = d["x"].shape
     G_ = np.random.default_rng(seed).normal(size=(T, H))
-    _, f0, b = _loss_and_grads(d, k, G_, balanced, shared)
+    _, f0, b = _loss_and_grads(d, k, G_, balanced, shared, capacity)
     eps = 1e-6
     names = [("x", "grad_x"), ("w_router", "grad_w_router"), ("w_gu", "grad_w_gate_up"),
              ("w_down", "grad_w_down")]
@@ -216,9 +216,9 @@ def _fd_check(d, k, balanced=False, shared=None, n_probe=12, seed=3):
             i = tuple(r.integers(0, s) for s in arr.shape)
             old = arr[i]
             arr[i] = old + eps
-            lp, fp_, _ = _loss_and_grads(d, k, G_, balanced, shared)
+            lp, fp_, _ = _loss_and_grads(d, k, G_, balanced, shared, capacity)
             arr[i] = old - eps
-            lm, fm_, _ = _loss_and_grads(d, k, G_, balanced, shared)
+            lm, fm_, _ = _loss_and_grads(d, k, G_, balanced, shared, capacity)
             arr[i] = old
             assert np.array_equal(fp_["topk_idx"], f0["topk_idx"]) and np.array_equal(fm_["topk_idx"], f0["topk_idx"])
             num = (lp - lm) / (2 * eps)
@@ -230,9 +230,9 @@ def _fd_check(d, k, balanced=False, shared=None, n_probe=12, seed=3):
                 i = tuple(r.integers(0, s) for s in arr.shape)
                 old = arr[i]
                 arr[i] = old + eps
-                lp = _loss_and_grads(d, k, G_, balanced, shared)[0]
+                lp = _loss_and_grads(d, k, G_, balanced, shared, capacity)[0]
                 arr[i] = old - eps
-                lm = _loss_and_grads(d, k, G_, balanced, shared)[0]
+                lm = _loss_and_grads(d, k, G_, balanced, shared, capacity)[0]
                 arr[i] = old
                 num = (lp - lm) / (2 * eps)
                 assert abs(num - b[gname][i]) <= 1e-6 * max(1.0, abs(num)), (pname, i)
@@ -369,6 +369,102 @@ def test_mutation_aux_coefficients_without_token_mean_is_caught(monkeypatch):
 
 
 # ---------------------------------------------------------------- whole workloads
+# ---------------------------------------------------------------- expert capacity
+def test_expert_capacity_closed_forms():
+    assert O.expert_capacity(4096, 8, 128, 1.0) == 256
+    assert O.expert_capacity(4096, 8, 128, 1.25) == 320
+    assert O.expert_capacity(10, 2, 3, 1.0) == 7          # ceil(20 / 3)
+    assert O.expert_capacity(10, 2, 3, 0.5) == 4          # ceil(10 / 3)
+    assert O.expert_capacity(8, 1, 4, 0.0) == 0
+
+
+def test_keep_slots_hand_example():
+    # slots in order: s0 t0->0, s1 t0->1, s2 t1->0, s3 t1->2, s4 t2->0, s5 t2->1,
+    # s6 t3->1, s7 t3->0.  Capacity 2: expert 0 keeps s0, s2 (drops s4, s7),
+    # expert 1 keeps s1, s5 (drops s6), expert 2 keeps s3.
+    idx = np.array([[0, 1], [0, 2], [0, 1], [1, 0]])
+    keep = O.keep_slots(idx, 3, 2)
+    assert np.array_equal(keep, [[True, True], [True, True], [False, True], [False, False]])
+    assert O.keep_slots(idx, 3, None).all()
+    assert not O.keep_slots(idx, 3, 0).any()
+    assert np.array_equal(O.keep_slots(idx, 3, 1), [[True, True], [False, True], [False, False],
+                                                    [False, False]])
+
+
+@pytest.mark.parametrize("T,E,k,C", [(50, 4, 2, 10), (200, 8, 3, 1), (64, 16, 4, 17), (9, 3, 3, 3)])
+def test_keep_slots_brute_force_rank(T, E, k, C):
+    """Kept iff the number of earlier slots with the same expert (counted one
+    by one) is below C; every expert keeps min(count, C) slots."""
+    idx = np.random.default_rng(T + C).integers(0, E, size=(T, k))
+    flat = idx.ravel()
+    rank = np.array([int(np.sum(flat[:s] == flat[s])) for s in range(flat.size)])
+    keep = O.keep_slots(idx, E, C)
+    assert np.array_equal(keep.ravel(), rank < C)
+    for e in range(E):
+        assert keep.ravel()[flat == e].sum() == min(int(np.sum(flat == e)), C)
+
+
+def test_capacity_at_or_above_max_count_drops_nothing():
+    d = _tiny(T=16, H=16, E=4, k=2, I=8, seed=51)
+    G_ = np.random.default_rng(2).normal(size=d["x"].shape)
+    _, f0, b0 = _loss_and_grads(d, 2, G_)
+    cmax = int(np.diff(f0["expert_offsets"]).max())
+    for C in (cmax, cmax + 5):
+        _, f1, b1 = _loss_and_grads(d, 2, G_, capacity=C)
+        assert f1["keep"].all()
+        assert np.array_equal(f1["out"], f0["out"])
+        for key in b0:
+            assert np.array_equal(b1[key], b0[key]), key
+
+
+def test_capacity_zero_leaves_the_shared_expert_only():
+    """Every slot dropped: out is the shared expert (a dense SwiGLU MLP, torch),
+    the routed experts and the router get no gradient, grad_x is the shared
+    expert's input gradient (torch autograd)."""
+    d = _tiny(T=10, H=16, E=4, k=2, I=8, seed=52)
+    r = np.random.default_rng(5)
+    sh = dict(w_sh_gu=r.normal(size=(24, 16)) * 0.2, w_sh_down=r.normal(size=(16, 12)) * 0.2)
+    G_ = r.normal(size=d["x"].shape)
+    _, f, b = _loss_and_grads(d, 2, G_, shared=sh, capacity=0)
+    xt = torch.from_numpy(d["x"]).requires_grad_()
+    wg = torch.from_numpy(sh["w_sh_gu"]).requires_grad_()
+    wdn = torch.from_numpy(sh["w_sh_down"]).requires_grad_()
+    gu = xt @ wg.T
+    y = (torch.nn.functional.silu(gu[:, :12]) * gu[:, 12:]) @ wdn.T
+    (y * torch.from_numpy(G_)).sum().backward()
+    assert np.allclose(f["out"], y.detach().numpy(), atol=1e-12)
+    assert np.allclose(b["grad_x"], xt.grad.numpy(), atol=1e-12)
+    assert np.allclose(b["grad_w_sh_gate_up"], wg.grad.numpy(), atol=1e-12)
+    for key in ("grad_w_gate_up", "grad_w_down", "grad_w_router", "grad_router_bias",
+                "grad_topk_w", "grad_logits"):
+        assert not np.any(b[key]), key
+
+
+def test_capacity_forward_matches_eager_backend_with_dropped_slots():
+    """The grouped path with drops equals the eager for-loop backend over the
+    kept slots, with the router's weights as they are (not renormalised)."""
+    T, E, k = 30, 5, 3
+    d = _tiny(T=T, H=16, E=E, k=k, I=8, seed=53)
+    f = O.layer_forward(d["x"], d["w_router"], d["w_gu"], d["w_down"], k, bias=d["bias"],
+                        capacity=10)
+    assert 0 < (~f["keep"]).sum() < T * k
+    idx, w, _ = O.route(O.router_logits(d["x"], d["w_router"], d["bias"]), k)
+    ye = O.experts_eager(d["x"], idx, d["w_gu"], d["w_down"])
+    flat = idx.ravel()
+    rank = np.array([int(np.sum(flat[:s] == flat[s])) for s in range(flat.size)]).reshape(T, k)
+    out = O.combine_slots(ye * (rank < 10)[:, :, None], w)
+    assert np.allclose(f["out"], out, rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("C", [1, 3])
+def test_capacity_backward_matches_finite_differences(C):
+    d = _tiny(T=10, H=8, E=3, k=2, I=8, seed=54)
+    f = O.layer_forward(d["x"], d["w_router"], d["w_gu"], d["w_down"], 2, bias=d["bias"],
+                        capacity=C)
+    assert 0 < (~f["keep"]).sum()
+    _fd_check(d, 2, n_probe=8, seed=11, capacity=C)
+
+
 def test_tiny_workload_forward_invariants():
     w = G.WORKLOADS["tiny"]
     inp = G.make_inputs(w, 0)
@@ -470,3 +566,35 @@ def test_mutation_combine_without_weights_is_caught(monkeypatch):
         return y_perm[slot_perm.reshape(T, k)].mean(1) + (0 if y_shared is None else y_shared)
     monkeypatch.setattr(O, "combine", bad)
     assert _pins_fail(test_combine_hand_example)
+
+
+def test_mutation_capacity_keeps_last_slots_is_caught(monkeypatch):
+    orig = O.keep_slots
+
+    def bad(idx, E, C):
+        return orig(idx[::-1, ::-1], E, C)[::-1, ::-1]
+    monkeypatch.setattr(O, "keep_slots", bad)
+    assert _pins_fail(test_keep_slots_hand_example)
+
+
+def test_mutation_capacity_renormalised_weights_is_caught(monkeypatch):
+    orig = O.combine
+
+    def bad(y_perm, slot_perm, topk_w, y_shared=None, keep=None):
+        if keep is not None:
+            kw = np.where(keep, topk_w, 0.0)
+            topk_w = kw / np.maximum(kw.sum(axis=1, keepdims=True), 1e-300)
+        return orig(y_perm, slot_perm, topk_w, y_shared, keep)
+    monkeypatch.setattr(O, "combine", bad)
+    assert _pins_fail(test_capacity_forward_matches_eager_backend_with_dropped_slots)
+
+
+def test_mutation_capacity_ignored_in_backward_is_caught(monkeypatch):
+    orig = O.layer_backward
+
+    def bad(fwd, *a, **kw):
+        f2 = dict(fwd)
+        f2["keep"] = None
+        return orig(f2, *a, **kw)
+    monkeypatch.setattr(O, "layer_backward", bad)
+    assert _pins_fail(lambda: test_capacity_backward_matches_finite_differences(1))

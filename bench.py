@@ -339,6 +339,11 @@ def run_ours(args, w, rank, world):
     # with the auxiliary load-balancing loss (alpha = 0.01)
     layer_aux = M.MoeLayer(dims, gate_mode=w.gate, device=dev, with_backward=True, aux_alpha=0.01)
     grads_aux = layer_aux.alloc_grads(with_bias=bias is not None)
+    # with an expert capacity of 0.75 x the even share (slots past it are dropped)
+    cap_factor = 0.75
+    cap = M.expert_capacity(w.T, w.k, w.E, cap_factor)
+    layer_cap = M.MoeLayer(dims, gate_mode=w.gate, device=dev, with_backward=True, capacity=cap)
+    grads_cap = layer_cap.alloc_grads(with_bias=bias is not None)
     stream = torch.cuda.current_stream(dev)
 
     def fwd():
@@ -358,6 +363,10 @@ def run_ours(args, w, rank, world):
     def step_aux():
         layer_aux.forward(x, wr, wgu, wd, bias, wsg, wsd)
         layer_aux.backward(go, x, wr, wgu, wd, grads_aux, wsg, wsd)
+
+    def step_cap():
+        layer_cap.forward(x, wr, wgu, wd, bias, wsg, wsd)
+        layer_cap.backward(go, x, wr, wgu, wd, grads_cap, wsg, wsd)
 
     def barrier():
         if world > 1:
@@ -411,6 +420,12 @@ def run_ours(args, w, rank, world):
         step_aux()
     ms_aux = timed(step_aux, args.steps)
     assert M.moe_read_device_status(layer_aux.workspace) == 0, "device reported an error"
+    # ---- forward + backward with the expert capacity
+    for _ in range(max(1, args.warmup // 2)):
+        step_cap()
+    ms_cap = timed(step_cap, args.steps)
+    assert M.moe_read_device_status(layer_cap.workspace) == 0, "device reported an error"
+    kept = int(np.minimum(np.diff(layer_cap.expert_offsets.cpu().numpy()), cap).sum())
 
     # ---- end to end: pinned host inputs in, result out, every step
     xh = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
@@ -502,6 +517,11 @@ def run_ours(args, w, rank, world):
         "aux_loss": {"tokens_per_s": job_tokens_per_s(w.T, world, args.steps, ms_aux),
                      "ms_per_step": ms_aux / args.steps,
                      "value": float(layer_aux.aux_loss.item()), "alpha": 0.01},
+        # forward+backward with an expert capacity (token dropping)
+        "capacity": {"factor": cap_factor, "capacity": cap,
+                     "dropped_fraction": 1.0 - kept / (w.T * w.k),
+                     "tokens_per_s": job_tokens_per_s(w.T, world, args.steps, ms_cap),
+                     "ms_per_step": ms_cap / args.steps},
         "layer_roofline": {
             "fwd": {"t_roof_us": t_roof_f * 1e6, "t_us": t_f * 1e6, "frac": t_roof_f / t_f,
                     "flops": f_fwd, "bytes": b_fwd},

@@ -53,6 +53,7 @@ struct GemmArgs {
   int M, N, K;           // see Sched: the ragged one is taken from the groups
   int G;                 // number of groups
   const int32_t* offsets;  // [G+1] row offsets (unpadded); nullptr: one group
+  int cap;               // > 0: a group (expert) takes only its first cap rows (capacity)
   int single_rows;       // rows of the one group when offsets == nullptr
   int ksplit;            // RAGGED_K without offsets: group g = K rows [g*ksplit, (g+1)*ksplit)
   int padded;            // 1: groups start on 128-row boundaries of a padded row space
@@ -178,6 +179,7 @@ __device__ __forceinline__ void build_group_tables(const GemmArgs& a, SmemTables
       if (a.offsets) {
         off = pre_off[c];
         cnt = pre_end[c] - off;
+        if (a.cap > 0) cnt = min(cnt, a.cap);
       } else if (a.ksplit > 0) {
         off = g * a.ksplit;
         cnt = min(a.ksplit, a.K - off);

@@ -199,11 +199,14 @@ __global__ void sort_histogram_kernel(const int32_t* __restrict__ topk_idx, int 
 // contiguous slots [b*C + w*C/8, b*C + (w+1)*C/8), held in registers, walked
 // 32 at a time in order; lanes holding the same expert are ranked by lane id
 // (match_any), so the sorted order within an expert is ascending slot id.
+// Expert capacity cap > 0: a slot whose rank inside its expert is cap or more
+// is dropped; it keeps its sorted row (perm_slot is the full sort) but its
+// slot_perm entry is -1.
 __global__ void sort_scatter_kernel(const int32_t* __restrict__ topk_idx, int S, int E,
                                     int num_blocks, const int32_t* __restrict__ block_counts,
                                     int32_t* __restrict__ expert_offsets,
                                     int32_t* __restrict__ perm_slot,
-                                    int32_t* __restrict__ slot_perm) {
+                                    int32_t* __restrict__ slot_perm, int cap) {
   __shared__ int base[256];
   __shared__ int total[256];
   __shared__ int wcount[8][256];
@@ -244,6 +247,7 @@ __global__ void sort_scatter_kernel(const int32_t* __restrict__ topk_idx, int S,
       if (e < E) {
         const int off = run + inc - v;
         base[e] += off;
+        total[e] = off;  // from here on: the expert's first sorted row
         if (blockIdx.x == 0) expert_offsets[e] = off;
       }
       run += __shfl_sync(0xffffffffu, inc, 31);
@@ -277,7 +281,7 @@ __global__ void sort_scatter_kernel(const int32_t* __restrict__ topk_idx, int S,
       const int pos = wcount[warp][e] + __popc(m & ((1u << lane) - 1u));
       const int s = w0 + i * 32 + lane;
       perm_slot[pos] = s;
-      slot_perm[s] = pos;
+      slot_perm[s] = (cap > 0 && pos - total[e] >= cap) ? -1 : pos;
     }
     __syncwarp();
     if (e >= 0 && lane == __ffs(m) - 1) wcount[warp][e] += __popc(m);
@@ -299,11 +303,12 @@ __global__ void combine_kernel(const __nv_bfloat16* __restrict__ y_perm,
   const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
-  int row_l = 0;
+  int row_l = -1;  // -1: slot dropped by the expert capacity (no row, adds nothing)
   float w_l = 0.f;
   if (lane < k) {
-    row_l = clampi(__ldg(slot_perm + (size_t)t * k + lane), 0, S - 1);
-    w_l = __ldg(topk_w + (size_t)t * k + lane);
+    const int r = __ldg(slot_perm + (size_t)t * k + lane);
+    row_l = r < 0 ? -1 : min(r, S - 1);
+    w_l = r < 0 ? 0.f : __ldg(topk_w + (size_t)t * k + lane);
   }
   int rows[KMAX];
   float ws[KMAX];
@@ -316,7 +321,9 @@ __global__ void combine_kernel(const __nv_bfloat16* __restrict__ y_perm,
     uint4 v[KMAX];
 #pragma unroll
     for (int j = 0; j < KMAX; ++j)
-      if (j < k) v[j] = __ldg(reinterpret_cast<const uint4*>(y_perm + (size_t)rows[j] * H) + c);
+      if (j < k)
+        v[j] = rows[j] < 0 ? make_uint4(0u, 0u, 0u, 0u)
+                           : __ldg(reinterpret_cast<const uint4*>(y_perm + (size_t)rows[j] * H) + c);
     uint4 vs = make_uint4(0, 0, 0, 0);
     if (y_shared) vs = __ldg(reinterpret_cast<const uint4*>(y_shared + (size_t)t * H) + c);
     float acc[8];
@@ -355,6 +362,8 @@ __global__ void combine_kernel(const __nv_bfloat16* __restrict__ y_perm,
 // dlogit_j = w_j (dw_j - sum_i w_i dw_i) (every other logit gets zero); dl is
 // written per slot for the router weight gradient.
 // dx[t] = sum_j dx_slot[p(t,j)] + sum_j dlogit_j W_r[e_j] (+ dx_shared[t]).
+// With accumulate set, dx[t] already holds a term (the dense router term of the
+// auxiliary loss) and the sum is added to it.
 template <int KMAX>
 __global__ void dx_gather_kernel(const __nv_bfloat16* __restrict__ dx_slot,
                                  const int32_t* __restrict__ topk_idx,
@@ -365,18 +374,21 @@ __global__ void dx_gather_kernel(const __nv_bfloat16* __restrict__ dx_slot,
                                  int nNB, const __nv_bfloat16* __restrict__ w_router,
                                  const __nv_bfloat16* __restrict__ dx_shared,
                                  float* __restrict__ dl_out, __nv_bfloat16* __restrict__ dl_dense,
-                                 int ldE, int router_term, __nv_bfloat16* __restrict__ dx, int T,
-                                 int H, int k, int E, int P) {
+                                 int ldE, int router_term, int accumulate,
+                                 __nv_bfloat16* __restrict__ dx, int T, int H, int k, int E, int P) {
   const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
-  int row_l = 0, e_l = 0;
+  int row_l = -1, e_l = 0;  // row -1: slot dropped by the expert capacity (dw = 0, no dx)
   float dw_l = 0.f, w_l = 0.f;
   if (lane < k) {
     const int s = t * k + lane;
     e_l = clampi(__ldg(topk_idx + s), 0, E - 1);
-    row_l = clampi(__ldg(slot_perm + s) - __ldg(expert_offsets + e_l) + __ldg(poff + e_l), 0, P - 1);
-    for (int b = 0; b < nNB; ++b) dw_l += __ldg(dw_part + (size_t)row_l * nNB + b);
+    const int sp = __ldg(slot_perm + s);
+    if (sp >= 0) {
+      row_l = clampi(sp - __ldg(expert_offsets + e_l) + __ldg(poff + e_l), 0, P - 1);
+      for (int b = 0; b < nNB; ++b) dw_l += __ldg(dw_part + (size_t)row_l * nNB + b);
+    }
     w_l = __ldg(topk_w + s);
   }
   float dot = w_l * dw_l;
@@ -406,16 +418,18 @@ __global__ void dx_gather_kernel(const __nv_bfloat16* __restrict__ dx_slot,
 #pragma unroll
     for (int j = 0; j < KMAX; ++j) {
       if (j < k) {
-        v[j] = __ldg(reinterpret_cast<const uint4*>(dx_slot + (size_t)rows[j] * H) + c);
+        v[j] = rows[j] < 0 ? make_uint4(0u, 0u, 0u, 0u)
+                           : __ldg(reinterpret_cast<const uint4*>(dx_slot + (size_t)rows[j] * H) + c);
         r[j] = router_term ? __ldg(reinterpret_cast<const uint4*>(w_router + (size_t)es[j] * H) + c)
                            : make_uint4(0u, 0u, 0u, 0u);
       }
     }
     uint4 vs = make_uint4(0, 0, 0, 0);
     if (dx_shared) vs = __ldg(reinterpret_cast<const uint4*>(dx_shared + (size_t)t * H) + c);
-    float acc[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+    const uint4 va = accumulate ? reinterpret_cast<const uint4*>(dx + (size_t)t * H)[c]
+                                : make_uint4(0u, 0u, 0u, 0u);
+    float acc[8] = {bf16lo(va.x), bf16hi(va.x), bf16lo(va.y), bf16hi(va.y),
+                    bf16lo(va.z), bf16hi(va.z), bf16lo(va.w), bf16hi(va.w)};
 #pragma unroll
     for (int j = 0; j < KMAX; ++j) {
       if (j < k) {
@@ -505,14 +519,27 @@ __global__ void router_wgrad_reduce_kernel(const float* __restrict__ part, int n
 // of slots routed to e and P_e = (1/T) sum_t p[t, e].  The counts pass no
 // gradient, so dL_aux/dp[t, e] = c_e = alpha E f_e / T.
 
-// prob_sum[e] = sum over the top-k kernel's blocks (in order) of their sums of p[t, e].
-__global__ void prob_sum_kernel(const float* __restrict__ psum_part, int nblk, int E,
-                                float* __restrict__ prob_sum) {
-  const int e = blockIdx.x * blockDim.x + threadIdx.x;
-  if (e >= E) return;
+// prob_sum[e] = sum over the top-k kernel's blocks of their sums of p[t, e].
+// Block = 32 experts (lane = expert, coalesced rows); warp w sums the partial
+// rows w, w + 32, ... in order, then a fixed tree over the 32 warps.
+constexpr int kProbSumWarps = 32;
+__global__ void __launch_bounds__(32 * kProbSumWarps)
+prob_sum_kernel(const float* __restrict__ psum_part, int nblk, int E, float* __restrict__ prob_sum) {
+  __shared__ float part[kProbSumWarps][33];
+  const int wi = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e = blockIdx.x * 32 + lane;
   float s = 0.f;
-  for (int b = 0; b < nblk; ++b) s += __ldg(psum_part + (size_t)b * E + e);
-  prob_sum[e] = s;
+  if (e < E) {
+#pragma unroll 4
+    for (int b = wi; b < nblk; b += kProbSumWarps) s += __ldg(psum_part + (size_t)b * E + e);
+  }
+  part[wi][lane] = s;
+  __syncthreads();
+  for (int w = kProbSumWarps / 2; w > 0; w >>= 1) {
+    if (wi < w) part[wi][lane] += part[wi + w][lane];
+    __syncthreads();
+  }
+  if (wi == 0 && e < E) prob_sum[e] = part[0][lane];
 }
 
 // One block: coef[e] = alpha E f_e / T and loss = sum_e alpha E f_e prob_sum[e] / T
@@ -543,14 +570,21 @@ __global__ void aux_loss_kernel(const float* __restrict__ prob_sum,
 //   p = softmax(logits[t]); s = sum_e c_e p_e;
 //   DL[t, e] = dl_main[t, e] + p_e (c_e - s)
 // where dl_main is the top-k weights' gradient on the token's selected experts
-// (fp32 per slot) and zero elsewhere; DL is written once in bf16 ([T, ldE],
-// zero padding), and each block (8 tokens) writes its fp32 column sums (warp
-// order) for the bias gradient.
+// and zero elsewhere: dl_j = w_j (dw_j - sum_i w_i dw_i), dw_j the sum of slot
+// j's down-projection partials (the same arithmetic as the per-token gather,
+// which is why the router term of grad_x can be formed before that gather);
+// dl is written per slot (fp32), DL once in bf16 ([T, ldE], zero padding), and
+// each block (8 tokens) writes its fp32 column sums (warp order) for the bias
+// gradient.
 constexpr int kAuxDlWarps = 8;
 template <int KMAX>
 __global__ void aux_dl_kernel(const float* __restrict__ logits, const float* __restrict__ coef,
-                              const int32_t* __restrict__ topk_idx, const float* __restrict__ dl,
-                              int T, int E, int k, int ldE, __nv_bfloat16* __restrict__ dl_dense,
+                              const int32_t* __restrict__ topk_idx, const float* __restrict__ topk_w,
+                              const int32_t* __restrict__ slot_perm,
+                              const int32_t* __restrict__ expert_offsets,
+                              const int32_t* __restrict__ poff, const float* __restrict__ dw_part,
+                              int nNB, int P, float* __restrict__ dl_out, int T, int E, int k,
+                              int ldE, __nv_bfloat16* __restrict__ dl_dense,
                               float* __restrict__ db_part) {
   __shared__ float rows[kAuxDlWarps][kMaxGroupsRouter];
   const int wi = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -583,21 +617,37 @@ __global__ void aux_dl_kernel(const float* __restrict__ logits, const float* __r
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
   int sel_e = -1;
-  float sel_d = 0.f;
+  float dw_l = 0.f, w_l = 0.f;
   if (t < T && lane < k) {
-    sel_e = __ldg(topk_idx + (size_t)t * k + lane);
-    sel_d = __ldg(dl + (size_t)t * k + lane);
+    const int sl = t * k + lane;
+    sel_e = clampi(__ldg(topk_idx + sl), 0, E - 1);
+    const int sp = __ldg(slot_perm + sl);  // -1: dropped by the expert capacity, dw = 0
+    if (sp >= 0) {
+      const int row = clampi(sp - __ldg(expert_offsets + sel_e) + __ldg(poff + sel_e), 0, P - 1);
+      for (int b = 0; b < nNB; ++b) dw_l += __ldg(dw_part + (size_t)row * nNB + b);
+    }
+    w_l = __ldg(topk_w + sl);
+  }
+  float dot = w_l * dw_l;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+  const float sel_d = w_l * (dw_l - dot);
+  if (t < T && lane < k) dl_out[(size_t)t * k + lane] = sel_d;
+  int es[KMAX];
+  float ds[KMAX];
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j) {
+    es[j] = __shfl_sync(0xffffffffu, sel_e, j);
+    ds[j] = __shfl_sync(0xffffffffu, sel_d, j);
   }
 #pragma unroll
   for (int i = 0; i < kRouterMaxPerLane; ++i) {
+    if (i * 32 >= ldE) break;  // warp-uniform
     const int e = i * 32 + lane;
     float main_d = 0.f;
 #pragma unroll
-    for (int j = 0; j < KMAX; ++j) {
-      const int ej = __shfl_sync(0xffffffffu, sel_e, j);
-      const float dj = __shfl_sync(0xffffffffu, sel_d, j);
-      if (j < k && ej == e) main_d = dj;
-    }
+    for (int j = 0; j < KMAX; ++j)
+      if (j < k && es[j] == e) main_d = ds[j];
     const float v = (e < E && t < T) ? main_d + lv[i] * (__ldg(coef + (e < E ? e : 0)) - s) : 0.f;
     if (e < E) rows[wi][e] = v;
     if (t < T && e < ldE) dl_dense[(size_t)t * ldE + e] = __float2bfloat16_rn(v);
@@ -609,20 +659,6 @@ __global__ void aux_dl_kernel(const float* __restrict__ logits, const float* __r
     for (int w = 0; w < kAuxDlWarps; ++w) acc += rows[w][e];
     db_part[(size_t)blockIdx.x * E + e] = acc;
   }
-}
-
-// grad_x += r (bf16, 8 elements per thread).
-__global__ void add_bf16_kernel(__nv_bfloat16* __restrict__ dst, const __nv_bfloat16* __restrict__ r,
-                                long long n8) {
-  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= n8) return;
-  uint4 a = reinterpret_cast<const uint4*>(dst)[i];
-  const uint4 b = __ldg(reinterpret_cast<const uint4*>(r) + i);
-  a.x = pack_bf16x2(bf16lo(a.x) + bf16lo(b.x), bf16hi(a.x) + bf16hi(b.x));
-  a.y = pack_bf16x2(bf16lo(a.y) + bf16lo(b.y), bf16hi(a.y) + bf16hi(b.y));
-  a.z = pack_bf16x2(bf16lo(a.z) + bf16lo(b.z), bf16hi(a.z) + bf16hi(b.z));
-  a.w = pack_bf16x2(bf16lo(a.w) + bf16lo(b.w), bf16hi(a.w) + bf16hi(b.w));
-  reinterpret_cast<uint4*>(dst)[i] = a;
 }
 
 }  // namespace moe

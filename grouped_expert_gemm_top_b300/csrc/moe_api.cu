@@ -22,7 +22,7 @@ namespace {
 using moe::GemmArgs;
 using moe::GemmCfg;
 
-constexpr int32_t kAbiVersion = 8;
+constexpr int32_t kAbiVersion = 10;
 constexpr size_t kAlign = 256;
 
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
@@ -32,6 +32,7 @@ moe_status check_dims(const moe_dims* d) {
   if (!d) return MOE_ERR_INVALID_ARG;
   if (d->T < 1 || d->H < 64 || d->E < 1 || d->k < 1 || d->I < 64 || d->I_shared < 0)
     return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (d->capacity < 0) return MOE_ERR_INVALID_ARG;
   if (d->H % 64 || d->I % 64 || d->I_shared % 64) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (d->E > moe::kMaxGroups || d->k > d->E || d->k > 32) return MOE_ERR_UNSUPPORTED_SHAPE;
   const long long S = (long long)d->T * d->k;
@@ -462,9 +463,10 @@ moe_status moe_route(const moe_dims* d, int32_t gate_mode, const moe_bf16* x,
     moe::router_topk_kernel<<<tk_blocks, 32 * moe::kTopkWarps, 0, st>>>(
         part, splits, router_bias, logits_out, topk_idx, topk_w, psum, T, E, d->k, gate_mode);
   }
-  if (prob_sum) {  // sum over tokens of the router softmax (auxiliary loss), in block order
+  if (prob_sum) {  // sum over tokens of the router softmax (auxiliary loss), fixed order
     KernelScope ks(MOE_K_AUX, st);
-    moe::prob_sum_kernel<<<(unsigned)cdiv(E, 128), 128, 0, st>>>(psum, (int)tk_blocks, E, prob_sum);
+    moe::prob_sum_kernel<<<(unsigned)cdiv(E, 32), 32 * moe::kProbSumWarps, 0, st>>>(
+        psum, (int)tk_blocks, E, prob_sum);
   }
   return launched(cudaGetLastError());
 }
@@ -498,7 +500,8 @@ moe_status moe_permute(const moe_dims* d, const int32_t* topk_idx, int32_t* expe
       topk_idx, (int)L.S, d->E, counts, at<int>(workspace, 0)); }
   { KernelScope ks(MOE_K_SORT_SCATTER, st);
   moe::sort_scatter_kernel<<<L.sort_blocks, moe::kSortThreads, 0, st>>>(
-      topk_idx, (int)L.S, d->E, L.sort_blocks, counts, expert_offsets, perm_slot, slot_perm); }
+      topk_idx, (int)L.S, d->E, L.sort_blocks, counts, expert_offsets, perm_slot, slot_perm,
+      d->capacity); }
   return launched(cudaGetLastError());
 }
 
@@ -516,7 +519,7 @@ moe_status launch_gate_up(const moe_dims& d, const moe_bf16* x, const int32_t* e
   if (h_out && !make_out_map(&tD1, h_out, I, S)) return MOE_ERR_CUDA;
   if (gu_out && !make_out_map(&tD0, gu_out, 2LL * I, S)) return MOE_ERR_CUDA;
   GemmArgs a = base_args(status);
-  a.N = 2 * I; a.K = H; a.G = E; a.offsets = expert_offsets;
+  a.N = 2 * I; a.K = H; a.G = E; a.offsets = expert_offsets; a.cap = d.capacity;
   a.gsrc = reinterpret_cast<const __nv_bfloat16*>(x); a.gld = H; a.gperm = perm_slot;
   a.gdiv = d.k; a.gsrc_rows = d.T;
   a.gu_out = reinterpret_cast<__nv_bfloat16*>(gu_out); a.h_out = h_out; a.inter = I;
@@ -575,7 +578,7 @@ moe_status moe_grouped_mlp_fwd(const moe_dims* d, const moe_bf16* x,
     CUtensorMap tD;
     if (!make_out_map(&tD, y_perm, H, S)) return MOE_ERR_CUDA;
     GemmArgs a = base_args(status);
-    a.N = H; a.K = I; a.G = E; a.offsets = expert_offsets;
+    a.N = H; a.K = I; a.G = E; a.offsets = expert_offsets; a.cap = d->capacity;
     a.d = reinterpret_cast<__nv_bfloat16*>(y_perm); a.ldd = H;
     s = launch_gemm<CfgDown>(MOE_K_DOWN, tA, tB, tD, tD, a, (cdiv(S, moe::BM) + E) * cdiv(H, 256), st);
     if (s != MOE_OK) return s;
@@ -693,7 +696,7 @@ moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_
     if (!make_map3(&tB, w_down, I, H, E, 64, 64)) return MOE_ERR_CUDA;
     const CUtensorMap& tA = tB;  // unused: A is gathered
     GemmArgs a = base_args(status);
-    a.N = I; a.K = H; a.G = E; a.offsets = expert_offsets; a.padded = 1;
+    a.N = I; a.K = H; a.G = E; a.offsets = expert_offsets; a.cap = d->capacity; a.padded = 1;
     a.gsrc = gob; a.gld = H; a.gperm = perm_slot; a.gdiv = k; a.gsrc_rows = T;
     a.poff_out = poff;
     a.inter = I; a.gu_saved = reinterpret_cast<const __nv_bfloat16*>(gu_saved);
@@ -708,7 +711,7 @@ moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_
     if (!make_map(&tA, dgu, 2LL * I, P, 1, 64, 128)) return MOE_ERR_CUDA;
     if (!make_map3(&tB, w_gate_up, H, 2LL * I, E, 64, 64)) return MOE_ERR_CUDA;
     GemmArgs a = base_args(status);
-    a.N = H; a.K = 2 * I; a.G = E; a.offsets = expert_offsets; a.padded = 1;
+    a.N = H; a.K = 2 * I; a.G = E; a.offsets = expert_offsets; a.cap = d->capacity; a.padded = 1;
     a.d = dxs; a.ldd = H;
     CUtensorMap tD;
     if (!make_out_map(&tD, dxs, H, P)) return MOE_ERR_CUDA;
@@ -748,6 +751,34 @@ moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_
       if (s != MOE_OK) return s;
     }
   }
+  float* dbp = at<float>(workspace, L.db_part);
+  const int aux_blocks = (int)cdiv((long long)T, moe::kAuxDlWarps);
+  if (aux) {
+    {  // dense logit gradient with the auxiliary loss's term (and its column sums)
+      KernelScope ks(MOE_K_AUX, st);
+      if (k <= 8)
+        moe::aux_dl_kernel<8><<<(unsigned)aux_blocks, 32 * moe::kAuxDlWarps, 0, st>>>(
+            router_logits, aux_coef, topk_idx, topk_w, slot_perm, expert_offsets, poff, dwp,
+            L.nDW, (int)P, dl, T, E, k, rs.ldE, dlb, dbp);
+      else
+        moe::aux_dl_kernel<32><<<(unsigned)aux_blocks, 32 * moe::kAuxDlWarps, 0, st>>>(
+            router_logits, aux_coef, topk_idx, topk_w, slot_perm, expert_offsets, poff, dwp,
+            L.nDW, (int)P, dl, T, E, k, rs.ldE, dlb, dbp);
+      if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+    }
+    // the router's term of grad_x, dense over the experts: grad_x = DL W_r (a
+    // small GEMM); the gather below adds the slot gradients into it
+    CUtensorMap tA, tB, tD;
+    if (!make_map(&tA, dlb, rs.ldE, T, 1, 64, 128)) return MOE_ERR_CUDA;
+    if (!make_map(&tB, w_router, H, E, 1, 64, 64)) return MOE_ERR_CUDA;
+    if (!make_out_map(&tD, grad_x, H, T)) return MOE_ERR_CUDA;
+    GemmArgs a = base_args(status);
+    a.N = H; a.K = (int)(cdiv(rs.ldE, moe::BK) * moe::BK); a.G = 1; a.single_rows = T;
+    a.d = reinterpret_cast<__nv_bfloat16*>(grad_x); a.ldd = H;
+    s = launch_gemm<CfgRouterDx>(MOE_K_ROUTER_DX, tA, tB, tD, tD, a,
+                                 cdiv(T, moe::BM) * cdiv(H, 256), st);
+    if (s != MOE_OK) return s;
+  }
   {  // router backward + per-token gather of the slot gradients
     KernelScope ks(MOE_K_DX_GATHER, st);
     const unsigned blocks = (unsigned)cdiv((long long)T * 32, 256);
@@ -757,23 +788,14 @@ moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_
       moe::dx_gather_kernel<8><<<blocks, 256, 0, st>>>(dxs, topk_idx, topk_w, slot_perm,
                                                        expert_offsets, poff, dwp, L.nDW, wr,
                                                        dxs_sh, dl, aux ? nullptr : dlb, rs.ldE,
-                                                       aux ? 0 : 1, gx, T, H, k, E, (int)P);
+                                                       aux ? 0 : 1, aux ? 1 : 0, gx, T, H, k, E,
+                                                       (int)P);
     else
       moe::dx_gather_kernel<32><<<blocks, 256, 0, st>>>(dxs, topk_idx, topk_w, slot_perm,
                                                         expert_offsets, poff, dwp, L.nDW, wr,
                                                         dxs_sh, dl, aux ? nullptr : dlb, rs.ldE,
-                                                        aux ? 0 : 1, gx, T, H, k, E, (int)P);
-  }
-  float* dbp = at<float>(workspace, L.db_part);
-  const int aux_blocks = (int)cdiv((long long)T, moe::kAuxDlWarps);
-  if (aux) {  // dense logit gradient with the auxiliary loss's term (and its column sums)
-    KernelScope ks(MOE_K_AUX, st);
-    if (k <= 8)
-      moe::aux_dl_kernel<8><<<(unsigned)aux_blocks, 32 * moe::kAuxDlWarps, 0, st>>>(
-          router_logits, aux_coef, topk_idx, dl, T, E, k, rs.ldE, dlb, dbp);
-    else
-      moe::aux_dl_kernel<32><<<(unsigned)aux_blocks, 32 * moe::kAuxDlWarps, 0, st>>>(
-          router_logits, aux_coef, topk_idx, dl, T, E, k, rs.ldE, dlb, dbp);
+                                                        aux ? 0 : 1, aux ? 1 : 0, gx, T, H, k, E,
+                                                        (int)P);
     if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
   }
   {  // router weight gradient: dW_r = DL^T x, split-K over the tokens (fp32 partials) ...
@@ -797,29 +819,12 @@ moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_
         reinterpret_cast<__nv_bfloat16*>(grad_w_router), grad_router_bias);
     if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
   }
-  if (aux) {  // the router's term of grad_x, dense over the experts: DL W_r (a small GEMM) ...
-    __nv_bfloat16* rx = dxs;  // free again after the gather-sum
-    CUtensorMap tA, tB, tD;
-    if (!make_map(&tA, dlb, rs.ldE, T, 1, 64, 128)) return MOE_ERR_CUDA;
-    if (!make_map(&tB, w_router, H, E, 1, 64, 64)) return MOE_ERR_CUDA;
-    if (!make_out_map(&tD, rx, H, T)) return MOE_ERR_CUDA;
-    GemmArgs a = base_args(status);
-    a.N = H; a.K = (int)(cdiv(rs.ldE, moe::BK) * moe::BK); a.G = 1; a.single_rows = T;
-    a.d = rx; a.ldd = H;
-    s = launch_gemm<CfgRouterDx>(MOE_K_AUX, tA, tB, tD, tD, a, cdiv(T, moe::BM) * cdiv(H, 256), st);
-    if (s != MOE_OK) return s;
-    KernelScope ks(MOE_K_AUX, st);  // ... added into grad_x
-    const long long n8 = (long long)T * H / 8;
-    moe::add_bf16_kernel<<<(unsigned)cdiv(n8, 256), 256, 0, st>>>(
-        reinterpret_cast<__nv_bfloat16*>(grad_x), rx, n8);
-    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
-  }
   {  // dW_down[e] = sum over the expert's rows of dout[token]^T (w h)
     CUtensorMap tA, tB;
     if (!make_map(&tB, hw, I, P, 1, 64, 64)) return MOE_ERR_CUDA;
     tA = tB;  // unused: A = grad_out rows, gathered
     GemmArgs a = base_args(status);
-    a.M = H; a.N = I; a.G = E; a.offsets = expert_offsets; a.padded = 1;
+    a.M = H; a.N = I; a.G = E; a.offsets = expert_offsets; a.cap = d->capacity; a.padded = 1;
     a.gsrc = gob; a.gld = H; a.gperm = perm_slot; a.gdiv = k; a.gsrc_rows = T;
     a.d = reinterpret_cast<__nv_bfloat16*>(grad_w_down); a.ldd = I;
     a.d_group_stride = (long long)H * I;
@@ -834,7 +839,7 @@ moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_
     if (!make_map(&tA, dgu, 2LL * I, P, 1, 64, 64)) return MOE_ERR_CUDA;
     tB = tA;  // unused: B = x rows, gathered by token
     GemmArgs a = base_args(status);
-    a.M = 2 * I; a.N = H; a.G = E; a.offsets = expert_offsets; a.padded = 1;
+    a.M = 2 * I; a.N = H; a.G = E; a.offsets = expert_offsets; a.cap = d->capacity; a.padded = 1;
     a.gsrc = xb; a.gld = H; a.gperm = perm_slot; a.gdiv = k; a.gsrc_rows = T;
     a.d = reinterpret_cast<__nv_bfloat16*>(grad_w_gate_up); a.ldd = H;
     a.d_group_stride = 2LL * I * H;
@@ -884,7 +889,7 @@ const char* moe_kernel_name(int32_t id) {
       "down", "shared_gate_up", "shared_down", "combine", "dgrad_down",
       "dgrad_gate_up", "shared_dgrad_down", "shared_dgrad_gate_up", "dx_gather",
       "router_wgrad", "wgrad_down", "wgrad_gate_up", "shared_wgrad_down",
-      "shared_wgrad_gate_up", "router_wgrad_reduce", "aux_loss"};
+      "shared_wgrad_gate_up", "router_wgrad_reduce", "aux_loss", "router_dx"};
   return (id >= 0 && id < MOE_K_COUNT) ? names[id] : "unknown";
 }
 
@@ -997,6 +1002,7 @@ extern "C" moe_status moe_permute_static_scratch(const moe_dims* d, const int32_
   moe::sort_histogram_kernel<<<(unsigned)blocks, moe::kSortThreads, 0, st>>>(
       topk_idx, (int)S, d->E, counts, device_status);
   moe::sort_scatter_kernel<<<(unsigned)blocks, moe::kSortThreads, 0, st>>>(
-      topk_idx, (int)S, d->E, (int)blocks, counts, expert_offsets, perm_slot, slot_perm);
+      topk_idx, (int)S, d->E, (int)blocks, counts, expert_offsets, perm_slot, slot_perm,
+      d->capacity);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -13,8 +13,10 @@ order (forward, then backward).
 from __future__ import annotations
 
 import ctypes
+import math
 import os
 import re
+from fractions import Fraction
 
 import torch
 
@@ -38,13 +40,15 @@ class MoeError(RuntimeError):
 
 class MoeDims(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int32), ("H", ctypes.c_int32), ("E", ctypes.c_int32),
-                ("k", ctypes.c_int32), ("I", ctypes.c_int32), ("I_shared", ctypes.c_int32)]
+                ("k", ctypes.c_int32), ("I", ctypes.c_int32), ("I_shared", ctypes.c_int32),
+                ("capacity", ctypes.c_int32)]
 
     @classmethod
-    def of(cls, T, H, E, k, I, I_shared=0):
-        return cls(int(T), int(H), int(E), int(k), int(I), int(I_shared))
+    def of(cls, T, H, E, k, I, I_shared=0, capacity=0):
+        return cls(int(T), int(H), int(E), int(k), int(I), int(I_shared), int(capacity))
 
     def as_tuple(self):
+        """The shape (T, H, E, k, I, I_shared); capacity is a separate field."""
         return (self.T, self.H, self.E, self.k, self.I, self.I_shared)
 
 
@@ -126,6 +130,18 @@ def _check(call: str, st: int):
 
 def _dims(d) -> MoeDims:
     return d if isinstance(d, MoeDims) else MoeDims.of(*d)
+
+
+def expert_capacity(T: int, k: int, E: int, factor: float) -> int:
+    """Slots each expert keeps for a capacity factor: ceil(factor * T * k / E).
+
+    The library takes the integer (moe_dims.capacity, 0 = no limit), so a
+    factor whose capacity rounds to 0 is refused here rather than silently
+    meaning "no limit"."""
+    c = math.ceil(Fraction(str(factor)) * T * k / E)   # the factor as written, exactly
+    if c < 1:
+        raise ValueError(f"capacity factor {factor} keeps no slot per expert")
+    return c
 
 
 # ----------------------------------------------------------------- C-ABI calls
@@ -244,12 +260,14 @@ class MoeLayer:
     """
 
     def __init__(self, dims, gate_mode=MOE_GATE_SOFTMAX_TOPK, device="cuda", with_backward=True,
-                 save_logits=False, recompute=False, aux_alpha=None):
+                 save_logits=False, recompute=False, aux_alpha=None, capacity=0):
         """recompute: the forward keeps no gate/up pre-activations; the
         backward recomputes them (activation recompute).  aux_alpha: add the
         auxiliary load-balancing loss with this coefficient (its value lands
-        in self.aux_loss after forward; its gradient is added in backward)."""
-        self.dims = _dims(dims)
+        in self.aux_loss after forward; its gradient is added in backward).
+        capacity: slots each expert keeps (0: no limit); the others are
+        dropped (slot_perm -1; their rows of y_perm / gu_saved are not written)."""
+        self.dims = MoeDims.of(*_dims(dims).as_tuple(), capacity=capacity)
         T, H, E, k, I, Is = self.dims.as_tuple()
         S = T * k
         self.gate_mode = gate_mode

@@ -67,8 +67,20 @@ typedef enum {
   MOE_GATE_BALANCED = 1      /* balanced gate: slot (t,j) -> expert (t*k+j) mod E */
 } moe_gate_mode;
 
+/*
+ * capacity: expert capacity, the most token-slots one expert processes
+ * (0 = no limit, < 0 rejected).  The pages name expert overflow as a risk of
+ * uneven routing ("NVIDIA NeMo AutoModel MoE 微調的 3.7 倍加速突破", closing
+ * paragraph on load balancing) but give no rule; the reading here: an expert
+ * keeps its first `capacity` slots in slot order s = t*k + j (the stable
+ * sort's order), the rest are dropped.  A dropped slot adds nothing to out
+ * (its weight is not redistributed), its expert never sees it, its dL/dw is
+ * 0, and the router gradient keeps its formula.  For a capacity factor f use
+ * capacity = ceil(f * T * k / E).
+ */
 typedef struct {
   int32_t T, H, E, k, I, I_shared;
+  int32_t capacity;
 } moe_dims;
 
 /* Version of this ABI (bumped on any signature or enum change). */
@@ -135,6 +147,9 @@ moe_status moe_aux_loss(const moe_dims* d, const float* prob_sum, const int32_t*
  *                   expert_offsets[e] .. expert_offsets[e+1]-1; offsets[E] = S
  *   perm_slot:      int32 [S], slot id at sorted row r (ascending within an expert)
  *   slot_perm:      int32 [S], sorted row of slot s (inverse of perm_slot)
+ * With d->capacity > 0, expert e's first min(count_e, capacity) rows are its
+ * kept slots; the rest are dropped, and slot_perm is -1 for a dropped slot
+ * (perm_slot and expert_offsets stay the full sort).
  * Only ids move; no expert weight is touched.  Expert ids outside [0, E) are
  * skipped and reported as MOE_ERR_DEVICE_INDEX in the status word.
  */
@@ -156,6 +171,8 @@ moe_status moe_permute(const moe_dims* d, const int32_t* topk_idx, int32_t* expe
  * w_sh_gate_up bf16 [2*I_shared,H], w_sh_down bf16 [H,I_shared]; sh_gu_saved
  * bf16 [T,2*I_shared] or NULL; y_shared bf16 [T,H].  Pass NULLs when
  * I_shared == 0.
+ * With d->capacity > 0 each expert runs only its first min(count_e, capacity)
+ * rows; the rows of dropped slots in y_perm and gu_saved are not written.
  */
 moe_status moe_grouped_mlp_fwd(const moe_dims* d, const moe_bf16* x,
                                const int32_t* expert_offsets, const int32_t* perm_slot,
@@ -170,8 +187,9 @@ moe_status moe_grouped_mlp_fwd(const moe_dims* d, const moe_bf16* x,
  * DeepEP paragraphs):
  *   out[t] = sum_{j=0..k-1} topk_w[t,j] * y_perm[slot_perm[t*k+j]]  (+ y_shared[t])
  * summed in fp32 in j order, rounded to bf16 once.  y_perm bf16 [S,H];
- * slot_perm int32 [S]; topk_w fp32 [T,k]; y_shared bf16 [T,H] or NULL;
- * out bf16 [T,H].  Needs no workspace.
+ * slot_perm int32 [S] (-1: slot dropped by the expert capacity, skipped);
+ * topk_w fp32 [T,k]; y_shared bf16 [T,H] or NULL; out bf16 [T,H].  Needs no
+ * workspace.
  */
 moe_status moe_unpermute_combine(const moe_dims* d, const moe_bf16* y_perm,
                                  const int32_t* slot_perm, const float* topk_w,
@@ -202,7 +220,9 @@ moe_status moe_unpermute_combine(const moe_dims* d, const moe_bf16* y_perm,
  * logits_out, fp32 [T,E]), its gradient p[t,e] (c_e - sum_e' c_e' p[t,e']) is
  * added for every expert of every token; NULL aux_coef: no auxiliary loss
  * (router_logits may then be NULL).  Experts that received no
- * token get exact-zero weight gradients.
+ * token get exact-zero weight gradients.  With d->capacity > 0 (the same
+ * value as in the forward), dropped slots (slot_perm -1) send no gradient to
+ * their expert and have dw_j = 0; their dlogit still follows the formula.
  */
 moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_bf16* x,
                          const moe_bf16* w_router, const int32_t* topk_idx, const float* topk_w,
@@ -285,8 +305,9 @@ typedef enum {
   MOE_K_SHARED_WGRAD_DOWN,
   MOE_K_SHARED_WGRAD_GATE_UP,
   MOE_K_ROUTER_WGRAD_REDUCE, /* backward: sum of the router weight-gradient splits, bias gradient */
-  MOE_K_AUX,                 /* auxiliary loss: probability sums, loss, dense logit gradient,
-                                and the router term of grad_x */
+  MOE_K_AUX,                 /* auxiliary loss: probability sums, loss, dense logit gradient */
+  MOE_K_ROUTER_DX,           /* backward with the auxiliary loss: grad_x = DL W_r (GEMM), before
+                                the per-token gather adds the slot gradients into it */
   MOE_K_COUNT
 } moe_kernel_id;
 

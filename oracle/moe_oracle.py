@@ -66,6 +66,7 @@ special cases, finite differences).
 from __future__ import annotations
 
 import math
+from fractions import Fraction
 
 import numpy as np
 
@@ -189,8 +190,9 @@ def permute(topk_idx: np.ndarray, E: int):
 
 
 def expert_capacity(T: int, k: int, E: int, factor: float) -> int:
-    """Slots an expert keeps for capacity factor `factor`: ceil(factor * T * k / E)."""
-    return int(math.ceil(factor * T * k / E))
+    """Slots an expert keeps for capacity factor `factor`: ceil(factor * T * k / E),
+    with the factor taken as the decimal it is written as (1.1 is 11/10)."""
+    return int(math.ceil(Fraction(str(factor)) * T * k / E))
 
 
 def keep_slots(topk_idx: np.ndarray, E: int, capacity: int | None) -> np.ndarray:

@@ -92,11 +92,11 @@ def run_forward(di: DeviceInputs, with_backward=True, save_logits=True):
     return layer
 
 
-def oracle_forward(di: DeviceInputs, topk_idx=None):
+def oracle_forward(di: DeviceInputs, topk_idx=None, capacity=None):
     return O.layer_forward(di.f64("x"), di.f64("w_router"), di.f64("w_gate_up"), di.f64("w_down"),
                            di.w.k, balanced=di.w.gate == G.GATE_BALANCED,
                            bias=di.f64("router_bias"), w_sh_gu=di.f64("w_sh_gate_up"),
-                           w_sh_down=di.f64("w_sh_down"), topk_idx=topk_idx)
+                           w_sh_down=di.f64("w_sh_down"), topk_idx=topk_idx, capacity=capacity)
 
 
 def logit_error_bound(x64, wr64):

@@ -35,7 +35,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert M.moe_abi_version() == 8
+    assert M.moe_abi_version() == 10
     assert M.moe_status_string(0) == "ok"
     for s in range(1, 7):
         assert M.moe_status_string(s) not in ("ok", "unknown status")
@@ -116,3 +116,22 @@ def test_binding_refuses_cpu_tensors(lib):
     x = torch.zeros(4, 4)
     with pytest.raises(ValueError):
         M._ptr(x)
+
+
+def test_capacity_field_validation(lib):
+    d = M.MoeDims.of(64, 128, 4, 2, 128, 0, capacity=-1)
+    out = ctypes.c_size_t(0)
+    assert lib.moe_workspace_size(ctypes.byref(d), 1, ctypes.byref(out)) == 1   # invalid arg
+    for cap in (0, 1, 1000):
+        d = M.MoeDims.of(64, 128, 4, 2, 128, 0, capacity=cap)
+        assert lib.moe_workspace_size(ctypes.byref(d), 1, ctypes.byref(out)) == 0
+    assert ctypes.sizeof(M.MoeDims) == 7 * 4
+
+
+def test_expert_capacity_helper():
+    assert M.expert_capacity(4096, 8, 128, 1.0) == 256
+    assert M.expert_capacity(4096, 8, 128, 0.75) == 192
+    assert M.expert_capacity(10, 2, 3, 1.0) == 7
+    assert M.expert_capacity(100, 1, 10, 1.1) == 11
+    with pytest.raises(ValueError):
+        M.expert_capacity(8, 1, 4, 0.0)

@@ -264,3 +264,62 @@ def test_aux_loss_forward_and_backward(name):
     else:
         assert np.allclose(U.to_f64(g["grad_w_router"]), U.to_f64(g0["grad_w_router"]),
                            rtol=1e-2, atol=1e-2 * np.abs(U.to_f64(g0["grad_w_router"])).max())
+
+
+def _run_layer(di, **kw):
+    w = di.w
+    layer = M.MoeLayer(di.dims, gate_mode=w.gate, with_backward=True, save_logits=True, **kw)
+    layer.forward(di.x, di.w_router, di.w_gate_up, di.w_down, di.router_bias, di.w_sh_gate_up,
+                  di.w_sh_down)
+    grads = layer.alloc_grads(with_bias=w.bias_std > 0)
+    layer.backward(di.grad_out, di.x, di.w_router, di.w_gate_up, di.w_down, grads,
+                   di.w_sh_gate_up, di.w_sh_down)
+    torch.cuda.synchronize()
+    assert M.moe_read_device_status(layer.workspace) == 0
+    return layer, {k: v.clone() for k, v in grads.items() if v is not None}
+
+
+@pytest.mark.parametrize("name,factor", [("ragged", 0.6), ("skewed_mid", 1.0),
+                                         ("ragged_shared", 0.8), ("balanced_small", 0.75),
+                                         ("tiny", None)])
+def test_capacity_forward_and_backward(name, factor):
+    """Expert capacity (token dropping): the full sort and the kept/dropped
+    split bit-exact (slot_perm -1 on dropped slots), out, the kept slots' rows
+    of y_perm and gu_saved, and every gradient against the oracle with the
+    same capacity.  factor None: capacity 1, nearly every slot dropped."""
+    w = CASES[name]
+    C = M.expert_capacity(w.T, w.k, w.E, factor) if factor else 1
+    di = U.DeviceInputs(w, seed=3, with_grad=True)
+    layer, g = _run_layer(di, capacity=C)
+    idx = layer.topk_idx.cpu().numpy()
+    off, perm, inv = O.permute(idx, w.E)
+    keep = O.keep_slots(idx, w.E, C)
+    assert (~keep).any()
+    assert np.array_equal(layer.expert_offsets.cpu().numpy(), off)
+    assert np.array_equal(layer.perm_slot.cpu().numpy(), perm)
+    assert np.array_equal(layer.slot_perm.cpu().numpy(), np.where(keep.ravel(), inv, -1))
+    f = U.oracle_forward(di, topk_idx=idx, capacity=C)
+    U.check_close(layer.out, f["out"], "out (capacity)")
+    rows = torch.from_numpy(inv[keep.ravel()].astype(np.int64)).cuda()
+    U.check_close(layer.y_perm[rows], f["y_perm"][inv[keep.ravel()]], "y_perm (kept rows)")
+    U.check_close(layer.gu_saved[rows], f["gu_perm"][inv[keep.ravel()]], "gu_saved (kept rows)")
+    b = O.layer_backward(f, di.f64("grad_out"), di.f64("x"), di.f64("w_router"),
+                         di.f64("w_gate_up"), di.f64("w_down"), w.k,
+                         w_sh_gu=di.f64("w_sh_gate_up"), w_sh_down=di.f64("w_sh_down"))
+    for key, got in g.items():
+        U.check_close(got, b[key], key + " (capacity)")
+
+
+@pytest.mark.parametrize("name", ["ragged", "balanced_small"])
+def test_capacity_at_or_above_max_count_is_bit_identical(name):
+    """A capacity no expert reaches drops nothing: outputs and gradients are
+    bit-identical to the layer without a capacity."""
+    w = CASES[name]
+    di = U.DeviceInputs(w, seed=4, with_grad=True)
+    l0, g0 = _run_layer(di)
+    cmax = int(np.diff(l0.expert_offsets.cpu().numpy()).max())
+    l1, g1 = _run_layer(di, capacity=cmax)
+    assert torch.equal(l1.slot_perm, l0.slot_perm)
+    assert torch.equal(l1.out, l0.out)
+    for key in g0:
+        assert torch.equal(g1[key], g0[key]), key

@@ -376,6 +376,7 @@ def test_expert_capacity_closed_forms():
     assert O.expert_capacity(10, 2, 3, 1.0) == 7          # ceil(20 / 3)
     assert O.expert_capacity(10, 2, 3, 0.5) == 4          # ceil(10 / 3)
     assert O.expert_capacity(8, 1, 4, 0.0) == 0
+    assert O.expert_capacity(100, 1, 10, 1.1) == 11     # 1.1 * 100 / 10, not 11.000000000000002
 
 
 def test_keep_slots_hand_example():

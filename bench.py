@@ -105,13 +105,13 @@ def kernel_model(name, w, counts, P):
 
 def measured_traffic(kernel, workload):
     """DRAM bytes per launch from the committed ncu capture, or None when the
-    GEMM kernel sources changed since the capture (or no capture covers it)."""
+    kernel sources changed since the capture (or no capture covers it)."""
     import hashlib
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             rec = json.load(f)
         h = hashlib.md5()
-        for name in ("gemm.cuh", "gemm_res.cuh", "ptx.cuh"):
+        for name in ("gemm.cuh", "gemm_res.cuh", "ptx.cuh", "kernels_misc.cuh"):
             with open(os.path.join(ROOT, "grouped_expert_gemm_top_b300", "csrc", name), "rb") as f:
                 h.update(f.read())
         k = rec["kernels"].get(kernel)
@@ -410,22 +410,31 @@ def run_ours(args, w, rank, world):
         fwd_inf()
     ms_f = timed(fwd_inf, args.steps)
     assert M.moe_read_device_status(layer.workspace) == 0, "device reported an error"
-    # ---- forward + backward with activation recompute
-    for _ in range(max(1, args.warmup // 2)):
-        step_rc()
-    ms_rc = timed(step_rc, args.steps)
-    assert M.moe_read_device_status(layer_rc.workspace) == 0, "device reported an error"
-    # ---- forward + backward with the auxiliary load-balancing loss
-    for _ in range(max(1, args.warmup // 2)):
-        step_aux()
-    ms_aux = timed(step_aux, args.steps)
-    assert M.moe_read_device_status(layer_aux.workspace) == 0, "device reported an error"
-    # ---- forward + backward with the expert capacity
-    for _ in range(max(1, args.warmup // 2)):
-        step_cap()
-    ms_cap = timed(step_cap, args.steps)
-    assert M.moe_read_device_status(layer_cap.workspace) == 0, "device reported an error"
+    # ---- the variants (activation recompute, auxiliary loss, expert
+    # capacity), each timed in alternating blocks with the plain step so that
+    # the GPU's drift over a run (it slows as it warms) cancels in the
+    # comparison: medians of 3 blocks of each
+    def paired(fn, lay):
+        for _ in range(max(1, args.warmup // 2)):
+            fn()
+        a, b = [], []
+        for _ in range(3):
+            a.append(timed(step, args.steps))
+            b.append(timed(fn, args.steps))
+        assert M.moe_read_device_status(lay.workspace) == 0, "device reported an error"
+        return statistics.median(b), statistics.median(a)
+
+    ms_rc, ms_rc_plain = paired(step_rc, layer_rc)
+    ms_aux, ms_aux_plain = paired(step_aux, layer_aux)
+    ms_cap, ms_cap_plain = paired(step_cap, layer_cap)
     kept = int(np.minimum(np.diff(layer_cap.expert_offsets.cpu().numpy()), cap).sum())
+    # ---- sustained: the plain step for ~3 s (the GPU's steady state under
+    # its power limit), clocks sampled meanwhile
+    n_sus = max(args.steps, int(args.sustain_s * 1e3 / (ms_fb / args.steps)))
+    ms_sus, clocks_sus = None, None
+    if args.sustain_s > 0:
+        with ClockSampler(local) as clocks_sus:
+            ms_sus = timed(step, n_sus)
 
     # ---- end to end: pinned host inputs in, result out, every step
     xh = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
@@ -510,18 +519,26 @@ def run_ours(args, w, rank, world):
         # pre-activations (S*2I bf16), the backward reruns the gate/up GEMM
         "recompute": {"tokens_per_s": job_tokens_per_s(w.T, world, args.steps, ms_rc),
                       "ms_per_step": ms_rc / args.steps,
+                      "plain_ms_per_step_adjacent": ms_rc_plain / args.steps,
                       "saved_bytes_not_held": w.T * w.k * 2 * w.I * 2 + w.T * 2 * w.I_shared * 2,
                       "extra_flops": 2.0 * w.T * w.k * w.H * 2 * w.I + 2.0 * w.T * w.H * 2 * w.I_shared},
         # forward+backward with the auxiliary load-balancing loss (alpha 0.01): its value
         # on the device, and the step time with its dense router gradient
         "aux_loss": {"tokens_per_s": job_tokens_per_s(w.T, world, args.steps, ms_aux),
                      "ms_per_step": ms_aux / args.steps,
+                     "plain_ms_per_step_adjacent": ms_aux_plain / args.steps,
                      "value": float(layer_aux.aux_loss.item()), "alpha": 0.01},
         # forward+backward with an expert capacity (token dropping)
         "capacity": {"factor": cap_factor, "capacity": cap,
                      "dropped_fraction": 1.0 - kept / (w.T * w.k),
                      "tokens_per_s": job_tokens_per_s(w.T, world, args.steps, ms_cap),
-                     "ms_per_step": ms_cap / args.steps},
+                     "ms_per_step": ms_cap / args.steps,
+                     "plain_ms_per_step_adjacent": ms_cap_plain / args.steps},
+        # the plain step repeated for ~3 s: steady-state rate and clocks
+        "sustained": None if ms_sus is None else {
+            "steps": n_sus, "seconds": ms_sus / 1e3,
+            "tokens_per_s": job_tokens_per_s(w.T, world, n_sus, ms_sus),
+            "ms_per_step": ms_sus / n_sus, "clocks": clocks_sus.summary()},
         "layer_roofline": {
             "fwd": {"t_roof_us": t_roof_f * 1e6, "t_us": t_f * 1e6, "frac": t_roof_f / t_f,
                     "flops": f_fwd, "bytes": b_fwd},
@@ -553,6 +570,8 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=2048)
     ap.add_argument("--ref-tokens", type=int, default=256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sustain-s", type=float, default=3.0,
+                    help="seconds of the extra steady-state pass (0: no such pass)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 

@@ -68,6 +68,7 @@ struct GemmArgs {
   const __nv_bfloat16* gu_saved; const int32_t* perm_slot; const float* slot_w;
   __nv_bfloat16* dgu_out; __nv_bfloat16* hw_out; float* dw_part;
   int* status;
+  int out_evict_first;   // 1: stores carry the L2 evict-first policy (weight gradients)
 };
 
 template <int BN_, int STAGES_, int AL_, int BL_, int SCH_, int EPI_, bool B3D_, bool SWIGLU_B_,
@@ -287,6 +288,8 @@ struct WarpOut {
   int lane;
   int next;       // next buffer to use
   int inflight;   // committed stores not yet known to have read their buffer
+  bool evict_first;  // stores carry the L2 evict-first policy
+  uint64_t policy;
 };
 
 // Take the next K staging buffers (the first is returned, the others follow at
@@ -313,8 +316,13 @@ __device__ __forceinline__ void stage_store(WarpOut<NB, BYTES>& w, uint32_t buf,
   fence_proxy_async_smem();
   __syncwarp();
   if (w.lane == 0) {
-    if (three_d) tma_store_3d(map, buf, x, y, z);
-    else tma_store_2d(map, buf, x, y);
+    if (w.evict_first) {
+      if (three_d) tma_store_3d_hint(map, buf, x, y, z, w.policy);
+      else tma_store_2d_hint(map, buf, x, y, w.policy);
+    } else {
+      if (three_d) tma_store_3d(map, buf, x, y, z);
+      else tma_store_2d(map, buf, x, y);
+    }
     bulk_commit();
   }
   __syncwarp();
@@ -1032,6 +1040,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     wo.lane = lane;
     wo.next = 0;
     wo.inflight = 0;
+    wo.evict_first = a.out_evict_first != 0;
+    wo.policy = wo.evict_first ? policy_evict_first() : 0;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = unit0; t < total && !*abort_flag; t += ustep) {

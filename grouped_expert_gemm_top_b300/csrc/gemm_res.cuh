@@ -470,6 +470,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     wo.lane = lane;
     wo.next = 0;
     wo.inflight = 0;
+    wo.evict_first = a.out_evict_first != 0;
+    wo.policy = wo.evict_first ? policy_evict_first() : 0;
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;

@@ -830,6 +830,7 @@ moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_
     a.d_group_stride = (long long)H * I;
     CUtensorMap tD;
     if (!make_out_map3(&tD, grad_w_down, I, H, E)) return MOE_ERR_CUDA;
+    a.out_evict_first = 1;  // nothing in the layer reads the weight gradients back
     s = launch_gemm<CfgWgradDownRes, true>(MOE_K_WGRAD_DOWN, tA, tB, tD, tD, a,
                                            (long long)E * cdiv(H, 2 * moe::BM) * cdiv(I, 256), st);
     if (s != MOE_OK) return s;
@@ -845,6 +846,7 @@ moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_
     a.d_group_stride = 2LL * I * H;
     CUtensorMap tD;
     if (!make_out_map3(&tD, grad_w_gate_up, H, 2LL * I, E)) return MOE_ERR_CUDA;
+    a.out_evict_first = 1;  // nothing in the layer reads the weight gradients back
     s = launch_gemm<CfgWgradRes, true>(MOE_K_WGRAD_GATE_UP, tA, tB, tD, tD, a,
                                        (long long)E * cdiv(2 * I, 2 * moe::BM) * cdiv(H, 256), st);
     if (s != MOE_OK) return s;
@@ -862,6 +864,7 @@ moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_
       a.d = reinterpret_cast<__nv_bfloat16*>(grad_w_sh_down); a.ldd = Is;
       CUtensorMap tD;
       if (!make_out_map3(&tD, grad_w_sh_down, Is, H, 1)) return MOE_ERR_CUDA;
+      a.out_evict_first = 1;  // nothing in the layer reads the weight gradients back
       s = launch_gemm<CfgWgrad>(MOE_K_SHARED_WGRAD_DOWN, tA, tB, tD, tD, a, cdiv(H, moe::BM) * cdiv(Is, 256), st);
       if (s != MOE_OK) return s;
     }
@@ -874,6 +877,7 @@ moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_
       a.d = reinterpret_cast<__nv_bfloat16*>(grad_w_sh_gate_up); a.ldd = H;
       CUtensorMap tD;
       if (!make_out_map3(&tD, grad_w_sh_gate_up, H, 2LL * Is, 1)) return MOE_ERR_CUDA;
+      a.out_evict_first = 1;  // nothing in the layer reads the weight gradients back
       s = launch_gemm<CfgWgrad>(MOE_K_SHARED_WGRAD_GATE_UP, tA, tB, tD, tD, a, cdiv(2 * Is, moe::BM) * cdiv(H, 256), st);
       if (s != MOE_OK) return s;
     }

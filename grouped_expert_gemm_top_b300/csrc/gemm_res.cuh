@@ -24,8 +24,8 @@
 // issues the UMMAs.  Roles:
 //   warp 0      streamed-operand TMA producer (idle when it is gathered)
 //   warp 1      TMEM allocator; UMMA issuer in the even CTA
-//   warps 2..5  epilogue (the streaming kernel's bf16 store epilogue)
-//   warps 6..9  gather warps (a gathered operand only)
+//   warps 2..    epilogue (the streaming kernel's bf16 store epilogue), 4, 8 or 16
+//   next 4      gather warps (a gathered operand only)
 //   last warp   resident-operand TMA loader (idle when it is gathered):
 //               refills k-block slot kb % 4 as soon as the last UMMA reading
 //               it has completed
@@ -36,7 +36,7 @@ namespace moe {
 
 enum ResMode : int { RES_A = 1, RES_B = 2 };
 
-template <int RES_, int AL_, int BL_, int STAGES_, int EPI_BUFS_>
+template <int RES_, int AL_, int BL_, int STAGES_, int EPI_BUFS_, int EPI_WARPS_ = 4>
 struct ResCfg {
   static constexpr int RES = RES_;
   static constexpr int AL = AL_;  // MN_TILE or (streamed, RES_B) MN_GATHER
@@ -47,7 +47,10 @@ struct ResCfg {
   static constexpr bool SWIGLU_B = false;
   static constexpr int SCH = RAGGED_K;
   static constexpr int EPI = EPI_STORE;
-  static constexpr int EPI_WARPS = 4;
+  // 4, 8 or 16 epilogue warps: 1, 2 or 4 per TMEM lane quarter, each on an
+  // equal share of the tile's four 64-column groups
+  static constexpr int EPI_WARPS = EPI_WARPS_;
+  static_assert(EPI_WARPS == 4 || EPI_WARPS == 8 || EPI_WARPS == 16, "epilogue warps per lane quarter");
   static constexpr int EPI_BUFS = EPI_BUFS_;
   static constexpr int EPI_BUF_BYTES = 4096;
   static constexpr bool A_GATHER = AL == MN_GATHER;
@@ -464,6 +467,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     // ================= epilogue =================
     const int quad = warp & 3;
     const int epi = warp - 2;
+    const int cpart = epi >> 2;  // column part of this warp
+    constexpr int nparts = C::EPI_WARPS / 4;
     const int row_in_tile = quad * 32 + lane;
     WarpOut<C::EPI_BUFS, C::EPI_BUF_BYTES> wo;
     wo.buf0 = smem_base + (C::STAGES + C::RSLOTS) * C::BLK + epi * (C::EPI_BUFS * C::EPI_BUF_BYTES);
@@ -482,7 +487,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         if (!mbar_wait(smem_u32(&tfull_bar[acc]), acc_phase, abort_flag, a.status)) { ok = false; break; }
         tc_fence_after();
         const uint32_t tacc = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * C::BN;
-        if (!ti.phantom) epilogue_store<C>(a, ti, tacc, row_in_tile, wo, &tmD0, 0, 1);
+        if (!ti.phantom) epilogue_store<C>(a, ti, tacc, row_in_tile, wo, &tmD0, cpart, nparts);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(&tempty_bar[acc]), 0));

@@ -33,6 +33,19 @@ __device__ __forceinline__ bool topk_before(float va, int ia, float vb, int ib) 
   return va > vb || (va == vb && ia < ib);
 }
 
+// Order-preserving 32-bit key of a logit for the warp argmax: a larger value
+// gives a larger key and -0 ties with +0 (the order above); NaN (outside the
+// contract: logits are finite) gets 1, below every number; 0 marks a slot
+// that is not a candidate (past E, or already taken).
+__device__ __forceinline__ uint32_t logit_key(float v) {
+  if (v != v) return 1u;
+  const uint32_t u = __float_as_uint(v == 0.f ? 0.f : v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_logit(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
+}
+
 constexpr int kMaxGroupsRouter = 256;  // E <= 256
 
 // This lane's experts' softmax probabilities p[t, e] (e = 32 i + lane) of
@@ -99,10 +112,11 @@ __global__ void router_topk_kernel(const float* __restrict__ partial, int splits
   float v[kRouterMaxPerLane];
   float mx = -INFINITY;
 #pragma unroll
+  for (int i = 0; i < kRouterMaxPerLane; ++i) v[i] = -INFINITY;
+#pragma unroll
   for (int i = 0; i < kRouterMaxPerLane; ++i) {
     const int e = i * 32 + lane;
-    v[i] = -INFINITY;
-    if (e < E) {
+    if (i * 32 < E && e < E) {  // the first test is warp-uniform
       float part[kMaxSplitsRouter];
 #pragma unroll
       for (int sp = 0; sp < kMaxSplitsRouter; ++sp)
@@ -122,44 +136,56 @@ __global__ void router_topk_kernel(const float* __restrict__ partial, int splits
   float z = 0.f;
 #pragma unroll
   for (int i = 0; i < kRouterMaxPerLane; ++i)
-    if (i * 32 + lane < E) z += expf(v[i] - mx);
+    if (i * 32 < E && i * 32 + lane < E) z += expf(v[i] - mx);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-  uint32_t taken = 0;
+  // softmax gate: this lane's candidate keys and its best one (ties: lower slot)
+  uint32_t kl[kRouterMaxPerLane];
+  uint32_t lbk = 0u, taken = 0u;
+  int lbi = 0;
+#pragma unroll
+  for (int i = 0; i < kRouterMaxPerLane; ++i) {
+    kl[i] = (gate_mode != 1 && i * 32 + lane < E) ? logit_key(v[i]) : 0u;
+    if (kl[i] > lbk) { lbk = kl[i]; lbi = i; }
+  }
   int my_e = 0;
   float my_p = 0.f;
-  for (int j = 0; j < k; ++j) {
-    float bv;
-    int bi;
-    if (gate_mode == 1) {
-      bi = (int)(((long long)t * k + j) % E);
-      float mine = 0.f;
+  if (gate_mode == 1) {
+    // balanced gate: lane j's expert is (t k + j) mod E; it sums that expert's
+    // logit again, in the owner lane's order, so the value is the same bits
+    if (lane < k) {
+      my_e = (int)(((long long)t * k + lane) % E);
+      float part[kMaxSplitsRouter];
 #pragma unroll
-      for (int i = 0; i < kRouterMaxPerLane; ++i)
-        if (i == (bi >> 5)) mine = v[i];
-      bv = __shfl_sync(0xffffffffu, mine, bi & 31);
-    } else {
-      bv = -INFINITY;
-      bi = 0x7fffffff;
+      for (int sp = 0; sp < kMaxSplitsRouter; ++sp)
+        part[sp] = sp < splits ? __ldg(partial + ((size_t)sp * T + t) * E + my_e) : 0.f;
+      float l = 0.f;
 #pragma unroll
-      for (int i = 0; i < kRouterMaxPerLane; ++i) {
-        const int e = i * 32 + lane;
-        if (e < E && !((taken >> i) & 1u) && topk_before(v[i], e, bv, bi)) {
-          bv = v[i];
-          bi = e;
-        }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (topk_before(ov, oi, bv, bi)) { bv = ov; bi = oi; }
-      }
-      if (bi == 0x7fffffff) bi = j;  // only with NaN logits: stay in range
-      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+      for (int sp = 0; sp < kMaxSplitsRouter; ++sp)
+        if (sp < splits) l += part[sp];
+      if (bias) l += __ldg(bias + my_e);
+      my_p = expf(l - mx) / z;
     }
-    const float p = expf(bv - mx) / z;
-    if (lane == j) { my_e = bi; my_p = p; }
+  } else {
+    for (int j = 0; j < k; ++j) {
+      // warp argmax in two single-instruction reductions: the largest key,
+      // then the lowest expert id holding it
+      const uint32_t kmax = __reduce_max_sync(0xffffffffu, lbk);
+      const int bi = (int)__reduce_min_sync(0xffffffffu,
+                                            lbk == kmax ? (uint32_t)(lbi * 32 + lane) : 0xffffffffu);
+      if ((bi & 31) == lane) {  // the owner drops it and finds its next best
+        taken |= 1u << (bi >> 5);
+        lbk = 0u;
+        lbi = 0;
+#pragma unroll
+        for (int i = 0; i < kRouterMaxPerLane; ++i)
+          if (!((taken >> i) & 1u) && kl[i] > lbk) { lbk = kl[i]; lbi = i; }
+      }
+      if (lane == j) {
+        my_e = bi;
+        my_p = expf(key_logit(kmax) - mx) / z;
+      }
+    }
   }
   float psum = lane < k ? my_p : 0.f;
 #pragma unroll
@@ -222,6 +248,7 @@ __global__ void sort_scatter_kernel(const int32_t* __restrict__ topk_idx, int S,
   // expert totals and this block's start inside each expert
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     int tot = 0, before = 0;
+#pragma unroll 8
     for (int b = 0; b < num_blocks; ++b) {
       const int c = __ldg(block_counts + (size_t)b * E + e);
       before += (b < (int)blockIdx.x) ? c : 0;
@@ -413,17 +440,11 @@ __global__ void dx_gather_kernel(const __nv_bfloat16* __restrict__ dx_slot,
       dl_dense[(size_t)t * ldE + e] = __float2bfloat16_rn(v);
     }
   }
+  // slot rows in chunks of up to 8 (k <= 8: one chunk); per chunk, every slot's
+  // gradient in j order, then every router term in j order; the shared expert
+  // last.  Chunks keep k up to 32 within the register file.
+  constexpr int CH = KMAX < 8 ? KMAX : 8;
   for (int c = lane; c < H / 8; c += 32) {
-    uint4 v[KMAX], r[KMAX];
-#pragma unroll
-    for (int j = 0; j < KMAX; ++j) {
-      if (j < k) {
-        v[j] = rows[j] < 0 ? make_uint4(0u, 0u, 0u, 0u)
-                           : __ldg(reinterpret_cast<const uint4*>(dx_slot + (size_t)rows[j] * H) + c);
-        r[j] = router_term ? __ldg(reinterpret_cast<const uint4*>(w_router + (size_t)es[j] * H) + c)
-                           : make_uint4(0u, 0u, 0u, 0u);
-      }
-    }
     uint4 vs = make_uint4(0, 0, 0, 0);
     if (dx_shared) vs = __ldg(reinterpret_cast<const uint4*>(dx_shared + (size_t)t * H) + c);
     const uint4 va = accumulate ? reinterpret_cast<const uint4*>(dx + (size_t)t * H)[c]
@@ -431,21 +452,37 @@ __global__ void dx_gather_kernel(const __nv_bfloat16* __restrict__ dx_slot,
     float acc[8] = {bf16lo(va.x), bf16hi(va.x), bf16lo(va.y), bf16hi(va.y),
                     bf16lo(va.z), bf16hi(va.z), bf16lo(va.w), bf16hi(va.w)};
 #pragma unroll
-    for (int j = 0; j < KMAX; ++j) {
-      if (j < k) {
-        acc[0] += bf16lo(v[j].x); acc[1] += bf16hi(v[j].x); acc[2] += bf16lo(v[j].y);
-        acc[3] += bf16hi(v[j].y); acc[4] += bf16lo(v[j].z); acc[5] += bf16hi(v[j].z);
-        acc[6] += bf16lo(v[j].w); acc[7] += bf16hi(v[j].w);
-      }
-    }
+    for (int j0 = 0; j0 < KMAX; j0 += CH) {
+      if (j0 < k) {  // warp-uniform
+        uint4 v[CH], r[CH];
 #pragma unroll
-    for (int j = 0; j < KMAX; ++j) {
-      if (j < k) {
-        const float d = dls[j];
-        acc[0] = fmaf(d, bf16lo(r[j].x), acc[0]); acc[1] = fmaf(d, bf16hi(r[j].x), acc[1]);
-        acc[2] = fmaf(d, bf16lo(r[j].y), acc[2]); acc[3] = fmaf(d, bf16hi(r[j].y), acc[3]);
-        acc[4] = fmaf(d, bf16lo(r[j].z), acc[4]); acc[5] = fmaf(d, bf16hi(r[j].z), acc[5]);
-        acc[6] = fmaf(d, bf16lo(r[j].w), acc[6]); acc[7] = fmaf(d, bf16hi(r[j].w), acc[7]);
+        for (int jj = 0; jj < CH; ++jj) {
+          const int j = j0 + jj;
+          v[jj] = (j < k && rows[j] >= 0)
+                      ? __ldg(reinterpret_cast<const uint4*>(dx_slot + (size_t)rows[j] * H) + c)
+                      : make_uint4(0u, 0u, 0u, 0u);
+          r[jj] = (j < k && router_term)
+                      ? __ldg(reinterpret_cast<const uint4*>(w_router + (size_t)es[j] * H) + c)
+                      : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int jj = 0; jj < CH; ++jj) {
+          if (j0 + jj < k) {
+            acc[0] += bf16lo(v[jj].x); acc[1] += bf16hi(v[jj].x); acc[2] += bf16lo(v[jj].y);
+            acc[3] += bf16hi(v[jj].y); acc[4] += bf16lo(v[jj].z); acc[5] += bf16hi(v[jj].z);
+            acc[6] += bf16lo(v[jj].w); acc[7] += bf16hi(v[jj].w);
+          }
+        }
+#pragma unroll
+        for (int jj = 0; jj < CH; ++jj) {
+          if (j0 + jj < k) {
+            const float d = dls[j0 + jj];
+            acc[0] = fmaf(d, bf16lo(r[jj].x), acc[0]); acc[1] = fmaf(d, bf16hi(r[jj].x), acc[1]);
+            acc[2] = fmaf(d, bf16lo(r[jj].y), acc[2]); acc[3] = fmaf(d, bf16hi(r[jj].y), acc[3]);
+            acc[4] = fmaf(d, bf16lo(r[jj].z), acc[4]); acc[5] = fmaf(d, bf16hi(r[jj].z), acc[5]);
+            acc[6] = fmaf(d, bf16lo(r[jj].w), acc[6]); acc[7] = fmaf(d, bf16hi(r[jj].w), acc[7]);
+          }
+        }
       }
     }
     if (dx_shared) {

@@ -25,6 +25,8 @@ CASES = {
     "ragged_shared": W("ragged_shared", T=200, H=128, E=5, k=2, I=192, I_shared=320, bias_std=0.5),
     "balanced_small": W("balanced_small", T=512, H=256, E=16, k=4, I=256, gate=G.GATE_BALANCED),
     "skewed_mid": W("skewed_mid", T=1024, H=512, E=32, k=4, I=384, bias_std=1.5),
+    # k > 8: the per-token kernels' wide variants (up to 32 slots a token)
+    "wide_k": W("wide_k", T=256, H=256, E=32, k=12, I=192, bias_std=0.5),
 }
 
 
@@ -210,7 +212,7 @@ def test_backward_recompute_matches_saved(name):
     U.check_close(g1["grad_x"], b["grad_x"], "grad_x (recompute)")
 
 
-@pytest.mark.parametrize("name", ["ragged", "skewed_mid", "balanced_small", "ragged_shared"])
+@pytest.mark.parametrize("name", ["ragged", "skewed_mid", "balanced_small", "ragged_shared", "wide_k"])
 def test_aux_loss_forward_and_backward(name):
     """Auxiliary load-balancing loss: the probability sums, the loss and its
     coefficients against the oracle on the device's routing and fp32 logits;
@@ -281,7 +283,7 @@ def _run_layer(di, **kw):
 
 @pytest.mark.parametrize("name,factor", [("ragged", 0.6), ("skewed_mid", 1.0),
                                          ("ragged_shared", 0.8), ("balanced_small", 0.75),
-                                         ("tiny", None)])
+                                         ("tiny", None), ("wide_k", 0.7)])
 def test_capacity_forward_and_backward(name, factor):
     """Expert capacity (token dropping): the full sort and the kept/dropped
     split bit-exact (slot_perm -1 on dropped slots), out, the kept slots' rows

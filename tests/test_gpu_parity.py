@@ -127,7 +127,8 @@ def test_backward_matches_oracle(case):
         assert torch.count_nonzero(grads["grad_w_gate_up"][e]) == 0
 
 
-@pytest.mark.parametrize("T,E,k", [(1, 1, 1), (5, 7, 3), (3000, 128, 8), (700, 256, 6), (2049, 3, 2)])
+@pytest.mark.parametrize("T,E,k", [(1, 1, 1), (5, 7, 3), (3000, 128, 8), (700, 256, 6), (2049, 3, 2),
+                                   (8192, 128, 8), (9000, 64, 8), (40000, 256, 2)])
 def test_permute_random_ids(T, E, k):
     r = np.random.default_rng(T * 31 + E)
     idx = r.integers(0, E, size=(T, k)).astype(np.int32)
@@ -147,8 +148,9 @@ def test_permute_random_ids(T, E, k):
     assert M.moe_read_device_status(ws) == 0
 
 
-def test_out_of_range_expert_ids_are_reported_not_used():
-    T, E, k = 64, 8, 2
+@pytest.mark.parametrize("T,k", [(64, 2), (9000, 8)])   # one and many sort blocks
+def test_out_of_range_expert_ids_are_reported_not_used(T, k):
+    E = 8
     idx = np.random.default_rng(0).integers(0, E, size=(T, k)).astype(np.int32)
     idx[3, 1] = E
     idx[10, 0] = -1
@@ -159,6 +161,9 @@ def test_out_of_range_expert_ids_are_reported_not_used():
     inv = torch.empty(T * k, dtype=torch.int32, device="cuda")
     M.moe_permute(dims, torch.from_numpy(idx).cuda(), off, perm, inv, ws)
     assert M.moe_read_device_status(ws) == 5
+    good = (idx >= 0) & (idx < E)
+    counts = np.bincount(idx[good].ravel(), minlength=E)
+    assert np.array_equal(np.diff(off.cpu().numpy()), counts)
     assert int(off[-1]) == T * k - 2
     assert M.moe_read_device_status(ws) == 0   # cleared by the previous read
 

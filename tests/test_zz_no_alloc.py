@@ -42,7 +42,7 @@ def _both(T, E, k, seed):
 
 
 def test_static_scratch_sort_matches_workspace_sort_twice():
-    for (T, E, k, seed) in [(4096, 128, 8, 0), (300, 7, 3, 1)]:
+    for (T, E, k, seed) in [(4096, 128, 8, 0), (300, 7, 3, 1), (9000, 64, 8, 2)]:
         a, b = _both(T, E, k, seed)
         for x, y in zip(a, b):
             assert torch.equal(x, y)

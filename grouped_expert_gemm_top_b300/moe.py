@@ -294,8 +294,10 @@ class MoeLayer:
         self.workspace = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
 
     def forward(self, x, w_router, w_gate_up, w_down, router_bias=None, w_sh_gate_up=None,
-                w_sh_down=None, stream=None):
+                w_sh_down=None, stream=None, out=None):
+        """out: bf16 [T, H] to write the layer output into (default: self.out)."""
         d, ws = self.dims, self.workspace
+        out = self.out if out is None else out
         moe_route(d, self.gate_mode, x, w_router, router_bias, self.logits, self.topk_idx,
                   self.topk_w, ws, stream, prob_sum=self.prob_sum)
         moe_permute(d, self.topk_idx, self.expert_offsets, self.perm_slot, self.slot_perm, ws, stream)
@@ -305,9 +307,8 @@ class MoeLayer:
         moe_grouped_mlp_fwd(d, x, self.expert_offsets, self.perm_slot, w_gate_up, w_down,
                             self.gu_saved, self.y_perm, w_sh_gate_up, w_sh_down, self.sh_gu_saved,
                             self.y_shared, ws, stream)
-        moe_unpermute_combine(d, self.y_perm, self.slot_perm, self.topk_w, self.y_shared, self.out,
-                              stream)
-        return self.out
+        moe_unpermute_combine(d, self.y_perm, self.slot_perm, self.topk_w, self.y_shared, out, stream)
+        return out
 
     def alloc_grads(self, with_bias=False):
         T, H, E, k, I, Is = self.dims.as_tuple()

@@ -1,0 +1,98 @@
+"""Host-fed layer steps with the host<->device copies overlapped.
+
+A forward+backward step whose inputs (x, grad_out) arrive from pinned host
+memory and whose results (out, grad_x) go back to it.  Two device slots hold
+each step's inputs and read-back results.  The host-to-device copies of step
+i+1 run on one stream and the device-to-host copies of step i-1 on another,
+while step i computes on the caller's stream, ordered by CUDA events:
+
+  * slot s's inputs are overwritten only after the step that last read them
+    (two steps earlier) has finished computing;
+  * a step writes its out/grad_x into slot s only after the read-back of the
+    step that last used the slot has finished.
+
+Every copy still happens once per step; only their overlap with compute
+changes.  This is stream plumbing: the copies are cudaMemcpyAsync (through
+torch), and every step of the layer runs in the library's kernels.
+"""
+
+from __future__ import annotations
+
+import torch
+
+
+class HostStepPipeline:
+    """Runs MoeLayer forward+backward steps fed from pinned host buffers.
+
+    layer: a MoeLayer built with_backward=True; grads: its alloc_grads()
+    dict (weight gradients stay on the device, overwritten every step);
+    weights: dict with w_router, w_gate_up, w_down and optionally
+    router_bias, w_sh_gate_up, w_sh_down (device tensors).
+    """
+
+    def __init__(self, layer, grads, weights, slots: int = 2):
+        self.layer, self.grads, self.w = layer, grads, weights
+        T, H = layer.out.shape
+        dev = layer.out.device
+        bf = torch.bfloat16
+        self.n = slots
+        self.x = [torch.empty(T, H, dtype=bf, device=dev) for _ in range(slots)]
+        self.go = [torch.empty(T, H, dtype=bf, device=dev) for _ in range(slots)]
+        self.out = [torch.empty(T, H, dtype=bf, device=dev) for _ in range(slots)]
+        self.gx = [torch.empty(T, H, dtype=bf, device=dev) for _ in range(slots)]
+        self.h2d = torch.cuda.Stream(device=dev)
+        self.d2h = torch.cuda.Stream(device=dev)
+        self.in_ready = [torch.cuda.Event() for _ in range(slots)]
+        self.computed = [torch.cuda.Event() for _ in range(slots)]
+        self.read_back = [torch.cuda.Event() for _ in range(slots)]
+        self.used = [False] * slots
+        self.i = 0
+
+    def step(self, x_host, go_host, out_host, gx_host):
+        """Enqueue one step: x_host, go_host in; out_host, gx_host written back.
+
+        Asynchronous: out_host/gx_host are valid after drain() (or a device
+        synchronize); a host buffer handed to a later step is not read
+        before this step's copies have been issued."""
+        s = self.i % self.n
+        compute = torch.cuda.current_stream(self.x[s].device)
+        with torch.cuda.stream(self.h2d):
+            if self.used[s]:
+                self.h2d.wait_event(self.computed[s])   # the step that last read slot s
+            self.x[s].copy_(x_host, non_blocking=True)
+            self.go[s].copy_(go_host, non_blocking=True)
+            self.in_ready[s].record(self.h2d)
+        compute.wait_event(self.in_ready[s])
+        if self.used[s]:
+            compute.wait_event(self.read_back[s])       # slot s's results were read back
+        w = self.w
+        self.layer.forward(self.x[s], w["w_router"], w["w_gate_up"], w["w_down"],
+                           w.get("router_bias"), w.get("w_sh_gate_up"), w.get("w_sh_down"),
+                           out=self.out[s])
+        g = dict(self.grads)
+        g["grad_x"] = self.gx[s]
+        self.layer.backward(self.go[s], self.x[s], w["w_router"], w["w_gate_up"], w["w_down"], g,
+                            w.get("w_sh_gate_up"), w.get("w_sh_down"))
+        self.computed[s].record(compute)
+        with torch.cuda.stream(self.d2h):
+            self.d2h.wait_event(self.computed[s])
+            out_host.copy_(self.out[s], non_blocking=True)
+            gx_host.copy_(self.gx[s], non_blocking=True)
+            self.read_back[s].record(self.d2h)
+        self.used[s] = True
+        self.i += 1
+
+    def drain(self):
+        """Make the caller's stream wait for every copy issued so far."""
+        compute = torch.cuda.current_stream(self.x[0].device)
+        for s in range(self.n):
+            if self.used[s]:
+                compute.wait_event(self.read_back[s])
+
+    @property
+    def h2d_bytes_per_step(self) -> int:
+        return (self.x[0].numel() + self.go[0].numel()) * 2
+
+    @property
+    def d2h_bytes_per_step(self) -> int:
+        return (self.out[0].numel() + self.gx[0].numel()) * 2

@@ -1,0 +1,62 @@
+"""The host-fed step pipeline against plain steps.
+
+Copies overlapped with compute must not change a bit of any step's results:
+three steps with different host inputs through the pipeline give the same
+out and grad_x per step, and the same weight gradients after the last step,
+as the same steps run one after the other on one stream.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import gpu_util as U
+from grouped_expert_gemm_top_b300 import inputs as G
+from grouped_expert_gemm_top_b300 import moe as M
+from grouped_expert_gemm_top_b300.pipeline import HostStepPipeline
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("shared", [False, True])
+def test_pipelined_steps_match_plain_steps(shared):
+    w = G.Workload("pipe", T=320, H=256, E=8, k=2, I=192, I_shared=128 if shared else 0, bias_std=0.5)
+    di = U.DeviceInputs(w, seed=5, with_grad=True)
+    weights = dict(w_router=di.w_router, w_gate_up=di.w_gate_up, w_down=di.w_down,
+                   router_bias=di.router_bias, w_sh_gate_up=di.w_sh_gate_up, w_sh_down=di.w_sh_down)
+    r = np.random.default_rng(9)
+    steps = []
+    for _ in range(3):
+        x = torch.from_numpy(r.normal(size=(w.T, w.H)).astype(np.float32)).to(torch.bfloat16)
+        go = torch.from_numpy(r.normal(size=(w.T, w.H)).astype(np.float32)).to(torch.bfloat16)
+        steps.append((x.pin_memory(), go.pin_memory()))
+
+    # plain: copy in, compute, copy out, one stream
+    plain = M.MoeLayer(di.dims, gate_mode=w.gate, with_backward=True)
+    pg = plain.alloc_grads(with_bias=True)
+    ref = []
+    for xh, goh in steps:
+        x, go = xh.cuda(), goh.cuda()
+        plain.forward(x, di.w_router, di.w_gate_up, di.w_down, di.router_bias, di.w_sh_gate_up,
+                      di.w_sh_down)
+        plain.backward(go, x, di.w_router, di.w_gate_up, di.w_down, pg, di.w_sh_gate_up, di.w_sh_down)
+        ref.append((plain.out.cpu(), pg["grad_x"].cpu()))
+    torch.cuda.synchronize()
+
+    layer = M.MoeLayer(di.dims, gate_mode=w.gate, with_backward=True)
+    grads = layer.alloc_grads(with_bias=True)
+    pipe = HostStepPipeline(layer, grads, weights)
+    outs = [(torch.empty(w.T, w.H, dtype=torch.bfloat16).pin_memory(),
+             torch.empty(w.T, w.H, dtype=torch.bfloat16).pin_memory()) for _ in steps]
+    for (xh, goh), (oh, gh) in zip(steps, outs):
+        pipe.step(xh, goh, oh, gh)
+    pipe.drain()
+    torch.cuda.synchronize()
+    assert M.moe_read_device_status(layer.workspace) == 0
+    for (o_ref, g_ref), (oh, gh) in zip(ref, outs):
+        assert torch.equal(oh, o_ref)
+        assert torch.equal(gh, g_ref)
+    for key, v in pg.items():
+        if v is not None and key != "grad_x":
+            assert torch.equal(grads[key], v), key
+    assert pipe.h2d_bytes_per_step == 2 * w.T * w.H * 2

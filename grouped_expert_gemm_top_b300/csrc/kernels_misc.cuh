@@ -29,12 +29,9 @@ constexpr int kPadRows = 128;      // per-expert row padding of the backward lay
 constexpr int kRouterMaxPerLane = 8;  // E <= 256
 constexpr int kMaxSplitsRouter = 8;   // split-K slices of the router GEMM
 
-__device__ __forceinline__ bool topk_before(float va, int ia, float vb, int ib) {
-  return va > vb || (va == vb && ia < ib);
-}
-
-// Order-preserving 32-bit key of a logit for the warp argmax: a larger value
-// gives a larger key and -0 ties with +0 (the order above); NaN (outside the
+// Order-preserving 32-bit key of a logit for the warp argmax (logit
+// descending; an equal key goes to the lower expert id): a larger value gives
+// a larger key and -0 ties with +0; NaN (outside the
 // contract: logits are finite) gets 1, below every number; 0 marks a slot
 // that is not a candidate (past E, or already taken).
 __device__ __forceinline__ uint32_t logit_key(float v) {

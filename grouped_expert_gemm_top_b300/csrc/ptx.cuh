@@ -121,13 +121,6 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
   return r;
 }
 
-// Arrive on an mbarrier given by its cluster shared-memory address (own or peer
-// CTA), ordering this thread's earlier writes at cluster scope.
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-               : "memory");
-}
-
 // Arrive on an mbarrier of the peer (or own) CTA by cluster address; orders
 // nothing beyond the CTA (tensor-memory hand-offs are ordered by tcgen05 fences).
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {

@@ -395,9 +395,18 @@ def run_ours(args, w, rank, world):
     counts = np.diff(layer.expert_offsets.cpu().numpy())
     P_pad = int(sum((int(c) + 127) // 128 * 128 for c in counts))
 
-    # ---- forward + backward (the headline), no per-kernel instrumentation
+    # ---- forward + backward (the headline): the step captured once as a CUDA
+    # graph and replayed (every kernel of the step runs each time; the graph
+    # only takes the host's launch calls out of the loop), no instrumentation
+    from grouped_expert_gemm_top_b300.pipeline import StepGraph
+    sg = StepGraph(layer, grads, dict(w_router=wr, w_gate_up=wgu, w_down=wd, router_bias=bias,
+                                      w_sh_gate_up=wsg, w_sh_down=wsd), x, go)
+    for _ in range(args.warmup):
+        sg.replay()
     with ClockSampler(local) as clocks:
-        ms_fb = timed(step, args.steps)
+        ms_fb = timed(sg.replay, args.steps)
+    # ---- the same step launched call by call (eager)
+    ms_fb_eager = timed(step, args.steps)
     # ---- the same steps again with every kernel bracketed by CUDA events on
     # its stream: per-kernel times and the dominant kernel's roofline
     M.moe_timing_enable(True)
@@ -405,11 +414,15 @@ def run_ours(args, w, rank, world):
     ms_fb_inst = timed(step, args.steps)
     kstats = M.moe_kernel_stats(reset=True)
     M.moe_timing_enable(False)
-    # ---- forward only (inference: no saved pre-activations), uninstrumented
+    # ---- forward only (inference: no saved pre-activations), uninstrumented:
+    # a captured graph as for the headline, and call by call
+    fg = StepGraph(layer_inf, None, dict(w_router=wr, w_gate_up=wgu, w_down=wd, router_bias=bias,
+                                         w_sh_gate_up=wsg, w_sh_down=wsd), x)
     for _ in range(max(1, args.warmup // 2)):
-        fwd_inf()
-    ms_f = timed(fwd_inf, args.steps)
-    assert M.moe_read_device_status(layer.workspace) == 0, "device reported an error"
+        fg.replay()
+    ms_f = timed(fg.replay, args.steps)
+    ms_f_eager = timed(fwd_inf, args.steps)
+    assert M.moe_read_device_status(layer_inf.workspace) == 0, "device reported an error"
     # ---- the variants (activation recompute, auxiliary loss, expert
     # capacity), each timed in alternating blocks with the plain step so that
     # the GPU's drift over a run (it slows as it warms) cancels in the
@@ -428,6 +441,8 @@ def run_ours(args, w, rank, world):
     ms_aux, ms_aux_plain = paired(step_aux, layer_aux)
     ms_cap, ms_cap_plain = paired(step_cap, layer_cap)
     kept = int(np.minimum(np.diff(layer_cap.expert_offsets.cpu().numpy()), cap).sum())
+    # ---- graph replay against the eager step, in alternating blocks
+    ms_graph, ms_graph_plain = paired(sg.replay, layer)
     # ---- sustained: the plain step for ~3 s (the GPU's steady state under
     # its power limit), clocks sampled meanwhile
     n_sus = max(args.steps, int(args.sustain_s * 1e3 / (ms_fb / args.steps)))
@@ -549,6 +564,12 @@ def run_ours(args, w, rank, world):
                      "tokens_per_s": job_tokens_per_s(w.T, world, args.steps, ms_cap),
                      "ms_per_step": ms_cap / args.steps,
                      "plain_ms_per_step_adjacent": ms_cap_plain / args.steps},
+        # the headline step is a CUDA-graph replay; the same step launched call
+        # by call right after it, and the two in alternating blocks
+        "eager": {"tokens_per_s": job_tokens_per_s(w.T, world, args.steps, ms_fb_eager),
+                  "ms_per_step": ms_fb_eager / args.steps,
+                  "fwd_ms_per_step": ms_f_eager / args.steps,
+                  "graph_vs_eager_adjacent_ms": [ms_graph / args.steps, ms_graph_plain / args.steps]},
         # the plain step repeated for ~3 s: steady-state rate and clocks
         "sustained": None if ms_sus is None else {
             "steps": n_sus, "seconds": ms_sus / 1e3,

@@ -96,3 +96,42 @@ class HostStepPipeline:
     @property
     def d2h_bytes_per_step(self) -> int:
         return (self.out[0].numel() + self.gx[0].numel()) * 2
+
+
+class StepGraph:
+    """One forward+backward step of a MoeLayer captured as a CUDA graph.
+
+    The step reads its inputs from the caller's device buffers x and
+    grad_out (copy new data into them before each replay) and writes
+    layer.out and grads as the eager step does; with grad_out None (and
+    grads None) it is the forward alone.  replay() launches every
+    kernel of the step at once from the graph instead of one call at a time
+    from the host.  The library's calls are stream-ordered and never
+    synchronise, so they capture as they are; the eager warm-up steps before
+    the capture make every one-time host set-up happen outside it.
+    """
+
+    def __init__(self, layer, grads, weights, x, grad_out=None, warmup: int = 2):
+        self.layer, self.grads, self.w = layer, grads, weights
+        self.x, self.grad_out = x, grad_out
+        side = torch.cuda.Stream(device=x.device)
+        side.wait_stream(torch.cuda.current_stream(x.device))
+        with torch.cuda.stream(side):
+            for _ in range(warmup):
+                self._step()
+        torch.cuda.current_stream(x.device).wait_stream(side)
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            self._step()
+
+    def _step(self):
+        w = self.w
+        self.layer.forward(self.x, w["w_router"], w["w_gate_up"], w["w_down"], w.get("router_bias"),
+                           w.get("w_sh_gate_up"), w.get("w_sh_down"))
+        if self.grad_out is None:
+            return
+        self.layer.backward(self.grad_out, self.x, w["w_router"], w["w_gate_up"], w["w_down"],
+                            self.grads, w.get("w_sh_gate_up"), w.get("w_sh_down"))
+
+    def replay(self):
+        self.graph.replay()

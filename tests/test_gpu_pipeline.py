@@ -60,3 +60,57 @@ def test_pipelined_steps_match_plain_steps(shared):
         if v is not None and key != "grad_x":
             assert torch.equal(grads[key], v), key
     assert pipe.h2d_bytes_per_step == 2 * w.T * w.H * 2
+
+
+@pytest.mark.parametrize("shared", [False, True])
+def test_graph_replay_matches_eager_steps(shared):
+    """A captured step replayed on new inputs gives the eager step's bits."""
+    from grouped_expert_gemm_top_b300.pipeline import StepGraph
+    w = G.Workload("graph", T=300, H=256, E=8, k=2, I=192, I_shared=128 if shared else 0, bias_std=0.5)
+    di = U.DeviceInputs(w, seed=6, with_grad=True)
+    weights = dict(w_router=di.w_router, w_gate_up=di.w_gate_up, w_down=di.w_down,
+                   router_bias=di.router_bias, w_sh_gate_up=di.w_sh_gate_up, w_sh_down=di.w_sh_down)
+    layer = M.MoeLayer(di.dims, gate_mode=w.gate, with_backward=True)
+    grads = layer.alloc_grads(with_bias=True)
+    x = torch.empty_like(di.x)
+    go = torch.empty_like(di.grad_out)
+    x.copy_(di.x)
+    go.copy_(di.grad_out)
+    g = StepGraph(layer, grads, weights, x, go)
+    eager = M.MoeLayer(di.dims, gate_mode=w.gate, with_backward=True)
+    eg = eager.alloc_grads(with_bias=True)
+    r = np.random.default_rng(2)
+    for _ in range(2):
+        xn = torch.from_numpy(r.normal(size=(w.T, w.H)).astype(np.float32)).to(torch.bfloat16).cuda()
+        gn = torch.from_numpy(r.normal(size=(w.T, w.H)).astype(np.float32)).to(torch.bfloat16).cuda()
+        x.copy_(xn)
+        go.copy_(gn)
+        g.replay()
+        eager.forward(xn, di.w_router, di.w_gate_up, di.w_down, di.router_bias, di.w_sh_gate_up,
+                      di.w_sh_down)
+        eager.backward(gn, xn, di.w_router, di.w_gate_up, di.w_down, eg, di.w_sh_gate_up, di.w_sh_down)
+        torch.cuda.synchronize()
+        assert M.moe_read_device_status(layer.workspace) == 0
+        assert torch.equal(layer.out, eager.out)
+        for key, v in eg.items():
+            if v is not None:
+                assert torch.equal(grads[key], v), key
+
+
+def test_forward_only_graph_matches_eager_forward():
+    from grouped_expert_gemm_top_b300.pipeline import StepGraph
+    w = G.Workload("graph_fwd", T=300, H=256, E=8, k=2, I=192, bias_std=0.5)
+    di = U.DeviceInputs(w, seed=8, with_grad=False)
+    weights = dict(w_router=di.w_router, w_gate_up=di.w_gate_up, w_down=di.w_down,
+                   router_bias=di.router_bias)
+    layer = M.MoeLayer(di.dims, gate_mode=w.gate, with_backward=False)
+    x = di.x.clone()
+    g = StepGraph(layer, None, weights, x)
+    eager = M.MoeLayer(di.dims, gate_mode=w.gate, with_backward=False)
+    xn = (di.x.float() * -1.5).to(torch.bfloat16)
+    x.copy_(xn)
+    g.replay()
+    eager.forward(xn, di.w_router, di.w_gate_up, di.w_down, di.router_bias)
+    torch.cuda.synchronize()
+    assert torch.equal(layer.out, eager.out)
+    assert torch.equal(layer.topk_idx, eager.topk_idx)

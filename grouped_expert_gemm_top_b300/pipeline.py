@@ -27,17 +27,20 @@ class HostStepPipeline:
     layer: a MoeLayer built with_backward=True; grads: its alloc_grads()
     dict (weight gradients stay on the device, overwritten every step);
     weights: dict with w_router, w_gate_up, w_down and optionally
-    router_bias, w_sh_gate_up, w_sh_down (device tensors).
+    router_bias, w_sh_gate_up, w_sh_down (device tensors).  use_graph: run
+    each slot's step as a captured CUDA graph (one per slot, captured here
+    after an eager warm-up step) instead of call by call.
     """
 
-    def __init__(self, layer, grads, weights, slots: int = 2):
+    def __init__(self, layer, grads, weights, slots: int = 2, use_graph: bool = True):
         self.layer, self.grads, self.w = layer, grads, weights
         T, H = layer.out.shape
         dev = layer.out.device
         bf = torch.bfloat16
         self.n = slots
-        self.x = [torch.empty(T, H, dtype=bf, device=dev) for _ in range(slots)]
-        self.go = [torch.empty(T, H, dtype=bf, device=dev) for _ in range(slots)]
+        # zeroed: the graph capture's warm-up step reads them before any data
+        self.x = [torch.zeros(T, H, dtype=bf, device=dev) for _ in range(slots)]
+        self.go = [torch.zeros(T, H, dtype=bf, device=dev) for _ in range(slots)]
         self.out = [torch.empty(T, H, dtype=bf, device=dev) for _ in range(slots)]
         self.gx = [torch.empty(T, H, dtype=bf, device=dev) for _ in range(slots)]
         self.h2d = torch.cuda.Stream(device=dev)
@@ -47,6 +50,30 @@ class HostStepPipeline:
         self.read_back = [torch.cuda.Event() for _ in range(slots)]
         self.used = [False] * slots
         self.i = 0
+        self.graphs = None
+        if use_graph:
+            side = torch.cuda.Stream(device=dev)
+            side.wait_stream(torch.cuda.current_stream(dev))
+            with torch.cuda.stream(side):
+                for s in range(slots):
+                    self._compute(s)
+            torch.cuda.current_stream(dev).wait_stream(side)
+            self.graphs = []
+            for s in range(slots):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    self._compute(s)
+                self.graphs.append(g)
+
+    def _compute(self, s):
+        w = self.w
+        self.layer.forward(self.x[s], w["w_router"], w["w_gate_up"], w["w_down"],
+                           w.get("router_bias"), w.get("w_sh_gate_up"), w.get("w_sh_down"),
+                           out=self.out[s])
+        g = dict(self.grads)
+        g["grad_x"] = self.gx[s]
+        self.layer.backward(self.go[s], self.x[s], w["w_router"], w["w_gate_up"], w["w_down"], g,
+                            w.get("w_sh_gate_up"), w.get("w_sh_down"))
 
     def step(self, x_host, go_host, out_host, gx_host):
         """Enqueue one step: x_host, go_host in; out_host, gx_host written back.
@@ -65,14 +92,10 @@ class HostStepPipeline:
         compute.wait_event(self.in_ready[s])
         if self.used[s]:
             compute.wait_event(self.read_back[s])       # slot s's results were read back
-        w = self.w
-        self.layer.forward(self.x[s], w["w_router"], w["w_gate_up"], w["w_down"],
-                           w.get("router_bias"), w.get("w_sh_gate_up"), w.get("w_sh_down"),
-                           out=self.out[s])
-        g = dict(self.grads)
-        g["grad_x"] = self.gx[s]
-        self.layer.backward(self.go[s], self.x[s], w["w_router"], w["w_gate_up"], w["w_down"], g,
-                            w.get("w_sh_gate_up"), w.get("w_sh_down"))
+        if self.graphs is not None:
+            self.graphs[s].replay()
+        else:
+            self._compute(s)
         self.computed[s].record(compute)
         with torch.cuda.stream(self.d2h):
             self.d2h.wait_event(self.computed[s])

@@ -18,8 +18,8 @@ from grouped_expert_gemm_top_b300.pipeline import HostStepPipeline
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("shared", [False, True])
-def test_pipelined_steps_match_plain_steps(shared):
+@pytest.mark.parametrize("shared,use_graph", [(False, False), (False, True), (True, True)])
+def test_pipelined_steps_match_plain_steps(shared, use_graph):
     w = G.Workload("pipe", T=320, H=256, E=8, k=2, I=192, I_shared=128 if shared else 0, bias_std=0.5)
     di = U.DeviceInputs(w, seed=5, with_grad=True)
     weights = dict(w_router=di.w_router, w_gate_up=di.w_gate_up, w_down=di.w_down,
@@ -45,7 +45,7 @@ def test_pipelined_steps_match_plain_steps(shared):
 
     layer = M.MoeLayer(di.dims, gate_mode=w.gate, with_backward=True)
     grads = layer.alloc_grads(with_bias=True)
-    pipe = HostStepPipeline(layer, grads, weights)
+    pipe = HostStepPipeline(layer, grads, weights, use_graph=use_graph)
     outs = [(torch.empty(w.T, w.H, dtype=torch.bfloat16).pin_memory(),
              torch.empty(w.T, w.H, dtype=torch.bfloat16).pin_memory()) for _ in steps]
     for (xh, goh), (oh, gh) in zip(steps, outs):

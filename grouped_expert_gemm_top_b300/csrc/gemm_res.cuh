@@ -95,18 +95,22 @@ __device__ __forceinline__ int res_nmb(const GemmArgs& a) { return (a.M + BM - 1
 template <class C>
 __device__ __forceinline__ int res_nnb(const GemmArgs& a) { return (a.N + C::BN - 1) / C::BN; }
 
+// Unit t: tile_prefix runs over the groups in the order `order` (position ->
+// group id).
 template <class C>
-__device__ __forceinline__ ResUnit res_unit(const GemmArgs& a, const SmemTables& T, int t) {
+__device__ __forceinline__ ResUnit res_unit(const GemmArgs& a, const SmemTables& T,
+                                            const int* order, int t) {
   int lo = 0, hi = a.G - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
     if (T.tile_prefix[mid] <= t) lo = mid; else hi = mid - 1;
   }
   ResUnit u;
-  u.g = lo;
+  const int g = order[lo];
+  u.g = g;
   const int local = t - T.tile_prefix[lo];
   const int mu = (res_nmb<C>(a) + 1) / 2;
-  u.stream = T.cnt[lo] > C::KRES;
+  u.stream = T.cnt[g] > C::KRES;
   if (u.stream) {  // one tile; m-block pairs fastest
     u.ntiles = 1;
     u.p = local % mu;
@@ -116,9 +120,56 @@ __device__ __forceinline__ ResUnit res_unit(const GemmArgs& a, const SmemTables&
     u.p = local;
     u.nb = local;
   }
-  u.kstart = T.start[lo];
-  u.kblocks = (T.cnt[lo] + BK - 1) / BK;
+  u.kstart = T.start[g];
+  u.kblocks = (T.cnt[g] + BK - 1) / BK;
   return u;
+}
+
+// Unit order.  Units are dealt to the CTA pairs round-robin.  When some group
+// has more rows than the resident slots hold, its units are single tiles whose
+// length grows with its rows, so the groups are taken in descending row count
+// (ties: lower id): the longest units start first, on different pairs.
+// Otherwise the order is the group ids' (tile_prefix as built).  One warp.
+template <class C, class UnitsFn>
+__device__ void res_order_groups(const GemmArgs& a, SmemTables& T, int* order, int lane,
+                                 UnitsFn units) {
+  int mx = 0;
+  for (int g = lane; g < a.G; g += 32) mx = max(mx, T.cnt[g]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if (mx <= C::KRES) {
+    for (int g = lane; g < a.G; g += 32) order[g] = g;
+    __syncwarp();
+    return;
+  }
+  for (int g = lane; g < a.G; g += 32) {
+    const int c = T.cnt[g];
+    int r = 0;
+    for (int h = 0; h < a.G; ++h) {
+      const int ch = T.cnt[h];
+      r += (ch > c) || (ch == c && h < g);
+    }
+    order[r] = g;
+  }
+  __syncwarp();
+  int run = 0;
+  for (int b0 = 0; b0 < a.G; b0 += 32) {
+    const int i = b0 + lane;
+    const int u = i < a.G ? units(T.cnt[order[i]]) : 0;
+    int inc = u;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int x = __shfl_up_sync(0xffffffffu, inc, d);
+      if (lane >= d) inc += x;
+    }
+    if (i < a.G) T.tile_prefix[i] = run + inc - u;
+    run += __shfl_sync(0xffffffffu, inc, 31);
+  }
+  if (lane == 0) {
+    T.tile_prefix[a.G] = run;
+    T.total_tiles = run;
+  }
+  __syncwarp();
 }
 
 template <class C>
@@ -182,6 +233,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   __shared__ __align__(8) uint64_t tempty_bar[2];
   __shared__ __align__(8) uint64_t drain_bar;
   __shared__ SmemTables T;
+  __shared__ int order[kMaxGroups];  // unit order: position -> group
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -215,11 +267,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   }
   if (warp == 2) {
     const int nMB = res_nmb<C>(a), nNB = res_nnb<C>(a);
-    build_group_tables(a, T, lane, [&](int cnt) {
+    const auto units = [&](int cnt) {
       const int mu = (nMB + 1) / 2;
       if (cnt > C::KRES) return mu * nNB;  // one unit per streamed tile
       return C::RES == RES_A ? mu : nNB;
-    });
+    };
+    build_group_tables(a, T, lane, units);
+    res_order_groups<C>(a, T, order, lane, units);
   }
   __syncthreads();
   if (T.total_tiles == 0) return;  // no work: leave before touching tensor memory or the peer
@@ -243,7 +297,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     uint32_t phase = 0;
     uint32_t filled = 0, fill_parity = 0;
     for (int t = unit0; t < total && !*abort_flag && !C::STREAM_GATHER; t += ustep) {
-      const ResUnit u = res_unit<C>(a, T, t);
+      const ResUnit u = res_unit<C>(a, T, order, t);
       bool ok = true;
       for (int j = 0; j < u.ntiles && ok; ++j) {
         const TileInfo ti = res_tile<C>(a, u, j, rank);
@@ -288,7 +342,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     uint32_t armed = 0;   // slots with a load issued (for the abort drain)
     uint32_t arm_par = 0;
     for (int t = unit0; t < total && !*abort_flag && !C::RES_GATHER; t += ustep) {
-      const ResUnit u = res_unit<C>(a, T, t);
+      const ResUnit u = res_unit<C>(a, T, order, t);
       bool ok = true;
       for (int kb = 0; kb < u.kblocks; ++kb) {
         const int sl = kb % C::RSLOTS;
@@ -328,7 +382,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     uint32_t rph = 0;  // per slot: parity of the next resident fill
     bool ok = true;
     for (int t = unit0; t < total && !*abort_flag && leader && ok; t += ustep) {
-      const ResUnit u = res_unit<C>(a, T, t);
+      const ResUnit u = res_unit<C>(a, T, order, t);
       for (int j = 0; j < u.ntiles && ok; ++j) {
         if (!mbar_wait(smem_u32(&tempty_bar[acc]), acc_phase ^ 1, abort_flag, a.status)) { ok = false; break; }
         tc_fence_after();
@@ -394,7 +448,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       int stage = 0;
       uint32_t phase = 0;
       for (int t = unit0; t < total && !*abort_flag && ok; t += ustep) {
-        const ResUnit u = res_unit<C>(a, T, t);
+        const ResUnit u = res_unit<C>(a, T, order, t);
         for (int j = 0; j < u.ntiles && ok; ++j) {
           const TileInfo ti = res_tile<C>(a, u, j, rank);
           for (int kb = 0; kb < u.kblocks; ++kb) {
@@ -434,7 +488,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       constexpr int LAG = 2;
       uint32_t rph = 0;
       for (int t = unit0; t < total && !*abort_flag && ok; t += ustep) {
-        const ResUnit u = res_unit<C>(a, T, t);
+        const ResUnit u = res_unit<C>(a, T, order, t);
         // A: the pair's m-block of this CTA; B: this CTA's half of the n-block
         const int x0 = C::A_GATHER ? (2 * u.p + rank) * BM : u.nb * C::BN + 128 * rank;
         for (int kb = 0; kb < u.kblocks; ++kb) {
@@ -481,7 +535,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     uint32_t acc_phase = 0;
     bool ok = true;
     for (int t = unit0; t < total && !*abort_flag && ok; t += ustep) {
-      const ResUnit u = res_unit<C>(a, T, t);
+      const ResUnit u = res_unit<C>(a, T, order, t);
       for (int j = 0; j < u.ntiles; ++j) {
         const TileInfo ti = res_tile<C>(a, u, j, rank);
         if (!mbar_wait(smem_u32(&tfull_bar[acc]), acc_phase, abort_flag, a.status)) { ok = false; break; }

@@ -599,3 +599,29 @@ def test_mutation_capacity_ignored_in_backward_is_caught(monkeypatch):
         return orig(f2, *a, **kw)
     monkeypatch.setattr(O, "layer_backward", bad)
     assert _pins_fail(lambda: test_capacity_backward_matches_finite_differences(1))
+
+
+# ---------------------------------------------------------------- page facts
+def test_workloads_and_oracle_follow_the_pages_printed_facts():
+    """tests/golden/pages_facts.json: the Qwen3-shaped workloads have the
+    expert count the pages print; experts are fused 3-D tensors (the oracle
+    and the generator take W_gu [E, 2I, H], W_down [E, H, I]); sharding the
+    expert dimension 8 ways leaves each GPU 1/8 of the expert weights, as the
+    pages' 55 GiB -> 6.8 GiB states (to the pages' rounding)."""
+    import json
+    import os
+    facts = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "pages_facts.json")))["facts"]
+    E = facts["qwen3_moe_experts"]["value"]
+    for name in ("qwen3_30b_a3b_balanced", "qwen3_30b_a3b_skewed", "qwen3_30b_a3b_balanced_fwd_bwd"):
+        assert G.WORKLOADS[name].E == E
+    w = G.WORKLOADS["tiny"]
+    inp = G.make_inputs(w, 0, with_grad=False)
+    assert facts["experts_as_fused_3d_tensors"]["value"]
+    assert inp["w_gate_up"].shape == (w.E, 2 * w.I, w.H) and inp["w_down"].shape == (w.E, w.H, w.I)
+    ep = facts["expert_parallel_size"]["value"]
+    mem = facts["expert_memory_per_gpu_at_ep8"]["value"]
+    assert abs(mem["total_gib"] / ep - mem["per_gpu_gib"]) < 0.1
+    # the balanced gate at that expert count splits the slots exactly evenly
+    w = G.WORKLOADS["qwen3_30b_a3b_balanced"]
+    idx = O.balanced_topk(w.T, E, w.k)
+    assert np.array_equal(np.bincount(idx.ravel(), minlength=E), np.full(E, w.T * w.k // E))

@@ -449,7 +449,7 @@ def run_ours(args, w, rank, world):
     ms_sus, clocks_sus = None, None
     if args.sustain_s > 0:
         with ClockSampler(local) as clocks_sus:
-            ms_sus = timed(step, n_sus)
+            ms_sus = timed(sg.replay, n_sus)   # the headline's step, replayed for seconds
 
     # ---- end to end: pinned host inputs in, result out, every step
     xh = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)

@@ -330,3 +330,25 @@ def test_capacity_at_or_above_max_count_is_bit_identical(name):
     assert torch.equal(l1.out, l0.out)
     for key in g0:
         assert torch.equal(g1[key], g0[key]), key
+
+
+@pytest.mark.parametrize("name", ["ragged", "skewed_mid", "balanced_small", "ragged_shared", "wide_k"])
+def test_inference_forward_matches_training_forward(name):
+    """The forward without saved pre-activations (its gate/up GEMM stores h
+    only and runs its own configuration) gives the training forward's bits,
+    and so matches the oracle as that one does."""
+    w = CASES[name]
+    di = U.DeviceInputs(w, seed=11, with_grad=False)
+    outs = []
+    for with_backward in (True, False):
+        layer = M.MoeLayer(di.dims, gate_mode=w.gate, with_backward=with_backward)
+        layer.forward(di.x, di.w_router, di.w_gate_up, di.w_down, di.router_bias, di.w_sh_gate_up,
+                      di.w_sh_down)
+        torch.cuda.synchronize()
+        assert M.moe_read_device_status(layer.workspace) == 0
+        outs.append((layer.out.clone(), layer.y_perm.clone(), layer.topk_idx.clone()))
+    assert torch.equal(outs[0][2], outs[1][2])
+    assert torch.equal(outs[0][1], outs[1][1])
+    assert torch.equal(outs[0][0], outs[1][0])
+    f = U.oracle_forward(di, topk_idx=outs[1][2].cpu().numpy())
+    U.check_close(outs[1][0], f["out"], "out (inference)")

@@ -4,7 +4,7 @@ Each case runs forward+backward on the device and compares every output and
 gradient with the float64 oracle on the device's routing: one token; one
 expert (the layer is a dense SwiGLU MLP); every token to every expert (k = E);
 the smallest hidden and intermediate sizes; one expert receiving almost every
-token; and the optional features together (capacity with the auxiliary loss;
+token; 160000 token-slots; and the optional features together (capacity with the auxiliary loss;
 activation recompute with capacity and a shared expert).
 """
 
@@ -26,6 +26,8 @@ EDGE = {
     "k_equals_E": W("k_equals_E", T=150, H=128, E=4, k=4, I=128, bias_std=0.5),
     "smallest_dims": W("smallest_dims", T=130, H=64, E=3, k=2, I=64, bias_std=0.5),
     "one_hot_expert": W("one_hot_expert", T=600, H=128, E=8, k=2, I=128, bias_std=6.0),
+    # 160000 slots: the multi-block sort and row indices past 2^17 through the whole layer
+    "many_tokens": W("many_tokens", T=20000, H=128, E=64, k=8, I=128, bias_std=0.5),
 }
 
 

@@ -135,3 +135,28 @@ def test_expert_capacity_helper():
     assert M.expert_capacity(100, 1, 10, 1.1) == 11
     with pytest.raises(ValueError):
         M.expert_capacity(8, 1, 4, 0.0)
+
+
+def test_backward_argument_checks_before_launch(lib):
+    """The backward refuses, before launching anything: the auxiliary loss's
+    coefficients without the router logits, and recomputation (no saved g,u)
+    with a workspace sized for the saved-pre-activation backward."""
+    dims = (256, 256, 8, 2, 512, 0)
+    d = M.MoeDims.of(*dims)
+    saved = M.moe_workspace_size(dims, 1)
+    recompute = M.moe_workspace_size(dims, 2)
+    assert recompute > saved
+    ws = ctypes.create_string_buffer(recompute + 256)
+    p = (ctypes.addressof(ws) + 255) // 256 * 256
+
+    def bwd(gu_saved, router_logits, aux_coef, nbytes):
+        # grad_out, x, w_router, topk_idx, topk_w, offsets, perm_slot, slot_perm,
+        # w_gate_up, w_down, gu_saved, w_sh_gate_up, w_sh_down, sh_gu_saved, grad_x,
+        # grad_w_router, grad_router_bias, grad_w_gate_up, grad_w_down,
+        # grad_w_sh_gate_up, grad_w_sh_down, router_logits, aux_coef
+        a = [p] * 10 + [gu_saved, None, None, None, p, p, None, p, p, None, None,
+                        router_logits, aux_coef]
+        return lib.moe_layer_bwd(ctypes.byref(d), *a, p, nbytes, None)
+
+    assert bwd(p, None, p, recompute) == 1          # aux coefficients, no logits
+    assert bwd(None, None, None, saved) == 3        # recompute needs the larger workspace

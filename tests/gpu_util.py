@@ -51,6 +51,52 @@ def check_close(got, ref, name, rel_l2=REL_L2, frac=MAX_ABS_FRAC):
     return dict(rel_l2=rl2, max_abs=mabs)
 
 
+def oracle_backward_with_device_gu(di, f, gu_dev, x=None, grad_out=None, aux_coef=None):
+    """The oracle's backward from the device's own bf16 gate/up pre-activations.
+
+    The router bias gradient db[e] = sum_t dlogit[t, e] sums terms that nearly
+    cancel: dlogit_j = w_j (dw_j - sum_i w_i dw_i) cancels within a token and
+    the tokens' contributions cancel again per expert (db can be ~1/500 of
+    sum_t |dlogit[t, e]|).  The device forms dw = <grad_out W_down, h> from
+    its saved bf16 (g, u), so that one rounding of g and u moves db by up to
+    a few percent of itself while every other gradient stays far inside the
+    tolerance.  As with the routing (compared on the device's fp32 logits),
+    the device's (g, u) go in here and everything after them (h, y, dw, the
+    logit gradient and its sums) is the oracle's, in float64.
+
+    f: the oracle forward dict; gu_dev [S, 2I] (device tensor): the device's
+    saved (g, u) in f's sorted row order (rows of dropped slots, which the
+    device never writes, are ignored)."""
+    w = di.w
+    I = w.I
+    keep = f["keep"].ravel()[f["perm_slot"]]
+    kept = torch.from_numpy(keep).to(gu_dev.device)[:, None]
+    gu_dev = torch.where(kept, gu_dev, torch.zeros((), dtype=gu_dev.dtype, device=gu_dev.device))
+    gu_dev = gu_dev.double().cpu().numpy()
+    gu = f["gu_perm"].copy()
+    gu[keep] = gu_dev[keep]
+    wd = di.f64("w_down")
+    y = np.zeros_like(f["y_perm"])
+    off = f["expert_offsets"]
+    for e in range(w.E):
+        r0, r1 = int(off[e]), int(off[e + 1])
+        if r1 > r0:
+            y[r0:r1] = (O.silu(gu[r0:r1, :I]) * gu[r0:r1, I:]) @ wd[e].T
+    f2 = dict(f, gu_perm=gu, y_perm=y)
+    x = di.f64("x") if x is None else x
+    grad_out = di.f64("grad_out") if grad_out is None else grad_out
+    return O.layer_backward(f2, grad_out, x, di.f64("w_router"), di.f64("w_gate_up"), wd, w.k,
+                            w_sh_gu=di.f64("w_sh_gate_up"), w_sh_down=di.f64("w_sh_down"),
+                            aux_coef=aux_coef)
+
+
+def check_bias_grad(got, di, f, gu_dev, name="grad_router_bias", **kw):
+    """The router bias gradient at the common tolerance against the oracle's
+    backward from the device's own (g, u) (see oracle_backward_with_device_gu)."""
+    b = oracle_backward_with_device_gu(di, f, gu_dev, **kw)
+    return check_close(got, b["grad_router_bias"], name)
+
+
 class DeviceInputs:
     """Seeded inputs on the device (bf16 tensors) plus their float64 copies."""
 

@@ -44,7 +44,9 @@ def _run(w, seed=7, **layer_kw):
     return di, layer, grads
 
 
-def _check_all(di, layer, grads, capacity=None, aux_coef=None):
+def _check_all(di, layer, grads, capacity=None, aux_coef=None, gu_layer=None):
+    """Routing bit-exact, out and every gradient against the oracle.  gu_layer:
+    the layer whose saved (g, u) the bias check uses (default: this one)."""
     w = di.w
     idx = layer.topk_idx.cpu().numpy()
     off, perm, inv = O.permute(idx, w.E)
@@ -64,6 +66,9 @@ def _check_all(di, layer, grads, capacity=None, aux_coef=None):
         ref = b[key]
         if not np.any(ref):          # e.g. the router gradient of a one-expert layer
             assert torch.count_nonzero(got) == 0, key
+        elif key == "grad_router_bias":
+            gu = (gu_layer or layer).gu_saved
+            U.check_bias_grad(got, di, f, gu, aux_coef=aux_coef)
         else:
             U.check_close(got, ref, key)
     return f, b
@@ -100,9 +105,11 @@ def test_recompute_with_capacity_and_shared_expert():
     C = M.expert_capacity(w.T, w.k, w.E, 0.8)
     di, layer, grads = _run(w, capacity=C, recompute=True)
     assert layer.gu_saved is None
-    _check_all(di, layer, grads, capacity=C)
-    # and bit-identical to the saved-pre-activation backward with the same capacity
+    # the saved-pre-activation run with the same capacity gives the (g, u)
+    # that the recompute forms again
     _, layer2, grads2 = _run(w, capacity=C)
+    _check_all(di, layer, grads, capacity=C, gu_layer=layer2)
+    # and bit-identical to that run's backward
     for key, v in grads.items():
         if v is not None:
             assert torch.equal(v, grads2[key]), key

@@ -161,7 +161,14 @@ def test_shared_expert_shape_sampled():
     gx[tokens] = b["grad_x"]
     U.check_close(grads["grad_x"], gx, "grad_x (grad_out on sampled tokens)")
     for key in GRAD_KEYS[1:]:
-        _check_by_expert(grads[key], b[key], key + " (grad_out on sampled tokens)")
+        if key == "grad_router_bias":
+            sub_slots = f["perm_slot"].astype(np.int64)
+            dev_rows = layer.slot_perm.cpu().numpy()[tokens[sub_slots // w.k] * w.k + sub_slots % w.k]
+            U.check_bias_grad(grads[key], di, f, _rows(layer.gu_saved, dev_rows),
+                              name=key + " (grad_out on sampled tokens)",
+                              x=di.f64("x")[tokens], grad_out=di.f64("grad_out")[tokens])
+        else:
+            _check_by_expert(grads[key], b[key], key + " (grad_out on sampled tokens)")
     del grads, f, b, gx
 
     # the real grad_out: sampled tokens' grad_x, sampled experts' weight gradients

@@ -30,10 +30,12 @@ CASES = {
 }
 
 
-@pytest.fixture(scope="module", params=list(CASES))
+@pytest.fixture(scope="module", params=[(n, seed) for n in CASES for seed in (0, 1, 2)],
+                ids=lambda p: f"{p[0]}-seed{p[1]}")
 def case(request):
-    w = CASES[request.param]
-    di = U.DeviceInputs(w, seed=0, with_grad=True)
+    name, seed = request.param
+    w = CASES[name]
+    di = U.DeviceInputs(w, seed=seed, with_grad=True)
     layer = U.run_forward(di)
     assert M.moe_read_device_status(layer.workspace) == 0
     return di, layer
@@ -116,7 +118,7 @@ def test_backward_matches_oracle(case):
     U.check_close(grads["grad_x"], b["grad_x"], "grad_x")
     U.check_close(grads["grad_w_router"], b["grad_w_router"], "grad_w_router")
     if grads["grad_router_bias"] is not None:
-        U.check_close(grads["grad_router_bias"], b["grad_router_bias"], "grad_router_bias")
+        U.check_bias_grad(grads["grad_router_bias"], di, f, layer.gu_saved)
     if di.w.I_shared:
         U.check_close(grads["grad_w_sh_gate_up"], b["grad_w_sh_gate_up"], "grad_w_sh_gate_up")
         U.check_close(grads["grad_w_sh_down"], b["grad_w_sh_down"], "grad_w_sh_down")
@@ -259,7 +261,8 @@ def test_aux_loss_forward_and_backward(name):
     U.check_close(g["grad_w_router"], b["grad_w_router"], "grad_w_router (aux)")
     U.check_close(g["grad_x"], b["grad_x"], "grad_x (aux)")
     if "grad_router_bias" in g:
-        U.check_close(g["grad_router_bias"], b["grad_router_bias"], "grad_router_bias (aux)")
+        U.check_bias_grad(g["grad_router_bias"], di, f, layer.gu_saved,
+                          name="grad_router_bias (aux)", aux_coef=c_ref)
     for key in ("grad_w_gate_up", "grad_w_down", "grad_w_sh_gate_up", "grad_w_sh_down"):
         if key in g:
             assert torch.equal(g[key], g0[key]), key
@@ -314,7 +317,10 @@ def test_capacity_forward_and_backward(name, factor):
                          di.f64("w_gate_up"), di.f64("w_down"), w.k,
                          w_sh_gu=di.f64("w_sh_gate_up"), w_sh_down=di.f64("w_sh_down"))
     for key, got in g.items():
-        U.check_close(got, b[key], key + " (capacity)")
+        if key == "grad_router_bias":
+            U.check_bias_grad(got, di, f, layer.gu_saved, name=key + " (capacity)")
+        else:
+            U.check_close(got, b[key], key + " (capacity)")
 
 
 @pytest.mark.parametrize("name", ["ragged", "balanced_small"])

@@ -16,8 +16,12 @@
 //          A streamed.
 // An operand comes by TMA from a row-per-slot matrix, or is gathered by the
 // LSU warps straight from the token rows it is a copy of.
-// An expert with more rows gets one unit per output tile instead, and the four
-// resident slots become a 4-deep ring through which that operand streams.
+// An expert with more rows gets one unit per output tile instead, and the
+// resident slots become a ring through which that operand streams.
+// The slots form one ring across units (RSLOTS >= 4 k-blocks): with more slots
+// than a unit's four k-blocks, the next unit's first blocks land in slots the
+// running unit does not use, so they are fetched while it still computes
+// instead of after its last UMMA.
 //
 // CTA pairs as in the streaming kernel (cta_group::2, 256 x 256 tiles): each
 // CTA holds its own 128 rows of A and half of the B columns; the even CTA
@@ -27,8 +31,8 @@
 //   warps 2..    epilogue (the streaming kernel's bf16 store epilogue), 4, 8 or 16
 //   next 4      gather warps (a gathered operand only)
 //   last warp   resident-operand TMA loader (idle when it is gathered):
-//               refills k-block slot kb % 4 as soon as the last UMMA reading
-//               it has completed
+//               refills the next slot of the ring as soon as the last UMMA
+//               reading it has completed
 #pragma once
 #include "gemm.cuh"
 
@@ -36,7 +40,8 @@ namespace moe {
 
 enum ResMode : int { RES_A = 1, RES_B = 2 };
 
-template <int RES_, int AL_, int BL_, int STAGES_, int EPI_BUFS_, int EPI_WARPS_ = 4>
+template <int RES_, int AL_, int BL_, int STAGES_, int EPI_BUFS_, int EPI_WARPS_ = 4,
+          int RSLOTS_ = 4>
 struct ResCfg {
   static constexpr int RES = RES_;
   static constexpr int AL = AL_;  // MN_TILE or (streamed, RES_B) MN_GATHER
@@ -69,8 +74,11 @@ struct ResCfg {
   static constexpr int GATHER_LAG = STAGES - 2;
   static_assert(!GATHER || GATHER_LAG >= 1, "gathers need >= 3 stages");
   static constexpr int BLK = BM * BK * 2;  // one operand's 128 x 64 block of a CTA: 16 KB
-  static constexpr int RSLOTS = 4;         // resident k-blocks
-  static constexpr int KRES = RSLOTS * BK;  // experts with at most 256 rows stay resident
+  static constexpr int RSLOTS = RSLOTS_;   // resident-operand ring (k-block slots)
+  static constexpr int KRES = 4 * BK;      // experts with at most 256 rows stay resident
+  // a resident unit's k-blocks fit the ring; the gather signals a slot 2 fills
+  // later, so the ring must be deeper than that; slot ids fit 4 bits
+  static_assert(RSLOTS >= KRES / BK && RSLOTS <= 16, "resident ring depth");
   static constexpr uint32_t IDESC = idesc_bf16_f32(2 * BM, BN, true, true);
   // the even CTA's full barriers (streamed stages) and rfull barriers (resident
   // slots): both CTAs' TMA bytes, or one arrival per gather warp of both CTAs
@@ -341,11 +349,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     uint32_t rph = 0;     // per slot: parity bit of its uses so far
     uint32_t armed = 0;   // slots with a load issued (for the abort drain)
     uint32_t arm_par = 0;
+    int rbase = 0;        // ring slot of the unit's first k-block
     for (int t = unit0; t < total && !*abort_flag && !C::RES_GATHER; t += ustep) {
       const ResUnit u = res_unit<C>(a, T, order, t);
       bool ok = true;
       for (int kb = 0; kb < u.kblocks; ++kb) {
-        const int sl = kb % C::RSLOTS;
+        const int sl = (rbase + kb) % C::RSLOTS;
         if (!mbar_wait(smem_u32(&rempty_bar[sl]), ((rph >> sl) & 1u) ^ 1u, abort_flag, a.status)) { ok = false; break; }
         const uint32_t rb = smem_u32(&rfull_bar[sl]);
         const uint32_t slot = res_base + sl * C::BLK;
@@ -363,6 +372,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         rph ^= 1u << sl;
       }
       if (!ok) break;
+      rbase = (rbase + u.kblocks) % C::RSLOTS;
     }
     if (*abort_flag) {
       for (int s = 0; s < C::RSLOTS; ++s) {
@@ -380,6 +390,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     uint32_t rph = 0;  // per slot: parity of the next resident fill
+    int rbase = 0;     // ring slot of the unit's first k-block
     bool ok = true;
     for (int t = unit0; t < total && !*abort_flag && leader && ok; t += ustep) {
       const ResUnit u = res_unit<C>(a, T, order, t);
@@ -389,9 +400,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const uint32_t d_tmem = tmem_base + acc * C::BN;
         const bool last = j == u.ntiles - 1;
         for (int kb = 0; kb < u.kblocks; ++kb) {
-          // the resident operand's block kb: in slot kb % 4, filled once per
-          // unit (the first tile waits for it) or, streamed, once per k-block
-          const int sl = kb % C::RSLOTS;
+          // the resident operand's block kb: in ring slot rbase + kb, filled
+          // once per unit (the first tile waits for it) or, streamed, once per
+          // k-block
+          const int sl = (rbase + kb) % C::RSLOTS;
           if (j == 0) {
             if (!mbar_wait(smem_u32(&rfull_bar[sl]), (rph >> sl) & 1u, abort_flag, a.status)) { ok = false; break; }
             rph ^= 1u << sl;
@@ -425,6 +437,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         __syncwarp();
         if (++acc == 2) { acc = 0; acc_phase ^= 1; }
       }
+      rbase = (rbase + u.kblocks) % C::RSLOTS;
     }
     if (*abort_flag && leader) {
       if (lane == 0) {
@@ -481,18 +494,21 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         --rn;
       }
     } else {
-      // the resident operand, slot by slot.  Every slot of a unit is signalled
-      // before the next unit's first fill (which waits for this unit's last
-      // UMMA, and so for all of its slots); within a streamed unit a slot is
-      // signalled 2 slots later.
+      // the resident operand, slot by slot along the ring.  Every slot of a
+      // unit is signalled before the next unit's first fill; within a
+      // streamed unit a slot is signalled 2 slots later.  A fill waits for
+      // the last UMMA that read its slot: with a ring deeper than a unit, the
+      // next unit's first fills need none of the running unit's slots.
       constexpr int LAG = 2;
+      static_assert(C::RSLOTS > LAG, "a slot is signalled before its next fill");
       uint32_t rph = 0;
+      int rbase = 0;
       for (int t = unit0; t < total && !*abort_flag && ok; t += ustep) {
         const ResUnit u = res_unit<C>(a, T, order, t);
         // A: the pair's m-block of this CTA; B: this CTA's half of the n-block
         const int x0 = C::A_GATHER ? (2 * u.p + rank) * BM : u.nb * C::BN + 128 * rank;
         for (int kb = 0; kb < u.kblocks; ++kb) {
-          const int sl = kb % C::RSLOTS;
+          const int sl = (rbase + kb) % C::RSLOTS;
           const int kid = gather_row(a, T, u.g, kb * BK + gw * 16 + (lane & 15));
           if (!mbar_wait(smem_u32(&rempty_bar[sl]), ((rph >> sl) & 1u) ^ 1u, abort_flag, a.status)) { ok = false; break; }
           rph ^= 1u << sl;
@@ -515,6 +531,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           ring >>= 4;
           --rn;
         }
+        rbase = (rbase + u.kblocks) % C::RSLOTS;
       }
     }
   } else if (warp >= 2 && warp < 2 + C::EPI_WARPS) {

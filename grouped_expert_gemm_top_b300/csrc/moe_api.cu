@@ -289,10 +289,12 @@ using CfgWgrad = PairCfg<4, MN_TILE, MN_TILE, RAGGED_K, EPI_STORE, false, false,
 //          [dg|du]^T streamed per m-block pair;
 // down: unit = (expert, 2 m-blocks of H), dout rows gathered once into the resident slots,
 //       w h streamed per n-block.
-// Their epilogue (a K = 256 tile's output is as large as its operands) is what
-// bounds them: 8 epilogue warps, 6 streamed stages, one staging buffer a warp.
-using CfgWgradRes = moe::ResCfg<moe::RES_B, MN_TILE, MN_GATHER, 6, 1, 8>;
-using CfgWgradDownRes = moe::ResCfg<moe::RES_A, MN_GATHER, MN_TILE, 6, 1, 8>;
+// Their epilogue (a K = 256 tile's output is as large as its operands) takes a
+// large share of each tile: 8 epilogue warps, one staging buffer a warp.  The
+// resident slots are a 6-deep ring (5 streamed stages): the next unit's first
+// two k-blocks are gathered while the running unit computes.
+using CfgWgradRes = moe::ResCfg<moe::RES_B, MN_TILE, MN_GATHER, 5, 1, 8, 6>;
+using CfgWgradDownRes = moe::ResCfg<moe::RES_A, MN_GATHER, MN_TILE, 5, 1, 8, 6>;
 
 // fp32 [depth][rows][inner] output map with 16x32 boxes (64-byte rows).
 bool make_out_map3_f32(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows,

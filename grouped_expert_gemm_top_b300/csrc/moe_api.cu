@@ -973,20 +973,60 @@ static __device__ __align__(256) int32_t g_sort_scratch[kStaticScratchInts];
 
 constexpr int kMaxScratchDevices = 64;
 std::mutex g_scratch_mu;
-int32_t* g_scratch_ptr[kMaxScratchDevices] = {};
+// Per device: the context the address was looked up in, and the address.  A
+// device reset (or a torn-down and re-created primary context) reloads the
+// module, so the array can move; the address is looked up again whenever the
+// current context is not the one it was taken in.
+struct ScratchSlot {
+  unsigned long long ctx_id;
+  int32_t* ptr;
+};
+ScratchSlot g_scratch_slot[kMaxScratchDevices] = {};
 
-// Device address of g_sort_scratch on the current device, looked up once per
-// device (in host code the symbol's name is only a stand-in, not an address).
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+// Unique id of the calling thread's current context (0: none, or the driver
+// could not be reached).
+unsigned long long current_context_id() {
+  static CtxGetCurrentFn get_cur = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_cur = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+  });
+  if (!get_cur || !get_id) return 0;
+  CUcontext c = nullptr;
+  unsigned long long id = 0;
+  if (get_cur(&c) != CUDA_SUCCESS || !c || get_id(c, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// Device address of g_sort_scratch on the current device (in host code the
+// symbol's name is only a stand-in, not an address).  Looked up once per
+// device and context: the first call on a device (or the first after a device
+// reset) performs the lookup.
 int32_t* static_scratch_for_current_device() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxScratchDevices) return nullptr;
   std::lock_guard<std::mutex> g(g_scratch_mu);
-  if (!g_scratch_ptr[dev]) {
+  ScratchSlot& slot = g_scratch_slot[dev];
+  const unsigned long long ctx = current_context_id();
+  if (!slot.ptr || ctx == 0 || ctx != slot.ctx_id) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_sort_scratch) != cudaSuccess || !p) return nullptr;
-    g_scratch_ptr[dev] = static_cast<int32_t*>(p);
+    slot.ptr = static_cast<int32_t*>(p);
+    slot.ctx_id = current_context_id();  // the lookup made the device's context current
   }
-  return g_scratch_ptr[dev];
+  return slot.ptr;
 }
 
 }  // namespace
@@ -1007,10 +1047,12 @@ extern "C" moe_status moe_permute_static_scratch(const moe_dims* d, const int32_
   // Nothing in the array needs clearing: pass 1 writes every (block, expert)
   // count that pass 2 reads.
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  { KernelScope ks(MOE_K_SORT_HISTOGRAM, st);
   moe::sort_histogram_kernel<<<(unsigned)blocks, moe::kSortThreads, 0, st>>>(
-      topk_idx, (int)S, d->E, counts, device_status);
+      topk_idx, (int)S, d->E, counts, device_status); }
+  { KernelScope ks(MOE_K_SORT_SCATTER, st);
   moe::sort_scatter_kernel<<<(unsigned)blocks, moe::kSortThreads, 0, st>>>(
       topk_idx, (int)S, d->E, (int)blocks, counts, expert_offsets, perm_slot, slot_perm,
-      d->capacity);
-  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+      d->capacity); }
+  return launched(cudaGetLastError());
 }

@@ -264,7 +264,12 @@ moe_status moe_read_device_status(void* workspace, size_t workspace_bytes, void*
  * The call allocates nothing (no cudaMalloc, cudaFree or allocating library
  * routine).  The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress) for that device; make that first call before any
- * stream capture.  Every call on a device shares the one array and it keeps
+ * stream capture.  The address is kept per device together with the id of
+ * the context it was taken in; after a device reset (or any re-created
+ * context) the next call sees a different context and looks the address up
+ * again, so make that call, too, outside a stream capture.  Both launches
+ * are counted by the kernel accounting below (sort_histogram, sort_scatter).
+ * Every call on a device shares the one array and it keeps
  * the last call's contents (nothing in it needs clearing: each call writes
  * every entry it reads); calls whose work overlaps on the GPU (different
  * streams, no ordering between them) race on it.

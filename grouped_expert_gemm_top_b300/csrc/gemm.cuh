@@ -8,7 +8,8 @@
 // matrix multiplication, with no copy of the expert parameters" step of the
 // grouped_mm expert backend (NeMo AutoModel blog, "专家后端 / Expert backends"
 // table): the expert weights are read in place from the fused [E, ...] 3-D
-// tensors, and the activations are read from their expert-sorted copy.
+// tensors, and the activations' token rows are gathered through the sort
+// inside the kernel (no expert-sorted copy of them is written).
 //
 // Roles (one CTA per SM, static round-robin over tiles):
 //   warp 0     TMA producer: fills a STAGES-deep ring of (A, B) k-blocks

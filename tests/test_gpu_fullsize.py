@@ -52,7 +52,9 @@ def _backward(di, layer, grad_out):
 
 
 def _check_routing(di, layer):
-    """Ids bit-exact against the oracle's selection on the device's fp32 logits; sort in full."""
+    """Ids bit-exact against the oracle's selection on the device's fp32 logits
+    (contract 1) and, for the softmax gate, equal to the selection on the
+    oracle's own logits except at near ties (contract 2); sort in full."""
     w = di.w
     idx = layer.topk_idx.cpu().numpy()
     balanced = w.gate == G.GATE_BALANCED
@@ -62,6 +64,9 @@ def _check_routing(di, layer):
     assert np.allclose(layer.topk_w.cpu().numpy(), w1, rtol=2e-6, atol=1e-7)
     if balanced:
         assert np.array_equal(idx, O.balanced_topk(w.T, w.E, w.k))
+    else:
+        # contract 2: against the oracle's own float64 logits, near ties only
+        U.check_routing_contract2(di, layer)
     off, perm, inv = O.permute(idx, w.E)
     assert np.array_equal(layer.expert_offsets.cpu().numpy(), off)
     assert np.array_equal(layer.perm_slot.cpu().numpy(), perm)

@@ -309,6 +309,72 @@ def config_of(w, args):
 
 
 # ----------------------------------------------------------------- GPU arm
+def time_other_shape(name, args, dev, peaks, timed):
+    """Forward (inference, no saved pre-activations) and, for a training
+    workload, forward+backward of another large workload, each a captured
+    CUDA graph replayed args.steps times, with the layer roofline from the
+    routing's actual per-expert histogram.  These shapes are not the headline
+    (which is the balanced Qwen3 step); they show ragged routing and the
+    shared expert."""
+    import numpy as np
+    import torch
+    from grouped_expert_gemm_top_b300 import inputs as G
+    from grouped_expert_gemm_top_b300 import moe as M
+    from grouped_expert_gemm_top_b300.pipeline import StepGraph
+
+    w = G.WORKLOADS[name]
+    inp = G.make_inputs(w, args.seed, with_grad=w.backward)
+
+    def up(b):
+        return torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).to(dev)
+
+    x, wr, wgu, wd = (up(inp[k]) for k in ("x", "w_router", "w_gate_up", "w_down"))
+    bias = None if inp["router_bias"] is None else torch.from_numpy(inp["router_bias"]).to(dev)
+    wsg = up(inp["w_sh_gate_up"]) if w.I_shared else None
+    wsd = up(inp["w_sh_down"]) if w.I_shared else None
+    weights = dict(w_router=wr, w_gate_up=wgu, w_down=wd, router_bias=bias, w_sh_gate_up=wsg,
+                   w_sh_down=wsd)
+    dims = (w.T, w.H, w.E, w.k, w.I, w.I_shared)
+    res = {"workload": name, "T": w.T, "H": w.H, "E": w.E, "k": w.k, "I": w.I,
+           "I_shared": w.I_shared, "gate": "balanced" if w.gate == 1 else "softmax_topk",
+           "router_bias_std": w.bias_std}
+    layer_inf = M.MoeLayer(dims, gate_mode=w.gate, device=dev, with_backward=False)
+    fg = StepGraph(layer_inf, None, weights, x)
+    for _ in range(args.warmup):
+        fg.replay()
+    ms_f = timed(fg.replay, args.steps)
+    assert M.moe_read_device_status(layer_inf.workspace) == 0, "device reported an error"
+    counts = np.diff(layer_inf.expert_offsets.cpu().numpy())
+    del fg, layer_inf
+    f_fwd, b_fwd, f_fb, b_fb = layer_model(w, counts)
+
+    def roof(f, b, ms):
+        t = ms / 1e3 / args.steps
+        t_roof = max(f / (peaks["bf16_tflops"] * 1e12), b / (peaks["hbm_gbs"] * 1e9))
+        return {"ms_per_step": ms / args.steps, "tokens_per_s": w.T / t, "t_roof_us": t_roof * 1e6,
+                "t_us": t * 1e6, "frac": t_roof / t, "flops": f, "bytes": b,
+                "bound": "tensor" if f / (peaks["bf16_tflops"] * 1e12) >= b / (peaks["hbm_gbs"] * 1e9)
+                else "hbm"}
+
+    res["active_experts"] = int((counts > 0).sum())
+    res["max_load_over_mean"] = float(counts.max() / counts.mean())
+    res["fwd"] = roof(f_fwd, b_fwd, ms_f)
+    if w.backward:
+        go = up(inp["grad_out"])
+        layer = M.MoeLayer(dims, gate_mode=w.gate, device=dev, with_backward=True)
+        grads = layer.alloc_grads(with_bias=bias is not None)
+        sg = StepGraph(layer, grads, weights, x, go)
+        for _ in range(args.warmup):
+            sg.replay()
+        ms_fb = timed(sg.replay, args.steps)
+        assert M.moe_read_device_status(layer.workspace) == 0, "device reported an error"
+        res["fwd_bwd"] = roof(f_fb, b_fb, ms_fb)
+        del sg, layer, grads
+    del x, wr, wgu, wd, bias, wsg, wsd, weights
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_ours(args, w, rank, world):
     import numpy as np
     import torch
@@ -487,11 +553,19 @@ def run_ours(args, w, rank, world):
     h2d = pipe.h2d_bytes_per_step
     d2h = pipe.d2h_bytes_per_step
 
+    # ---- the other large workloads: the skewed router (ragged expert tiles,
+    # forward) and the shared-expert shape (forward and forward+backward)
+    peaks, peak_src = load_peaks()
+    other = {}
+    if not args.no_other_shapes:
+        for name in ("qwen3_30b_a3b_skewed", "shared_expert_skewed"):
+            if name != w.name:
+                other[name] = time_other_shape(name, args, dev, peaks, timed)
+
     value = job_tokens_per_s(w.T, world, args.steps, ms_fb)
     fwd_value = job_tokens_per_s(w.T, world, args.steps, ms_f)
     e2e_value = job_tokens_per_s(w.T, world, args.steps, ms_e2e)
 
-    peaks, peak_src = load_peaks()
     f_fwd, b_fwd, f_fb, b_fb = layer_model(w, counts)
     t_roof_f = max(f_fwd / (peaks["bf16_tflops"] * 1e12), b_fwd / (peaks["hbm_gbs"] * 1e9))
     t_roof_fb = max(f_fb / (peaks["bf16_tflops"] * 1e12), b_fb / (peaks["hbm_gbs"] * 1e9))
@@ -583,6 +657,8 @@ def run_ours(args, w, rank, world):
             "peaks": peaks, "peak_source": peak_src},
         "roofline": roofline,
         "kernel_roofline_frac": per_kernel_roof,
+        # other workloads, each with its own layer roofline from its histogram
+        "other_shapes": other,
         "kernels": kernels,
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
@@ -609,6 +685,8 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=2048)
     ap.add_argument("--ref-tokens", type=int, default=256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-other-shapes", action="store_true",
+                    help="skip timing the skewed-router and shared-expert workloads")
     ap.add_argument("--sustain-s", type=float, default=3.0,
                     help="seconds of the extra steady-state pass (0: no such pass)")
     args = ap.parse_args()

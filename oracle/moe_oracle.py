@@ -58,9 +58,14 @@ design notes):
   assignment before dropping.  C = ceil(factor * T * k / E) for a capacity
   factor; C >= max count drops nothing.
 
+* expert parallelism (NeMo AutoModel blog, "专家并行与 DeepEP"; the pages give
+  no exchange layout): the readings are stated above ``ep_expert_ranges``.
+
 Parity status: every function below is pinned by a test in
 ``tests/test_oracle_pins.py`` (closed forms, invariants, brute force, library
-special cases, finite differences).
+special cases, finite differences) or, for the expert-parallel functions,
+``tests/test_ep_oracle.py`` (torch's chunking, brute-force counts, the global
+stable sort, equality with the one-rank layer).
 """
 
 from __future__ import annotations
@@ -342,6 +347,138 @@ def layer_forward(x, w_router, w_gu, w_down, k, balanced=False, bias=None,
     return dict(logits=logits, p=p, topk_idx=idx, topk_w=w, expert_offsets=offsets,
                 perm_slot=perm_slot, slot_perm=slot_perm, gu_perm=gu_perm, h_perm=h_perm,
                 y_perm=y_perm, y_shared=y_sh, gu_shared=gu_sh, out=out, keep=keep)
+
+
+# --------------------------------------------------------------------------
+# Expert parallelism: dispatch to the experts' ranks and combine back
+# --------------------------------------------------------------------------
+# NeMo AutoModel blog (zh-CN), "专家并行与 DeepEP": expert parallelism is its
+# own mesh dimension beside data parallelism; every rank trains on its own
+# data shard and holds 1/ep of the experts, the expert weights being split
+# along the expert dimension (DTensor Shard(0)).  DeepEP paragraphs: tokens are
+# dispatched to the ranks of their experts and the results combined back
+# (all-to-all).  The pages give no exchange layout; the readings here:
+# * rank r owns the experts Shard(0) gives it: chunks of ceil(E / n) in rank
+#   order (the last ranks may own fewer, or none);
+# * a source sends its slots in its expert-sorted order (permute), which is
+#   rank order because every rank's experts are contiguous; the rows for
+#   rank q are the block of q's experts;
+# * a receiver's buffer holds the sources' blocks in source order; its one
+#   grouped GEMM takes the rows expert by expert, within an expert source by
+#   source, within a source in the source's order;
+# * each output row goes back to its source in the order it came, so the
+#   source holds its rows' outputs in its own sorted order and combines them
+#   exactly as on one rank.
+
+
+def ep_expert_ranges(E: int, n_ranks: int) -> np.ndarray:
+    """int [n+1]: rank r owns experts bounds[r] .. bounds[r+1]-1 (Shard(0) chunks)."""
+    c = -(-E // n_ranks)
+    return np.minimum(np.arange(n_ranks + 1) * c, E)
+
+
+def ep_dispatch(topk_idx: np.ndarray, E: int, n_ranks: int):
+    """A source rank's dispatch plan from its own slots' expert ids.
+
+    Returns (expert_offsets, perm_slot, slot_perm, send_counts [n], expert_counts
+    [E]): the sort of permute; send_counts[q] = rows of the sorted order that go
+    to rank q (the block expert_offsets[bounds[q]] .. expert_offsets[bounds[q+1]]);
+    expert_counts[e] = the source's slots routed to e (what it tells the
+    receivers so that they can lay out their buffers).
+    """
+    offsets, perm_slot, slot_perm = permute(topk_idx, E)
+    b = ep_expert_ranges(E, n_ranks)
+    send_counts = np.array([int(offsets[b[q + 1]]) - int(offsets[b[q]]) for q in range(n_ranks)])
+    return offsets, perm_slot, slot_perm, send_counts, np.diff(offsets.astype(np.int64))
+
+
+def ep_receive(expert_counts_from, lo: int, hi: int):
+    """The receive layout of the rank owning experts lo .. hi-1.
+
+    expert_counts_from[s]: source s's expert counts [E].  The receive buffer
+    holds, source by source, that source's rows for experts lo .. hi-1 in
+    expert order.  Returns (local_offsets [E_loc+1], recv_perm [R]): grouped
+    row g (expert-major, then source, then the source's order) is receive row
+    recv_perm[g]; local expert e owns grouped rows local_offsets[e] ..
+    local_offsets[e+1]-1.
+    """
+    n = len(expert_counts_from)
+    E_loc = hi - lo
+    C = np.array([[int(expert_counts_from[s][lo + e]) for e in range(E_loc)] for s in range(n)],
+                 dtype=np.int64).reshape(n, E_loc)
+    seg = np.zeros((n, E_loc), dtype=np.int64)   # receive row where (source, expert) starts
+    pos = 0
+    for s in range(n):
+        for e in range(E_loc):
+            seg[s, e] = pos
+            pos += C[s, e]
+    local_offsets = np.zeros(E_loc + 1, dtype=np.int64)
+    recv_perm = np.empty(pos, dtype=np.int64)
+    g = 0
+    for e in range(E_loc):
+        local_offsets[e] = g
+        for s in range(n):
+            for i in range(C[s, e]):
+                recv_perm[g] = seg[s, e] + i
+                g += 1
+    local_offsets[E_loc] = g
+    return local_offsets.astype(np.int32), recv_perm.astype(np.int32)
+
+
+def ep_layer_forward(x_ranks, w_router, w_gu, w_down, k, balanced=False, bias=None,
+                     topk_idx_ranks=None):
+    """The layer over n ranks with expert parallelism, every step written out.
+
+    x_ranks[r]: rank r's tokens [T_r, H] (its data shard); the router is
+    replicated; rank q runs only the experts ep_expert_ranges gives it.
+    Steps: each rank routes its tokens (topk_idx_ranks overrides the
+    selection) and sorts its slots (ep_dispatch); it sends the token rows of
+    its sorted order, block q to rank q; rank q lays out what it received
+    (ep_receive), runs its experts on the grouped rows (one grouped GEMM per
+    projection), and sends every output row back to its source in the order
+    it came; each source combines its rows' outputs with its weights.
+    Returns a list of per-rank dicts: out, the plans, the receive layouts and
+    the exchanged buffers (for the tests).
+    """
+    n = len(x_ranks)
+    E = w_gu.shape[0]
+    b = ep_expert_ranges(E, n)
+    src = []
+    for r in range(n):
+        logits = router_logits(x_ranks[r], w_router, bias)
+        idx, w, p = route(logits, k, balanced=balanced)
+        if topk_idx_ranks is not None:
+            idx = np.asarray(topk_idx_ranks[r], dtype=np.int32)
+            w = renormalised_weights(p, idx)
+        off, perm, inv, send_counts, counts = ep_dispatch(idx, E, n)
+        x_send = x_ranks[r][perm.astype(np.int64) // k]
+        src.append(dict(topk_idx=idx, topk_w=w, expert_offsets=off, perm_slot=perm,
+                        slot_perm=inv, send_counts=send_counts, expert_counts=counts,
+                        x_send=x_send))
+    dst = []
+    for q in range(n):
+        blocks = [src[s]["x_send"][int(src[s]["expert_offsets"][b[q]]):
+                                   int(src[s]["expert_offsets"][b[q + 1]])] for s in range(n)]
+        x_recv = np.concatenate(blocks, axis=0)
+        loc_off, recv_perm = ep_receive([src[s]["expert_counts"] for s in range(n)], int(b[q]),
+                                        int(b[q + 1]))
+        y_grouped = experts_grouped(x_recv, loc_off, recv_perm, 1, w_gu[b[q]:b[q + 1]],
+                                    w_down[b[q]:b[q + 1]])[0]
+        y_recv = np.zeros_like(x_recv)
+        y_recv[recv_perm.astype(np.int64)] = y_grouped
+        recv_counts = [len(bl) for bl in blocks]
+        dst.append(dict(x_recv=x_recv, local_offsets=loc_off, recv_perm=recv_perm,
+                        y_recv=y_recv, recv_counts=recv_counts))
+    outs = []
+    for s in range(n):
+        back = []
+        for q in range(n):
+            start = int(sum(dst[q]["recv_counts"][:s]))
+            back.append(dst[q]["y_recv"][start:start + dst[q]["recv_counts"][s]])
+        y_sorted = np.concatenate(back, axis=0)
+        out = combine(y_sorted, src[s]["slot_perm"], src[s]["topk_w"])
+        outs.append(dict(src[s], y_sorted=y_sorted, out=out, **dst[s]))
+    return outs
 
 
 # --------------------------------------------------------------------------

@@ -69,7 +69,10 @@ struct GemmArgs {
   const __nv_bfloat16* gu_saved; const int32_t* perm_slot; const float* slot_w;
   __nv_bfloat16* dgu_out; __nv_bfloat16* hw_out; float* dw_part;
   int* status;
-  int out_evict_first;   // 1: stores carry the L2 evict-first policy (weight gradients)
+  // L2 hints (0 none, 1 evict-first, 2 evict-last): out_l2[i] for the stores
+  // through output map i, a_l2 for A's TMA tile loads (CTA-pair K-major A only)
+  int out_l2[2];
+  int a_l2;
 };
 
 template <int BN_, int STAGES_, int AL_, int BL_, int SCH_, int EPI_, bool B3D_, bool SWIGLU_B_,
@@ -289,8 +292,8 @@ struct WarpOut {
   int lane;
   int next;       // next buffer to use
   int inflight;   // committed stores not yet known to have read their buffer
-  bool evict_first;  // stores carry the L2 evict-first policy
-  uint64_t policy;
+  int hint[2];        // L2 hint code of the stores through output map 0 / 1
+  uint64_t policy[2];
 };
 
 // Take the next K staging buffers (the first is returned, the others follow at
@@ -310,16 +313,17 @@ __device__ __forceinline__ uint32_t stage_acquire(WarpOut<NB, BYTES>& w) {
   return buf;
 }
 
+// which: the output map (0 or 1) the store goes through (its L2 hint).
 template <int NB, int BYTES>
 __device__ __forceinline__ void stage_store(WarpOut<NB, BYTES>& w, uint32_t buf,
                                             const CUtensorMap* map, int x, int y, int z,
-                                            bool three_d) {
+                                            bool three_d, int which = 0) {
   fence_proxy_async_smem();
   __syncwarp();
   if (w.lane == 0) {
-    if (w.evict_first) {
-      if (three_d) tma_store_3d_hint(map, buf, x, y, z, w.policy);
-      else tma_store_2d_hint(map, buf, x, y, w.policy);
+    if (w.hint[which]) {
+      if (three_d) tma_store_3d_hint(map, buf, x, y, z, w.policy[which]);
+      else tma_store_2d_hint(map, buf, x, y, w.policy[which]);
     } else {
       if (three_d) tma_store_3d(map, buf, x, y, z);
       else tma_store_2d(map, buf, x, y);
@@ -474,7 +478,7 @@ __device__ void epilogue_swiglu(const GemmArgs& a, const TileInfo& ti, uint32_t 
         stage_store(w, bg, tmD0, j, y, 0, false);
         stage_store(w, bu, tmD0, I + j, y, 0, false);
       }
-      if (keep_h) stage_store(w, bh, tmD1, j, y, 0, false);
+      if (keep_h) stage_store(w, bh, tmD1, j, y, 0, false, 1);
     }
   }
 }
@@ -630,7 +634,7 @@ __device__ void epilogue_dgrad_swiglu(const GemmArgs& a, const SmemTables& T, co
     if (warp_full) {
       stage_store(w, bdg, tmD0, j, y, 0, false);
       stage_store(w, bdu, tmD0, I + j, y, 0, false);
-      stage_store(w, bhw, tmD1, j, y, 0, false);
+      stage_store(w, bhw, tmD1, j, y, 0, false, 1);
     }
   }
   if (a.dw_part && (valid || pad_row)) a.dw_part[p * npart_cols + ti.nb * nparts + cpart] = dwp;
@@ -868,6 +872,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     int stage = 0;
     uint32_t phase = 0;
     uint32_t filled = 0, fill_parity = 0;  // per stage: armed at least once, parity of last fill
+    const uint64_t a_policy = l2_policy(a.a_l2);
     for (int t = unit0; t < total && !*abort_flag; t += ustep) {
       const TileInfo ti = decode_tile<C>(a, T, t, rank);
       const int n0 = C::SWIGLU_B ? ti.nb * (C::BN / 2) : ti.nb * C::BN;
@@ -893,8 +898,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           // A comes from the gather warps
         } else if constexpr (C::AL == KMAJ_TILE) {
           if (lane == 0) {
-            if constexpr (C::PAIR) tma_load_2d_pair(sA, &tmA, fbp, kx, C::SCH == RAGGED_K ? m0 : ti.row0);
-            else tma_load_2d(sA, &tmA, fb, kx, C::SCH == RAGGED_K ? m0 : ti.row0);
+            if constexpr (C::PAIR) {
+              if (a.a_l2) tma_load_2d_pair_hint(sA, &tmA, fbp, kx, C::SCH == RAGGED_K ? m0 : ti.row0, a_policy);
+              else tma_load_2d_pair(sA, &tmA, fbp, kx, C::SCH == RAGGED_K ? m0 : ti.row0);
+            } else {
+              tma_load_2d(sA, &tmA, fb, kx, C::SCH == RAGGED_K ? m0 : ti.row0);
+            }
           }
         } else {  // MN_TILE: two 64-wide groups along M, 64 k-rows each
           if (lane == 0) {
@@ -1041,8 +1050,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     wo.lane = lane;
     wo.next = 0;
     wo.inflight = 0;
-    wo.evict_first = a.out_evict_first != 0;
-    wo.policy = wo.evict_first ? policy_evict_first() : 0;
+    wo.hint[0] = a.out_l2[0];
+    wo.hint[1] = a.out_l2[1];
+    wo.policy[0] = l2_policy(a.out_l2[0]);
+    wo.policy[1] = l2_policy(a.out_l2[1]);
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = unit0; t < total && !*abort_flag; t += ustep) {

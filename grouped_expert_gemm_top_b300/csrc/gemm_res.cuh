@@ -546,8 +546,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     wo.lane = lane;
     wo.next = 0;
     wo.inflight = 0;
-    wo.evict_first = a.out_evict_first != 0;
-    wo.policy = wo.evict_first ? policy_evict_first() : 0;
+    wo.hint[0] = a.out_l2[0];
+    wo.hint[1] = a.out_l2[1];
+    wo.policy[0] = l2_policy(a.out_l2[0]);
+    wo.policy[1] = l2_policy(a.out_l2[1]);
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;

@@ -1,7 +1,6 @@
-// Memory-bound kernels of the MoE layer: the router's softmax/top-k, the
-// expert sort (permutation and expert offsets), the weighted
-// un-permute/combine, and the backward's router gradient and token
-// gather-sums.
+// Memory-bound kernels of the MoE layer: the expert sort from given ids
+// (permutation and expert offsets), the weighted un-permute/combine, the
+// backward's router gradient and token gather-sums, and the auxiliary loss.
 //
 // All of them are written so that every output is a fixed-order function of
 // the inputs: no floating-point atomics, so results are bit-identical run to
@@ -19,15 +18,11 @@ constexpr int kSortPerLane = 4;                       // slots per lane
 constexpr int kSortChunk = kSortThreads * kSortPerLane;  // slots per block
 constexpr int kPadRows = 128;      // per-expert row padding of the backward layout
 
-// ---------------------------------------------------------------- router top-k
-// One warp per token.  logits[e] = sum of the split-K partial products (in
-// split order) + bias[e]; p = softmax over all E; the k experts are taken by k
-// rounds of a warp-wide argmax under the order (logit descending, expert id
-// ascending); w_j = p[e_j] / sum_j p[e_j].  The balanced gate takes
-// e_j = (t*k + j) mod E instead of the argmax rounds.  Reductions use a fixed
-// butterfly order, so results are bit-identical run to run.
+// ---------------------------------------------------------------- router top-k helpers
+// The router (route.cuh) takes the k experts of a token by k rounds of a
+// warp-wide argmax under the order (logit descending, expert id ascending),
+// each lane holding up to kRouterMaxPerLane experts (e = 32 i + lane).
 constexpr int kRouterMaxPerLane = 8;  // E <= 256
-constexpr int kMaxSplitsRouter = 8;   // split-K slices of the router GEMM
 
 // Order-preserving 32-bit key of a logit for the warp argmax (logit
 // descending; an equal key goes to the lower expert id): a larger value gives
@@ -44,154 +39,6 @@ __device__ __forceinline__ float key_logit(uint32_t key) {
 }
 
 constexpr int kMaxGroupsRouter = 256;  // E <= 256
-
-// This lane's experts' softmax probabilities p[t, e] (e = 32 i + lane) of
-// token t, from the split-K partial logits (summed in split order) + bias;
-// zero for t >= T or e >= E.
-__device__ __forceinline__ void router_token_probs(const float* __restrict__ partial, int splits,
-                                                   const float* __restrict__ bias, int t, int T,
-                                                   int E, int lane, float (&pl)[kRouterMaxPerLane]) {
-  float mx = -INFINITY;
-#pragma unroll
-  for (int i = 0; i < kRouterMaxPerLane; ++i) {
-    const int e = i * 32 + lane;
-    pl[i] = -INFINITY;
-    if (t < T && e < E) {
-      float l = 0.f;
-      for (int sp = 0; sp < splits; ++sp) l += __ldg(partial + ((size_t)sp * T + t) * E + e);
-      if (bias) l += __ldg(bias + e);
-      pl[i] = l;
-      mx = fmaxf(mx, l);
-    }
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  float z = 0.f;
-#pragma unroll
-  for (int i = 0; i < kRouterMaxPerLane; ++i) {
-    pl[i] = (i * 32 + lane < E && t < T) ? expf(pl[i] - mx) : 0.f;
-    z += pl[i];
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-#pragma unroll
-  for (int i = 0; i < kRouterMaxPerLane; ++i) pl[i] = t < T ? pl[i] / z : 0.f;
-}
-
-// psum_part (optional): per block (8 tokens), sum over its tokens of p[t, e]
-// for every expert (warp order), for the auxiliary load-balancing loss.
-constexpr int kTopkWarps = 8;  // tokens per block of the top-k kernel
-__global__ void router_topk_kernel(const float* __restrict__ partial, int splits,
-                                   const float* __restrict__ bias, float* __restrict__ logits_out,
-                                   int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
-                                   float* __restrict__ psum_part, int T, int E, int k,
-                                   int gate_mode) {
-  const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (psum_part) {
-    // block-wide sum of the tokens' softmax rows (the only block-level step)
-    __shared__ float prow[kTopkWarps][kMaxGroupsRouter];
-    float pl[kRouterMaxPerLane];
-    router_token_probs(partial, splits, bias, t, T, E, lane, pl);
-    const int wi = threadIdx.x >> 5;
-#pragma unroll
-    for (int i = 0; i < kRouterMaxPerLane; ++i)
-      if (i * 32 + lane < E) prow[wi][i * 32 + lane] = pl[i];
-    __syncthreads();
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
-      float acc = 0.f;
-#pragma unroll
-      for (int w = 0; w < kTopkWarps; ++w) acc += prow[w][e];
-      psum_part[(size_t)blockIdx.x * E + e] = acc;
-    }
-  }
-  if (t >= T) return;
-  float v[kRouterMaxPerLane];
-  float mx = -INFINITY;
-#pragma unroll
-  for (int i = 0; i < kRouterMaxPerLane; ++i) v[i] = -INFINITY;
-#pragma unroll
-  for (int i = 0; i < kRouterMaxPerLane; ++i) {
-    const int e = i * 32 + lane;
-    if (i * 32 < E && e < E) {  // the first test is warp-uniform
-      float part[kMaxSplitsRouter];
-#pragma unroll
-      for (int sp = 0; sp < kMaxSplitsRouter; ++sp)
-        part[sp] = sp < splits ? __ldg(partial + ((size_t)sp * T + t) * E + e) : 0.f;
-      float l = 0.f;
-#pragma unroll
-      for (int sp = 0; sp < kMaxSplitsRouter; ++sp)
-        if (sp < splits) l += part[sp];
-      if (bias) l += __ldg(bias + e);
-      v[i] = l;
-      mx = fmaxf(mx, l);
-      if (logits_out) logits_out[(size_t)t * E + e] = l;
-    }
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  float z = 0.f;
-#pragma unroll
-  for (int i = 0; i < kRouterMaxPerLane; ++i)
-    if (i * 32 < E && i * 32 + lane < E) z += expf(v[i] - mx);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-  // softmax gate: this lane's candidate keys and its best one (ties: lower slot)
-  uint32_t kl[kRouterMaxPerLane];
-  uint32_t lbk = 0u, taken = 0u;
-  int lbi = 0;
-#pragma unroll
-  for (int i = 0; i < kRouterMaxPerLane; ++i) {
-    kl[i] = (gate_mode != 1 && i * 32 + lane < E) ? logit_key(v[i]) : 0u;
-    if (kl[i] > lbk) { lbk = kl[i]; lbi = i; }
-  }
-  int my_e = 0;
-  float my_p = 0.f;
-  if (gate_mode == 1) {
-    // balanced gate: lane j's expert is (t k + j) mod E; it sums that expert's
-    // logit again, in the owner lane's order, so the value is the same bits
-    if (lane < k) {
-      my_e = (int)(((long long)t * k + lane) % E);
-      float part[kMaxSplitsRouter];
-#pragma unroll
-      for (int sp = 0; sp < kMaxSplitsRouter; ++sp)
-        part[sp] = sp < splits ? __ldg(partial + ((size_t)sp * T + t) * E + my_e) : 0.f;
-      float l = 0.f;
-#pragma unroll
-      for (int sp = 0; sp < kMaxSplitsRouter; ++sp)
-        if (sp < splits) l += part[sp];
-      if (bias) l += __ldg(bias + my_e);
-      my_p = expf(l - mx) / z;
-    }
-  } else {
-    for (int j = 0; j < k; ++j) {
-      // warp argmax in two single-instruction reductions: the largest key,
-      // then the lowest expert id holding it
-      const uint32_t kmax = __reduce_max_sync(0xffffffffu, lbk);
-      const int bi = (int)__reduce_min_sync(0xffffffffu,
-                                            lbk == kmax ? (uint32_t)(lbi * 32 + lane) : 0xffffffffu);
-      if ((bi & 31) == lane) {  // the owner drops it and finds its next best
-        taken |= 1u << (bi >> 5);
-        lbk = 0u;
-        lbi = 0;
-#pragma unroll
-        for (int i = 0; i < kRouterMaxPerLane; ++i)
-          if (!((taken >> i) & 1u) && kl[i] > lbk) { lbk = kl[i]; lbi = i; }
-      }
-      if (lane == j) {
-        my_e = bi;
-        my_p = expf(key_logit(kmax) - mx) / z;
-      }
-    }
-  }
-  float psum = lane < k ? my_p : 0.f;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) psum += __shfl_xor_sync(0xffffffffu, psum, o);
-  if (lane < k) {
-    topk_idx[(size_t)t * k + lane] = my_e;
-    topk_w[(size_t)t * k + lane] = my_p / psum;
-  }
-}
 
 // ---------------------------------------------------------------- expert sort
 // Pass 1: per-block expert histogram of the slots s = t*k + j.
@@ -341,13 +188,16 @@ __global__ void combine_kernel(const __nv_bfloat16* __restrict__ y_perm,
     rows[j] = __shfl_sync(0xffffffffu, row_l, j);
     ws[j] = __shfl_sync(0xffffffffu, w_l, j);
   }
+  // y_perm is read once: its lines become the first to leave L2
+  const uint64_t once = policy_evict_first();
   for (int c = lane; c < H / 8; c += 32) {
     uint4 v[KMAX];
 #pragma unroll
     for (int j = 0; j < KMAX; ++j)
       if (j < k)
         v[j] = rows[j] < 0 ? make_uint4(0u, 0u, 0u, 0u)
-                           : __ldg(reinterpret_cast<const uint4*>(y_perm + (size_t)rows[j] * H) + c);
+                           : ld_nc_v4_hint(reinterpret_cast<const uint4*>(y_perm + (size_t)rows[j] * H) + c,
+                                           once);
     uint4 vs = make_uint4(0, 0, 0, 0);
     if (y_shared) vs = __ldg(reinterpret_cast<const uint4*>(y_shared + (size_t)t * H) + c);
     float acc[8];

@@ -13,16 +13,18 @@
 #include <vector>
 
 #include "gemm.cuh"
+#include "ep.cuh"
 #include "gemm_res.cuh"
 #include "kernels_misc.cuh"
 #include "moe.h"
+#include "route.cuh"
 
 namespace {
 
 using moe::GemmArgs;
 using moe::GemmCfg;
 
-constexpr int32_t kAbiVersion = 10;
+constexpr int32_t kAbiVersion = 11;
 constexpr size_t kAlign = 256;
 
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
@@ -43,11 +45,10 @@ moe_status check_dims(const moe_dims* d) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-constexpr int kMaxRouterSplits = 8;
 constexpr int kDwParts = 1;  // column parts of the down data-gradient epilogue (epilogue warps / 4)
 
 struct Layout {
-  size_t status, counts, logits_part, psum_part, h, h_sh, fwd_end;
+  size_t status, counts, hist, psum_part, route_end, h, h_sh, fwd_end;
   size_t poff, dgu, hw, dxs, dwp, dl, dlb, rwp, db_part, dgu_sh, hw_sh, dxs_sh, gu_rc,
       sh_gu_rc, total;
   int sort_blocks;
@@ -86,8 +87,12 @@ Layout make_layout(const moe_dims& d, bool bwd, bool recompute = false) {
   size_t o = 0;
   L.status = o; o += kAlign;
   L.counts = o; o = align_up(o + (size_t)L.sort_blocks * d.E * 4);
-  L.logits_part = o; o = align_up(o + (size_t)kMaxRouterSplits * d.T * d.E * 4);
-  L.psum_part = o; o = align_up(o + (size_t)((d.T + moe::kTopkWarps - 1) / moe::kTopkWarps) * d.E * 4);
+  // the router's per-CTA expert counts [E][hist_ld] and probability sums [CTAs][E],
+  // sized for the largest cluster (every tile split over kRouteMaxSplits CTAs)
+  const size_t route_ctas_max = (size_t)((d.T + moe::kRouteBM - 1) / moe::kRouteBM) * moe::kRouteMaxSplits;
+  L.hist = o; o = align_up(o + (size_t)d.E * ((route_ctas_max + 3) / 4 * 4) * 4);
+  L.psum_part = o; o = align_up(o + route_ctas_max * d.E * 4);
+  L.route_end = o;
   L.h = o; o = align_up(o + (size_t)L.S * d.I * 2);
   L.h_sh = o; o = align_up(o + (size_t)d.T * d.I_shared * 2);
   L.fwd_end = o;
@@ -258,9 +263,6 @@ using moe::MN_TILE;
 using moe::RAGGED_K;
 using moe::RAGGED_M;
 
-template <int BN>
-using CfgRouter =
-    GemmCfg<BN, (BN >= 256 ? 4 : 6), KMAJ_TILE, KMAJ_TILE, RAGGED_K, EPI_STORE_F32, false, false>;
 // router weight gradient: A = DL [tokens, E] and B = x [tokens, H], both MN-major
 using CfgRouterW = GemmCfg<256, 4, MN_TILE, MN_TILE, RAGGED_K, EPI_STORE_F32, false, false>;
 // router term of grad_x with the auxiliary loss: DL [tokens, E] (K-major) x W_r [E, H] (MN-major)
@@ -388,6 +390,79 @@ long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
 
 moe_status launched(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
+// The router's cluster shape: one cluster per 128-token tile, split over as many
+// CTAs (K slices) as fill the SMs in about one wave, at most 8 and at most one
+// 64-deep k-block each.
+struct RouteSplit {
+  int ntiles, splits, ncta, hist_ld;
+};
+RouteSplit route_split(const moe_dims& d) {
+  RouteSplit r;
+  r.ntiles = (d.T + moe::kRouteBM - 1) / moe::kRouteBM;
+  r.splits = std::max(1, std::min(moe::kRouteMaxSplits, sm_count() / r.ntiles));
+  r.splits = std::min(r.splits, d.H / moe::BK);
+  r.ncta = r.ntiles * r.splits;
+  r.hist_ld = (r.ncta + 3) / 4 * 4;
+  return r;
+}
+
+template <int BN>
+moe_status launch_route_bn(const CUtensorMap& tX, const CUtensorMap& tW, const moe::RouteArgs& a,
+                           int ncta, cudaStream_t st) {
+  using C = moe::RouteCfg<BN>;
+  static std::atomic<uint64_t> configured{0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(configured.load() & bit)) {
+    if (cudaFuncSetAttribute(moe::route_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::SMEM_BYTES) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    configured.fetch_or(bit);
+  }
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)a.splits;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)ncta);
+  cfg.blockDim = dim3(moe::kRouteThreads);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  KernelScope ks(MOE_K_ROUTER, st);
+  if (cudaLaunchKernelEx(&cfg, moe::route_kernel<BN>, tX, tW, a) != cudaSuccess) return MOE_ERR_CUDA;
+  return launched(cudaGetLastError());
+}
+
+// Router GEMM + softmax + top-k (+ per-CTA expert counts when hist is set, +
+// per-CTA probability sums when psum is set), one launch.
+moe_status launch_route(const moe_dims& d, int gate_mode, const moe_bf16* x,
+                        const moe_bf16* w_router, const float* bias, float* logits_out,
+                        int32_t* topk_idx, float* topk_w, float* psum, int32_t* hist,
+                        const RouteSplit& rs, int* status, cudaStream_t st) {
+  int bn = 16;
+  while (bn < d.E) bn *= 2;
+  CUtensorMap tX, tW;
+  if (!make_map(&tX, x, d.H, d.T, 1, 64, moe::kRouteBM)) return MOE_ERR_CUDA;
+  if (!make_map(&tW, w_router, d.H, d.E, 1, 64, (uint32_t)bn)) return MOE_ERR_CUDA;
+  moe::RouteArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.T = d.T; a.H = d.H; a.E = d.E; a.k = d.k; a.gate_mode = gate_mode;
+  a.splits = rs.splits;
+  a.bias = bias; a.logits_out = logits_out; a.topk_idx = topk_idx; a.topk_w = topk_w;
+  a.psum_part = psum; a.hist = hist; a.hist_ld = rs.hist_ld; a.status = status;
+  switch (bn) {
+    case 16: return launch_route_bn<16>(tX, tW, a, rs.ncta, st);
+    case 32: return launch_route_bn<32>(tX, tW, a, rs.ncta, st);
+    case 64: return launch_route_bn<64>(tX, tW, a, rs.ncta, st);
+    case 128: return launch_route_bn<128>(tX, tW, a, rs.ncta, st);
+    default: return launch_route_bn<256>(tX, tW, a, rs.ncta, st);
+  }
+}
+
 }  // namespace
 
 // =====================================================================================
@@ -427,50 +502,56 @@ moe_status moe_route(const moe_dims* d, int32_t gate_mode, const moe_bf16* x,
     return MOE_ERR_INVALID_ARG;
   if (!x || !w_router || !topk_idx || !topk_w || !workspace) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(w_router) || !aligned16(workspace)) return MOE_ERR_INVALID_ARG;
-  if (workspace_bytes < kAlign) return MOE_ERR_WORKSPACE_TOO_SMALL;
   const Layout L = make_layout(*d, false);
-  if (workspace_bytes < L.h) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  if (workspace_bytes < L.route_end) return MOE_ERR_WORKSPACE_TOO_SMALL;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int T = d->T, H = d->H, E = d->E;
-  // split K so that the router GEMM's tiles fill the SMs in one wave; partial
-  // logits are summed in split order by the top-k kernel
-  const long long mt = cdiv(T, moe::BM);
-  int splits = (int)std::min<long long>(kMaxRouterSplits, std::max<long long>(1, sm_count() / mt));
-  const int kblocks = H / moe::BK;
-  if (splits > kblocks) splits = kblocks;
-  const int ksplit = (int)cdiv(kblocks, splits) * moe::BK;
-  splits = (int)cdiv(H, ksplit);
-  int bn = 16;
-  while (bn < E) bn *= 2;
-  float* part = at<float>(workspace, L.logits_part);
-  CUtensorMap tA, tB;
-  if (!make_map(&tA, x, H, T, 1, 64, 128)) return MOE_ERR_CUDA;
-  if (!make_map(&tB, w_router, H, E, 1, 64, bn)) return MOE_ERR_CUDA;
-  GemmArgs a = base_args(at<int>(workspace, 0));
-  a.M = T; a.N = E; a.K = H; a.G = splits; a.ksplit = ksplit;
-  a.d_f32 = part; a.ldd = E; a.d_group_stride = (long long)T * E;
-  CUtensorMap tD = tA;
-  a.f32_tma = (E % 4 == 0) && make_out_map3_f32(&tD, part, E, T, splits) ? 1 : 0;
-  const long long tiles = mt * splits;
-  switch (bn) {
-    case 16: s = launch_gemm<CfgRouter<16>>(MOE_K_ROUTER, tA, tB, tD, tD, a, tiles, st); break;
-    case 32: s = launch_gemm<CfgRouter<32>>(MOE_K_ROUTER, tA, tB, tD, tD, a, tiles, st); break;
-    case 64: s = launch_gemm<CfgRouter<64>>(MOE_K_ROUTER, tA, tB, tD, tD, a, tiles, st); break;
-    case 128: s = launch_gemm<CfgRouter<128>>(MOE_K_ROUTER, tA, tB, tD, tD, a, tiles, st); break;
-    default: s = launch_gemm<CfgRouter<256>>(MOE_K_ROUTER, tA, tB, tD, tD, a, tiles, st); break;
-  }
-  if (s != MOE_OK) return s;
-  const unsigned tk_blocks = (unsigned)cdiv((long long)T, moe::kTopkWarps);
+  const RouteSplit rs = route_split(*d);
   float* psum = prob_sum ? at<float>(workspace, L.psum_part) : nullptr;
-  {
-    KernelScope ks(MOE_K_ROUTER_TOPK, st);
-    moe::router_topk_kernel<<<tk_blocks, 32 * moe::kTopkWarps, 0, st>>>(
-        part, splits, router_bias, logits_out, topk_idx, topk_w, psum, T, E, d->k, gate_mode);
-  }
+  s = launch_route(*d, gate_mode, x, w_router, router_bias, logits_out, topk_idx, topk_w, psum,
+                   nullptr, rs, at<int>(workspace, 0), st);
+  if (s != MOE_OK) return s;
   if (prob_sum) {  // sum over tokens of the router softmax (auxiliary loss), fixed order
     KernelScope ks(MOE_K_AUX, st);
-    moe::prob_sum_kernel<<<(unsigned)cdiv(E, 32), 32 * moe::kProbSumWarps, 0, st>>>(
-        psum, (int)tk_blocks, E, prob_sum);
+    moe::prob_sum_kernel<<<(unsigned)cdiv(d->E, 32), 32 * moe::kProbSumWarps, 0, st>>>(
+        psum, rs.ncta, d->E, prob_sum);
+  }
+  return launched(cudaGetLastError());
+}
+
+moe_status moe_route_permute(const moe_dims* d, int32_t gate_mode, const moe_bf16* x,
+                             const moe_bf16* w_router, const float* router_bias,
+                             float* logits_out, int32_t* topk_idx, float* topk_w,
+                             float* prob_sum, int32_t* expert_offsets, int32_t* perm_slot,
+                             int32_t* slot_perm, void* workspace, size_t workspace_bytes,
+                             void* stream) {
+  moe_status s = check_dims(d);
+  if (s != MOE_OK) return s;
+  if (gate_mode != MOE_GATE_SOFTMAX_TOPK && gate_mode != MOE_GATE_BALANCED)
+    return MOE_ERR_INVALID_ARG;
+  if (!x || !w_router || !topk_idx || !topk_w || !expert_offsets || !perm_slot || !slot_perm ||
+      !workspace)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w_router) || !aligned16(workspace)) return MOE_ERR_INVALID_ARG;
+  const Layout L = make_layout(*d, false);
+  if (workspace_bytes < L.route_end) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const RouteSplit rs = route_split(*d);
+  int* status = at<int>(workspace, 0);
+  int32_t* hist = at<int32_t>(workspace, L.hist);
+  float* psum = prob_sum ? at<float>(workspace, L.psum_part) : nullptr;
+  s = launch_route(*d, gate_mode, x, w_router, router_bias, logits_out, topk_idx, topk_w, psum,
+                   hist, rs, status, st);
+  if (s != MOE_OK) return s;
+  {
+    KernelScope ks(MOE_K_ROUTE_SORT, st);
+    moe::route_sort_kernel<<<(unsigned)rs.ncta, moe::kRouteSortThreads, 0, st>>>(
+        topk_idx, d->T, d->k, d->E, rs.splits, rs.ncta, hist, rs.hist_ld, expert_offsets,
+        perm_slot, slot_perm, d->capacity, status);
+  }
+  if (prob_sum) {
+    KernelScope ks(MOE_K_AUX, st);
+    moe::prob_sum_kernel<<<(unsigned)cdiv(d->E, 32), 32 * moe::kProbSumWarps, 0, st>>>(
+        psum, rs.ncta, d->E, prob_sum);
   }
   return launched(cudaGetLastError());
 }
@@ -496,7 +577,7 @@ moe_status moe_permute(const moe_dims* d, const int32_t* topk_idx, int32_t* expe
     return MOE_ERR_INVALID_ARG;
   if (!aligned16(workspace)) return MOE_ERR_INVALID_ARG;
   const Layout L = make_layout(*d, false);
-  if (workspace_bytes < L.logits_part) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  if (workspace_bytes < L.hist) return MOE_ERR_WORKSPACE_TOO_SMALL;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int32_t* counts = at<int32_t>(workspace, L.counts);
   { KernelScope ks(MOE_K_SORT_HISTOGRAM, st);
@@ -527,6 +608,7 @@ moe_status launch_gate_up(const moe_dims& d, const moe_bf16* x, const int32_t* e
   a.gsrc = reinterpret_cast<const __nv_bfloat16*>(x); a.gld = H; a.gperm = perm_slot;
   a.gdiv = d.k; a.gsrc_rows = d.T;
   a.gu_out = reinterpret_cast<__nv_bfloat16*>(gu_out); a.h_out = h_out; a.inter = I;
+  a.out_l2[1] = 2;  // h: evict-last, the down GEMM reads it next while streaming W_down
   return launch_gemm<CfgGateUp>(MOE_K_GATE_UP, tA, tB, tD0, tD1, a,
                                 (cdiv(S, moe::BM) + E) * cdiv(I, 128), st);
 }
@@ -584,6 +666,11 @@ moe_status moe_grouped_mlp_fwd(const moe_dims* d, const moe_bf16* x,
     GemmArgs a = base_args(status);
     a.N = H; a.K = I; a.G = E; a.offsets = expert_offsets; a.cap = d->capacity;
     a.d = reinterpret_cast<__nv_bfloat16*>(y_perm); a.ldd = H;
+    a.a_l2 = 1;  // h is read once: evict-first as it arrives
+    // without saved pre-activations (no backward, or one that recomputes them)
+    // y_perm is kept in L2 for the combine that follows; a training forward
+    // leaves it normal, so that it does not hold L2 into the backward
+    if (!gu_saved) a.out_l2[0] = 2;
     s = launch_gemm<CfgDown>(MOE_K_DOWN, tA, tB, tD, tD, a, (cdiv(S, moe::BM) + E) * cdiv(H, 256), st);
     if (s != MOE_OK) return s;
   }
@@ -834,7 +921,7 @@ moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_
     a.d_group_stride = (long long)H * I;
     CUtensorMap tD;
     if (!make_out_map3(&tD, grad_w_down, I, H, E)) return MOE_ERR_CUDA;
-    a.out_evict_first = 1;  // nothing in the layer reads the weight gradients back
+    a.out_l2[0] = 1;  // evict-first: nothing in the layer reads the weight gradients back
     s = launch_gemm<CfgWgradDownRes, true>(MOE_K_WGRAD_DOWN, tA, tB, tD, tD, a,
                                            (long long)E * cdiv(H, 2 * moe::BM) * cdiv(I, 256), st);
     if (s != MOE_OK) return s;
@@ -850,7 +937,7 @@ moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_
     a.d_group_stride = 2LL * I * H;
     CUtensorMap tD;
     if (!make_out_map3(&tD, grad_w_gate_up, H, 2LL * I, E)) return MOE_ERR_CUDA;
-    a.out_evict_first = 1;  // nothing in the layer reads the weight gradients back
+    a.out_l2[0] = 1;  // evict-first: nothing in the layer reads the weight gradients back
     s = launch_gemm<CfgWgradRes, true>(MOE_K_WGRAD_GATE_UP, tA, tB, tD, tD, a,
                                        (long long)E * cdiv(2 * I, 2 * moe::BM) * cdiv(H, 256), st);
     if (s != MOE_OK) return s;
@@ -868,7 +955,7 @@ moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_
       a.d = reinterpret_cast<__nv_bfloat16*>(grad_w_sh_down); a.ldd = Is;
       CUtensorMap tD;
       if (!make_out_map3(&tD, grad_w_sh_down, Is, H, 1)) return MOE_ERR_CUDA;
-      a.out_evict_first = 1;  // nothing in the layer reads the weight gradients back
+      a.out_l2[0] = 1;  // evict-first: nothing in the layer reads the weight gradients back
       s = launch_gemm<CfgWgrad>(MOE_K_SHARED_WGRAD_DOWN, tA, tB, tD, tD, a, cdiv(H, moe::BM) * cdiv(Is, 256), st);
       if (s != MOE_OK) return s;
     }
@@ -881,7 +968,7 @@ moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_
       a.d = reinterpret_cast<__nv_bfloat16*>(grad_w_sh_gate_up); a.ldd = H;
       CUtensorMap tD;
       if (!make_out_map3(&tD, grad_w_sh_gate_up, H, 2LL * Is, 1)) return MOE_ERR_CUDA;
-      a.out_evict_first = 1;  // nothing in the layer reads the weight gradients back
+      a.out_l2[0] = 1;  // evict-first: nothing in the layer reads the weight gradients back
       s = launch_gemm<CfgWgrad>(MOE_K_SHARED_WGRAD_GATE_UP, tA, tB, tD, tD, a, cdiv(2 * Is, moe::BM) * cdiv(H, 256), st);
       if (s != MOE_OK) return s;
     }
@@ -889,15 +976,48 @@ moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_
   return MOE_OK;
 }
 
+moe_status moe_gather_rows(const moe_bf16* src, int64_t src_rows, int32_t H, const int32_t* idx,
+                           int32_t n, int32_t div, moe_bf16* dst, int32_t* device_status,
+                           void* stream) {
+  if (n < 0 || src_rows < 0 || div < 1) return MOE_ERR_INVALID_ARG;
+  if (H < 8 || H % 8) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (n == 0) return MOE_OK;
+  if (!src || !idx || !dst) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(src) || !aligned16(dst)) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  KernelScope ks(MOE_K_GATHER_ROWS, st);
+  moe::gather_rows_kernel<<<(unsigned)cdiv((long long)n * 32, 256), 256, 0, st>>>(
+      reinterpret_cast<const __nv_bfloat16*>(src), (long long)src_rows, H, idx, n, div,
+      reinterpret_cast<__nv_bfloat16*>(dst), device_status);
+  return launched(cudaGetLastError());
+}
+
+moe_status moe_ep_receive_layout(int32_t n_src, int32_t E_local, const int32_t* counts, int32_t R,
+                                 int32_t* local_offsets, int32_t* recv_perm, int32_t* recv_inv,
+                                 int32_t* device_status, void* stream) {
+  if (n_src < 1 || E_local < 1 || R < 0) return MOE_ERR_INVALID_ARG;
+  if (E_local > moe::kEpMaxLocalExperts || (long long)n_src * E_local > moe::kEpMaxCells)
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!counts || !local_offsets || (R > 0 && (!recv_perm || !recv_inv))) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const long long blocks =
+      std::max<long long>(1, std::min<long long>(cdiv(R, moe::kEpLayoutThreads), 4LL * sm_count()));
+  KernelScope ks(MOE_K_EP_LAYOUT, st);
+  moe::ep_recv_layout_kernel<<<(unsigned)blocks, moe::kEpLayoutThreads, 0, st>>>(
+      counts, n_src, E_local, R, local_offsets, recv_perm, recv_inv, device_status);
+  return launched(cudaGetLastError());
+}
+
 int32_t moe_kernel_count(void) { return MOE_K_COUNT; }
 
 const char* moe_kernel_name(int32_t id) {
   static const char* names[MOE_K_COUNT] = {
-      "router", "router_topk", "sort_histogram", "sort_scatter", "gate_up",
+      "router", "route_sort", "sort_histogram", "sort_scatter", "gate_up",
       "down", "shared_gate_up", "shared_down", "combine", "dgrad_down",
       "dgrad_gate_up", "shared_dgrad_down", "shared_dgrad_gate_up", "dx_gather",
       "router_wgrad", "wgrad_down", "wgrad_gate_up", "shared_wgrad_down",
-      "shared_wgrad_gate_up", "router_wgrad_reduce", "aux_loss", "router_dx"};
+      "shared_wgrad_gate_up", "router_wgrad_reduce", "aux_loss", "router_dx", "gather_rows",
+      "ep_recv_layout"};
   return (id >= 0 && id < MOE_K_COUNT) ? names[id] : "unknown";
 }
 

@@ -62,6 +62,7 @@ _SIGS = {
     "moe_status_string": ([_I32], ctypes.c_char_p),
     "moe_workspace_size": ([_DIMS, _I32, ctypes.POINTER(_SZ)], _I32),
     "moe_route": ([_DIMS, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P], _I32),
+    "moe_route_permute": ([_DIMS, _I32] + [_P] * 11 + [_SZ, _P], _I32),
     "moe_aux_loss": ([_DIMS, _P, _P, ctypes.c_float, _P, _P, _P], _I32),
     "moe_permute": ([_DIMS, _P, _P, _P, _P, _P, _SZ, _P], _I32),
     "moe_grouped_mlp_fwd": ([_DIMS, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P], _I32),
@@ -69,6 +70,8 @@ _SIGS = {
     "moe_layer_bwd": ([_DIMS] + [_P] * 23 + [_P, _SZ, _P], _I32),
     "moe_read_device_status": ([_P, _SZ, _P, _I32, ctypes.POINTER(_I32)], _I32),
     "moe_permute_static_scratch": ([_DIMS, _P, _P, _P, _P, _P, _P], _I32),
+    "moe_gather_rows": ([_P, ctypes.c_int64, _I32, _P, _I32, _I32, _P, _P, _P], _I32),
+    "moe_ep_receive_layout": ([_I32, _I32, _P, _I32, _P, _P, _P, _P, _P], _I32),
     "moe_kernel_count": ([], _I32),
     "moe_kernel_name": ([_I32], ctypes.c_char_p),
     "moe_timing_enable": ([_I32], _I32),
@@ -170,6 +173,15 @@ def moe_route(dims, gate_mode, x, w_router, router_bias, logits_out, topk_idx, t
         _ptr(logits_out), _ptr(topk_idx), _ptr(topk_w), _ptr(prob_sum), p, n, _stream(stream)))
 
 
+def moe_route_permute(dims, gate_mode, x, w_router, router_bias, logits_out, topk_idx, topk_w,
+                      expert_offsets, perm_slot, slot_perm, workspace, stream=None, prob_sum=None):
+    p, n = _ws(workspace)
+    _check("moe_route_permute", load_library().moe_route_permute(
+        ctypes.byref(_dims(dims)), int(gate_mode), _ptr(x), _ptr(w_router), _ptr(router_bias),
+        _ptr(logits_out), _ptr(topk_idx), _ptr(topk_w), _ptr(prob_sum), _ptr(expert_offsets),
+        _ptr(perm_slot), _ptr(slot_perm), p, n, _stream(stream)))
+
+
 def moe_aux_loss(dims, prob_sum, expert_offsets, alpha, loss, coef, stream=None):
     _check("moe_aux_loss", load_library().moe_aux_loss(
         ctypes.byref(_dims(dims)), _ptr(prob_sum), _ptr(expert_offsets), ctypes.c_float(alpha),
@@ -228,6 +240,26 @@ def moe_permute_static_scratch(dims, topk_idx, expert_offsets, perm_slot, slot_p
     _check("moe_permute_static_scratch", load_library().moe_permute_static_scratch(
         ctypes.byref(_dims(dims)), _ptr(topk_idx), _ptr(expert_offsets), _ptr(perm_slot),
         _ptr(slot_perm), _ptr(device_status), _stream(stream)))
+
+
+def moe_gather_rows(src, idx, div, dst, device_status=None, stream=None):
+    """dst[i] = src[idx[i] // div] (bf16 rows; idx int32 [n]; dst [n, H])."""
+    n = int(idx.numel())
+    _check("moe_gather_rows", load_library().moe_gather_rows(
+        _ptr(src) if src.numel() else None, int(src.shape[0]), int(src.shape[1]),
+        _ptr(idx) if n else None, n, int(div), _ptr(dst) if n else None, _ptr(device_status),
+        _stream(stream)))
+
+
+def moe_ep_receive_layout(counts, local_offsets, recv_perm, recv_inv, device_status=None,
+                          stream=None):
+    """counts int32 [n_src, E_local] (device) -> local_offsets [E_local+1],
+    recv_perm / recv_inv [R] with R = counts.sum() (given by their length)."""
+    n_src, E_loc = int(counts.shape[0]), int(counts.shape[1])
+    R = int(recv_perm.numel())
+    _check("moe_ep_receive_layout", load_library().moe_ep_receive_layout(
+        n_src, E_loc, _ptr(counts), R, _ptr(local_offsets), _ptr(recv_perm) if R else None,
+        _ptr(recv_inv) if R else None, _ptr(device_status), _stream(stream)))
 
 
 def moe_kernel_count() -> int:
@@ -298,9 +330,9 @@ class MoeLayer:
         """out: bf16 [T, H] to write the layer output into (default: self.out)."""
         d, ws = self.dims, self.workspace
         out = self.out if out is None else out
-        moe_route(d, self.gate_mode, x, w_router, router_bias, self.logits, self.topk_idx,
-                  self.topk_w, ws, stream, prob_sum=self.prob_sum)
-        moe_permute(d, self.topk_idx, self.expert_offsets, self.perm_slot, self.slot_perm, ws, stream)
+        moe_route_permute(d, self.gate_mode, x, w_router, router_bias, self.logits, self.topk_idx,
+                          self.topk_w, self.expert_offsets, self.perm_slot, self.slot_perm, ws,
+                          stream, prob_sum=self.prob_sum)
         if self.aux_alpha is not None:
             moe_aux_loss(d, self.prob_sum, self.expert_offsets, self.aux_alpha, self.aux_loss,
                          self.aux_coef, stream)

@@ -91,7 +91,8 @@ const char* moe_status_string(int32_t status);
 
 /*
  * Bytes of device workspace the calls below need for these dims.  One
- * workspace can serve moe_route, moe_permute, moe_grouped_mlp_fwd and, with
+ * workspace can serve moe_route, moe_route_permute, moe_permute,
+ * moe_grouped_mlp_fwd and, with
  * with_backward = 1, moe_layer_bwd given the saved pre-activations; with
  * with_backward = 2, also moe_layer_bwd recomputing them (gu_saved and/or
  * sh_gu_saved NULL: room for [S,2I] and [T,2*I_shared] bf16 more).
@@ -116,11 +117,35 @@ moe_status moe_workspace_size(const moe_dims* d, int32_t with_backward, size_t* 
  * x: bf16 [T,H]; w_router: bf16 [E,H]; router_bias: fp32 [E] or NULL;
  * logits_out: fp32 [T,E] or NULL; topk_idx: int32 [T,k]; topk_w: fp32 [T,k];
  * prob_sum: fp32 [E] or NULL (a fixed-order sum: bit-identical run to run).
+ * One kernel computes the logits on the tensor cores (K split over a cluster
+ * of CTAs whose partial sums are added on chip, in a fixed order) and the
+ * softmax, selection and weights; a second one sums prob_sum when asked for.
+ * Errors: MOE_ERR_INVALID_ARG (null, misaligned x / w_router / workspace, bad
+ * gate_mode), MOE_ERR_UNSUPPORTED_SHAPE, MOE_ERR_WORKSPACE_TOO_SMALL,
+ * MOE_ERR_CUDA.
  */
 moe_status moe_route(const moe_dims* d, int32_t gate_mode, const moe_bf16* x,
                      const moe_bf16* w_router, const float* router_bias, float* logits_out,
                      int32_t* topk_idx, float* topk_w, float* prob_sum, void* workspace,
                      size_t workspace_bytes, void* stream);
+
+/*
+ * moe_route followed by moe_permute, in two kernels instead of four: the
+ * router kernel also counts, per CTA, the chosen slots of each expert, and
+ * one sort pass places every slot from those counts (the grouped_mm row's
+ * "sort the tokens by their assigned expert", fused with the router).
+ * Outputs are bit-identical to moe_route then moe_permute on the same
+ * inputs: logits_out, topk_idx, topk_w, prob_sum as moe_route;
+ * expert_offsets [E+1], perm_slot [S], slot_perm [S] (with d->capacity) as
+ * moe_permute.  All pointers are caller-owned device memory; logits_out and
+ * prob_sum may be NULL.  Errors: as moe_route.
+ */
+moe_status moe_route_permute(const moe_dims* d, int32_t gate_mode, const moe_bf16* x,
+                             const moe_bf16* w_router, const float* router_bias,
+                             float* logits_out, int32_t* topk_idx, float* topk_w,
+                             float* prob_sum, int32_t* expert_offsets, int32_t* perm_slot,
+                             int32_t* slot_perm, void* workspace, size_t workspace_bytes,
+                             void* stream);
 
 /*
  * Auxiliary load-balancing loss ("NVIDIA NeMo AutoModel MoE 微調的 3.7 倍加速突破",
@@ -284,14 +309,58 @@ moe_status moe_permute_static_scratch(const moe_dims* d, const int32_t* topk_idx
                                       int32_t* slot_perm, int32_t* device_status, void* stream);
 
 /*
+ * Expert parallelism (NeMo AutoModel blog, "专家并行与 DeepEP": every rank holds
+ * 1/ep of the experts, split along the expert dimension as Shard(0) splits it,
+ * and trains on its own tokens; DeepEP dispatches the tokens to their experts'
+ * ranks and combines the outputs back with all-to-all exchanges).  The
+ * exchange is the caller's collective; these two calls lay the rows out
+ * around it.  A source sorts its slots with moe_route_permute (expert order is
+ * rank order, because every rank's experts are contiguous) and gathers its
+ * token rows in that order; a receiver groups what it got by expert with
+ * moe_ep_receive_layout, runs moe_grouped_mlp_fwd over its local experts
+ * (dims T = rows received, k = 1, E = local experts; perm_slot = recv_perm),
+ * puts the outputs back in receive order with moe_gather_rows (idx =
+ * recv_inv), and exchanges them back; the source then holds y_perm in its
+ * own sorted order and calls moe_unpermute_combine.
+ */
+
+/*
+ * dst[i] = src[idx[i] / div] for i < n: rows of H bf16 (H a multiple of 8),
+ * src [src_rows, H], dst [n, H], idx int32 [n]; all device memory, caller-owned.
+ * A row index outside [0, src_rows) gives a zero row and MOE_ERR_DEVICE_INDEX
+ * in *device_status (optional, device int32; recorded only over MOE_OK).
+ * Errors: MOE_ERR_INVALID_ARG (null, misaligned src/dst, n < 0, div < 1),
+ * MOE_ERR_UNSUPPORTED_SHAPE (H), MOE_ERR_CUDA.
+ */
+moe_status moe_gather_rows(const moe_bf16* src, int64_t src_rows, int32_t H, const int32_t* idx,
+                           int32_t n, int32_t div, moe_bf16* dst, int32_t* device_status,
+                           void* stream);
+
+/*
+ * A receiving rank's layout.  counts: int32 [n_src, E_local] (device), the
+ * rows source s sent for local expert e; the receive buffer holds source 0's
+ * rows, then source 1's, ..., each source's in expert order; R = their total.
+ * Writes local_offsets [E_local+1] (local expert e owns grouped rows
+ * local_offsets[e] .. local_offsets[e+1]-1), recv_perm [R] (grouped row g is
+ * receive row recv_perm[g]; grouped order: expert, then source, then the
+ * source's order) and recv_inv [R] (its inverse).  A total that is not R is
+ * recorded as MOE_ERR_DEVICE_INDEX in *device_status (optional).  Limits:
+ * E_local <= 256, n_src * E_local <= 4096.  Errors: MOE_ERR_INVALID_ARG,
+ * MOE_ERR_UNSUPPORTED_SHAPE, MOE_ERR_CUDA.
+ */
+moe_status moe_ep_receive_layout(int32_t n_src, int32_t E_local, const int32_t* counts, int32_t R,
+                                 int32_t* local_offsets, int32_t* recv_perm, int32_t* recv_inv,
+                                 int32_t* device_status, void* stream);
+
+/*
  * Kernel accounting, for benchmarks and tests (no counterpart on the pages).
  * Every kernel the calls above launch is counted under one of the ids below.
  * While timing is enabled, each launch is also bracketed by a pair of CUDA
  * events recorded on the launch stream.
  */
 typedef enum {
-  MOE_K_ROUTER = 0,          /* moe_route: split-K router GEMM (fp32 partial logits) */
-  MOE_K_ROUTER_TOPK,         /* moe_route: softmax + top-k (one warp per token) */
+  MOE_K_ROUTER = 0,          /* moe_route(_permute): router GEMM + softmax + top-k (+ expert counts) */
+  MOE_K_ROUTE_SORT,          /* moe_route_permute: sort pass from the router's expert counts */
   MOE_K_SORT_HISTOGRAM,      /* moe_permute, pass 1: per-block expert histograms */
   MOE_K_SORT_SCATTER,        /* moe_permute, pass 2: scan + stable scatter */
   MOE_K_GATE_UP,             /* grouped gate/up GEMM + SwiGLU (token rows gathered in-kernel) */
@@ -313,6 +382,8 @@ typedef enum {
   MOE_K_AUX,                 /* auxiliary loss: probability sums, loss, dense logit gradient */
   MOE_K_ROUTER_DX,           /* backward with the auxiliary loss: grad_x = DL W_r (GEMM), before
                                 the per-token gather adds the slot gradients into it */
+  MOE_K_GATHER_ROWS,         /* moe_gather_rows */
+  MOE_K_EP_LAYOUT,           /* moe_ep_receive_layout */
   MOE_K_COUNT
 } moe_kernel_id;
 

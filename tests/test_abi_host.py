@@ -23,7 +23,7 @@ def lib():
 
 def test_header_declares_the_five_layer_calls():
     names = M.declared_functions()
-    for n in ["moe_route", "moe_permute", "moe_grouped_mlp_fwd", "moe_unpermute_combine",
+    for n in ["moe_route", "moe_route_permute", "moe_permute", "moe_grouped_mlp_fwd", "moe_unpermute_combine",
               "moe_layer_bwd", "moe_workspace_size", "moe_read_device_status",
               "moe_status_string", "moe_abi_version"]:
         assert n in names
@@ -35,7 +35,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert M.moe_abi_version() == 10
+    assert M.moe_abi_version() == 11
     assert M.moe_status_string(0) == "ok"
     for s in range(1, 7):
         assert M.moe_status_string(s) not in ("ok", "unknown status")
@@ -89,6 +89,13 @@ def test_null_and_misaligned_arguments_rejected_before_launch(lib):
     # workspace too small
     assert lib.moe_route(ctypes.byref(d), 0, wsp, wsp, None, None, wsp, wsp, None, wsp, 16, None) == 3
     assert lib.moe_permute(ctypes.byref(d), wsp, wsp, wsp, wsp, wsp, 64, None) == 3
+    # router + sort in one call: null outputs, bad gate, misaligned x, small workspace
+    rp = [wsp, wsp, None, None, wsp, wsp, None, wsp, wsp, wsp]   # x .. slot_perm
+    assert lib.moe_route_permute(ctypes.byref(d), 0, *rp[:7], None, wsp, wsp, wsp, 1 << 19, None) == 1
+    assert lib.moe_route_permute(ctypes.byref(d), 0, *rp[:9], None, wsp, 1 << 19, None) == 1
+    assert lib.moe_route_permute(ctypes.byref(d), 3, *rp, wsp, 1 << 19, None) == 1
+    assert lib.moe_route_permute(ctypes.byref(d), 0, wsp + 8, *rp[1:], wsp, 1 << 19, None) == 1
+    assert lib.moe_route_permute(ctypes.byref(d), 0, *rp, wsp, 64, None) == 3
     args = [wsp] * 12
     assert lib.moe_grouped_mlp_fwd(ctypes.byref(d), *args[:6], None, None, None, None, None, wsp, 64, None) == 1
     assert lib.moe_unpermute_combine(ctypes.byref(d), None, wsp, wsp, None, wsp, None) == 1
@@ -160,3 +167,24 @@ def test_backward_argument_checks_before_launch(lib):
 
     assert bwd(p, None, p, recompute) == 1          # aux coefficients, no logits
     assert bwd(None, None, None, saved) == 3        # recompute needs the larger workspace
+
+
+def test_expert_parallel_calls_validate_before_launch(lib):
+    ws = ctypes.create_string_buffer(4096)
+    p = (ctypes.addressof(ws) + 255) // 256 * 256
+    g = lib.moe_gather_rows
+    assert g(p, 10, 64, p, 0, 1, p, None, None) == 0          # nothing to copy
+    assert g(None, 10, 64, p, 4, 1, p, None, None) == 1       # null source
+    assert g(p, 10, 64, p, 4, 0, p, None, None) == 1          # div < 1
+    assert g(p, 10, 64, p, -1, 1, p, None, None) == 1         # negative count
+    assert g(p + 8, 10, 64, p, 4, 1, p, None, None) == 1      # misaligned rows
+    assert g(p, 10, 60, p, 4, 1, p, None, None) == 2          # H not a multiple of 8
+    L = lib.moe_ep_receive_layout
+    assert L(0, 4, p, 0, p, None, None, None, None) == 1      # no sources
+    assert L(2, 0, p, 0, p, None, None, None, None) == 1      # no local experts
+    assert L(2, 4, None, 0, p, None, None, None, None) == 1   # no counts
+    assert L(2, 4, p, 8, p, None, None, None, None) == 1      # rows but no outputs
+    assert L(2, 300, p, 0, p, None, None, None, None) == 2    # > 256 local experts
+    assert L(64, 128, p, 0, p, None, None, None, None) == 2   # > 4096 cells
+    assert "moe_gather_rows" in M.declared_functions()
+    assert "moe_ep_receive_layout" in M.declared_functions()

@@ -62,6 +62,43 @@ def test_router_logits_and_topk(case):
         assert np.array_equal(idx, O.balanced_topk(di.w.T, di.w.E, di.w.k))
 
 
+def test_route_permute_equals_route_then_permute(case):
+    """The fused call (router kernel counting experts + one sort pass) gives the
+    same bits as moe_route then moe_permute, with and without an expert
+    capacity and the probability sums."""
+    di, _ = case
+    w = di.w
+    T, E, k = w.T, w.E, w.k
+    counts = None
+    for cap in (0, None):
+        if cap is None:   # a capacity that drops slots of the busiest experts
+            cap = max(1, int(counts.max()) - 1)
+        d = M.MoeDims.of(*di.dims, capacity=cap)
+        ws = torch.zeros(M.moe_workspace_size(d, False), dtype=torch.uint8, device="cuda")
+        outs = []
+        for fused in (False, True):
+            lg = torch.empty(T, E, dtype=torch.float32, device="cuda")
+            idx = torch.empty(T, k, dtype=torch.int32, device="cuda")
+            tw = torch.empty(T, k, dtype=torch.float32, device="cuda")
+            ps = torch.empty(E, dtype=torch.float32, device="cuda")
+            off = torch.full((E + 1,), -7, dtype=torch.int32, device="cuda")
+            perm = torch.full((T * k,), -7, dtype=torch.int32, device="cuda")
+            inv = torch.full((T * k,), -7, dtype=torch.int32, device="cuda")
+            if fused:
+                M.moe_route_permute(d, w.gate, di.x, di.w_router, di.router_bias, lg, idx, tw, off,
+                                    perm, inv, ws, prob_sum=ps)
+            else:
+                M.moe_route(d, w.gate, di.x, di.w_router, di.router_bias, lg, idx, tw, ws, prob_sum=ps)
+                M.moe_permute(d, idx, off, perm, inv, ws)
+            torch.cuda.synchronize()
+            assert M.moe_read_device_status(ws) == 0
+            outs.append([t.cpu() for t in (lg, idx, tw, ps, off, perm, inv)])
+        for a, b in zip(*outs):
+            assert torch.equal(a.view(torch.int32) if a.dtype == torch.float32 else a,
+                               b.view(torch.int32) if b.dtype == torch.float32 else b)
+        counts = np.diff(outs[1][4].numpy())
+
+
 def test_permute_bit_exact(case):
     di, layer = case
     idx = layer.topk_idx.cpu().numpy()

@@ -69,10 +69,8 @@ struct GemmArgs {
   const __nv_bfloat16* gu_saved; const int32_t* perm_slot; const float* slot_w;
   __nv_bfloat16* dgu_out; __nv_bfloat16* hw_out; float* dw_part;
   int* status;
-  // L2 hints (0 none, 1 evict-first, 2 evict-last): out_l2[i] for the stores
-  // through output map i, a_l2 for A's TMA tile loads (CTA-pair K-major A only)
+  // L2 hint of the stores through output map i (0 none, 1 evict-first, 2 evict-last)
   int out_l2[2];
-  int a_l2;
 };
 
 template <int BN_, int STAGES_, int AL_, int BL_, int SCH_, int EPI_, bool B3D_, bool SWIGLU_B_,
@@ -642,7 +640,8 @@ __device__ void epilogue_dgrad_swiglu(const GemmArgs& a, const SmemTables& T, co
 
 // ---------------------------------------------------------------- gather warps
 // Source token row for row i of group g (rows past the group's tokens reuse its
-// last token: finite values, results masked or multiplied by zero).
+// last token: finite values, for the K-side gathers whose padding rows multiply
+// zeros; the M-side gathers skip those rows).
 __device__ __forceinline__ int gather_row(const GemmArgs& a, const SmemTables& T, int g, int i) {
   const int n = T.cnt[g];
   const int r = T.off[g] + (i < n ? i : n - 1);
@@ -726,12 +725,16 @@ __device__ void gather_role(const GemmArgs& a, const SmemTables& T, uint32_t sme
     if (ti.phantom) {
       // pair slot past the group's last tile: the stage is not read into any output
     } else if constexpr (KM) {
+      // rows of the M-tile past the group's rows are not copied: each feeds
+      // only its own output row, which is never stored (K-side gathers below
+      // keep their finite padding rows, which multiply zeros)
       const int c = lane & 7;
       const __nv_bfloat16* col = a.gsrc + kb * BK + c * 8;
+      const int nvalid = T.cnt[ti.g] - ti.mb * BM;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int r = gw * 32 + 4 * i + (lane >> 3);
-        cp_async_16(sA + r * 128 + ((c ^ (r & 7)) << 4), col + (size_t)src[i] * a.gld);
+        if (r < nvalid) cp_async_16(sA + r * 128 + ((c ^ (r & 7)) << 4), col + (size_t)src[i] * a.gld);
       }
     } else {
       // MN-major: operand extent X along M/N, X/8 16-byte chunks per k-row
@@ -872,7 +875,6 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     int stage = 0;
     uint32_t phase = 0;
     uint32_t filled = 0, fill_parity = 0;  // per stage: armed at least once, parity of last fill
-    const uint64_t a_policy = l2_policy(a.a_l2);
     for (int t = unit0; t < total && !*abort_flag; t += ustep) {
       const TileInfo ti = decode_tile<C>(a, T, t, rank);
       const int n0 = C::SWIGLU_B ? ti.nb * (C::BN / 2) : ti.nb * C::BN;
@@ -898,12 +900,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           // A comes from the gather warps
         } else if constexpr (C::AL == KMAJ_TILE) {
           if (lane == 0) {
-            if constexpr (C::PAIR) {
-              if (a.a_l2) tma_load_2d_pair_hint(sA, &tmA, fbp, kx, C::SCH == RAGGED_K ? m0 : ti.row0, a_policy);
-              else tma_load_2d_pair(sA, &tmA, fbp, kx, C::SCH == RAGGED_K ? m0 : ti.row0);
-            } else {
-              tma_load_2d(sA, &tmA, fb, kx, C::SCH == RAGGED_K ? m0 : ti.row0);
-            }
+            if constexpr (C::PAIR) tma_load_2d_pair(sA, &tmA, fbp, kx, C::SCH == RAGGED_K ? m0 : ti.row0);
+            else tma_load_2d(sA, &tmA, fb, kx, C::SCH == RAGGED_K ? m0 : ti.row0);
           }
         } else {  // MN_TILE: two 64-wide groups along M, 64 k-rows each
           if (lane == 0) {

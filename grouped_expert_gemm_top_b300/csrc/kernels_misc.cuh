@@ -188,16 +188,13 @@ __global__ void combine_kernel(const __nv_bfloat16* __restrict__ y_perm,
     rows[j] = __shfl_sync(0xffffffffu, row_l, j);
     ws[j] = __shfl_sync(0xffffffffu, w_l, j);
   }
-  // y_perm is read once: its lines become the first to leave L2
-  const uint64_t once = policy_evict_first();
   for (int c = lane; c < H / 8; c += 32) {
     uint4 v[KMAX];
 #pragma unroll
     for (int j = 0; j < KMAX; ++j)
       if (j < k)
         v[j] = rows[j] < 0 ? make_uint4(0u, 0u, 0u, 0u)
-                           : ld_nc_v4_hint(reinterpret_cast<const uint4*>(y_perm + (size_t)rows[j] * H) + c,
-                                           once);
+                           : __ldg(reinterpret_cast<const uint4*>(y_perm + (size_t)rows[j] * H) + c);
     uint4 vs = make_uint4(0, 0, 0, 0);
     if (y_shared) vs = __ldg(reinterpret_cast<const uint4*>(y_shared + (size_t)t * H) + c);
     float acc[8];

@@ -608,7 +608,6 @@ moe_status launch_gate_up(const moe_dims& d, const moe_bf16* x, const int32_t* e
   a.gsrc = reinterpret_cast<const __nv_bfloat16*>(x); a.gld = H; a.gperm = perm_slot;
   a.gdiv = d.k; a.gsrc_rows = d.T;
   a.gu_out = reinterpret_cast<__nv_bfloat16*>(gu_out); a.h_out = h_out; a.inter = I;
-  a.out_l2[1] = 2;  // h: evict-last, the down GEMM reads it next while streaming W_down
   return launch_gemm<CfgGateUp>(MOE_K_GATE_UP, tA, tB, tD0, tD1, a,
                                 (cdiv(S, moe::BM) + E) * cdiv(I, 128), st);
 }
@@ -666,11 +665,6 @@ moe_status moe_grouped_mlp_fwd(const moe_dims* d, const moe_bf16* x,
     GemmArgs a = base_args(status);
     a.N = H; a.K = I; a.G = E; a.offsets = expert_offsets; a.cap = d->capacity;
     a.d = reinterpret_cast<__nv_bfloat16*>(y_perm); a.ldd = H;
-    a.a_l2 = 1;  // h is read once: evict-first as it arrives
-    // without saved pre-activations (no backward, or one that recomputes them)
-    // y_perm is kept in L2 for the combine that follows; a training forward
-    // leaves it normal, so that it does not hold L2 into the backward
-    if (!gu_saved) a.out_l2[0] = 2;
     s = launch_gemm<CfgDown>(MOE_K_DOWN, tA, tB, tD, tD, a, (cdiv(S, moe::BM) + E) * cdiv(H, 256), st);
     if (s != MOE_OK) return s;
   }

@@ -187,23 +187,6 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
 __device__ __forceinline__ uint64_t l2_policy(int code) {
   return code == 2 ? policy_evict_last() : code == 1 ? policy_evict_first() : 0ull;
 }
-// CTA-pair tile load (as tma_load_2d_pair) with an L2 cache policy.
-__device__ __forceinline__ void tma_load_2d_pair_hint(uint32_t dst, const void* tmap, uint32_t bar,
-                                                      int x, int y, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar), "l"(policy)
-      : "memory");
-}
-// 16-byte read-only load with an L2 cache policy (no L1 allocation).
-__device__ __forceinline__ uint4 ld_nc_v4_hint(const void* p, uint64_t policy) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p), "l"(policy));
-  return v;
-}
 __device__ __forceinline__ void tma_store_2d_hint(const void* tmap, uint32_t src, int x, int y,
                                                   uint64_t policy) {
   asm volatile(

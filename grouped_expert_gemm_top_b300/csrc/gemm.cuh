@@ -71,11 +71,24 @@ struct GemmArgs {
   int* status;
   // L2 hint of the stores through output map i (0 none, 1 evict-first, 2 evict-last)
   int out_l2[2];
+  // Cross-kernel overlap (CTA-pair RAGGED_M GEMMs).  Producer side
+  // (dep_signal): every epilogue warp, once the stores of a unit are complete,
+  // adds 1 to dep_flags[pair] (pair = the unit's 256-row block: the group's
+  // earlier blocks + its m-block pair), and every CTA lets the next grid
+  // launch early.  Consumer side (a DYN config): work units come from the
+  // counter *sched_counter in the order CTAs ask for them, and a unit's
+  // operand loads wait until dep_flags[pair] >= dep_target.
+  int* dep_flags;
+  int dep_signal;
+  int dep_target;
+  int* sched_counter;
 };
 
 template <int BN_, int STAGES_, int AL_, int BL_, int SCH_, int EPI_, bool B3D_, bool SWIGLU_B_,
-          int EPI_WARPS_ = 4, bool PAIR_ = false, int EPI_BUFS_ = 3>
+          int EPI_WARPS_ = 4, bool PAIR_ = false, int EPI_BUFS_ = 3, bool DYN_ = false>
 struct GemmCfg {
+  // DYN: units handed out dynamically (consumer side of a cross-kernel overlap)
+  static constexpr bool DYN = DYN_;
   // PAIR: 2-CTA clusters computing one 256 x BN tile with CTA-pair UMMAs
   // (cta_group::2): each CTA stages its own 128 A rows and only HALF of the B
   // tile, the even CTA issues the UMMAs, and each CTA's TMEM receives its own
@@ -92,7 +105,9 @@ struct GemmCfg {
   static constexpr bool B_GATHER = (BL_ == MN_GATHER);
   static constexpr bool GATHER = A_GATHER || B_GATHER;
   static constexpr int GATHER_WARPS = GATHER ? 4 : 0;
-  static constexpr int THREADS = 64 + 32 * (EPI_WARPS + GATHER_WARPS);
+  // DYN: one more warp hands out the units and clears their dependencies
+  static constexpr int SCHED_WARP = 2 + EPI_WARPS + GATHER_WARPS;
+  static constexpr int THREADS = 64 + 32 * (EPI_WARPS + GATHER_WARPS + (DYN_ ? 1 : 0));
   static constexpr int GATHER_LAG = STAGES_ - 2;  // stages a gather thread keeps in flight
   static_assert(!GATHER || GATHER_LAG >= 1, "gathers need >= 3 stages");
   static_assert(BL_ != KMAJ_GATHER, "B is gathered only MN-major");
@@ -131,6 +146,8 @@ struct GemmCfg {
   static_assert(!B_MN || BN % 64 == 0, "MN-major B needs 64-wide groups");
   static_assert(2 * BN <= kTmemCols, "two accumulators must fit TMEM");
   static_assert(SMEM_BYTES <= 227 * 1024 - 8 * 1024, "dynamic + static shared memory per CTA");
+  static_assert(!DYN || (PAIR && !GATHER && SCH_ == RAGGED_M), "dynamic units: CTA-pair TMA GEMMs");
+  static_assert(!DYN || STAGES_ + 2 + 2 + 1 < 32, "unit ring deeper than any role's lag");
 };
 
 struct TileInfo {
@@ -227,6 +244,67 @@ __device__ __forceinline__ int num_nblocks(const GemmArgs& a) {
   if (C::SWIGLU_B) return (a.inter + C::BN / 2 - 1) / (C::BN / 2);
   return (a.N + C::BN - 1) / C::BN;
 }
+
+// 256-row block of a unit (the group's earlier blocks + its m-block pair): the
+// index of the dependency flag between a producer and a consumer GEMM over the
+// same groups (both see the same blocks: units = blocks x n-blocks per group).
+template <class C>
+__device__ __forceinline__ int dep_pair(const GemmArgs& a, const SmemTables& T, int g, int mb) {
+  return T.tile_prefix[g] / num_nblocks<C>(a) + (mb >> 1);
+}
+
+// ---------------------------------------------------------------- dynamic units
+// The leader CTA's producer thread takes unit ids from a global counter and
+// publishes them in order to a ring in both CTAs of the pair (own shared
+// memory, and the peer's through the cluster); every role of both CTAs reads
+// the same sequence from its own ring.  No role lags the producer's thread by
+// more than its look-ahead (2 ids), the stage ring (at most STAGES units of one
+// k-block), the two accumulators and the unit in hand, so kSchedRing slots are
+// never overwritten while a role still has to read them.  An id >= total ends
+// every role's loop.
+constexpr int kSchedRing = 32;
+
+struct UnitRing {
+  int id[kSchedRing];
+  uint64_t full[kSchedRing];
+  uint64_t dep_ok[kSchedRing];  // this CTA's scheduler: the unit's dependency is met
+  int prod_pos;                 // units the producer has started (the scheduler stays near it)
+};
+
+__device__ __forceinline__ void ring_publish(UnitRing& R, int pos, int t) {
+  const int s = pos % kSchedRing;
+  R.id[s] = t;
+  mbar_arrive(smem_u32(&R.full[s]));
+  st_shared_cluster_u32(mapa_shared(smem_u32(&R.id[s]), 1), (uint32_t)t);
+  mbar_arrive_release_cluster(mapa_shared(smem_u32(&R.full[s]), 1));
+}
+
+// Next unit id of this role (pos counts its reads); total on abort.
+__device__ __forceinline__ int ring_read(UnitRing& R, int& pos, int total, volatile int* abort_flag,
+                                        int* status) {
+  const int s = pos % kSchedRing;
+  const uint32_t par = (uint32_t)(pos / kSchedRing) & 1u;
+  ++pos;
+  if (!mbar_wait_cluster(smem_u32(&R.full[s]), par, abort_flag, status)) return total;
+  return *reinterpret_cast<volatile int*>(&R.id[s]);
+}
+
+// A role's walk over its units: static round-robin, or the ring.
+template <bool DYN>
+struct UnitWalk {
+  UnitRing* ring;
+  int pos, ustep, total;
+  volatile int* abort_flag;
+  int* status;
+  __device__ __forceinline__ int first(int unit0) {
+    if constexpr (DYN) return ring_read(*ring, pos, total, abort_flag, status);
+    else return unit0;
+  }
+  __device__ __forceinline__ int next(int t) {
+    if constexpr (DYN) return ring_read(*ring, pos, total, abort_flag, status);
+    else return t + ustep;
+  }
+};
 
 // Work unit t -> tile.  Without PAIR a unit is one tile (m-block fastest).  With
 // PAIR a unit is a pair of adjacent m-blocks of one (group, n-block); CTA rank r
@@ -805,6 +883,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   __shared__ __align__(8) uint64_t tempty_bar[2];
   __shared__ __align__(8) uint64_t drain_bar;
   __shared__ SmemTables T;
+  __shared__ UnitRing ring;  // DYN only
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -825,6 +904,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       mbar_init(smem_u32(&tempty_bar[b]), C::TEMPTY_ARRIVALS);
     }
     mbar_init(smem_u32(&drain_bar), 1);
+    if constexpr (C::DYN) {
+      for (int s = 0; s < kSchedRing; ++s) {
+        mbar_init(smem_u32(&ring.full[s]), 1);
+        mbar_init(smem_u32(&ring.dep_ok[s]), 1);
+      }
+      ring.prod_pos = 0;
+    }
     T.abort_flag = 0;
     fence_mbar_init();
   }
@@ -869,14 +955,33 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   const bool leader = rank == 0;  // PAIR: the CTA whose thread issues the pair's UMMAs
   const int unit0 = blockIdx.x / C::CL;
   const int ustep = gridDim.x / C::CL;
+  // producer side of a cross-kernel overlap: every CTA is running, so the
+  // consumer grid may start on the SMs this grid frees
+  if (a.dep_signal && threadIdx.x == 0) griddep_launch_dependents();
 
   if (warp == 0) {
     // ================= TMA producer =================
     int stage = 0;
     uint32_t phase = 0;
     uint32_t filled = 0, fill_parity = 0;  // per stage: armed at least once, parity of last fill
-    for (int t = unit0; t < total && !*abort_flag; t += ustep) {
+    UnitWalk<C::DYN> uw{&ring, 0, ustep, total, abort_flag, a.status};
+    for (int t = uw.first(unit0); t < total && !*abort_flag; t = uw.next(t)) {
       const TileInfo ti = decode_tile<C>(a, T, t, rank);
+      if constexpr (C::DYN) {
+        // the scheduler warp has seen the unit's dependency met (its acquire,
+        // released to this CTA through dep_ok); the proxy fence then orders this
+        // thread's tensor loads after it.  This thread takes no other fence: a
+        // release here would wait for its own copies in flight.
+        const int j = uw.pos - 1;
+        if (lane == 0) *reinterpret_cast<volatile int*>(&ring.prod_pos) = uw.pos;
+        if (a.dep_flags) {
+          if (!mbar_wait(smem_u32(&ring.dep_ok[j % kSchedRing]), (uint32_t)(j / kSchedRing) & 1u,
+                         abort_flag, a.status))
+            break;
+          if (lane == 0) fence_proxy_async_global();
+        }
+        __syncwarp();
+      }
       const int n0 = C::SWIGLU_B ? ti.nb * (C::BN / 2) : ti.nb * C::BN;
       const int m0 = ti.mb * BM;
       bool ok = true;
@@ -978,7 +1083,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     // with PAIR the odd CTA issues nothing: the even CTA's UMMAs cover both
-    for (int t = unit0; t < total && !*abort_flag && (!C::PAIR || leader); t += ustep) {
+    UnitWalk<C::DYN> uw{&ring, 0, ustep, total, abort_flag, a.status};
+    for (int t = (!C::PAIR || leader) ? uw.first(unit0) : total; t < total && !*abort_flag;
+         t = uw.next(t)) {
       const TileInfo ti = decode_tile<C>(a, T, t, rank);
       if (!mbar_wait(smem_u32(&tempty_bar[acc]), acc_phase ^ 1, abort_flag, a.status)) break;
       tc_fence_after();
@@ -1032,6 +1139,52 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       }
       __syncwarp();
     }
+  } else if (C::DYN && warp == C::SCHED_WARP) {
+    // ================= scheduler (DYN) =================
+    // Leader CTA: takes unit ids from the global counter and publishes them to
+    // both CTAs' rings, staying a few units ahead of its producer.  Both CTAs:
+    // walks its own ring and, per unit, waits until the producer kernel's count
+    // for the unit's 256-row block is complete, then clears the unit to this
+    // CTA's producer (dep_ok).  No thread of this warp issues copies, so its
+    // releases and fences wait for nothing of the data path.
+    if (lane == 0) {
+      int published = 0;
+      bool sent_end = false;
+      int pending = leader ? atomicAdd(a.sched_counter, 1) : 0;
+      int pos = 0;  // next ring position to clear
+      unsigned long long t0 = globaltimer();
+      while (!*abort_flag) {
+        if (leader && !sent_end &&
+            published < *reinterpret_cast<volatile int*>(&ring.prod_pos) + 3) {
+          ring_publish(ring, published++, pending);
+          if (pending >= total) sent_end = true;
+          else pending = atomicAdd(a.sched_counter, 1);
+          t0 = globaltimer();
+          continue;
+        }
+        // clear the next published unit
+        const int s = pos % kSchedRing;
+        const uint32_t par = (uint32_t)(pos / kSchedRing) & 1u;
+        if (mbar_test_wait_cluster(smem_u32(&ring.full[s]), par)) {
+          const int t = *reinterpret_cast<volatile int*>(&ring.id[s]);
+          if (t >= total) break;
+          if (a.dep_flags) {
+            const TileInfo ti = decode_tile<C>(a, T, t, rank);
+            if (!dep_wait(a.dep_flags + dep_pair<C>(a, T, ti.g, ti.mb), a.dep_target, abort_flag,
+                          a.status))
+              break;
+            mbar_arrive(smem_u32(&ring.dep_ok[s]));
+          }
+          ++pos;
+          t0 = globaltimer();
+        } else if (globaltimer() - t0 > kWaitLimitNs) {
+          *abort_flag = 1;
+          record_status(a.status, MOE_DEV_TIMEOUT);
+          break;
+        }
+      }
+    }
+    __syncwarp();
   } else if (C::GATHER && warp >= 2 + C::EPI_WARPS) {
     // ================= gather warps (LSU cp.async) =================
     gather_role<C>(a, T, smem_base, full_bar, empty_bar, abort_flag, warp - 2 - C::EPI_WARPS,
@@ -1054,7 +1207,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     wo.policy[1] = l2_policy(a.out_l2[1]);
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int t = unit0; t < total && !*abort_flag; t += ustep) {
+    UnitWalk<C::DYN> uw{&ring, 0, ustep, total, abort_flag, a.status};
+    for (int t = uw.first(unit0); t < total && !*abort_flag; t = uw.next(t)) {
       const TileInfo ti = decode_tile<C>(a, T, t, rank);
       if (!mbar_wait(smem_u32(&tfull_bar[acc]), acc_phase, abort_flag, a.status)) break;
       tc_fence_after();
@@ -1076,6 +1230,20 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       if (lane == 0) {
         if constexpr (C::PAIR) mbar_arrive_remote(mapa_shared(smem_u32(&tempty_bar[acc]), 0));
         else mbar_arrive(smem_u32(&tempty_bar[acc]));
+      }
+      if (a.dep_signal) {
+        // producer side: once this warp's rows of the unit are in global memory
+        // (its direct stores, and its TMA stores complete), count it on the
+        // unit's 256-row block
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) {
+          bulk_wait_all();
+          fence_proxy_async_global();
+          red_release_gpu_add(a.dep_flags + dep_pair<C>(a, T, ti.g, ti.mb), 1);
+        }
+        __syncwarp();
+        wo.inflight = 0;
       }
       if (++acc == 2) { acc = 0; acc_phase ^= 1; }
     }

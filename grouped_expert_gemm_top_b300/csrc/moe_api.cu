@@ -48,7 +48,8 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 constexpr int kDwParts = 1;  // column parts of the down data-gradient epilogue (epilogue warps / 4)
 
 struct Layout {
-  size_t status, counts, hist, psum_part, route_end, h, h_sh, fwd_end;
+  size_t status, counts, hist, psum_part, route_end, dep_fwd, h, h_sh, fwd_end;
+  size_t dep_bwd, dep_bytes;
   size_t poff, dgu, hw, dxs, dwp, dl, dlb, rwp, db_part, dgu_sh, hw_sh, dxs_sh, gu_rc,
       sh_gu_rc, total;
   int sort_blocks;
@@ -93,11 +94,16 @@ Layout make_layout(const moe_dims& d, bool bwd, bool recompute = false) {
   L.hist = o; o = align_up(o + (size_t)d.E * ((route_ctas_max + 3) / 4 * 4) * 4);
   L.psum_part = o; o = align_up(o + route_ctas_max * d.E * 4);
   L.route_end = o;
+  // cross-kernel overlap: one flag per 256-row block of the sorted (or padded)
+  // rows, then the consumer's unit counter; forward and backward each have one
+  L.dep_bytes = ((size_t)(L.S + 255 * (long long)d.E) / 256 + d.E + 2) * 4;
+  L.dep_fwd = o; o = align_up(o + L.dep_bytes);
   L.h = o; o = align_up(o + (size_t)L.S * d.I * 2);
   L.h_sh = o; o = align_up(o + (size_t)d.T * d.I_shared * 2);
   L.fwd_end = o;
   if (bwd) {
     const size_t P = (size_t)L.S_pad_max;
+    L.dep_bwd = o; o = align_up(o + L.dep_bytes);
     L.poff = o; o = align_up(o + (size_t)(d.E + 1) * 4);
     L.dgu = o; o = align_up(o + P * 2 * d.I * 2);
     L.hw = o; o = align_up(o + P * d.I * 2);
@@ -277,12 +283,14 @@ template <int STAGES, int AL, int BL, int SCH, int EPI, bool B3D, bool SWIGLU_B,
 using PairCfg = GemmCfg<256, STAGES, AL, BL, SCH, EPI, B3D, SWIGLU_B, EPI_WARPS, true, EPI_BUFS>;
 using CfgGateUp = PairCfg<5, KMAJ_GATHER, KMAJ_TILE, RAGGED_M, EPI_SWIGLU, true, true>;
 using CfgGateUpShared = PairCfg<5, KMAJ_TILE, KMAJ_TILE, RAGGED_M, EPI_SWIGLU, false, true>;
-using CfgDown = PairCfg<5, KMAJ_TILE, KMAJ_TILE, RAGGED_M, EPI_STORE, true, false>;
+// the down GEMM as the consumer of the gate/up GEMM's h, units taken as SMs free up
+using CfgDownDyn = GemmCfg<256, 5, KMAJ_TILE, KMAJ_TILE, RAGGED_M, EPI_STORE, true, false, 4, true, 3, true>;
 using CfgDownShared = PairCfg<5, KMAJ_TILE, KMAJ_TILE, RAGGED_M, EPI_STORE, false, false>;
 using CfgDgradDown =
     PairCfg<5, KMAJ_GATHER, MN_TILE, RAGGED_M, EPI_DGRAD_SWIGLU, true, false, 4 * kDwParts>;
 using CfgDgradDownShared = PairCfg<5, KMAJ_TILE, MN_TILE, RAGGED_M, EPI_DGRAD_SWIGLU, false, false>;
-using CfgDgradGateUp = PairCfg<5, KMAJ_TILE, MN_TILE, RAGGED_M, EPI_STORE, true, false>;
+// the gate/up data gradient as the consumer of the down data gradient's dgu
+using CfgDgradGateUpDyn = GemmCfg<256, 5, KMAJ_TILE, MN_TILE, RAGGED_M, EPI_STORE, true, false, 4, true, 3, true>;
 using CfgDgradGateUpShared = PairCfg<5, KMAJ_TILE, MN_TILE, RAGGED_M, EPI_STORE, false, false>;
 using CfgWgrad = PairCfg<4, MN_TILE, MN_TILE, RAGGED_K, EPI_STORE, false, false, 4, 5>;
 // Expert weight gradients: one operand resident in shared memory for experts
@@ -321,10 +329,12 @@ bool make_out_map3(CUtensorMap* m, const void* base, uint64_t inner, uint64_t ro
 }
 
 // RES: the resident-operand weight-gradient kernel (same parameters).
+// pdl: launch with programmatic stream serialisation (the consumer side of a
+// cross-kernel overlap: it may start on SMs the previous grid frees).
 template <class C, bool RES = false>
 moe_status launch_gemm(int kid, const CUtensorMap& A, const CUtensorMap& B, const CUtensorMap& D0,
                        const CUtensorMap& D1, const GemmArgs& a, long long tile_bound,
-                       cudaStream_t st) {
+                       cudaStream_t st, bool pdl = false) {
   void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, GemmArgs);
   if constexpr (RES) kern = moe::res_gemm_kernel<C>;
   else kern = moe::grouped_gemm_kernel<C>;
@@ -340,11 +350,13 @@ moe_status launch_gemm(int kid, const CUtensorMap& A, const CUtensorMap& B, cons
   }
   if constexpr (C::CL == 2) {
     // 2-CTA clusters; as many as can be resident at once (one CTA per SM)
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(C::THREADS);
     cfg.dynamicSmemBytes = C::SMEM_BYTES;
@@ -363,6 +375,7 @@ moe_status launch_gemm(int kid, const CUtensorMap& A, const CUtensorMap& B, cons
     const long long clusters = std::min<long long>(mc, (tile_bound + 1) / 2 + 1);
     if (clusters < 1) return MOE_OK;
     cfg.gridDim = dim3((unsigned)(2 * clusters));
+    if (pdl) cfg.numAttrs = 2;
     KernelScope ks(kid, st);
     if (cudaLaunchKernelEx(&cfg, kern, A, B, D0, D1, a) != cudaSuccess)
       return MOE_ERR_CUDA;
@@ -592,9 +605,12 @@ moe_status moe_permute(const moe_dims* d, const int32_t* topk_idx, int32_t* expe
 
 // Grouped gate/up GEMM + SwiGLU of the routed experts (A = token rows of x
 // gathered through the sort): gu_out [S,2I] and h_out [S,I] are each optional.
+// dep_flags (optional): count each finished unit on its 256-row block for a
+// consumer GEMM launched next (the down GEMM), and let it launch early.
 moe_status launch_gate_up(const moe_dims& d, const moe_bf16* x, const int32_t* expert_offsets,
                           const int32_t* perm_slot, const moe_bf16* w_gate_up, moe_bf16* gu_out,
-                          __nv_bfloat16* h_out, int* status, cudaStream_t st) {
+                          __nv_bfloat16* h_out, int* status, cudaStream_t st,
+                          int* dep_flags = nullptr) {
   const int H = d.H, E = d.E, I = d.I;
   const long long S = (long long)d.T * d.k;
   CUtensorMap tB;
@@ -608,6 +624,7 @@ moe_status launch_gate_up(const moe_dims& d, const moe_bf16* x, const int32_t* e
   a.gsrc = reinterpret_cast<const __nv_bfloat16*>(x); a.gld = H; a.gperm = perm_slot;
   a.gdiv = d.k; a.gsrc_rows = d.T;
   a.gu_out = reinterpret_cast<__nv_bfloat16*>(gu_out); a.h_out = h_out; a.inter = I;
+  a.dep_flags = dep_flags; a.dep_signal = dep_flags ? 1 : 0;
   return launch_gemm<CfgGateUp>(MOE_K_GATE_UP, tA, tB, tD0, tD1, a,
                                 (cdiv(S, moe::BM) + E) * cdiv(I, 128), st);
 }
@@ -654,7 +671,13 @@ moe_status moe_grouped_mlp_fwd(const moe_dims* d, const moe_bf16* x,
   __nv_bfloat16* h = at<__nv_bfloat16>(workspace, L.h);
   const int T = d->T, H = d->H, E = d->E, I = d->I;
   const long long S = L.S;
-  s = launch_gate_up(*d, x, expert_offsets, perm_slot, w_gate_up, gu_saved, h, status, st);
+  // the down GEMM starts on the SMs the gate/up GEMM frees, each unit once the
+  // gate/up GEMM has written its 256 rows of h (every n-block, both CTAs, every
+  // epilogue warp)
+  int32_t* dep = at<int32_t>(workspace, L.dep_fwd);
+  if (cudaMemsetAsync(dep, 0, L.dep_bytes, st) != cudaSuccess) return MOE_ERR_CUDA;
+  const int gu_nblocks = (I + 127) / 128;
+  s = launch_gate_up(*d, x, expert_offsets, perm_slot, w_gate_up, gu_saved, h, status, st, dep);
   if (s != MOE_OK) return s;
   {  // down grouped GEMM
     CUtensorMap tA, tB;
@@ -665,7 +688,10 @@ moe_status moe_grouped_mlp_fwd(const moe_dims* d, const moe_bf16* x,
     GemmArgs a = base_args(status);
     a.N = H; a.K = I; a.G = E; a.offsets = expert_offsets; a.cap = d->capacity;
     a.d = reinterpret_cast<__nv_bfloat16*>(y_perm); a.ldd = H;
-    s = launch_gemm<CfgDown>(MOE_K_DOWN, tA, tB, tD, tD, a, (cdiv(S, moe::BM) + E) * cdiv(H, 256), st);
+    a.dep_flags = dep; a.dep_target = gu_nblocks * CfgGateUp::EPI_WARPS * 2;
+    a.sched_counter = dep + (L.dep_bytes / 4 - 1);
+    s = launch_gemm<CfgDownDyn>(MOE_K_DOWN, tA, tB, tD, tD, a, (cdiv(S, moe::BM) + E) * cdiv(H, 256), st,
+                                /*pdl=*/true);
     if (s != MOE_OK) return s;
   }
   if (d->I_shared > 0) {
@@ -776,6 +802,10 @@ moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_
 
   const auto* gob = reinterpret_cast<const __nv_bfloat16*>(grad_out);
   const auto* xb = reinterpret_cast<const __nv_bfloat16*>(x);
+  // the gate/up data gradient starts on the SMs the down data gradient frees,
+  // each unit once its 256 rows of dgu are written
+  int32_t* dep = at<int32_t>(workspace, L.dep_bwd);
+  if (cudaMemsetAsync(dep, 0, L.dep_bytes, st) != cudaSuccess) return MOE_ERR_CUDA;
   {  // down-projection data gradient + SwiGLU backward (+ dw partials); A = grad_out rows
     CUtensorMap tB;
     if (!make_map3(&tB, w_down, I, H, E, 64, 64)) return MOE_ERR_CUDA;
@@ -786,6 +816,7 @@ moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_
     a.poff_out = poff;
     a.inter = I; a.gu_saved = reinterpret_cast<const __nv_bfloat16*>(gu_saved);
     a.perm_slot = perm_slot; a.slot_w = topk_w; a.dgu_out = dgu; a.hw_out = hw; a.dw_part = dwp;
+    a.dep_flags = dep; a.dep_signal = 1;
     CUtensorMap tD0, tD1;
     if (!make_out_map(&tD0, dgu, 2LL * I, P) || !make_out_map(&tD1, hw, I, P)) return MOE_ERR_CUDA;
     s = launch_gemm<CfgDgradDown>(MOE_K_DGRAD_DOWN, tA, tB, tD0, tD1, a, cdiv(P, moe::BM) * L.nNB_I, st);
@@ -798,9 +829,12 @@ moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_
     GemmArgs a = base_args(status);
     a.N = H; a.K = 2 * I; a.G = E; a.offsets = expert_offsets; a.cap = d->capacity; a.padded = 1;
     a.d = dxs; a.ldd = H;
+    a.dep_flags = dep; a.dep_target = L.nNB_I * CfgDgradDown::EPI_WARPS * 2;
+    a.sched_counter = dep + (L.dep_bytes / 4 - 1);
     CUtensorMap tD;
     if (!make_out_map(&tD, dxs, H, P)) return MOE_ERR_CUDA;
-    s = launch_gemm<CfgDgradGateUp>(MOE_K_DGRAD_GATE_UP, tA, tB, tD, tD, a, cdiv(P, moe::BM) * cdiv(H, 256), st);
+    s = launch_gemm<CfgDgradGateUpDyn>(MOE_K_DGRAD_GATE_UP, tA, tB, tD, tD, a,
+                                       cdiv(P, moe::BM) * cdiv(H, 256), st, /*pdl=*/true);
     if (s != MOE_OK) return s;
   }
   __nv_bfloat16* dxs_sh = nullptr;

@@ -85,8 +85,17 @@ struct GemmArgs {
 };
 
 template <int BN_, int STAGES_, int AL_, int BL_, int SCH_, int EPI_, bool B3D_, bool SWIGLU_B_,
-          int EPI_WARPS_ = 4, bool PAIR_ = false, int EPI_BUFS_ = 3, bool DYN_ = false>
+          int EPI_WARPS_ = 4, bool PAIR_ = false, int EPI_BUFS_ = 3, bool DYN_ = false,
+          bool WIDE_ = false>
 struct GemmCfg {
+  // WIDE: a unit is two adjacent n-blocks that share every A stage: each stage
+  // carries two B tiles, and the two TMEM accumulators (all 512 columns) take
+  // one n-block each, so the A operand enters the SM once per 2 x BN columns
+  // instead of once per BN.  The accumulators are then not double-buffered
+  // across units: the next unit's UMMAs wait until the epilogue has drained
+  // both.  (Gate/up GEMM with SwiGLU only.)
+  static constexpr bool WIDE = WIDE_;
+  static constexpr int NSUB = WIDE ? 2 : 1;  // n-blocks (accumulators) per unit
   // DYN: units handed out dynamically (consumer side of a cross-kernel overlap)
   static constexpr bool DYN = DYN_;
   // PAIR: 2-CTA clusters computing one 256 x BN tile with CTA-pair UMMAs
@@ -122,7 +131,7 @@ struct GemmCfg {
   static constexpr bool SWIGLU_B = SWIGLU_B_;
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_ROWS = PAIR ? BN / 2 : BN;  // B rows (N extent) staged by this CTA
-  static constexpr int B_BYTES = B_ROWS * BK * 2;
+  static constexpr int B_BYTES = NSUB * B_ROWS * BK * 2;  // NSUB tiles of B_ROWS rows
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   // K-major B is loaded in boxes of at most 128 rows.
   static constexpr int B_BOX_ROWS = BN < 128 ? BN : 128;
@@ -148,6 +157,8 @@ struct GemmCfg {
   static_assert(SMEM_BYTES <= 227 * 1024 - 8 * 1024, "dynamic + static shared memory per CTA");
   static_assert(!DYN || (PAIR && !GATHER && SCH_ == RAGGED_M), "dynamic units: CTA-pair TMA GEMMs");
   static_assert(!DYN || STAGES_ + 2 + 2 + 1 < 32, "unit ring deeper than any role's lag");
+  static_assert(!WIDE || (PAIR && BL_ == KMAJ_TILE && EPI_ == EPI_SWIGLU && SWIGLU_B_ && !DYN_),
+                "wide units: the CTA-pair gate/up GEMM");
 };
 
 struct TileInfo {
@@ -239,10 +250,11 @@ __device__ __forceinline__ void build_group_tables(const GemmArgs& a, SmemTables
   }
 }
 
+// n-blocks of a group's units (WIDE: pairs of BN-column blocks)
 template <class C>
 __device__ __forceinline__ int num_nblocks(const GemmArgs& a) {
-  if (C::SWIGLU_B) return (a.inter + C::BN / 2 - 1) / (C::BN / 2);
-  return (a.N + C::BN - 1) / C::BN;
+  constexpr int W = C::SWIGLU_B ? C::NSUB * C::BN / 2 : C::NSUB * C::BN;
+  return ((C::SWIGLU_B ? a.inter : a.N) + W - 1) / W;
 }
 
 // 256-row block of a unit (the group's earlier blocks + its m-block pair): the
@@ -432,9 +444,35 @@ __device__ __forceinline__ void block_range(int cpart, int nparts, int nblk, int
   if (g1 > inside) g1 = inside;
 }
 
-// silu(g) = g * sigmoid(g), with CUDA's fast exponential and division intrinsics.
+// sigmoid(g) with CUDA's fast exponential and division intrinsics.
 __device__ __forceinline__ float sigmoid_f(float g) { return __fdividef(1.0f, 1.0f + __expf(-g)); }
-__device__ __forceinline__ float silu_f(float g) { return g * sigmoid_f(g); }
+
+// 2^x and 1/x on the special-function unit (PTX ex2.approx / rcp.approx).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// sigmoid of two values with one reciprocal: with d = 1 + e^(-g) = 1 +
+// 2^(-g log2 e), 1/d0 = d1 / (d0 d1) and 1/d1 = d0 / (d0 d1).  The forward
+// epilogue is bound by the special-function unit (an exponential and a
+// reciprocal per element); sharing the reciprocal takes 1.5 operations per
+// element instead of 2.  Each exponent is capped at 2^62 so that the product
+// stays finite: for g < -43 the sigmoid comes out as about 2^-62 instead of
+// e^g (both below 1e-18).  Relative error a few fp32 ulps.
+__device__ __forceinline__ float2 sigmoid2_f(float g0, float g1) {
+  constexpr float kLog2e = 1.4426950408889634f;
+  const float d0 = 1.0f + ex2_approx(fminf(-g0 * kLog2e, 62.0f));
+  const float d1 = 1.0f + ex2_approx(fminf(-g1 * kLog2e, 62.0f));
+  const float r = rcp_approx(d0 * d1);
+  return make_float2(d1 * r, d0 * r);
+}
 
 // fp32 output (split-K router partials).  RAGGED_K: D is the group's (split's)
 // M x N slice, map tmD0 3-D [groups][M][N] with 16x32 fp32 boxes.
@@ -499,7 +537,9 @@ __device__ void epilogue_swiglu(const GemmArgs& a, const TileInfo& ti, uint32_t 
   const int I = a.inter;
   constexpr int HALF = C::BN / 2;
   const int n0 = ti.nb * HALF;
-  const bool keep_gu = a.gu_out != nullptr;
+  // (g, u stores need three staging buffers per warp; configs with fewer
+  // serve the inference forward, which keeps h only)
+  const bool keep_gu = C::EPI_BUFS >= 3 && a.gu_out != nullptr;
   const bool keep_h = a.h_out != nullptr;  // a backward recomputing g, u needs no h
   int g0, g1;
   block_range(cpart, nparts, HALF / 64, n0, I, g0, g1);
@@ -508,9 +548,11 @@ __device__ void epilogue_swiglu(const GemmArgs& a, const TileInfo& ti, uint32_t 
     const int j = n0 + gi * 64;
     uint32_t bg = 0, bu = 0, bh = 0;
     if (warp_full) {
-      if (keep_gu) {
-        bg = stage_acquire<3>(w);
-        bu = stage_acquire<1>(w);  // inside the three just made free
+      if constexpr (C::EPI_BUFS >= 3) {
+        if (keep_gu) {
+          bg = stage_acquire<3>(w);
+          bu = stage_acquire<1>(w);  // inside the three just made free
+        }
       }
       if (keep_h) bh = stage_acquire<1>(w);
     }
@@ -520,32 +562,40 @@ __device__ void epilogue_swiglu(const GemmArgs& a, const TileInfo& ti, uint32_t 
       tmem_ld32_issue(tacc + gi * 64 + h * 32, g);
       tmem_ld32_issue(tacc + HALF + gi * 64 + h * 32, u);
       tmem_ld_wait2(g, u);
+      // each output is formed only when it is kept (the conversions and the
+      // special-function work are a large share of this epilogue)
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        uint32_t pg[4], pu[4], ph[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int e = 8 * q + 2 * i;
-          const float ga = __uint_as_float(g[e]), gb = __uint_as_float(g[e + 1]);
-          const float ua = __uint_as_float(u[e]), ub = __uint_as_float(u[e + 1]);
-          pg[i] = pack_bf16x2(ga, gb);
-          pu[i] = pack_bf16x2(ua, ub);
-          ph[i] = pack_bf16x2(silu_f(ga) * ua, silu_f(gb) * ub);
-        }
         const int pc = 4 * h + q;  // piece within the 64-column block
-        if (warp_full) {
-          if (keep_gu) {
+        const int col = j + 8 * pc;
+        if (keep_gu) {
+          uint32_t pg[4], pu[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int e = 8 * q + 2 * i;
+            pg[i] = pack_bf16x2(__uint_as_float(g[e]), __uint_as_float(g[e + 1]));
+            pu[i] = pack_bf16x2(__uint_as_float(u[e]), __uint_as_float(u[e + 1]));
+          }
+          if (warp_full) {
             put128(bg, w.lane, pc, pg[0], pg[1], pg[2], pg[3]);
             put128(bu, w.lane, pc, pu[0], pu[1], pu[2], pu[3]);
-          }
-          if (keep_h) put128(bh, w.lane, pc, ph[0], ph[1], ph[2], ph[3]);
-        } else if (valid) {
-          const int col = j + 8 * pc;
-          if (keep_gu) {
+          } else if (valid) {
             st_global_16(a.gu_out + r * (2LL * I) + col, pg[0], pg[1], pg[2], pg[3]);
             st_global_16(a.gu_out + r * (2LL * I) + I + col, pu[0], pu[1], pu[2], pu[3]);
           }
-          if (keep_h) st_global_16(a.h_out + r * (long long)I + col, ph[0], ph[1], ph[2], ph[3]);
+        }
+        if (keep_h) {
+          uint32_t ph[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int e = 8 * q + 2 * i;
+            const float ga = __uint_as_float(g[e]), gb = __uint_as_float(g[e + 1]);
+            const float2 sg = sigmoid2_f(ga, gb);
+            ph[i] = pack_bf16x2(ga * sg.x * __uint_as_float(u[e]),
+                                gb * sg.y * __uint_as_float(u[e + 1]));
+          }
+          if (warp_full) put128(bh, w.lane, pc, ph[0], ph[1], ph[2], ph[3]);
+          else if (valid) st_global_16(a.h_out + r * (long long)I + col, ph[0], ph[1], ph[2], ph[3]);
         }
       }
     }
@@ -982,7 +1032,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         }
         __syncwarp();
       }
-      const int n0 = C::SWIGLU_B ? ti.nb * (C::BN / 2) : ti.nb * C::BN;
+      const int n0 = C::SWIGLU_B ? ti.nb * (C::NSUB * C::BN / 2) : ti.nb * C::BN;
       const int m0 = ti.mb * BM;
       bool ok = true;
       for (int kb = 0; kb < ti.kblocks; ++kb) {
@@ -1021,11 +1071,17 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         }
         // ---- B
         if constexpr (C::PAIR && C::BL == KMAJ_TILE) {
-          // this CTA's half of the B tile: 128 rows (SwiGLU: rank 0 gate, rank 1 up)
+          // this CTA's half of the B tile: 128 rows (SwiGLU: rank 0 gate, rank 1
+          // up); WIDE: the halves of two tiles, the second 128 columns further
           if (lane == 0) {
-            const int nc = C::SWIGLU_B ? (rank == 0 ? n0 : a.inter + n0) : n0 + rank * 128;
-            if constexpr (C::B3D) tma_load_3d_pair(sB, &tmB, fbp, kc, nc, ti.g);
-            else tma_load_2d_pair(sB, &tmB, fbp, kx, nc);
+#pragma unroll
+            for (int b = 0; b < C::NSUB; ++b) {
+              const int nc = C::SWIGLU_B ? (rank == 0 ? n0 : a.inter + n0) + 128 * b
+                                         : n0 + rank * 128;
+              const uint32_t dst = sB + b * (C::B_ROWS * BK * 2);
+              if constexpr (C::B3D) tma_load_3d_pair(dst, &tmB, fbp, kc, nc, ti.g);
+              else tma_load_2d_pair(dst, &tmB, fbp, kx, nc);
+            }
           }
         } else if constexpr (C::PAIR && C::BL == MN_TILE) {
           // this CTA's half: two 64-wide N groups
@@ -1088,6 +1144,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
          t = uw.next(t)) {
       const TileInfo ti = decode_tile<C>(a, T, t, rank);
       if (!mbar_wait(smem_u32(&tempty_bar[acc]), acc_phase ^ 1, abort_flag, a.status)) break;
+      // WIDE: the unit takes both accumulators
+      if (C::WIDE && !mbar_wait(smem_u32(&tempty_bar[1]), acc_phase ^ 1, abort_flag, a.status)) break;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + acc * C::BN;
       bool ok = true;
@@ -1105,6 +1163,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                                         : smem_desc_sw128(sB + kk * 32, 16, 1024);
             if constexpr (C::PAIR) umma_bf16_pair(d_tmem, ad, bd, C::IDESC, (kb | kk) != 0 ? 1u : 0u);
             else umma_bf16(d_tmem, ad, bd, C::IDESC, (kb | kk) != 0 ? 1u : 0u);
+            if constexpr (C::WIDE) {
+              // the second n-block: same A, the next B tile, the other accumulator
+              const uint64_t bd1 = smem_desc_sw128(sB + C::B_ROWS * 128 + kk * 32, 16, 1024);
+              umma_bf16_pair(d_tmem + C::BN, ad, bd1, C::IDESC, (kb | kk) != 0 ? 1u : 0u);
+            }
           }
           if constexpr (C::PAIR) umma_commit_pair(smem_u32(&empty_bar[stage]));
           else umma_commit(smem_u32(&empty_bar[stage]));
@@ -1114,19 +1177,24 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       }
       if (!ok) break;
       if (lane == 0) {
-        if constexpr (C::PAIR) {
-          if (ti.kblocks > 0) umma_commit_pair(smem_u32(&tfull_bar[acc]));
-          else {
-            mbar_arrive(smem_u32(&tfull_bar[acc]));
-            mbar_arrive_remote(mapa_shared(smem_u32(&tfull_bar[acc]), 1));
+#pragma unroll
+        for (int sub = 0; sub < C::NSUB; ++sub) {
+          const int ab = C::WIDE ? sub : acc;
+          if constexpr (C::PAIR) {
+            if (ti.kblocks > 0) umma_commit_pair(smem_u32(&tfull_bar[ab]));
+            else {
+              mbar_arrive(smem_u32(&tfull_bar[ab]));
+              mbar_arrive_remote(mapa_shared(smem_u32(&tfull_bar[ab]), 1));
+            }
+          } else {
+            if (ti.kblocks > 0) umma_commit(smem_u32(&tfull_bar[ab]));
+            else mbar_arrive(smem_u32(&tfull_bar[ab]));
           }
-        } else {
-          if (ti.kblocks > 0) umma_commit(smem_u32(&tfull_bar[acc]));
-          else mbar_arrive(smem_u32(&tfull_bar[acc]));
         }
       }
       __syncwarp();
-      if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+      if (C::WIDE) acc_phase ^= 1;
+      else if (++acc == 2) { acc = 0; acc_phase ^= 1; }
     }
     if (*abort_flag && (!C::PAIR || leader)) {
       // wait (bounded) for UMMAs already issued before TMEM is released
@@ -1209,43 +1277,50 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     uint32_t acc_phase = 0;
     UnitWalk<C::DYN> uw{&ring, 0, ustep, total, abort_flag, a.status};
     for (int t = uw.first(unit0); t < total && !*abort_flag; t = uw.next(t)) {
-      const TileInfo ti = decode_tile<C>(a, T, t, rank);
-      if (!mbar_wait(smem_u32(&tfull_bar[acc]), acc_phase, abort_flag, a.status)) break;
-      tc_fence_after();
-      const uint32_t tacc = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * C::BN;
-      if (ti.phantom) {
-        // pair slot past the group's last tile: nothing to store
-      } else if constexpr (C::EPI == EPI_STORE_F32)
-        epilogue_store_f32<C>(a, ti, tacc, row_in_tile, wo, &tmD0, cpart, nparts);
-      else if constexpr (C::EPI == EPI_SWIGLU)
-        epilogue_swiglu<C>(a, ti, tacc, row_in_tile, wo, &tmD0, &tmD1, cpart, nparts);
-      else if constexpr (C::EPI == EPI_STORE)
-        epilogue_store<C>(a, ti, tacc, row_in_tile, wo, &tmD0, cpart, nparts);
-      else
-        epilogue_dgrad_swiglu<C>(a, T, ti, tacc, row_in_tile, wo, &tmD0, &tmD1, cpart, nparts);
-      // the accumulator's TMEM has been read: one arrival per warp (PAIR: on the
-      // even CTA's barrier, whose thread overwrites both CTAs' accumulators)
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        if constexpr (C::PAIR) mbar_arrive_remote(mapa_shared(smem_u32(&tempty_bar[acc]), 0));
-        else mbar_arrive(smem_u32(&tempty_bar[acc]));
-      }
-      if (a.dep_signal) {
-        // producer side: once this warp's rows of the unit are in global memory
-        // (its direct stores, and its TMA stores complete), count it on the
-        // unit's 256-row block
-        __threadfence();
+      const TileInfo tu = decode_tile<C>(a, T, t, rank);
+      bool ok = true;
+      // WIDE: the unit's n-blocks one after the other, accumulator 0 then 1
+      for (int sub = 0; sub < C::NSUB; ++sub) {
+        TileInfo ti = tu;
+        if constexpr (C::WIDE) ti.nb = 2 * tu.nb + sub;
+        if (!mbar_wait(smem_u32(&tfull_bar[acc]), acc_phase, abort_flag, a.status)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t tacc = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * C::BN;
+        if (ti.phantom) {
+          // pair slot past the group's last tile: nothing to store
+        } else if constexpr (C::EPI == EPI_STORE_F32)
+          epilogue_store_f32<C>(a, ti, tacc, row_in_tile, wo, &tmD0, cpart, nparts);
+        else if constexpr (C::EPI == EPI_SWIGLU)
+          epilogue_swiglu<C>(a, ti, tacc, row_in_tile, wo, &tmD0, &tmD1, cpart, nparts);
+        else if constexpr (C::EPI == EPI_STORE)
+          epilogue_store<C>(a, ti, tacc, row_in_tile, wo, &tmD0, cpart, nparts);
+        else
+          epilogue_dgrad_swiglu<C>(a, T, ti, tacc, row_in_tile, wo, &tmD0, &tmD1, cpart, nparts);
+        // the accumulator's TMEM has been read: one arrival per warp (PAIR: on the
+        // even CTA's barrier, whose thread overwrites both CTAs' accumulators)
+        tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          bulk_wait_all();
-          fence_proxy_async_global();
-          red_release_gpu_add(a.dep_flags + dep_pair<C>(a, T, ti.g, ti.mb), 1);
+          if constexpr (C::PAIR) mbar_arrive_remote(mapa_shared(smem_u32(&tempty_bar[acc]), 0));
+          else mbar_arrive(smem_u32(&tempty_bar[acc]));
         }
-        __syncwarp();
-        wo.inflight = 0;
+        if (a.dep_signal) {
+          // producer side: once this warp's rows of the unit are in global memory
+          // (its direct stores, and its TMA stores complete), count it on the
+          // unit's 256-row block
+          __threadfence();
+          __syncwarp();
+          if (lane == 0) {
+            bulk_wait_all();
+            fence_proxy_async_global();
+            red_release_gpu_add(a.dep_flags + dep_pair<C>(a, T, ti.g, ti.mb), 1);
+          }
+          __syncwarp();
+          wo.inflight = 0;
+        }
+        if (++acc == 2) { acc = 0; acc_phase ^= 1; }
       }
-      if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+      if (!ok) break;
     }
     // every TMA store must have completed before the CTA exits
     if (lane == 0) bulk_wait_all();

@@ -282,6 +282,10 @@ template <int STAGES, int AL, int BL, int SCH, int EPI, bool B3D, bool SWIGLU_B,
           int EPI_BUFS = 3>
 using PairCfg = GemmCfg<256, STAGES, AL, BL, SCH, EPI, B3D, SWIGLU_B, EPI_WARPS, true, EPI_BUFS>;
 using CfgGateUp = PairCfg<5, KMAJ_GATHER, KMAJ_TILE, RAGGED_M, EPI_SWIGLU, true, true>;
+// the inference gate/up GEMM (h only): units of two n-blocks that share every
+// token-row stage (48 KB a stage: 4 stages and one staging buffer a warp fit)
+using CfgGateUpWide =
+    GemmCfg<256, 4, KMAJ_GATHER, KMAJ_TILE, RAGGED_M, EPI_SWIGLU, true, true, 4, true, 1, false, true>;
 using CfgGateUpShared = PairCfg<5, KMAJ_TILE, KMAJ_TILE, RAGGED_M, EPI_SWIGLU, false, true>;
 // the down GEMM as the consumer of the gate/up GEMM's h, units taken as SMs free up
 using CfgDownDyn = GemmCfg<256, 5, KMAJ_TILE, KMAJ_TILE, RAGGED_M, EPI_STORE, true, false, 4, true, 3, true>;
@@ -607,6 +611,15 @@ moe_status moe_permute(const moe_dims* d, const int32_t* topk_idx, int32_t* expe
 // gathered through the sort): gu_out [S,2I] and h_out [S,I] are each optional.
 // dep_flags (optional): count each finished unit on its 256-row block for a
 // consumer GEMM launched next (the down GEMM), and let it launch early.
+// Epilogue passes of the gate/up GEMM per 256-row block (each passes once per
+// epilogue warp and CTA of the pair): the consumer's dependency target.
+bool gate_up_wide(const moe_bf16* gu_out) { return gu_out == nullptr; }
+int gate_up_block_passes(const moe_dims& d, const moe_bf16* gu_out) {
+  const int sub = (int)(gate_up_wide(gu_out) ? 2 * cdiv(d.I, 256) : cdiv(d.I, 128));
+  return sub * CfgGateUp::EPI_WARPS * 2;
+}
+static_assert(CfgGateUp::EPI_WARPS == CfgGateUpWide::EPI_WARPS, "one dependency count");
+
 moe_status launch_gate_up(const moe_dims& d, const moe_bf16* x, const int32_t* expert_offsets,
                           const int32_t* perm_slot, const moe_bf16* w_gate_up, moe_bf16* gu_out,
                           __nv_bfloat16* h_out, int* status, cudaStream_t st,
@@ -625,6 +638,9 @@ moe_status launch_gate_up(const moe_dims& d, const moe_bf16* x, const int32_t* e
   a.gdiv = d.k; a.gsrc_rows = d.T;
   a.gu_out = reinterpret_cast<__nv_bfloat16*>(gu_out); a.h_out = h_out; a.inter = I;
   a.dep_flags = dep_flags; a.dep_signal = dep_flags ? 1 : 0;
+  if (gate_up_wide(gu_out))
+    return launch_gemm<CfgGateUpWide>(MOE_K_GATE_UP, tA, tB, tD0, tD1, a,
+                                      (cdiv(S, moe::BM) + E) * cdiv(I, 256), st);
   return launch_gemm<CfgGateUp>(MOE_K_GATE_UP, tA, tB, tD0, tD1, a,
                                 (cdiv(S, moe::BM) + E) * cdiv(I, 128), st);
 }
@@ -676,7 +692,6 @@ moe_status moe_grouped_mlp_fwd(const moe_dims* d, const moe_bf16* x,
   // epilogue warp)
   int32_t* dep = at<int32_t>(workspace, L.dep_fwd);
   if (cudaMemsetAsync(dep, 0, L.dep_bytes, st) != cudaSuccess) return MOE_ERR_CUDA;
-  const int gu_nblocks = (I + 127) / 128;
   s = launch_gate_up(*d, x, expert_offsets, perm_slot, w_gate_up, gu_saved, h, status, st, dep);
   if (s != MOE_OK) return s;
   {  // down grouped GEMM
@@ -688,7 +703,7 @@ moe_status moe_grouped_mlp_fwd(const moe_dims* d, const moe_bf16* x,
     GemmArgs a = base_args(status);
     a.N = H; a.K = I; a.G = E; a.offsets = expert_offsets; a.cap = d->capacity;
     a.d = reinterpret_cast<__nv_bfloat16*>(y_perm); a.ldd = H;
-    a.dep_flags = dep; a.dep_target = gu_nblocks * CfgGateUp::EPI_WARPS * 2;
+    a.dep_flags = dep; a.dep_target = gate_up_block_passes(*d, gu_saved);
     a.sched_counter = dep + (L.dep_bytes / 4 - 1);
     s = launch_gemm<CfgDownDyn>(MOE_K_DOWN, tA, tB, tD, tD, a, (cdiv(S, moe::BM) + E) * cdiv(H, 256), st,
                                 /*pdl=*/true);

@@ -108,8 +108,12 @@ struct GemmCfg {
   // staging buffers per epilogue warp = TMA stores it keeps in flight; the
   // weight-gradient GEMMs, whose output is most of their traffic, need more
   static constexpr int EPI_BUFS = EPI_BUFS_;
-  // one staging buffer: 32 rows x 64 bf16 columns, or 32 rows x 16 fp32 columns
-  static constexpr int EPI_BUF_BYTES = EPI_ == EPI_STORE_F32 ? 2048 : 4096;
+  // bf16 columns of a staging block: 64 (128-byte rows), or 32 (64-byte rows)
+  // for the wide gate/up GEMM with 8 epilogue warps, whose 48 KB stages leave
+  // room for one 2 KB block a warp
+  static constexpr int EPI_COLS = (WIDE_ && EPI_WARPS_ == 8) ? 32 : 64;
+  // one staging buffer: 32 rows x EPI_COLS bf16 columns, or 32 rows x 16 fp32 columns
+  static constexpr int EPI_BUF_BYTES = EPI_ == EPI_STORE_F32 ? 2048 : EPI_COLS * 64;
   static constexpr bool A_GATHER = (AL_ == KMAJ_GATHER || AL_ == MN_GATHER);
   static constexpr bool B_GATHER = (BL_ == MN_GATHER);
   static constexpr bool GATHER = A_GATHER || B_GATHER;
@@ -609,6 +613,60 @@ __device__ void epilogue_swiglu(const GemmArgs& a, const TileInfo& ti, uint32_t 
   }
 }
 
+// Gate/up epilogue of the wide inference GEMM with 8 epilogue warps: h only,
+// in 32-column blocks staged as 32 rows x 64 bytes (64-byte swizzle, 2 KB)
+// and stored through tmD1 = h_out [rows, I] with 32 x 32 boxes.  The two warps
+// of a lane quadrant take half of the tile's h columns each.
+template <class C, class W>
+__device__ void epilogue_swiglu_h32(const GemmArgs& a, const TileInfo& ti, uint32_t tacc,
+                                    int row_in_tile, W& w, const CUtensorMap* tmD1, int cpart,
+                                    int nparts) {
+  const int quad = row_in_tile >> 5;
+  const bool valid = row_in_tile < ti.rows_valid;
+  const bool warp_full = quad * 32 + 32 <= ti.rows_valid;
+  const long long r = ti.row0 + row_in_tile;
+  const int y = ti.row0 + quad * 32;
+  const int I = a.inter;
+  constexpr int HALF = C::BN / 2;
+  constexpr int NBLK = HALF / 32;
+  const int n0 = ti.nb * HALF;
+  const int b0 = cpart * NBLK / nparts;
+  int b1 = (cpart + 1) * NBLK / nparts;
+  const int inside = I > n0 ? (I - n0) / 32 : 0;  // I is a multiple of 64
+  if (b1 > inside) b1 = inside;
+  const int sw = (w.lane >> 1) & 3;
+#pragma unroll 1
+  for (int bi = b0; bi < b1; ++bi) {
+    const int j = n0 + bi * 32;
+    uint32_t g[32], u[32];
+    tmem_ld32_issue(tacc + bi * 32, g);
+    tmem_ld32_issue(tacc + HALF + bi * 32, u);
+    tmem_ld_wait2(g, u);
+    uint32_t ph[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float ga = __uint_as_float(g[2 * i]), gb = __uint_as_float(g[2 * i + 1]);
+      const float2 sg = sigmoid2_f(ga, gb);
+      ph[i] = pack_bf16x2(ga * sg.x * __uint_as_float(u[2 * i]),
+                          gb * sg.y * __uint_as_float(u[2 * i + 1]));
+    }
+    if (warp_full) {
+      // the buffer is taken after the math, so the wait for the previous
+      // store's read of it overlaps the work above
+      const uint32_t rowp = stage_acquire<1>(w) + w.lane * 64;
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        st_shared_v4(rowp + ((q ^ sw) << 4), ph[4 * q], ph[4 * q + 1], ph[4 * q + 2], ph[4 * q + 3]);
+      stage_store(w, rowp - w.lane * 64, tmD1, j, y, 0, false, 1);
+    } else if (valid) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        st_global_16(a.h_out + r * (long long)I + j + 8 * q, ph[4 * q], ph[4 * q + 1], ph[4 * q + 2],
+                     ph[4 * q + 3]);
+    }
+  }
+}
+
 // Plain bf16 output.  RAGGED_M: D rows are the tile's rows (map tmD0 2-D);
 // RAGGED_K: D is the group's full M x N matrix (map tmD0 3-D, group = depth).
 template <class C, class W>
@@ -919,6 +977,104 @@ __device__ void gather_role(const GemmArgs& a, const SmemTables& T, uint32_t sme
   }
 }
 
+// ---------------------------------------------------------------- wide units
+// The UMMA issuer's work for one WIDE unit (CTA-pair leader, warp-uniform
+// control; lane 0 issues).  Stage s, k-block kb: the four K=16 steps into
+// accumulator `which` (0 or 1), whose B tile is the stage's tile `which`.
+template <class C>
+__device__ __forceinline__ void wide_issue(uint32_t smem_base, uint32_t tmem_base, int s, int kb,
+                                           int which) {
+  const uint32_t sA = smem_base + s * C::STAGE_BYTES;
+  const uint32_t sB = sA + C::A_BYTES + which * (C::B_ROWS * 128);
+#pragma unroll
+  for (int kk = 0; kk < BK / 16; ++kk)
+    umma_bf16_pair(tmem_base + which * C::BN, smem_desc_sw128(sA + kk * 32, 16, 1024),
+                   smem_desc_sw128(sB + kk * 32, 16, 1024), C::IDESC, (kb | kk) != 0 ? 1u : 0u);
+}
+
+// Returns false on abort.  stage/phase: the stage ring position (advanced);
+// acc_phase: the accumulators' phase (flipped once the unit is issued).
+template <class C>
+__device__ bool wide_unit(const TileInfo& ti, uint32_t smem_base, uint32_t tmem_base,
+                          uint64_t* full_bar, uint64_t* empty_bar, uint64_t* tfull_bar,
+                          uint64_t* tempty_bar, int& stage,
+                          uint32_t& phase, uint32_t& acc_phase, int lane, volatile int* abort_flag,
+                          int* status) {
+  static_assert(C::WIDE && C::PAIR, "wide units run on CTA pairs");
+  // Stages that may be held while waiting for the next one to fill.  A stage
+  // fills only once the producers could claim the stages after it: the gather
+  // warps complete stage s after issuing the copies of the next GATHER_LAG
+  // stages, so those (STAGES later in the ring than stages before the held
+  // ones) must not be held.  Beyond this, wait for accumulator 1.
+  constexpr int kMaxHeld = C::STAGES - 1 - (C::A_GATHER ? C::GATHER_LAG : 0);
+  static_assert(kMaxHeld >= 0, "stage ring too shallow");
+  if (!mbar_wait(smem_u32(&tempty_bar[0]), acc_phase ^ 1, abort_flag, status)) return false;
+  tc_fence_after();
+  bool acc1 = false;           // accumulator 1 is free
+  int held = 0, h_stage = 0, h_kb = 0;  // stages with only their first half issued
+  auto flush = [&]() {         // second halves of the held stages, then release them
+    if (lane == 0) {
+      for (int i = 0; i < held; ++i) {
+        const int s = (h_stage + i) % C::STAGES;
+        wide_issue<C>(smem_base, tmem_base, s, h_kb + i, 1);
+        umma_commit_pair(smem_u32(&empty_bar[s]));
+      }
+    }
+    __syncwarp();
+    held = 0;
+  };
+  for (int kb = 0; kb < ti.kblocks; ++kb) {
+    if (!mbar_wait(smem_u32(&full_bar[stage]), phase, abort_flag, status)) return false;
+    tc_fence_after();
+    if (lane == 0) wide_issue<C>(smem_base, tmem_base, stage, kb, 0);
+    __syncwarp();
+    if (!acc1) {
+      const bool free1 = __shfl_sync(0xffffffffu,
+                                     lane == 0 ? (int)mbar_test_wait(smem_u32(&tempty_bar[1]),
+                                                                     acc_phase ^ 1)
+                                               : 0,
+                                     0) != 0;
+      if (free1 || held + 1 > kMaxHeld) {
+        if (!free1 && !mbar_wait(smem_u32(&tempty_bar[1]), acc_phase ^ 1, abort_flag, status))
+          return false;
+        tc_fence_after();
+        acc1 = true;
+        flush();
+      } else {
+        if (held == 0) { h_stage = stage; h_kb = kb; }
+        ++held;
+      }
+    }
+    if (acc1) {
+      if (lane == 0) {
+        wide_issue<C>(smem_base, tmem_base, stage, kb, 1);
+        umma_commit_pair(smem_u32(&empty_bar[stage]));
+      }
+      __syncwarp();
+    }
+    if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
+  }
+  if (!acc1) {
+    if (!mbar_wait(smem_u32(&tempty_bar[1]), acc_phase ^ 1, abort_flag, status)) return false;
+    tc_fence_after();
+    flush();
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+      if (ti.kblocks > 0) {
+        umma_commit_pair(smem_u32(&tfull_bar[b]));
+      } else {
+        mbar_arrive(smem_u32(&tfull_bar[b]));
+        mbar_arrive_remote(mapa_shared(smem_u32(&tfull_bar[b]), 1));
+      }
+    }
+  }
+  __syncwarp();
+  acc_phase ^= 1;
+  return true;
+}
+
 // ---------------------------------------------------------------- the kernel
 template <class C>
 __global__ void __launch_bounds__(C::THREADS, 1)
@@ -1143,9 +1299,17 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     for (int t = (!C::PAIR || leader) ? uw.first(unit0) : total; t < total && !*abort_flag;
          t = uw.next(t)) {
       const TileInfo ti = decode_tile<C>(a, T, t, rank);
+      if constexpr (C::WIDE) {
+        // The unit takes both accumulators, which the epilogue drains one after
+        // the other.  Once accumulator 0 is free its UMMAs start; each stage is
+        // held (not released to the producer) until accumulator 1 is free too
+        // and the stage's second half has been issued.
+        if (!wide_unit<C>(ti, smem_base, tmem_base, full_bar, empty_bar, tfull_bar, tempty_bar, stage,
+                          phase, acc_phase, lane, abort_flag, a.status))
+          break;
+        continue;
+      }
       if (!mbar_wait(smem_u32(&tempty_bar[acc]), acc_phase ^ 1, abort_flag, a.status)) break;
-      // WIDE: the unit takes both accumulators
-      if (C::WIDE && !mbar_wait(smem_u32(&tempty_bar[1]), acc_phase ^ 1, abort_flag, a.status)) break;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + acc * C::BN;
       bool ok = true;
@@ -1163,11 +1327,6 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                                         : smem_desc_sw128(sB + kk * 32, 16, 1024);
             if constexpr (C::PAIR) umma_bf16_pair(d_tmem, ad, bd, C::IDESC, (kb | kk) != 0 ? 1u : 0u);
             else umma_bf16(d_tmem, ad, bd, C::IDESC, (kb | kk) != 0 ? 1u : 0u);
-            if constexpr (C::WIDE) {
-              // the second n-block: same A, the next B tile, the other accumulator
-              const uint64_t bd1 = smem_desc_sw128(sB + C::B_ROWS * 128 + kk * 32, 16, 1024);
-              umma_bf16_pair(d_tmem + C::BN, ad, bd1, C::IDESC, (kb | kk) != 0 ? 1u : 0u);
-            }
           }
           if constexpr (C::PAIR) umma_commit_pair(smem_u32(&empty_bar[stage]));
           else umma_commit(smem_u32(&empty_bar[stage]));
@@ -1177,24 +1336,19 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       }
       if (!ok) break;
       if (lane == 0) {
-#pragma unroll
-        for (int sub = 0; sub < C::NSUB; ++sub) {
-          const int ab = C::WIDE ? sub : acc;
-          if constexpr (C::PAIR) {
-            if (ti.kblocks > 0) umma_commit_pair(smem_u32(&tfull_bar[ab]));
-            else {
-              mbar_arrive(smem_u32(&tfull_bar[ab]));
-              mbar_arrive_remote(mapa_shared(smem_u32(&tfull_bar[ab]), 1));
-            }
-          } else {
-            if (ti.kblocks > 0) umma_commit(smem_u32(&tfull_bar[ab]));
-            else mbar_arrive(smem_u32(&tfull_bar[ab]));
+        if constexpr (C::PAIR) {
+          if (ti.kblocks > 0) umma_commit_pair(smem_u32(&tfull_bar[acc]));
+          else {
+            mbar_arrive(smem_u32(&tfull_bar[acc]));
+            mbar_arrive_remote(mapa_shared(smem_u32(&tfull_bar[acc]), 1));
           }
+        } else {
+          if (ti.kblocks > 0) umma_commit(smem_u32(&tfull_bar[acc]));
+          else mbar_arrive(smem_u32(&tfull_bar[acc]));
         }
       }
       __syncwarp();
-      if (C::WIDE) acc_phase ^= 1;
-      else if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+      if (++acc == 2) { acc = 0; acc_phase ^= 1; }
     }
     if (*abort_flag && (!C::PAIR || leader)) {
       // wait (bounded) for UMMAs already issued before TMEM is released
@@ -1290,6 +1444,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           // pair slot past the group's last tile: nothing to store
         } else if constexpr (C::EPI == EPI_STORE_F32)
           epilogue_store_f32<C>(a, ti, tacc, row_in_tile, wo, &tmD0, cpart, nparts);
+        else if constexpr (C::EPI == EPI_SWIGLU && C::EPI_COLS == 32)
+          epilogue_swiglu_h32<C>(a, ti, tacc, row_in_tile, wo, &tmD1, cpart, nparts);
         else if constexpr (C::EPI == EPI_SWIGLU)
           epilogue_swiglu<C>(a, ti, tacc, row_in_tile, wo, &tmD0, &tmD1, cpart, nparts);
         else if constexpr (C::EPI == EPI_STORE)

@@ -283,9 +283,11 @@ template <int STAGES, int AL, int BL, int SCH, int EPI, bool B3D, bool SWIGLU_B,
 using PairCfg = GemmCfg<256, STAGES, AL, BL, SCH, EPI, B3D, SWIGLU_B, EPI_WARPS, true, EPI_BUFS>;
 using CfgGateUp = PairCfg<5, KMAJ_GATHER, KMAJ_TILE, RAGGED_M, EPI_SWIGLU, true, true>;
 // the inference gate/up GEMM (h only): units of two n-blocks that share every
-// token-row stage (48 KB a stage: 4 stages and one staging buffer a warp fit)
+// token-row stage; its epilogue is not hidden behind the next unit's mainloop,
+// so 8 warps share it (48 KB a stage: 4 stages and one 2 KB staging block a
+// warp fit)
 using CfgGateUpWide =
-    GemmCfg<256, 4, KMAJ_GATHER, KMAJ_TILE, RAGGED_M, EPI_SWIGLU, true, true, 4, true, 1, false, true>;
+    GemmCfg<256, 4, KMAJ_GATHER, KMAJ_TILE, RAGGED_M, EPI_SWIGLU, true, true, 8, true, 1, false, true>;
 using CfgGateUpShared = PairCfg<5, KMAJ_TILE, KMAJ_TILE, RAGGED_M, EPI_SWIGLU, false, true>;
 // the down GEMM as the consumer of the gate/up GEMM's h, units taken as SMs free up
 using CfgDownDyn = GemmCfg<256, 5, KMAJ_TILE, KMAJ_TILE, RAGGED_M, EPI_STORE, true, false, 4, true, 3, true>;
@@ -615,10 +617,9 @@ moe_status moe_permute(const moe_dims* d, const int32_t* topk_idx, int32_t* expe
 // epilogue warp and CTA of the pair): the consumer's dependency target.
 bool gate_up_wide(const moe_bf16* gu_out) { return gu_out == nullptr; }
 int gate_up_block_passes(const moe_dims& d, const moe_bf16* gu_out) {
-  const int sub = (int)(gate_up_wide(gu_out) ? 2 * cdiv(d.I, 256) : cdiv(d.I, 128));
-  return sub * CfgGateUp::EPI_WARPS * 2;
+  if (gate_up_wide(gu_out)) return (int)(2 * cdiv(d.I, 256)) * CfgGateUpWide::EPI_WARPS * 2;
+  return (int)cdiv(d.I, 128) * CfgGateUp::EPI_WARPS * 2;
 }
-static_assert(CfgGateUp::EPI_WARPS == CfgGateUpWide::EPI_WARPS, "one dependency count");
 
 moe_status launch_gate_up(const moe_dims& d, const moe_bf16* x, const int32_t* expert_offsets,
                           const int32_t* perm_slot, const moe_bf16* w_gate_up, moe_bf16* gu_out,
@@ -630,7 +631,9 @@ moe_status launch_gate_up(const moe_dims& d, const moe_bf16* x, const int32_t* e
   if (!make_map3(&tB, w_gate_up, H, 2LL * I, E, 64, 128)) return MOE_ERR_CUDA;
   const CUtensorMap& tA = tB;  // unused: A is gathered
   CUtensorMap tD0 = tB, tD1 = tB;
-  if (h_out && !make_out_map(&tD1, h_out, I, S)) return MOE_ERR_CUDA;
+  const bool wide = gate_up_wide(gu_out);
+  // h leaves in 32 x 64-column blocks, or 32 x 32 in the wide GEMM
+  if (h_out && !make_map(&tD1, h_out, I, S, 1, wide ? 32 : 64, 32)) return MOE_ERR_CUDA;
   if (gu_out && !make_out_map(&tD0, gu_out, 2LL * I, S)) return MOE_ERR_CUDA;
   GemmArgs a = base_args(status);
   a.N = 2 * I; a.K = H; a.G = E; a.offsets = expert_offsets; a.cap = d.capacity;
@@ -638,7 +641,7 @@ moe_status launch_gate_up(const moe_dims& d, const moe_bf16* x, const int32_t* e
   a.gdiv = d.k; a.gsrc_rows = d.T;
   a.gu_out = reinterpret_cast<__nv_bfloat16*>(gu_out); a.h_out = h_out; a.inter = I;
   a.dep_flags = dep_flags; a.dep_signal = dep_flags ? 1 : 0;
-  if (gate_up_wide(gu_out))
+  if (wide)
     return launch_gemm<CfgGateUpWide>(MOE_K_GATE_UP, tA, tB, tD0, tD1, a,
                                       (cdiv(S, moe::BM) + E) * cdiv(I, 256), st);
   return launch_gemm<CfgGateUp>(MOE_K_GATE_UP, tA, tB, tD0, tD1, a,

@@ -448,9 +448,6 @@ __device__ __forceinline__ void block_range(int cpart, int nparts, int nblk, int
   if (g1 > inside) g1 = inside;
 }
 
-// sigmoid(g) with CUDA's fast exponential and division intrinsics.
-__device__ __forceinline__ float sigmoid_f(float g) { return __fdividef(1.0f, 1.0f + __expf(-g)); }
-
 // 2^x and 1/x on the special-function unit (PTX ex2.approx / rcp.approx).
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
@@ -779,12 +776,13 @@ __device__ void epilogue_dgrad_swiglu(const GemmArgs& a, const SmemTables& T, co
           for (int i = 0; i < 4; ++i) {
             const uint32_t gw = (&gs[q].x)[i], uw = (&us[q].x)[i];
             float dg2[2], du2[2], hw2[2];
+            const float2 s2 = sigmoid2_f(bf16lo(gw), bf16hi(gw));
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
               const float gg = t ? bf16hi(gw) : bf16lo(gw);
               const float uu = t ? bf16hi(uw) : bf16lo(uw);
               const float ac = __uint_as_float(acc[8 * q + 2 * i + t]);
-              const float s = sigmoid_f(gg);
+              const float s = t ? s2.y : s2.x;
               const float sl = gg * s;
               const float hh = sl * uu;
               dwp = fmaf(ac, hh, dwp);

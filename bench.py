@@ -167,14 +167,18 @@ class _CtypesNvml:
 
 
 class ClockSampler:
-    """Samples SM clock and throttle reasons through NVML while running."""
+    """Samples SM clock and throttle reasons through NVML while running, and
+    for `tail_s` after: NVML's clock and reason readings trail the GPU by about
+    0.1 s (they change in steps every ~0.1 s), so samples taken only inside a
+    region of tens of milliseconds would show the state before it."""
 
     REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
                0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, device_index=0, period_s=0.002):
+    def __init__(self, device_index=0, period_s=0.002, tail_s=0.15):
         self.samples, self.reasons, self.ok = [], set(), False
         self.period = period_s
+        self.tail = tail_s
         try:
             try:
                 import pynvml
@@ -222,6 +226,7 @@ class ClockSampler:
 
     def __exit__(self, *a):
         if self.ok:
+            time.sleep(self.tail)
             self._stop.set()
             self._t.join()
 
@@ -306,7 +311,8 @@ def config_of(w, args):
             "router_bias_std": w.bias_std, "step": "forward+backward", "seed": args.seed,
             "l2": "inputs larger than L2: each step streams 1.21 GB of expert weights and "
                   "writes 1.21 GB of weight gradients (L2 126 MB)",
-            "parallelism": f"replicas x{args.gpus}"}
+            "parallelism": f"replicas x{args.gpus}",
+            "rest_s": args.rest_s}
 
 
 # ----------------------------------------------------------------- GPU arm
@@ -341,6 +347,8 @@ def time_other_shape(name, args, dev, peaks, timed):
            "router_bias_std": w.bias_std}
     layer_inf = M.MoeLayer(dims, gate_mode=w.gate, device=dev, with_backward=False)
     fg = StepGraph(layer_inf, None, weights, x)
+    torch.cuda.synchronize(dev)
+    time.sleep(args.rest_s)   # a burst from a rested GPU, as the headline
     for _ in range(args.warmup):
         fg.replay()
     ms_f = timed(fg.replay, args.steps)
@@ -365,6 +373,8 @@ def time_other_shape(name, args, dev, peaks, timed):
         layer = M.MoeLayer(dims, gate_mode=w.gate, device=dev, with_backward=True)
         grads = layer.alloc_grads(with_bias=bias is not None)
         sg = StepGraph(layer, grads, weights, x, go)
+        torch.cuda.synchronize(dev)
+        time.sleep(args.rest_s)
         for _ in range(args.warmup):
             sg.replay()
         ms_fb = timed(sg.replay, args.steps)
@@ -468,6 +478,11 @@ def run_ours(args, w, rank, world):
     from grouped_expert_gemm_top_b300.pipeline import StepGraph
     sg = StepGraph(layer, grads, dict(w_router=wr, w_gate_up=wgu, w_down=wd, router_bias=bias,
                                       w_sh_gate_up=wsg, w_sh_down=wsd), x, go)
+    # Each headline number is a short burst from a rested GPU: under a
+    # continuous load the board reaches its power limit within ~0.1 s and the
+    # SM clock drops (the sustained pass below measures that state).
+    torch.cuda.synchronize(dev)
+    time.sleep(args.rest_s)
     for _ in range(args.warmup):
         sg.replay()
     with ClockSampler(local) as clocks:
@@ -476,6 +491,8 @@ def run_ours(args, w, rank, world):
     # headline and in the same state of the GPU: a captured graph, clocks sampled
     fg = StepGraph(layer_inf, None, dict(w_router=wr, w_gate_up=wgu, w_down=wd, router_bias=bias,
                                          w_sh_gate_up=wsg, w_sh_down=wsd), x)
+    torch.cuda.synchronize(dev)
+    time.sleep(args.rest_s)
     for _ in range(max(1, args.warmup // 2)):
         fg.replay()
     with ClockSampler(local) as clocks_f:
@@ -551,6 +568,9 @@ def run_ours(args, w, rank, world):
             pipe.step(xh, goh, outh, gxh)
         pipe.drain()
 
+    e2e_pipelined(3)
+    torch.cuda.synchronize(dev)
+    time.sleep(args.rest_s)
     e2e_pipelined(3)
     ms_e2e = timed(lambda: e2e_pipelined(args.steps), 1)   # all K steps and the last read-back
     assert M.moe_read_device_status(layer.workspace) == 0, "device reported an error"
@@ -694,6 +714,9 @@ def main():
                     help="skip timing the skewed-router and shared-expert workloads")
     ap.add_argument("--sustain-s", type=float, default=3.0,
                     help="seconds of the extra steady-state pass (0: no such pass)")
+    ap.add_argument("--rest-s", type=float, default=1.0,
+                    help="idle seconds before each headline measurement (forward+backward, "
+                         "forward, end to end), so that each is a burst from a rested GPU")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 

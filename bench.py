@@ -502,6 +502,11 @@ def run_ours(args, w, rank, world):
     ms_fb_eager = timed(step, args.steps)
     # ---- the same steps again with every kernel bracketed by CUDA events on
     # its stream: per-kernel times and the dominant kernel's roofline
+    # (a burst from a rested GPU too, after a few untimed steps)
+    torch.cuda.synchronize(dev)
+    time.sleep(args.rest_s)
+    for _ in range(3):
+        step()
     M.moe_timing_enable(True)
     M.moe_kernel_stats(reset=True)
     ms_fb_inst = timed(step, args.steps)
@@ -716,7 +721,8 @@ def main():
                     help="seconds of the extra steady-state pass (0: no such pass)")
     ap.add_argument("--rest-s", type=float, default=1.0,
                     help="idle seconds before each headline measurement (forward+backward, "
-                         "forward, end to end), so that each is a burst from a rested GPU")
+                         "forward, per-kernel times, end to end), so that each is a burst "
+                         "from a rested GPU")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 

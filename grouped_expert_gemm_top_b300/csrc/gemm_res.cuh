@@ -309,6 +309,15 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       bool ok = true;
       for (int j = 0; j < u.ntiles && ok; ++j) {
         const TileInfo ti = res_tile<C>(a, u, j, rank);
+        // the tile after this one (the next of this unit, or the next unit's
+        // first): its k-blocks are sent to L2 one tile ahead of their loads
+        ResUnit un = u;
+        bool has_next = j + 1 < u.ntiles;
+        if (!has_next && t + ustep < total) {
+          un = res_unit<C>(a, T, order, t + ustep);
+          has_next = true;
+        }
+        const TileInfo tn = has_next ? res_tile<C>(a, un, j + 1 < u.ntiles ? j + 1 : 0, rank) : ti;
         for (int kb = 0; kb < u.kblocks; ++kb) {
           if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1, abort_flag, a.status)) { ok = false; break; }
           const uint32_t fb = smem_u32(&full_bar[stage]);
@@ -322,6 +331,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             const int kr = u.kstart + kb * BK;
             if constexpr (C::RES == RES_A) res_load_block(sS, &tmB, mapa_shared(fb, 0), ti.nb * C::BN + 128 * rank, kr);
             else res_load_block(sS, &tmA, mapa_shared(fb, 0), ti.mb * BM, kr);
+            if (has_next && kb < un.kblocks && !tn.phantom) {
+              const int kn = un.kstart + kb * BK;
+              const CUtensorMap* m = C::RES == RES_A ? &tmB : &tmA;
+              const int xn = C::RES == RES_A ? tn.nb * C::BN + 128 * rank : tn.mb * BM;
+              tma_prefetch_l2_2d(m, xn, kn);
+              tma_prefetch_l2_2d(m, xn + 64, kn);
+            }
           }
           __syncwarp();
           if (++stage == C::STAGES) { stage = 0; phase ^= 1; }

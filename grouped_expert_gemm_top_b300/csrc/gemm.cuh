@@ -664,6 +664,57 @@ __device__ void epilogue_swiglu_h32(const GemmArgs& a, const TileInfo& ti, uint3
   }
 }
 
+// Plain bf16 output in 32-column blocks staged as 32 rows x 64 bytes (64-byte
+// swizzle, 2 KB), for kernels whose shared memory leaves room for no more:
+// tmD0 has 32 x 32 boxes (RAGGED_K: 3-D, group = depth).  Rows and columns as
+// in epilogue_store.
+template <class C, class W>
+__device__ void epilogue_store32(const GemmArgs& a, const TileInfo& ti, uint32_t tacc,
+                                 int row_in_tile, W& w, const CUtensorMap* tmD0, int cpart,
+                                 int nparts) {
+  const int quad = row_in_tile >> 5;
+  const bool valid = row_in_tile < ti.rows_valid;
+  const bool warp_full = quad * 32 + 32 <= ti.rows_valid;
+  const int n0 = ti.nb * C::BN;
+  constexpr bool k3 = C::SCH == RAGGED_K;
+  const long long row = (k3 ? ti.mb * BM : ti.row0) + row_in_tile;
+  const int y = (k3 ? ti.mb * BM : ti.row0) + quad * 32;
+  const bool live = ti.kblocks > 0;  // an expert with no rows has an exact zero gradient
+  __nv_bfloat16* drow = a.d + (k3 ? (long long)ti.g * a.d_group_stride : 0) + row * a.ldd;
+  constexpr int NBLK = C::BN / 32;
+  const int b0 = cpart * NBLK / nparts;
+  int b1 = (cpart + 1) * NBLK / nparts;
+  const int inside = a.N > n0 ? (a.N - n0) / 32 : 0;  // N is a multiple of 64
+  if (b1 > inside) b1 = inside;
+  const int sw = (w.lane >> 1) & 3;
+#pragma unroll 1
+  for (int bi = b0; bi < b1; ++bi) {
+    const int col = n0 + bi * 32;
+    uint32_t v[32];
+    if (live) {
+      tmem_ld32_issue(tacc + bi * 32, v);
+      tmem_ld_wait(v);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = 0u;
+    }
+    uint32_t x[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) x[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+    if (warp_full) {
+      const uint32_t buf = stage_acquire<1>(w);
+      const uint32_t rowp = buf + w.lane * 64;
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        st_shared_v4(rowp + ((q ^ sw) << 4), x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+      stage_store(w, buf, tmD0, col, y, ti.g, k3);
+    } else if (valid) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) st_global_16(drow + col + 8 * q, x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+    }
+  }
+}
+
 // Plain bf16 output.  RAGGED_M: D rows are the tile's rows (map tmD0 2-D);
 // RAGGED_K: D is the group's full M x N matrix (map tmD0 3-D, group = depth).
 template <class C, class W>

@@ -41,7 +41,7 @@ namespace moe {
 enum ResMode : int { RES_A = 1, RES_B = 2 };
 
 template <int RES_, int AL_, int BL_, int STAGES_, int EPI_BUFS_, int EPI_WARPS_ = 4,
-          int RSLOTS_ = 4>
+          int RSLOTS_ = 4, int EPI_COLS_ = 64>
 struct ResCfg {
   static constexpr int RES = RES_;
   static constexpr int AL = AL_;  // MN_TILE or (streamed, RES_B) MN_GATHER
@@ -57,7 +57,11 @@ struct ResCfg {
   static constexpr int EPI_WARPS = EPI_WARPS_;
   static_assert(EPI_WARPS == 4 || EPI_WARPS == 8 || EPI_WARPS == 16, "epilogue warps per lane quarter");
   static constexpr int EPI_BUFS = EPI_BUFS_;
-  static constexpr int EPI_BUF_BYTES = 4096;
+  // bf16 columns of a staging block: 64 (4 KB, 128-byte rows) or 32 (2 KB,
+  // 64-byte rows: half the staging memory, for one more streamed stage)
+  static constexpr int EPI_COLS = EPI_COLS_;
+  static_assert(EPI_COLS == 64 || EPI_COLS == 32, "staging block width");
+  static constexpr int EPI_BUF_BYTES = EPI_COLS * 64;
   static constexpr bool A_GATHER = AL == MN_GATHER;
   static constexpr bool B_GATHER = BL == MN_GATHER;
   static constexpr bool GATHER = A_GATHER || B_GATHER;
@@ -576,7 +580,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         if (!mbar_wait(smem_u32(&tfull_bar[acc]), acc_phase, abort_flag, a.status)) { ok = false; break; }
         tc_fence_after();
         const uint32_t tacc = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * C::BN;
-        if (!ti.phantom) epilogue_store<C>(a, ti, tacc, row_in_tile, wo, &tmD0, cpart, nparts);
+        if (!ti.phantom) {
+          if constexpr (C::EPI_COLS == 32) epilogue_store32<C>(a, ti, tacc, row_in_tile, wo, &tmD0, cpart, nparts);
+          else epilogue_store<C>(a, ti, tacc, row_in_tile, wo, &tmD0, cpart, nparts);
+        }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(&tempty_bar[acc]), 0));

@@ -306,11 +306,12 @@ using CfgWgrad = PairCfg<4, MN_TILE, MN_TILE, RAGGED_K, EPI_STORE, false, false,
 // down: unit = (expert, 2 m-blocks of H), dout rows gathered once into the resident slots,
 //       w h streamed per n-block.
 // Their epilogue (a K = 256 tile's output is as large as its operands) takes a
-// large share of each tile: 8 epilogue warps, one staging buffer a warp.  The
-// resident slots are a 6-deep ring (5 streamed stages): the next unit's first
-// two k-blocks are gathered while the running unit computes.
-using CfgWgradRes = moe::ResCfg<moe::RES_B, MN_TILE, MN_GATHER, 5, 1, 8, 6>;
-using CfgWgradDownRes = moe::ResCfg<moe::RES_A, MN_GATHER, MN_TILE, 5, 1, 8, 6>;
+// large share of each tile: 8 epilogue warps, one 2 KB staging block a warp
+// (32 columns), which leaves room for 6 streamed stages beside the resident
+// slots, a 6-deep ring: the next unit's first two k-blocks are gathered while
+// the running unit computes.
+using CfgWgradRes = moe::ResCfg<moe::RES_B, MN_TILE, MN_GATHER, 6, 1, 8, 6, 32>;
+using CfgWgradDownRes = moe::ResCfg<moe::RES_A, MN_GATHER, MN_TILE, 6, 1, 8, 6, 32>;
 
 // fp32 [depth][rows][inner] output map with 16x32 boxes (64-byte rows).
 bool make_out_map3_f32(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows,
@@ -966,7 +967,7 @@ moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_
     a.d = reinterpret_cast<__nv_bfloat16*>(grad_w_down); a.ldd = I;
     a.d_group_stride = (long long)H * I;
     CUtensorMap tD;
-    if (!make_out_map3(&tD, grad_w_down, I, H, E)) return MOE_ERR_CUDA;
+    if (!make_map3(&tD, grad_w_down, I, H, E, CfgWgradDownRes::EPI_COLS, 32)) return MOE_ERR_CUDA;
     a.out_l2[0] = 1;  // evict-first: nothing in the layer reads the weight gradients back
     s = launch_gemm<CfgWgradDownRes, true>(MOE_K_WGRAD_DOWN, tA, tB, tD, tD, a,
                                            (long long)E * cdiv(H, 2 * moe::BM) * cdiv(I, 256), st);
@@ -982,7 +983,7 @@ moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_
     a.d = reinterpret_cast<__nv_bfloat16*>(grad_w_gate_up); a.ldd = H;
     a.d_group_stride = 2LL * I * H;
     CUtensorMap tD;
-    if (!make_out_map3(&tD, grad_w_gate_up, H, 2LL * I, E)) return MOE_ERR_CUDA;
+    if (!make_map3(&tD, grad_w_gate_up, H, 2LL * I, E, CfgWgradRes::EPI_COLS, 32)) return MOE_ERR_CUDA;
     a.out_l2[0] = 1;  // evict-first: nothing in the layer reads the weight gradients back
     s = launch_gemm<CfgWgradRes, true>(MOE_K_WGRAD_GATE_UP, tA, tB, tD, tD, a,
                                        (long long)E * cdiv(2 * I, 2 * moe::BM) * cdiv(H, 256), st);

@@ -194,7 +194,7 @@ __global__ void combine_kernel(const __nv_bfloat16* __restrict__ y_perm,
     for (int j = 0; j < KMAX; ++j)
       if (j < k)
         v[j] = rows[j] < 0 ? make_uint4(0u, 0u, 0u, 0u)
-                           : __ldg(reinterpret_cast<const uint4*>(y_perm + (size_t)rows[j] * H) + c);
+                           : ld_stream_v4(reinterpret_cast<const uint4*>(y_perm + (size_t)rows[j] * H) + c);
     uint4 vs = make_uint4(0, 0, 0, 0);
     if (y_shared) vs = __ldg(reinterpret_cast<const uint4*>(y_shared + (size_t)t * H) + c);
     float acc[8];
@@ -303,7 +303,7 @@ __global__ void dx_gather_kernel(const __nv_bfloat16* __restrict__ dx_slot,
         for (int jj = 0; jj < CH; ++jj) {
           const int j = j0 + jj;
           v[jj] = (j < k && rows[j] >= 0)
-                      ? __ldg(reinterpret_cast<const uint4*>(dx_slot + (size_t)rows[j] * H) + c)
+                      ? ld_stream_v4(reinterpret_cast<const uint4*>(dx_slot + (size_t)rows[j] * H) + c)
                       : make_uint4(0u, 0u, 0u, 0u);
           r[jj] = (j < k && router_term)
                       ? __ldg(reinterpret_cast<const uint4*>(w_router + (size_t)es[j] * H) + c)

@@ -4,7 +4,7 @@ Each case runs forward+backward on the device and compares every output and
 gradient with the float64 oracle on the device's routing: one token; one
 expert (the layer is a dense SwiGLU MLP); every token to every expert (k = E);
 the smallest hidden and intermediate sizes; one expert receiving almost every
-token; 160000 token-slots; and the optional features together (capacity with the auxiliary loss;
+token; 160000 token-slots; 128, 200 and 256 experts; and the optional features together (capacity with the auxiliary loss;
 activation recompute with capacity and a shared expert).
 """
 
@@ -28,6 +28,12 @@ EDGE = {
     "one_hot_expert": W("one_hot_expert", T=600, H=128, E=8, k=2, I=128, bias_std=6.0),
     # 160000 slots: the multi-block sort and row indices past 2^17 through the whole layer
     "many_tokens": W("many_tokens", T=20000, H=128, E=64, k=8, I=128, bias_std=0.5),
+    # more than 128 experts: the router kernel's 256-wide tile (8 experts a lane)
+    # and the router weight gradient's split-K path (the cluster kernel takes
+    # at most 128 experts); exactly 128 and 256 at the limits
+    "experts_200": W("experts_200", T=700, H=192, E=200, k=6, I=128, bias_std=0.5),
+    "experts_128": W("experts_128", T=300, H=320, E=128, k=8, I=128, bias_std=0.5),
+    "experts_256": W("experts_256", T=400, H=128, E=256, k=8, I=128, bias_std=0.5),
 }
 
 

@@ -39,6 +39,61 @@ __global__ void gather_rows_kernel(const __nv_bfloat16* __restrict__ src, long l
   for (int c = lane; c < H / 8; c += 32) d[c] = ok ? __ldg(s + c) : make_uint4(0u, 0u, 0u, 0u);
 }
 
+// dst[i] = src[idx[i] / div] for 4-byte elements (a source's routing weights
+// in its sorted order).  Indices outside [0, src_n) give 0 and MOE_DEV_BAD_INDEX.
+__global__ void gather_scalars_kernel(const uint32_t* __restrict__ src, long long src_n,
+                                      const int32_t* __restrict__ idx, int n, int div,
+                                      uint32_t* __restrict__ dst, int* status) {
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const long long r = (long long)__ldg(idx + i) / div;
+  const bool ok = r >= 0 && r < src_n;
+  if (!ok) record_status(status, MOE_DEV_BAD_INDEX);
+  dst[i] = ok ? __ldg(src + r) : 0u;
+}
+
+// The expert side of the expert-parallel backward hands its results back in
+// receive order: received row i sits at grouped row g = slot_perm[i] of local
+// expert e (offsets[e] <= g < offsets[e+1]), i.e. at row poff[e] + g -
+// offsets[e] of the padded row space the backward GEMMs use.  A warp per row
+// copies that row of the per-slot dx and sums its dw partials in column-part
+// order (the order the one-GPU router backward sums them in).
+__global__ void ep_rows_out_kernel(const __nv_bfloat16* __restrict__ dxs,
+                                   const float* __restrict__ dwp, int nDW,
+                                   const int32_t* __restrict__ poff,
+                                   const int32_t* __restrict__ offsets, int E,
+                                   const int32_t* __restrict__ slot_perm, int R, int H,
+                                   long long P, __nv_bfloat16* __restrict__ dx_rows,
+                                   float* __restrict__ dw_rows, int* status) {
+  const long long i = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (i >= R) return;
+  long long p = -1;
+  if (lane == 0) {
+    const int g = __ldg(slot_perm + i);
+    if (g >= 0 && g < __ldg(offsets + E)) {
+      int lo = 0, hi = E - 1;  // the last expert whose first row is <= g
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (__ldg(offsets + mid) <= g) lo = mid; else hi = mid - 1;
+      }
+      p = (long long)__ldg(poff + lo) + g - __ldg(offsets + lo);
+      if (p >= P) p = -1;
+    }
+    if (p < 0) record_status(status, MOE_DEV_BAD_INDEX);
+  }
+  p = __shfl_sync(0xffffffffu, p, 0);
+  const uint4* s = reinterpret_cast<const uint4*>(dxs + (p < 0 ? 0 : p) * (long long)H);
+  uint4* d = reinterpret_cast<uint4*>(dx_rows + i * (long long)H);
+  for (int c = lane; c < H / 8; c += 32) d[c] = p < 0 ? make_uint4(0u, 0u, 0u, 0u) : ld_stream_v4(s + c);
+  if (lane == 0) {
+    float dw = 0.f;
+    if (p >= 0)
+      for (int b = 0; b < nDW; ++b) dw += __ldg(dwp + p * nDW + b);
+    dw_rows[i] = dw;
+  }
+}
+
 constexpr int kEpLayoutThreads = 256;
 constexpr int kEpMaxCells = 4096;     // sources x local experts
 constexpr int kEpMaxLocalExperts = 256;

@@ -24,7 +24,7 @@ namespace {
 using moe::GemmArgs;
 using moe::GemmCfg;
 
-constexpr int32_t kAbiVersion = 11;
+constexpr int32_t kAbiVersion = 12;
 constexpr size_t kAlign = 256;
 
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
@@ -757,26 +757,47 @@ moe_status moe_unpermute_combine(const moe_dims* d, const moe_bf16* y_perm,
   return launched(cudaGetLastError());
 }
 
-moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_bf16* x,
-                         const moe_bf16* w_router, const int32_t* topk_idx, const float* topk_w,
-                         const int32_t* expert_offsets, const int32_t* perm_slot,
-                         const int32_t* slot_perm, const moe_bf16* w_gate_up,
-                         const moe_bf16* w_down, const moe_bf16* gu_saved,
-                         const moe_bf16* w_sh_gate_up, const moe_bf16* w_sh_down,
-                         const moe_bf16* sh_gu_saved, moe_bf16* grad_x, moe_bf16* grad_w_router,
-                         float* grad_router_bias, moe_bf16* grad_w_gate_up,
-                         moe_bf16* grad_w_down, moe_bf16* grad_w_sh_gate_up,
-                         moe_bf16* grad_w_sh_down, const float* router_logits,
-                         const float* aux_coef, void* workspace, size_t workspace_bytes,
-                         void* stream) {
+// The backward in two parts.  Experts: the data gradients of both projections
+// (per slot dx, per slot dw partials) and the expert weight gradients.
+// Router: the logit gradient, grad_x (the slots' dx summed per token, plus the
+// router term) and the router's weight and bias gradients.  moe_layer_bwd runs
+// both; the expert-parallel backward runs the experts part on the experts'
+// rank (its results handed back in receive order: dx_rows_out, dw_rows_out)
+// and the router part on the tokens' rank (from dx_sorted_in, dw_sorted_in:
+// the slots' dx and dw in the rank's sorted order).
+constexpr int kBwdExperts = 1, kBwdRouter = 2;
+
+static moe_status layer_bwd_impl(const moe_dims* d, const moe_bf16* grad_out, const moe_bf16* x,
+                                 const moe_bf16* w_router, const int32_t* topk_idx,
+                                 const float* topk_w, const int32_t* expert_offsets,
+                                 const int32_t* perm_slot, const int32_t* slot_perm,
+                                 const moe_bf16* w_gate_up, const moe_bf16* w_down,
+                                 const moe_bf16* gu_saved, const moe_bf16* w_sh_gate_up,
+                                 const moe_bf16* w_sh_down, const moe_bf16* sh_gu_saved,
+                                 moe_bf16* grad_x, moe_bf16* grad_w_router,
+                                 float* grad_router_bias, moe_bf16* grad_w_gate_up,
+                                 moe_bf16* grad_w_down, moe_bf16* grad_w_sh_gate_up,
+                                 moe_bf16* grad_w_sh_down, const float* router_logits,
+                                 const float* aux_coef, void* workspace, size_t workspace_bytes,
+                                 void* stream, int parts, moe_bf16* dx_rows_out,
+                                 float* dw_rows_out, const moe_bf16* dx_sorted_in,
+                                 const float* dw_sorted_in) {
   moe_status s = check_dims(d);
   const bool aux = aux_coef != nullptr;
+  const bool do_exp = (parts & kBwdExperts) != 0, do_rt = (parts & kBwdRouter) != 0;
   if (aux && !router_logits) return MOE_ERR_INVALID_ARG;
   if (s != MOE_OK) return s;
-  if (!grad_out || !x || !w_router || !topk_idx || !topk_w || !expert_offsets || !perm_slot ||
-      !slot_perm || !w_gate_up || !w_down || !grad_x || !grad_w_router || !grad_w_gate_up ||
-      !grad_w_down || !workspace)
+  if (!topk_w || !expert_offsets || !perm_slot || !slot_perm || !workspace)
     return MOE_ERR_INVALID_ARG;
+  if (do_exp && (!grad_out || !x || !w_gate_up || !w_down || !grad_w_gate_up || !grad_w_down))
+    return MOE_ERR_INVALID_ARG;
+  if (do_rt && (!x || !w_router || !topk_idx || !grad_x || !grad_w_router))
+    return MOE_ERR_INVALID_ARG;
+  if (!do_exp && (!dx_sorted_in || !dw_sorted_in || !aligned16(dx_sorted_in)))
+    return MOE_ERR_INVALID_ARG;
+  if (!do_rt && (!dx_rows_out || !dw_rows_out || !aligned16(dx_rows_out)))
+    return MOE_ERR_INVALID_ARG;
+  if ((!do_exp || !do_rt) && (d->I_shared > 0 || aux)) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (d->I_shared > 0 && (!w_sh_gate_up || !w_sh_down || !grad_w_sh_gate_up || !grad_w_sh_down))
     return MOE_ERR_INVALID_ARG;
   for (const void* p : {(const void*)grad_out, (const void*)x, (const void*)w_router,
@@ -789,7 +810,7 @@ moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_
     if (!aligned16(p)) return MOE_ERR_INVALID_ARG;
   // pre-activations not saved by the forward are recomputed here (activation
   // recompute), into the workspace
-  const bool rc_gu = gu_saved == nullptr;
+  const bool rc_gu = do_exp && gu_saved == nullptr;
   const bool rc_sh = d->I_shared > 0 && sh_gu_saved == nullptr;
   const Layout L = make_layout(*d, true, rc_gu || rc_sh);
   if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
@@ -824,8 +845,8 @@ moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_
   // the gate/up data gradient starts on the SMs the down data gradient frees,
   // each unit once its 256 rows of dgu are written
   int32_t* dep = at<int32_t>(workspace, L.dep_bwd);
-  if (cudaMemsetAsync(dep, 0, L.dep_bytes, st) != cudaSuccess) return MOE_ERR_CUDA;
-  {  // down-projection data gradient + SwiGLU backward (+ dw partials); A = grad_out rows
+  if (do_exp && cudaMemsetAsync(dep, 0, L.dep_bytes, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (do_exp) {  // down-projection data gradient + SwiGLU backward (+ dw partials); A = grad_out rows
     CUtensorMap tB;
     if (!make_map3(&tB, w_down, I, H, E, 64, 64)) return MOE_ERR_CUDA;
     const CUtensorMap& tA = tB;  // unused: A is gathered
@@ -841,7 +862,7 @@ moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_
     s = launch_gemm<CfgDgradDown>(MOE_K_DGRAD_DOWN, tA, tB, tD0, tD1, a, cdiv(P, moe::BM) * L.nNB_I, st);
     if (s != MOE_OK) return s;
   }
-  {  // gate/up data gradient -> per-slot dx
+  if (do_exp) {  // gate/up data gradient -> per-slot dx
     CUtensorMap tA, tB;
     if (!make_map(&tA, dgu, 2LL * I, P, 1, 64, 128)) return MOE_ERR_CUDA;
     if (!make_map3(&tB, w_gate_up, H, 2LL * I, E, 64, 64)) return MOE_ERR_CUDA;
@@ -889,19 +910,34 @@ moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_
       if (s != MOE_OK) return s;
     }
   }
+  if (!do_rt) {  // experts part only: the slots' dx and dw back in receive order
+    KernelScope ks(MOE_K_EP_ROWS_OUT, st);
+    moe::ep_rows_out_kernel<<<(unsigned)cdiv((long long)T * 32, 256), 256, 0, st>>>(
+        dxs, dwp, L.nDW, poff, expert_offsets, E, slot_perm, T, H, P,
+        reinterpret_cast<__nv_bfloat16*>(dx_rows_out), dw_rows_out, status);
+    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  // router part: the slots' dx and dw partials from the experts part above
+  // (padded row space), or given in the sorted order (one partial a slot)
+  const __nv_bfloat16* dxs_r =
+      do_exp ? dxs : reinterpret_cast<const __nv_bfloat16*>(dx_sorted_in);
+  const int32_t* poff_r = do_exp ? poff : expert_offsets;
+  const float* dwp_r = do_exp ? dwp : dw_sorted_in;
+  const int nDW_r = do_exp ? L.nDW : 1;
+  const long long P_r = do_exp ? P : L.S;
   float* dbp = at<float>(workspace, L.db_part);
   const int aux_blocks = (int)cdiv((long long)T, moe::kAuxDlWarps);
-  if (aux) {
+  if (do_rt && aux) {
     {  // dense logit gradient with the auxiliary loss's term (and its column sums)
       KernelScope ks(MOE_K_AUX, st);
       if (k <= 8)
         moe::aux_dl_kernel<8><<<(unsigned)aux_blocks, 32 * moe::kAuxDlWarps, 0, st>>>(
-            router_logits, aux_coef, topk_idx, topk_w, slot_perm, expert_offsets, poff, dwp,
-            L.nDW, (int)P, dl, T, E, k, rs.ldE, dlb, dbp);
+            router_logits, aux_coef, topk_idx, topk_w, slot_perm, expert_offsets, poff_r, dwp_r,
+            nDW_r, (int)P_r, dl, T, E, k, rs.ldE, dlb, dbp);
       else
         moe::aux_dl_kernel<32><<<(unsigned)aux_blocks, 32 * moe::kAuxDlWarps, 0, st>>>(
-            router_logits, aux_coef, topk_idx, topk_w, slot_perm, expert_offsets, poff, dwp,
-            L.nDW, (int)P, dl, T, E, k, rs.ldE, dlb, dbp);
+            router_logits, aux_coef, topk_idx, topk_w, slot_perm, expert_offsets, poff_r, dwp_r,
+            nDW_r, (int)P_r, dl, T, E, k, rs.ldE, dlb, dbp);
       if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
     }
     // the router's term of grad_x, dense over the experts: grad_x = DL W_r (a
@@ -917,26 +953,26 @@ moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_
                                  cdiv(T, moe::BM) * cdiv(H, 256), st);
     if (s != MOE_OK) return s;
   }
-  {  // router backward + per-token gather of the slot gradients
+  if (do_rt) {  // router backward + per-token gather of the slot gradients
     KernelScope ks(MOE_K_DX_GATHER, st);
     const unsigned blocks = (unsigned)cdiv((long long)T * 32, 256);
     auto* wr = reinterpret_cast<const __nv_bfloat16*>(w_router);
     auto* gx = reinterpret_cast<__nv_bfloat16*>(grad_x);
     if (k <= 8)
-      moe::dx_gather_kernel<8><<<blocks, 256, 0, st>>>(dxs, topk_idx, topk_w, slot_perm,
-                                                       expert_offsets, poff, dwp, L.nDW, wr,
+      moe::dx_gather_kernel<8><<<blocks, 256, 0, st>>>(dxs_r, topk_idx, topk_w, slot_perm,
+                                                       expert_offsets, poff_r, dwp_r, nDW_r, wr,
                                                        dxs_sh, dl, aux ? nullptr : dlb, rs.ldE,
                                                        aux ? 0 : 1, aux ? 1 : 0, gx, T, H, k, E,
-                                                       (int)P);
+                                                       (int)P_r);
     else
-      moe::dx_gather_kernel<32><<<blocks, 256, 0, st>>>(dxs, topk_idx, topk_w, slot_perm,
-                                                        expert_offsets, poff, dwp, L.nDW, wr,
+      moe::dx_gather_kernel<32><<<blocks, 256, 0, st>>>(dxs_r, topk_idx, topk_w, slot_perm,
+                                                        expert_offsets, poff_r, dwp_r, nDW_r, wr,
                                                         dxs_sh, dl, aux ? nullptr : dlb, rs.ldE,
                                                         aux ? 0 : 1, aux ? 1 : 0, gx, T, H, k, E,
-                                                        (int)P);
+                                                        (int)P_r);
     if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
   }
-  {  // router weight gradient: dW_r = DL^T x, split-K over the tokens (fp32 partials) ...
+  if (do_rt) {  // router weight gradient: dW_r = DL^T x, split-K over the tokens (fp32 partials) ...
     CUtensorMap tA, tB, tD;
     if (!make_map(&tA, dlb, rs.ldE, T, 1, 64, 64)) return MOE_ERR_CUDA;
     if (!make_map(&tB, x, H, T, 1, 64, 64)) return MOE_ERR_CUDA;
@@ -948,7 +984,7 @@ moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_
                                 (long long)rs.nsplit * cdiv(E, moe::BM) * cdiv(H, 256), st);
     if (s != MOE_OK) return s;
   }
-  {  // ... then the ordered sum of the splits (and the bias gradient)
+  if (do_rt) {  // ... then the ordered sum of the splits (and the bias gradient)
     KernelScope ks(MOE_K_ROUTER_WGRAD_REDUCE, st);
     const long long n4 = (long long)E * H / 4;
     const long long blocks = std::max<long long>(cdiv(n4, 256), cdiv((long long)E * 32, 256));
@@ -957,7 +993,7 @@ moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_
         reinterpret_cast<__nv_bfloat16*>(grad_w_router), grad_router_bias);
     if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
   }
-  {  // dW_down[e] = sum over the expert's rows of dout[token]^T (w h)
+  if (do_exp) {  // dW_down[e] = sum over the expert's rows of dout[token]^T (w h)
     CUtensorMap tA, tB;
     if (!make_map(&tB, hw, I, P, 1, 64, 64)) return MOE_ERR_CUDA;
     tA = tB;  // unused: A = grad_out rows, gathered
@@ -973,7 +1009,7 @@ moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_
                                            (long long)E * cdiv(H, 2 * moe::BM) * cdiv(I, 256), st);
     if (s != MOE_OK) return s;
   }
-  {  // dW_gu[e] = sum over the expert's rows of [dg|du]^T x[token]
+  if (do_exp) {  // dW_gu[e] = sum over the expert's rows of [dg|du]^T x[token]
     CUtensorMap tA, tB;
     if (!make_map(&tA, dgu, 2LL * I, P, 1, 64, 64)) return MOE_ERR_CUDA;
     tB = tA;  // unused: B = x rows, gathered by token
@@ -1023,6 +1059,73 @@ moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_
   return MOE_OK;
 }
 
+moe_status moe_layer_bwd(const moe_dims* d, const moe_bf16* grad_out, const moe_bf16* x,
+                         const moe_bf16* w_router, const int32_t* topk_idx, const float* topk_w,
+                         const int32_t* expert_offsets, const int32_t* perm_slot,
+                         const int32_t* slot_perm, const moe_bf16* w_gate_up,
+                         const moe_bf16* w_down, const moe_bf16* gu_saved,
+                         const moe_bf16* w_sh_gate_up, const moe_bf16* w_sh_down,
+                         const moe_bf16* sh_gu_saved, moe_bf16* grad_x, moe_bf16* grad_w_router,
+                         float* grad_router_bias, moe_bf16* grad_w_gate_up,
+                         moe_bf16* grad_w_down, moe_bf16* grad_w_sh_gate_up,
+                         moe_bf16* grad_w_sh_down, const float* router_logits,
+                         const float* aux_coef, void* workspace, size_t workspace_bytes,
+                         void* stream) {
+  return layer_bwd_impl(d, grad_out, x, w_router, topk_idx, topk_w, expert_offsets, perm_slot,
+                        slot_perm, w_gate_up, w_down, gu_saved, w_sh_gate_up, w_sh_down,
+                        sh_gu_saved, grad_x, grad_w_router, grad_router_bias, grad_w_gate_up,
+                        grad_w_down, grad_w_sh_gate_up, grad_w_sh_down, router_logits, aux_coef,
+                        workspace, workspace_bytes, stream, kBwdExperts | kBwdRouter, nullptr,
+                        nullptr, nullptr, nullptr);
+}
+
+moe_status moe_experts_bwd(const moe_dims* d, const moe_bf16* grad_out_rows,
+                           const moe_bf16* x_rows, const float* row_w,
+                           const int32_t* expert_offsets, const int32_t* perm_slot,
+                           const int32_t* slot_perm, const moe_bf16* w_gate_up,
+                           const moe_bf16* w_down, const moe_bf16* gu_saved, moe_bf16* dx_rows,
+                           float* dw_rows, moe_bf16* grad_w_gate_up, moe_bf16* grad_w_down,
+                           void* workspace, size_t workspace_bytes, void* stream) {
+  if (!d) return MOE_ERR_INVALID_ARG;
+  if (d->k != 1 || d->I_shared != 0 || d->capacity != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+  return layer_bwd_impl(d, grad_out_rows, x_rows, nullptr, nullptr, row_w, expert_offsets,
+                        perm_slot, slot_perm, w_gate_up, w_down, gu_saved, nullptr, nullptr,
+                        nullptr, nullptr, nullptr, nullptr, grad_w_gate_up, grad_w_down, nullptr,
+                        nullptr, nullptr, nullptr, workspace, workspace_bytes, stream,
+                        kBwdExperts, dx_rows, dw_rows, nullptr, nullptr);
+}
+
+moe_status moe_router_bwd(const moe_dims* d, const moe_bf16* x, const moe_bf16* w_router,
+                          const int32_t* topk_idx, const float* topk_w,
+                          const int32_t* expert_offsets, const int32_t* perm_slot,
+                          const int32_t* slot_perm, const moe_bf16* dx_sorted,
+                          const float* dw_sorted, moe_bf16* grad_x, moe_bf16* grad_w_router,
+                          float* grad_router_bias, void* workspace, size_t workspace_bytes,
+                          void* stream) {
+  if (!d) return MOE_ERR_INVALID_ARG;
+  if (d->I_shared != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+  return layer_bwd_impl(d, nullptr, x, w_router, topk_idx, topk_w, expert_offsets, perm_slot,
+                        slot_perm, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, grad_x,
+                        grad_w_router, grad_router_bias, nullptr, nullptr, nullptr, nullptr,
+                        nullptr, nullptr, workspace, workspace_bytes, stream, kBwdRouter, nullptr,
+                        nullptr, dx_sorted, dw_sorted);
+}
+
+moe_status moe_gather_scalars(const void* src, int64_t src_n, const int32_t* idx, int32_t n,
+                              int32_t div, void* dst, int32_t* device_status, void* stream) {
+  if (n < 0 || src_n < 0 || div < 1) return MOE_ERR_INVALID_ARG;
+  if (n == 0) return MOE_OK;
+  if (!src || !idx || !dst) return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst)) & 3u)
+    return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  KernelScope ks(MOE_K_GATHER_SCALARS, st);
+  moe::gather_scalars_kernel<<<(unsigned)cdiv(n, 256), 256, 0, st>>>(
+      static_cast<const uint32_t*>(src), (long long)src_n, idx, n, div, static_cast<uint32_t*>(dst),
+      device_status);
+  return launched(cudaGetLastError());
+}
+
 moe_status moe_gather_rows(const moe_bf16* src, int64_t src_rows, int32_t H, const int32_t* idx,
                            int32_t n, int32_t div, moe_bf16* dst, int32_t* device_status,
                            void* stream) {
@@ -1064,7 +1167,7 @@ const char* moe_kernel_name(int32_t id) {
       "dgrad_gate_up", "shared_dgrad_down", "shared_dgrad_gate_up", "dx_gather",
       "router_wgrad", "wgrad_down", "wgrad_gate_up", "shared_wgrad_down",
       "shared_wgrad_gate_up", "router_wgrad_reduce", "aux_loss", "router_dx", "gather_rows",
-      "ep_recv_layout"};
+      "ep_recv_layout", "ep_rows_out", "gather_scalars"};
   return (id >= 0 && id < MOE_K_COUNT) ? names[id] : "unknown";
 }
 

@@ -25,6 +25,17 @@ The rows of an expert meet on its rank in global slot order (sources in rank
 order, each in its slot order), as on one GPU, so with tokens numbered rank
 by rank the result equals the one-GPU layer's.
 
+The backward (``ExpertParallelMoe.backward``, for a layer built with
+``with_backward=True``) is the reverse trip: each source sends its slots'
+grad_out rows (``moe_gather_rows``) and routing weights
+(``moe_gather_scalars``) in its sorted order, as it sent the token rows; the
+experts' rank runs ``moe_experts_bwd`` on them (the saved pre-activations of
+its forward) and sends each row's dx and dL/dw back; the source runs
+``moe_router_bwd``.  Every gradient equals the one-GPU ``moe_layer_bwd``'s
+bit for bit except the router's, which each rank forms over its own tokens:
+the caller sums it over the ranks, as data parallelism sums any replicated
+parameter's gradient.
+
 The exchange is an object with ``all_to_all_single(out, inp, out_splits,
 in_splits)`` along dim 0 (a torch.distributed process group wrapper, see
 ``DistExchange``); bf16 rows travel as int16 words.  The compute steps are the
@@ -63,12 +74,12 @@ class DistExchange:
 class DeviceOps:
     """The forward's compute steps, each one or two library kernels on the device."""
 
-    def __init__(self, dims, gate_mode, device):
+    def __init__(self, dims, gate_mode, device, with_backward=False):
         self.dims = M.MoeDims.of(*M._dims(dims).as_tuple())
         self.gate_mode = gate_mode
         self.device = torch.device(device)
         # a rank without tokens still takes part in the exchanges (routes nothing)
-        nbytes = M.moe_workspace_size(self.dims, False) if self.dims.T > 0 else 256
+        nbytes = M.moe_workspace_size(self.dims, with_backward) if self.dims.T > 0 else 256
         self.ws = torch.zeros(nbytes, dtype=torch.uint8, device=self.device)
         self._loc_ws = None
 
@@ -101,18 +112,53 @@ class DeviceOps:
                                 recv_perm, recv_inv, device_status=self.ws.view(torch.int32)[:1])
         return loc_off, recv_perm, recv_inv
 
-    def experts(self, x_recv, loc_off, recv_perm, w_gate_up_local, w_down_local):
+    def _local_ws(self, d, with_backward):
+        need = M.moe_workspace_size(d, with_backward)
+        if self._loc_ws is None or self._loc_ws.numel() < need:
+            self._loc_ws = torch.zeros(need, dtype=torch.uint8, device=self.device)
+        return self._loc_ws
+
+    def experts(self, x_recv, loc_off, recv_perm, w_gate_up_local, w_down_local, gu_out=None):
         R, H = x_recv.shape
         E_loc = w_gate_up_local.shape[0]
         I = w_down_local.shape[2]
         y = torch.empty(R, H, dtype=torch.bfloat16, device=self.device)
         d = M.MoeDims.of(R, H, E_loc, 1, I, 0)
-        need = M.moe_workspace_size(d, False)
-        if self._loc_ws is None or self._loc_ws.numel() < need:
-            self._loc_ws = torch.zeros(need, dtype=torch.uint8, device=self.device)
-        M.moe_grouped_mlp_fwd(d, x_recv, loc_off, recv_perm, w_gate_up_local, w_down_local, None, y,
-                              None, None, None, None, self._loc_ws)
+        M.moe_grouped_mlp_fwd(d, x_recv, loc_off, recv_perm, w_gate_up_local, w_down_local, gu_out,
+                              y, None, None, None, None, self._local_ws(d, gu_out is not None))
         return y
+
+    def gather_scalars(self, src, idx, div):
+        dst = torch.empty(idx.numel(), dtype=src.dtype, device=self.device)
+        M.moe_gather_scalars(src, idx, div, dst, device_status=self.ws.view(torch.int32)[:1])
+        return dst
+
+    def experts_bwd(self, go_recv, x_recv, w_recv, loc_off, recv_perm, recv_inv, w_gate_up_local,
+                    w_down_local, gu_saved):
+        """Each received row's dx and dL/dw (receive order) and the local
+        experts' weight gradients."""
+        R, H = x_recv.shape
+        E_loc = w_gate_up_local.shape[0]
+        I = w_down_local.shape[2]
+        d = M.MoeDims.of(R, H, E_loc, 1, I, 0)
+        dx = torch.empty(R, H, dtype=torch.bfloat16, device=self.device)
+        dw = torch.empty(R, dtype=torch.float32, device=self.device)
+        gwgu = torch.empty_like(w_gate_up_local)
+        gwd = torch.empty_like(w_down_local)
+        M.moe_experts_bwd(d, go_recv, x_recv, w_recv, loc_off, recv_perm, recv_inv, w_gate_up_local,
+                          w_down_local, gu_saved, dx, dw, gwgu, gwd, self._local_ws(d, True))
+        return dx, dw, gwgu, gwd
+
+    def router_bwd(self, x, w_router, idx, w, off, perm, inv, dx_sorted, dw_sorted, with_bias):
+        T, H = x.shape
+        E = w_router.shape[0]
+        gx = torch.empty(T, H, dtype=torch.bfloat16, device=self.device)
+        gwr = torch.zeros(E, H, dtype=torch.bfloat16, device=self.device)
+        gb = torch.zeros(E, dtype=torch.float32, device=self.device) if with_bias else None
+        if T > 0:
+            M.moe_router_bwd(self.dims, x, w_router, idx, w, off, perm, inv, dx_sorted, dw_sorted,
+                             gx, gwr, gb, self.ws)
+        return gx, gwr, gb
 
     def combine(self, y_sorted, slot_perm, topk_w):
         T, H = self.dims.T, self.dims.H
@@ -134,14 +180,16 @@ class ExpertParallelMoe:
     """
 
     def __init__(self, dims, rank: int, world: int, exchange, gate_mode=M.MOE_GATE_SOFTMAX_TOPK,
-                 device="cuda", ops=None):
+                 device="cuda", ops=None, with_backward=False):
         T, H, E, k, I = dims[:5]
         self.T, self.H, self.E, self.k, self.I = T, H, E, k, I
         self.rank, self.world = rank, world
         self.bounds = expert_ranges(E, world)
         self.lo, self.hi = self.bounds[rank], self.bounds[rank + 1]
         self.exchange = exchange
-        self.ops = ops if ops is not None else DeviceOps((T, H, E, k, I, 0), gate_mode, device)
+        self.with_backward = with_backward
+        self.ops = ops if ops is not None else DeviceOps((T, H, E, k, I, 0), gate_mode, device,
+                                                         with_backward)
         self.last = {}
 
     def _xdev(self):
@@ -158,6 +206,14 @@ class ExpertParallelMoe:
         else:
             self.exchange.all_to_all_single(out, src, out_splits, in_splits)
         return out if out.device == rows.device else out.to(rows.device)
+
+    def _a2a_vec(self, v, in_splits, out_splits):
+        """One value a row (fp32), block q to rank q; returns what arrives."""
+        xdev = self._xdev()
+        src = v if v.device == xdev else v.to(xdev)
+        out = torch.empty(sum(out_splits), dtype=v.dtype, device=xdev)
+        self.exchange.all_to_all_single(out, src, out_splits, in_splits)
+        return out if out.device == v.device else out.to(v.device)
 
     def forward(self, x, w_router, w_gate_up_local, w_down_local, router_bias=None):
         ops, b, n = self.ops, self.bounds, self.world
@@ -180,9 +236,12 @@ class ExpertParallelMoe:
         x_recv = self._a2a_rows(x_send, send_rows, recv_rows)
         # 4. the local experts on the rows grouped by expert
         R = sum(recv_rows)
+        gu = None
         if E_loc and R:
             loc_off, recv_perm, recv_inv = ops.receive_layout(recv_counts)
-            y_grouped = ops.experts(x_recv, loc_off, recv_perm, w_gate_up_local, w_down_local)
+            if self.with_backward:   # the experts' pre-activations, for the backward
+                gu = torch.empty(R, 2 * self.I, dtype=torch.bfloat16, device=x_recv.device)
+            y_grouped = ops.experts(x_recv, loc_off, recv_perm, w_gate_up_local, w_down_local, gu)
             y_recv = ops.gather_rows(y_grouped, recv_inv, 1)
         else:
             loc_off = recv_perm = recv_inv = None
@@ -193,5 +252,44 @@ class ExpertParallelMoe:
         self.last = dict(topk_idx=idx, topk_w=w, expert_offsets=off, perm_slot=perm, slot_perm=inv,
                          send_rows=send_rows, recv_rows=recv_rows, recv_counts=recv_counts,
                          x_recv=x_recv, local_offsets=loc_off, recv_perm=recv_perm,
-                         recv_inv=recv_inv, y_sorted=y_sorted)
+                         recv_inv=recv_inv, y_sorted=y_sorted, gu_saved=gu)
         return out
+
+    def backward(self, grad_out, x, w_router, w_gate_up_local, w_down_local, with_bias=False):
+        """Gradients of the last forward (built with with_backward=True).
+
+        Returns grad_x [T, H] (this rank's tokens), grad_w_gate_up /
+        grad_w_down of the local experts, and grad_w_router (and
+        grad_router_bias with with_bias) over this rank's tokens: sum those
+        over the ranks.
+        """
+        if not self.with_backward:
+            raise RuntimeError("the layer was built without with_backward=True")
+        ops, L = self.ops, self.last
+        send_rows, recv_rows = L["send_rows"], L["recv_rows"]
+        perm = L["perm_slot"]
+        # 1. this rank's slots' grad_out rows and weights, in its sorted order
+        go_send = ops.gather_rows(grad_out, perm, self.k)
+        w_send = ops.gather_scalars(L["topk_w"].reshape(-1), perm, 1)
+        go_recv = self._a2a_rows(go_send, send_rows, recv_rows)
+        w_recv = self._a2a_vec(w_send, send_rows, recv_rows)
+        # 2. the local experts: each received row's dx and dL/dw, the weight gradients
+        E_loc = self.hi - self.lo
+        R = sum(recv_rows)
+        if E_loc and R:
+            dx_recv, dw_recv, gwgu, gwd = ops.experts_bwd(
+                go_recv, L["x_recv"], w_recv, L["local_offsets"], L["recv_perm"], L["recv_inv"],
+                w_gate_up_local, w_down_local, L["gu_saved"])
+        else:   # no rows: exact-zero weight gradients
+            dx_recv = torch.empty(0, self.H, dtype=go_send.dtype, device=go_send.device)
+            dw_recv = torch.empty(0, dtype=w_send.dtype, device=w_send.device)
+            gwgu, gwd = torch.zeros_like(w_gate_up_local), torch.zeros_like(w_down_local)
+        # 3. back to their sources, then the router's backward there
+        dx_sorted = self._a2a_rows(dx_recv, recv_rows, send_rows)
+        dw_sorted = self._a2a_vec(dw_recv, recv_rows, send_rows)
+        gx, gwr, gb = ops.router_bwd(x, w_router, L["topk_idx"], L["topk_w"], L["expert_offsets"],
+                                     perm, L["slot_perm"], dx_sorted, dw_sorted, with_bias)
+        self.last.update(go_recv=go_recv, w_recv=w_recv, dx_recv=dx_recv, dw_recv=dw_recv,
+                         dx_sorted=dx_sorted, dw_sorted=dw_sorted)
+        return dict(grad_x=gx, grad_w_router=gwr, grad_router_bias=gb, grad_w_gate_up=gwgu,
+                    grad_w_down=gwd)

@@ -72,6 +72,9 @@ _SIGS = {
     "moe_permute_static_scratch": ([_DIMS, _P, _P, _P, _P, _P, _P], _I32),
     "moe_gather_rows": ([_P, ctypes.c_int64, _I32, _P, _I32, _I32, _P, _P, _P], _I32),
     "moe_ep_receive_layout": ([_I32, _I32, _P, _I32, _P, _P, _P, _P, _P], _I32),
+    "moe_gather_scalars": ([_P, ctypes.c_int64, _P, _I32, _I32, _P, _P, _P], _I32),
+    "moe_experts_bwd": ([_DIMS] + [_P] * 13 + [_P, _SZ, _P], _I32),
+    "moe_router_bwd": ([_DIMS] + [_P] * 12 + [_P, _SZ, _P], _I32),
     "moe_kernel_count": ([], _I32),
     "moe_kernel_name": ([_I32], ctypes.c_char_p),
     "moe_timing_enable": ([_I32], _I32),
@@ -260,6 +263,38 @@ def moe_ep_receive_layout(counts, local_offsets, recv_perm, recv_inv, device_sta
     _check("moe_ep_receive_layout", load_library().moe_ep_receive_layout(
         n_src, E_loc, _ptr(counts), R, _ptr(local_offsets), _ptr(recv_perm) if R else None,
         _ptr(recv_inv) if R else None, _ptr(device_status), _stream(stream)))
+
+
+def moe_gather_scalars(src, idx, div, dst, device_status=None, stream=None):
+    """dst[i] = src.flat[idx[i] // div] for 4-byte elements (idx int32 [n], dst [n])."""
+    n = int(idx.numel())
+    _check("moe_gather_scalars", load_library().moe_gather_scalars(
+        _ptr(src) if src.numel() else None, int(src.numel()), _ptr(idx) if n else None, n,
+        int(div), _ptr(dst) if n else None, _ptr(device_status), _stream(stream)))
+
+
+def moe_experts_bwd(dims, grad_out_rows, x_rows, row_w, expert_offsets, perm_slot, slot_perm,
+                    w_gate_up, w_down, gu_saved, dx_rows, dw_rows, grad_w_gate_up, grad_w_down,
+                    workspace, stream=None):
+    """The experts part of the expert-parallel backward (dims: T = rows received,
+    k = 1, E = local experts); see include/moe.h."""
+    p, n = _ws(workspace)
+    args = [grad_out_rows, x_rows, row_w, expert_offsets, perm_slot, slot_perm, w_gate_up, w_down,
+            gu_saved, dx_rows, dw_rows, grad_w_gate_up, grad_w_down]
+    _check("moe_experts_bwd", load_library().moe_experts_bwd(
+        ctypes.byref(_dims(dims)), *[_ptr(a) for a in args], p, n, _stream(stream)))
+
+
+def moe_router_bwd(dims, x, w_router, topk_idx, topk_w, expert_offsets, perm_slot, slot_perm,
+                   dx_sorted, dw_sorted, grad_x, grad_w_router, grad_router_bias, workspace,
+                   stream=None):
+    """The router part of the expert-parallel backward on the tokens' rank; see
+    include/moe.h."""
+    p, n = _ws(workspace)
+    args = [x, w_router, topk_idx, topk_w, expert_offsets, perm_slot, slot_perm, dx_sorted,
+            dw_sorted, grad_x, grad_w_router, grad_router_bias]
+    _check("moe_router_bwd", load_library().moe_router_bwd(
+        ctypes.byref(_dims(dims)), *[_ptr(a) for a in args], p, n, _stream(stream)))
 
 
 def moe_kernel_count() -> int:

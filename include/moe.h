@@ -353,6 +353,69 @@ moe_status moe_ep_receive_layout(int32_t n_src, int32_t E_local, const int32_t* 
                                  int32_t* device_status, void* stream);
 
 /*
+ * dst[i] = src[idx[i] / div] for i < n, 4-byte elements (a source's routing
+ * weights topk_w, read as [T*k], in its sorted order: idx = perm_slot, div =
+ * 1).  src [src_n], dst [n], idx int32 [n], 4-byte aligned device memory.  An
+ * index outside [0, src_n) gives 0 and MOE_ERR_DEVICE_INDEX in
+ * *device_status (optional).  Errors: MOE_ERR_INVALID_ARG, MOE_ERR_CUDA.
+ */
+moe_status moe_gather_scalars(const void* src, int64_t src_n, const int32_t* idx, int32_t n,
+                              int32_t div, void* dst, int32_t* device_status, void* stream);
+
+/*
+ * The expert-parallel backward, in two calls around the exchanges (same
+ * pages; the backward of dispatch is a combine of the slots' gradients and the
+ * backward of combine a dispatch of grad_out).  A source gathers its
+ * grad_out rows (moe_gather_rows, idx = perm_slot, div = k) and its routing
+ * weights (moe_gather_scalars) in its sorted order and sends them like the
+ * forward's token rows.  The experts' rank runs moe_experts_bwd on what it
+ * received and sends dx_rows and dw_rows back; the source, now holding its
+ * slots' dx and dw in its sorted order, runs moe_router_bwd.  The results
+ * equal moe_layer_bwd's on the same rows bit for bit, except the router's
+ * weight and bias gradients, which each rank forms over its own tokens (the
+ * caller sums them over the ranks, as data parallelism sums any replicated
+ * parameter's gradient).
+ *
+ * moe_experts_bwd: the experts part.  d: T = rows received, k = 1, E = local
+ * experts, I, I_shared = 0, capacity = 0 (MOE_ERR_UNSUPPORTED_SHAPE
+ * otherwise).  grad_out_rows, x_rows bf16 [T,H]: the received rows' grad_out
+ * and token rows, receive order; row_w fp32 [T]: each row's routing weight;
+ * expert_offsets [E+1], perm_slot [T] (= recv_perm), slot_perm [T] (=
+ * recv_inv): moe_ep_receive_layout's grouping; gu_saved bf16 [T, 2I] from
+ * the experts' moe_grouped_mlp_fwd on the same grouping (or NULL: recomputed
+ * into the workspace).  Writes dx_rows bf16 [T,H] (each row's input
+ * gradient), dw_rows fp32 [T] (each row's d loss / d routing weight),
+ * grad_w_gate_up [E,2I,H], grad_w_down [E,H,I].  Workspace:
+ * moe_workspace_size(d, 1 or 2, ...).
+ *
+ * moe_router_bwd: the router part on the tokens' rank.  d: the rank's own
+ * dims (T tokens, E = all experts, k), I_shared = 0; x, w_router and the
+ * forward's routing (topk_idx, topk_w, expert_offsets, perm_slot, slot_perm);
+ * dx_sorted bf16 [T*k, H] and dw_sorted fp32 [T*k]: the slots' dx and dw in
+ * the rank's sorted order (slot s at row slot_perm[s]).  Writes grad_x
+ * [T,H], grad_w_router [E,H] (this rank's tokens' part), grad_router_bias fp32
+ * [E] or NULL.  No auxiliary loss in this form.  Workspace as moe_layer_bwd.
+ *
+ * Errors: MOE_ERR_INVALID_ARG (null, misaligned), MOE_ERR_UNSUPPORTED_SHAPE,
+ * MOE_ERR_WORKSPACE_TOO_SMALL, MOE_ERR_CUDA; device-detected bad indices in the
+ * workspace's status word.
+ */
+moe_status moe_experts_bwd(const moe_dims* d, const moe_bf16* grad_out_rows,
+                           const moe_bf16* x_rows, const float* row_w,
+                           const int32_t* expert_offsets, const int32_t* perm_slot,
+                           const int32_t* slot_perm, const moe_bf16* w_gate_up,
+                           const moe_bf16* w_down, const moe_bf16* gu_saved, moe_bf16* dx_rows,
+                           float* dw_rows, moe_bf16* grad_w_gate_up, moe_bf16* grad_w_down,
+                           void* workspace, size_t workspace_bytes, void* stream);
+moe_status moe_router_bwd(const moe_dims* d, const moe_bf16* x, const moe_bf16* w_router,
+                          const int32_t* topk_idx, const float* topk_w,
+                          const int32_t* expert_offsets, const int32_t* perm_slot,
+                          const int32_t* slot_perm, const moe_bf16* dx_sorted,
+                          const float* dw_sorted, moe_bf16* grad_x, moe_bf16* grad_w_router,
+                          float* grad_router_bias, void* workspace, size_t workspace_bytes,
+                          void* stream);
+
+/*
  * Kernel accounting, for benchmarks and tests (no counterpart on the pages).
  * Every kernel the calls above launch is counted under one of the ids below.
  * While timing is enabled, each launch is also bracketed by a pair of CUDA
@@ -384,6 +447,8 @@ typedef enum {
                                 the per-token gather adds the slot gradients into it */
   MOE_K_GATHER_ROWS,         /* moe_gather_rows */
   MOE_K_EP_LAYOUT,           /* moe_ep_receive_layout */
+  MOE_K_EP_ROWS_OUT,         /* moe_experts_bwd: the slots' dx and dw back in receive order */
+  MOE_K_GATHER_SCALARS,      /* moe_gather_scalars */
   MOE_K_COUNT
 } moe_kernel_id;
 

@@ -369,6 +369,14 @@ def layer_forward(x, w_router, w_gu, w_down, k, balanced=False, bias=None,
 # * each output row goes back to its source in the order it came, so the
 #   source holds its rows' outputs in its own sorted order and combines them
 #   exactly as on one rank.
+# * backward (the pages time the backward but give no layout for it): the
+#   reverse trip.  A source sends every slot's grad_out row and routing
+#   weight in its sorted order, as it sent the token rows; the experts' rank
+#   forms each row's dx and dL/dw and its experts' weight gradients, and sends
+#   dx and dL/dw back; the source sums its tokens' slot gradients and runs the
+#   router's backward.  The router is replicated, so each rank's router
+#   gradient covers its own tokens and the ranks' gradients add up (as data
+#   parallelism adds any replicated parameter's).
 
 
 def ep_expert_ranges(E: int, n_ranks: int) -> np.ndarray:
@@ -479,6 +487,108 @@ def ep_layer_forward(x_ranks, w_router, w_gu, w_down, k, balanced=False, bias=No
         out = combine(y_sorted, src[s]["slot_perm"], src[s]["topk_w"])
         outs.append(dict(src[s], y_sorted=y_sorted, out=out, **dst[s]))
     return outs
+
+
+def ep_experts_backward(x_recv, go_recv, w_recv, local_offsets, recv_perm, w_gu_loc, w_down_loc):
+    """The experts' rank's part of the expert-parallel backward.
+
+    Received rows (receive order): token rows x_recv [R, H], their grad_out
+    rows go_recv [R, H] and routing weights w_recv [R]; the grouping of
+    ep_receive.  Per local expert e, for its rows: y = MLP_e(x), dL/dw =
+    <dout, y>, the expert sees dy = w dout (as layer_backward).  Returns
+    (dx_recv [R, H], dw_recv [R], dW_gu [E_loc, 2I, H], dW_down [E_loc, H, I]).
+    """
+    R, H = x_recv.shape
+    E_loc = w_gu_loc.shape[0]
+    dx = np.zeros((R, H))
+    dw = np.zeros(R)
+    dW_gu = np.zeros_like(w_gu_loc)
+    dW_down = np.zeros_like(w_down_loc)
+    for e in range(E_loc):
+        rows = np.asarray(recv_perm[int(local_offsets[e]):int(local_offsets[e + 1])], dtype=np.int64)
+        if rows.size == 0:
+            continue
+        y, gu, _ = swiglu_mlp(x_recv[rows], w_gu_loc[e], w_down_loc[e])
+        dw[rows] = np.sum(go_recv[rows] * y, axis=1)
+        dy = np.asarray(w_recv)[rows][:, None] * go_recv[rows]
+        dx[rows], dW_gu[e], dW_down[e] = swiglu_mlp_backward(x_recv[rows], gu, w_gu_loc[e],
+                                                              w_down_loc[e], dy)
+    return dx, dw, dW_gu, dW_down
+
+
+def router_backward(x, w_router, topk_idx, topk_w, dw):
+    """The router's backward from each slot's dL/dw (no auxiliary loss).
+
+    The renormalised weights are a softmax over the chosen logits, so the
+    gradient reaches only those: dl[t, e_j] = w_j (dw_j - sum_i w_i dw_i), and
+    0 at every other expert.  Returns (dl [T, E], dx_router = dl W_r,
+    dW_r = dl^T x, db = sum_t dl).
+    """
+    T = x.shape[0]
+    E = w_router.shape[0]
+    w = np.asarray(topk_w, dtype=np.float64)
+    dwv = np.asarray(dw, dtype=np.float64)
+    dl_sel = w * (dwv - np.sum(w * dwv, axis=1, keepdims=True))
+    dl = np.zeros((T, E))
+    np.add.at(dl, (np.repeat(np.arange(T), topk_idx.shape[1]), np.asarray(topk_idx).ravel()),
+              dl_sel.ravel())
+    return dl, dl @ w_router, dl.T @ x, dl.sum(axis=0)
+
+
+def ep_layer_backward(ranks, grad_out_ranks, x_ranks, w_router, w_gu, w_down):
+    """The backward over n ranks with expert parallelism, every step written out.
+
+    ranks: ep_layer_forward's per-rank dicts; grad_out_ranks[r]: rank r's
+    dL/d(out) [T_r, H].  Each source gathers its slots' grad_out rows and
+    weights in its sorted order and sends block q to rank q; rank q runs
+    ep_experts_backward on what it received (rows in the forward's receive
+    order) and sends dx and dL/dw back in the order they came; the source
+    sums each token's slot gradients and adds the router's term.  Returns a
+    list of per-rank dicts: grad_x, grad_w_router and grad_router_bias (over
+    the rank's tokens), the rank's local expert gradients, and the exchanged
+    buffers.
+    """
+    n = len(ranks)
+    E = w_gu.shape[0]
+    k = ranks[0]["topk_idx"].shape[1] if len(ranks) else 1
+    b = ep_expert_ranges(E, n)
+    send = []
+    for r in range(n):
+        perm = ranks[r]["perm_slot"].astype(np.int64)
+        send.append(dict(go=grad_out_ranks[r][perm // k], w=np.asarray(ranks[r]["topk_w"]).ravel()[perm]))
+    back = []
+    for q in range(n):
+        off = [ranks[s]["expert_offsets"] for s in range(n)]
+        go_recv = np.concatenate([send[s]["go"][int(off[s][b[q]]):int(off[s][b[q + 1]])]
+                                  for s in range(n)], axis=0)
+        w_recv = np.concatenate([send[s]["w"][int(off[s][b[q]]):int(off[s][b[q + 1]])]
+                                 for s in range(n)], axis=0)
+        dx_recv, dw_recv, dW_gu, dW_down = ep_experts_backward(
+            ranks[q]["x_recv"], go_recv, w_recv, ranks[q]["local_offsets"], ranks[q]["recv_perm"],
+            w_gu[b[q]:b[q + 1]], w_down[b[q]:b[q + 1]])
+        back.append(dict(go_recv=go_recv, w_recv=w_recv, dx_recv=dx_recv, dw_recv=dw_recv,
+                         grad_w_gate_up=dW_gu, grad_w_down=dW_down))
+    res = []
+    for s in range(n):
+        parts_dx, parts_dw = [], []
+        for q in range(n):
+            start = int(sum(ranks[q]["recv_counts"][:s]))
+            cnt = int(ranks[q]["recv_counts"][s])
+            parts_dx.append(back[q]["dx_recv"][start:start + cnt])
+            parts_dw.append(back[q]["dw_recv"][start:start + cnt])
+        H = x_ranks[s].shape[1]
+        dx_sorted = np.concatenate(parts_dx, axis=0) if parts_dx else np.zeros((0, H))
+        dw_sorted = np.concatenate(parts_dw, axis=0) if parts_dw else np.zeros(0)
+        T = x_ranks[s].shape[0]
+        inv = ranks[s]["slot_perm"].astype(np.int64)
+        dx_slot = dx_sorted[inv].reshape(T, k, H)
+        dw = dw_sorted[inv].reshape(T, k)
+        _, dx_router, dW_r, db = router_backward(x_ranks[s], w_router, ranks[s]["topk_idx"],
+                                                 ranks[s]["topk_w"], dw)
+        res.append(dict(grad_x=dx_slot.sum(axis=1) + dx_router, grad_w_router=dW_r,
+                        grad_router_bias=db, dx_sorted=dx_sorted, dw_sorted=dw_sorted,
+                        **back[s]))
+    return res
 
 
 # --------------------------------------------------------------------------

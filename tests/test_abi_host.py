@@ -35,7 +35,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert M.moe_abi_version() == 11
+    assert M.moe_abi_version() == 12
     assert M.moe_status_string(0) == "ok"
     for s in range(1, 7):
         assert M.moe_status_string(s) not in ("ok", "unknown status")
@@ -188,3 +188,48 @@ def test_expert_parallel_calls_validate_before_launch(lib):
     assert L(64, 128, p, 0, p, None, None, None, None) == 2   # > 4096 cells
     assert "moe_gather_rows" in M.declared_functions()
     assert "moe_ep_receive_layout" in M.declared_functions()
+
+
+def test_expert_parallel_backward_calls_validate_before_launch(lib):
+    """The two halves of the expert-parallel backward and the scalar gather
+    refuse bad arguments before launching anything."""
+    dims_loc = M.MoeDims.of(64, 256, 4, 1, 512, 0)      # rows received, local experts, k = 1
+    dims_src = M.MoeDims.of(32, 256, 8, 2, 512, 0)
+    nbytes = max(M.moe_workspace_size(dims_loc, 1), M.moe_workspace_size(dims_src, 1))
+    ws = ctypes.create_string_buffer(nbytes + 256)
+    p = (ctypes.addressof(ws) + 255) // 256 * 256
+
+    def experts(d, dx=p, dw=p, row_w=p, n=nbytes):
+        # grad_out_rows, x_rows, row_w, offsets, perm_slot, slot_perm, w_gate_up, w_down,
+        # gu_saved, dx_rows, dw_rows, grad_w_gate_up, grad_w_down
+        a = [p, p, row_w, p, p, p, p, p, p, dx, dw, p, p]
+        return lib.moe_experts_bwd(ctypes.byref(d), *a, p, n, None)
+
+    assert experts(M.MoeDims.of(64, 256, 4, 2, 512, 0)) == 2      # k != 1
+    assert experts(M.MoeDims.of(64, 256, 4, 1, 512, 128)) == 2    # a shared expert
+    assert experts(dims_loc, dx=None) == 1                        # nowhere to put dx
+    assert experts(dims_loc, dw=None) == 1
+    assert experts(dims_loc, row_w=None) == 1                     # no routing weights
+    assert experts(dims_loc, dx=p + 8) == 1                       # misaligned rows
+    assert experts(dims_loc, n=256) == 3                          # workspace too small
+
+    def router(d, dxs=p, dws=p, gx=p):
+        # x, w_router, topk_idx, topk_w, offsets, perm_slot, slot_perm, dx_sorted,
+        # dw_sorted, grad_x, grad_w_router, grad_router_bias
+        a = [p, p, p, p, p, p, p, dxs, dws, gx, p, None]
+        return lib.moe_router_bwd(ctypes.byref(d), *a, p, nbytes, None)
+
+    assert router(M.MoeDims.of(32, 256, 8, 2, 512, 128)) == 2     # a shared expert
+    assert router(dims_src, dxs=None) == 1                        # no slot gradients
+    assert router(dims_src, dws=None) == 1
+    assert router(dims_src, gx=None) == 1                         # nowhere to put grad_x
+    assert router(dims_src, dxs=p + 8) == 1
+
+    g = lib.moe_gather_scalars
+    assert g(p, 10, p, 0, 1, p, None, None) == 0                  # nothing to copy
+    assert g(None, 10, p, 4, 1, p, None, None) == 1
+    assert g(p, 10, p, 4, 0, p, None, None) == 1                  # div < 1
+    assert g(p, 10, p, -1, 1, p, None, None) == 1
+    assert g(p + 2, 10, p, 4, 1, p, None, None) == 1              # not 4-byte aligned
+    for name in ("moe_experts_bwd", "moe_router_bwd", "moe_gather_scalars"):
+        assert name in M.declared_functions()

@@ -146,3 +146,67 @@ def test_ep_layer_on_the_seeded_inputs():
                               f(n_["w_down"]), w.k, bias=bias)
     ref = O.layer_forward(x, f(n_["w_router"]), f(n_["w_gate_up"]), f(n_["w_down"]), w.k, bias=bias)
     assert np.allclose(np.concatenate([o["out"] for o in outs]), ref["out"], rtol=1e-13, atol=1e-16)
+
+
+@pytest.mark.parametrize("E,n,Ts,k", [(8, 2, [24, 17], 2), (6, 4, [9, 0, 11, 8], 3),
+                                      (16, 4, [12, 12, 12, 12], 4), (5, 3, [7, 3, 10], 5)])
+def test_ep_backward_equals_one_rank_backward(E, n, Ts, k):
+    """Every gradient of the n-rank backward equals the one-rank layer_backward
+    (pinned by finite differences): grad_x rank by rank, the local experts'
+    weight gradients chunk by chunk, and the router's summed over the ranks.
+    The router step here (dl from w and dL/dw only) is a different formula from
+    layer_backward's (through the softmax p), so their equality also pins it."""
+    H, I = 16, 12
+    wr, wgu, wd = _weights(E, H, I, seed=E + n + 1)
+    r = np.random.default_rng(E * n + 1)
+    xs = [r.normal(0, 1, (T, H)) for T in Ts]
+    gos = [r.normal(0, 1, (T, H)) for T in Ts]
+    fwd = O.ep_layer_forward(xs, wr, wgu, wd, k)
+    got = O.ep_layer_backward(fwd, gos, xs, wr, wgu, wd)
+    x_all = np.concatenate(xs, axis=0)
+    ref_f = O.layer_forward(x_all, wr, wgu, wd, k)
+    ref = O.layer_backward(ref_f, np.concatenate(gos, axis=0), x_all, wr, wgu, wd, k)
+    tol = dict(rtol=1e-11, atol=1e-13)
+    assert np.allclose(np.concatenate([g["grad_x"] for g in got], axis=0), ref["grad_x"], **tol)
+    assert np.allclose(sum(g["grad_w_router"] for g in got), ref["grad_w_router"], **tol)
+    assert np.allclose(sum(g["grad_router_bias"] for g in got), ref["grad_router_bias"], **tol)
+    b = O.ep_expert_ranges(E, n)
+    for q in range(n):
+        assert np.allclose(got[q]["grad_w_gate_up"], ref["grad_w_gate_up"][b[q]:b[q + 1]], **tol)
+        assert np.allclose(got[q]["grad_w_down"], ref["grad_w_down"][b[q]:b[q + 1]], **tol)
+    # each source's slots' dL/dw, back in its sorted order, are layer_backward's
+    start = 0
+    for g, o, T in zip(got, fwd, Ts):
+        dw_slot = g["dw_sorted"][o["slot_perm"].astype(np.int64)].reshape(T, k)
+        assert np.allclose(dw_slot, ref["grad_topk_w"][start:start + T], **tol)
+        start += T
+
+
+def test_router_backward_is_zero_off_the_chosen_experts():
+    """dl vanishes at every expert a token did not choose, and its row sums are
+    zero (the renormalised weights sum to one whatever the logits)."""
+    r = np.random.default_rng(9)
+    T, E, k, H = 20, 10, 3, 8
+    idx = np.stack([r.choice(E, size=k, replace=False) for _ in range(T)]).astype(np.int32)
+    w = r.random((T, k)); w /= w.sum(axis=1, keepdims=True)
+    dl, _, _, _ = O.router_backward(r.normal(0, 1, (T, H)), r.normal(0, 1, (E, H)), idx, w,
+                                    r.normal(0, 1, (T, k)))
+    chosen = np.zeros((T, E), dtype=bool)
+    chosen[np.repeat(np.arange(T), k), idx.ravel()] = True
+    assert np.all(dl[~chosen] == 0.0)
+    assert np.allclose(dl.sum(axis=1), 0.0, atol=1e-14)
+
+
+def test_returning_dx_unsorted_is_caught():
+    """Planted in the oracle: the source takes the returned dx rows in slot
+    order instead of its sorted order; grad_x then no longer matches."""
+    E, n, Ts, k, H, I = 8, 2, [20, 20], 2, 16, 12
+    wr, wgu, wd = _weights(E, H, I, seed=6)
+    xs = [np.random.default_rng(6 + i).normal(0, 1, (T, H)) for i, T in enumerate(Ts)]
+    gos = [np.random.default_rng(60 + i).normal(0, 1, (T, H)) for i, T in enumerate(Ts)]
+    fwd = O.ep_layer_forward(xs, wr, wgu, wd, k)
+    got = O.ep_layer_backward(fwd, gos, xs, wr, wgu, wd)
+    g, o = got[0], fwd[0]
+    right = g["dx_sorted"][o["slot_perm"].astype(np.int64)].reshape(Ts[0], k, H).sum(axis=1)
+    wrong = g["dx_sorted"].reshape(Ts[0], k, H).sum(axis=1)
+    assert not np.allclose(right, wrong)

@@ -186,3 +186,87 @@ def test_gather_rows_kernel():
     torch.cuda.synchronize()
     assert int(st.item()) == 5
     assert torch.equal(dstb[0], src[1]) and torch.count_nonzero(dstb[1]) == 0
+
+
+def _run_ep_train(name, seed=0):
+    """Forward and backward of the expert-parallel layer, ranks as threads."""
+    E, world, Ts, k, H, I, bs = CASES[name]
+    w = G.Workload(name, T=sum(Ts), H=H, E=E, k=k, I=I, bias_std=bs)
+    di = U.DeviceInputs(w, seed=seed, with_grad=True)
+    b = ep.expert_ranges(E, world)
+    ex = ThreadExchange(world)
+    starts = np.cumsum([0] + Ts)
+    layers = [ep.ExpertParallelMoe((Ts[r], H, E, k, I), r, world, ex.rank_view(r), with_backward=True)
+              for r in range(world)]
+    grads, errs = [None] * world, []
+
+    def run(r):
+        try:
+            sl = slice(int(starts[r]), int(starts[r + 1]))
+            xr = di.x[sl].contiguous()
+            wgu, wd = di.w_gate_up[b[r]:b[r + 1]].contiguous(), di.w_down[b[r]:b[r + 1]].contiguous()
+            layers[r].forward(xr, di.w_router, wgu, wd, di.router_bias)
+            grads[r] = layers[r].backward(di.grad_out[sl].contiguous(), xr, di.w_router, wgu, wd,
+                                          with_bias=True)
+            torch.cuda.synchronize()
+        except Exception as e:   # surfaced below
+            errs.append(e)
+            ex.barrier.abort()
+
+    th = [threading.Thread(target=run, args=(r,)) for r in range(world)]
+    for t in th:
+        t.start()
+    for t in th:
+        t.join()
+    if errs:
+        raise errs[0]
+    for L in layers:
+        assert L.ops.status() == 0
+    return di, w, layers, grads
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_expert_parallel_backward_bit_exact_against_one_gpu(name):
+    """grad_x and every local expert's weight gradients equal moe_layer_bwd on
+    all ranks' tokens with the ranks' routing bit for bit; the router's weight
+    and bias gradients, formed by each rank over its own tokens, add up to the
+    one-GPU ones within their rounding."""
+    di, w, layers, grads = _run_ep_train(name)
+    E, world = w.E, CASES[name][1]
+    idx, tw, _, _, _ = _one_gpu_with_ranks_routing(di, w, layers)
+    dims = (w.T, w.H, w.E, w.k, w.I, 0)
+    ws = torch.zeros(M.moe_workspace_size(dims, True), dtype=torch.uint8, device="cuda")
+    S = w.T * w.k
+    off = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    perm = torch.empty(S, dtype=torch.int32, device="cuda")
+    inv = torch.empty(S, dtype=torch.int32, device="cuda")
+    M.moe_permute(dims, idx, off, perm, inv, ws)
+    y = torch.empty(S, w.H, dtype=torch.bfloat16, device="cuda")
+    gu = torch.empty(S, 2 * w.I, dtype=torch.bfloat16, device="cuda")
+    M.moe_grouped_mlp_fwd(dims, di.x, off, perm, di.w_gate_up, di.w_down, gu, y, None, None, None,
+                          None, ws)
+    gx = torch.empty(w.T, w.H, dtype=torch.bfloat16, device="cuda")
+    gwr = torch.empty(E, w.H, dtype=torch.bfloat16, device="cuda")
+    gb = torch.empty(E, dtype=torch.float32, device="cuda")
+    gwgu = torch.empty_like(di.w_gate_up)
+    gwd = torch.empty_like(di.w_down)
+    M.moe_layer_bwd(dims, di.grad_out, di.x, di.w_router, idx, tw, off, perm, inv, di.w_gate_up,
+                    di.w_down, gu, None, None, None, gx, gwr, gb, gwgu, gwd, None, None, ws)
+    torch.cuda.synchronize()
+    assert M.moe_read_device_status(ws) == 0
+    got_x = torch.cat([g["grad_x"] for g in grads])
+    assert torch.equal(got_x.view(torch.int16), gx.view(torch.int16))
+    b = ep.expert_ranges(E, world)
+    for r in range(world):
+        assert torch.equal(grads[r]["grad_w_gate_up"].view(torch.int16),
+                           gwgu[b[r]:b[r + 1]].view(torch.int16)), r
+        assert torch.equal(grads[r]["grad_w_down"].view(torch.int16),
+                           gwd[b[r]:b[r + 1]].view(torch.int16)), r
+    # router: per-rank bf16 parts against the one-GPU bf16 whole
+    parts = [g["grad_w_router"].double().cpu() for g in grads]
+    one = gwr.double().cpu()
+    err = (sum(parts) - one).abs()
+    bound = 2.0 ** -7 * (sum(p.abs() for p in parts) + one.abs()) + 1e-6 * float(one.abs().max())
+    assert bool((err <= bound).all()), float((err - bound).max())
+    bsum = sum(g["grad_router_bias"].double().cpu() for g in grads)
+    assert torch.allclose(bsum, gb.double().cpu(), rtol=1e-4, atol=1e-6 * float(gb.abs().max()))

@@ -11,18 +11,21 @@
 // tensors, and the activations' token rows are gathered through the sort
 // inside the kernel (no expert-sorted copy of them is written).
 //
-// Roles (one CTA per SM, static round-robin over tiles):
+// Roles (one CTA per SM, static round-robin over tiles, or units handed out
+// as CTAs free up in the consumer of a cross-kernel overlap):
 //   warp 0     TMA producer: fills a STAGES-deep ring of (A, B) k-blocks
 //   warp 1     TMEM allocator and single-thread UMMA issuer
 //   warps 2..  EPI_WARPS epilogue warps: warp w reads TMEM lanes
 //              32*(w%4) .. 32*(w%4)+31; with 8 epilogue warps the two warps of
 //              a lane quadrant split the tile's columns in halves
-//   last 4     gather warps (only when an operand is gathered): copy the
+//   then 4     gather warps (only when an operand is gathered): copy the
 //              token rows of that operand straight from the unsorted matrix
 //              into the swizzled stage with 16-byte cp.async (LSU path), so
 //              no expert-sorted copy of the activations is ever written
+//   last       (dynamic units only) the scheduler warp
 // Two TMEM accumulators (2 x BN fp32 columns) let the epilogue of tile i run
-// while the mainloop of tile i+1 fills the other one.
+// while the mainloop of tile i+1 fills the other one; a WIDE unit takes both
+// for two n-blocks that share every A stage (see GemmCfg).
 //
 // Schedules:
 //   RAGGED_M  groups are row ranges of A/D (forward and data-gradient GEMMs);

@@ -114,6 +114,13 @@ def test_qwen3_shape_full_oracle(name):
     U.check_close(layer.gu_saved, f["gu_perm"], "gu_saved")
     U.check_close(layer.y_perm, f["y_perm"], "y_perm")
     U.check_close(layer.out, f["out"], "out")
+    # the inference forward (h only: wide gate/up units, bench.py's forward)
+    # gives the same bits at this size too
+    inf = U.run_forward(di, with_backward=False, save_logits=False)
+    assert M.moe_read_device_status(inf.workspace) == 0
+    assert torch.equal(inf.y_perm.view(torch.int16), layer.y_perm.view(torch.int16))
+    assert torch.equal(inf.out.view(torch.int16), layer.out.view(torch.int16))
+    del inf
     if not di.w.backward:
         return
     grads = _backward(di, layer, di.grad_out)

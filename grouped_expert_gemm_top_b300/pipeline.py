@@ -11,6 +11,12 @@ while step i computes on the caller's stream, ordered by CUDA events:
   * a step writes its out/grad_x into slot s only after the read-back of the
     step that last used the slot has finished.
 
+Within a step the forward and the backward are ordered separately: the
+forward waits only for x, the backward for grad_out, and out goes back as
+soon as the forward has written it, so a step's grad_out copy and out
+read-back overlap its own compute (this matters for the first and last steps
+of a run, which have no neighbours to hide behind).
+
 Every copy still happens once per step; only their overlap with compute
 changes.  This is stream plumbing: the copies are cudaMemcpyAsync (through
 torch), and every step of the layer runs in the library's kernels.
@@ -45,9 +51,10 @@ class HostStepPipeline:
         self.gx = [torch.empty(T, H, dtype=bf, device=dev) for _ in range(slots)]
         self.h2d = torch.cuda.Stream(device=dev)
         self.d2h = torch.cuda.Stream(device=dev)
-        self.in_ready = [torch.cuda.Event() for _ in range(slots)]
-        self.computed = [torch.cuda.Event() for _ in range(slots)]
-        self.read_back = [torch.cuda.Event() for _ in range(slots)]
+        ev = lambda: [torch.cuda.Event() for _ in range(slots)]
+        self.x_ready, self.go_ready = ev(), ev()
+        self.fwd_done, self.computed = ev(), ev()
+        self.out_back, self.gx_back = ev(), ev()
         self.used = [False] * slots
         self.i = 0
         self.graphs = None
@@ -56,20 +63,26 @@ class HostStepPipeline:
             side.wait_stream(torch.cuda.current_stream(dev))
             with torch.cuda.stream(side):
                 for s in range(slots):
-                    self._compute(s)
+                    self._forward(s)
+                    self._backward(s)
             torch.cuda.current_stream(dev).wait_stream(side)
             self.graphs = []
             for s in range(slots):
-                g = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g):
-                    self._compute(s)
-                self.graphs.append(g)
+                gf, gb = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+                with torch.cuda.graph(gf):
+                    self._forward(s)
+                with torch.cuda.graph(gb):
+                    self._backward(s)
+                self.graphs.append((gf, gb))
 
-    def _compute(self, s):
+    def _forward(self, s):
         w = self.w
         self.layer.forward(self.x[s], w["w_router"], w["w_gate_up"], w["w_down"],
                            w.get("router_bias"), w.get("w_sh_gate_up"), w.get("w_sh_down"),
                            out=self.out[s])
+
+    def _backward(self, s):
+        w = self.w
         g = dict(self.grads)
         g["grad_x"] = self.gx[s]
         self.layer.backward(self.go[s], self.x[s], w["w_router"], w["w_gate_up"], w["w_down"], g,
@@ -87,21 +100,32 @@ class HostStepPipeline:
             if self.used[s]:
                 self.h2d.wait_event(self.computed[s])   # the step that last read slot s
             self.x[s].copy_(x_host, non_blocking=True)
+            self.x_ready[s].record(self.h2d)
             self.go[s].copy_(go_host, non_blocking=True)
-            self.in_ready[s].record(self.h2d)
-        compute.wait_event(self.in_ready[s])
+            self.go_ready[s].record(self.h2d)
+        compute.wait_event(self.x_ready[s])
         if self.used[s]:
-            compute.wait_event(self.read_back[s])       # slot s's results were read back
+            compute.wait_event(self.out_back[s])        # slot s's out was read back
         if self.graphs is not None:
-            self.graphs[s].replay()
+            self.graphs[s][0].replay()
         else:
-            self._compute(s)
+            self._forward(s)
+        self.fwd_done[s].record(compute)
+        compute.wait_event(self.go_ready[s])
+        if self.used[s]:
+            compute.wait_event(self.gx_back[s])         # slot s's grad_x was read back
+        if self.graphs is not None:
+            self.graphs[s][1].replay()
+        else:
+            self._backward(s)
         self.computed[s].record(compute)
         with torch.cuda.stream(self.d2h):
-            self.d2h.wait_event(self.computed[s])
+            self.d2h.wait_event(self.fwd_done[s])
             out_host.copy_(self.out[s], non_blocking=True)
+            self.out_back[s].record(self.d2h)
+            self.d2h.wait_event(self.computed[s])
             gx_host.copy_(self.gx[s], non_blocking=True)
-            self.read_back[s].record(self.d2h)
+            self.gx_back[s].record(self.d2h)
         self.used[s] = True
         self.i += 1
 
@@ -110,7 +134,8 @@ class HostStepPipeline:
         compute = torch.cuda.current_stream(self.x[0].device)
         for s in range(self.n):
             if self.used[s]:
-                compute.wait_event(self.read_back[s])
+                compute.wait_event(self.out_back[s])
+                compute.wait_event(self.gx_back[s])
 
     @property
     def h2d_bytes_per_step(self) -> int:

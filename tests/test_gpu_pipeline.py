@@ -1,7 +1,7 @@
 """The host-fed step pipeline against plain steps.
 
 Copies overlapped with compute must not change a bit of any step's results:
-three steps with different host inputs through the pipeline give the same
+five steps with different host inputs through the pipeline give the same
 out and grad_x per step, and the same weight gradients after the last step,
 as the same steps run one after the other on one stream.
 """
@@ -26,7 +26,7 @@ def test_pipelined_steps_match_plain_steps(shared, use_graph):
                    router_bias=di.router_bias, w_sh_gate_up=di.w_sh_gate_up, w_sh_down=di.w_sh_down)
     r = np.random.default_rng(9)
     steps = []
-    for _ in range(3):
+    for _ in range(5):   # every slot reused twice
         x = torch.from_numpy(r.normal(size=(w.T, w.H)).astype(np.float32)).to(torch.bfloat16)
         go = torch.from_numpy(r.normal(size=(w.T, w.H)).astype(np.float32)).to(torch.bfloat16)
         steps.append((x.pin_memory(), go.pin_memory()))

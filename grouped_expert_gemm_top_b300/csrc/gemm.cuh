@@ -89,7 +89,7 @@ struct GemmArgs {
 
 template <int BN_, int STAGES_, int AL_, int BL_, int SCH_, int EPI_, bool B3D_, bool SWIGLU_B_,
           int EPI_WARPS_ = 4, bool PAIR_ = false, int EPI_BUFS_ = 3, bool DYN_ = false,
-          bool WIDE_ = false>
+          bool WIDE_ = false, bool NARROW_ = false>
 struct GemmCfg {
   // WIDE: a unit is two adjacent n-blocks that share every A stage: each stage
   // carries two B tiles, and the two TMEM accumulators (all 512 columns) take
@@ -99,6 +99,14 @@ struct GemmCfg {
   // both.  (Gate/up GEMM with SwiGLU only.)
   static constexpr bool WIDE = WIDE_;
   static constexpr int NSUB = WIDE ? 2 : 1;  // n-blocks (accumulators) per unit
+  // NARROW (wide gate/up GEMM): a pair unit whose odd m-block would hold no
+  // rows (an expert's last <= 128 rows) swaps the operands' roles: each CTA
+  // stages gate and up rows of the same 128 columns, the UMMAs' 256-row sides,
+  // and its half of the token rows, their N side (N = the rows rounded up to
+  // 32), so the tensor work follows the tokens instead of a full 256-row
+  // tile.  TMEM lanes are then intermediate columns and TMEM columns tokens;
+  // the epilogue stores each thread's column of h directly.
+  static constexpr bool NARROW = NARROW_;
   // DYN: units handed out dynamically (consumer side of a cross-kernel overlap)
   static constexpr bool DYN = DYN_;
   // PAIR: 2-CTA clusters computing one 256 x BN tile with CTA-pair UMMAs
@@ -166,6 +174,8 @@ struct GemmCfg {
   static_assert(!DYN || STAGES_ + 2 + 2 + 1 < 32, "unit ring deeper than any role's lag");
   static_assert(!WIDE || (PAIR && BL_ == KMAJ_TILE && EPI_ == EPI_SWIGLU && SWIGLU_B_ && !DYN_),
                 "wide units: the CTA-pair gate/up GEMM");
+  static_assert(!NARROW || (WIDE && AL_ == KMAJ_GATHER && SCH_ == RAGGED_M),
+                "narrow units: the wide gate/up GEMM");
 };
 
 struct TileInfo {
@@ -173,9 +183,25 @@ struct TileInfo {
   bool phantom;    // pair slot past the group's last M-tile: loads only, no output
   int row0;        // RAGGED_M: first row of the M-tile in the A/D row space
   int rows_valid;  // RAGGED_M: rows of the group inside this tile (<= 128)
+  int narrow;      // NARROW unit: its token columns (rows_valid rounded up to 32;
+                   // row0, rows_valid: the pair's, the same in both CTAs); else 0
   int kstart;      // RAGGED_K: first K row of the group
   int kblocks;     // number of 64-deep k-blocks
 };
+
+// The unit's token columns when it is a NARROW unit of config C, else 0.
+template <class C>
+__device__ __forceinline__ int narrow_cols(const TileInfo& ti) {
+  if constexpr (C::NARROW) return ti.narrow;
+  else return 0;
+}
+
+// First row (within the tile) of this CTA's staged token rows: a NARROW unit's
+// N side is split between the pair, rank r staging rows [r N/2, (r+1) N/2).
+template <class C>
+__device__ __forceinline__ int tile_row_base(const TileInfo& ti, int rank) {
+  return rank * (narrow_cols<C>(ti) / 2);
+}
 
 struct SmemTables {
   int tile_prefix[kMaxGroups + 1];
@@ -348,6 +374,17 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, const SmemTab
     ti.phantom = ti.mb >= mt;
     ti.row0 = T.start[lo] + ti.mb * BM;
     ti.rows_valid = ti.phantom ? 0 : min(BM, T.cnt[lo] - ti.mb * BM);
+    ti.narrow = 0;
+    if constexpr (C::NARROW) {
+      const int mbe = ti.mb - rank;  // the pair's even m-block
+      if (mbe + 1 == mt) {
+        ti.mb = mbe;
+        ti.phantom = false;
+        ti.row0 = T.start[lo] + mbe * BM;
+        ti.rows_valid = T.cnt[lo] - mbe * BM;
+        ti.narrow = (ti.rows_valid + 31) & ~31;
+      }
+    }
     ti.kstart = 0;
     ti.kblocks = a.K / BK;
   } else {
@@ -366,6 +403,7 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, const SmemTab
     ti.phantom = ti.mb >= nMB;
     ti.row0 = ti.mb * BM;
     ti.rows_valid = ti.phantom ? 0 : min(BM, a.M - ti.mb * BM);
+    ti.narrow = 0;
     ti.kstart = T.start[ti.g];
     ti.kblocks = (T.cnt[ti.g] + BK - 1) / BK;
   }
@@ -764,6 +802,45 @@ __device__ void epilogue_store(const GemmArgs& a, const TileInfo& ti, uint32_t t
   }
 }
 
+// NARROW units: TMEM lane = output column (weight row) of this CTA's 128, TMEM
+// column = token t of the pair's rows_valid rows (row0 + t).  Each thread
+// stores its column of every token directly: a warp writes 32 consecutive
+// bf16 (64 bytes) per token.  The two column parts of a lane quadrant take
+// alternate 32-token chunks.
+__device__ __forceinline__ void st_bf16_col(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
+
+// Wide gate/up GEMM: gate in columns [0, narrow), up in [narrow, 2 narrow) of
+// accumulator 0; h[row0 + t, j] for j = 128 ti.nb (the unit's first n-block) +
+// 128 rank + lane row.
+template <class C>
+__device__ __noinline__ void epilogue_narrow_swiglu(const GemmArgs& a, const TileInfo& ti, uint32_t tacc,
+                                       int row_in_tile, int rank, int cpart, int nparts) {
+  const int I = a.inter;
+  const int j = ti.nb * (C::BN / 2) + 128 * rank + row_in_tile;
+  const bool col_ok = j < I && a.h_out != nullptr;
+  __nv_bfloat16* hcol = a.h_out + (long long)ti.row0 * I + j;
+#pragma unroll 1
+  for (int c0 = 32 * cpart; c0 < ti.rows_valid; c0 += 32 * nparts) {
+    uint32_t g[32], u[32];
+    tmem_ld32_issue(tacc + c0, g);
+    tmem_ld32_issue(tacc + ti.narrow + c0, u);
+    tmem_ld_wait2(g, u);
+    // the sigmoids of columns 2m and 2m+1 share one reciprocal, as in the
+    // other gate/up epilogues (so h is the same bits whichever unit forms it):
+    // the pair's two columns are the lanes l and l^1
+    const bool odd = (row_in_tile & 1) != 0;
+    const int nt = min(32, ti.rows_valid - c0);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float gv = __uint_as_float(g[i]);
+      const float go = __shfl_xor_sync(0xffffffffu, gv, 1);
+      const float2 sg = odd ? sigmoid2_f(go, gv) : sigmoid2_f(gv, go);
+      if (col_ok && i < nt)
+        st_bf16_col(hcol + (long long)(c0 + i) * I, gv * (odd ? sg.y : sg.x) * __uint_as_float(u[i]));
+    }
+  }
+}
+
 // Down-projection data gradient with the SwiGLU backward fused in.
 // acc = dh_unw = dout[token] * W_down[e]  (columns n0.. of the intermediate)
 // From the saved pre-activations (g, u): h = silu(g) u; dw partial = <acc, h>;
@@ -934,7 +1011,8 @@ __device__ void gather_role(const GemmArgs& a, const SmemTables& T, uint32_t sme
     if constexpr (KM) {
 #pragma unroll
       for (int i = 0; i < 8; ++i)
-        src[i] = gather_row(a, T, ti.g, ti.mb * BM + gw * 32 + 4 * i + (lane >> 3));
+        src[i] = gather_row(a, T, ti.g,
+                            ti.mb * BM + tile_row_base<C>(ti, rank) + gw * 32 + 4 * i + (lane >> 3));
     } else {
       kid = gather_row(a, T, ti.g, gw * 16 + (lane & 15));
     }
@@ -948,7 +1026,8 @@ __device__ void gather_role(const GemmArgs& a, const SmemTables& T, uint32_t sme
         if (t_next < total) {
 #pragma unroll
           for (int i = 0; i < 8; ++i)
-            src_n[i] = gather_row(a, T, tn.g, tn.mb * BM + gw * 32 + 4 * i + (lane >> 3));
+            src_n[i] = gather_row(a, T, tn.g, tn.mb * BM + tile_row_base<C>(tn, rank) + gw * 32 +
+                                                  4 * i + (lane >> 3));
         }
       }
     }
@@ -965,10 +1044,14 @@ __device__ void gather_role(const GemmArgs& a, const SmemTables& T, uint32_t sme
     } else if constexpr (KM) {
       // rows of the M-tile past the group's rows are not copied: each feeds
       // only its own output row, which is never stored (K-side gathers below
-      // keep their finite padding rows, which multiply zeros)
+      // keep their finite padding rows, which multiply zeros).  A NARROW unit
+      // stages this CTA's half of its token columns, whose other rows are
+      // likewise never stored.
       const int c = lane & 7;
       const __nv_bfloat16* col = a.gsrc + kb * BK + c * 8;
-      const int nvalid = T.cnt[ti.g] - ti.mb * BM;
+      const int rb = tile_row_base<C>(ti, rank);
+      const int nvalid = narrow_cols<C>(ti) ? min(narrow_cols<C>(ti) / 2, ti.rows_valid - rb)
+                                            : T.cnt[ti.g] - ti.mb * BM;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int r = gw * 32 + 4 * i + (lane >> 3);
@@ -1121,6 +1204,52 @@ __device__ bool wide_unit(const TileInfo& ti, uint32_t smem_base, uint32_t tmem_
         mbar_arrive_remote(mapa_shared(smem_u32(&tfull_bar[b]), 1));
       }
     }
+  }
+  __syncwarp();
+  acc_phase ^= 1;
+  return true;
+}
+
+// The UMMA issuer's work for one NARROW wide unit: every stage's gate tile
+// (B tile 0) and up tile (B tile 1) are the 256-row sides of two pair UMMAs
+// with the stage's token rows as their N side, into columns [0, N) and [N, 2N)
+// of accumulator 0.  Accumulator 1 is left unwritten: it is handed to the
+// epilogue (which stores nothing for it) once free, keeping both barriers'
+// phases in step with the other units.
+template <class C>
+__device__ __noinline__ bool narrow_wide_unit(const TileInfo& ti, uint32_t smem_base, uint32_t tmem_base,
+                                 uint64_t* full_bar, uint64_t* empty_bar, uint64_t* tfull_bar,
+                                 uint64_t* tempty_bar, int& stage, uint32_t& phase,
+                                 uint32_t& acc_phase, int lane, volatile int* abort_flag,
+                                 int* status) {
+  const int nt = narrow_cols<C>(ti);
+  const uint32_t idesc = idesc_bf16_f32(2 * BM, nt, false, false);
+  if (!mbar_wait(smem_u32(&tempty_bar[0]), acc_phase ^ 1, abort_flag, status)) return false;
+  tc_fence_after();
+  for (int kb = 0; kb < ti.kblocks; ++kb) {
+    if (!mbar_wait(smem_u32(&full_bar[stage]), phase, abort_flag, status)) return false;
+    tc_fence_after();
+    if (lane == 0) {
+      const uint32_t sA = smem_base + stage * C::STAGE_BYTES;
+#pragma unroll
+      for (int w = 0; w < 2; ++w) {
+        const uint32_t sW = sA + C::A_BYTES + w * (C::B_ROWS * 128);
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk)
+          umma_bf16_pair(tmem_base + w * nt, smem_desc_sw128(sW + kk * 32, 16, 1024),
+                         smem_desc_sw128(sA + kk * 32, 16, 1024), idesc, (kb | kk) != 0 ? 1u : 0u);
+      }
+      umma_commit_pair(smem_u32(&empty_bar[stage]));
+    }
+    __syncwarp();
+    if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
+  }
+  if (lane == 0) umma_commit_pair(smem_u32(&tfull_bar[0]));
+  __syncwarp();
+  if (!mbar_wait(smem_u32(&tempty_bar[1]), acc_phase ^ 1, abort_flag, status)) return false;
+  if (lane == 0) {
+    mbar_arrive(smem_u32(&tfull_bar[1]));
+    mbar_arrive_remote(mapa_shared(smem_u32(&tfull_bar[1]), 1));
   }
   __syncwarp();
   acc_phase ^= 1;
@@ -1280,12 +1409,16 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         // ---- B
         if constexpr (C::PAIR && C::BL == KMAJ_TILE) {
           // this CTA's half of the B tile: 128 rows (SwiGLU: rank 0 gate, rank 1
-          // up); WIDE: the halves of two tiles, the second 128 columns further
+          // up); WIDE: the halves of two tiles, the second 128 columns further.
+          // A NARROW wide unit: CTA r takes gate rows n0 + 128 r (tile 0) and the
+          // up rows of the same columns (tile 1), the UMMAs' 256-row sides.
           if (lane == 0) {
 #pragma unroll
             for (int b = 0; b < C::NSUB; ++b) {
-              const int nc = C::SWIGLU_B ? (rank == 0 ? n0 : a.inter + n0) + 128 * b
-                                         : n0 + rank * 128;
+              const int nc = C::SWIGLU_B
+                                 ? (narrow_cols<C>(ti) ? (b == 0 ? n0 : a.inter + n0) + 128 * rank
+                                              : (rank == 0 ? n0 : a.inter + n0) + 128 * b)
+                                 : n0 + rank * 128;
               const uint32_t dst = sB + b * (C::B_ROWS * BK * 2);
               if constexpr (C::B3D) tma_load_3d_pair(dst, &tmB, fbp, kc, nc, ti.g);
               else tma_load_2d_pair(dst, &tmB, fbp, kx, nc);
@@ -1356,9 +1489,14 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         // the other.  Once accumulator 0 is free its UMMAs start; each stage is
         // held (not released to the producer) until accumulator 1 is free too
         // and the stage's second half has been issued.
-        if (!wide_unit<C>(ti, smem_base, tmem_base, full_bar, empty_bar, tfull_bar, tempty_bar, stage,
-                          phase, acc_phase, lane, abort_flag, a.status))
+        if (narrow_cols<C>(ti)) {
+          if (!narrow_wide_unit<C>(ti, smem_base, tmem_base, full_bar, empty_bar, tfull_bar,
+                                   tempty_bar, stage, phase, acc_phase, lane, abort_flag, a.status))
+            break;
+        } else if (!wide_unit<C>(ti, smem_base, tmem_base, full_bar, empty_bar, tfull_bar,
+                                 tempty_bar, stage, phase, acc_phase, lane, abort_flag, a.status)) {
           break;
+        }
         continue;
       }
       if (!mbar_wait(smem_u32(&tempty_bar[acc]), acc_phase ^ 1, abort_flag, a.status)) break;
@@ -1494,6 +1632,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const uint32_t tacc = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * C::BN;
         if (ti.phantom) {
           // pair slot past the group's last tile: nothing to store
+        } else if (narrow_cols<C>(ti)) {
+          // a NARROW unit: accumulator 0 holds both halves, accumulator 1 nothing
+          if constexpr (C::NARROW)
+            if (sub == 0) epilogue_narrow_swiglu<C>(a, ti, tacc, row_in_tile, rank, cpart, nparts);
         } else if constexpr (C::EPI == EPI_STORE_F32)
           epilogue_store_f32<C>(a, ti, tacc, row_in_tile, wo, &tmD0, cpart, nparts);
         else if constexpr (C::EPI == EPI_SWIGLU && C::EPI_COLS == 32)

@@ -285,9 +285,10 @@ using CfgGateUp = PairCfg<5, KMAJ_GATHER, KMAJ_TILE, RAGGED_M, EPI_SWIGLU, true,
 // the inference gate/up GEMM (h only): units of two n-blocks that share every
 // token-row stage; its epilogue is not hidden behind the next unit's mainloop,
 // so 8 warps share it (48 KB a stage: 4 stages and one 2 KB staging block a
-// warp fit)
-using CfgGateUpWide =
-    GemmCfg<256, 4, KMAJ_GATHER, KMAJ_TILE, RAGGED_M, EPI_SWIGLU, true, true, 8, true, 1, false, true>;
+// warp fit).  An expert's last <= 128 rows run as narrow units (the weights
+// taking the UMMAs' 256-row side).
+using CfgGateUpWide = GemmCfg<256, 4, KMAJ_GATHER, KMAJ_TILE, RAGGED_M, EPI_SWIGLU, true, true, 8,
+                              true, 1, false, true, true>;
 using CfgGateUpShared = PairCfg<5, KMAJ_TILE, KMAJ_TILE, RAGGED_M, EPI_SWIGLU, false, true>;
 // the down GEMM as the consumer of the gate/up GEMM's h, units taken as SMs free up
 using CfgDownDyn = GemmCfg<256, 5, KMAJ_TILE, KMAJ_TILE, RAGGED_M, EPI_STORE, true, false, 4, true, 3, true>;

@@ -810,26 +810,27 @@ __device__ void epilogue_store(const GemmArgs& a, const TileInfo& ti, uint32_t t
 __device__ __forceinline__ void st_bf16_col(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
 
 // Wide gate/up GEMM: gate in columns [0, narrow), up in [narrow, 2 narrow) of
-// accumulator 0; h[row0 + t, j] for j = 128 ti.nb (the unit's first n-block) +
-// 128 rank + lane row.
-template <class C>
-__device__ __noinline__ void epilogue_narrow_swiglu(const GemmArgs& a, const TileInfo& ti, uint32_t tacc,
-                                       int row_in_tile, int rank, int cpart, int nparts) {
-  const int I = a.inter;
-  const int j = ti.nb * (C::BN / 2) + 128 * rank + row_in_tile;
-  const bool col_ok = j < I && a.h_out != nullptr;
-  __nv_bfloat16* hcol = a.h_out + (long long)ti.row0 * I + j;
+// accumulator 0; h[row0 + t, j] for j = j0 + lane row (j0 = 128 x the unit's
+// first n-block + 128 rank).  Out of line, every argument by value: the
+// callers' loop state stays in registers.
+__device__ __noinline__ void epilogue_narrow_swiglu(__nv_bfloat16* h_out, int I, int j0,
+                                                    long long row0, int rows_valid, int narrow,
+                                                    uint32_t tacc, int row_in_tile, int cpart,
+                                                    int nparts) {
+  const int j = j0 + row_in_tile;
+  const bool col_ok = j < I && h_out != nullptr;
+  __nv_bfloat16* hcol = h_out + row0 * I + j;
+  // the sigmoids of columns 2m and 2m+1 share one reciprocal, as in the
+  // other gate/up epilogues (so h is the same bits whichever unit forms it):
+  // the pair's two columns are the lanes l and l^1
+  const bool odd = (row_in_tile & 1) != 0;
 #pragma unroll 1
-  for (int c0 = 32 * cpart; c0 < ti.rows_valid; c0 += 32 * nparts) {
+  for (int c0 = 32 * cpart; c0 < rows_valid; c0 += 32 * nparts) {
     uint32_t g[32], u[32];
     tmem_ld32_issue(tacc + c0, g);
-    tmem_ld32_issue(tacc + ti.narrow + c0, u);
+    tmem_ld32_issue(tacc + narrow + c0, u);
     tmem_ld_wait2(g, u);
-    // the sigmoids of columns 2m and 2m+1 share one reciprocal, as in the
-    // other gate/up epilogues (so h is the same bits whichever unit forms it):
-    // the pair's two columns are the lanes l and l^1
-    const bool odd = (row_in_tile & 1) != 0;
-    const int nt = min(32, ti.rows_valid - c0);
+    const int nt = min(32, rows_valid - c0);
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
       const float gv = __uint_as_float(g[i]);
@@ -1215,19 +1216,20 @@ __device__ bool wide_unit(const TileInfo& ti, uint32_t smem_base, uint32_t tmem_
 // with the stage's token rows as their N side, into columns [0, N) and [N, 2N)
 // of accumulator 0.  Accumulator 1 is left unwritten: it is handed to the
 // epilogue (which stores nothing for it) once free, keeping both barriers'
-// phases in step with the other units.
+// phases in step with the other units.  Out of line, every argument by value
+// (the issuer's ring position stays in registers): returns the advanced
+// position as stage | phase << 16, or -1 on abort.
 template <class C>
-__device__ __noinline__ bool narrow_wide_unit(const TileInfo& ti, uint32_t smem_base, uint32_t tmem_base,
-                                 uint64_t* full_bar, uint64_t* empty_bar, uint64_t* tfull_bar,
-                                 uint64_t* tempty_bar, int& stage, uint32_t& phase,
-                                 uint32_t& acc_phase, int lane, volatile int* abort_flag,
-                                 int* status) {
-  const int nt = narrow_cols<C>(ti);
+__device__ __noinline__ int narrow_wide_unit(int kblocks, int nt, uint32_t smem_base,
+                                             uint32_t tmem_base, uint32_t full0, uint32_t empty0,
+                                             uint32_t tfull0, uint32_t tempty0, int stage,
+                                             uint32_t phase, uint32_t acc_phase, int lane,
+                                             volatile int* abort_flag, int* status) {
   const uint32_t idesc = idesc_bf16_f32(2 * BM, nt, false, false);
-  if (!mbar_wait(smem_u32(&tempty_bar[0]), acc_phase ^ 1, abort_flag, status)) return false;
+  if (!mbar_wait(tempty0, acc_phase ^ 1, abort_flag, status)) return -1;
   tc_fence_after();
-  for (int kb = 0; kb < ti.kblocks; ++kb) {
-    if (!mbar_wait(smem_u32(&full_bar[stage]), phase, abort_flag, status)) return false;
+  for (int kb = 0; kb < kblocks; ++kb) {
+    if (!mbar_wait(full0 + 8 * stage, phase, abort_flag, status)) return -1;
     tc_fence_after();
     if (lane == 0) {
       const uint32_t sA = smem_base + stage * C::STAGE_BYTES;
@@ -1239,21 +1241,20 @@ __device__ __noinline__ bool narrow_wide_unit(const TileInfo& ti, uint32_t smem_
           umma_bf16_pair(tmem_base + w * nt, smem_desc_sw128(sW + kk * 32, 16, 1024),
                          smem_desc_sw128(sA + kk * 32, 16, 1024), idesc, (kb | kk) != 0 ? 1u : 0u);
       }
-      umma_commit_pair(smem_u32(&empty_bar[stage]));
+      umma_commit_pair(empty0 + 8 * stage);
     }
     __syncwarp();
     if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
   }
-  if (lane == 0) umma_commit_pair(smem_u32(&tfull_bar[0]));
+  if (lane == 0) umma_commit_pair(tfull0);
   __syncwarp();
-  if (!mbar_wait(smem_u32(&tempty_bar[1]), acc_phase ^ 1, abort_flag, status)) return false;
+  if (!mbar_wait(tempty0 + 8, acc_phase ^ 1, abort_flag, status)) return -1;
   if (lane == 0) {
-    mbar_arrive(smem_u32(&tfull_bar[1]));
-    mbar_arrive_remote(mapa_shared(smem_u32(&tfull_bar[1]), 1));
+    mbar_arrive(tfull0 + 8);
+    mbar_arrive_remote(mapa_shared(tfull0 + 8, 1));
   }
   __syncwarp();
-  acc_phase ^= 1;
-  return true;
+  return stage | (int)(phase << 16);
 }
 
 // ---------------------------------------------------------------- the kernel
@@ -1490,9 +1491,14 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         // held (not released to the producer) until accumulator 1 is free too
         // and the stage's second half has been issued.
         if (narrow_cols<C>(ti)) {
-          if (!narrow_wide_unit<C>(ti, smem_base, tmem_base, full_bar, empty_bar, tfull_bar,
-                                   tempty_bar, stage, phase, acc_phase, lane, abort_flag, a.status))
-            break;
+          const int r = narrow_wide_unit<C>(ti.kblocks, narrow_cols<C>(ti), smem_base, tmem_base,
+                                            smem_u32(&full_bar[0]), smem_u32(&empty_bar[0]),
+                                            smem_u32(&tfull_bar[0]), smem_u32(&tempty_bar[0]),
+                                            stage, phase, acc_phase, lane, abort_flag, a.status);
+          if (r < 0) break;
+          stage = r & 0xFFFF;
+          phase = (uint32_t)r >> 16;
+          acc_phase ^= 1;
         } else if (!wide_unit<C>(ti, smem_base, tmem_base, full_bar, empty_bar, tfull_bar,
                                  tempty_bar, stage, phase, acc_phase, lane, abort_flag, a.status)) {
           break;
@@ -1635,7 +1641,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         } else if (narrow_cols<C>(ti)) {
           // a NARROW unit: accumulator 0 holds both halves, accumulator 1 nothing
           if constexpr (C::NARROW)
-            if (sub == 0) epilogue_narrow_swiglu<C>(a, ti, tacc, row_in_tile, rank, cpart, nparts);
+            if (sub == 0)
+              epilogue_narrow_swiglu(a.h_out, a.inter, ti.nb * (C::BN / 2) + 128 * rank, ti.row0,
+                                     ti.rows_valid, ti.narrow, tacc, row_in_tile, cpart, nparts);
         } else if constexpr (C::EPI == EPI_STORE_F32)
           epilogue_store_f32<C>(a, ti, tacc, row_in_tile, wo, &tmD0, cpart, nparts);
         else if constexpr (C::EPI == EPI_SWIGLU && C::EPI_COLS == 32)

@@ -387,3 +387,26 @@ def test_inference_forward_matches_training_forward(name):
     assert torch.equal(outs[0][0], outs[1][0])
     f = U.oracle_forward(di, topk_idx=outs[1][2].cpu().numpy())
     U.check_close(outs[1][0], f["out"], "out (inference)")
+
+
+@pytest.mark.parametrize("name,factor", [("ragged", 0.6), ("skewed_mid", 1.0), ("ragged_shared", 0.8)])
+def test_inference_forward_with_capacity_matches_training_forward(name, factor):
+    """With an expert capacity the groups are the experts' first C rows, so the
+    inference gate/up GEMM's tails (and its narrow units) follow the capped
+    counts: y_perm and out equal the training forward's bit for bit."""
+    w = CASES[name]
+    C = M.expert_capacity(w.T, w.k, w.E, factor)
+    di = U.DeviceInputs(w, seed=12, with_grad=False)
+    outs = []
+    for with_backward in (True, False):
+        layer = M.MoeLayer(di.dims, gate_mode=w.gate, with_backward=with_backward, capacity=C)
+        layer.forward(di.x, di.w_router, di.w_gate_up, di.w_down, di.router_bias, di.w_sh_gate_up,
+                      di.w_sh_down)
+        torch.cuda.synchronize()
+        assert M.moe_read_device_status(layer.workspace) == 0
+        outs.append((layer.out.clone(), layer.y_perm.clone(), layer.slot_perm.clone()))
+    assert torch.equal(outs[0][2], outs[1][2])
+    assert (outs[1][2] < 0).any()  # the capacity drops slots
+    kept = outs[1][2][outs[1][2] >= 0].long()
+    assert torch.equal(outs[0][1][kept], outs[1][1][kept])
+    assert torch.equal(outs[0][0], outs[1][0])

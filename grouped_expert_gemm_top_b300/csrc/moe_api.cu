@@ -1257,7 +1257,7 @@ ScratchSlot g_scratch_slot[kMaxScratchDevices] = {};
 typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
 typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
 
-// Unique id of the calling thread's current context (0: none, or the driver
+// Unique id of the calling thread's current context (0: none, or the CUDA driver
 // could not be reached).
 unsigned long long current_context_id() {
   static CtxGetCurrentFn get_cur = nullptr;

@@ -66,19 +66,22 @@ def test_overlapped_steps_are_bit_identical(name, steps):
     assert M.moe_read_device_status(layer.workspace) == 0
 
 
-def test_overlapped_forward_only_is_bit_identical():
+@pytest.mark.parametrize("name", ["qwen3_30b_a3b_balanced", "qwen3_30b_a3b_skewed"])
+def test_overlapped_forward_only_is_bit_identical(name):
     """The inference forward (no saved pre-activations) repeated, against its
-    first run and against the training forward's output."""
-    w = G.WORKLOADS["qwen3_30b_a3b_balanced"]
+    first run and against the training forward's output; the skewed routing
+    also runs the gate/up GEMM's narrow units."""
+    w = G.WORKLOADS[name]
     di = U.DeviceInputs(w, seed=2, with_grad=False)
     inf = M.MoeLayer(di.dims, gate_mode=w.gate, with_backward=False)
     tr = M.MoeLayer(di.dims, gate_mode=w.gate, with_backward=True)
-    tr.forward(di.x, di.w_router, di.w_gate_up, di.w_down)
+    tr.forward(di.x, di.w_router, di.w_gate_up, di.w_down, di.router_bias)
     outs = []
     for _ in range(16):
-        inf.forward(di.x, di.w_router, di.w_gate_up, di.w_down)
+        inf.forward(di.x, di.w_router, di.w_gate_up, di.w_down, di.router_bias)
         torch.cuda.synchronize()
-        outs.append(_bits(inf.out).clone())
-    for o in outs:
+        outs.append((_bits(inf.out).clone(), _bits(inf.y_perm).clone()))
+    for o, y in outs:
         assert torch.equal(o, _bits(tr.out))
+        assert torch.equal(y, _bits(tr.y_perm))
     assert M.moe_read_device_status(inf.workspace) == 0
